@@ -1,0 +1,64 @@
+"""Pins of the GEMM and MoE oracles (float64 NumPy on dequantized operands)."""
+from fractions import Fraction
+
+import numpy as np
+
+
+def test_gemm_ref_against_exact_rationals(oracle):
+    # Y = A . B^T: every product of E2M1 values and power-of-two scales is exact,
+    # so an exact rational triple loop pins the float64 matmul to 1 ulp-ish.
+    rng = np.random.default_rng(0)
+    M, N, K = 6, 5, 64
+    qa = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    qb = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = rng.integers(120, 135, (M, K // 32), dtype=np.uint8)
+    sb = rng.integers(120, 135, (N, K // 32), dtype=np.uint8)
+    y = oracle.mx_gemm_ref(qa, sa, qb, sb)
+    a = oracle.mx_dequantize_f64(qa, sa)
+    b = oracle.mx_dequantize_f64(qb, sb)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(Fraction(float(a[m, k])) * Fraction(float(b[n, k])) for k in range(K))
+            assert abs(Fraction(float(y[m, n])) - exact) <= abs(exact) * Fraction(1, 2 ** 48) + Fraction(1, 2 ** 200)
+
+
+def test_nv_dequant_products_exact(oracle):
+    # value(q) * s_b * s_t has at most 2 + 4 + 24 significant bits: exact in float64
+    q = np.array([[0x7F, 0x21] + [0] * 6], dtype=np.uint8)
+    s = np.array([[0x7E]], dtype=np.uint8)
+    s_t = np.float32(3.0) / np.float32(2688.0)
+    y = oracle.nv_dequantize_f64(q, s, s_t)
+    # byte 0x7F: element 0 = low nibble 0xF (-6), element 1 = high nibble 0x7 (6)
+    assert y[0, 0] == -6.0 * 448.0 * float(s_t) and y[0, 1] == 6.0 * 448.0 * float(s_t)
+    # byte 0x21: element 2 = 0x1 (0.5), element 3 = 0x2 (1.0)
+    assert y[0, 2] == 0.5 * 448.0 * float(s_t) and y[0, 3] == 1.0 * 448.0 * float(s_t)
+
+
+def test_rel_frobenius(oracle):
+    ref = np.array([[3.0, 4.0]])
+    assert oracle.rel_frobenius(ref, ref) == 0.0
+    assert abs(oracle.rel_frobenius(ref * 1.001, ref) - 1e-3) < 1e-12
+
+
+def test_moe_dispatch_brute_force(oracle):
+    rng = np.random.default_rng(1)
+    T, k, E = 37, 3, 5
+    topk = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    rows, offs = oracle.moe_dispatch(topk, E)
+    # brute force: for every expert, the tokens that chose it, in ascending order
+    expect = []
+    eoffs = [0]
+    for e in range(E):
+        toks = [t for t in range(T) if e in topk[t]]
+        expect += toks
+        eoffs.append(eoffs[-1] + len(toks))
+    assert list(rows) == expect and list(offs) == eoffs
+
+
+def test_silu_closed_forms(oracle):
+    g = np.array([0.0, 1.0, -1.0, 30.0, -30.0])
+    s = oracle.silu(g)
+    assert s[0] == 0.0
+    assert abs(s[1] - 1.0 / (1.0 + np.exp(-1.0))) < 1e-16
+    assert abs(s[1] - s[2] - 1.0) < 1e-15          # silu(x) - silu(-x) = x
+    assert abs(s[3] - 30.0) < 1e-11 and abs(s[4]) < 1e-11
