@@ -1,0 +1,474 @@
+"""Benchmark of the FP4 hot path on GB300 (one JSON line on rank 0).
+
+Step (N = 1 workload): one pass of the FP8 activation pipeline on an
+8192 x 7168 E4M3 tensor with one FP32 scale per 1x128 tile (0.5 % outlier
+columns x40): direct FP8 -> MXFP4 quantization, then scaled MXFP4 -> FP8
+conversion.  `value` is algorithmic GB/s of the step (bytes each kernel must
+read and write, summed over both kernels) with inputs resident in HBM; input
+sets rotate through 4 copies (608 MB > the 126 MB L2) so every step reads
+cold data.  `e2e` is the same metric through the C ABI with pinned host
+buffers: host->device copy of the step's inputs, both kernels, device->host
+copy of both outputs, all inside the timed region.
+
+The other hot-path rows are measured after the timed region and reported
+under "rows": MXFP4 round trip of BF16 256x4096; NVFP4 (RHT + SR, then RNE)
+of a BF16 8192x14336 gradient; block-scaled FP4 GEMM 8192^3 (MXFP4, and NVFP4
+with RHT operands).
+
+--impl reference times the CPU oracle (the only reference this method has)
+on a bounded sample of the same workload and prints the same kind of line.
+Multi-GPU (torchrun): every rank runs its own copy of the workload (weak
+scaling, no collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantize/convert GB/s (frac. HBM peak); FP4 block-scaled GEMM TFLOPS vs peak"
+WORKLOAD = "fp8_e4m3[8192x7168]+fp32 1x128 tile scales -> MXFP4 -> FP8_e4m3 (0.5% outlier cols x40)"
+ROWS, COLS = 8192, 7168
+NSETS = 4
+L2_BYTES = 126 * 2 ** 20
+
+# DRAM traffic per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum)
+# for the named kernel on the workload above; null once the kernel source changed.
+TRAFFIC = {}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def _src_hash(name: str) -> str:
+    p = os.path.join(ROOT, "micro_scaled_fp4_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _traffic(kernel: str, src: str):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not t or t.get("src_sha") != _src_hash(src):
+        return None
+    return t.get("bytes_per_launch")
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured (MEASURED_PEAKS.json)"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback (6.8 TB/s, 1.9 PF bf16)"}
+
+
+FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense FP4 : BF16 tensor ratio on GB300
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+def bytes_fp8_to_mx(r, c):       # e4m3 + tile scales in, codes + E8M0 out
+    return r * c + r * (c // 128) * 4 + r * c // 2 + r * (c // 32)
+
+
+def bytes_mx_to_fp8(r, c):       # codes + E8M0 in, e4m3 + tile scales out
+    return r * c // 2 + r * (c // 32) + r * c + r * (c // 128) * 4
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[4], f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        mx = max(r[1] for r in rows)
+        load = [r for r in rows if r[0] > 0.5 * mx] or rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in load:
+            for n, v in zip(names, r[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(load)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+def cpu_oracle_rate(sample_rows: int, repeats: int = 1):
+    """Oracle a3 + a4 on `sample_rows` rows of the workload; returns (GB/s, seconds, cores)."""
+    import oracle
+    from micro_scaled_fp4_gb300 import workloads as W
+    oracle.build()
+    e4, ts = W.fp8_activation(sample_rows, COLS, seed=1, outlier_seed=2)
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        q, s = oracle.fp8_to_mx(e4, ts)
+        oracle.mx_to_fp8(q, s)
+    dt = (time.perf_counter() - t0) / repeats
+    nbytes = bytes_fp8_to_mx(sample_rows, COLS) + bytes_mx_to_fp8(sample_rows, COLS)
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return nbytes / dt / 1e9, dt, cores
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    sample = 256
+    for _ in range(args.warmup):
+        cpu_oracle_rate(sample)
+    vals, t_total = [], 0.0
+    for _ in range(args.steps):
+        v, dt, cores = cpu_oracle_rate(sample)
+        vals.append(v)
+        t_total += dt
+    value = statistics.mean(vals)
+    desc = f"{sample} of {ROWS} rows of the workload per step (a3 + a4, scalar C oracle, OpenMP)"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_total / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_rows": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def _events(torch, n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def main_rows(fq, W, torch, peaks):
+    """The other hot-path rows, each timed with CUDA events (inputs > L2 or L2 flushed)."""
+    rows = {}
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
+
+    def timed(fn, iters, do_flush):
+        ts = []
+        for i in range(iters + 3):
+            if do_flush:
+                flush.zero_()
+            e0, e1 = _events(torch, 2)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= 3:
+                ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ts)
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+    # C1: MXFP4 round trip, BF16 256x4096 (5 MB: L2-resident, launch-latency bound)
+    x = dev_bf16(W.activation_bf16())
+    q = torch.empty((256, 2048), dtype=torch.uint8, device="cuda")
+    s = torch.empty((256, 128), dtype=torch.uint8, device="cuda")
+    y = torch.empty((256, 4096), dtype=torch.bfloat16, device="cuda")
+
+    def c1():
+        fq.fp4q_mx_quantize(x, fq.FP4Q_BF16, None, 256, 4096, 4096, 1, q, s, 0, stream)
+        fq.fp4q_mx_dequantize(q, s, 256, 4096, 1, y, fq.FP4Q_BF16, stream)
+    ms = timed(c1, 50, True)
+    nb = 2 * (256 * 4096 * 2 + 256 * 2048 + 256 * 128)
+    rows["mx_roundtrip_bf16_256x4096"] = {"ms": round(ms, 4), "GB_per_s": round(nb / ms / 1e6, 1),
+                                          "frac_hbm": round(nb / ms / 1e6 / peaks["hbm_gbs"], 3),
+                                          "note": "5.3 MB, L2 flushed before each pass; launch-latency bound"}
+    g = graph_c1 = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(20):
+                fq.fp4q_mx_quantize(x, fq.FP4Q_BF16, None, 256, 4096, 4096, 1, q, s, 0,
+                                    torch.cuda.current_stream())
+                fq.fp4q_mx_dequantize(q, s, 256, 4096, 1, y, fq.FP4Q_BF16, torch.cuda.current_stream())
+        ms_g = timed(g.replay, 20, False) / 20
+        rows["mx_roundtrip_bf16_256x4096"]["graph_ms"] = round(ms_g, 4)
+        rows["mx_roundtrip_bf16_256x4096"]["graph_GB_per_s"] = round(nb / ms_g / 1e6, 1)
+    except Exception as e:  # noqa: BLE001 - graph capture is an optional extra figure
+        rows["mx_roundtrip_bf16_256x4096"]["graph_error"] = str(e)[:120]
+    del x, q, s, y, g, graph_c1
+
+    # C3: NVFP4 of a BF16 8192x14336 Student-t gradient, RHT, SR then RNE (235 MB > L2)
+    R3, C3 = 8192, 14336
+    xg = dev_bf16(W.gradient_bf16(R3, C3))
+    q3 = torch.empty((R3, C3 // 2), dtype=torch.uint8, device="cuda")
+    s3 = torch.empty((R3, C3 // 16), dtype=torch.uint8, device="cuda")
+    st = torch.empty(1, dtype=torch.float32, device="cuda")
+    am = torch.empty(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+
+    def c3(rounding, amax_in=None):
+        fq.fp4q_nv_quantize(xg, R3, C3, C3, 1, 1, 7, rounding, 1234, amax_in, am, st, q3, s3, 0, ws, 256, stream)
+    b_amax = R3 * C3 * 2
+    b_quant = R3 * C3 * 2 + R3 * C3 // 2 + R3 * C3 // 16
+    ms_sr = timed(lambda: c3(fq.FP4Q_SR), 10, True)
+    ms_rne = timed(lambda: c3(fq.FP4Q_RNE), 10, True)
+    amax_dev = am.clone()
+    ms_sr1 = timed(lambda: c3(fq.FP4Q_SR, amax_dev), 10, True)
+    ms_rne1 = timed(lambda: c3(fq.FP4Q_RNE, amax_dev), 10, True)
+    rows["nvfp4_rht_8192x14336"] = {
+        "sr_two_pass_ms": round(ms_sr, 4), "rne_two_pass_ms": round(ms_rne, 4),
+        "sr_two_pass_GB_per_s": round((b_amax + b_quant) / ms_sr / 1e6, 1),
+        "rne_two_pass_GB_per_s": round((b_amax + b_quant) / ms_rne / 1e6, 1),
+        "sr_quant_pass_ms": round(ms_sr1, 4), "rne_quant_pass_ms": round(ms_rne1, 4),
+        "sr_quant_pass_GB_per_s": round(b_quant / ms_sr1 / 1e6, 1),
+        "rne_quant_pass_GB_per_s": round(b_quant / ms_rne1 / 1e6, 1),
+        "frac_hbm_rne_quant_pass": round(b_quant / ms_rne1 / 1e6 / peaks["hbm_gbs"], 3),
+        "frac_hbm_sr_quant_pass": round(b_quant / ms_sr1 / 1e6 / peaks["hbm_gbs"], 3)}
+    del xg, q3, s3
+
+    # C4: block-scaled GEMM 8192^3, MXFP4 and NVFP4 (RHT), BF16 out
+    lib = fq.load()
+    if getattr(lib, "fp4q_block_scaled_gemm", None) is not None:
+        a, b = W.gemm_operands()
+        ad, bd = dev_bf16(a), dev_bf16(b)
+        qa, sa = fq.mx_quantize(ad, layout=fq.FP4Q_SCALES_MMA)
+        qb, sb = fq.mx_quantize(bd, layout=fq.FP4Q_SCALES_MMA)
+        ms_qa = timed(lambda: fq.mx_quantize(ad, layout=fq.FP4Q_SCALES_MMA), 10, True)
+        D = torch.empty((8192, 8192), dtype=torch.bfloat16, device="cuda")
+        A = fq.make_operand(qa, sa, fq.FP4Q_MXFP4)
+        B = fq.make_operand(qb, sb, fq.FP4Q_MXFP4)
+        flops = 2.0 * 8192 ** 3
+        ms_mx = timed(lambda: fq.fp4q_block_scaled_gemm(A, B, 8192, 8192, 8192, D, fq.FP4Q_BF16, 8192, stream), 10,
+                      True)
+        ra = fq.nv_quantize(ad, rht=True, rht_seed=7, layout=fq.FP4Q_SCALES_MMA)
+        rb = fq.nv_quantize(bd, rht=True, rht_seed=7, layout=fq.FP4Q_SCALES_MMA)
+        An = fq.make_operand(ra["q"], ra["scales"], fq.FP4Q_NVFP4, ra["s_t"])
+        Bn = fq.make_operand(rb["q"], rb["scales"], fq.FP4Q_NVFP4, rb["s_t"])
+        ms_nv = timed(lambda: fq.fp4q_block_scaled_gemm(An, Bn, 8192, 8192, 8192, D, fq.FP4Q_BF16, 8192, stream),
+                      10, True)
+        peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+        rows["gemm_fp4_8192^3"] = {
+            "mxfp4_ms": round(ms_mx, 4), "mxfp4_TFLOPS": round(flops / ms_mx / 1e9, 1),
+            "mxfp4_frac_peak": round(flops / ms_mx / 1e9 / peak, 3),
+            "nvfp4_ms": round(ms_nv, 4), "nvfp4_TFLOPS": round(flops / ms_nv / 1e9, 1),
+            "nvfp4_frac_peak": round(flops / ms_nv / 1e9 / peak, 3),
+            "peak_TFLOPS": round(peak, 1),
+            "peak_source": f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
+            "mx_quantize_operand_ms": round(ms_qa, 4)}
+        del ad, bd, qa, sa, qb, sb, D, ra, rb
+    return rows
+
+
+def run_gpu(args, rank, world):
+    import torch
+    import micro_scaled_fp4_gb300.fp4q as fq
+    from micro_scaled_fp4_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    fq.load()
+    peaks = _peaks()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    # ---- inputs: NSETS rotating copies, resident in HBM ----
+    e4, ts = W.fp8_activation(ROWS, COLS)
+    stream = torch.cuda.current_stream()
+    sets = []
+    for i in range(NSETS):
+        x = torch.from_numpy(e4).cuda()
+        t = torch.from_numpy(ts).cuda()
+        q = torch.empty((ROWS, COLS // 2), dtype=torch.uint8, device="cuda")
+        s = torch.empty((ROWS, COLS // 32), dtype=torch.uint8, device="cuda")
+        y = torch.empty((ROWS, COLS), dtype=torch.uint8, device="cuda")
+        yt = torch.empty((ROWS, COLS // 128), dtype=torch.float32, device="cuda")
+        sets.append((x, t, q, s, y, yt))
+
+    def step(i, ev=None):
+        x, t, q, s, y, yt = sets[i % NSETS]
+        if ev:
+            ev[0].record(stream)
+        fq.fp4q_mx_quantize(x, fq.FP4Q_E4M3, t, ROWS, COLS, COLS, 1, q, s, fq.FP4Q_SCALES_ROWMAJOR, stream)
+        if ev:
+            ev[1].record(stream)
+        fq.fp4q_fp4_to_fp8(q, s, ROWS, COLS, 1, y, yt, stream)
+        if ev:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = [_events(torch, 3) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = _events(torch, 1)[0]
+    t_end = _events(torch, 1)[0]
+    wall0 = time.perf_counter()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    ms_total = t_start.elapsed_time(t_end)
+    a3_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    a4_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    if dist:
+        tt = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    nbytes = bytes_fp8_to_mx(ROWS, COLS) + bytes_mx_to_fp8(ROWS, COLS)
+    value = world * nbytes / ms_step / 1e6          # GB/s over all ranks
+
+    # ---- e2e through the C ABI with pinned host buffers ----
+    hx = torch.from_numpy(e4).pin_memory()
+    ht = torch.from_numpy(ts).pin_memory()
+    hq = torch.empty((ROWS, COLS // 2), dtype=torch.uint8).pin_memory()
+    hs = torch.empty((ROWS, COLS // 32), dtype=torch.uint8).pin_memory()
+    hy = torch.empty((ROWS, COLS), dtype=torch.uint8).pin_memory()
+    hyt = torch.empty((ROWS, COLS // 128), dtype=torch.float32).pin_memory()
+    x, t, q, s, y, yt = sets[0]
+
+    def e2e_step():
+        x.copy_(hx, non_blocking=True)
+        t.copy_(ht, non_blocking=True)
+        fq.fp4q_mx_quantize(x, fq.FP4Q_E4M3, t, ROWS, COLS, COLS, 1, q, s, fq.FP4Q_SCALES_ROWMAJOR, stream)
+        fq.fp4q_fp4_to_fp8(q, s, ROWS, COLS, 1, y, yt, stream)
+        hq.copy_(q, non_blocking=True)
+        hs.copy_(s, non_blocking=True)
+        hy.copy_(y, non_blocking=True)
+        hyt.copy_(yt, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = _events(torch, 2)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = hx.numel() + ht.numel() * 4
+    d2h = hq.numel() + hs.numel() + hy.numel() + hyt.numel() * 4
+    clk = clocks.stop()
+
+    # ---- roofline of the dominant kernel ----
+    dom = ("fp8_to_mx", a3_ms, bytes_fp8_to_mx(ROWS, COLS), "mx_quant.cu") if a3_ms >= a4_ms else \
+          ("mx_to_fp8", a4_ms, bytes_mx_to_fp8(ROWS, COLS), "fp4_to_fp8.cu")
+    achieved = dom[2] / dom[1] / 1e6
+    roof = {"kernel": dom[0], "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 3), "traffic": _traffic(dom[0], dom[3]),
+            "algorithmic_bytes_per_launch": dom[2], "ms_per_launch": round(dom[1], 5),
+            "peak_source": peaks["source"],
+            "kernels": {"fp8_to_mx": {"ms": round(a3_ms, 5), "GB_per_s": round(bytes_fp8_to_mx(ROWS, COLS) / a3_ms / 1e6, 1)},
+                        "mx_to_fp8": {"ms": round(a4_ms, 5), "GB_per_s": round(bytes_mx_to_fp8(ROWS, COLS) / a4_ms / 1e6, 1)}}}
+
+    rows = None
+    cpu = None
+    if rank == 0 and not args.no_rows:
+        del sets
+        torch.cuda.empty_cache()
+        rows = main_rows(fq, W, torch, peaks)
+    if rank == 0 and not args.no_cpu:
+        sample = 256
+        v, dt, cores = cpu_oracle_rate(sample)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{sample} of {ROWS} rows of the workload (a3 + a4), {dt:.2f} s"}
+    if dist:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "rows": ROWS, "cols": COLS, "parallelism": f"replicas{world}",
+                       "l2": f"{NSETS} rotating input sets ({NSETS * (nbytes // 2**20)} MB > L2)",
+                       "frac_hbm": round(value / world / peaks["hbm_gbs"], 3)},
+            "wall_s_timed_region": round(wall, 4),
+            "e2e": {"value": round(nbytes / e2e_ms / 1e6, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": 2 * args.steps, "roofline": roof, "cpu_baseline": cpu, "clocks": clk, "rows": rows}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="fp4q", choices=["fp4q", "reference"])
+    ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * fp4q -- micro-scaled FP4 quantize / convert / block-scaled GEMM for GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer named "device" is GPU global memory owned by the
+ * caller; the library allocates no device memory.  Every call is
+ * asynchronous on `stream` (never synchronises) and validates its
+ * arguments before launching: an argument error is returned immediately and
+ * nothing is launched.  A launch failure returns FP4Q_ERR_CUDA.  Device-side
+ * wait timeouts are recorded in a device status word read by
+ * fp4q_device_status().  Inputs must be finite; non-finite inputs give
+ * unspecified codes but never a fault.
+ *
+ * Conventions shared by all calls:
+ *  - Tensors are row-major [rows, cols]; blocks run along the last
+ *    (contiguous) axis.  block_axis must be 1 (the last axis); 0 is
+ *    reserved for column-wise blocks and returns FP4Q_ERR_UNSUPPORTED_SHAPE.
+ *  - Packed FP4 (E2M1): element i of a row sits in the low nibble of byte
+ *    i/2 when i is even and in the high nibble when i is odd; a row of C
+ *    elements takes C/2 bytes and rows are contiguous (row stride C/2).
+ *  - Block scales come in one of two layouts (fp4q_scale_layout):
+ *      ROWMAJOR: [rows, cols/B] bytes, row-major, no padding.
+ *      MMA:      the layout the tcgen05 block-scaled MMA reads.  The scale
+ *                matrix (rows x S, S = cols/B) is cut into 128 x 4 tiles,
+ *                stored tile-row-major (tile (rt, ct) at byte
+ *                (rt * ceil(S/4) + ct) * 512); inside a tile, scale (r, c)
+ *                sits at byte (r % 32) * 16 + (r / 32) * 4 + c.  Size:
+ *                fp4q_scales_bytes().  Padding entries are not written.
+ *  - Pointers to packed data, scales and outputs must be 16-byte aligned.
+ *
+ * The operations follow three web pages:
+ *  [MXN] "Pretraining large language models with MXFP4 on Native FP4
+ *        Hardware" (news article): the MX format section (32-element
+ *        blocks, E8M0 shared exponent, X = 2^E * Q_FP4(X / 2^E)) and the
+ *        investigation section (Fprop / Dgrad / Wgrad GEMMs).
+ *  [HOP] "Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs"
+ *        (technical summaries): section 2 (direct FP8 -> FP4, bitwise
+ *        FP4 -> FP8 with hierarchical scale alignment, ragged MoE tensors).
+ *  [NVF] "Pretraining Large Language Models with NVFP4" (technical
+ *        summary): section 2.A (NVFP4 format) and 2.B (random Hadamard
+ *        transform, stochastic rounding).
+ */
+#ifndef FP4Q_H
+#define FP4Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* fp4q_stream_t;
+
+typedef enum fp4q_status {
+    FP4Q_OK = 0,
+    FP4Q_ERR_INVALID_ARGUMENT = 1,   /* null pointer, bad enum, negative size   */
+    FP4Q_ERR_UNSUPPORTED_SHAPE = 2,  /* partial block, K % 128, block_axis != 1  */
+    FP4Q_ERR_MISALIGNED = 3,         /* pointer not 16-byte aligned              */
+    FP4Q_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute cap. 10.3  */
+    FP4Q_ERR_CUDA = 5,               /* a CUDA call or launch failed             */
+    FP4Q_ERR_TIMEOUT = 6             /* a device-side wait ran out (status word) */
+} fp4q_status;
+
+typedef enum fp4q_dtype { FP4Q_BF16 = 0, FP4Q_FP32 = 1, FP4Q_E4M3 = 2 } fp4q_dtype;
+typedef enum fp4q_scale_layout { FP4Q_SCALES_ROWMAJOR = 0, FP4Q_SCALES_MMA = 1 } fp4q_scale_layout;
+typedef enum fp4q_rounding { FP4Q_RNE = 0, FP4Q_SR = 1 } fp4q_rounding;
+typedef enum fp4q_format { FP4Q_MXFP4 = 0, FP4Q_NVFP4 = 1 } fp4q_format;
+
+/* Human-readable name of a status code (static string). */
+const char* fp4q_status_string(fp4q_status status);
+
+/* Detail of the last failing call on this host thread (static per thread). */
+const char* fp4q_last_error(void);
+
+/* Bytes of a block-scale matrix of `rows` x `scale_cols` in `layout`
+ * (ROWMAJOR: rows * scale_cols; MMA: padded to 128 x 4 tiles). */
+size_t fp4q_scales_bytes(int64_t rows, int64_t scale_cols, fp4q_scale_layout layout);
+
+/*
+ * fp4q_mx_quantize -- BF16 / FP32 / FP8-E4M3 -> MXFP4.
+ * [MXN] MX section: blocks of 32 elements share one E8M0 exponent
+ * E = floor(log2(block amax)) - 2 (clamped to [-127, 127]; an all-zero block
+ * takes E = -127), and each element is stored as the E2M1 code nearest to
+ * x / 2^E (ties to even, saturating at +-6, sign kept also for zeros).
+ * [HOP] abstract and section 1: with x_type == FP4Q_E4M3 the source is FP8
+ * quantized straight to FP4 with no BF16 intermediate: element value =
+ * decode(e4m3) * tile_scale[r, c / 128] (one FP32 multiply), then the rule
+ * above.
+ *   x          device, [rows, ld_x] elements of x_type (ld_x >= cols; for
+ *              E4M3 ld_x % 16 == 0, for BF16 ld_x % 8 == 0, FP32 ld_x % 4 == 0)
+ *   tile_scale device FP32 [rows, cols/128] when x_type == FP4Q_E4M3
+ *              (cols % 128 == 0), else NULL
+ *   cols       multiple of 32
+ *   q          device out, [rows, cols/2] packed codes
+ *   scales     device out, E8M0 bytes in `layout` (rows x cols/32)
+ */
+fp4q_status fp4q_mx_quantize(const void* x, fp4q_dtype x_type, const float* tile_scale,
+                             int64_t rows, int64_t cols, int64_t ld_x, int block_axis,
+                             uint8_t* q, uint8_t* scales, fp4q_scale_layout layout,
+                             fp4q_stream_t stream);
+
+/*
+ * fp4q_mx_dequantize -- MXFP4 -> BF16 / FP32: y = 2^E * value(code), exact
+ * (rounded only where it overflows the output type).  [MXN] reconstruction.
+ *   q       device, [rows, cols/2];  scales device, ROWMAJOR E8M0 [rows, cols/32]
+ *   y       device out, [rows, cols] of y_type (FP4Q_BF16 or FP4Q_FP32)
+ */
+fp4q_status fp4q_mx_dequantize(const uint8_t* q, const uint8_t* scales, int64_t rows,
+                               int64_t cols, int block_axis, void* y, fp4q_dtype y_type,
+                               fp4q_stream_t stream);
+
+/*
+ * fp4q_fp4_to_fp8 -- scaled MXFP4 -> FP8-E4M3 with one FP32 scale per 1x128 tile.
+ * [HOP] section 2.B: hierarchical scale alignment -- the tile scale is the
+ * largest of the tile's four E8M0 block scales, 2^Emax; each element is the
+ * E4M3 encoding of value(code) * 2^(E_i - Emax), produced by remapping the
+ * sign / exponent / mantissa fields (no floating-point arithmetic).
+ * [HOP, Spanish summary] section 2: subnormal results keep their value.
+ * Magnitudes below the smallest E4M3 subnormal (2^-9) become signed zero;
+ * values are exact whenever E_i - Emax >= -8.
+ *   q           device, [rows, cols/2];  scales device, ROWMAJOR E8M0 [rows, cols/32]
+ *   cols        multiple of 128
+ *   y           device out, E4M3 [rows, cols]
+ *   tile_scale  device out, FP32 [rows, cols/128]
+ */
+fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, int64_t rows,
+                            int64_t cols, int block_axis, uint8_t* y, float* tile_scale,
+                            fp4q_stream_t stream);
+
+/*
+ * fp4q_nv_quantize -- BF16 -> NVFP4 (optional 16-point RHT, RNE or SR).
+ * [NVF] 2.A: 16-element blocks of E2M1 with one E4M3 scale each under one
+ * FP32 tensor scale.  With y the (optionally rotated) values and amax the
+ * tensor max |y|:  s_t = amax / 2688;  s_b = E4M3_rn_satfinite(blockamax /
+ * (6 s_t));  sf = float(s_b) * s_t;  q = ROUND(y * (1 / sf)); all in FP32
+ * with IEEE round-to-nearest operations.  amax == 0 or s_b == 0 gives
+ * signed-zero codes.
+ * [NVF] 2.B: rht != 0 applies y = (1/4) H16 diag(d) x on every 16-element
+ * tile (Sylvester H16; d_j = -1 iff bit j of word 0 of Philox4x32-10 with
+ * key = rht_seed and counter 0; butterflies with strides 1, 2, 4, 8 in FP32).
+ * rounding == FP4Q_SR rounds each element up with probability equal to its
+ * distance fraction: up iff r < frac * 2^32, r the (i mod 4)-th word of
+ * Philox4x32-10(key = sr_seed, counter = i / 4), i = row * cols + col.
+ *   x                device BF16 [rows, ld_x], ld_x % 8 == 0;  cols % 16 == 0
+ *   amax_in          device FP32 scalar or NULL (NULL: computed, two passes)
+ *   amax_out         device FP32 scalar out or NULL
+ *   tensor_scale_out device FP32 scalar out (s_t)
+ *   q                device out, [rows, cols/2];  scales device out, E4M3 in `layout`
+ *   workspace        device, >= fp4q_nv_quantize_workspace_bytes() bytes, 16-B
+ *                    aligned; used only when amax_in == NULL (may be NULL then
+ *                    not); reset by the call itself.
+ */
+size_t fp4q_nv_quantize_workspace_bytes(int64_t rows, int64_t cols);
+fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                             int block_axis, int rht, uint64_t rht_seed,
+                             fp4q_rounding rounding, uint64_t sr_seed, const float* amax_in,
+                             float* amax_out, float* tensor_scale_out, uint8_t* q,
+                             uint8_t* scales, fp4q_scale_layout layout, void* workspace,
+                             size_t workspace_bytes, fp4q_stream_t stream);
+
+/* One FP4 GEMM operand.  Host struct; the pointers in it are device pointers. */
+typedef struct fp4q_operand {
+    const uint8_t* q;           /* packed E2M1 [rows, K/2], row stride K/2 bytes      */
+    const uint8_t* scales;      /* block scales in FP4Q_SCALES_MMA layout              */
+    fp4q_format format;         /* MXFP4: E8M0 per 32; NVFP4: E4M3 per 16              */
+    const float* tensor_scale;  /* NVFP4: device FP32 scalar s_t; MXFP4: NULL          */
+} fp4q_operand;
+
+/*
+ * fp4q_block_scaled_gemm -- D = A . B^T on the tcgen05 block-scaled tensor cores.
+ * [MXN] investigation section: the forward GEMM of a linear layer, Y = X W^T,
+ * with both operands FP4 along the reduction axis K.  [NVF] 2.B: for NVFP4
+ * operands the result is scaled by s_tA * s_tB, and a Hadamard rotation
+ * applied to both operands along K cancels in the product.
+ *   A, B     operands of the same format; A has M rows, B has N rows, both K columns
+ *   K        multiple of 128;  M, N >= 1
+ *   D        device out, [M, ldd] of d_type (FP4Q_BF16, RNE from FP32, or FP4Q_FP32),
+ *            ldd >= N, ldd * element size a multiple of 16 bytes
+ * FP32 accumulation.
+ */
+fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M,
+                                   int64_t N, int64_t K, void* D, fp4q_dtype d_type,
+                                   int64_t ldd, fp4q_stream_t stream);
+
+/*
+ * fp4q_device_status -- read (and, if reset != 0, clear) the device status
+ * word of the current device: 0 when no device-side wait has timed out since
+ * the last reset, else a bit mask of the kernels that gave up (FP4Q_ERR_TIMEOUT
+ * is returned in that case).  Synchronous: waits for the device first.
+ */
+fp4q_status fp4q_device_status(uint32_t* status_out, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4Q_H */

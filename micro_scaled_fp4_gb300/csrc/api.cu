@@ -1,0 +1,123 @@
+// Status codes, per-thread error detail, device checks and the device status
+// word of the fp4q library.
+#include <mutex>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "common.cuh"
+
+namespace fp4q {
+
+// One status word per device: kernels OR a bit into it when a bounded
+// device-side wait gives up (they then skip their remaining work and return).
+__device__ uint32_t g_status_word;
+
+static thread_local char t_last_error[512] = "";
+
+fp4q_status fail(fp4q_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof t_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+fp4q_status check_launch(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return FP4Q_OK;
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sms = 0;
+    uint32_t* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+}  // namespace
+
+fp4q_status current_device(int* sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(FP4Q_ERR_UNSUPPORTED_DEVICE, "device index %d", dev);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        std::lock_guard<std::mutex> lock(g_dev_mutex);
+        if (!d.ready) {
+            int major = 0, minor = 0, count = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return fail(FP4Q_ERR_CUDA, "cudaDeviceGetAttribute failed on device %d", dev);
+            d.supported = (major == 10 && minor == 3);
+            d.sms = count;
+            if (d.supported) {
+                void* p = nullptr;
+                e = cudaGetSymbolAddress(&p, g_status_word);
+                if (e != cudaSuccess)
+                    return fail(FP4Q_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+                d.status = static_cast<uint32_t*>(p);
+            }
+            d.ready = true;
+        }
+    }
+    if (!d.supported)
+        return fail(FP4Q_ERR_UNSUPPORTED_DEVICE, "device %d is not compute capability 10.3 (sm_103a)", dev);
+    if (sms) *sms = d.sms;
+    return FP4Q_OK;
+}
+
+uint32_t* status_word() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return g_dev[dev].status;
+}
+
+}  // namespace fp4q
+
+using namespace fp4q;
+
+extern "C" const char* fp4q_status_string(fp4q_status s) {
+    switch (s) {
+        case FP4Q_OK: return "FP4Q_OK";
+        case FP4Q_ERR_INVALID_ARGUMENT: return "FP4Q_ERR_INVALID_ARGUMENT";
+        case FP4Q_ERR_UNSUPPORTED_SHAPE: return "FP4Q_ERR_UNSUPPORTED_SHAPE";
+        case FP4Q_ERR_MISALIGNED: return "FP4Q_ERR_MISALIGNED";
+        case FP4Q_ERR_UNSUPPORTED_DEVICE: return "FP4Q_ERR_UNSUPPORTED_DEVICE";
+        case FP4Q_ERR_CUDA: return "FP4Q_ERR_CUDA";
+        case FP4Q_ERR_TIMEOUT: return "FP4Q_ERR_TIMEOUT";
+    }
+    return "FP4Q_UNKNOWN_STATUS";
+}
+
+extern "C" const char* fp4q_last_error(void) { return t_last_error; }
+
+extern "C" size_t fp4q_scales_bytes(int64_t rows, int64_t scale_cols, fp4q_scale_layout layout) {
+    if (rows < 0 || scale_cols < 0) return 0;
+    if (layout == FP4Q_SCALES_MMA)
+        return size_t((rows + 127) / 128) * size_t((scale_cols + 3) / 4) * 512u;
+    return size_t(rows) * size_t(scale_cols);
+}
+
+extern "C" fp4q_status fp4q_device_status(uint32_t* status_out, int reset) {
+    if (!status_out) return fail(FP4Q_ERR_INVALID_ARGUMENT, "status_out is NULL");
+    fp4q_status st = current_device(nullptr);
+    if (st != FP4Q_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+    uint32_t v = 0;
+    e = cudaMemcpy(&v, status_word(), sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "read status word: %s", cudaGetErrorString(e));
+    if (reset) {
+        uint32_t z = 0;
+        e = cudaMemcpy(status_word(), &z, sizeof z, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "reset status word: %s", cudaGetErrorString(e));
+    }
+    *status_out = v;
+    return v ? FP4Q_ERR_TIMEOUT : FP4Q_OK;
+}

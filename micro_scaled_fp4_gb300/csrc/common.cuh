@@ -1,0 +1,142 @@
+// Shared device and host helpers of the fp4q CUDA library (sm_103a).
+//
+// Number formats (OCP MX / OCP FP8):
+//   E2M1  4-bit float, codes 0..7 = {0, .5, 1, 1.5, 2, 3, 4, 6}, bit 3 = sign.
+//   E8M0  unsigned power-of-two exponent byte, value 2^(byte - 127).
+//   E4M3  "FN" 8-bit float, bias 7, max 448, smallest subnormal 2^-9.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp4q.h"
+
+namespace fp4q {
+
+// ---------------------------------------------------------------------------
+// Host side: status plumbing (api.cu)
+// ---------------------------------------------------------------------------
+fp4q_status fail(fp4q_status st, const char* fmt, ...);
+fp4q_status check_launch(const char* what);
+// Validates the current device (compute capability 10.3) and caches its
+// properties; returns the SM count through *sms.
+fp4q_status current_device(int* sms);
+// Device address of the library's status word on the current device.
+uint32_t* status_word();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Status-word bits (which kernel gave up a bounded wait).
+enum : uint32_t { kStatusGemmTimeout = 1u << 0, kStatusGroupedTimeout = 1u << 1 };
+
+// ---------------------------------------------------------------------------
+// Device side
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+
+// 2^e as an FP32 (exact), e in [-127, 127]; 2^-127 is the subnormal 0x00400000.
+__device__ __forceinline__ float exp2i(int e) {
+    return e >= -126 ? u2f(uint32_t(e + 127) << 23) : u2f(0x00400000u);
+}
+
+// floor(log2 |f|) of a positive finite FP32 bit pattern (subnormals included).
+__device__ __forceinline__ int floor_log2_bits(uint32_t bits) {
+    uint32_t ex = (bits >> 23) & 0xffu;
+    if (ex != 0) return int(ex) - 127;
+    uint32_t m = bits & 0x7fffffu;
+    return -149 + (31 - __clz(m));
+}
+
+// MX shared exponent of a block from the FP32 bits of its amax:
+// floor(log2 amax) - 2, clamped to [-127, 127]; amax == 0 -> -127.
+__device__ __forceinline__ int mx_exponent_from_amax_bits(uint32_t amax_bits) {
+    if (amax_bits == 0) return -127;
+    int e = floor_log2_bits(amax_bits) - 2;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// Two FP32 -> one byte of two E2M1 codes, round-to-nearest-even, saturating
+// at +-6: `lo` goes to the low nibble, `hi` to the high nibble.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+    uint16_t r;
+    asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;\n}"
+        : "=h"(r) : "f"(hi), "f"(lo));
+    return r & 0xffu;
+}
+
+// FP32 -> E4M3 byte, round-to-nearest-even, saturating at +-448.
+__device__ __forceinline__ uint32_t cvt_e4m3(float v) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+    return r & 0xffu;
+}
+
+// Two E4M3 bytes (low byte = element 0) -> two FP32 (exact).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_bytes) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_bytes));
+    float2 f;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f.x) : "h"((uint16_t)(h2 & 0xffffu)));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f.y) : "h"((uint16_t)(h2 >> 16)));
+    return f;
+}
+
+// One byte of two E2M1 codes (low nibble = element 0) -> two FP32 (exact).
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
+    uint32_t h2;
+    asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(h2) : "r"(byte));
+    float2 f;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f.x) : "h"((uint16_t)(h2 & 0xffffu)));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f.y) : "h"((uint16_t)(h2 >> 16)));
+    return f;
+}
+
+// Byte offset of scale (r, c) in the tcgen05 scale-factor layout of an
+// R x S scale matrix: 128 x 4 tiles of 512 bytes, tile-row-major, and inside
+// a tile (r % 32) * 16 + (r / 32 % 4) * 4 + c % 4.
+__device__ __forceinline__ uint64_t mma_scale_offset(uint64_t r, uint32_t c, uint32_t S) {
+    uint32_t s4 = (S + 3) >> 2;
+    return ((r >> 7) * s4 + (c >> 2)) * 512ull + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + (c & 3);
+}
+
+// 256-bit global load (read-only path, no L1 allocation) and store.
+struct u32x8 { uint32_t v[8]; };
+__device__ __forceinline__ u32x8 ldg256(const void* p) {
+    u32x8 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]),
+                   "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7]) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void stg256(void* p, const u32x8& r) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" :: "l"(p),
+                 "r"(r.v[0]), "r"(r.v[1]), "r"(r.v[2]), "r"(r.v[3]),
+                 "r"(r.v[4]), "r"(r.v[5]), "r"(r.v[6]), "r"(r.v[7]) : "memory");
+}
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
+// 32x32->64 multiplies whose halves are xored with the other counter words
+// and the key; the key advances by the two Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+        uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+// Launch shape for row-wise block kernels: one thread per block of a row,
+// `bpr` blocks per row; returns threads per CTA and CTAs along the row.
+inline void row_launch_shape(int64_t bpr, int* tpb, int* nx) {
+    int64_t n = (bpr + 255) / 256;
+    int64_t per = (bpr + n - 1) / n;
+    per = (per + 31) / 32 * 32;
+    *tpb = int(per);
+    *nx = int(n);
+}
+
+}  // namespace fp4q

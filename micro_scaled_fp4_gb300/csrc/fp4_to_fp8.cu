@@ -1,0 +1,113 @@
+// Scaled MXFP4 -> FP8-E4M3 with one FP32 scale per 1x128 tile.
+//
+// "Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs",
+// section 2.B: the E2M1 sign / exponent / mantissa fields are rewritten as
+// E4M3 fields with no floating-point arithmetic in between, and the four
+// 32-element block scales of a 128-element tile are aligned to their maximum
+// (the tile's FP8 scale), each element's exponent being shifted by its
+// block's distance to that maximum.  The Spanish summary, section 2, adds
+// that subnormal results keep their implicit bit.
+//
+// Kernel: one thread per 32-element block (16 bytes of codes in, 32 bytes of
+// E4M3 out).  The shift d = E_i - Emax is the same for the whole block, so
+// the block's 8 possible magnitudes are one 64-bit row of a small table
+// indexed by -d (rows for -d >= 12 are all zero); eight output bytes then
+// cost two byte-permute lookups plus the sign-bit spread.
+#include "common.cuh"
+
+namespace fp4q {
+namespace {
+
+constexpr int kShiftRows = 13;   // -d = 0..11 explicit, 12 = "12 or more"
+
+// E4M3 magnitude byte of E2M1 magnitude code c (0..7) shifted by 2^-sh.
+// E2M1 c = (1 + m/2) * 2^k with (k, m) = (-1, 0) for c = 1 and
+// ((c >> 1) - 1, c & 1) for c >= 2.  t = k - sh:  t >= -6 is a normal E4M3
+// (exponent field t + 7, mantissa m << 2); t = -7, -8, -9 are the subnormals
+// 4 + 2m, 2 + m and 1 + m (the last one rounds 1.5 to 2, ties to even);
+// smaller t lies below 2^-9 and flushes to zero.
+__device__ uint32_t shifted_magnitude(uint32_t c, int sh) {
+    if (c == 0) return 0;
+    int k = c == 1 ? -1 : int(c >> 1) - 1;
+    uint32_t m = c == 1 ? 0u : (c & 1u);
+    int t = k - sh;
+    if (t >= -6) return (uint32_t(t + 7) << 3) | (m << 2);
+    if (t == -7) return 4u + 2u * m;
+    if (t == -8) return 2u + m;
+    if (t == -9) return 1u + m;
+    return 0u;
+}
+
+// Eight packed codes (one 32-bit word, element j in nibble j) -> eight E4M3
+// bytes, given the magnitude row (lut.x = codes 0..3, lut.y = codes 4..7).
+__device__ __forceinline__ uint2 remap8(uint32_t w, uint2 lut) {
+    const uint32_t mag_lo = __byte_perm(lut.x, lut.y, w & 0x7777u);
+    const uint32_t mag_hi = __byte_perm(lut.x, lut.y, (w >> 16) & 0x7777u);
+    // nibble j's sign bit (4j + 3) goes to bit 8j + 7 of the output
+    const uint32_t a = __byte_perm(w, 0, 0x4140);   // bytes 0, 1 of w -> bytes 0, 2
+    const uint32_t c = __byte_perm(w, 0, 0x4342);   // bytes 2, 3 of w -> bytes 0, 2
+    const uint32_t sgn_lo = ((a << 4) & 0x00800080u) | ((a << 8) & 0x80008000u);
+    const uint32_t sgn_hi = ((c << 4) & 0x00800080u) | ((c << 8) & 0x80008000u);
+    return make_uint2(mag_lo | sgn_lo, mag_hi | sgn_hi);
+}
+
+__global__ void __launch_bounds__(256) fp4_to_fp8_kernel(
+    const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, uint32_t bpr,
+    uint8_t* __restrict__ y, float* __restrict__ tile_scale) {
+    __shared__ uint2 lut[kShiftRows];
+    if (threadIdx.x < kShiftRows) {
+        uint32_t lo = 0, hi = 0;
+        for (uint32_t c = 0; c < 4; ++c) {
+            lo |= shifted_magnitude(c, threadIdx.x) << (8 * c);
+            hi |= shifted_magnitude(c + 4, threadIdx.x) << (8 * c);
+        }
+        lut[threadIdx.x] = make_uint2(lo, hi);
+    }
+    __syncthreads();
+    const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= bpr) return;
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const uint64_t blk = uint64_t(r) * bpr + b;
+        const uint4 cw = *reinterpret_cast<const uint4*>(q + blk * 16);
+        // the tile's four E8M0 bytes, one aligned 32-bit load
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(s + uint64_t(r) * bpr + (b & ~3u));
+        const uint32_t e_own = (sw >> (8 * (b & 3))) & 0xffu;
+        const uint32_t m2 = __vmaxu4(sw, sw >> 16);
+        const uint32_t emax = max(m2 & 0xffu, (m2 >> 8) & 0xffu);
+        const uint32_t sh = min(emax - e_own, uint32_t(kShiftRows - 1));
+        const uint2 L = lut[sh];
+        const uint2 o0 = remap8(cw.x, L), o1 = remap8(cw.y, L), o2 = remap8(cw.z, L), o3 = remap8(cw.w, L);
+        u32x8 o;
+        o.v[0] = o0.x; o.v[1] = o0.y; o.v[2] = o1.x; o.v[3] = o1.y;
+        o.v[4] = o2.x; o.v[5] = o2.y; o.v[6] = o3.x; o.v[7] = o3.y;
+        stg256(y + blk * 32, o);
+        if ((b & 3) == 0) tile_scale[uint64_t(r) * (bpr >> 2) + (b >> 2)] = exp2i(int(emax) - 127);
+    }
+}
+
+}  // namespace
+}  // namespace fp4q
+
+using namespace fp4q;
+
+extern "C" fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, int64_t rows,
+                                       int64_t cols, int block_axis, uint8_t* y, float* tile_scale,
+                                       fp4q_stream_t stream) {
+    if (rows < 0 || cols < 0) return fail(FP4Q_ERR_INVALID_ARGUMENT, "fp4_to_fp8: negative size");
+    if (block_axis != 1) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "fp4_to_fp8: only block_axis = 1");
+    if (cols % 128) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "fp4_to_fp8: cols %% 128 != 0");
+    if (rows == 0 || cols == 0) return FP4Q_OK;
+    if (!q || !scales || !y || !tile_scale) return fail(FP4Q_ERR_INVALID_ARGUMENT, "fp4_to_fp8: null pointer");
+    if (!aligned16(q) || (reinterpret_cast<uintptr_t>(y) & 31u) ||
+        (reinterpret_cast<uintptr_t>(scales) & 3u) || (reinterpret_cast<uintptr_t>(tile_scale) & 3u))
+        return fail(FP4Q_ERR_MISALIGNED, "fp4_to_fp8: q 16-byte, y 32-byte, scales/tile_scale 4-byte aligned");
+    fp4q_status st = current_device(nullptr);
+    if (st != FP4Q_OK) return st;
+    const uint32_t bpr = uint32_t(cols / 32);
+    int tpb, nx;
+    row_launch_shape(bpr, &tpb, &nx);
+    int64_t gy = rows < 65535 ? rows : 65535;
+    dim3 grid(unsigned(nx), unsigned(gy), 1);
+    fp4_to_fp8_kernel<<<grid, tpb, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, scales, rows, bpr, y, tile_scale);
+    return check_launch("fp4_to_fp8");
+}

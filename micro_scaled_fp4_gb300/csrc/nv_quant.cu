@@ -1,0 +1,243 @@
+// NVFP4 quantize of BF16 with an optional 16-point random Hadamard
+// transform and round-to-nearest-even or Philox stochastic rounding.
+//
+// "Pretraining Large Language Models with NVFP4", technical summary:
+//  2.A  16-element E2M1 blocks, one E4M3 scale per block and one FP32
+//       scale per tensor (two-level scaling);
+//  2.B  random Hadamard transforms on the weight-gradient inputs to spread
+//       outliers, stochastic rounding (unbiased) on gradients.
+//
+// Two passes over the input (the tensor amax must be known before any block
+// scale): pass 1 rotates and reduces max|y| into a 32-bit word of the caller's
+// workspace (atomicMax on the float bits of non-negative values); pass 2
+// rotates again and quantizes.  With a caller-supplied amax only pass 2 runs.
+// One thread owns one 16-element block = one Hadamard tile: a single 256-bit
+// load, the butterflies in registers, the block amax in-thread, 8 bytes of
+// codes and one scale byte out.  The FP32 steps use explicit round-to-nearest
+// intrinsics so that no contraction or reassociation changes a result.
+#include "common.cuh"
+
+namespace fp4q {
+namespace {
+
+// (1/4) H16 diag(d) x, d_j = -1 iff bit j of `signs` is set.  Butterflies with
+// strides 1, 2, 4, 8 map (a, b) -> (a + b, a - b) in FP32.
+__device__ __forceinline__ void rht16(float (&t)[16], uint32_t signs) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = u2f(f2u(t[j]) ^ (((signs >> j) & 1u) << 31));
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (!(i & h)) {
+                const float a = t[i], b = t[i + h];
+                t[i] = __fadd_rn(a, b);
+                t[i + h] = __fsub_rn(a, b);
+            }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = __fmul_rn(t[j], 0.25f);
+}
+
+__device__ __forceinline__ uint32_t rht_signs(uint64_t seed) {
+    return philox4x32_10(make_uint4(0, 0, 0, 0), uint32_t(seed), uint32_t(seed >> 32)).x & 0xffffu;
+}
+
+__device__ __forceinline__ void load_tile(const uint8_t* p, float (&t)[16]) {
+    const u32x8 a = ldg256(p);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        t[2 * i] = u2f(a.v[i] << 16);
+        t[2 * i + 1] = u2f(a.v[i] & 0xffff0000u);
+    }
+}
+
+__global__ void __launch_bounds__(256) nv_amax_kernel(const uint8_t* __restrict__ x, int64_t rows,
+                                                      uint32_t tpr, int64_t ld_x_bytes, int rht,
+                                                      uint64_t rht_seed, uint32_t* __restrict__ amax_bits) {
+    const uint32_t signs = rht ? rht_signs(rht_seed) : 0u;
+    const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t m = 0;
+    if (b < tpr) {
+        for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+            float t[16];
+            load_tile(x + r * ld_x_bytes + uint64_t(b) * 32, t);
+            if (rht) rht16(t, signs);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) m = max(m, f2u(t[j]) & 0x7fffffffu);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ uint32_t wmax[8];
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t v = 0;
+        for (int w = 0; w < int(blockDim.x >> 5); ++w) v = max(v, wmax[w]);
+        if (v) atomicMax(amax_bits, v);
+    }
+}
+
+// Stochastic rounding of v onto E2M1 with the 32-bit word r: up iff
+// r < frac * 2^32, frac the exact position of |v| between its two grid
+// neighbours; |v| >= 6 saturates; the sign is kept.  Returns an FP32 grid
+// value (exactly representable, so the E2M1 convert of it is exact).
+__device__ __forceinline__ float sr_e2m1(float v, uint32_t r) {
+    const float a = fabsf(v);
+    float res;
+    if (a >= 6.0f) {
+        res = 6.0f;
+    } else {
+        float lo, step;
+        if (a >= 4.0f) { lo = 4.0f; step = 2.0f; }
+        else if (a >= 2.0f) { lo = floorf(a); step = 1.0f; }
+        else { lo = __fmul_rn(floorf(__fmul_rn(a, 2.0f)), 0.5f); step = 0.5f; }
+        const float frac = __fmul_rn(__fsub_rn(a, lo), __frcp_rn(step));   // exact
+        const uint32_t thr = __float2uint_ru(__fmul_rn(frac, 4294967296.0f));
+        res = r < thr ? __fadd_rn(lo, step) : lo;
+    }
+    return u2f(f2u(res) | (f2u(v) & 0x80000000u));
+}
+
+template <bool SR>
+__global__ void __launch_bounds__(256) nv_quant_kernel(
+    const uint8_t* __restrict__ x, int64_t rows, uint32_t tpr, int64_t ld_x_bytes, int rht,
+    uint64_t rht_seed, uint64_t sr_seed, const float* __restrict__ amax_ptr, float* __restrict__ amax_out,
+    float* __restrict__ st_out, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout) {
+    const uint32_t signs = rht ? rht_signs(rht_seed) : 0u;
+    const float amax = *amax_ptr;
+    const float s_t = __fdiv_rn(amax, 2688.0f);        // 6 * 448
+    const float denom = __fmul_rn(6.0f, s_t);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        if (amax_out) *amax_out = amax;
+        *st_out = s_t;
+    }
+    const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= tpr) return;
+    const uint64_t cols = uint64_t(tpr) * 16;
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        float t[16];
+        load_tile(x + r * ld_x_bytes + uint64_t(b) * 32, t);
+        if (rht) rht16(t, signs);
+        uint32_t ab = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ab = max(ab, f2u(t[j]) & 0x7fffffffu);
+        uint32_t sb = 0;
+        float rcp = 0.0f;
+        if (s_t > 0.0f) {
+            sb = cvt_e4m3(__fdiv_rn(u2f(ab), denom));
+            if (sb & 0x7fu) rcp = __frcp_rn(__fmul_rn(e4m3x2_to_f32x2(sb).x, s_t));
+        }
+        uint32_t words[2];
+        if (rcp == 0.0f) {
+            // zero tensor or block scale underflow: signed-zero codes
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                uint32_t w = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) w |= ((f2u(t[8 * k + j]) >> 31) << 3) << (4 * j);
+                words[k] = w;
+            }
+        } else if constexpr (!SR) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                uint32_t w = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    w |= cvt_e2m1x2(__fmul_rn(t[8 * k + 2 * j], rcp), __fmul_rn(t[8 * k + 2 * j + 1], rcp)) << (8 * j);
+                words[k] = w;
+            }
+        } else {
+            const uint64_t i0 = uint64_t(r) * cols + uint64_t(b) * 16;   // linear index, % 16 == 0
+            const uint32_t k0 = uint32_t(sr_seed), k1 = uint32_t(sr_seed >> 32);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                uint32_t w = 0;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint64_t ctr = (i0 >> 2) + uint64_t(2 * k + h);
+                    const uint4 rnd = philox4x32_10(make_uint4(uint32_t(ctr), uint32_t(ctr >> 32), 0, 0), k0, k1);
+                    const int base = 8 * k + 4 * h;
+                    const float v0 = sr_e2m1(__fmul_rn(t[base + 0], rcp), rnd.x);
+                    const float v1 = sr_e2m1(__fmul_rn(t[base + 1], rcp), rnd.y);
+                    const float v2 = sr_e2m1(__fmul_rn(t[base + 2], rcp), rnd.z);
+                    const float v3 = sr_e2m1(__fmul_rn(t[base + 3], rcp), rnd.w);
+                    w |= (cvt_e2m1x2(v0, v1) | (cvt_e2m1x2(v2, v3) << 8)) << (16 * h);
+                }
+                words[k] = w;
+            }
+        }
+        *reinterpret_cast<uint2*>(q + uint64_t(r) * (cols / 2) + uint64_t(b) * 8) = make_uint2(words[0], words[1]);
+        const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(r), b, tpr) : uint64_t(r) * tpr + b;
+        s[so] = uint8_t(sb);
+    }
+}
+
+}  // namespace
+}  // namespace fp4q
+
+using namespace fp4q;
+
+extern "C" size_t fp4q_nv_quantize_workspace_bytes(int64_t rows, int64_t cols) {
+    (void)rows;
+    (void)cols;
+    return 256;   // one 32-bit amax word (padded)
+}
+
+extern "C" fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                        int block_axis, int rht, uint64_t rht_seed,
+                                        fp4q_rounding rounding, uint64_t sr_seed, const float* amax_in,
+                                        float* amax_out, float* tensor_scale_out, uint8_t* q,
+                                        uint8_t* scales, fp4q_scale_layout layout, void* workspace,
+                                        size_t workspace_bytes, fp4q_stream_t stream) {
+    if (rounding != FP4Q_RNE && rounding != FP4Q_SR)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: bad rounding mode");
+    if (layout != FP4Q_SCALES_ROWMAJOR && layout != FP4Q_SCALES_MMA)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: bad scale layout");
+    if (rows < 0 || cols < 0 || ld_x < cols)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: need rows >= 0, cols >= 0, ld_x >= cols");
+    if (block_axis != 1) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "nv_quantize: only block_axis = 1");
+    if (cols % 16) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "nv_quantize: cols %% 16 != 0");
+    if (!tensor_scale_out) return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: tensor_scale_out is NULL");
+    if (rows > 0 && cols > 0 && (!x || !q || !scales))
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: null pointer");
+    if (!amax_in && (!workspace || workspace_bytes < fp4q_nv_quantize_workspace_bytes(rows, cols)))
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: workspace missing or too small");
+    if ((reinterpret_cast<uintptr_t>(x) & 31u) || (ld_x * 2) % 32 || (q && !aligned16(q)) ||
+        (workspace && !aligned16(workspace)))
+        return fail(FP4Q_ERR_MISALIGNED, "nv_quantize: x 32-byte aligned with ld_x %% 16 == 0; q, workspace 16-byte aligned");
+    fp4q_status st = current_device(nullptr);
+    if (st != FP4Q_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint32_t tpr = uint32_t(cols / 16);
+    int tpb = 32, nx = 1;
+    if (tpr) row_launch_shape(tpr, &tpb, &nx);
+    int64_t gy = rows < 65535 ? rows : 65535;
+    if (gy < 1) gy = 1;
+    dim3 grid(unsigned(nx), unsigned(gy), 1);
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    const float* amax_ptr = amax_in;
+    if (!amax_in) {
+        uint32_t* w = static_cast<uint32_t*>(workspace);
+        cudaError_t e = cudaMemsetAsync(w, 0, sizeof(uint32_t), s);
+        if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "nv_quantize: memset: %s", cudaGetErrorString(e));
+        if (rows > 0 && cols > 0) {
+            nv_amax_kernel<<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, w);
+            if ((st = check_launch("nv_quantize amax")) != FP4Q_OK) return st;
+        }
+        amax_ptr = reinterpret_cast<const float*>(w);
+    }
+    if (rows == 0 || cols == 0) {
+        // still publish s_t (and amax) for an empty tensor: both are 0
+        nv_quant_kernel<false><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, 0, amax_ptr, amax_out, tensor_scale_out, q, scales, 0);
+        return check_launch("nv_quantize");
+    }
+    const int mma = layout == FP4Q_SCALES_MMA;
+    if (rounding == FP4Q_SR)
+        nv_quant_kernel<true><<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, sr_seed, amax_ptr,
+                                                   amax_out, tensor_scale_out, q, scales, mma);
+    else
+        nv_quant_kernel<false><<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, sr_seed, amax_ptr,
+                                                    amax_out, tensor_scale_out, q, scales, mma);
+    return check_launch("nv_quantize");
+}

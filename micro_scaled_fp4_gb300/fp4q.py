@@ -1,0 +1,241 @@
+"""ctypes binding of the fp4q C ABI (include/fp4q.h).
+
+Argument marshalling only: every function here has the name of the C entry
+point it calls and forwards plain pointers (``tensor.data_ptr()`` or ints),
+sizes and the CUDA stream (``torch.cuda.current_stream().cuda_stream`` unless
+given).  All compute happens in the CUDA library; if libfp4q.so is missing the
+first call raises.  The helpers at the bottom (``mx_quantize`` ...) allocate
+their outputs with torch and call the same entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+# enums of include/fp4q.h
+FP4Q_OK = 0
+STATUS_NAMES = {0: "FP4Q_OK", 1: "FP4Q_ERR_INVALID_ARGUMENT", 2: "FP4Q_ERR_UNSUPPORTED_SHAPE",
+                3: "FP4Q_ERR_MISALIGNED", 4: "FP4Q_ERR_UNSUPPORTED_DEVICE", 5: "FP4Q_ERR_CUDA",
+                6: "FP4Q_ERR_TIMEOUT"}
+FP4Q_BF16, FP4Q_FP32, FP4Q_E4M3 = 0, 1, 2
+FP4Q_SCALES_ROWMAJOR, FP4Q_SCALES_MMA = 0, 1
+FP4Q_RNE, FP4Q_SR = 0, 1
+FP4Q_MXFP4, FP4Q_NVFP4 = 0, 1
+
+EXPORTED = [
+    "fp4q_status_string", "fp4q_last_error", "fp4q_scales_bytes", "fp4q_mx_quantize",
+    "fp4q_mx_dequantize", "fp4q_fp4_to_fp8", "fp4q_nv_quantize_workspace_bytes", "fp4q_nv_quantize",
+    "fp4q_block_scaled_gemm", "fp4q_device_status",
+]
+
+
+class Fp4qError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str):
+        super().__init__(f"{fn} -> {STATUS_NAMES.get(status, status)}: {detail}")
+        self.status = status
+
+
+class fp4q_operand(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("format", ctypes.c_int),
+                ("tensor_scale", ctypes.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libfp4q.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB_PATH):
+                raise RuntimeError(f"fp4q CUDA library not built ({_build.LIB_PATH}); run __graft_entry__.build()")
+            L = ctypes.CDLL(_build.LIB_PATH)
+            i64, u64, vp, ci = ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_int
+            L.fp4q_status_string.restype = ctypes.c_char_p
+            L.fp4q_status_string.argtypes = [ci]
+            L.fp4q_last_error.restype = ctypes.c_char_p
+            L.fp4q_last_error.argtypes = []
+            L.fp4q_scales_bytes.restype = ctypes.c_size_t
+            L.fp4q_scales_bytes.argtypes = [i64, i64, ci]
+            L.fp4q_nv_quantize_workspace_bytes.restype = ctypes.c_size_t
+            L.fp4q_nv_quantize_workspace_bytes.argtypes = [i64, i64]
+            sigs = {
+                "fp4q_mx_quantize": [vp, ci, vp, i64, i64, i64, ci, vp, vp, ci, vp],
+                "fp4q_mx_dequantize": [vp, vp, i64, i64, ci, vp, ci, vp],
+                "fp4q_fp4_to_fp8": [vp, vp, i64, i64, ci, vp, vp, vp],
+                "fp4q_nv_quantize": [vp, i64, i64, i64, ci, ci, u64, ci, u64, vp, vp, vp, vp, vp, ci, vp,
+                                     ctypes.c_size_t, vp],
+                "fp4q_block_scaled_gemm": [ctypes.POINTER(fp4q_operand), ctypes.POINTER(fp4q_operand), i64, i64,
+                                           i64, vp, ci, i64, vp],
+                "fp4q_device_status": [ctypes.POINTER(ctypes.c_uint32), ci],
+            }
+            for name, args in sigs.items():
+                fn = getattr(L, name, None)     # resolved here; a missing symbol fails at its call
+                if fn is not None:
+                    fn.restype = ci
+                    fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, status: int) -> int:
+    if status != FP4Q_OK:
+        raise Fp4qError(fn, status, load().fp4q_last_error().decode())
+    return status
+
+
+# ---------------------------------------------------------------------------
+# 1:1 wrappers of the C entry points
+# ---------------------------------------------------------------------------
+def fp4q_status_string(status: int) -> str:
+    return load().fp4q_status_string(status).decode()
+
+
+def fp4q_scales_bytes(rows: int, scale_cols: int, layout: int) -> int:
+    return load().fp4q_scales_bytes(rows, scale_cols, layout)
+
+
+def fp4q_nv_quantize_workspace_bytes(rows: int, cols: int) -> int:
+    return load().fp4q_nv_quantize_workspace_bytes(rows, cols)
+
+
+def fp4q_mx_quantize(x, x_type, tile_scale, rows, cols, ld_x, block_axis, q, scales, layout, stream=None):
+    return _check("fp4q_mx_quantize", load().fp4q_mx_quantize(
+        _ptr(x), x_type, _ptr(tile_scale), rows, cols, ld_x, block_axis, _ptr(q), _ptr(scales), layout,
+        _stream(stream)))
+
+
+def fp4q_mx_dequantize(q, scales, rows, cols, block_axis, y, y_type, stream=None):
+    return _check("fp4q_mx_dequantize", load().fp4q_mx_dequantize(
+        _ptr(q), _ptr(scales), rows, cols, block_axis, _ptr(y), y_type, _stream(stream)))
+
+
+def fp4q_fp4_to_fp8(q, scales, rows, cols, block_axis, y, tile_scale, stream=None):
+    return _check("fp4q_fp4_to_fp8", load().fp4q_fp4_to_fp8(
+        _ptr(q), _ptr(scales), rows, cols, block_axis, _ptr(y), _ptr(tile_scale), _stream(stream)))
+
+
+def fp4q_nv_quantize(x, rows, cols, ld_x, block_axis, rht, rht_seed, rounding, sr_seed, amax_in, amax_out,
+                     tensor_scale_out, q, scales, layout, workspace, workspace_bytes, stream=None):
+    return _check("fp4q_nv_quantize", load().fp4q_nv_quantize(
+        _ptr(x), rows, cols, ld_x, block_axis, int(rht), rht_seed, rounding, sr_seed, _ptr(amax_in),
+        _ptr(amax_out), _ptr(tensor_scale_out), _ptr(q), _ptr(scales), layout, _ptr(workspace),
+        workspace_bytes, _stream(stream)))
+
+
+def make_operand(q, scales, fmt, tensor_scale=None) -> fp4q_operand:
+    return fp4q_operand(_ptr(q), _ptr(scales), fmt, _ptr(tensor_scale))
+
+
+def fp4q_block_scaled_gemm(A: fp4q_operand, B: fp4q_operand, M, N, K, D, d_type, ldd, stream=None):
+    return _check("fp4q_block_scaled_gemm", load().fp4q_block_scaled_gemm(
+        ctypes.byref(A), ctypes.byref(B), M, N, K, _ptr(D), d_type, ldd, _stream(stream)))
+
+
+def fp4q_device_status(reset: bool = False) -> int:
+    """Returns the device status word (0 = no device-side wait timed out)."""
+    v = ctypes.c_uint32(0)
+    st = load().fp4q_device_status(ctypes.byref(v), int(bool(reset)))
+    if st not in (FP4Q_OK, 6):
+        _check("fp4q_device_status", st)
+    return int(v.value)
+
+
+# ---------------------------------------------------------------------------
+# Allocating helpers (torch for device memory; compute in the entry points)
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def mx_quantize(x, tile_scale=None, layout=FP4Q_SCALES_ROWMAJOR, stream=None):
+    """BF16 / FP32 / float8_e4m3fn [R, C] -> (q uint8 [R, C/2], scales uint8)."""
+    torch = _torch()
+    R, C = x.shape
+    xt = {torch.bfloat16: FP4Q_BF16, torch.float32: FP4Q_FP32, torch.float8_e4m3fn: FP4Q_E4M3,
+          torch.uint8: FP4Q_E4M3}[x.dtype]
+    q = torch.empty((R, C // 2), dtype=torch.uint8, device=x.device)
+    s = torch.empty(fp4q_scales_bytes(R, C // 32, layout), dtype=torch.uint8, device=x.device)
+    fp4q_mx_quantize(x, xt, tile_scale, R, C, x.stride(0), 1, q, s, layout, stream)
+    return q, (s.view(R, C // 32) if layout == FP4Q_SCALES_ROWMAJOR else s)
+
+
+def mx_dequantize(q, s, dtype=None, stream=None):
+    torch = _torch()
+    dtype = dtype or torch.bfloat16
+    R, C = q.shape[0], q.shape[1] * 2
+    y = torch.empty((R, C), dtype=dtype, device=q.device)
+    fp4q_mx_dequantize(q, s, R, C, 1, y, FP4Q_BF16 if dtype == torch.bfloat16 else FP4Q_FP32, stream)
+    return y
+
+
+def fp4_to_fp8(q, s, stream=None):
+    torch = _torch()
+    R, C = q.shape[0], q.shape[1] * 2
+    y = torch.empty((R, C), dtype=torch.uint8, device=q.device)
+    ts = torch.empty((R, C // 128), dtype=torch.float32, device=q.device)
+    fp4q_fp4_to_fp8(q, s, R, C, 1, y, ts, stream)
+    return y, ts
+
+
+def nv_quantize(x, rht=False, rht_seed=0, rounding=FP4Q_RNE, sr_seed=0, amax=None,
+                layout=FP4Q_SCALES_ROWMAJOR, stream=None):
+    """BF16 [R, C] -> dict(q, scales, s_t (device [1]), amax (device [1]))."""
+    torch = _torch()
+    R, C = x.shape
+    q = torch.empty((R, C // 2), dtype=torch.uint8, device=x.device)
+    s = torch.empty(fp4q_scales_bytes(R, C // 16, layout), dtype=torch.uint8, device=x.device)
+    st = torch.empty(1, dtype=torch.float32, device=x.device)
+    am = torch.empty(1, dtype=torch.float32, device=x.device)
+    wsb = fp4q_nv_quantize_workspace_bytes(R, C)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=x.device)
+    fp4q_nv_quantize(x, R, C, x.stride(0), 1, rht, rht_seed, rounding, sr_seed, amax, am, st, q, s, layout,
+                     ws, wsb, stream)
+    return {"q": q, "scales": s.view(R, C // 16) if layout == FP4Q_SCALES_ROWMAJOR else s, "s_t": st,
+            "amax": am}
+
+
+def gemm(qa, sa, qb, sb, fmt=FP4Q_MXFP4, ts_a=None, ts_b=None, out_dtype=None, stream=None):
+    """D = A . B^T for packed FP4 operands with MMA-layout scales.
+
+    qa [M, K/2], qb [N, K/2] uint8; sa / sb scale buffers in FP4Q_SCALES_MMA
+    layout; ts_a / ts_b device FP32 [1] tensor scales for NVFP4.  Returns a
+    [M, N] view of a row-padded output (row stride a multiple of 16 bytes).
+    """
+    torch = _torch()
+    out_dtype = out_dtype or torch.bfloat16
+    M, N, K = qa.shape[0], qb.shape[0], qa.shape[1] * 2
+    esz = 2 if out_dtype == torch.bfloat16 else 4
+    ldd = (N * esz + 15) // 16 * 16 // esz
+    D = torch.empty((M, ldd), dtype=out_dtype, device=qa.device)
+    A = make_operand(qa, sa, fmt, ts_a)
+    B = make_operand(qb, sb, fmt, ts_b)
+    fp4q_block_scaled_gemm(A, B, M, N, K, D, FP4Q_BF16 if out_dtype == torch.bfloat16 else FP4Q_FP32, ldd, stream)
+    return D[:, :N]

@@ -83,7 +83,7 @@ def _L():
                 "or_rht16_signs": [u64, vp],
                 "or_rht16": [vp, vp, vp],
                 "or_nv_quantize": [vp, i64, i64, i64, ctypes.c_int, u64, ctypes.c_int, u64,
-                                   vp, vp, vp, vp, vp],
+                                   vp, vp, vp, vp, vp, i64],
                 "or_nv_dequantize": [vp, vp, ctypes.c_float, i64, i64, vp],
                 "or_e2m1_rne_array": [vp, i64, vp],
                 "or_e4m3_rn_satfinite_array": [vp, i64, vp],
@@ -278,9 +278,12 @@ def nv_amax(x_bf16: np.ndarray, rht: bool, rht_seed: int) -> float:
 
 
 def nv_quantize(x_bf16: np.ndarray, rht: bool = False, rht_seed: int = 0, rounding: str = "rne",
-                sr_seed: int = 0, amax: float | None = None):
+                sr_seed: int = 0, amax: float | None = None, row_offset: int = 0):
     """NVFP4 quantize of a BF16 tensor along the last axis.
 
+    x_bf16 may be a slice of rows of a larger tensor: row_offset is its first
+    row's index there (the stochastic-rounding words follow the full tensor's
+    linear element index); pass that tensor's amax too.
     Returns dict(q [R, C/2], s [R, C/16] E4M3 bytes, s_t float32, amax float32).
     """
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
@@ -293,7 +296,7 @@ def nv_quantize(x_bf16: np.ndarray, rht: bool = False, rht_seed: int = 0, roundi
     amax_in = None if amax is None else np.array([amax], dtype=np.float32)
     _L().or_nv_quantize(_p(x), R, C, C, int(bool(rht)), int(rht_seed), 1 if rounding == "sr" else 0,
                         int(sr_seed), None if amax_in is None else _p(amax_in), _p(amax_out),
-                        _p(st_out), _p(q), _p(s))
+                        _p(st_out), _p(q), _p(s), int(row_offset))
     return {"q": q, "s": s, "s_t": np.float32(st_out[0]), "amax": np.float32(amax_out[0])}
 
 

@@ -421,12 +421,14 @@ float or_nv_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, in
 }
 
 /* rounding: 0 = RNE, 1 = SR.  amax_in: if non-NULL, used as the tensor
- * amax instead of computing it.  Outputs: q [rows, cols/2], s_e4m3
+ * amax instead of computing it.  row_offset: index of x's first row in the
+ * full tensor (the SR stream is indexed by the full tensor's linear element
+ * index (row_offset + r) * cols + c).  Outputs: q [rows, cols/2], s_e4m3
  * [rows, cols/16], *s_t_out (the FP32 tensor scale), *amax_out. */
 void or_nv_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
                     int rht, uint64_t rht_seed, int rounding, uint64_t sr_seed,
                     const float* amax_in, float* amax_out, float* s_t_out,
-                    uint8_t* q, uint8_t* s_e4m3) {
+                    uint8_t* q, uint8_t* s_e4m3, int64_t row_offset) {
     float d[16];
     or_rht16_signs(rht_seed, d);
     float amax = amax_in ? *amax_in : or_nv_amax(x, rows, cols, ld_x, rht, rht_seed);
@@ -463,7 +465,7 @@ void or_nv_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
                 } else {
                     float v = y[j] * rcp;
                     if (rounding == 1)
-                        code = or_e2m1_sr_d((double)v, or_sr_word(sr_seed, (uint64_t)(r * cols + c)));
+                        code = or_e2m1_sr_d((double)v, or_sr_word(sr_seed, (uint64_t)((row_offset + r) * cols + c)));
                     else
                         code = or_e2m1_rne_d((double)v);
                 }

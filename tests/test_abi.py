@@ -1,0 +1,106 @@
+"""The C-ABI library loads, exports every entry point include/fp4q.h declares,
+and rejects bad arguments before it touches a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w ]*?[\s\*]+(fp4q_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from micro_scaled_fp4_gb300 import _build
+    _build.build()
+    import micro_scaled_fp4_gb300.fp4q as fq
+    return fq
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ["fp4q_mx_quantize", "fp4q_mx_dequantize", "fp4q_fp4_to_fp8", "fp4q_nv_quantize",
+              "fp4q_block_scaled_gemm", "fp4q_status_string", "fp4q_device_status"]:
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    L = lib.load()
+    missing = [n for n in _declared() if getattr(L, n, None) is None]
+    assert not missing, missing
+    for n in lib.EXPORTED:
+        assert getattr(L, n, None) is not None, n
+
+
+def test_status_strings(lib):
+    for code, name in lib.STATUS_NAMES.items():
+        assert lib.fp4q_status_string(code) == name
+    assert lib.fp4q_status_string(99) == "FP4Q_UNKNOWN_STATUS"
+
+
+def test_scales_bytes(lib):
+    assert lib.fp4q_scales_bytes(256, 128, lib.FP4Q_SCALES_ROWMAJOR) == 256 * 128
+    assert lib.fp4q_scales_bytes(256, 128, lib.FP4Q_SCALES_MMA) == 2 * 32 * 512
+    assert lib.fp4q_scales_bytes(129, 5, lib.FP4Q_SCALES_MMA) == 2 * 2 * 512
+    assert lib.fp4q_scales_bytes(0, 5, lib.FP4Q_SCALES_MMA) == 0
+    assert lib.fp4q_nv_quantize_workspace_bytes(8192, 14336) >= 4
+
+
+def test_argument_errors_need_no_gpu(lib):
+    E = lib.Fp4qError
+    x = 1 << 20           # an aligned, never dereferenced address
+    cases = [
+        (lambda: lib.fp4q_mx_quantize(x, 7, None, 4, 64, 64, 1, x, x, 0, 0), 1),        # bad dtype
+        (lambda: lib.fp4q_mx_quantize(x, 0, None, 4, 48, 64, 1, x, x, 0, 0), 2),        # cols % 32
+        (lambda: lib.fp4q_mx_quantize(x, 0, None, 4, 64, 64, 0, x, x, 0, 0), 2),        # block axis
+        (lambda: lib.fp4q_mx_quantize(x, 2, None, 4, 128, 128, 1, x, x, 0, 0), 1),     # E4M3 w/o scales
+        (lambda: lib.fp4q_mx_quantize(x, 2, x, 4, 96, 96, 1, x, x, 0, 0), 2),          # E4M3 cols % 128
+        (lambda: lib.fp4q_mx_quantize(x + 16, 0, None, 4, 64, 64, 1, x, x, 0, 0), 3),  # x not 32-B aligned
+        (lambda: lib.fp4q_mx_quantize(x, 0, None, 4, 64, 72, 1, x, x, 0, 0), 3),       # ld_x*2 % 32
+        (lambda: lib.fp4q_mx_dequantize(x, x, 4, 64, 1, x, 2, 0), 1),                  # y_type
+        (lambda: lib.fp4q_fp4_to_fp8(x, x, 4, 96, 1, x, x, 0), 2),                     # cols % 128
+        (lambda: lib.fp4q_fp4_to_fp8(None, x, 4, 128, 1, x, x, 0), 1),
+        (lambda: lib.fp4q_nv_quantize(x, 4, 24, 24, 1, 0, 0, 0, 0, None, None, x, x, x, 0, x, 256, 0), 2),
+        (lambda: lib.fp4q_nv_quantize(x, 4, 32, 32, 1, 0, 0, 5, 0, None, None, x, x, x, 0, x, 256, 0), 1),
+        (lambda: lib.fp4q_nv_quantize(x, 4, 32, 32, 1, 0, 0, 0, 0, None, None, x, x, x, 0, None, 0, 0), 1),
+        (lambda: lib.fp4q_nv_quantize(x, 4, 32, 32, 1, 0, 0, 0, 0, None, None, None, x, x, 0, x, 256, 0), 1),
+    ]
+    for fn, status in cases:
+        with pytest.raises(E) as e:
+            fn()
+        assert e.value.status == status, (e.value, status)
+    A = lib.make_operand(x, x, lib.FP4Q_MXFP4)
+    B = lib.make_operand(x, x, lib.FP4Q_NVFP4, x)
+    for args, status in [((A, B, 128, 128, 128, x, 0, 128), 1), ((A, A, 128, 128, 96, x, 0, 128), 2),
+                         ((A, A, 128, 128, 128, x + 2, 0, 128), 3), ((A, A, 128, 128, 128, x, 0, 100), 1),
+                         ((A, A, 128, 128, 128, x, 0, 132), 3)]:
+        with pytest.raises(E) as e:
+            lib.fp4q_block_scaled_gemm(*args, stream=0)
+        assert e.value.status == status, (args, e.value)
+
+
+def test_empty_tensors_are_no_ops(lib):
+    lib.fp4q_mx_quantize(None, 0, None, 0, 64, 64, 1, None, None, 0, 0)
+    lib.fp4q_mx_dequantize(None, None, 0, 64, 1, None, 0, 0)
+    lib.fp4q_fp4_to_fp8(None, None, 5, 0, 1, None, None, 0)
+
+
+def test_no_cpu_fallback_when_library_missing(monkeypatch, tmp_path):
+    # the binding refuses to run without the compiled library (no silent fallback)
+    import micro_scaled_fp4_gb300.fp4q as fq
+    from micro_scaled_fp4_gb300 import _build
+    monkeypatch.setattr(_build, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(fq, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        fq.load()

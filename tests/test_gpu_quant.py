@@ -1,0 +1,273 @@
+"""GPU parity of the streaming kernels against the oracle (bit-exact).
+
+MXFP4 quantize / dequantize, direct FP8 -> MXFP4, scaled MXFP4 -> FP8 and
+NVFP4 quantize (RHT, RNE, SR), called through the C ABI on the same seeded
+inputs as the oracle, at sizes that span several CTAs and ragged row tails,
+and at the full workload sizes the benchmark times.
+"""
+import numpy as np
+import pytest
+
+from _helpers import dev, dev_bf16, from_mma_layout, host, unpack
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fq():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import micro_scaled_fp4_gb300.fp4q as fq
+    fq.load()
+    return fq
+
+
+# ---------------------------------------------------------------------------
+# hardware rounding instructions against the oracle's rounding rules
+# ---------------------------------------------------------------------------
+def test_e2m1_rounding_every_fp32_in_range(fq, oracle):
+    """Every FP32 pattern with |v| in [2^-6, 8), both signs, quantized in blocks
+    whose first element is 4.0 (so E = 0 and the code is the rounding of v
+    itself): GPU codes == oracle round-to-nearest-even codes."""
+    import torch
+    lo_bits, hi_bits = (127 - 6) << 23, (127 + 3) << 23
+    chunk = 31 * (1 << 19)
+    for sign in (0, 1):
+        for start in range(lo_bits, hi_bits, chunk):
+            bits = np.arange(start, min(start + chunk, hi_bits), dtype=np.uint32) | np.uint32(sign << 31)
+            v = bits.view(np.float32)
+            nblk = (v.size + 30) // 31
+            x = np.zeros((nblk, 32), dtype=np.float32)
+            x[:, 0] = 4.0
+            flat = x[:, 1:].reshape(-1)
+            flat[: v.size] = v
+            x[:, 1:] = flat.reshape(nblk, 31)
+            xd = dev(x.reshape(-1, 256) if nblk % 8 == 0 else x)
+            q, s = fq.mx_quantize(xd)
+            torch.cuda.synchronize()
+            codes = unpack(host(q)).reshape(nblk, 32)
+            assert np.all(host(s).reshape(-1) == 127)
+            got = codes[:, 1:].reshape(-1)[: v.size]
+            assert np.array_equal(got, oracle.e2m1_rne(v)), hex(start)
+
+
+def test_e4m3_scale_rounding_all_bf16_block_amax(fq, oracle):
+    """NVFP4 block scale = E4M3 RNE-satfinite of blockamax / (6 s_t): every
+    finite BF16 value as the block's only non-zero element, several tensor
+    amax values supplied by the caller."""
+    import torch
+    b = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f = oracle.bf16_bits_to_f32(b)
+    b = b[np.isfinite(f)]
+    x = np.zeros((b.size, 16), dtype=np.uint16)
+    x[:, 5] = b
+    xd = dev_bf16(x)
+    for amax in (1.0, 3.0e-3, 2.5e4, 1e-30):
+        r = fq.nv_quantize(xd, amax=torch.tensor([amax], dtype=torch.float32, device="cuda"))
+        ref = oracle.nv_quantize(x, amax=np.float32(amax))
+        assert np.array_equal(host(r["scales"]), ref["s"]), amax
+        assert np.array_equal(host(r["q"]), ref["q"]), amax
+        assert host(r["s_t"])[0] == ref["s_t"]
+
+
+# ---------------------------------------------------------------------------
+# MXFP4 quantize / dequantize
+# ---------------------------------------------------------------------------
+SHAPES = [(1, 32), (3, 96), (256, 4096), (129, 7168), (70, 2048 + 32), (5, 14336)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_mx_quantize_bf16(fq, oracle, shape, layout):
+    from micro_scaled_fp4_gb300 import workloads as W
+    R, C = shape
+    rng = np.random.default_rng(R * 7 + C)
+    x32 = (rng.standard_normal((R, C)) * np.exp2(rng.integers(-40, 40, (R, 1)))).astype(np.float32)
+    x32[0, :32] = 0.0                      # an all-zero block
+    if R > 2:
+        x32[2, :] *= np.float32(1e-38)     # subnormal values
+    x = W.to_bf16_bits(x32)
+    q, s = fq.mx_quantize(dev_bf16(x), layout=layout)
+    qr, sr = oracle.mx_quantize(x)
+    assert np.array_equal(host(q), qr)
+    sg = host(s)
+    assert np.array_equal(from_mma_layout(sg, R, C // 32) if layout else sg, sr)
+
+
+def test_mx_quantize_bf16_strided(fq, oracle):
+    from micro_scaled_fp4_gb300 import workloads as W
+    x = W.activation_bf16(64, 1024 + 256, seed=3)
+    xd = dev_bf16(x)[:, 128:128 + 1024]          # ld_x = 1280 elements
+    q, s = fq.mx_quantize(xd)
+    qr, sr = oracle.mx_quantize(np.ascontiguousarray(x[:, 128:128 + 1024]))
+    assert np.array_equal(host(q), qr) and np.array_equal(host(s), sr)
+
+
+@pytest.mark.parametrize("shape", [(3, 96), (256, 4096), (129, 2048)])
+def test_mx_quantize_fp32(fq, oracle, shape):
+    R, C = shape
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal((R, C)) * np.exp2(rng.integers(-60, 60, (R, C // 32)).repeat(32, 1))).astype(np.float32)
+    q, s = fq.mx_quantize(dev(x))
+    qr, sr = oracle.mx_quantize(x)
+    assert np.array_equal(host(q), qr) and np.array_equal(host(s), sr)
+
+
+def test_mx_roundtrip_c1(fq, oracle):
+    """256x4096 BF16 N(0,1), seed 0: quantize then dequantize (BF16 and FP32)."""
+    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
+    x = W.activation_bf16()
+    q, s = fq.mx_quantize(dev_bf16(x))
+    yb = fq.mx_dequantize(q, s, torch.bfloat16)
+    yf = fq.mx_dequantize(q, s, torch.float32)
+    rf, rb = oracle.mx_dequantize(*oracle.mx_quantize(x))
+    assert np.array_equal(host(yb.view(torch.int16)).view(np.uint16), rb)
+    assert np.array_equal(host(yf), rf)
+    # quantize(dequantize(q)) == q
+    q2, s2 = fq.mx_quantize(yb)
+    assert torch.equal(q2, q) and torch.equal(s2, s)
+
+
+def test_mx_dequantize_edge_scales(fq, oracle):
+    import torch
+    rng = np.random.default_rng(2)
+    q = rng.integers(0, 256, (8, 64), dtype=np.uint8)
+    s = np.array([[0, 1, 2, 127], [126, 125, 200, 250], [254, 253, 130, 3], [10, 20, 30, 40]] * 2, dtype=np.uint8)
+    yf = fq.mx_dequantize(dev(q), dev(s), torch.float32)
+    yb = fq.mx_dequantize(dev(q), dev(s), torch.bfloat16)
+    rf, rb = oracle.mx_dequantize(q, s)
+    assert np.array_equal(host(yf).view(np.uint32), rf.view(np.uint32))
+    assert np.array_equal(host(yb.view(torch.int16)).view(np.uint16), rb)
+
+
+# ---------------------------------------------------------------------------
+# Direct FP8 -> MXFP4 and scaled MXFP4 -> FP8
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(1, 128), (37, 1024), (300, 7168)])
+def test_fp8_to_mx_and_back(fq, oracle, shape):
+    from micro_scaled_fp4_gb300 import workloads as W
+    R, C = shape
+    e4, ts = W.fp8_activation(R, C, seed=R, outlier_seed=C)
+    q, s = fq.mx_quantize(dev(e4).view(__import__("torch").float8_e4m3fn), tile_scale=dev(ts))
+    qr, sr = oracle.fp8_to_mx(e4, ts)
+    assert np.array_equal(host(q), qr) and np.array_equal(host(s), sr)
+    y, yts = fq.fp4_to_fp8(q, s)
+    yr, ytsr = oracle.mx_to_fp8(qr, sr)
+    assert np.array_equal(host(y), yr)
+    assert np.array_equal(host(yts).view(np.uint32), ytsr.view(np.uint32))
+
+
+def test_fp4_to_fp8_every_shift(fq, oracle):
+    """Random codes under block exponents spread over the whole E8M0 range, so
+    every shift d in [-254, 0] and every code meets the kernel's remap."""
+    rng = np.random.default_rng(3)
+    R, C = 512, 1024
+    q = rng.integers(0, 256, (R, C // 2), dtype=np.uint8)
+    s = rng.integers(0, 255, (R, C // 32), dtype=np.uint8)
+    s[:, ::8] = 254
+    s[::3, 1::8] = 0
+    s[1::5] = (s[1::5] % 14) + 120          # small spreads: the exact/subnormal region
+    y, ts = fq.fp4_to_fp8(dev(q), dev(s))
+    yr, tsr = oracle.mx_to_fp8(q, s)
+    assert np.array_equal(host(y), yr)
+    assert np.array_equal(host(ts).view(np.uint32), tsr.view(np.uint32))
+
+
+def test_fp8_pipeline_full_size(fq, oracle):
+    """8192x7168 E4M3 activation (0.5 % outlier columns x40, 1x128 tile scales):
+    direct FP8 -> MXFP4, then MXFP4 -> FP8, both bit-exact over the whole tensor."""
+    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
+    e4, ts = W.fp8_activation()
+    q, s = fq.mx_quantize(dev(e4).view(torch.float8_e4m3fn), tile_scale=dev(ts))
+    y, yts = fq.fp4_to_fp8(q, s)
+    qr, sr = oracle.fp8_to_mx(e4, ts)
+    assert np.array_equal(host(q), qr) and np.array_equal(host(s), sr)
+    yr, ytsr = oracle.mx_to_fp8(qr, sr)
+    assert np.array_equal(host(y), yr)
+    assert np.array_equal(host(yts).view(np.uint32), ytsr.view(np.uint32))
+    # lossless: the FP8 copy represents the MXFP4 values exactly (no flush here)
+    e8 = oracle.e4m3_values()[yr[:64]] * np.repeat(ytsr[:64].astype(np.float64), 128, axis=1)
+    assert np.array_equal(e8, oracle.mx_dequantize_f64(qr[:64], sr[:64]))
+
+
+# ---------------------------------------------------------------------------
+# NVFP4
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(1, 16), (5, 48), (129, 2048), (64, 14336)])
+@pytest.mark.parametrize("rht", [False, True])
+@pytest.mark.parametrize("rounding", [0, 1])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_nv_quantize(fq, oracle, shape, rht, rounding, layout):
+    from micro_scaled_fp4_gb300 import workloads as W
+    R, C = shape
+    x = W.gradient_bf16(R, C, seed=R + C)
+    r = fq.nv_quantize(dev_bf16(x), rht=rht, rht_seed=7, rounding=rounding, sr_seed=1234, layout=layout)
+    ref = oracle.nv_quantize(x, rht=rht, rht_seed=7, rounding="sr" if rounding else "rne", sr_seed=1234)
+    assert host(r["amax"])[0] == ref["amax"]
+    assert host(r["s_t"])[0] == ref["s_t"]
+    assert np.array_equal(host(r["q"]), ref["q"])
+    sg = host(r["scales"])
+    assert np.array_equal(from_mma_layout(sg, R, C // 16) if layout else sg, ref["s"])
+
+
+def test_nv_quantize_zero_and_tiny(fq, oracle):
+    x = np.zeros((4, 64), dtype=np.uint16)
+    r = fq.nv_quantize(dev_bf16(x))
+    ref = oracle.nv_quantize(x)
+    assert host(r["s_t"])[0] == 0.0
+    assert np.array_equal(host(r["q"]), ref["q"]) and np.array_equal(host(r["scales"]), ref["s"])
+    x[1, 3] = 0x8000                      # -0.0
+    x[2, :] = 0x0001                      # smallest BF16 subnormal
+    x[3, 0] = 0x4000                      # 2.0: makes the subnormal blocks' scales underflow
+    r = fq.nv_quantize(dev_bf16(x))
+    ref = oracle.nv_quantize(x)
+    assert np.array_equal(host(r["q"]), ref["q"]) and np.array_equal(host(r["scales"]), ref["s"])
+
+
+def test_nv_quantize_full_size_sampled(fq, oracle):
+    """8192x14336 Student-t(3)*1e-3 gradient with the RHT (seed 7): SR pass
+    (seed 1234) then RNE pass, as the benchmark runs them.  The tensor amax is
+    checked exactly; codes and scales on 96 sampled rows (the oracle quantizes
+    those rows with the full tensor's amax)."""
+    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
+    x = W.gradient_bf16()
+    xd = dev_bf16(x)
+    rows = np.sort(np.random.default_rng(0).choice(x.shape[0], 96, replace=False))
+    amax = oracle.nv_amax(x, True, 7)
+    for rounding in (1, 0):
+        r = fq.nv_quantize(xd, rht=True, rht_seed=7, rounding=rounding, sr_seed=1234)
+        assert host(r["amax"])[0] == np.float32(amax)
+        qg, sg = host(r["q"]), host(r["scales"])
+        for i in rows:
+            ref = oracle.nv_quantize(x[i:i + 1], rht=True, rht_seed=7, rounding="sr" if rounding else "rne",
+                                     sr_seed=1234, amax=amax, row_offset=int(i))
+            assert np.array_equal(qg[i], ref["q"][0]), i
+            assert np.array_equal(sg[i], ref["s"][0]), i
+
+
+# ---------------------------------------------------------------------------
+# argument validation through the C ABI (no launch happens)
+# ---------------------------------------------------------------------------
+def test_argument_errors(fq):
+    import torch
+    x = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((4, 32), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((4, 2), dtype=torch.uint8, device="cuda")
+    with pytest.raises(fq.Fp4qError) as e:
+        fq.fp4q_mx_quantize(x, 0, None, 4, 48, 64, 1, q, s, 0)
+    assert e.value.status == 2
+    with pytest.raises(fq.Fp4qError) as e:
+        fq.fp4q_mx_quantize(x, 0, None, 4, 64, 64, 0, q, s, 0)
+    assert e.value.status == 2
+    with pytest.raises(fq.Fp4qError) as e:
+        fq.fp4q_mx_quantize(None, 0, None, 4, 64, 64, 1, q, s, 0)
+    assert e.value.status == 1
+    with pytest.raises(fq.Fp4qError) as e:
+        fq.fp4q_mx_quantize(x.data_ptr() + 2, 0, None, 4, 64, 64, 1, q, s, 0)
+    assert e.value.status == 3
+    # empty tensors are fine and launch nothing
+    fq.fp4q_mx_quantize(None, 0, None, 0, 64, 64, 1, None, None, 0)
