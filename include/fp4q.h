@@ -25,7 +25,8 @@
  *                (rt * ceil(S/4) + ct) * 512); inside a tile, scale (r, c)
  *                sits at byte (r % 32) * 16 + (r / 32) * 4 + c.  Size:
  *                fp4q_scales_bytes().  Padding entries are not written.
- *  - Pointers to packed data, scales and outputs must be 16-byte aligned.
+ *  - Pointers to packed data, scales and outputs must be 16-byte aligned
+ *    (32-byte where a call says so).
  *
  * The operations follow three web pages:
  *  [MXN] "Pretraining large language models with MXFP4 on Native FP4
@@ -88,8 +89,8 @@ size_t fp4q_scales_bytes(int64_t rows, int64_t scale_cols, fp4q_scale_layout lay
  * quantized straight to FP4 with no BF16 intermediate: element value =
  * decode(e4m3) * tile_scale[r, c / 128] (one FP32 multiply), then the rule
  * above.
- *   x          device, [rows, ld_x] elements of x_type (ld_x >= cols; for
- *              E4M3 ld_x % 16 == 0, for BF16 ld_x % 8 == 0, FP32 ld_x % 4 == 0)
+ *   x          device, [rows, ld_x] elements of x_type, ld_x >= cols; x must
+ *              be 32-byte aligned and ld_x * element size a multiple of 32 bytes
  *   tile_scale device FP32 [rows, cols/128] when x_type == FP4Q_E4M3
  *              (cols % 128 == 0), else NULL
  *   cols       multiple of 32
@@ -105,7 +106,7 @@ fp4q_status fp4q_mx_quantize(const void* x, fp4q_dtype x_type, const float* tile
  * fp4q_mx_dequantize -- MXFP4 -> BF16 / FP32: y = 2^E * value(code), exact
  * (rounded only where it overflows the output type).  [MXN] reconstruction.
  *   q       device, [rows, cols/2];  scales device, ROWMAJOR E8M0 [rows, cols/32]
- *   y       device out, [rows, cols] of y_type (FP4Q_BF16 or FP4Q_FP32)
+ *   y       device out, [rows, cols] of y_type (FP4Q_BF16 or FP4Q_FP32), 32-byte aligned
  */
 fp4q_status fp4q_mx_dequantize(const uint8_t* q, const uint8_t* scales, int64_t rows,
                                int64_t cols, int block_axis, void* y, fp4q_dtype y_type,
@@ -122,7 +123,7 @@ fp4q_status fp4q_mx_dequantize(const uint8_t* q, const uint8_t* scales, int64_t 
  * values are exact whenever E_i - Emax >= -8.
  *   q           device, [rows, cols/2];  scales device, ROWMAJOR E8M0 [rows, cols/32]
  *   cols        multiple of 128
- *   y           device out, E4M3 [rows, cols]
+ *   y           device out, E4M3 [rows, cols], 32-byte aligned
  *   tile_scale  device out, FP32 [rows, cols/128]
  */
 fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, int64_t rows,
@@ -143,7 +144,8 @@ fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, int64_t row
  * rounding == FP4Q_SR rounds each element up with probability equal to its
  * distance fraction: up iff r < frac * 2^32, r the (i mod 4)-th word of
  * Philox4x32-10(key = sr_seed, counter = i / 4), i = row * cols + col.
- *   x                device BF16 [rows, ld_x], ld_x % 8 == 0;  cols % 16 == 0
+ *   x                device BF16 [rows, ld_x], 32-byte aligned, ld_x % 16 == 0;
+ *                    cols % 16 == 0
  *   amax_in          device FP32 scalar or NULL (NULL: computed, two passes)
  *   amax_out         device FP32 scalar out or NULL
  *   tensor_scale_out device FP32 scalar out (s_t)
@@ -183,6 +185,87 @@ typedef struct fp4q_operand {
 fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M,
                                    int64_t N, int64_t K, void* D, fp4q_dtype d_type,
                                    int64_t ldd, fp4q_stream_t stream);
+
+/*
+ * ---------------------------------------------------------------------------
+ * MoE expert FFN in FP4 ("Practical FP4 Training for Large-Scale MoE Models
+ * on Hopper GPUs", section 2.A: activations are quantized to MXFP4 before the
+ * expert dispatch; section 2.C: ragged per-expert tensors with precomputed
+ * offsets and no padding; section 4: the expert layers dominate the compute).
+ * ---------------------------------------------------------------------------
+ */
+
+/*
+ * fp4q_moe_dispatch -- group the MXFP4 rows of the tokens by expert.
+ * Dispatched row p of expert e (offsets[e] <= p < offsets[e+1]) is a copy of
+ * the codes and E8M0 bytes of one token that chose e; inside an expert the
+ * tokens are in ascending order (stable).  Ragged, no padding.
+ *   topk        device int32 [tokens, top_k]: the experts of each token,
+ *               distinct per token, in [0, n_experts) (other ids are dropped)
+ *   q, scales   device, the tokens' MXFP4 codes [tokens, cols/2] and ROWMAJOR
+ *               E8M0 [tokens, cols/32]; cols % 32 == 0
+ *   offsets     device int64 out [n_experts + 1]
+ *   row_token   device int32 out [tokens * top_k]: token of each dispatched row
+ *   q_out, scales_out  device out [tokens * top_k, cols/2], [tokens * top_k, cols/32]
+ *   workspace   device, >= fp4q_moe_dispatch_workspace_bytes(), 16-byte aligned
+ * Limits: 1 <= top_k <= 16, 1 <= n_experts <= 256.
+ */
+size_t fp4q_moe_dispatch_workspace_bytes(int64_t tokens, int top_k, int n_experts);
+fp4q_status fp4q_moe_dispatch(const int32_t* topk, int64_t tokens, int top_k, int n_experts,
+                              const uint8_t* q, const uint8_t* scales, int64_t cols,
+                              int64_t* offsets, int32_t* row_token, uint8_t* q_out,
+                              uint8_t* scales_out, void* workspace, size_t workspace_bytes,
+                              fp4q_stream_t stream);
+
+/*
+ * fp4q_mx_rebase_scales -- MXFP4 block scales -> UE4M3 per-16 scales + a row
+ * factor, so MXFP4 rows can meet NVFP4 operands in one block-scaled MMA.
+ * Per row r: B_r = max_j E_j - 8; each 32-block's 2^E_j becomes the UE4M3
+ * value 2^(E_j - B_r) for both 16-element halves; row_scale[r] = 2^B_r.
+ * Exact when E_j >= B_r - 9 for every block; blocks below that get scale 0
+ * and are counted in *violations (if non-NULL; the caller zeroes it).
+ * Output in the MMA layout with every group padded to whole 128-row tiles
+ * (group g's tiles follow those of groups < g).
+ *   scales     device ROWMAJOR E8M0 [rows, cols/32];  cols % 128 == 0
+ *   offsets    device int64 [groups + 1] row offsets (rows beyond offsets[groups] ignored)
+ *   ue4m3_mma  device out, fp4q_rebased_scales_bytes(rows, cols, groups) bytes
+ *   row_scale  device FP32 out [rows]
+ */
+size_t fp4q_rebased_scales_bytes(int64_t rows, int64_t cols, int64_t groups);
+fp4q_status fp4q_mx_rebase_scales(const uint8_t* scales, int64_t rows, int64_t cols,
+                                  const int64_t* offsets, int64_t groups, uint8_t* ue4m3_mma,
+                                  float* row_scale, uint32_t* violations, fp4q_stream_t stream);
+
+typedef enum fp4q_epilogue {
+    FP4Q_EPI_STORE_BF16 = 0,       /* D = BF16(acc * row_scale * tensor_scale[g])           */
+    FP4Q_EPI_SILU_GATE_MXFP4 = 1   /* h = SiLU(U[:, :N/2]) * U[:, N/2:], U = acc * factors;
+                                      h -> MXFP4 (codes into D, E8M0 into d_scales)         */
+} fp4q_epilogue;
+
+/*
+ * fp4q_grouped_gemm -- per group g: rows offsets[g] .. offsets[g+1] of A times
+ * B_g^T (the MoE expert GEMMs on tcgen05, kind::mxf4nvf4 with UE4M3 per 16).
+ *   a_q            device [rows, K/2] packed codes (dispatched rows)
+ *   a_scales       device, UE4M3 per 16 in the padded MMA layout of
+ *                  fp4q_mx_rebase_scales (or NVFP4 scales laid out the same way)
+ *   a_row_scale    device FP32 [rows]
+ *   b_q            device [groups, N, K/2];  b_scales device, the groups' NVFP4
+ *                  E4M3 scales in MMA layout, back to back;  b_tensor_scale
+ *                  device FP32 [groups]
+ *   offsets        device int64 [groups + 1]
+ *   N, K           N % 128 == 0 (gated: N % 256 == 0), K % 128 == 0
+ *   D              STORE_BF16: device BF16 [rows, N];  SILU_GATE: device codes
+ *                  [rows, N/4] (h has N/2 columns)
+ *   d_scales       SILU_GATE: device ROWMAJOR E8M0 [rows, N/64]; else unused
+ *   h_debug        SILU_GATE: optional device FP32 [rows, N/2] copy of h before
+ *                  quantization (NULL: not written)
+ * FP32 accumulation; limits: 1 <= groups <= 256.
+ */
+fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_scales, const float* a_row_scale,
+                              const uint8_t* b_q, const uint8_t* b_scales, const float* b_tensor_scale,
+                              const int64_t* offsets, int64_t rows, int64_t groups, int64_t N,
+                              int64_t K, fp4q_epilogue epilogue, void* D, uint8_t* d_scales,
+                              float* h_debug, fp4q_stream_t stream);
 
 /*
  * fp4q_device_status -- read (and, if reset != 0, clear) the device status

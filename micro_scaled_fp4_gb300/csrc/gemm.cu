@@ -1,24 +1,30 @@
-// Block-scaled FP4 GEMM D = A . B^T on the sm_103a tensor cores.
+// Block-scaled FP4 GEMMs on the sm_103a tensor cores: dense D = A . B^T and
+// the grouped (per-expert, ragged) form of the MoE expert FFN.
 //
 // "Pretraining large language models with MXFP4 on Native FP4 Hardware",
 // investigation section: the forward GEMM of a linear layer Y = X W^T with
 // both operands in FP4 along the reduction axis, run on native FP4 tensor
 // cores.  "Pretraining Large Language Models with NVFP4", section 2: NVFP4
 // operands (E4M3 scale per 16, FP32 tensor scale); a Hadamard rotation of
-// both operands along K cancels in the product.
+// both operands along K cancels in the product.  "Practical FP4 Training for
+// Large-Scale MoE Models on Hopper GPUs", section 2: MoE expert GEMMs over
+// ragged per-expert row groups located by precomputed offsets, no padding.
 //
 // Persistent, warp-specialised kernel, one CTA per SM, 128 x 256 output tile
 // per step, K consumed 256 elements (128 bytes) per pipeline stage:
-//   warp 0      TMA producer: A and B tiles (128-byte swizzle) and the
-//               stage's block scales (contiguous chunks of the MMA scale
-//               layout) into a 4-stage shared-memory ring.
+//   warp 0      TMA producer: A and B tiles (128-byte swizzle; B as two
+//               128-row halves) and the stage's block scales (contiguous
+//               chunks of the MMA scale layout) into a 4-stage ring.
 //   warp 1      allocates TMEM; one thread issues tcgen05.cp (scales ->
 //               TMEM) and tcgen05.mma kind::mxf4 (UE8M0 per 32) or
 //               kind::mxf4nvf4 (UE4M3 per 16), FP32 accumulator in TMEM.
 //   warps 2..5  epilogue: tcgen05.ld of the 128 x 256 FP32 accumulator,
-//               tensor-scale multiply (NVFP4), BF16 round-to-nearest-even
-//               or FP32, stores; the accumulator is handed back to the MMA
-//               thread as soon as it has been read.
+//               one row per thread; the accumulator goes back to the MMA
+//               thread as soon as it has been read.  STORE: scale, BF16
+//               (round to nearest even) or FP32 stores.  SILU_GATE: the two
+//               B halves are the gate and up rows of the same 128 outputs;
+//               h = SiLU(gate) * up in FP32, then MXFP4 (one 32-element
+//               block per 32 accumulator columns) straight from registers.
 // Every mbarrier wait is bounded in time; a wait that gives up sets a bit in
 // the library's status word, tells the other roles to stop, and the kernel
 // drains its own asynchronous work and frees TMEM before returning.
@@ -34,9 +40,10 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 256;           // elements
 constexpr int STAGES = 4;
 constexpr uint32_t A_BYTES = BM * BK / 2;             // 16384
-constexpr uint32_t B_BYTES = BN * BK / 2;             // 32768
+constexpr uint32_t B_HALF_BYTES = 128 * BK / 2;       // 16384
+constexpr uint32_t B_BYTES = 2 * B_HALF_BYTES;
 constexpr uint32_t SFA_BYTES = 4 * 512;               // up to 4 chunks (NVFP4)
-constexpr uint32_t SFB_BYTES = 2 * 4 * 512;           // 2 row tiles x 4 chunks
+constexpr uint32_t SFB_BYTES = 2 * 4 * 512;           // 2 halves x 4 chunks
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;   // 55296
 constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
 constexpr int kThreads = 192;
@@ -44,30 +51,85 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SFA = 256;                    // 16 columns
 constexpr uint32_t TMEM_SFB = 272;                    // 32 columns
 constexpr uint64_t kWaitLimitNs = 4000000000ull;      // 4 s
+constexpr int kMaxGroups = 256;
+
+enum Epi { kStore = 0, kSiluGate = 1 };
 
 struct GemmArgs {
+    // dense: M rows of A, N rows of B.  grouped: rows of the dispatched A,
+    // N rows of each group's B.
     int M, N, K;
-    int m_tiles, n_tiles, k_stages;
-    int nv;                          // 0 = MXFP4, 1 = NVFP4
+    int n_tiles;                     // output tiles along N
+    int k_stages;
+    int nv;                          // 0 = MXFP4 (UE8M0 / 32), 1 = UE4M3 / 16
+    int groups;                      // 0 = dense
+    const int64_t* offsets;          // grouped: [groups + 1] row offsets
     const uint8_t* sfa;
     const uint8_t* sfb;
-    uint64_t sfa_tile_stride;        // bytes per 128-row tile of A's scales
-    uint64_t sfb_tile_stride;
-    const float* ts_a;
-    const float* ts_b;
-    uint8_t* D;
-    int64_t ldd;                     // elements
+    uint64_t sf_tile_stride;         // bytes per 128-row tile of scales (A and B)
+    const float* ts_a;               // dense NVFP4: A tensor scale
+    const float* ts_b;               // dense NVFP4: B tensor scale; grouped: [groups]
+    const float* a_row_scale;        // grouped: per-row factor of A
+    uint8_t* D;                      // STORE: [rows, ldd]; SILU_GATE: h codes [rows, N/4]
+    int64_t ldd;                     // STORE: elements
     int d_bf16;
+    uint8_t* h_scales;               // SILU_GATE: E8M0 [rows, N/64]
+    float* h_debug;                  // SILU_GATE: optional FP32 h [rows, N/2]
     uint32_t* status;
+    uint32_t status_bit;
 };
 
-__device__ __forceinline__ void flag_abort(volatile int* abort, uint32_t* status) {
+struct TileInfo {
+    int a_row0;       // first A row of the tile
+    int row_end;      // rows >= row_end are not stored
+    int a_sf_tile;    // 128-row scale tile of A
+    int b_row0;       // first B row of each half (b_row1 < 0: half absent)
+    int b_row1;
+    int group;
+    int col0;         // first output column
+};
+
+__device__ __forceinline__ void flag_abort(volatile int* abort, uint32_t* status, uint32_t bit) {
     if (!*abort) {
         *abort = 1;
-        atomicOr(status, kStatusGemmTimeout);
+        atomicOr(status, bit);
     }
 }
 
+// Output tile `tile` -> rows / columns / scale tiles.  Grouped tiles run
+// N-fastest, so the CTAs working at one time share A rows and one group's B.
+template <int EPI>
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile, const int* tile_prefix, int m_tiles) {
+    TileInfo t;
+    const int nt = a.groups ? tile % a.n_tiles : tile / m_tiles;
+    const int mt = a.groups ? tile / a.n_tiles : tile % m_tiles;
+    if (a.groups) {
+        int e = 0;
+        while (e + 1 < a.groups && tile_prefix[e + 1] <= mt) ++e;
+        const int local = mt - tile_prefix[e];
+        t.group = e;
+        t.a_row0 = int(a.offsets[e]) + local * BM;
+        t.row_end = int(a.offsets[e + 1]);
+    } else {
+        t.group = 0;
+        t.a_row0 = mt * BM;
+        t.row_end = a.M;
+    }
+    t.a_sf_tile = mt;
+    const int gbase = t.group * a.N;
+    if (EPI == kSiluGate) {
+        t.b_row0 = gbase + nt * 128;
+        t.b_row1 = gbase + a.N / 2 + nt * 128;
+        t.col0 = nt * 128;
+    } else {
+        t.b_row0 = gbase + nt * BN;
+        t.b_row1 = (nt * BN + 128 < a.N) ? t.b_row0 + 128 : -1;
+        t.col0 = nt * BN;
+    }
+    return t;
+}
+
+template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const GemmArgs args) {
@@ -77,6 +139,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     // bars[0..3] full, [4..7] empty, [8] tmem_full, [9] tmem_empty, [10] mma drain
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
     volatile int* abort = reinterpret_cast<volatile int*>(bars + 13);
+    __shared__ int tile_prefix[kMaxGroups + 1];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bar0 = tc::smem_u32(bars);
@@ -96,6 +159,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&tmap_a);
         tc::tma_prefetch_desc(&tmap_b);
+        // 128-row tiles per group, prefix-summed (grouped form)
+        int acc = 0;
+        tile_prefix[0] = 0;
+        for (int e = 0; e < args.groups; ++e) {
+            const int n = int(args.offsets[e + 1] - args.offsets[e]);
+            acc += (n + BM - 1) / BM;
+            tile_prefix[e + 1] = acc;
+        }
     }
     if (warp == 1) {
         tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
@@ -106,7 +177,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    const int num_tiles = args.m_tiles * args.n_tiles;
+    const int m_tiles = args.groups ? tile_prefix[args.groups] : (args.M + BM - 1) / BM;
+    const int num_tiles = m_tiles * args.n_tiles;
     const uint32_t chunk_elems = args.nv ? 64 : 128;  // K elements per 512-byte scale chunk
 
     if (warp == 0 && lane == 0) {
@@ -116,33 +188,33 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         int issued = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            const int mt = tile % args.m_tiles, nt = tile / args.m_tiles;
+            const TileInfo t = decode_tile<EPI>(args, tile, tile_prefix, m_tiles);
             for (int kb = 0; kb < args.k_stages; ++kb) {
                 if (!tc::mbar_wait(empty_bar(stage), phase ^ 1, abort, kWaitLimitNs)) {
-                    flag_abort(abort, args.status);
+                    flag_abort(abort, args.status, args.status_bit);
                     ok = false;
                     break;
                 }
                 const int k_elems = min(BK, args.K - kb * BK);
                 const uint32_t chunks = uint32_t(k_elems) / chunk_elems;
-                const uint32_t ct0 = uint32_t(kb * BK) / chunk_elems;
-                const bool rt1 = (2 * nt + 1) * 128 < args.N;
-                const uint32_t sf_bytes = chunks * 512u * (rt1 ? 3u : 2u);
+                const uint64_t ct0 = uint64_t(kb * BK) / chunk_elems;
+                const uint32_t sf_bytes = chunks * 512u * (t.b_row1 >= 0 ? 3u : 2u);
                 uint8_t* st = smem + stage * STAGE_BYTES;
                 const uint32_t fb = full_bar(stage);
                 tc::mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + sf_bytes);
-                tc::tma_load_2d(tc::smem_u32(st), &tmap_a, fb, kb * (BK / 2), mt * BM);
-                tc::tma_load_2d(tc::smem_u32(st + A_BYTES), &tmap_b, fb, kb * (BK / 2), nt * BN);
+                tc::tma_load_2d(tc::smem_u32(st), &tmap_a, fb, kb * (BK / 2), t.a_row0);
+                tc::tma_load_2d(tc::smem_u32(st + A_BYTES), &tmap_b, fb, kb * (BK / 2), t.b_row0);
+                // an absent second half still lands: rows past the end are zero-filled
+                tc::tma_load_2d(tc::smem_u32(st + A_BYTES + B_HALF_BYTES), &tmap_b, fb, kb * (BK / 2),
+                                t.b_row1 >= 0 ? t.b_row1 : t.b_row0 + 128);
                 tc::bulk_load(tc::smem_u32(st + A_BYTES + B_BYTES),
-                              args.sfa + uint64_t(mt) * args.sfa_tile_stride + uint64_t(ct0) * 512u,
-                              chunks * 512u, fb);
+                              args.sfa + uint64_t(t.a_sf_tile) * args.sf_tile_stride + ct0 * 512u, chunks * 512u, fb);
                 uint8_t* sfb_smem = st + A_BYTES + B_BYTES + SFA_BYTES;
                 tc::bulk_load(tc::smem_u32(sfb_smem),
-                              args.sfb + uint64_t(2 * nt) * args.sfb_tile_stride + uint64_t(ct0) * 512u,
-                              chunks * 512u, fb);
-                if (rt1)
+                              args.sfb + uint64_t(t.b_row0 / 128) * args.sf_tile_stride + ct0 * 512u, chunks * 512u, fb);
+                if (t.b_row1 >= 0)
                     tc::bulk_load(tc::smem_u32(sfb_smem + 4 * 512),
-                                  args.sfb + uint64_t(2 * nt + 1) * args.sfb_tile_stride + uint64_t(ct0) * 512u,
+                                  args.sfb + uint64_t(t.b_row1 / 128) * args.sf_tile_stride + ct0 * 512u,
                                   chunks * 512u, fb);
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -151,7 +223,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         // drain: every stage issued last must have landed before the CTA exits
         for (int i = 0; i < STAGES && i < issued; ++i) {
             if (--stage < 0) { stage = STAGES - 1; phase ^= 1; }
-            if (!tc::mbar_wait(full_bar(stage), phase, abort, kWaitLimitNs)) { flag_abort(abort, args.status); break; }
+            if (!tc::mbar_wait(full_bar(stage), phase, abort, kWaitLimitNs)) {
+                flag_abort(abort, args.status, args.status_bit);
+                break;
+            }
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
@@ -161,13 +236,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tcount) {
             if (!tc::mbar_wait(tmem_empty, (tcount & 1) ^ 1, abort, kWaitLimitNs)) {
-                flag_abort(abort, args.status);
+                flag_abort(abort, args.status, args.status_bit);
                 break;
             }
             tc::fence_after_sync();
             for (int kb = 0; kb < args.k_stages; ++kb) {
                 if (!tc::mbar_wait(full_bar(stage), phase, abort, kWaitLimitNs)) {
-                    flag_abort(abort, args.status);
+                    flag_abort(abort, args.status, args.status_bit);
                     ok = false;
                     break;
                 }
@@ -180,7 +255,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 const uint32_t ssfa = tc::smem_u32(st + A_BYTES + B_BYTES);
                 const uint32_t ssfb = tc::smem_u32(st + A_BYTES + B_BYTES + SFA_BYTES);
                 // block scales -> TMEM: chunk c of A at column TMEM_SFA + 4c, chunk c
-                // of B's row tile r at TMEM_SFB + 8c + 4r
+                // of B's half h at TMEM_SFB + 8c + 4h
                 for (uint32_t c = 0; c < chunks; ++c) {
                     tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFA + 4 * c, tc::smem_desc(ssfa + 512 * c, 0, 128, 0));
                     tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c, tc::smem_desc(ssfb + 512 * c, 0, 128, 0));
@@ -207,64 +282,116 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             if (!ok) break;
             tc::tc_commit(tmem_full);
         }
-        // drain: all MMAs and scale copies of this thread complete
-        tc::tc_commit(drain_bar);
-        if (!tc::mbar_wait(drain_bar, 0, abort, kWaitLimitNs)) flag_abort(abort, args.status);
+        // drain: all MMAs and scale copies of this thread complete (a CTA that got
+        // no tile issued none)
+        if (tcount > 0 || !ok) {
+            tc::tc_commit(drain_bar);
+            if (!tc::mbar_wait(drain_bar, 0, abort, kWaitLimitNs)) flag_abort(abort, args.status, args.status_bit);
+        }
     } else if (warp >= 2) {
         // ---------------- epilogue ----------------
         const int q = warp & 3;                         // TMEM lane quadrant of this warp
-        const float alpha = args.nv ? __fmul_rn(*args.ts_a, *args.ts_b) : 1.0f;
+        const float dense_alpha = (!args.groups && args.nv) ? __fmul_rn(*args.ts_a, *args.ts_b) : 1.0f;
         int tcount = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
             if (!tc::mbar_wait(tmem_full, tcount & 1, abort, kWaitLimitNs)) {
-                flag_abort(abort, args.status);
+                flag_abort(abort, args.status, args.status_bit);
                 break;
             }
             tc::fence_after_sync();
-            const int mt = tile % args.m_tiles, nt = tile / args.m_tiles;
-            const int row = mt * BM + q * 32 + lane;
-            const int col0 = nt * BN;
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tc::tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(c * 32), r);
-                tc::tmem_ld_wait();
-                if (c == BN / 32 - 1) {
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(tmem_empty);
+            const TileInfo t = decode_tile<EPI>(args, tile, tile_prefix, m_tiles);
+            const int row = t.a_row0 + q * 32 + lane;
+            const bool row_ok = row < t.row_end;
+            float alpha = dense_alpha;
+            if (args.groups && row_ok) alpha = __fmul_rn(args.a_row_scale[row], args.ts_b[t.group]);
+            const uint32_t lane_addr = tmem + (uint32_t(q * 32) << 16);
+            if constexpr (EPI == kSiluGate) {
+                const int hcols = args.N / 2;
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t g[32], u[32];
+                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(c * 32), g);
+                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(128 + c * 32), u);
+                    tc::tmem_ld_wait();
+                    if (c == 3) {
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(tmem_empty);
+                    }
+                    if (!row_ok) continue;
+                    float h[32];
+                    uint32_t amax = 0;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float gv = __fmul_rn(u2f(g[i]), alpha);
+                        const float uv = __fmul_rn(u2f(u[i]), alpha);
+                        const float sig = __fdiv_rn(gv, __fadd_rn(1.0f, expf(-gv)));   // SiLU
+                        h[i] = __fmul_rn(sig, uv);
+                        amax = max(amax, f2u(h[i]) & 0x7fffffffu);
+                    }
+                    const int col = t.col0 + c * 32;
+                    if (args.h_debug) {
+                        float4* dbg = reinterpret_cast<float4*>(args.h_debug + int64_t(row) * hcols + col);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) dbg[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                    }
+                    const int e = mx_exponent_from_amax_bits(amax);
+                    const float inv = exp2i(-e);
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t v = 0;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            v |= cvt_e2m1x2(__fmul_rn(h[8 * k + 2 * j], inv), __fmul_rn(h[8 * k + 2 * j + 1], inv))
+                                 << (8 * j);
+                        w[k] = v;
+                    }
+                    *reinterpret_cast<uint4*>(args.D + int64_t(row) * (hcols / 2) + col / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+                    args.h_scales[int64_t(row) * (hcols / 32) + col / 32] = uint8_t(e + 127);
                 }
-                const int col = col0 + c * 32;
-                if (row >= args.M || col >= args.N) continue;
-                const int ncol = min(32, args.N - col);
-                if (args.d_bf16) {
-                    uint32_t p[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float lo = __fmul_rn(u2f(r[2 * i]), alpha), hi = __fmul_rn(u2f(r[2 * i + 1]), alpha);
-                        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(p[i]) : "f"(hi), "f"(lo));
+            } else {
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(c * 32), r);
+                    tc::tmem_ld_wait();
+                    if (c == BN / 32 - 1) {
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(tmem_empty);
                     }
-                    uint8_t* dst = args.D + (int64_t(row) * args.ldd + col) * 2;
-                    if (ncol == 32) {
+                    const int col = t.col0 + c * 32;
+                    if (!row_ok || col >= args.N) continue;
+                    const int ncol = min(32, args.N - col);
+                    if (args.d_bf16) {
+                        uint32_t p[16];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            reinterpret_cast<uint4*>(dst)[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+                        for (int i = 0; i < 16; ++i) {
+                            const float lo = __fmul_rn(u2f(r[2 * i]), alpha), hi = __fmul_rn(u2f(r[2 * i + 1]), alpha);
+                            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(p[i]) : "f"(hi), "f"(lo));
+                        }
+                        uint8_t* dst = args.D + (int64_t(row) * args.ldd + col) * 2;
+                        if (ncol == 32) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                reinterpret_cast<uint4*>(dst)[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (i < ncol) reinterpret_cast<uint16_t*>(dst)[i] = uint16_t(p[i >> 1] >> (16 * (i & 1)));
+                        }
                     } else {
+                        float* dst = reinterpret_cast<float*>(args.D) + int64_t(row) * args.ldd + col;
+                        if (ncol == 32) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (i < ncol) reinterpret_cast<uint16_t*>(dst)[i] = uint16_t(p[i >> 1] >> (16 * (i & 1)));
-                    }
-                } else {
-                    float* dst = reinterpret_cast<float*>(args.D) + int64_t(row) * args.ldd + col;
-                    if (ncol == 32) {
+                            for (int i = 0; i < 8; ++i)
+                                reinterpret_cast<float4*>(dst)[i] =
+                                    make_float4(__fmul_rn(u2f(r[4 * i]), alpha), __fmul_rn(u2f(r[4 * i + 1]), alpha),
+                                                __fmul_rn(u2f(r[4 * i + 2]), alpha), __fmul_rn(u2f(r[4 * i + 3]), alpha));
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            reinterpret_cast<float4*>(dst)[i] =
-                                make_float4(__fmul_rn(u2f(r[4 * i]), alpha), __fmul_rn(u2f(r[4 * i + 1]), alpha),
-                                            __fmul_rn(u2f(r[4 * i + 2]), alpha), __fmul_rn(u2f(r[4 * i + 3]), alpha));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (i < ncol) dst[i] = __fmul_rn(u2f(r[i]), alpha);
+                            for (int i = 0; i < 32; ++i)
+                                if (i < ncol) dst[i] = __fmul_rn(u2f(r[i]), alpha);
+                        }
                     }
                 }
             }
@@ -295,17 +422,34 @@ fp4q_status get_encoder() {
     return FP4Q_OK;
 }
 
-// 2D map over packed FP4 bytes [rows, K/2], box (128 bytes) x box_rows, 128B swizzle.
-fp4q_status encode_operand_map(CUtensorMap* map, const uint8_t* q, int64_t rows, int64_t K, uint32_t box_rows) {
+// 2D map over packed FP4 bytes [rows, K/2]: 128-byte x 128-row boxes, 128B swizzle.
+fp4q_status encode_operand_map(CUtensorMap* map, const uint8_t* q, int64_t rows, int64_t K) {
     cuuint64_t dims[2] = {cuuint64_t(K / 2), cuuint64_t(rows)};
     cuuint64_t strides[1] = {cuuint64_t(K / 2)};
-    cuuint32_t box[2] = {128u, box_rows};
+    cuuint32_t box[2] = {128u, 128u};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(q), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(FP4Q_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
     return FP4Q_OK;
+}
+
+template <int EPI>
+fp4q_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int tiles_upper, int sms,
+                   cudaStream_t stream) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_set[dev & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(SMEM_BYTES));
+        if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
+        attr_set[dev & 63] = true;
+    }
+    const int grid = tiles_upper < sms ? tiles_upper : sms;
+    gemm_kernel<EPI><<<grid, kThreads, SMEM_BYTES, stream>>>(ma, mb, a);
+    return check_launch("block_scaled_gemm");
 }
 
 }  // namespace
@@ -323,7 +467,7 @@ extern "C" fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_
         return fail(FP4Q_ERR_INVALID_ARGUMENT, "gemm: d_type must be BF16 or FP32");
     if (M < 0 || N < 0 || K < 0 || ldd < N) return fail(FP4Q_ERR_INVALID_ARGUMENT, "gemm: bad sizes");
     if (K % 128) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "gemm: K %% 128 != 0");
-    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
+    if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30))
         return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "gemm: sizes beyond 2^30");
     if (M == 0 || N == 0) return FP4Q_OK;
     if (!A->q || !B->q || !A->scales || !B->scales || !D)
@@ -345,38 +489,87 @@ extern "C" fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_
     if (st != FP4Q_OK) return st;
     if ((st = get_encoder()) != FP4Q_OK) return st;
     CUtensorMap ma, mb;
-    if ((st = encode_operand_map(&ma, A->q, M, K, BM)) != FP4Q_OK) return st;
-    if ((st = encode_operand_map(&mb, B->q, N, K, BN)) != FP4Q_OK) return st;
-
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!attr_set[dev & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
-        if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
-        attr_set[dev & 63] = true;
-    }
-    GemmArgs a;
+    if ((st = encode_operand_map(&ma, A->q, M, K)) != FP4Q_OK) return st;
+    if ((st = encode_operand_map(&mb, B->q, N, K)) != FP4Q_OK) return st;
+    GemmArgs a = {};
     a.M = int(M);
     a.N = int(N);
     a.K = int(K);
-    a.m_tiles = int((M + BM - 1) / BM);
     a.n_tiles = int((N + BN - 1) / BN);
     a.k_stages = int((K + BK - 1) / BK);
     a.nv = nv ? 1 : 0;
+    a.groups = 0;
     a.sfa = A->scales;
     a.sfb = B->scales;
-    const int64_t s4 = nv ? K / 64 : K / 128;          // 4-scale chunks per row tile
-    a.sfa_tile_stride = uint64_t(s4) * 512u;
-    a.sfb_tile_stride = uint64_t(s4) * 512u;
+    a.sf_tile_stride = uint64_t(nv ? K / 64 : K / 128) * 512u;
     a.ts_a = A->tensor_scale;
     a.ts_b = B->tensor_scale;
     a.D = static_cast<uint8_t*>(D);
     a.ldd = ldd;
     a.d_bf16 = d_type == FP4Q_BF16;
     a.status = status_word();
-    const int tiles = a.m_tiles * a.n_tiles;
-    const int grid = tiles < sms ? tiles : sms;
-    gemm_kernel<<<grid, kThreads, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(ma, mb, a);
-    return check_launch("block_scaled_gemm");
+    a.status_bit = kStatusGemmTimeout;
+    const int tiles = int((M + BM - 1) / BM) * a.n_tiles;
+    return launch<kStore>(ma, mb, a, tiles, sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_scales, const float* a_row_scale,
+                                         const uint8_t* b_q, const uint8_t* b_scales, const float* b_tensor_scale,
+                                         const int64_t* offsets, int64_t rows, int64_t groups, int64_t N, int64_t K,
+                                         fp4q_epilogue epilogue, void* D, uint8_t* d_scales, float* h_debug,
+                                         fp4q_stream_t stream) {
+    if (epilogue != FP4Q_EPI_STORE_BF16 && epilogue != FP4Q_EPI_SILU_GATE_MXFP4)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "grouped_gemm: bad epilogue");
+    if (rows < 0 || groups < 1 || groups > kMaxGroups || N < 1 || K < 0)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "grouped_gemm: need rows >= 0, 1 <= groups <= %d, N >= 1", kMaxGroups);
+    if (K % 128) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "grouped_gemm: K %% 128 != 0");
+    if (N % 128) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "grouped_gemm: N %% 128 != 0");
+    if (epilogue == FP4Q_EPI_SILU_GATE_MXFP4 && N % 256)
+        return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "grouped_gemm: gated epilogue needs N %% 256 == 0");
+    if (rows > (1 << 30) || groups * N > (1 << 30) || K > (1 << 30))
+        return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "grouped_gemm: sizes beyond 2^30");
+    if (rows == 0) return FP4Q_OK;
+    if (!a_q || !a_scales || !a_row_scale || !b_q || !b_scales || !b_tensor_scale || !offsets || !D ||
+        (epilogue == FP4Q_EPI_SILU_GATE_MXFP4 && !d_scales))
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "grouped_gemm: null pointer");
+    if (!aligned16(a_q) || !aligned16(b_q) || !aligned16(a_scales) || !aligned16(b_scales) || !aligned16(D) ||
+        (h_debug && !aligned16(h_debug)) || (reinterpret_cast<uintptr_t>(offsets) & 7u) ||
+        (reinterpret_cast<uintptr_t>(a_row_scale) & 3u) || (reinterpret_cast<uintptr_t>(b_tensor_scale) & 3u))
+        return fail(FP4Q_ERR_MISALIGNED, "grouped_gemm: operands and outputs must be 16-byte aligned");
+    if (K == 0) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "grouped_gemm: K == 0");
+    int sms = 0;
+    fp4q_status st = current_device(&sms);
+    if (st != FP4Q_OK) return st;
+    if ((st = get_encoder()) != FP4Q_OK) return st;
+    CUtensorMap ma, mb;
+    if ((st = encode_operand_map(&ma, a_q, rows, K)) != FP4Q_OK) return st;
+    if ((st = encode_operand_map(&mb, b_q, groups * N, K)) != FP4Q_OK) return st;
+    GemmArgs a = {};
+    a.M = int(rows);
+    a.N = int(N);
+    a.K = int(K);
+    a.k_stages = int((K + BK - 1) / BK);
+    a.nv = 1;
+    a.groups = int(groups);
+    a.offsets = offsets;
+    a.sfa = a_scales;
+    a.sfb = b_scales;
+    a.sf_tile_stride = uint64_t(K / 64) * 512u;
+    a.ts_b = b_tensor_scale;
+    a.a_row_scale = a_row_scale;
+    a.D = static_cast<uint8_t*>(D);
+    a.ldd = N;
+    a.d_bf16 = 1;
+    a.h_scales = d_scales;
+    a.h_debug = h_debug;
+    a.status = status_word();
+    a.status_bit = kStatusGroupedTimeout;
+    const int m_tiles_upper = int((rows + BM - 1) / BM + groups);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (epilogue == FP4Q_EPI_SILU_GATE_MXFP4) {
+        a.n_tiles = int(N / 256);
+        return launch<kSiluGate>(ma, mb, a, m_tiles_upper * a.n_tiles, sms, s);
+    }
+    a.n_tiles = int((N + BN - 1) / BN);
+    return launch<kStore>(ma, mb, a, m_tiles_upper * a.n_tiles, sms, s);
 }

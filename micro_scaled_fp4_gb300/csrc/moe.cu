@@ -1,0 +1,252 @@
+// MoE dispatch of packed MXFP4 rows and the MXFP4 -> UE4M3 scale rebase
+// that lets MXFP4 activations meet NVFP4 expert weights in one tcgen05
+// block-scaled MMA kind.
+//
+// "Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs",
+// section 2.A: activations are quantized to MXFP4 before the expert
+// dispatch, so what moves is packed FP4 plus scales; section 2.C: ragged
+// per-expert tensors with precomputed offsets and no padding.
+//
+// Dispatch (stable: inside an expert, ascending token id):
+//   1. count:  one CTA per 256 tokens; per expert, a ballot over each warp
+//              gives every (token, slot) its rank among the chunk's tokens
+//              that chose the same expert, and the chunk's expert counts.
+//   2. scan:   one CTA; chunk bases per expert, expert offsets [E + 1].
+//   3. gather: one warp per dispatched row copies the packed codes
+//              (16-byte vectors) and the E8M0 bytes of its token.
+// Rebase: per row, B = max_j E_j - 8 and each 32-block's 2^E_j becomes the
+// UE4M3 value 2^(E_j - B) for both of its 16-element halves (exact for
+// E_j - B >= -9), written in the MMA scale layout with every group padded to
+// whole 128-row tiles; the row factor 2^B goes to the GEMM epilogue.
+#include "common.cuh"
+
+namespace fp4q {
+namespace {
+
+constexpr int kChunk = 256;      // tokens per count CTA (8 warps)
+constexpr int kMaxExperts = 256;
+
+struct DispatchWs {
+    int32_t* chunk_count;        // [chunks][E]
+    int32_t* chunk_base;         // [chunks][E]
+    int32_t* local_rank;         // [T * k]
+};
+
+__global__ void __launch_bounds__(kChunk) moe_count_kernel(const int32_t* __restrict__ topk, int64_t tokens, int k,
+                                                           int E, int32_t* __restrict__ chunk_count,
+                                                           int32_t* __restrict__ local_rank) {
+    __shared__ int32_t warp_cnt[kChunk / 32][kMaxExperts];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = int64_t(blockIdx.x) * kChunk + threadIdx.x;
+    const bool valid = t < tokens;
+    int32_t mine[16];
+    int32_t rank_in_warp[16];
+    for (int j = 0; j < k; ++j) {
+        mine[j] = valid ? topk[t * k + j] : -1;
+        rank_in_warp[j] = 0;
+    }
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int e = 0; e < E; ++e) {
+        bool has = false;
+        for (int j = 0; j < k; ++j) has |= (mine[j] == e);
+        const uint32_t m = __ballot_sync(0xffffffffu, has);
+        if (lane == 0) warp_cnt[warp][e] = __popc(m);
+        if (has)
+            for (int j = 0; j < k; ++j)
+                if (mine[j] == e) rank_in_warp[j] = __popc(m & lt);
+    }
+    __syncthreads();
+    if (valid) {
+        for (int j = 0; j < k; ++j) {
+            const int e = mine[j];
+            int r = -1;
+            if (e >= 0 && e < E) {
+                r = rank_in_warp[j];
+                for (int w = 0; w < warp; ++w) r += warp_cnt[w][e];
+            }
+            local_rank[t * k + j] = r;
+        }
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t c = 0;
+        for (int w = 0; w < kChunk / 32; ++w) c += warp_cnt[w][e];
+        chunk_count[int64_t(blockIdx.x) * E + e] = c;
+    }
+}
+
+__global__ void moe_scan_kernel(const int32_t* __restrict__ chunk_count, int64_t chunks, int E,
+                                int32_t* __restrict__ chunk_base, int64_t* __restrict__ offsets) {
+    __shared__ int64_t total[kMaxExperts];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int64_t acc = 0;
+        for (int64_t c = 0; c < chunks; ++c) {
+            chunk_base[c * E + e] = int32_t(acc);
+            acc += chunk_count[c * E + e];
+        }
+        total[e] = acc;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int64_t acc = 0;
+        for (int e = 0; e < E; ++e) {
+            offsets[e] = acc;
+            acc += total[e];
+        }
+        offsets[E] = acc;
+    }
+}
+
+__global__ void __launch_bounds__(256) moe_gather_kernel(
+    const int32_t* __restrict__ topk, int64_t tokens, int k, int E, const int32_t* __restrict__ chunk_base,
+    const int32_t* __restrict__ local_rank, const int64_t* __restrict__ offsets, const uint8_t* __restrict__ q,
+    const uint8_t* __restrict__ s, int64_t qbytes, int64_t sbytes, int32_t* __restrict__ row_token,
+    uint8_t* __restrict__ q_out, uint8_t* __restrict__ s_out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t pair = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;   // (token, slot)
+    if (pair >= tokens * k) return;
+    const int64_t t = pair / k;
+    const int e = topk[pair];
+    const int32_t r = local_rank[pair];
+    if (e < 0 || e >= E || r < 0) return;
+    const int64_t pos = offsets[e] + chunk_base[(t / kChunk) * E + e] + r;
+    if (lane == 0) row_token[pos] = int32_t(t);
+    const uint4* src = reinterpret_cast<const uint4*>(q + t * qbytes);
+    uint4* dst = reinterpret_cast<uint4*>(q_out + pos * qbytes);
+    for (int64_t i = lane; i < qbytes / 16; i += 32) dst[i] = src[i];
+    for (int64_t i = lane; i < sbytes; i += 32) s_out[pos * sbytes + i] = s[t * sbytes + i];
+}
+
+// 2^k as FP32 for k in [-149, 127] (subnormal below -126).
+__device__ __forceinline__ float exp2_wide(int k) {
+    if (k >= -126) return u2f(uint32_t(k + 127) << 23);
+    return u2f(1u << (k + 149));
+}
+
+// UE4M3 byte of 2^k: normal for k >= -6 (exponent field k + 7), subnormal
+// 1, 2, 4 for k = -9, -8, -7; 0 when k < -9 (not representable).
+__device__ __forceinline__ uint32_t ue4m3_pow2(int k) {
+    if (k >= -6) return uint32_t(k + 7) << 3;
+    if (k >= -9) return 1u << (k + 9);
+    return 0u;
+}
+
+__global__ void __launch_bounds__(256) mx_rebase_kernel(const uint8_t* __restrict__ s, int64_t rows, int S32,
+                                                        const int64_t* __restrict__ offsets, int groups,
+                                                        uint8_t* __restrict__ out, float* __restrict__ row_scale,
+                                                        uint32_t* __restrict__ violations) {
+    __shared__ int64_t off[kMaxExperts + 1];
+    __shared__ int64_t tpre[kMaxExperts + 1];
+    if (threadIdx.x == 0) {
+        int64_t acc = 0;
+        for (int g = 0; g <= groups; ++g) {
+            off[g] = offsets[g];
+            tpre[g] = acc;
+            if (g < groups) acc += (offsets[g + 1] - offsets[g] + 127) / 128;
+        }
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (r >= rows || r >= off[groups]) return;
+    int lo = 0, hi = groups - 1;                     // group of row r: off[g] <= r < off[g + 1]
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    const int64_t prow = tpre[lo] * 128 + (r - off[lo]);   // row in the padded scale layout
+    uint32_t m = 0;
+    for (int j = lane; j < S32; j += 32) m = max(m, uint32_t(s[r * S32 + j]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int base = int(m) - 127 - 8;
+    uint32_t bad = 0;
+    const uint32_t S16 = uint32_t(S32) * 2;
+    for (int j = lane; j < S32; j += 32) {
+        const int kexp = int(s[r * S32 + j]) - 127 - base;
+        const uint32_t b = ue4m3_pow2(kexp);
+        bad += (kexp < -9);
+        *reinterpret_cast<uint16_t*>(out + mma_scale_offset(uint64_t(prow), uint32_t(2 * j), S16)) =
+            uint16_t(b | (b << 8));
+    }
+    if (lane == 0) row_scale[r] = exp2_wide(base);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    if (lane == 0 && bad && violations) atomicAdd(violations, bad);
+}
+
+}  // namespace
+}  // namespace fp4q
+
+using namespace fp4q;
+
+extern "C" size_t fp4q_moe_dispatch_workspace_bytes(int64_t tokens, int top_k, int n_experts) {
+    if (tokens < 0 || top_k < 0 || n_experts < 0) return 0;
+    const int64_t chunks = (tokens + kChunk - 1) / kChunk;
+    return size_t(2 * chunks * n_experts + tokens * top_k) * 4u + 256u;
+}
+
+extern "C" fp4q_status fp4q_moe_dispatch(const int32_t* topk, int64_t tokens, int top_k, int n_experts,
+                                         const uint8_t* q, const uint8_t* scales, int64_t cols, int64_t* offsets,
+                                         int32_t* row_token, uint8_t* q_out, uint8_t* scales_out, void* workspace,
+                                         size_t workspace_bytes, fp4q_stream_t stream) {
+    if (tokens < 0 || top_k < 1 || top_k > 16 || n_experts < 1 || n_experts > kMaxExperts || cols < 0)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "moe_dispatch: need 1 <= top_k <= 16, 1 <= n_experts <= %d",
+                    kMaxExperts);
+    if (cols % 32) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "moe_dispatch: cols %% 32 != 0");
+    if (!offsets) return fail(FP4Q_ERR_INVALID_ARGUMENT, "moe_dispatch: offsets is NULL");
+    if (tokens > 0 && (!topk || !q || !scales || !row_token || !q_out || !scales_out))
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "moe_dispatch: null pointer");
+    if (!workspace || workspace_bytes < fp4q_moe_dispatch_workspace_bytes(tokens, top_k, n_experts))
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "moe_dispatch: workspace missing or too small");
+    if (!aligned16(q) || !aligned16(q_out) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(offsets) & 7u) ||
+        (reinterpret_cast<uintptr_t>(topk) & 3u) || (reinterpret_cast<uintptr_t>(row_token) & 3u))
+        return fail(FP4Q_ERR_MISALIGNED, "moe_dispatch: q, q_out, workspace 16-byte aligned; offsets 8-byte");
+    fp4q_status st = current_device(nullptr);
+    if (st != FP4Q_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t chunks = (tokens + kChunk - 1) / kChunk;
+    int32_t* ws = static_cast<int32_t*>(workspace);
+    int32_t* chunk_count = ws;
+    int32_t* chunk_base = ws + chunks * n_experts;
+    int32_t* local_rank = ws + 2 * chunks * n_experts;
+    if (chunks > 0) {
+        moe_count_kernel<<<unsigned(chunks), kChunk, 0, s>>>(topk, tokens, top_k, n_experts, chunk_count, local_rank);
+        if ((st = check_launch("moe_dispatch count")) != FP4Q_OK) return st;
+    }
+    moe_scan_kernel<<<1, 256, 0, s>>>(chunk_count, chunks, n_experts, chunk_base, offsets);
+    if ((st = check_launch("moe_dispatch scan")) != FP4Q_OK) return st;
+    const int64_t pairs = tokens * top_k;
+    if (pairs > 0 && cols > 0) {
+        const int64_t blocks = (pairs * 32 + 255) / 256;
+        moe_gather_kernel<<<unsigned(blocks), 256, 0, s>>>(topk, tokens, top_k, n_experts, chunk_base, local_rank,
+                                                           offsets, q, scales, cols / 2, cols / 32, row_token, q_out,
+                                                           scales_out);
+        if ((st = check_launch("moe_dispatch gather")) != FP4Q_OK) return st;
+    }
+    return FP4Q_OK;
+}
+
+extern "C" size_t fp4q_rebased_scales_bytes(int64_t rows, int64_t cols, int64_t groups) {
+    if (rows < 0 || cols < 0 || groups < 0) return 0;
+    return size_t((rows + 127) / 128 + groups) * size_t((cols / 16 + 3) / 4) * 512u;
+}
+
+extern "C" fp4q_status fp4q_mx_rebase_scales(const uint8_t* scales, int64_t rows, int64_t cols,
+                                             const int64_t* offsets, int64_t groups, uint8_t* ue4m3_mma,
+                                             float* row_scale, uint32_t* violations, fp4q_stream_t stream) {
+    if (rows < 0 || cols < 0 || groups < 1 || groups > kMaxExperts)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "mx_rebase_scales: need rows >= 0, 1 <= groups <= %d", kMaxExperts);
+    if (cols % 128) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "mx_rebase_scales: cols %% 128 != 0");
+    if (rows == 0 || cols == 0) return FP4Q_OK;
+    if (!scales || !offsets || !ue4m3_mma || !row_scale)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "mx_rebase_scales: null pointer");
+    if ((reinterpret_cast<uintptr_t>(offsets) & 7u) || (reinterpret_cast<uintptr_t>(ue4m3_mma) & 15u) ||
+        (reinterpret_cast<uintptr_t>(row_scale) & 3u) || (reinterpret_cast<uintptr_t>(violations) & 3u))
+        return fail(FP4Q_ERR_MISALIGNED, "mx_rebase_scales: offsets 8-byte, output 16-byte aligned");
+    fp4q_status st = current_device(nullptr);
+    if (st != FP4Q_OK) return st;
+    const int64_t blocks = (rows * 32 + 255) / 256;
+    mx_rebase_kernel<<<unsigned(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        scales, rows, int(cols / 32), offsets, int(groups), ue4m3_mma, row_scale, violations);
+    return check_launch("mx_rebase_scales");
+}

@@ -25,10 +25,13 @@ FP4Q_SCALES_ROWMAJOR, FP4Q_SCALES_MMA = 0, 1
 FP4Q_RNE, FP4Q_SR = 0, 1
 FP4Q_MXFP4, FP4Q_NVFP4 = 0, 1
 
+FP4Q_EPI_STORE_BF16, FP4Q_EPI_SILU_GATE_MXFP4 = 0, 1
+
 EXPORTED = [
     "fp4q_status_string", "fp4q_last_error", "fp4q_scales_bytes", "fp4q_mx_quantize",
     "fp4q_mx_dequantize", "fp4q_fp4_to_fp8", "fp4q_nv_quantize_workspace_bytes", "fp4q_nv_quantize",
-    "fp4q_block_scaled_gemm", "fp4q_device_status",
+    "fp4q_block_scaled_gemm", "fp4q_device_status", "fp4q_moe_dispatch_workspace_bytes",
+    "fp4q_moe_dispatch", "fp4q_rebased_scales_bytes", "fp4q_mx_rebase_scales", "fp4q_grouped_gemm",
 ]
 
 
@@ -68,6 +71,12 @@ def load() -> ctypes.CDLL:
             L.fp4q_scales_bytes.argtypes = [i64, i64, ci]
             L.fp4q_nv_quantize_workspace_bytes.restype = ctypes.c_size_t
             L.fp4q_nv_quantize_workspace_bytes.argtypes = [i64, i64]
+            for name, args in {"fp4q_moe_dispatch_workspace_bytes": [i64, ci, ci],
+                               "fp4q_rebased_scales_bytes": [i64, i64, i64]}.items():
+                fn = getattr(L, name, None)
+                if fn is not None:
+                    fn.restype = ctypes.c_size_t
+                    fn.argtypes = args
             sigs = {
                 "fp4q_mx_quantize": [vp, ci, vp, i64, i64, i64, ci, vp, vp, ci, vp],
                 "fp4q_mx_dequantize": [vp, vp, i64, i64, ci, vp, ci, vp],
@@ -77,6 +86,9 @@ def load() -> ctypes.CDLL:
                 "fp4q_block_scaled_gemm": [ctypes.POINTER(fp4q_operand), ctypes.POINTER(fp4q_operand), i64, i64,
                                            i64, vp, ci, i64, vp],
                 "fp4q_device_status": [ctypes.POINTER(ctypes.c_uint32), ci],
+                "fp4q_moe_dispatch": [vp, i64, ci, ci, vp, vp, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp],
+                "fp4q_mx_rebase_scales": [vp, i64, i64, vp, i64, vp, vp, vp, vp],
+                "fp4q_grouped_gemm": [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ci, vp, vp, vp, vp],
             }
             for name, args in sigs.items():
                 fn = getattr(L, name, None)     # resolved here; a missing symbol fails at its call
@@ -156,6 +168,34 @@ def make_operand(q, scales, fmt, tensor_scale=None) -> fp4q_operand:
 def fp4q_block_scaled_gemm(A: fp4q_operand, B: fp4q_operand, M, N, K, D, d_type, ldd, stream=None):
     return _check("fp4q_block_scaled_gemm", load().fp4q_block_scaled_gemm(
         ctypes.byref(A), ctypes.byref(B), M, N, K, _ptr(D), d_type, ldd, _stream(stream)))
+
+
+def fp4q_moe_dispatch_workspace_bytes(tokens: int, top_k: int, n_experts: int) -> int:
+    return load().fp4q_moe_dispatch_workspace_bytes(tokens, top_k, n_experts)
+
+
+def fp4q_rebased_scales_bytes(rows: int, cols: int, groups: int) -> int:
+    return load().fp4q_rebased_scales_bytes(rows, cols, groups)
+
+
+def fp4q_moe_dispatch(topk, tokens, top_k, n_experts, q, scales, cols, offsets, row_token, q_out, scales_out,
+                      workspace, workspace_bytes, stream=None):
+    return _check("fp4q_moe_dispatch", load().fp4q_moe_dispatch(
+        _ptr(topk), tokens, top_k, n_experts, _ptr(q), _ptr(scales), cols, _ptr(offsets), _ptr(row_token),
+        _ptr(q_out), _ptr(scales_out), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def fp4q_mx_rebase_scales(scales, rows, cols, offsets, groups, ue4m3_mma, row_scale, violations, stream=None):
+    return _check("fp4q_mx_rebase_scales", load().fp4q_mx_rebase_scales(
+        _ptr(scales), rows, cols, _ptr(offsets), groups, _ptr(ue4m3_mma), _ptr(row_scale), _ptr(violations),
+        _stream(stream)))
+
+
+def fp4q_grouped_gemm(a_q, a_scales, a_row_scale, b_q, b_scales, b_tensor_scale, offsets, rows, groups, N, K,
+                      epilogue, D, d_scales, h_debug, stream=None):
+    return _check("fp4q_grouped_gemm", load().fp4q_grouped_gemm(
+        _ptr(a_q), _ptr(a_scales), _ptr(a_row_scale), _ptr(b_q), _ptr(b_scales), _ptr(b_tensor_scale),
+        _ptr(offsets), rows, groups, N, K, epilogue, _ptr(D), _ptr(d_scales), _ptr(h_debug), _stream(stream)))
 
 
 def fp4q_device_status(reset: bool = False) -> int:
@@ -239,3 +279,49 @@ def gemm(qa, sa, qb, sb, fmt=FP4Q_MXFP4, ts_a=None, ts_b=None, out_dtype=None, s
     B = make_operand(qb, sb, fmt, ts_b)
     fp4q_block_scaled_gemm(A, B, M, N, K, D, FP4Q_BF16 if out_dtype == torch.bfloat16 else FP4Q_FP32, ldd, stream)
     return D[:, :N]
+
+
+def moe_dispatch(topk, q, s, n_experts, stream=None):
+    """topk int32 [T, k] (device); q [T, C/2], s [T, C/32] ROWMAJOR.  Returns
+    dict(offsets int64 [E+1], row_token int32 [T*k], q, s) of the dispatched rows."""
+    torch = _torch()
+    T, k = topk.shape
+    C = q.shape[1] * 2
+    dev = q.device
+    offsets = torch.empty(n_experts + 1, dtype=torch.int64, device=dev)
+    row_token = torch.empty(T * k, dtype=torch.int32, device=dev)
+    qo = torch.empty((T * k, C // 2), dtype=torch.uint8, device=dev)
+    so = torch.empty((T * k, C // 32), dtype=torch.uint8, device=dev)
+    wsb = fp4q_moe_dispatch_workspace_bytes(T, k, n_experts)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    fp4q_moe_dispatch(topk, T, k, n_experts, q, s, C, offsets, row_token, qo, so, ws, wsb, stream)
+    return {"offsets": offsets, "row_token": row_token, "q": qo, "s": so}
+
+
+def mx_rebase_scales(s, offsets, cols, groups, violations=None, stream=None):
+    """ROWMAJOR E8M0 [R, cols/32] -> (UE4M3 MMA layout padded per group, FP32 row factor [R])."""
+    torch = _torch()
+    R = s.shape[0]
+    out = torch.zeros(fp4q_rebased_scales_bytes(R, cols, groups), dtype=torch.uint8, device=s.device)
+    rs = torch.empty(R, dtype=torch.float32, device=s.device)
+    fp4q_mx_rebase_scales(s, R, cols, offsets, groups, out, rs, violations, stream)
+    return out, rs
+
+
+def grouped_gemm(a_q, a_scales, a_row_scale, b_q, b_scales, b_ts, offsets, groups, N, epilogue=FP4Q_EPI_STORE_BF16,
+                 h_debug=False, stream=None):
+    """Returns D (BF16 [R, N]) or (h codes [R, N/4], h E8M0 [R, N/64], h FP32 or None) for the gated form."""
+    torch = _torch()
+    R, K = a_q.shape[0], a_q.shape[1] * 2
+    dev = a_q.device
+    if epilogue == FP4Q_EPI_STORE_BF16:
+        D = torch.empty((R, N), dtype=torch.bfloat16, device=dev)
+        fp4q_grouped_gemm(a_q, a_scales, a_row_scale, b_q, b_scales, b_ts, offsets, R, groups, N, K, epilogue, D,
+                          None, None, stream)
+        return D
+    hq = torch.empty((R, N // 4), dtype=torch.uint8, device=dev)
+    hs = torch.empty((R, N // 64), dtype=torch.uint8, device=dev)
+    hd = torch.empty((R, N // 2), dtype=torch.float32, device=dev) if h_debug else None
+    fp4q_grouped_gemm(a_q, a_scales, a_row_scale, b_q, b_scales, b_ts, offsets, R, groups, N, K, epilogue, hq, hs,
+                      hd, stream)
+    return hq, hs, hd
