@@ -218,6 +218,31 @@ fp4q_status fp4q_moe_dispatch(const int32_t* topk, int64_t tokens, int top_k, in
                               fp4q_stream_t stream);
 
 /*
+ * fp4q_moe_dispatch_static -- fp4q_moe_dispatch for callers that cannot pass a
+ * workspace.  The pages have no counterpart: this is a library convenience.
+ * Who needs it: callers that cannot allocate device memory on this path --
+ * processes that fix their device-memory budget at start-up and treat any
+ * later allocation as an error, plain C code that only receives device
+ * pointers from the framework owning the memory, and latency-sensitive loops
+ * where a cudaMalloc (it can synchronize the device) is not acceptable.
+ * Same arguments, results and limits as fp4q_moe_dispatch, minus the
+ * workspace: the scratch is a static device array of
+ * FP4Q_MOE_DISPATCH_STATIC_SCRATCH_BYTES that every GPU loading the library
+ * holds until exit.  A call whose fp4q_moe_dispatch_workspace_bytes(tokens,
+ * top_k, n_experts) exceeds it returns FP4Q_ERR_UNSUPPORTED_SHAPE (4 MiB covers
+ * e.g. 65536 tokens x top-8 over 64 experts).  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  The call
+ * allocates nothing.  All calls share the array: calls that overlap on the GPU
+ * (different streams, no ordering) race on it and give wrong results.
+ */
+#define FP4Q_MOE_DISPATCH_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)
+fp4q_status fp4q_moe_dispatch_static(const int32_t* topk, int64_t tokens, int top_k, int n_experts,
+                                     const uint8_t* q, const uint8_t* scales, int64_t cols,
+                                     int64_t* offsets, int32_t* row_token, uint8_t* q_out,
+                                     uint8_t* scales_out, fp4q_stream_t stream);
+
+/*
  * fp4q_mx_rebase_scales -- MXFP4 block scales -> UE4M3 per-16 scales + a row
  * factor, so MXFP4 rows can meet NVFP4 operands in one block-scaled MMA.
  * Per row r: B_r = max_j E_j - 8; each 32-block's 2^E_j becomes the UE4M3

@@ -250,3 +250,92 @@ extern "C" fp4q_status fp4q_mx_rebase_scales(const uint8_t* scales, int64_t rows
         scales, rows, int(cols / 32), offsets, int(groups), ue4m3_mma, row_scale, violations);
     return check_launch("mx_rebase_scales");
 }
+
+// ---------------------------------------------------------------------------
+// Dispatch without a caller workspace.
+//
+// Some callers cannot hand the library a device workspace: processes that fix
+// their whole device-memory budget at start-up and treat any later
+// allocation as an error, plain C callers that only receive device pointers
+// from the framework that owns the memory, and latency-sensitive loops where
+// a cudaMalloc (which can synchronize the device) is not acceptable.  For
+// them the dispatch scratch lives in this file-scope device array instead.
+// Every GPU that loads the library holds it until the process exits; every
+// call shares it, so calls that overlap on the GPU race on it.  Nothing in it
+// needs to start at zero: the count, scan and gather kernels write every
+// entry they later read.
+// ---------------------------------------------------------------------------
+namespace fp4q {
+namespace {
+
+static __device__ __align__(256) uint8_t g_dispatch_scratch[FP4Q_MOE_DISPATCH_STATIC_SCRATCH_BYTES];
+
+void* g_dispatch_scratch_addr[64] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the host-side name of the array is not a device address).
+fp4q_status dispatch_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(FP4Q_ERR_UNSUPPORTED_DEVICE, "device index %d", dev);
+    if (!g_dispatch_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(FP4Q_ERR_CUDA, "cudaGetSymbolAddress(dispatch scratch): %s", cudaGetErrorString(e));
+        g_dispatch_scratch_addr[dev] = p;
+    }
+    *out = g_dispatch_scratch_addr[dev];
+    return FP4Q_OK;
+}
+
+}  // namespace
+}  // namespace fp4q
+
+extern "C" fp4q_status fp4q_moe_dispatch_static(const int32_t* topk, int64_t tokens, int top_k, int n_experts,
+                                                const uint8_t* q, const uint8_t* scales, int64_t cols,
+                                                int64_t* offsets, int32_t* row_token, uint8_t* q_out,
+                                                uint8_t* scales_out, fp4q_stream_t stream) {
+    if (tokens < 0 || top_k < 1 || top_k > 16 || n_experts < 1 || n_experts > kMaxExperts || cols < 0)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "moe_dispatch_static: need 1 <= top_k <= 16, 1 <= n_experts <= %d",
+                    kMaxExperts);
+    const size_t need = fp4q_moe_dispatch_workspace_bytes(tokens, top_k, n_experts);
+    if (need > size_t(FP4Q_MOE_DISPATCH_STATIC_SCRATCH_BYTES))
+        return fail(FP4Q_ERR_UNSUPPORTED_SHAPE,
+                    "moe_dispatch_static: %lld tokens x top-%d over %d experts need %zu scratch bytes, more than the "
+                    "%u-byte static array; use fp4q_moe_dispatch with a workspace",
+                    (long long)tokens, top_k, n_experts, need, unsigned(FP4Q_MOE_DISPATCH_STATIC_SCRATCH_BYTES));
+    if (cols % 32) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "moe_dispatch_static: cols %% 32 != 0");
+    if (!offsets) return fail(FP4Q_ERR_INVALID_ARGUMENT, "moe_dispatch_static: offsets is NULL");
+    if (tokens > 0 && (!topk || !q || !scales || !row_token || !q_out || !scales_out))
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "moe_dispatch_static: null pointer");
+    if (!aligned16(q) || !aligned16(q_out) || (reinterpret_cast<uintptr_t>(offsets) & 7u) ||
+        (reinterpret_cast<uintptr_t>(topk) & 3u) || (reinterpret_cast<uintptr_t>(row_token) & 3u))
+        return fail(FP4Q_ERR_MISALIGNED, "moe_dispatch_static: q, q_out 16-byte aligned; offsets 8-byte");
+    fp4q_status st = current_device(nullptr);
+    if (st != FP4Q_OK) return st;
+    void* scratch = nullptr;
+    if ((st = dispatch_scratch(&scratch)) != FP4Q_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t chunks = (tokens + kChunk - 1) / kChunk;
+    int32_t* ws = static_cast<int32_t*>(scratch);
+    int32_t* chunk_count = ws;
+    int32_t* chunk_base = ws + chunks * n_experts;
+    int32_t* local_rank = ws + 2 * chunks * n_experts;
+    if (chunks > 0) {
+        moe_count_kernel<<<unsigned(chunks), kChunk, 0, s>>>(topk, tokens, top_k, n_experts, chunk_count, local_rank);
+        if ((st = check_launch("moe_dispatch_static count")) != FP4Q_OK) return st;
+    }
+    moe_scan_kernel<<<1, 256, 0, s>>>(chunk_count, chunks, n_experts, chunk_base, offsets);
+    if ((st = check_launch("moe_dispatch_static scan")) != FP4Q_OK) return st;
+    const int64_t pairs = tokens * top_k;
+    if (pairs > 0 && cols > 0) {
+        const int64_t blocks = (pairs * 32 + 255) / 256;
+        moe_gather_kernel<<<unsigned(blocks), 256, 0, s>>>(topk, tokens, top_k, n_experts, chunk_base, local_rank,
+                                                           offsets, q, scales, cols / 2, cols / 32, row_token, q_out,
+                                                           scales_out);
+        if ((st = check_launch("moe_dispatch_static gather")) != FP4Q_OK) return st;
+    }
+    return FP4Q_OK;
+}

@@ -32,7 +32,9 @@ EXPORTED = [
     "fp4q_mx_dequantize", "fp4q_fp4_to_fp8", "fp4q_nv_quantize_workspace_bytes", "fp4q_nv_quantize",
     "fp4q_block_scaled_gemm", "fp4q_device_status", "fp4q_moe_dispatch_workspace_bytes",
     "fp4q_moe_dispatch", "fp4q_rebased_scales_bytes", "fp4q_mx_rebase_scales", "fp4q_grouped_gemm",
+    "fp4q_moe_dispatch_static",
 ]
+MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 * 1024 * 1024
 
 
 class Fp4qError(RuntimeError):
@@ -88,6 +90,7 @@ def load() -> ctypes.CDLL:
                 "fp4q_device_status": [ctypes.POINTER(ctypes.c_uint32), ci],
                 "fp4q_moe_dispatch": [vp, i64, ci, ci, vp, vp, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp],
                 "fp4q_mx_rebase_scales": [vp, i64, i64, vp, i64, vp, vp, vp, vp],
+                "fp4q_moe_dispatch_static": [vp, i64, ci, ci, vp, vp, i64, vp, vp, vp, vp, vp],
                 "fp4q_grouped_gemm": [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ci, vp, vp, vp, vp],
             }
             for name, args in sigs.items():
@@ -183,6 +186,15 @@ def fp4q_moe_dispatch(topk, tokens, top_k, n_experts, q, scales, cols, offsets, 
     return _check("fp4q_moe_dispatch", load().fp4q_moe_dispatch(
         _ptr(topk), tokens, top_k, n_experts, _ptr(q), _ptr(scales), cols, _ptr(offsets), _ptr(row_token),
         _ptr(q_out), _ptr(scales_out), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def fp4q_moe_dispatch_static(topk, tokens, top_k, n_experts, q, scales, cols, offsets, row_token, q_out,
+                             scales_out, stream=None):
+    """fp4q_moe_dispatch with the library's static scratch instead of a workspace
+    (for callers that must not allocate device memory on this path)."""
+    return _check("fp4q_moe_dispatch_static", load().fp4q_moe_dispatch_static(
+        _ptr(topk), tokens, top_k, n_experts, _ptr(q), _ptr(scales), cols, _ptr(offsets), _ptr(row_token),
+        _ptr(q_out), _ptr(scales_out), _stream(stream)))
 
 
 def fp4q_mx_rebase_scales(scales, rows, cols, offsets, groups, ue4m3_mma, row_scale, violations, stream=None):
