@@ -65,6 +65,31 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
     return r & 0xffu;
 }
 
+// Eight FP32 -> one 32-bit word of eight E2M1 codes (element j in nibble j),
+// round-to-nearest-even, saturating at +-6.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float v0, float v1, float v2, float v3, float v4, float v5,
+                                               float v6, float v7) {
+    uint32_t out;
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+        " mov.b32 %0, {b0, b1, b2, b3};\n}"
+        : "=r"(out) : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+    return out;
+}
+
+// Four E4M3 bytes of a 32-bit word (byte j = element j) -> four FP32 (exact).
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&f)[4]) {
+    asm("{\n .reg .b16 lo, hi, x0, x1, x2, x3;\n .reg .b32 h01, h23;\n"
+        " mov.b32 {lo, hi}, %4;\n"
+        " cvt.rn.f16x2.e4m3x2 h01, lo;\n cvt.rn.f16x2.e4m3x2 h23, hi;\n"
+        " mov.b32 {x0, x1}, h01;\n mov.b32 {x2, x3}, h23;\n"
+        " cvt.f32.f16 %0, x0;\n cvt.f32.f16 %1, x1;\n cvt.f32.f16 %2, x2;\n cvt.f32.f16 %3, x3;\n}"
+        : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]) : "r"(w));
+}
+
 // FP32 -> E4M3 byte, round-to-nearest-even, saturating at +-448.
 __device__ __forceinline__ uint32_t cvt_e4m3(float v) {
     uint16_t r;
@@ -137,6 +162,33 @@ inline void row_launch_shape(int64_t bpr, int* tpb, int* nx) {
     per = (per + 31) / 32 * 32;
     *tpb = int(per);
     *nx = int(n);
+}
+
+// CTAs along the rows for a row-wise kernel: one full wave of resident CTAs
+// (`per_sm` per SM), each then looping over its share of rows.
+inline unsigned row_grid_y(int64_t rows, int nx, int sms, int per_sm = 8) {
+    int64_t want = (int64_t(sms > 0 ? sms : 148) * (per_sm > 0 ? per_sm : 1)) / nx;
+    if (want < 1) want = 1;
+    int64_t gy = rows < want ? rows : want;
+    if (gy > 65535) gy = 65535;
+    return unsigned(gy > 0 ? gy : 1);
+}
+
+// Resident CTAs per SM of `kernel` at `threads` per CTA (no dynamic shared
+// memory), looked up once per kernel and device.
+template <typename Kernel>
+inline int resident_per_sm(Kernel kernel, int threads) {
+    static int cache[64][5] = {};      // [device][threads / 64 bucket], 0 = unknown
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int bucket = threads <= 64 ? 0 : threads <= 128 ? 1 : threads <= 192 ? 2 : threads <= 256 ? 3 : 4;
+    int& v = cache[dev & 63][bucket];
+    if (v == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 4;
+        v = n;
+    }
+    return v;
 }
 
 }  // namespace fp4q

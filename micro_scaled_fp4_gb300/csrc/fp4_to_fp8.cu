@@ -51,6 +51,23 @@ __device__ __forceinline__ uint2 remap8(uint32_t w, uint2 lut) {
     return make_uint2(mag_lo | sgn_lo, mag_hi | sgn_hi);
 }
 
+// One 32-element block: `cw` its 16 bytes of codes, `sw` the four E8M0 bytes of
+// its 1x128 tile, b its block index (b % 4 = position in the tile).
+__device__ __forceinline__ void convert_block(const uint4& cw, uint32_t sw, uint32_t b, const uint2* lut,
+                                              uint8_t* __restrict__ yb, float* __restrict__ ts) {
+    const uint32_t e_own = (sw >> (8 * (b & 3))) & 0xffu;
+    const uint32_t m2 = __vmaxu4(sw, sw >> 16);
+    const uint32_t emax = max(m2 & 0xffu, (m2 >> 8) & 0xffu);
+    const uint32_t sh = min(emax - e_own, uint32_t(kShiftRows - 1));
+    const uint2 L = lut[sh];
+    const uint2 o0 = remap8(cw.x, L), o1 = remap8(cw.y, L), o2 = remap8(cw.z, L), o3 = remap8(cw.w, L);
+    u32x8 o;
+    o.v[0] = o0.x; o.v[1] = o0.y; o.v[2] = o1.x; o.v[3] = o1.y;
+    o.v[4] = o2.x; o.v[5] = o2.y; o.v[6] = o3.x; o.v[7] = o3.y;
+    stg256(yb, o);
+    if ((b & 3) == 0) *ts = exp2i(int(emax) - 127);
+}
+
 __global__ void __launch_bounds__(256) fp4_to_fp8_kernel(
     const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, uint32_t bpr,
     uint8_t* __restrict__ y, float* __restrict__ tile_scale) {
@@ -66,22 +83,22 @@ __global__ void __launch_bounds__(256) fp4_to_fp8_kernel(
     __syncthreads();
     const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= bpr) return;
-    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-        const uint64_t blk = uint64_t(r) * bpr + b;
+    const int64_t step = gridDim.y;
+    for (int64_t r = blockIdx.y; r < rows; r += 2 * step) {
+        // two rows in flight: both rows' codes and tile exponents are loaded first
+        const int64_t r2 = r + step;
+        const bool two = r2 < rows;
+        const uint64_t blk = uint64_t(r) * bpr + b, blk2 = uint64_t(r2) * bpr + b;
         const uint4 cw = *reinterpret_cast<const uint4*>(q + blk * 16);
-        // the tile's four E8M0 bytes, one aligned 32-bit load
         const uint32_t sw = *reinterpret_cast<const uint32_t*>(s + uint64_t(r) * bpr + (b & ~3u));
-        const uint32_t e_own = (sw >> (8 * (b & 3))) & 0xffu;
-        const uint32_t m2 = __vmaxu4(sw, sw >> 16);
-        const uint32_t emax = max(m2 & 0xffu, (m2 >> 8) & 0xffu);
-        const uint32_t sh = min(emax - e_own, uint32_t(kShiftRows - 1));
-        const uint2 L = lut[sh];
-        const uint2 o0 = remap8(cw.x, L), o1 = remap8(cw.y, L), o2 = remap8(cw.z, L), o3 = remap8(cw.w, L);
-        u32x8 o;
-        o.v[0] = o0.x; o.v[1] = o0.y; o.v[2] = o1.x; o.v[3] = o1.y;
-        o.v[4] = o2.x; o.v[5] = o2.y; o.v[6] = o3.x; o.v[7] = o3.y;
-        stg256(y + blk * 32, o);
-        if ((b & 3) == 0) tile_scale[uint64_t(r) * (bpr >> 2) + (b >> 2)] = exp2i(int(emax) - 127);
+        uint4 cw2 = make_uint4(0, 0, 0, 0);
+        uint32_t sw2 = 0;
+        if (two) {
+            cw2 = *reinterpret_cast<const uint4*>(q + blk2 * 16);
+            sw2 = *reinterpret_cast<const uint32_t*>(s + uint64_t(r2) * bpr + (b & ~3u));
+        }
+        convert_block(cw, sw, b, lut, y + blk * 32, tile_scale + uint64_t(r) * (bpr >> 2) + (b >> 2));
+        if (two) convert_block(cw2, sw2, b, lut, y + blk2 * 32, tile_scale + uint64_t(r2) * (bpr >> 2) + (b >> 2));
     }
 }
 
@@ -101,13 +118,13 @@ extern "C" fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, 
     if (!aligned16(q) || (reinterpret_cast<uintptr_t>(y) & 31u) ||
         (reinterpret_cast<uintptr_t>(scales) & 3u) || (reinterpret_cast<uintptr_t>(tile_scale) & 3u))
         return fail(FP4Q_ERR_MISALIGNED, "fp4_to_fp8: q 16-byte, y 32-byte, scales/tile_scale 4-byte aligned");
-    fp4q_status st = current_device(nullptr);
+    int sms = 0;
+    fp4q_status st = current_device(&sms);
     if (st != FP4Q_OK) return st;
     const uint32_t bpr = uint32_t(cols / 32);
     int tpb, nx;
     row_launch_shape(bpr, &tpb, &nx);
-    int64_t gy = rows < 65535 ? rows : 65535;
-    dim3 grid(unsigned(nx), unsigned(gy), 1);
+    dim3 grid(unsigned(nx), row_grid_y(rows, nx, sms, resident_per_sm(fp4_to_fp8_kernel, tpb)), 1);
     fp4_to_fp8_kernel<<<grid, tpb, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, scales, rows, bpr, y, tile_scale);
     return check_launch("fp4_to_fp8");
 }

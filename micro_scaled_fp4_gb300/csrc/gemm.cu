@@ -30,6 +30,7 @@
 // drains its own asynchronous work and frees TMEM before returning.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "tc.cuh"
@@ -38,14 +39,21 @@ namespace fp4q {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 256;           // elements
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr uint32_t A_BYTES = BM * BK / 2;             // 16384
 constexpr uint32_t B_HALF_BYTES = 128 * BK / 2;       // 16384
 constexpr uint32_t B_BYTES = 2 * B_HALF_BYTES;
 constexpr uint32_t SFA_BYTES = 4 * 512;               // up to 4 chunks (NVFP4)
 constexpr uint32_t SFB_BYTES = 2 * 4 * 512;           // 2 halves x 4 chunks
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;   // 55296
-constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
+// BF16 output staging: two 64-column x 128-row boxes, rows of 128 bytes with the
+// TMA 128-byte swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)).
+constexpr uint32_t BOX_BYTES = 128 * 128;             // 64 BF16 columns x 128 rows
+constexpr uint32_t STAGING_BYTES = 2 * BOX_BYTES;
+constexpr uint32_t STAGING_OFF = STAGES * STAGE_BYTES;
+constexpr uint32_t BARS_OFF = STAGING_OFF + STAGING_BYTES;
+constexpr uint32_t PREFIX_OFF = BARS_OFF + 256;
+constexpr uint32_t SMEM_BYTES = PREFIX_OFF + 4 * 260 + 1024;
 constexpr int kThreads = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SFA = 256;                    // 16 columns
@@ -129,23 +137,44 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile, con
     return t;
 }
 
+// Converts 32 accumulator columns (FP32 bits) times alpha to 16 BF16 pairs.
+__device__ __forceinline__ void to_bf16x32(const uint32_t (&r)[32], float alpha, uint32_t (&p)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float lo = __fmul_rn(u2f(r[2 * i]), alpha), hi = __fmul_rn(u2f(r[2 * i + 1]), alpha);
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(p[i]) : "f"(hi), "f"(lo));
+    }
+}
+
+// Writes 32 BF16 columns (chunk c of a 128-column half) of staging row `row`.
+__device__ __forceinline__ void stage_bf16x32(uint32_t staging, int row, int c, const uint32_t (&p)[16]) {
+    const uint32_t box = staging + uint32_t(c >> 1) * BOX_BYTES + uint32_t(row) * 128u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t j = uint32_t((c & 1) * 4 + i);
+        tc::st_shared_v4(box + ((j ^ uint32_t(row & 7)) << 4), p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+    }
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-            const GemmArgs args) {
+            const __grid_constant__ CUtensorMap tmap_d, const GemmArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    // bars[0..3] full, [4..7] empty, [8] tmem_full, [9] tmem_empty, [10] mma drain
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BARS_OFF);
+    // bars[0..STAGES) full, [STAGES..2 STAGES) empty, then tmem_full, tmem_empty, mma drain
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
     volatile int* abort = reinterpret_cast<volatile int*>(bars + 13);
-    __shared__ int tile_prefix[kMaxGroups + 1];
+    int* tile_prefix = reinterpret_cast<int*>(smem + PREFIX_OFF);
+    const uint32_t staging = tc::smem_u32(smem + STAGING_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bar0 = tc::smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    const uint32_t tmem_full = bar0 + 8u * 8, tmem_empty = bar0 + 8u * 9, drain_bar = bar0 + 8u * 10;
+    const uint32_t tmem_full = bar0 + 8u * (2 * STAGES), tmem_empty = bar0 + 8u * (2 * STAGES + 1),
+                   drain_bar = bar0 + 8u * (2 * STAGES + 2);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -230,6 +259,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
+        // Stage-0 descriptors, split into the low word (address field, advanced per
+        // stage / K step) and the constant high word.
+        const uint64_t d0 = tc::smem_desc(tc::smem_u32(smem), 16, 1024, 2);
+        const uint64_t sf0 = tc::smem_desc(tc::smem_u32(smem + A_BYTES + B_BYTES), 0, 128, 0);
+        const uint32_t d_lo0 = uint32_t(d0), d_hi = uint32_t(d0 >> 32);
+        const uint32_t sf_lo0 = uint32_t(sf0), sf_hi = uint32_t(sf0 >> 32);
+        const uint32_t idesc_nv = tc::idesc_block_scaled(BM, BN, false, 0, 0);
+        const uint32_t idesc_mx0 = tc::idesc_block_scaled(BM, BN, true, 0, 0);
+        const uint32_t idesc_mx1 = tc::idesc_block_scaled(BM, BN, true, 2, 2);
         int stage = 0;
         uint32_t phase = 0;
         int tcount = 0;
@@ -241,39 +279,67 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             }
             tc::fence_after_sync();
             for (int kb = 0; kb < args.k_stages; ++kb) {
+                // The stage's tiles and scales were written by TMA (async proxy) and
+                // completed on the mbarrier; the MMAs read them through the async proxy
+                // too, so no tcgen05 fence is needed here (one per stage costs about
+                // 300 cycles of tensor-pipe time).  The TMEM hand-off with the epilogue
+                // keeps its fences.
                 if (!tc::mbar_wait(full_bar(stage), phase, abort, kWaitLimitNs)) {
                     flag_abort(abort, args.status, args.status_bit);
                     ok = false;
                     break;
                 }
-                tc::fence_after_sync();
                 const int k_elems = min(BK, args.K - kb * BK);
-                const uint32_t chunks = uint32_t(k_elems) / chunk_elems;
-                const uint32_t nmma = uint32_t(k_elems) / 64;
-                uint8_t* st = smem + stage * STAGE_BYTES;
-                const uint32_t sa = tc::smem_u32(st), sb = tc::smem_u32(st + A_BYTES);
-                const uint32_t ssfa = tc::smem_u32(st + A_BYTES + B_BYTES);
-                const uint32_t ssfb = tc::smem_u32(st + A_BYTES + B_BYTES + SFA_BYTES);
-                // block scales -> TMEM: chunk c of A at column TMEM_SFA + 4c, chunk c
-                // of B's half h at TMEM_SFB + 8c + 4h
-                for (uint32_t c = 0; c < chunks; ++c) {
-                    tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFA + 4 * c, tc::smem_desc(ssfa + 512 * c, 0, 128, 0));
-                    tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c, tc::smem_desc(ssfb + 512 * c, 0, 128, 0));
-                    tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c + 4,
-                                             tc::smem_desc(ssfb + 4 * 512 + 512 * c, 0, 128, 0));
-                }
-                for (uint32_t j = 0; j < nmma; ++j) {
-                    const uint64_t da = tc::smem_desc(sa + 32 * j, 16, 1024, 2);
-                    const uint64_t db = tc::smem_desc(sb + 32 * j, 16, 1024, 2);
-                    const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+                // descriptors of this stage: the 14-bit address field (bytes >> 4)
+                // of the stage-0 descriptors advanced by the stage offset
+                const uint32_t so = uint32_t(stage) * (STAGE_BYTES >> 4);
+                const uint32_t a_lo = d_lo0 + so, b_lo = d_lo0 + so + (A_BYTES >> 4);
+                const uint32_t sfa_lo = sf_lo0 + so, sfb_lo = sf_lo0 + so + (SFA_BYTES >> 4);
+                if (k_elems == BK) {
                     if (args.nv) {
-                        const uint32_t id = tc::idesc_block_scaled(BM, BN, false, 0, 0);
-                        tc::mma_nvf4(tmem, da, db, id, tmem + TMEM_SFA + 4 * j, tmem + TMEM_SFB + 8 * j, acc);
+#pragma unroll
+                        for (uint32_t c = 0; c < 4; ++c) {
+                            tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFA + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
+                            tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
+                            tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c + 4,
+                                                     tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
+                        }
+#pragma unroll
+                        for (uint32_t j = 0; j < 4; ++j)
+                            tc::mma_nvf4(tmem, tc::desc_from(a_lo + 2 * j, d_hi), tc::desc_from(b_lo + 2 * j, d_hi),
+                                         idesc_nv, tmem + TMEM_SFA + 4 * j, tmem + TMEM_SFB + 8 * j,
+                                         (kb | int(j)) ? 1u : 0u);
                     } else {
-                        const uint32_t sfid = (j & 1) * 2;
-                        const uint32_t id = tc::idesc_block_scaled(BM, BN, true, sfid, sfid);
-                        tc::mma_mxf4(tmem, da, db, id, tmem + TMEM_SFA + 4 * (j >> 1), tmem + TMEM_SFB + 8 * (j >> 1),
-                                     acc);
+#pragma unroll
+                        for (uint32_t c = 0; c < 2; ++c) {
+                            tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFA + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
+                            tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
+                            tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c + 4,
+                                                     tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
+                        }
+#pragma unroll
+                        for (uint32_t j = 0; j < 4; ++j)
+                            tc::mma_mxf4(tmem, tc::desc_from(a_lo + 2 * j, d_hi), tc::desc_from(b_lo + 2 * j, d_hi),
+                                         (j & 1) ? idesc_mx1 : idesc_mx0, tmem + TMEM_SFA + 4 * (j >> 1),
+                                         tmem + TMEM_SFB + 8 * (j >> 1), (kb | int(j)) ? 1u : 0u);
+                    }
+                } else {
+                    // K tail: 128 elements (K % 256 == 128)
+                    const uint32_t chunks = uint32_t(k_elems) / chunk_elems;
+                    const uint32_t nmma = uint32_t(k_elems) / 64;
+                    for (uint32_t c = 0; c < chunks; ++c) {
+                        tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFA + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
+                        tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
+                        tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c + 4, tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
+                    }
+                    for (uint32_t j = 0; j < nmma; ++j) {
+                        const uint64_t da = tc::desc_from(a_lo + 2 * j, d_hi), db = tc::desc_from(b_lo + 2 * j, d_hi);
+                        const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+                        if (args.nv)
+                            tc::mma_nvf4(tmem, da, db, idesc_nv, tmem + TMEM_SFA + 4 * j, tmem + TMEM_SFB + 8 * j, acc);
+                        else
+                            tc::mma_mxf4(tmem, da, db, (j & 1) ? idesc_mx1 : idesc_mx0, tmem + TMEM_SFA + 4 * (j >> 1),
+                                         tmem + TMEM_SFB + 8 * (j >> 1), acc);
                     }
                 }
                 tc::tc_commit(empty_bar(stage));
@@ -349,6 +415,52 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     *reinterpret_cast<uint4*>(args.D + int64_t(row) * (hcols / 2) + col / 2) = make_uint4(w[0], w[1], w[2], w[3]);
                     args.h_scales[int64_t(row) * (hcols / 32) + col / 32] = uint8_t(e + 127);
                 }
+            } else if (args.d_bf16 && t.a_row0 + BM <= t.row_end + (args.groups ? 0 : BM)) {
+                // BF16 through shared memory and TMA stores.  All 256 columns leave
+                // TMEM first (half 0 into the staging buffer, half 1 into registers),
+                // then the accumulator goes back to the MMA thread.
+                const int et = int(threadIdx.x) - 64;            // epilogue thread 0..127
+                const int srow = q * 32 + lane;                  // row within the tile
+                if (et == 0) tc::bulk_wait_read0();              // previous tile's stores have read the staging
+                tc::named_bar_sync(1, 128);
+                uint32_t hold[4][16];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t r[32];
+                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(c * 32), r);
+                    tc::tmem_ld_wait();
+                    if (c < 4) {
+                        uint32_t p[16];
+                        to_bf16x32(r, alpha, p);
+                        stage_bf16x32(staging, srow, c, p);
+                    } else {
+                        to_bf16x32(r, alpha, hold[c - 4]);
+                    }
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tmem_empty);
+                tc::fence_proxy_async_smem();
+                tc::named_bar_sync(1, 128);
+                if (et == 0) {
+                    for (int b = 0; b < 2; ++b)
+                        if (t.col0 + 64 * b < args.N)
+                            tc::tma_store_2d(&tmap_d, staging + uint32_t(b) * BOX_BYTES, t.col0 + 64 * b, t.a_row0);
+                    tc::bulk_commit();
+                    tc::bulk_wait_read0();
+                }
+                tc::named_bar_sync(1, 128);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) stage_bf16x32(staging, srow, c, hold[c]);
+                tc::fence_proxy_async_smem();
+                tc::named_bar_sync(1, 128);
+                if (et == 0) {
+                    for (int b = 2; b < 4; ++b)
+                        if (t.col0 + 64 * b < args.N)
+                            tc::tma_store_2d(&tmap_d, staging + uint32_t(b - 2) * BOX_BYTES, t.col0 + 64 * b,
+                                             t.a_row0);
+                    tc::bulk_commit();
+                }
             } else {
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
@@ -397,6 +509,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             }
         }
     }
+    if (EPI == kStore && threadIdx.x == 64) tc::bulk_wait0();   // the TMA stores this thread issued
     __syncwarp();          // the elected lanes rejoin their warps before the block barrier
     tc::fence_before_sync();
     __syncthreads();
@@ -435,9 +548,23 @@ fp4q_status encode_operand_map(CUtensorMap* map, const uint8_t* q, int64_t rows,
     return FP4Q_OK;
 }
 
+// 2D map over a BF16 output [rows, ld] (N columns used): 64-column x 128-row
+// boxes, 128B swizzle, for the TMA stores of the epilogue.
+fp4q_status encode_output_map(CUtensorMap* map, void* D, int64_t rows, int64_t N, int64_t ld) {
+    cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(ld * 2)};
+    cuuint32_t box[2] = {64u, 128u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FP4Q_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d)", int(r));
+    return FP4Q_OK;
+}
+
 template <int EPI>
-fp4q_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int tiles_upper, int sms,
-                   cudaStream_t stream) {
+fp4q_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const GemmArgs& a,
+                   int tiles_upper, int sms, cudaStream_t stream) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -448,7 +575,7 @@ fp4q_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs&
         attr_set[dev & 63] = true;
     }
     const int grid = tiles_upper < sms ? tiles_upper : sms;
-    gemm_kernel<EPI><<<grid, kThreads, SMEM_BYTES, stream>>>(ma, mb, a);
+    gemm_kernel<EPI><<<grid, kThreads, SMEM_BYTES, stream>>>(ma, mb, md, a);
     return check_launch("block_scaled_gemm");
 }
 
@@ -509,8 +636,11 @@ extern "C" fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_
     a.d_bf16 = d_type == FP4Q_BF16;
     a.status = status_word();
     a.status_bit = kStatusGemmTimeout;
+    CUtensorMap md;
+    memset(&md, 0, sizeof md);
+    if (a.d_bf16 && (st = encode_output_map(&md, D, M, N, ldd)) != FP4Q_OK) return st;
     const int tiles = int((M + BM - 1) / BM) * a.n_tiles;
-    return launch<kStore>(ma, mb, a, tiles, sms, reinterpret_cast<cudaStream_t>(stream));
+    return launch<kStore>(ma, mb, md, a, tiles, sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_scales, const float* a_row_scale,
@@ -566,10 +696,13 @@ extern "C" fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sc
     a.status_bit = kStatusGroupedTimeout;
     const int m_tiles_upper = int((rows + BM - 1) / BM + groups);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUtensorMap md;
+    memset(&md, 0, sizeof md);
     if (epilogue == FP4Q_EPI_SILU_GATE_MXFP4) {
         a.n_tiles = int(N / 256);
-        return launch<kSiluGate>(ma, mb, a, m_tiles_upper * a.n_tiles, sms, s);
+        return launch<kSiluGate>(ma, mb, md, a, m_tiles_upper * a.n_tiles, sms, s);
     }
+    if ((st = encode_output_map(&md, D, rows, N, N)) != FP4Q_OK) return st;
     a.n_tiles = int((N + BN - 1) / BN);
-    return launch<kStore>(ma, mb, a, m_tiles_upper * a.n_tiles, sms, s);
+    return launch<kStore>(ma, mb, md, a, m_tiles_upper * a.n_tiles, sms, s);
 }

@@ -21,10 +21,125 @@ namespace {
 
 enum Src { kBF16 = 0, kFP32 = 1, kE4M3 = 2 };
 
-__device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
-    return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+// One 32-element block as loaded from memory.
+template <int SRC> struct RawBlock;
+template <> struct RawBlock<kBF16> { u32x8 a, b; };
+template <> struct RawBlock<kFP32> { u32x8 a[4]; };
+template <> struct RawBlock<kE4M3> { u32x8 a; float ts; };
+
+template <int SRC>
+__device__ __forceinline__ void load_block(const uint8_t* __restrict__ x, const float* __restrict__ tile_scale,
+                                           int64_t r, uint32_t b, uint32_t bpr, int64_t ld_x_bytes,
+                                           RawBlock<SRC>& raw) {
+    if constexpr (SRC == kBF16) {
+        const uint8_t* p = x + r * ld_x_bytes + uint64_t(b) * 64;
+        raw.a = ldg256(p);
+        raw.b = ldg256(p + 32);
+    } else if constexpr (SRC == kFP32) {
+        const uint8_t* p = x + r * ld_x_bytes + uint64_t(b) * 128;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) raw.a[i] = ldg256(p + 32 * i);
+    } else {
+        raw.a = ldg256(x + r * ld_x_bytes + uint64_t(b) * 32);
+        raw.ts = __ldg(tile_scale + r * (bpr >> 2) + (b >> 2));
+    }
 }
 
+// Block -> 16 bytes of codes and the E8M0 byte.
+template <int SRC>
+__device__ __forceinline__ void quantize_block(const RawBlock<SRC>& raw, uint4& codes, uint32_t& sbyte) {
+    uint32_t w[4];
+    if constexpr (SRC == kBF16) {
+        uint32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { v[i] = raw.a.v[i]; v[8 + i] = raw.b.v[i]; }
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = __vmaxu2(m, v[i] & 0x7fff7fffu);
+        const int e = mx_exponent_from_amax_bits(max(m & 0xffffu, m >> 16) << 16);
+        sbyte = uint32_t(e + 127);
+        const float inv = exp2i(-e);    // exact power of two: x * inv is exact or below E2M1's range
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[2 * j] = __fmul_rn(u2f(v[4 * k + j] << 16), inv);
+                f[2 * j + 1] = __fmul_rn(u2f(v[4 * k + j] & 0xffff0000u), inv);
+            }
+            w[k] = cvt_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
+        }
+    } else if constexpr (SRC == kFP32) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m = max(m, raw.a[i].v[j] & 0x7fffffffu);
+        const int e = mx_exponent_from_amax_bits(m);
+        sbyte = uint32_t(e + 127);
+        const float inv = exp2i(-e);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const u32x8& a = raw.a[k];
+            w[k] = cvt_e2m1x8(__fmul_rn(u2f(a.v[0]), inv), __fmul_rn(u2f(a.v[1]), inv), __fmul_rn(u2f(a.v[2]), inv),
+                              __fmul_rn(u2f(a.v[3]), inv), __fmul_rn(u2f(a.v[4]), inv), __fmul_rn(u2f(a.v[5]), inv),
+                              __fmul_rn(u2f(a.v[6]), inv), __fmul_rn(u2f(a.v[7]), inv));
+        }
+    } else {
+        const float ts = raw.ts;
+        // The E4M3 encoding is monotone in magnitude, and so is the FP32
+        // product with the tile scale: the block amax is the product of the
+        // largest magnitude byte.
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = __vmaxu4(m, raw.a.v[i] & 0x7f7f7f7fu);
+        m = __vmaxu4(m, m >> 16);
+        m = max(m & 0xffu, (m >> 8) & 0xffu);
+        const float amax = fabsf(__fmul_rn(e4m3x2_to_f32x2(m).x, ts));
+        const int e = mx_exponent_from_amax_bits(f2u(amax));
+        sbyte = uint32_t(e + 127);
+        const float inv = exp2i(-e);
+        if (fabsf(ts) >= 0x1p-117f) {
+            // Every non-zero product decode(e4m3) * ts is a normal FP32, so
+            // fl(fl(d * ts) * 2^-E) == fl(d * (ts * 2^-E)) whenever the result
+            // is normal, and both lie below E2M1's smallest step otherwise:
+            // one multiply by the exact ts * 2^-E gives the same codes.
+            const float sc = amax == 0.0f ? copysignf(1.0f, ts) : __fmul_rn(ts, inv);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float f[4], g[4];
+                e4m3x4_to_f32(raw.a.v[2 * k], f);
+                e4m3x4_to_f32(raw.a.v[2 * k + 1], g);
+                w[k] = cvt_e2m1x8(__fmul_rn(f[0], sc), __fmul_rn(f[1], sc), __fmul_rn(f[2], sc), __fmul_rn(f[3], sc),
+                                  __fmul_rn(g[0], sc), __fmul_rn(g[1], sc), __fmul_rn(g[2], sc), __fmul_rn(g[3], sc));
+            }
+        } else {
+            // tiny tile scale: products may be subnormal; round them first
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float f[4], g[4];
+                e4m3x4_to_f32(raw.a.v[2 * k], f);
+                e4m3x4_to_f32(raw.a.v[2 * k + 1], g);
+                w[k] = cvt_e2m1x8(__fmul_rn(__fmul_rn(f[0], ts), inv), __fmul_rn(__fmul_rn(f[1], ts), inv),
+                                  __fmul_rn(__fmul_rn(f[2], ts), inv), __fmul_rn(__fmul_rn(f[3], ts), inv),
+                                  __fmul_rn(__fmul_rn(g[0], ts), inv), __fmul_rn(__fmul_rn(g[1], ts), inv),
+                                  __fmul_rn(__fmul_rn(g[2], ts), inv), __fmul_rn(__fmul_rn(g[3], ts), inv));
+            }
+        }
+    }
+    codes = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int SRC>
+__device__ __forceinline__ void store_block(uint8_t* __restrict__ q, uint8_t* __restrict__ s, int64_t r, uint32_t b,
+                                            uint32_t bpr, int mma_layout, const uint4& codes, uint32_t sbyte) {
+    *reinterpret_cast<uint4*>(q + r * (uint64_t(bpr) * 16) + uint64_t(b) * 16) = codes;
+    const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(r), b, bpr) : uint64_t(r) * bpr + b;
+    s[so] = uint8_t(sbyte);
+}
+
+// Each thread owns block b of rows blockIdx.y, blockIdx.y + gridDim.y, ...;
+// two rows are loaded before either is processed.
 template <int SRC>
 __global__ void __launch_bounds__(256) mx_quantize_kernel(
     const uint8_t* __restrict__ x, const float* __restrict__ tile_scale, int64_t rows,
@@ -32,93 +147,20 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(
     int mma_layout) {
     const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= bpr) return;
-    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-        uint32_t codes[4];
-        uint32_t sbyte;
-        if constexpr (SRC == kBF16) {
-            const uint8_t* p = x + r * ld_x_bytes + uint64_t(b) * 64;
-            u32x8 a = ldg256(p), c = ldg256(p + 32);
-            uint32_t w[16];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) { w[i] = a.v[i]; w[8 + i] = c.v[i]; }
-            uint32_t m = 0;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) m = __vmaxu2(m, w[i] & 0x7fff7fffu);
-            uint32_t amax16 = max(m & 0xffffu, m >> 16);
-            int e = mx_exponent_from_amax_bits(amax16 << 16);
-            sbyte = uint32_t(e + 127);
-            const float inv = exp2i(-e);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t bytes[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t ww = w[4 * k + j];
-                    float lo = __fmul_rn(u2f(ww << 16), inv);
-                    float hi = __fmul_rn(u2f(ww & 0xffff0000u), inv);
-                    bytes[j] = cvt_e2m1x2(lo, hi);
-                }
-                codes[k] = pack4(bytes[0], bytes[1], bytes[2], bytes[3]);
-            }
-        } else if constexpr (SRC == kFP32) {
-            const uint8_t* p = x + r * ld_x_bytes + uint64_t(b) * 128;
-            uint32_t w[32];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                u32x8 a = ldg256(p + 32 * i);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) w[8 * i + j] = a.v[j];
-            }
-            uint32_t m = 0;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) m = max(m, w[i] & 0x7fffffffu);
-            int e = mx_exponent_from_amax_bits(m);
-            sbyte = uint32_t(e + 127);
-            const float inv = exp2i(-e);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t bytes[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    bytes[j] = cvt_e2m1x2(__fmul_rn(u2f(w[8 * k + 2 * j]), inv),
-                                          __fmul_rn(u2f(w[8 * k + 2 * j + 1]), inv));
-                codes[k] = pack4(bytes[0], bytes[1], bytes[2], bytes[3]);
-            }
-        } else {
-            const uint8_t* p = x + r * ld_x_bytes + uint64_t(b) * 32;
-            u32x8 a = ldg256(p);
-            const float ts = tile_scale[r * (bpr >> 2) + (b >> 2)];
-            // The E4M3 encoding is monotone in magnitude, and so is the FP32
-            // product with the tile scale: the block amax is the product of
-            // the largest magnitude byte.
-            uint32_t m = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) m = __vmaxu4(m, a.v[i] & 0x7f7f7f7fu);
-            m = max(max(m & 0xffu, (m >> 8) & 0xffu), max((m >> 16) & 0xffu, m >> 24));
-            float amax = fabsf(__fmul_rn(e4m3x2_to_f32x2(m).x, ts));
-            int e = mx_exponent_from_amax_bits(f2u(amax));
-            sbyte = uint32_t(e + 127);
-            const float inv = exp2i(-e);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t bytes[4];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    uint32_t ww = a.v[2 * k + j];
-                    float2 f01 = e4m3x2_to_f32x2(ww & 0xffffu);
-                    float2 f23 = e4m3x2_to_f32x2(ww >> 16);
-                    bytes[2 * j] = cvt_e2m1x2(__fmul_rn(__fmul_rn(f01.x, ts), inv),
-                                              __fmul_rn(__fmul_rn(f01.y, ts), inv));
-                    bytes[2 * j + 1] = cvt_e2m1x2(__fmul_rn(__fmul_rn(f23.x, ts), inv),
-                                                  __fmul_rn(__fmul_rn(f23.y, ts), inv));
-                }
-                codes[k] = pack4(bytes[0], bytes[1], bytes[2], bytes[3]);
-            }
+    const int64_t step = gridDim.y;
+    for (int64_t r = blockIdx.y; r < rows; r += 2 * step) {
+        const int64_t r2 = r + step;
+        RawBlock<SRC> A, B;
+        load_block<SRC>(x, tile_scale, r, b, bpr, ld_x_bytes, A);
+        if (r2 < rows) load_block<SRC>(x, tile_scale, r2, b, bpr, ld_x_bytes, B);
+        uint4 c;
+        uint32_t sb;
+        quantize_block<SRC>(A, c, sb);
+        store_block<SRC>(q, s, r, b, bpr, mma_layout, c, sb);
+        if (r2 < rows) {
+            quantize_block<SRC>(B, c, sb);
+            store_block<SRC>(q, s, r2, b, bpr, mma_layout, c, sb);
         }
-        *reinterpret_cast<uint4*>(q + r * (uint64_t(bpr) * 16) + uint64_t(b) * 16) =
-            make_uint4(codes[0], codes[1], codes[2], codes[3]);
-        const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(r), b, bpr) : uint64_t(r) * bpr + b;
-        s[so] = uint8_t(sbyte);
     }
 }
 
@@ -164,9 +206,9 @@ __global__ void __launch_bounds__(256) mx_dequantize_kernel(
     }
 }
 
-inline dim3 grid_for_rows(int64_t rows, int nx) {
-    int64_t gy = rows < 65535 ? rows : 65535;
-    return dim3(unsigned(nx), unsigned(gy > 0 ? gy : 1), 1);
+template <typename Kernel>
+inline dim3 grid_for_rows(Kernel k, int tpb, int64_t rows, int nx, int sms) {
+    return dim3(unsigned(nx), row_grid_y(rows, nx, sms, resident_per_sm(k, tpb)), 1);
 }
 
 }  // namespace
@@ -196,25 +238,31 @@ extern "C" fp4q_status fp4q_mx_quantize(const void* x, fp4q_dtype x_type, const 
         return fail(FP4Q_ERR_MISALIGNED, "mx_quantize: x must be 32-byte aligned with ld_x*elem %% 32 == 0, q 16-byte aligned");
     if (x_type == FP4Q_E4M3 && (reinterpret_cast<uintptr_t>(tile_scale) & 3u))
         return fail(FP4Q_ERR_MISALIGNED, "mx_quantize: tile_scale must be 4-byte aligned");
-    fp4q_status st = current_device(nullptr);
+    int sms = 0;
+    fp4q_status st = current_device(&sms);
     if (st != FP4Q_OK) return st;
     const uint32_t bpr = uint32_t(cols / 32);
     int tpb, nx;
     row_launch_shape(bpr, &tpb, &nx);
-    dim3 grid = grid_for_rows(rows, nx);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint8_t* xb = static_cast<const uint8_t*>(x);
     const int mma = layout == FP4Q_SCALES_MMA;
     switch (x_type) {
-        case FP4Q_BF16:
+        case FP4Q_BF16: {
+            dim3 grid = grid_for_rows(mx_quantize_kernel<kBF16>, tpb, rows, nx, sms);
             mx_quantize_kernel<kBF16><<<grid, tpb, 0, s>>>(xb, nullptr, rows, bpr, ld_x * 2, q, scales, mma);
             break;
-        case FP4Q_FP32:
+        }
+        case FP4Q_FP32: {
+            dim3 grid = grid_for_rows(mx_quantize_kernel<kFP32>, tpb, rows, nx, sms);
             mx_quantize_kernel<kFP32><<<grid, tpb, 0, s>>>(xb, nullptr, rows, bpr, ld_x * 4, q, scales, mma);
             break;
-        default:
+        }
+        default: {
+            dim3 grid = grid_for_rows(mx_quantize_kernel<kE4M3>, tpb, rows, nx, sms);
             mx_quantize_kernel<kE4M3><<<grid, tpb, 0, s>>>(xb, tile_scale, rows, bpr, ld_x, q, scales, mma);
             break;
+        }
     }
     return check_launch("mx_quantize");
 }
@@ -231,16 +279,18 @@ extern "C" fp4q_status fp4q_mx_dequantize(const uint8_t* q, const uint8_t* scale
     if (!q || !scales || !y) return fail(FP4Q_ERR_INVALID_ARGUMENT, "mx_dequantize: null pointer");
     if (!aligned16(q) || (reinterpret_cast<uintptr_t>(y) & 31u))
         return fail(FP4Q_ERR_MISALIGNED, "mx_dequantize: q must be 16-byte and y 32-byte aligned");
-    fp4q_status st = current_device(nullptr);
+    int sms = 0;
+    fp4q_status st = current_device(&sms);
     if (st != FP4Q_OK) return st;
     const uint32_t bpr = uint32_t(cols / 32);
     int tpb, nx;
     row_launch_shape(bpr, &tpb, &nx);
-    dim3 grid = grid_for_rows(rows, nx);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (y_type == FP4Q_BF16)
-        mx_dequantize_kernel<true><<<grid, tpb, 0, s>>>(q, scales, rows, bpr, static_cast<uint8_t*>(y));
+        mx_dequantize_kernel<true><<<grid_for_rows(mx_dequantize_kernel<true>, tpb, rows, nx, sms), tpb, 0, s>>>(
+            q, scales, rows, bpr, static_cast<uint8_t*>(y));
     else
-        mx_dequantize_kernel<false><<<grid, tpb, 0, s>>>(q, scales, rows, bpr, static_cast<uint8_t*>(y));
+        mx_dequantize_kernel<false><<<grid_for_rows(mx_dequantize_kernel<false>, tpb, rows, nx, sms), tpb, 0, s>>>(
+            q, scales, rows, bpr, static_cast<uint8_t*>(y));
     return check_launch("mx_dequantize");
 }

@@ -140,31 +140,28 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(
             }
         } else if constexpr (!SR) {
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                uint32_t w = 0;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    w |= cvt_e2m1x2(__fmul_rn(t[8 * k + 2 * j], rcp), __fmul_rn(t[8 * k + 2 * j + 1], rcp)) << (8 * j);
-                words[k] = w;
-            }
+            for (int k = 0; k < 2; ++k)
+                words[k] = cvt_e2m1x8(__fmul_rn(t[8 * k], rcp), __fmul_rn(t[8 * k + 1], rcp),
+                                      __fmul_rn(t[8 * k + 2], rcp), __fmul_rn(t[8 * k + 3], rcp),
+                                      __fmul_rn(t[8 * k + 4], rcp), __fmul_rn(t[8 * k + 5], rcp),
+                                      __fmul_rn(t[8 * k + 6], rcp), __fmul_rn(t[8 * k + 7], rcp));
         } else {
             const uint64_t i0 = uint64_t(r) * cols + uint64_t(b) * 16;   // linear index, % 16 == 0
             const uint32_t k0 = uint32_t(sr_seed), k1 = uint32_t(sr_seed >> 32);
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-                uint32_t w = 0;
+                float v[8];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint64_t ctr = (i0 >> 2) + uint64_t(2 * k + h);
                     const uint4 rnd = philox4x32_10(make_uint4(uint32_t(ctr), uint32_t(ctr >> 32), 0, 0), k0, k1);
                     const int base = 8 * k + 4 * h;
-                    const float v0 = sr_e2m1(__fmul_rn(t[base + 0], rcp), rnd.x);
-                    const float v1 = sr_e2m1(__fmul_rn(t[base + 1], rcp), rnd.y);
-                    const float v2 = sr_e2m1(__fmul_rn(t[base + 2], rcp), rnd.z);
-                    const float v3 = sr_e2m1(__fmul_rn(t[base + 3], rcp), rnd.w);
-                    w |= (cvt_e2m1x2(v0, v1) | (cvt_e2m1x2(v2, v3) << 8)) << (16 * h);
+                    v[4 * h + 0] = sr_e2m1(__fmul_rn(t[base + 0], rcp), rnd.x);
+                    v[4 * h + 1] = sr_e2m1(__fmul_rn(t[base + 1], rcp), rnd.y);
+                    v[4 * h + 2] = sr_e2m1(__fmul_rn(t[base + 2], rcp), rnd.z);
+                    v[4 * h + 3] = sr_e2m1(__fmul_rn(t[base + 3], rcp), rnd.w);
                 }
-                words[k] = w;
+                words[k] = cvt_e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
             }
         }
         *reinterpret_cast<uint2*>(q + uint64_t(r) * (cols / 2) + uint64_t(b) * 8) = make_uint2(words[0], words[1]);
@@ -206,15 +203,14 @@ extern "C" fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t col
     if ((reinterpret_cast<uintptr_t>(x) & 31u) || (ld_x * 2) % 32 || (q && !aligned16(q)) ||
         (workspace && !aligned16(workspace)))
         return fail(FP4Q_ERR_MISALIGNED, "nv_quantize: x 32-byte aligned with ld_x %% 16 == 0; q, workspace 16-byte aligned");
-    fp4q_status st = current_device(nullptr);
+    int sms = 0;
+    fp4q_status st = current_device(&sms);
     if (st != FP4Q_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint32_t tpr = uint32_t(cols / 16);
     int tpb = 32, nx = 1;
     if (tpr) row_launch_shape(tpr, &tpb, &nx);
-    int64_t gy = rows < 65535 ? rows : 65535;
-    if (gy < 1) gy = 1;
-    dim3 grid(unsigned(nx), unsigned(gy), 1);
+    dim3 grid(unsigned(nx), row_grid_y(rows, nx, sms, resident_per_sm(nv_quant_kernel<true>, tpb)), 1);
     const uint8_t* xb = static_cast<const uint8_t*>(x);
     const float* amax_ptr = amax_in;
     if (!amax_in) {
