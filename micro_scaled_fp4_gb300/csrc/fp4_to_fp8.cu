@@ -81,24 +81,35 @@ __global__ void __launch_bounds__(256) fp4_to_fp8_kernel(
         lut[threadIdx.x] = make_uint2(lo, hi);
     }
     __syncthreads();
-    const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= bpr) return;
+    // two adjacent blocks (2u, 2u + 1) of one 1x128 tile per thread
+    const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= (bpr >> 1)) return;
+    const uint32_t b = 2 * u;
     const int64_t step = gridDim.y;
     for (int64_t r = blockIdx.y; r < rows; r += 2 * step) {
         // two rows in flight: both rows' codes and tile exponents are loaded first
         const int64_t r2 = r + step;
         const bool two = r2 < rows;
         const uint64_t blk = uint64_t(r) * bpr + b, blk2 = uint64_t(r2) * bpr + b;
-        const uint4 cw = *reinterpret_cast<const uint4*>(q + blk * 16);
+        const uint4* c1p = reinterpret_cast<const uint4*>(q + blk * 16);
+        const uint4 cw0 = c1p[0], cw1 = c1p[1];
         const uint32_t sw = *reinterpret_cast<const uint32_t*>(s + uint64_t(r) * bpr + (b & ~3u));
-        uint4 cw2 = make_uint4(0, 0, 0, 0);
+        uint4 dw0 = make_uint4(0, 0, 0, 0), dw1 = dw0;
         uint32_t sw2 = 0;
         if (two) {
-            cw2 = *reinterpret_cast<const uint4*>(q + blk2 * 16);
+            const uint4* c2p = reinterpret_cast<const uint4*>(q + blk2 * 16);
+            dw0 = c2p[0];
+            dw1 = c2p[1];
             sw2 = *reinterpret_cast<const uint32_t*>(s + uint64_t(r2) * bpr + (b & ~3u));
         }
-        convert_block(cw, sw, b, lut, y + blk * 32, tile_scale + uint64_t(r) * (bpr >> 2) + (b >> 2));
-        if (two) convert_block(cw2, sw2, b, lut, y + blk2 * 32, tile_scale + uint64_t(r2) * (bpr >> 2) + (b >> 2));
+        float* ts = tile_scale + uint64_t(r) * (bpr >> 2) + (b >> 2);
+        convert_block(cw0, sw, b, lut, y + blk * 32, ts);
+        convert_block(cw1, sw, b + 1, lut, y + blk * 32 + 32, ts);
+        if (two) {
+            float* ts2 = tile_scale + uint64_t(r2) * (bpr >> 2) + (b >> 2);
+            convert_block(dw0, sw2, b, lut, y + blk2 * 32, ts2);
+            convert_block(dw1, sw2, b + 1, lut, y + blk2 * 32 + 32, ts2);
+        }
     }
 }
 
@@ -123,7 +134,7 @@ extern "C" fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, 
     if (st != FP4Q_OK) return st;
     const uint32_t bpr = uint32_t(cols / 32);
     int tpb, nx;
-    row_launch_shape(bpr, &tpb, &nx);
+    row_launch_shape(bpr / 2, &tpb, &nx);
     dim3 grid(unsigned(nx), row_grid_y(rows, nx, sms, resident_per_sm(fp4_to_fp8_kernel, tpb)), 1);
     fp4_to_fp8_kernel<<<grid, tpb, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, scales, rows, bpr, y, tile_scale);
     return check_launch("fp4_to_fp8");

@@ -425,16 +425,21 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 tc::named_bar_sync(1, 128);
                 uint32_t hold[4][16];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t r[32];
-                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(c * 32), r);
+                for (int c = 0; c < 8; c += 2) {
+                    // two TMEM loads in flight per wait
+                    uint32_t r0[32], r1[32];
+                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(c * 32), r0);
+                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(c * 32 + 32), r1);
                     tc::tmem_ld_wait();
                     if (c < 4) {
                         uint32_t p[16];
-                        to_bf16x32(r, alpha, p);
+                        to_bf16x32(r0, alpha, p);
                         stage_bf16x32(staging, srow, c, p);
+                        to_bf16x32(r1, alpha, p);
+                        stage_bf16x32(staging, srow, c + 1, p);
                     } else {
-                        to_bf16x32(r, alpha, hold[c - 4]);
+                        to_bf16x32(r0, alpha, hold[c - 4]);
+                        to_bf16x32(r1, alpha, hold[c - 3]);
                     }
                 }
                 tc::fence_before_sync();

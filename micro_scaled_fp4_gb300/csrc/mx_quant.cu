@@ -87,15 +87,26 @@ __device__ __forceinline__ void quantize_block(const RawBlock<SRC>& raw, uint4& 
         }
     } else {
         const float ts = raw.ts;
-        // The E4M3 encoding is monotone in magnitude, and so is the FP32
-        // product with the tile scale: the block amax is the product of the
-        // largest magnitude byte.
-        uint32_t m = 0;
+        // Decode the 32 codes to FP16 pairs (exact: E4M3 is a subset of FP16).
+        // The FP32 product with the tile scale is monotone in the magnitude, so
+        // the block amax is the product of the largest |code| (found on the
+        // FP16 pairs).
+        uint32_t h[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m = __vmaxu4(m, raw.a.v[i] & 0x7f7f7f7fu);
-        m = __vmaxu4(m, m >> 16);
-        m = max(m & 0xffu, (m >> 8) & 0xffu);
-        const float amax = fabsf(__fmul_rn(e4m3x2_to_f32x2(m).x, ts));
+        for (int i = 0; i < 8; ++i) {
+            asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n"
+                " cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+                : "=r"(h[2 * i]), "=r"(h[2 * i + 1]) : "r"(raw.a.v[i]));
+        }
+        uint32_t hm;
+        asm("abs.f16x2 %0, %1;" : "=r"(hm) : "r"(h[0]));
+#pragma unroll
+        for (int i = 1; i < 16; ++i)
+            asm("{\n .reg .b32 t;\n abs.f16x2 t, %1;\n max.f16x2 %0, %0, t;\n}" : "+r"(hm) : "r"(h[i]));
+        float mlo, mhi;
+        asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.f32.f16 %0, lo;\n cvt.f32.f16 %1, hi;\n}"
+            : "=f"(mlo), "=f"(mhi) : "r"(hm));
+        const float amax = fabsf(__fmul_rn(fmaxf(mlo, mhi), ts));
         const int e = mx_exponent_from_amax_bits(f2u(amax));
         sbyte = uint32_t(e + 127);
         const float inv = exp2i(-e);
@@ -107,11 +118,13 @@ __device__ __forceinline__ void quantize_block(const RawBlock<SRC>& raw, uint4& 
             const float sc = amax == 0.0f ? copysignf(1.0f, ts) : __fmul_rn(ts, inv);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                float f[4], g[4];
-                e4m3x4_to_f32(raw.a.v[2 * k], f);
-                e4m3x4_to_f32(raw.a.v[2 * k + 1], g);
+                float f[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.f32.f16 %0, lo;\n cvt.f32.f16 %1, hi;\n}"
+                        : "=f"(f[2 * j]), "=f"(f[2 * j + 1]) : "r"(h[4 * k + j]));
                 w[k] = cvt_e2m1x8(__fmul_rn(f[0], sc), __fmul_rn(f[1], sc), __fmul_rn(f[2], sc), __fmul_rn(f[3], sc),
-                                  __fmul_rn(g[0], sc), __fmul_rn(g[1], sc), __fmul_rn(g[2], sc), __fmul_rn(g[3], sc));
+                                  __fmul_rn(f[4], sc), __fmul_rn(f[5], sc), __fmul_rn(f[6], sc), __fmul_rn(f[7], sc));
             }
         } else {
             // tiny tile scale: products may be subnormal; round them first
@@ -161,6 +174,48 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(
             quantize_block<SRC>(B, c, sb);
             store_block<SRC>(q, s, r2, b, bpr, mma_layout, c, sb);
         }
+    }
+}
+
+// E4M3 source with two adjacent blocks per thread (one 1x128 tile holds both):
+// one tile-scale load, one index computation and 64 bytes of loads per row.
+struct RawPair { u32x8 a, b; float ts; };
+
+__global__ void __launch_bounds__(256) mx_quantize_e4m3x2_kernel(
+    const uint8_t* __restrict__ x, const float* __restrict__ tile_scale, int64_t rows,
+    uint32_t bpr, int64_t ld_x, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout) {
+    const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;      // pair index in the row
+    if (u >= (bpr >> 1)) return;
+    const int64_t step = gridDim.y;
+    auto load = [&](int64_t r, RawPair& p) {
+        const uint8_t* src = x + r * ld_x + uint64_t(u) * 64;
+        p.a = ldg256(src);
+        p.b = ldg256(src + 32);
+        p.ts = __ldg(tile_scale + r * (bpr >> 2) + (u >> 1));
+    };
+    auto process = [&](int64_t r, const RawPair& p) {
+        RawBlock<kE4M3> blk;
+        uint4 c0, c1;
+        uint32_t s0, s1;
+        blk.ts = p.ts;
+        blk.a = p.a;
+        quantize_block<kE4M3>(blk, c0, s0);
+        blk.a = p.b;
+        quantize_block<kE4M3>(blk, c1, s1);
+        uint4* dst = reinterpret_cast<uint4*>(q + r * (uint64_t(bpr) * 16) + uint64_t(u) * 32);
+        dst[0] = c0;
+        dst[1] = c1;
+        const uint32_t b0 = 2 * u;
+        const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(r), b0, bpr) : uint64_t(r) * bpr + b0;
+        *reinterpret_cast<uint16_t*>(s + so) = uint16_t(s0 | (s1 << 8));   // blocks 2u, 2u+1 are adjacent bytes
+    };
+    for (int64_t r = blockIdx.y; r < rows; r += 2 * step) {
+        const int64_t r2 = r + step;
+        RawPair A, B;
+        load(r, A);
+        if (r2 < rows) load(r2, B);
+        process(r, A);
+        if (r2 < rows) process(r2, B);
     }
 }
 
@@ -259,8 +314,10 @@ extern "C" fp4q_status fp4q_mx_quantize(const void* x, fp4q_dtype x_type, const 
             break;
         }
         default: {
-            dim3 grid = grid_for_rows(mx_quantize_kernel<kE4M3>, tpb, rows, nx, sms);
-            mx_quantize_kernel<kE4M3><<<grid, tpb, 0, s>>>(xb, tile_scale, rows, bpr, ld_x, q, scales, mma);
+            int tpb2, nx2;
+            row_launch_shape(bpr / 2, &tpb2, &nx2);
+            dim3 grid = grid_for_rows(mx_quantize_e4m3x2_kernel, tpb2, rows, nx2, sms);
+            mx_quantize_e4m3x2_kernel<<<grid, tpb2, 0, s>>>(xb, tile_scale, rows, bpr, ld_x, q, scales, mma);
             break;
         }
     }

@@ -80,23 +80,31 @@ __global__ void __launch_bounds__(256) nv_amax_kernel(const uint8_t* __restrict_
 
 // Stochastic rounding of v onto E2M1 with the 32-bit word r: up iff
 // r < frac * 2^32, frac the exact position of |v| between its two grid
-// neighbours; |v| >= 6 saturates; the sign is kept.  Returns an FP32 grid
-// value (exactly representable, so the E2M1 convert of it is exact).
-__device__ __forceinline__ float sr_e2m1(float v, uint32_t r) {
-    const float a = fabsf(v);
-    float res;
-    if (a >= 6.0f) {
-        res = 6.0f;
-    } else {
-        float lo, step;
-        if (a >= 4.0f) { lo = 4.0f; step = 2.0f; }
-        else if (a >= 2.0f) { lo = floorf(a); step = 1.0f; }
-        else { lo = __fmul_rn(floorf(__fmul_rn(a, 2.0f)), 0.5f); step = 0.5f; }
-        const float frac = __fmul_rn(__fsub_rn(a, lo), __frcp_rn(step));   // exact
-        const uint32_t thr = __float2uint_ru(__fmul_rn(frac, 4294967296.0f));
-        res = r < thr ? __fadd_rn(lo, step) : lo;
+// neighbours; |v| >= 6 saturates; the sign is kept.  Returns the 4-bit code.
+// Integer form on the FP32 bits u of |v|: for |v| in [2^k, 2^(k+1)), k >= 0,
+// the grid points are 2^k and 1.5 * 2^k (step 2^(k-1)), the code below |v| is
+// 2(k + 1) + (mantissa bit 22) and frac * 2^32 = (mantissa bits 0..21) << 10;
+// in [0.5, 1) the step is 0.5 from 0.5 (code 1), frac * 2^32 = mantissa << 9;
+// below 0.5 the step is 0.5 from 0 and frac * 2^32 = |v| * 2^33 (exact),
+// whose ceiling decides the strict comparison.
+__device__ __forceinline__ uint32_t sr_e2m1_code(float v, uint32_t r) {
+    const uint32_t bits = f2u(v);
+    const uint32_t u = bits & 0x7fffffffu;
+    const uint32_t sign = (bits >> 28) & 8u;
+    uint32_t code, thr;
+    if (u >= 0x40c00000u) {                       // |v| >= 6
+        return sign | 7u;
+    } else if (u >= 0x3f800000u) {                // [1, 6)
+        code = (((u >> 23) - 126u) << 1) | ((u >> 22) & 1u);
+        thr = (u & 0x3fffffu) << 10;
+    } else if (u >= 0x3f000000u) {                // [0.5, 1)
+        code = 1u;
+        thr = (u & 0x7fffffu) << 9;
+    } else {                                      // [0, 0.5)
+        code = 0u;
+        thr = __float2uint_ru(__fmul_rn(u2f(u), 8589934592.0f));   // |v| * 2^33 < 2^32
     }
-    return u2f(f2u(res) | (f2u(v) & 0x80000000u));
+    return sign | (code + (r < thr ? 1u : 0u));
 }
 
 template <bool SR>
@@ -150,18 +158,18 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(
             const uint32_t k0 = uint32_t(sr_seed), k1 = uint32_t(sr_seed >> 32);
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-                float v[8];
+                uint32_t w = 0;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint64_t ctr = (i0 >> 2) + uint64_t(2 * k + h);
                     const uint4 rnd = philox4x32_10(make_uint4(uint32_t(ctr), uint32_t(ctr >> 32), 0, 0), k0, k1);
                     const int base = 8 * k + 4 * h;
-                    v[4 * h + 0] = sr_e2m1(__fmul_rn(t[base + 0], rcp), rnd.x);
-                    v[4 * h + 1] = sr_e2m1(__fmul_rn(t[base + 1], rcp), rnd.y);
-                    v[4 * h + 2] = sr_e2m1(__fmul_rn(t[base + 2], rcp), rnd.z);
-                    v[4 * h + 3] = sr_e2m1(__fmul_rn(t[base + 3], rcp), rnd.w);
+                    const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w |= sr_e2m1_code(__fmul_rn(t[base + e], rcp), rr[e]) << (4 * (4 * h + e));
                 }
-                words[k] = cvt_e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+                words[k] = w;
             }
         }
         *reinterpret_cast<uint2*>(q + uint64_t(r) * (cols / 2) + uint64_t(b) * 8) = make_uint2(words[0], words[1]);
