@@ -206,6 +206,7 @@ def main_rows(fq, W, torch, peaks):
     rows = {}
     stream = torch.cuda.current_stream()
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
+    lib = fq.load()
 
     def timed(fn, iters, do_flush):
         ts = []
@@ -283,7 +284,6 @@ def main_rows(fq, W, torch, peaks):
     del xg, q3, s3
 
     # C4: block-scaled GEMM 8192^3, MXFP4 and NVFP4 (RHT), BF16 out
-    lib = fq.load()
     if getattr(lib, "fp4q_block_scaled_gemm", None) is not None:
         a, b = W.gemm_operands()
         ad, bd = dev_bf16(a), dev_bf16(b)
@@ -312,7 +312,100 @@ def main_rows(fq, W, torch, peaks):
             "peak_source": f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
             "mx_quantize_operand_ms": round(ms_qa, 4)}
         del ad, bd, qa, sa, qb, sb, D, ra, rb
+    torch.cuda.empty_cache()
+    if getattr(lib, "fp4q_grouped_gemm", None) is not None:
+        rows["moe_ffn_65536x7168_top8_of_64"] = moe_row(fq, W, torch, peaks, timed)
     return rows
+
+
+def moe_row(fq, W, torch, peaks, timed):
+    """MoE expert FFN forward in FP4: 65536 tokens x 7168, top-8 of 64 experts
+    (Zipf 1.1), experts 7168 -> 2x2048 (SiLU gate) -> 7168, NVFP4 weights."""
+    T, H, I, E, k = 65536, 7168, 2048, 64, 8
+    R = T * k
+    stream = torch.cuda.current_stream()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(8)
+    x = torch.randn((T, H), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    topk = torch.from_numpy(W.moe_routing(tokens=T, experts=E, top_k=k, seed=9)).cuda()
+    w1 = W.moe_weights_torch(E, 2 * I, H, 10, "cuda")
+    w2 = W.moe_weights_torch(E, H, I, 11, "cuda")
+
+    def quant_weights(w, rows, cols):
+        q = torch.empty((E * rows, cols // 2), dtype=torch.uint8, device="cuda")
+        per = fq.fp4q_scales_bytes(rows, cols // 16, fq.FP4Q_SCALES_MMA)
+        sc = torch.empty(E * per, dtype=torch.uint8, device="cuda")
+        st = torch.empty(E, dtype=torch.float32, device="cuda")
+        wsb = fq.fp4q_nv_quantize_workspace_bytes(rows, cols)
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        for e in range(E):
+            fq.fp4q_nv_quantize(w[e], rows, cols, cols, 1, 0, 0, fq.FP4Q_RNE, 0, None, None, st.data_ptr() + 4 * e,
+                                q.data_ptr() + e * rows * (cols // 2), sc.data_ptr() + e * per, fq.FP4Q_SCALES_MMA,
+                                ws, wsb, stream)
+        return q, sc, st
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    w1q, w1s, w1t = quant_weights(w1, 2 * I, H)
+    w2q, w2s, w2t = quant_weights(w2, H, I)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wq_ms = e0.elapsed_time(e1)
+    del w1, w2
+
+    # buffers
+    xq = torch.empty((T, H // 2), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((T, H // 32), dtype=torch.uint8, device="cuda")
+    offs = torch.empty(E + 1, dtype=torch.int64, device="cuda")
+    rtok = torch.empty(R, dtype=torch.int32, device="cuda")
+    dq = torch.empty((R, H // 2), dtype=torch.uint8, device="cuda")
+    ds = torch.empty((R, H // 32), dtype=torch.uint8, device="cuda")
+    wsb = fq.fp4q_moe_dispatch_workspace_bytes(T, k, E)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    ue1 = torch.empty(fq.fp4q_rebased_scales_bytes(R, H, E), dtype=torch.uint8, device="cuda")
+    rs1 = torch.empty(R, dtype=torch.float32, device="cuda")
+    hq = torch.empty((R, I // 2), dtype=torch.uint8, device="cuda")
+    hs = torch.empty((R, I // 32), dtype=torch.uint8, device="cuda")
+    ue2 = torch.empty(fq.fp4q_rebased_scales_bytes(R, I, E), dtype=torch.uint8, device="cuda")
+    rs2 = torch.empty(R, dtype=torch.float32, device="cuda")
+    y = torch.empty((R, H), dtype=torch.bfloat16, device="cuda")
+    viol = torch.zeros(2, dtype=torch.int32, device="cuda")
+
+    stages = [
+        ("a1_quantize_tokens", lambda: fq.fp4q_mx_quantize(x, fq.FP4Q_BF16, None, T, H, H, 1, xq, xs, 0, stream)),
+        ("a9_dispatch", lambda: fq.fp4q_moe_dispatch(topk, T, k, E, xq, xs, H, offs, rtok, dq, ds, ws, wsb, stream)),
+        ("rebase_tokens", lambda: fq.fp4q_mx_rebase_scales(ds, R, H, offs, E, ue1, rs1, viol, stream)),
+        ("a10_up_silu_gate_mxfp4", lambda: fq.fp4q_grouped_gemm(dq, ue1, rs1, w1q, w1s, w1t, offs, R, E, 2 * I, H,
+                                                              fq.FP4Q_EPI_SILU_GATE_MXFP4, hq, hs, None, stream)),
+        ("rebase_h", lambda: fq.fp4q_mx_rebase_scales(hs, R, I, offs, E, ue2, rs2, viol[1:], stream)),
+        ("a11_down", lambda: fq.fp4q_grouped_gemm(hq, ue2, rs2, w2q, w2s, w2t, offs, R, E, H, I,
+                                                fq.FP4Q_EPI_STORE_BF16, y, None, None, stream)),
+    ]
+    for _, fn in stages:          # warm-up pass (the dispatch must precede the rest)
+        fn()
+    torch.cuda.synchronize()
+    out = {}
+    total = 0.0
+    for name, fn in stages:
+        ms = timed(fn, 5, True)
+        out[name + "_ms"] = round(ms, 4)
+        total += ms
+    f_up = 2.0 * R * H * (2 * I)
+    f_down = 2.0 * R * I * H
+    peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    out["total_ms"] = round(total, 4)
+    out["TFLOPS_end_to_end"] = round((f_up + f_down) / total / 1e9, 1)
+    out["up_TFLOPS"] = round(f_up / out["a10_up_silu_gate_mxfp4_ms"] / 1e9, 1)
+    out["down_TFLOPS"] = round(f_down / out["a11_down_ms"] / 1e9, 1)
+    out["up_frac_peak"] = round(f_up / out["a10_up_silu_gate_mxfp4_ms"] / 1e9 / peak, 3)
+    out["down_frac_peak"] = round(f_down / out["a11_down_ms"] / 1e9 / peak, 3)
+    nb_q = T * H * 2 + T * H // 2 + T * H // 32
+    out["a1_GB_per_s"] = round(nb_q / out["a1_quantize_tokens_ms"] / 1e6, 1)
+    nb_d = 2 * R * (H // 2 + H // 32) + T * k * 4
+    out["a9_GB_per_s"] = round(nb_d / out["a9_dispatch_ms"] / 1e6, 1)
+    out["rebase_violations"] = int(viol.sum().item())
+    out["weight_quantize_ms_offline"] = round(wq_ms, 3)
+    out["tokens_per_expert_min_max"] = [int(v) for v in torch.diff(offs).aminmax()]
+    return out
 
 
 def run_gpu(args, rank, world):

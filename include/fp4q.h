@@ -300,6 +300,16 @@ fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_scales, const
  */
 fp4q_status fp4q_device_status(uint32_t* status_out, int reset);
 
+/*
+ * fp4q_check_wait_timeout -- self-check of the device-side failure path.  The
+ * pages have no counterpart: this is library infrastructure.  Launches one
+ * thread that waits, with the same bounded mbarrier wait the GEMM kernels use,
+ * on a barrier that nothing completes; after `limit_ns` (at most 2 s) it gives
+ * up and sets bit 31 of the device status word, which fp4q_device_status()
+ * then reports as FP4Q_ERR_TIMEOUT.  The GPU context stays usable.
+ */
+fp4q_status fp4q_check_wait_timeout(uint64_t limit_ns, fp4q_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

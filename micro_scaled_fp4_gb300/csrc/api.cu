@@ -5,6 +5,7 @@
 #include <stdio.h>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace fp4q {
 
@@ -78,9 +79,33 @@ uint32_t* status_word() {
     return g_dev[dev].status;
 }
 
+namespace {
+// One thread waits, with the library's bounded wait, on an mbarrier that
+// nothing will ever complete; when the limit runs out it records the
+// self-check bit in the status word and returns.
+__global__ void wait_timeout_kernel(uint64_t limit_ns, uint32_t* status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    tc::mbar_init(tc::smem_u32(&bar), 1);
+    tc::fence_barrier_init();
+    if (!tc::mbar_wait(tc::smem_u32(&bar), 0, &abort_flag, limit_ns)) atomicOr(status, kStatusSelfCheck);
+}
+}  // namespace
+
 }  // namespace fp4q
 
 using namespace fp4q;
+
+extern "C" fp4q_status fp4q_check_wait_timeout(uint64_t limit_ns, fp4q_stream_t stream) {
+    if (limit_ns == 0 || limit_ns > 2000000000ull)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "check_wait_timeout: limit must be in (0, 2 s]");
+    fp4q_status st = current_device(nullptr);
+    if (st != FP4Q_OK) return st;
+    wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns, status_word());
+    return check_launch("check_wait_timeout");
+}
 
 extern "C" const char* fp4q_status_string(fp4q_status s) {
     switch (s) {

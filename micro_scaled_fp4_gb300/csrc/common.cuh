@@ -27,7 +27,7 @@ uint32_t* status_word();
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Status-word bits (which kernel gave up a bounded wait).
-enum : uint32_t { kStatusGemmTimeout = 1u << 0, kStatusGroupedTimeout = 1u << 1 };
+enum : uint32_t { kStatusGemmTimeout = 1u << 0, kStatusGroupedTimeout = 1u << 1, kStatusSelfCheck = 1u << 31 };
 
 // ---------------------------------------------------------------------------
 // Device side

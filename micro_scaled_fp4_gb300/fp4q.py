@@ -32,7 +32,7 @@ EXPORTED = [
     "fp4q_mx_dequantize", "fp4q_fp4_to_fp8", "fp4q_nv_quantize_workspace_bytes", "fp4q_nv_quantize",
     "fp4q_block_scaled_gemm", "fp4q_device_status", "fp4q_moe_dispatch_workspace_bytes",
     "fp4q_moe_dispatch", "fp4q_rebased_scales_bytes", "fp4q_mx_rebase_scales", "fp4q_grouped_gemm",
-    "fp4q_moe_dispatch_static",
+    "fp4q_moe_dispatch_static", "fp4q_check_wait_timeout",
 ]
 MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 * 1024 * 1024
 
@@ -91,6 +91,7 @@ def load() -> ctypes.CDLL:
                 "fp4q_moe_dispatch": [vp, i64, ci, ci, vp, vp, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp],
                 "fp4q_mx_rebase_scales": [vp, i64, i64, vp, i64, vp, vp, vp, vp],
                 "fp4q_moe_dispatch_static": [vp, i64, ci, ci, vp, vp, i64, vp, vp, vp, vp, vp],
+                "fp4q_check_wait_timeout": [u64, vp],
                 "fp4q_grouped_gemm": [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ci, vp, vp, vp, vp],
             }
             for name, args in sigs.items():
@@ -208,6 +209,10 @@ def fp4q_grouped_gemm(a_q, a_scales, a_row_scale, b_q, b_scales, b_tensor_scale,
     return _check("fp4q_grouped_gemm", load().fp4q_grouped_gemm(
         _ptr(a_q), _ptr(a_scales), _ptr(a_row_scale), _ptr(b_q), _ptr(b_scales), _ptr(b_tensor_scale),
         _ptr(offsets), rows, groups, N, K, epilogue, _ptr(D), _ptr(d_scales), _ptr(h_debug), _stream(stream)))
+
+
+def fp4q_check_wait_timeout(limit_ns: int, stream=None):
+    return _check("fp4q_check_wait_timeout", load().fp4q_check_wait_timeout(limit_ns, _stream(stream)))
 
 
 def fp4q_device_status(reset: bool = False) -> int:

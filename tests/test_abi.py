@@ -80,6 +80,13 @@ def test_argument_errors_need_no_gpu(lib):
         with pytest.raises(E) as e:
             fn()
         assert e.value.status == status, (e.value, status)
+    for limit in (0, 3_000_000_000):
+        with pytest.raises(E) as e:
+            lib.fp4q_check_wait_timeout(limit, stream=0)
+        assert e.value.status == 1
+    with pytest.raises(E) as e:       # scratch of the static-array dispatch would not fit
+        lib.fp4q_moe_dispatch_static(x, 1 << 22, 8, 64, x, x, 64, x, x, x, x, stream=0)
+    assert e.value.status == 2
     A = lib.make_operand(x, x, lib.FP4Q_MXFP4)
     B = lib.make_operand(x, x, lib.FP4Q_NVFP4, x)
     for args, status in [((A, B, 128, 128, 128, x, 0, 128), 1), ((A, A, 128, 128, 96, x, 0, 128), 2),
