@@ -54,7 +54,7 @@ constexpr uint32_t STAGING_OFF = STAGES * STAGE_BYTES;
 constexpr uint32_t BARS_OFF = STAGING_OFF + STAGING_BYTES;
 constexpr uint32_t PREFIX_OFF = BARS_OFF + 256;
 constexpr uint32_t SMEM_BYTES = PREFIX_OFF + 4 * 260 + 1024;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;          // producer warp, MMA warp, 8 epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SFA = 256;                    // 16 columns
 constexpr uint32_t TMEM_SFB = 272;                    // 32 columns
@@ -182,7 +182,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             tc::mbar_init(empty_bar(s), 1);
         }
         tc::mbar_init(tmem_full, 1);
-        tc::mbar_init(tmem_empty, 4);       // one arrival per epilogue warp
+        tc::mbar_init(tmem_empty, 8);       // one arrival per epilogue warp
         tc::mbar_init(drain_bar, 1);
         *abort = 0;
         tc::fence_barrier_init();
@@ -356,7 +356,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         }
     } else if (warp >= 2) {
         // ---------------- epilogue ----------------
-        const int q = warp & 3;                         // TMEM lane quadrant of this warp
+        // Eight warps: warp w reads TMEM lane quadrant w % 4 (rows 32q .. 32q + 31 of
+        // the tile) and the column half hf of the tile, so each warp's share of
+        // the accumulator read (the part the MMA thread waits for) is 128 columns.
+        const int q = warp & 3;
+        const int hf = (warp - 2) >> 2;
+        const int et = int(threadIdx.x) - 64;            // epilogue thread 0..255
         const float dense_alpha = (!args.groups && args.nv) ? __fmul_rn(*args.ts_a, *args.ts_b) : 1.0f;
         int tcount = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
@@ -372,120 +377,110 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             if (args.groups && row_ok) alpha = __fmul_rn(args.a_row_scale[row], args.ts_b[t.group]);
             const uint32_t lane_addr = tmem + (uint32_t(q * 32) << 16);
             if constexpr (EPI == kSiluGate) {
+                // h columns [64 hf, 64 hf + 64) of the tile: gate accumulator columns
+                // 64 hf + j, up columns 128 + 64 hf + j
                 const int hcols = args.N / 2;
+                uint32_t g0[32], u0[32], g1[32], u1[32];
+                tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(64 * hf), g0);
+                tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(128 + 64 * hf), u0);
+                tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(64 * hf + 32), g1);
+                tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(128 + 64 * hf + 32), u1);
+                tc::tmem_ld_wait();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tmem_empty);
+                if (row_ok) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const uint32_t(&g)[32] = c ? g1 : g0;
+                        const uint32_t(&u)[32] = c ? u1 : u0;
+                        float h[32];
+                        uint32_t amax = 0;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float gv = __fmul_rn(u2f(g[i]), alpha);
+                            const float uv = __fmul_rn(u2f(u[i]), alpha);
+                            const float sig = __fdiv_rn(gv, __fadd_rn(1.0f, expf(-gv)));   // SiLU
+                            h[i] = __fmul_rn(sig, uv);
+                            amax = max(amax, f2u(h[i]) & 0x7fffffffu);
+                        }
+                        const int col = t.col0 + 64 * hf + 32 * c;
+                        if (args.h_debug) {
+                            float4* dbg = reinterpret_cast<float4*>(args.h_debug + int64_t(row) * hcols + col);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                dbg[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                        }
+                        const int e = mx_exponent_from_amax_bits(amax);
+                        const float inv = exp2i(-e);
+                        uint32_t w[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            w[k] = cvt_e2m1x8(__fmul_rn(h[8 * k], inv), __fmul_rn(h[8 * k + 1], inv),
+                                              __fmul_rn(h[8 * k + 2], inv), __fmul_rn(h[8 * k + 3], inv),
+                                              __fmul_rn(h[8 * k + 4], inv), __fmul_rn(h[8 * k + 5], inv),
+                                              __fmul_rn(h[8 * k + 6], inv), __fmul_rn(h[8 * k + 7], inv));
+                        *reinterpret_cast<uint4*>(args.D + int64_t(row) * (hcols / 2) + col / 2) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                        args.h_scales[int64_t(row) * (hcols / 32) + col / 32] = uint8_t(e + 127);
+                    }
+                }
+            } else if (args.d_bf16 && t.a_row0 + BM <= t.row_end + (args.groups ? 0 : BM)) {
+                // BF16 through shared memory and TMA stores.  Each warp moves its 32 rows
+                // x 128 columns out of TMEM into registers, then the accumulator goes
+                // back to the MMA thread; half 0 is staged and stored, then half 1.
+                const int srow = q * 32 + lane;                  // row within the tile
+                uint32_t hold[4][16];
+#pragma unroll
+                for (int c = 0; c < 4; c += 2) {
+                    uint32_t r0[32], r1[32];
+                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(128 * hf + 32 * c), r0);
+                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(128 * hf + 32 * c + 32), r1);
+                    tc::tmem_ld_wait();
+                    to_bf16x32(r0, alpha, hold[c]);
+                    to_bf16x32(r1, alpha, hold[c + 1]);
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tmem_empty);
+                if (et == 0) tc::bulk_wait_read0();              // previous tile's stores have read the staging
+                tc::named_bar_sync(1, 256);
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    if (hf == h2) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) stage_bf16x32(staging, srow, c, hold[c]);
+                    }
+                    tc::fence_proxy_async_smem();
+                    tc::named_bar_sync(1, 256);
+                    if (et == 0) {
+                        for (int b = 0; b < 2; ++b) {
+                            const int col = t.col0 + 128 * h2 + 64 * b;
+                            if (col < args.N)
+                                tc::tma_store_2d(&tmap_d, staging + uint32_t(b) * BOX_BYTES, col, t.a_row0);
+                        }
+                        tc::bulk_commit();
+                        if (h2 == 0) tc::bulk_wait_read0();
+                    }
+                    if (h2 == 0) tc::named_bar_sync(1, 256);
+                }
+            } else {
+                // direct stores (FP32 output, or a tile that ends inside its group)
                 for (int c = 0; c < 4; ++c) {
-                    uint32_t g[32], u[32];
-                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(c * 32), g);
-                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(128 + c * 32), u);
+                    uint32_t r[32];
+                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(128 * hf + 32 * c), r);
                     tc::tmem_ld_wait();
                     if (c == 3) {
                         tc::fence_before_sync();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(tmem_empty);
                     }
-                    if (!row_ok) continue;
-                    float h[32];
-                    uint32_t amax = 0;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float gv = __fmul_rn(u2f(g[i]), alpha);
-                        const float uv = __fmul_rn(u2f(u[i]), alpha);
-                        const float sig = __fdiv_rn(gv, __fadd_rn(1.0f, expf(-gv)));   // SiLU
-                        h[i] = __fmul_rn(sig, uv);
-                        amax = max(amax, f2u(h[i]) & 0x7fffffffu);
-                    }
-                    const int col = t.col0 + c * 32;
-                    if (args.h_debug) {
-                        float4* dbg = reinterpret_cast<float4*>(args.h_debug + int64_t(row) * hcols + col);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) dbg[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-                    }
-                    const int e = mx_exponent_from_amax_bits(amax);
-                    const float inv = exp2i(-e);
-                    uint32_t w[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint32_t v = 0;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            v |= cvt_e2m1x2(__fmul_rn(h[8 * k + 2 * j], inv), __fmul_rn(h[8 * k + 2 * j + 1], inv))
-                                 << (8 * j);
-                        w[k] = v;
-                    }
-                    *reinterpret_cast<uint4*>(args.D + int64_t(row) * (hcols / 2) + col / 2) = make_uint4(w[0], w[1], w[2], w[3]);
-                    args.h_scales[int64_t(row) * (hcols / 32) + col / 32] = uint8_t(e + 127);
-                }
-            } else if (args.d_bf16 && t.a_row0 + BM <= t.row_end + (args.groups ? 0 : BM)) {
-                // BF16 through shared memory and TMA stores.  All 256 columns leave
-                // TMEM first (half 0 into the staging buffer, half 1 into registers),
-                // then the accumulator goes back to the MMA thread.
-                const int et = int(threadIdx.x) - 64;            // epilogue thread 0..127
-                const int srow = q * 32 + lane;                  // row within the tile
-                if (et == 0) tc::bulk_wait_read0();              // previous tile's stores have read the staging
-                tc::named_bar_sync(1, 128);
-                uint32_t hold[4][16];
-#pragma unroll
-                for (int c = 0; c < 8; c += 2) {
-                    // two TMEM loads in flight per wait
-                    uint32_t r0[32], r1[32];
-                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(c * 32), r0);
-                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(c * 32 + 32), r1);
-                    tc::tmem_ld_wait();
-                    if (c < 4) {
-                        uint32_t p[16];
-                        to_bf16x32(r0, alpha, p);
-                        stage_bf16x32(staging, srow, c, p);
-                        to_bf16x32(r1, alpha, p);
-                        stage_bf16x32(staging, srow, c + 1, p);
-                    } else {
-                        to_bf16x32(r0, alpha, hold[c - 4]);
-                        to_bf16x32(r1, alpha, hold[c - 3]);
-                    }
-                }
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(tmem_empty);
-                tc::fence_proxy_async_smem();
-                tc::named_bar_sync(1, 128);
-                if (et == 0) {
-                    for (int b = 0; b < 2; ++b)
-                        if (t.col0 + 64 * b < args.N)
-                            tc::tma_store_2d(&tmap_d, staging + uint32_t(b) * BOX_BYTES, t.col0 + 64 * b, t.a_row0);
-                    tc::bulk_commit();
-                    tc::bulk_wait_read0();
-                }
-                tc::named_bar_sync(1, 128);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) stage_bf16x32(staging, srow, c, hold[c]);
-                tc::fence_proxy_async_smem();
-                tc::named_bar_sync(1, 128);
-                if (et == 0) {
-                    for (int b = 2; b < 4; ++b)
-                        if (t.col0 + 64 * b < args.N)
-                            tc::tma_store_2d(&tmap_d, staging + uint32_t(b - 2) * BOX_BYTES, t.col0 + 64 * b,
-                                             t.a_row0);
-                    tc::bulk_commit();
-                }
-            } else {
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(c * 32), r);
-                    tc::tmem_ld_wait();
-                    if (c == BN / 32 - 1) {
-                        tc::fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(tmem_empty);
-                    }
-                    const int col = t.col0 + c * 32;
+                    const int col = t.col0 + 128 * hf + c * 32;
                     if (!row_ok || col >= args.N) continue;
                     const int ncol = min(32, args.N - col);
                     if (args.d_bf16) {
                         uint32_t p[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float lo = __fmul_rn(u2f(r[2 * i]), alpha), hi = __fmul_rn(u2f(r[2 * i + 1]), alpha);
-                            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(p[i]) : "f"(hi), "f"(lo));
-                        }
+                        to_bf16x32(r, alpha, p);
                         uint8_t* dst = args.D + (int64_t(row) * args.ldd + col) * 2;
                         if (ncol == 32) {
 #pragma unroll
