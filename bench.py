@@ -201,8 +201,13 @@ def _events(torch, n):
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
 
-def main_rows(fq, W, torch, peaks):
-    """The other hot-path rows, each timed with CUDA events (inputs > L2 or L2 flushed)."""
+ROW_NAMES = ("c1", "c3", "gemm", "moe")
+
+
+def main_rows(fq, W, torch, peaks, which=ROW_NAMES, moe_tokens=65536):
+    """The other hot-path rows, each timed with CUDA events (inputs > L2 or L2 flushed).
+    `which` selects the rows: c1 (MXFP4 round trip), c3 (NVFP4 of a gradient),
+    gemm (dense block-scaled GEMM), moe (MoE expert FFN)."""
     rows = {}
     stream = torch.cuda.current_stream()
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
@@ -225,7 +230,21 @@ def main_rows(fq, W, torch, peaks):
     def dev_bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
-    # C1: MXFP4 round trip, BF16 256x4096 (5 MB: L2-resident, launch-latency bound)
+    if "c1" in which:
+        c1_row(fq, W, torch, peaks, timed, dev_bf16, rows)
+    if "c3" in which:
+        c3_row(fq, W, torch, peaks, timed, dev_bf16, rows)
+    if "gemm" in which and getattr(lib, "fp4q_block_scaled_gemm", None) is not None:
+        gemm_row(fq, W, torch, peaks, timed, dev_bf16, rows)
+    torch.cuda.empty_cache()
+    if "moe" in which and getattr(lib, "fp4q_grouped_gemm", None) is not None:
+        rows[f"moe_ffn_{moe_tokens}x7168_top8_of_64"] = moe_row(fq, W, torch, peaks, timed, moe_tokens)
+    return rows
+
+
+def c1_row(fq, W, torch, peaks, timed, dev_bf16, rows):
+    """C1: MXFP4 round trip, BF16 256x4096 (5 MB: L2-resident, launch-latency bound)."""
+    stream = torch.cuda.current_stream()
     x = dev_bf16(W.activation_bf16())
     q = torch.empty((256, 2048), dtype=torch.uint8, device="cuda")
     s = torch.empty((256, 128), dtype=torch.uint8, device="cuda")
@@ -254,7 +273,10 @@ def main_rows(fq, W, torch, peaks):
         rows["mx_roundtrip_bf16_256x4096"]["graph_error"] = str(e)[:120]
     del x, q, s, y, g, graph_c1
 
-    # C3: NVFP4 of a BF16 8192x14336 Student-t gradient, RHT, SR then RNE (235 MB > L2)
+
+def c3_row(fq, W, torch, peaks, timed, dev_bf16, rows):
+    """C3: NVFP4 of a BF16 8192x14336 Student-t gradient, RHT, SR then RNE (235 MB > L2)."""
+    stream = torch.cuda.current_stream()
     R3, C3 = 8192, 14336
     xg = dev_bf16(W.gradient_bf16(R3, C3))
     q3 = torch.empty((R3, C3 // 2), dtype=torch.uint8, device="cuda")
@@ -283,45 +305,43 @@ def main_rows(fq, W, torch, peaks):
         "frac_hbm_sr_quant_pass": round(b_quant / ms_sr1 / 1e6 / peaks["hbm_gbs"], 3)}
     del xg, q3, s3
 
-    # C4: block-scaled GEMM 8192^3, MXFP4 and NVFP4 (RHT), BF16 out
-    if getattr(lib, "fp4q_block_scaled_gemm", None) is not None:
-        a, b = W.gemm_operands()
-        ad, bd = dev_bf16(a), dev_bf16(b)
-        qa, sa = fq.mx_quantize(ad, layout=fq.FP4Q_SCALES_MMA)
-        qb, sb = fq.mx_quantize(bd, layout=fq.FP4Q_SCALES_MMA)
-        ms_qa = timed(lambda: fq.mx_quantize(ad, layout=fq.FP4Q_SCALES_MMA), 10, True)
-        D = torch.empty((8192, 8192), dtype=torch.bfloat16, device="cuda")
-        A = fq.make_operand(qa, sa, fq.FP4Q_MXFP4)
-        B = fq.make_operand(qb, sb, fq.FP4Q_MXFP4)
-        flops = 2.0 * 8192 ** 3
-        ms_mx = timed(lambda: fq.fp4q_block_scaled_gemm(A, B, 8192, 8192, 8192, D, fq.FP4Q_BF16, 8192, stream), 10,
-                      True)
-        ra = fq.nv_quantize(ad, rht=True, rht_seed=7, layout=fq.FP4Q_SCALES_MMA)
-        rb = fq.nv_quantize(bd, rht=True, rht_seed=7, layout=fq.FP4Q_SCALES_MMA)
-        An = fq.make_operand(ra["q"], ra["scales"], fq.FP4Q_NVFP4, ra["s_t"])
-        Bn = fq.make_operand(rb["q"], rb["scales"], fq.FP4Q_NVFP4, rb["s_t"])
-        ms_nv = timed(lambda: fq.fp4q_block_scaled_gemm(An, Bn, 8192, 8192, 8192, D, fq.FP4Q_BF16, 8192, stream),
-                      10, True)
-        peak = peaks["bf16_tflops"] * FP4_OVER_BF16
-        rows["gemm_fp4_8192^3"] = {
-            "mxfp4_ms": round(ms_mx, 4), "mxfp4_TFLOPS": round(flops / ms_mx / 1e9, 1),
-            "mxfp4_frac_peak": round(flops / ms_mx / 1e9 / peak, 3),
-            "nvfp4_ms": round(ms_nv, 4), "nvfp4_TFLOPS": round(flops / ms_nv / 1e9, 1),
-            "nvfp4_frac_peak": round(flops / ms_nv / 1e9 / peak, 3),
-            "peak_TFLOPS": round(peak, 1),
-            "peak_source": f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
-            "mx_quantize_operand_ms": round(ms_qa, 4)}
-        del ad, bd, qa, sa, qb, sb, D, ra, rb
-    torch.cuda.empty_cache()
-    if getattr(lib, "fp4q_grouped_gemm", None) is not None:
-        rows["moe_ffn_65536x7168_top8_of_64"] = moe_row(fq, W, torch, peaks, timed)
-    return rows
+
+def gemm_row(fq, W, torch, peaks, timed, dev_bf16, rows):
+    """C4: block-scaled GEMM 8192^3, MXFP4 and NVFP4 (RHT), BF16 out."""
+    stream = torch.cuda.current_stream()
+    a, b = W.gemm_operands()
+    ad, bd = dev_bf16(a), dev_bf16(b)
+    qa, sa = fq.mx_quantize(ad, layout=fq.FP4Q_SCALES_MMA)
+    qb, sb = fq.mx_quantize(bd, layout=fq.FP4Q_SCALES_MMA)
+    ms_qa = timed(lambda: fq.mx_quantize(ad, layout=fq.FP4Q_SCALES_MMA), 10, True)
+    D = torch.empty((8192, 8192), dtype=torch.bfloat16, device="cuda")
+    A = fq.make_operand(qa, sa, fq.FP4Q_MXFP4)
+    B = fq.make_operand(qb, sb, fq.FP4Q_MXFP4)
+    flops = 2.0 * 8192 ** 3
+    ms_mx = timed(lambda: fq.fp4q_block_scaled_gemm(A, B, 8192, 8192, 8192, D, fq.FP4Q_BF16, 8192, stream), 10,
+                  True)
+    ra = fq.nv_quantize(ad, rht=True, rht_seed=7, layout=fq.FP4Q_SCALES_MMA)
+    rb = fq.nv_quantize(bd, rht=True, rht_seed=7, layout=fq.FP4Q_SCALES_MMA)
+    An = fq.make_operand(ra["q"], ra["scales"], fq.FP4Q_NVFP4, ra["s_t"])
+    Bn = fq.make_operand(rb["q"], rb["scales"], fq.FP4Q_NVFP4, rb["s_t"])
+    ms_nv = timed(lambda: fq.fp4q_block_scaled_gemm(An, Bn, 8192, 8192, 8192, D, fq.FP4Q_BF16, 8192, stream),
+                  10, True)
+    peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    rows["gemm_fp4_8192^3"] = {
+        "mxfp4_ms": round(ms_mx, 4), "mxfp4_TFLOPS": round(flops / ms_mx / 1e9, 1),
+        "mxfp4_frac_peak": round(flops / ms_mx / 1e9 / peak, 3),
+        "nvfp4_ms": round(ms_nv, 4), "nvfp4_TFLOPS": round(flops / ms_nv / 1e9, 1),
+        "nvfp4_frac_peak": round(flops / ms_nv / 1e9 / peak, 3),
+        "peak_TFLOPS": round(peak, 1),
+        "peak_source": f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
+        "mx_quantize_operand_ms": round(ms_qa, 4)}
+    del ad, bd, qa, sa, qb, sb, D, ra, rb
 
 
-def moe_row(fq, W, torch, peaks, timed):
-    """MoE expert FFN forward in FP4: 65536 tokens x 7168, top-8 of 64 experts
+def moe_row(fq, W, torch, peaks, timed, T=65536):
+    """MoE expert FFN forward in FP4: T tokens x 7168, top-8 of 64 experts
     (Zipf 1.1), experts 7168 -> 2x2048 (SiLU gate) -> 7168, NVFP4 weights."""
-    T, H, I, E, k = 65536, 7168, 2048, 64, 8
+    H, I, E, k = 7168, 2048, 64, 8
     R = T * k
     stream = torch.cuda.current_stream()
     g = torch.Generator(device="cuda")
@@ -351,6 +371,7 @@ def moe_row(fq, W, torch, peaks, timed):
     torch.cuda.synchronize()
     wq_ms = e0.elapsed_time(e1)
     del w1, w2
+    torch.cuda.empty_cache()
 
     # buffers
     xq = torch.empty((T, H // 2), dtype=torch.uint8, device="cuda")
@@ -528,7 +549,7 @@ def run_gpu(args, rank, world):
     if rank == 0 and not args.no_rows:
         del sets
         torch.cuda.empty_cache()
-        rows = main_rows(fq, W, torch, peaks)
+        rows = main_rows(fq, W, torch, peaks, args.rows.split(","), args.moe_tokens)
     if rank == 0 and not args.no_cpu:
         sample = 256
         v, dt, cores = cpu_oracle_rate(sample)
@@ -559,7 +580,13 @@ def main():
     ap.add_argument("--impl", default="fp4q", choices=["fp4q", "reference"])
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--rows", default=",".join(ROW_NAMES),
+                    help="comma-separated rows to report besides the step: " + ", ".join(ROW_NAMES))
+    ap.add_argument("--moe-tokens", type=int, default=65536, help="tokens of the MoE row")
     args = ap.parse_args()
+    bad = [r for r in args.rows.split(",") if r not in ROW_NAMES]
+    if bad:
+        ap.error(f"unknown rows {bad}")
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -296,7 +296,10 @@ fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_scales, const
  * fp4q_device_status -- read (and, if reset != 0, clear) the device status
  * word of the current device: 0 when no device-side wait has timed out since
  * the last reset, else a bit mask of the kernels that gave up (FP4Q_ERR_TIMEOUT
- * is returned in that case).  Synchronous: waits for the device first.
+ * is returned in that case): bit 0 fp4q_block_scaled_gemm, bit 1
+ * fp4q_grouped_gemm, bit 2 the shared-memory-staged conversions of
+ * fp4q_mx_quantize (E4M3 source) and fp4q_fp4_to_fp8, bit 31
+ * fp4q_check_wait_timeout.  Synchronous: waits for the device first.
  */
 fp4q_status fp4q_device_status(uint32_t* status_out, int reset);
 

@@ -27,7 +27,12 @@ uint32_t* status_word();
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Status-word bits (which kernel gave up a bounded wait).
-enum : uint32_t { kStatusGemmTimeout = 1u << 0, kStatusGroupedTimeout = 1u << 1, kStatusSelfCheck = 1u << 31 };
+enum : uint32_t {
+    kStatusGemmTimeout = 1u << 0,
+    kStatusGroupedTimeout = 1u << 1,
+    kStatusStreamTimeout = 1u << 2,
+    kStatusSelfCheck = 1u << 31
+};
 
 // ---------------------------------------------------------------------------
 // Device side
@@ -63,6 +68,24 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
     asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;\n}"
         : "=h"(r) : "f"(hi), "f"(lo));
     return r & 0xffu;
+}
+
+// Packed FP32 pairs (Blackwell mul.rn.f32x2): two IEEE round-to-nearest-even
+// multiplies per instruction, identical results to the scalar ones.
+__device__ __forceinline__ uint64_t f32x2_splat(float s) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(s));
+    return r;
+}
+__device__ __forceinline__ void mul_f32x2(float& a, float& b, uint64_t s2) {
+    asm("{\n .reg .b64 x;\n mov.b64 x, {%0, %1};\n mul.rn.f32x2 x, x, %2;\n mov.b64 {%0, %1}, x;\n}"
+        : "+f"(a), "+f"(b) : "l"(s2));
+}
+// FP16 pair (one 32-bit word) -> two FP32, each times the scale pair s2.
+__device__ __forceinline__ void f16x2_mul_f32x2(uint32_t h, uint64_t s2, float& o0, float& o1) {
+    asm("{\n .reg .b16 lo, hi;\n .reg .f32 a, b;\n .reg .b64 x;\n mov.b32 {lo, hi}, %2;\n"
+        " cvt.f32.f16 a, lo;\n cvt.f32.f16 b, hi;\n mov.b64 x, {a, b};\n mul.rn.f32x2 x, x, %3;\n"
+        " mov.b64 {%0, %1}, x;\n}" : "=f"(o0), "=f"(o1) : "r"(h), "l"(s2));
 }
 
 // Eight FP32 -> one 32-bit word of eight E2M1 codes (element j in nibble j),
@@ -164,6 +187,23 @@ inline void row_launch_shape(int64_t bpr, int* tpb, int* nx) {
     *nx = int(n);
 }
 
+// Like row_launch_shape, but when `units` (threads of work per row) does not
+// fill whole warps, a CTA takes *rpc rows side by side (rpc * units threads, a
+// multiple of 32, at most 512) so that no lane idles.
+inline void packed_row_shape(int64_t units, int* tpb, int* nx, int* rpc) {
+    int64_t g = 32;
+    while (units % g) g >>= 1;
+    const int64_t r = 32 / g;
+    if (r > 1 && r * units <= 512) {
+        *tpb = int(r * units);
+        *nx = 1;
+        *rpc = int(r);
+    } else {
+        row_launch_shape(units, tpb, nx);
+        *rpc = 1;
+    }
+}
+
 // CTAs along the rows for a row-wise kernel: one full wave of resident CTAs
 // (`per_sm` per SM), each then looping over its share of rows.
 inline unsigned row_grid_y(int64_t rows, int nx, int sms, int per_sm = 8) {
@@ -172,6 +212,26 @@ inline unsigned row_grid_y(int64_t rows, int nx, int sms, int per_sm = 8) {
     int64_t gy = rows < want ? rows : want;
     if (gy > 65535) gy = 65535;
     return unsigned(gy > 0 ? gy : 1);
+}
+
+// Resident CTAs per SM of `kernel` at `threads` per CTA and `smem` bytes of
+// dynamic shared memory (raising the kernel's dynamic shared memory limit when
+// needed), remembered per kernel, device and size.
+template <typename Kernel>
+inline int resident_per_sm_smem(Kernel kernel, int threads, uint32_t smem) {
+    struct Entry { int dev; int threads; uint32_t smem; int n; };
+    static Entry cache[16] = {};
+    static int next = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    for (const Entry& e : cache)
+        if (e.n && e.dev == dev && e.threads == threads && e.smem == smem) return e.n;
+    if (smem > 48 * 1024) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
+    cache[next] = Entry{dev, threads, smem, n};
+    next = (next + 1) % 16;
+    return n;
 }
 
 // Resident CTAs per SM of `kernel` at `threads` per CTA (no dynamic shared

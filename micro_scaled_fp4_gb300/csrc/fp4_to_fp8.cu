@@ -13,7 +13,10 @@
 // the block's 8 possible magnitudes are one 64-bit row of a small table
 // indexed by -d (rows for -d >= 12 are all zero); eight output bytes then
 // cost two byte-permute lookups plus the sign-bit spread.
+#include <algorithm>
+
 #include "common.cuh"
+#include "ring.cuh"
 
 namespace fp4q {
 namespace {
@@ -68,9 +71,10 @@ __device__ __forceinline__ void convert_block(const uint4& cw, uint32_t sw, uint
     if ((b & 3) == 0) *ts = exp2i(int(emax) - 127);
 }
 
-__global__ void __launch_bounds__(256) fp4_to_fp8_kernel(
+// A CTA covers rpc rows side by side (blockDim.x / rpc threads per row).
+__global__ void __launch_bounds__(512) fp4_to_fp8_kernel(
     const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, uint32_t bpr,
-    uint8_t* __restrict__ y, float* __restrict__ tile_scale) {
+    uint8_t* __restrict__ y, float* __restrict__ tile_scale, int rpc) {
     __shared__ uint2 lut[kShiftRows];
     if (threadIdx.x < kShiftRows) {
         uint32_t lo = 0, hi = 0;
@@ -82,11 +86,12 @@ __global__ void __launch_bounds__(256) fp4_to_fp8_kernel(
     }
     __syncthreads();
     // two adjacent blocks (2u, 2u + 1) of one 1x128 tile per thread
-    const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t upc = blockDim.x / uint32_t(rpc);
+    const uint32_t u = blockIdx.x * upc + threadIdx.x % upc;
     if (u >= (bpr >> 1)) return;
     const uint32_t b = 2 * u;
-    const int64_t step = gridDim.y;
-    for (int64_t r = blockIdx.y; r < rows; r += 2 * step) {
+    const int64_t step = int64_t(gridDim.y) * rpc;
+    for (int64_t r = int64_t(blockIdx.y) * rpc + threadIdx.x / upc; r < rows; r += 2 * step) {
         // two rows in flight: both rows' codes and tile exponents are loaded first
         const int64_t r2 = r + step;
         const bool two = r2 < rows;
@@ -113,6 +118,78 @@ __global__ void __launch_bounds__(256) fp4_to_fp8_kernel(
     }
 }
 
+__device__ __forceinline__ void lut_setup(uint2* lut) {
+    for (uint32_t t = threadIdx.x; t < kShiftRows; t += blockDim.x) {
+        uint32_t lo = 0, hi = 0;
+        for (uint32_t c = 0; c < 4; ++c) {
+            lo |= shifted_magnitude(c, int(t)) << (8 * c);
+            hi |= shifted_magnitude(c + 4, int(t)) << (8 * c);
+        }
+        lut[t] = make_uint2(lo, hi);
+    }
+}
+
+// Shared-memory-staged form (ring.cuh): each group of `rps` rows arrives as one
+// bulk copy of its codes and one of its E8M0 bytes.  A consumer thread converts
+// a pair of blocks (32 bytes of codes) per step, reading its two 16-byte blocks
+// in the order k ^ ((lane >> 2) & 1), which puts any 8 consecutive lanes on 8
+// different 16-byte bank groups.
+__global__ void __launch_bounds__(ring::kMaxThreads) fp4_to_fp8_staged_kernel(
+    const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, uint32_t cols,
+    uint8_t* __restrict__ y, float* __restrict__ tile_scale, uint32_t rps, uint32_t* status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint2 lut[kShiftRows];
+    lut_setup(lut);                                      // make_ring's barrier publishes it
+    const uint32_t code_bytes = cols / 2, scale_bytes = cols / 32;
+    const ring::Ring rg = ring::make_ring(smem, rps * (code_bytes + scale_bytes));
+    const int64_t ngroups = (rows + rps - 1) / rps;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bpr = cols / 32, ppr = cols / 64;
+    if (warp == 0) {
+        if (lane == 0)
+            ring::produce(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, uint32_t fb, int64_t g) {
+                const int64_t r0 = g * rps;
+                const uint32_t nr = uint32_t(min(int64_t(rps), rows - r0));
+                tc::mbar_arrive_expect_tx(fb, nr * (code_bytes + scale_bytes));
+                tc::bulk_load(tc::smem_u32(st), q + r0 * int64_t(code_bytes), nr * code_bytes, fb);
+                tc::bulk_load(tc::smem_u32(st + rps * code_bytes), s + r0 * int64_t(scale_bytes), nr * scale_bytes,
+                              fb);
+            });
+        return;
+    }
+    const uint32_t ct = threadIdx.x - 32;
+    const uint32_t stride = blockDim.x - 32;
+    const uint32_t rr0 = ct / ppr, u0 = ct % ppr, dr = stride / ppr, du = stride % ppr;
+    const uint32_t sw = (uint32_t(lane) >> 2) & 1u;
+    ring::consume(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, int64_t g) {
+        const int64_t r0 = g * rps;
+        const uint32_t nr = uint32_t(min(int64_t(rps), rows - r0));
+        const uint32_t units = nr * ppr;
+        const uint32_t cbase = tc::smem_u32(st), sbase = cbase + rps * code_bytes;
+        uint32_t rr = rr0, u = u0;
+        for (uint32_t un = ct; un < units; un += stride) {
+            uint4 c[2];
+#pragma unroll
+            for (uint32_t k = 0; k < 2; ++k)
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(c[k].x), "=r"(c[k].y), "=r"(c[k].z), "=r"(c[k].w)
+                             : "r"(cbase + 32 * un + 16 * (k ^ sw)));
+            uint32_t swd;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(swd) : "r"(sbase + rr * scale_bytes + 4 * (u >> 1)));
+            const int64_t r = r0 + rr;
+            float* ts = tile_scale + r * int64_t(bpr / 4) + (u >> 1);
+#pragma unroll
+            for (uint32_t k = 0; k < 2; ++k) {
+                const uint32_t b = 2 * u + (k ^ sw);
+                convert_block(c[k], swd, b, lut, y + (r * int64_t(bpr) + b) * 32, ts);
+            }
+            u += du;
+            rr += dr;
+            if (u >= ppr) { u -= ppr; ++rr; }
+        }
+    });
+}
+
 }  // namespace
 }  // namespace fp4q
 
@@ -133,9 +210,23 @@ extern "C" fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, 
     fp4q_status st = current_device(&sms);
     if (st != FP4Q_OK) return st;
     const uint32_t bpr = uint32_t(cols / 32);
-    int tpb, nx;
-    row_launch_shape(bpr / 2, &tpb, &nx);
-    dim3 grid(unsigned(nx), row_grid_y(rows, nx, sms, resident_per_sm(fp4_to_fp8_kernel, tpb)), 1);
-    fp4_to_fp8_kernel<<<grid, tpb, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, scales, rows, bpr, y, tile_scale);
+    const uint32_t row_bytes = uint32_t(cols / 2 + cols / 32);
+    const ring::Shape sh = cols % 512 == 0 && aligned16(scales) && cols <= (1 << 20)
+                               ? ring::ring_shape(uint32_t(cols / 64), row_bytes) : ring::Shape{0, 0};
+    if (sh.rps) {
+        const uint32_t smem = ring::smem_bytes(sh.rps * row_bytes);
+        const int threads = 32 * int(1 + sh.warps);
+        const int per_sm = resident_per_sm_smem(fp4_to_fp8_staged_kernel, threads, smem);
+        const int64_t ngroups = (rows + sh.rps - 1) / sh.rps;
+        const int64_t grid = std::min<int64_t>(ngroups, int64_t(per_sm) * sms);
+        fp4_to_fp8_staged_kernel<<<unsigned(grid), threads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
+            q, scales, rows, uint32_t(cols), y, tile_scale, sh.rps, status_word());
+        return check_launch("fp4_to_fp8");
+    }
+    int tpb, nx, rpc;
+    packed_row_shape(bpr / 2, &tpb, &nx, &rpc);
+    dim3 grid(unsigned(nx), row_grid_y((rows + rpc - 1) / rpc, nx, sms, resident_per_sm(fp4_to_fp8_kernel, tpb)), 1);
+    fp4_to_fp8_kernel<<<grid, tpb, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, scales, rows, bpr, y, tile_scale,
+                                                                                rpc);
     return check_launch("fp4_to_fp8");
 }

@@ -14,20 +14,23 @@
 // per step, K consumed 256 elements (128 bytes) per pipeline stage:
 //   warp 0      TMA producer: A and B tiles (128-byte swizzle; B as two
 //               128-row halves) and the stage's block scales (contiguous
-//               chunks of the MMA scale layout) into a 4-stage ring.
+//               chunks of the MMA scale layout) into a 3-stage ring.
 //   warp 1      allocates TMEM; one thread issues tcgen05.cp (scales ->
 //               TMEM) and tcgen05.mma kind::mxf4 (UE8M0 per 32) or
 //               kind::mxf4nvf4 (UE4M3 per 16), FP32 accumulator in TMEM.
-//   warps 2..5  epilogue: tcgen05.ld of the 128 x 256 FP32 accumulator,
-//               one row per thread; the accumulator goes back to the MMA
-//               thread as soon as it has been read.  STORE: scale, BF16
+//   warps 2..9  epilogue: tcgen05.ld of the 128 x 256 FP32 accumulator,
+//               one row and half the columns per thread (two warps per TMEM
+//               lane quadrant); the accumulator goes back to the MMA thread
+//               as soon as it has been read.  STORE: scale, BF16
 //               (round to nearest even) or FP32 stores.  SILU_GATE: the two
 //               B halves are the gate and up rows of the same 128 outputs;
 //               h = SiLU(gate) * up in FP32, then MXFP4 (one 32-element
 //               block per 32 accumulator columns) straight from registers.
 // Every mbarrier wait is bounded in time; a wait that gives up sets a bit in
-// the library's status word, tells the other roles to stop, and the kernel
-// drains its own asynchronous work and frees TMEM before returning.
+// the library's status word and tells the other roles to stop.  The drain
+// waits that follow (TMA loads issued, MMAs issued) do not stop on that flag,
+// only on their own time limit, so the CTA frees TMEM and exits with no
+// asynchronous work of its own in flight.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
@@ -252,7 +255,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         // drain: every stage issued last must have landed before the CTA exits
         for (int i = 0; i < STAGES && i < issued; ++i) {
             if (--stage < 0) { stage = STAGES - 1; phase ^= 1; }
-            if (!tc::mbar_wait(full_bar(stage), phase, abort, kWaitLimitNs)) {
+            if (!tc::mbar_wait_drain(full_bar(stage), phase, kWaitLimitNs)) {
                 flag_abort(abort, args.status, args.status_bit);
                 break;
             }
@@ -352,7 +355,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         // no tile issued none)
         if (tcount > 0 || !ok) {
             tc::tc_commit(drain_bar);
-            if (!tc::mbar_wait(drain_bar, 0, abort, kWaitLimitNs)) flag_abort(abort, args.status, args.status_bit);
+            if (!tc::mbar_wait_drain(drain_bar, 0, kWaitLimitNs)) flag_abort(abort, args.status, args.status_bit);
         }
     } else if (warp >= 2) {
         // ---------------- epilogue ----------------
@@ -365,7 +368,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         const float dense_alpha = (!args.groups && args.nv) ? __fmul_rn(*args.ts_a, *args.ts_b) : 1.0f;
         int tcount = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
-            if (!tc::mbar_wait(tmem_full, tcount & 1, abort, kWaitLimitNs)) {
+            // The eight warps decide together whether the tile goes ahead: a warp
+            // that gave up while another saw the accumulator arrive would leave
+            // that one alone at the staging barriers below.
+            const bool got = tc::mbar_wait(tmem_full, tcount & 1, abort, kWaitLimitNs);
+            if (!tc::named_bar_and(1, 256, got)) {
                 flag_abort(abort, args.status, args.status_bit);
                 break;
             }

@@ -14,12 +14,21 @@
 // (a warp writes 32 contiguous bytes in row-major layout).  The rounding is
 // the hardware cvt.rn.satfinite.e2m1x2.f32, after an exact power-of-two
 // multiply by 2^-E.
+#include <algorithm>
+
 #include "common.cuh"
+#include "ring.cuh"
 
 namespace fp4q {
 namespace {
 
 enum Src { kBF16 = 0, kFP32 = 1, kE4M3 = 2 };
+
+#ifndef FP4Q_E4M3_STAGED
+#define FP4Q_E4M3_STAGED 0
+#endif
+// E4M3 -> MXFP4 through the shared-memory ring (1) or the register path (0).
+constexpr bool kE4M3Staged = FP4Q_E4M3_STAGED != 0;
 
 // One 32-element block as loaded from memory.
 template <int SRC> struct RawBlock;
@@ -58,14 +67,15 @@ __device__ __forceinline__ void quantize_block(const RawBlock<SRC>& raw, uint4& 
         for (int i = 0; i < 16; ++i) m = __vmaxu2(m, v[i] & 0x7fff7fffu);
         const int e = mx_exponent_from_amax_bits(max(m & 0xffffu, m >> 16) << 16);
         sbyte = uint32_t(e + 127);
-        const float inv = exp2i(-e);    // exact power of two: x * inv is exact or below E2M1's range
+        const uint64_t inv2 = f32x2_splat(exp2i(-e));   // exact power of two: x * inv is exact or below E2M1's range
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             float f[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                f[2 * j] = __fmul_rn(u2f(v[4 * k + j] << 16), inv);
-                f[2 * j + 1] = __fmul_rn(u2f(v[4 * k + j] & 0xffff0000u), inv);
+                f[2 * j] = u2f(v[4 * k + j] << 16);
+                f[2 * j + 1] = u2f(v[4 * k + j] & 0xffff0000u);
+                mul_f32x2(f[2 * j], f[2 * j + 1], inv2);
             }
             w[k] = cvt_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
         }
@@ -77,13 +87,15 @@ __device__ __forceinline__ void quantize_block(const RawBlock<SRC>& raw, uint4& 
             for (int j = 0; j < 8; ++j) m = max(m, raw.a[i].v[j] & 0x7fffffffu);
         const int e = mx_exponent_from_amax_bits(m);
         sbyte = uint32_t(e + 127);
-        const float inv = exp2i(-e);
+        const uint64_t inv2 = f32x2_splat(exp2i(-e));
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const u32x8& a = raw.a[k];
-            w[k] = cvt_e2m1x8(__fmul_rn(u2f(a.v[0]), inv), __fmul_rn(u2f(a.v[1]), inv), __fmul_rn(u2f(a.v[2]), inv),
-                              __fmul_rn(u2f(a.v[3]), inv), __fmul_rn(u2f(a.v[4]), inv), __fmul_rn(u2f(a.v[5]), inv),
-                              __fmul_rn(u2f(a.v[6]), inv), __fmul_rn(u2f(a.v[7]), inv));
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = u2f(raw.a[k].v[j]);
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) mul_f32x2(f[j], f[j + 1], inv2);
+            w[k] = cvt_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
         }
     } else {
         const float ts = raw.ts;
@@ -98,11 +110,17 @@ __device__ __forceinline__ void quantize_block(const RawBlock<SRC>& raw, uint4& 
                 " cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
                 : "=r"(h[2 * i]), "=r"(h[2 * i + 1]) : "r"(raw.a.v[i]));
         }
-        uint32_t hm;
-        asm("abs.f16x2 %0, %1;" : "=r"(hm) : "r"(h[0]));
+        // max of magnitudes, two chains (max.xorsign.abs: |result| = max(|a|, |b|))
+        uint32_t m0, m1, hm;
+        asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(m0) : "r"(h[0]), "r"(h[1]));
+        asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(m1) : "r"(h[2]), "r"(h[3]));
 #pragma unroll
-        for (int i = 1; i < 16; ++i)
-            asm("{\n .reg .b32 t;\n abs.f16x2 t, %1;\n max.f16x2 %0, %0, t;\n}" : "+r"(hm) : "r"(h[i]));
+        for (int i = 4; i < 16; i += 2) {
+            asm("max.xorsign.abs.f16x2 %0, %0, %1;" : "+r"(m0) : "r"(h[i]));
+            asm("max.xorsign.abs.f16x2 %0, %0, %1;" : "+r"(m1) : "r"(h[i + 1]));
+        }
+        asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(hm) : "r"(m0), "r"(m1));
+        asm("abs.f16x2 %0, %0;" : "+r"(hm));
         float mlo, mhi;
         asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.f32.f16 %0, lo;\n cvt.f32.f16 %1, hi;\n}"
             : "=f"(mlo), "=f"(mhi) : "r"(hm));
@@ -116,15 +134,13 @@ __device__ __forceinline__ void quantize_block(const RawBlock<SRC>& raw, uint4& 
             // is normal, and both lie below E2M1's smallest step otherwise:
             // one multiply by the exact ts * 2^-E gives the same codes.
             const float sc = amax == 0.0f ? copysignf(1.0f, ts) : __fmul_rn(ts, inv);
+            const uint64_t sc2 = f32x2_splat(sc);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 float f[8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.f32.f16 %0, lo;\n cvt.f32.f16 %1, hi;\n}"
-                        : "=f"(f[2 * j]), "=f"(f[2 * j + 1]) : "r"(h[4 * k + j]));
-                w[k] = cvt_e2m1x8(__fmul_rn(f[0], sc), __fmul_rn(f[1], sc), __fmul_rn(f[2], sc), __fmul_rn(f[3], sc),
-                                  __fmul_rn(f[4], sc), __fmul_rn(f[5], sc), __fmul_rn(f[6], sc), __fmul_rn(f[7], sc));
+                for (int j = 0; j < 4; ++j) f16x2_mul_f32x2(h[4 * k + j], sc2, f[2 * j], f[2 * j + 1]);
+                w[k] = cvt_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
             }
         } else {
             // tiny tile scale: products may be subnormal; round them first
@@ -181,12 +197,14 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(
 // one tile-scale load, one index computation and 64 bytes of loads per row.
 struct RawPair { u32x8 a, b; float ts; };
 
-__global__ void __launch_bounds__(256) mx_quantize_e4m3x2_kernel(
+// A CTA covers rpc rows side by side (blockDim.x / rpc threads per row).
+__global__ void __launch_bounds__(512, 1) mx_quantize_e4m3x2_kernel(
     const uint8_t* __restrict__ x, const float* __restrict__ tile_scale, int64_t rows,
-    uint32_t bpr, int64_t ld_x, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout) {
-    const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;      // pair index in the row
+    uint32_t bpr, int64_t ld_x, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout, int rpc) {
+    const uint32_t upc = blockDim.x / uint32_t(rpc);
+    const uint32_t u = blockIdx.x * upc + threadIdx.x % upc;      // pair index in the row
     if (u >= (bpr >> 1)) return;
-    const int64_t step = gridDim.y;
+    const int64_t step = int64_t(gridDim.y) * rpc;
     auto load = [&](int64_t r, RawPair& p) {
         const uint8_t* src = x + r * ld_x + uint64_t(u) * 64;
         p.a = ldg256(src);
@@ -209,7 +227,7 @@ __global__ void __launch_bounds__(256) mx_quantize_e4m3x2_kernel(
         const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(r), b0, bpr) : uint64_t(r) * bpr + b0;
         *reinterpret_cast<uint16_t*>(s + so) = uint16_t(s0 | (s1 << 8));   // blocks 2u, 2u+1 are adjacent bytes
     };
-    for (int64_t r = blockIdx.y; r < rows; r += 2 * step) {
+    for (int64_t r = int64_t(blockIdx.y) * rpc + threadIdx.x / upc; r < rows; r += 2 * step) {
         const int64_t r2 = r + step;
         RawPair A, B;
         load(r, A);
@@ -217,6 +235,95 @@ __global__ void __launch_bounds__(256) mx_quantize_e4m3x2_kernel(
         process(r, A);
         if (r2 < rows) process(r2, B);
     }
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+// E4M3 source staged through shared memory (ring.cuh): each group of `rps` rows
+// arrives as one bulk copy of the codes (one per row when ld_x > cols) and one
+// of the rows' tile scales.  A consumer thread converts a pair of adjacent
+// blocks (64 codes, one 1x128 tile half) per step.  Its four 16-byte chunks
+// are read in the order k ^ ((lane >> 1) & 3): over any 8 consecutive lanes the
+// 16-byte bank groups are then all different (the plain order would put four
+// lanes on each group).  Chunk order does not matter to the block amax, and the
+// codes of chunk c go to bytes 8c .. 8c + 7 of the pair's output.
+__global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_e4m3_staged_kernel(
+    const uint8_t* __restrict__ x, const float* __restrict__ tile_scale, int64_t rows, uint32_t cols,
+    int64_t ld_x, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout, uint32_t rps,
+    uint32_t* status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t tile_bytes = cols / 32;                     // cols / 128 FP32 tile scales
+    const ring::Ring rg = ring::make_ring(smem, rps * (cols + tile_bytes));
+    const int64_t ngroups = (rows + rps - 1) / rps;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bpr = cols / 32, ppr = cols / 64;
+    if (warp == 0) {
+        if (lane == 0)
+            ring::produce(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, uint32_t fb, int64_t g) {
+                const int64_t r0 = g * rps;
+                const uint32_t nr = uint32_t(min(int64_t(rps), rows - r0));
+                tc::mbar_arrive_expect_tx(fb, nr * (cols + tile_bytes));
+                if (ld_x == int64_t(cols)) {
+                    tc::bulk_load(tc::smem_u32(st), x + r0 * int64_t(cols), nr * cols, fb);
+                } else {
+                    for (uint32_t i = 0; i < nr; ++i)
+                        tc::bulk_load(tc::smem_u32(st + i * cols), x + (r0 + i) * ld_x, cols, fb);
+                }
+                tc::bulk_load(tc::smem_u32(st + rps * cols), tile_scale + r0 * (cols / 128), nr * tile_bytes, fb);
+            });
+        return;
+    }
+    const uint32_t ct = threadIdx.x - 32;                      // consumer thread
+    const uint32_t stride = blockDim.x - 32;
+    const uint32_t rr0 = ct / ppr, u0 = ct % ppr, dr = stride / ppr, du = stride % ppr;
+    const uint32_t sw = (uint32_t(lane) >> 1) & 3u;
+    ring::consume(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, int64_t g) {
+        const int64_t r0 = g * rps;
+        const uint32_t nr = uint32_t(min(int64_t(rps), rows - r0));
+        const uint32_t units = nr * ppr;
+        const uint32_t sbase = tc::smem_u32(st), tbase = sbase + rps * cols;
+        uint32_t rr = rr0, u = u0;
+        for (uint32_t un = ct; un < units; un += stride) {
+            const uint32_t a = sbase + 64 * un;
+            const uint4 c0 = lds128(a + 16 * (0 ^ sw)), c1 = lds128(a + 16 * (1 ^ sw));
+            const uint4 c2 = lds128(a + 16 * (2 ^ sw)), c3 = lds128(a + 16 * (3 ^ sw));
+            RawBlock<kE4M3> A, B;
+            A.ts = B.ts = u2f(lds32(tbase + 4 * (rr * (cols / 128) + (u >> 1))));
+            A.a = u32x8{{c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w}};
+            B.a = u32x8{{c2.x, c2.y, c2.z, c2.w, c3.x, c3.y, c3.z, c3.w}};
+            uint4 qa, qb;
+            uint32_t sa, sb;
+            quantize_block<kE4M3>(A, qa, sa);
+            quantize_block<kE4M3>(B, qb, sb);
+            const int64_t r = r0 + rr;
+            uint8_t* qp = q + r * int64_t(cols / 2) + 32 * u;
+            *reinterpret_cast<uint2*>(qp + 8 * (0 ^ sw)) = make_uint2(qa.x, qa.y);
+            *reinterpret_cast<uint2*>(qp + 8 * (1 ^ sw)) = make_uint2(qa.z, qa.w);
+            *reinterpret_cast<uint2*>(qp + 8 * (2 ^ sw)) = make_uint2(qb.x, qb.y);
+            *reinterpret_cast<uint2*>(qp + 8 * (3 ^ sw)) = make_uint2(qb.z, qb.w);
+            // block A holds chunks of block (sw >> 1) of the pair, block B the other one
+            const uint32_t ba = 2 * u + (sw >> 1), bb = 2 * u + 1 - (sw >> 1);
+            if (mma_layout) {
+                s[mma_scale_offset(uint64_t(r), ba, bpr)] = uint8_t(sa);
+                s[mma_scale_offset(uint64_t(r), bb, bpr)] = uint8_t(sb);
+            } else {
+                *reinterpret_cast<uint16_t*>(s + r * int64_t(bpr) + 2 * u) =
+                    uint16_t((sw >> 1) ? (sb | (sa << 8)) : (sa | (sb << 8)));
+            }
+            u += du;
+            rr += dr;
+            if (u >= ppr) { u -= ppr; ++rr; }
+        }
+    });
 }
 
 template <bool OUT_BF16>
@@ -314,10 +421,23 @@ extern "C" fp4q_status fp4q_mx_quantize(const void* x, fp4q_dtype x_type, const 
             break;
         }
         default: {
-            int tpb2, nx2;
-            row_launch_shape(bpr / 2, &tpb2, &nx2);
-            dim3 grid = grid_for_rows(mx_quantize_e4m3x2_kernel, tpb2, rows, nx2, sms);
-            mx_quantize_e4m3x2_kernel<<<grid, tpb2, 0, s>>>(xb, tile_scale, rows, bpr, ld_x, q, scales, mma);
+            const uint32_t row_bytes = uint32_t(cols) + uint32_t(cols / 32);
+            const ring::Shape sh = kE4M3Staged && cols % 512 == 0 && aligned16(tile_scale) && cols <= (1 << 20)
+                                       ? ring::ring_shape(uint32_t(cols / 64), row_bytes) : ring::Shape{0, 0};
+            if (sh.rps) {
+                const uint32_t smem = ring::smem_bytes(sh.rps * row_bytes);
+                const int threads = 32 * int(1 + sh.warps);
+                const int per_sm = resident_per_sm_smem(mx_quantize_e4m3_staged_kernel, threads, smem);
+                const int64_t ngroups = (rows + sh.rps - 1) / sh.rps;
+                const int64_t grid = std::min<int64_t>(ngroups, int64_t(per_sm) * sms);
+                mx_quantize_e4m3_staged_kernel<<<unsigned(grid), threads, smem, s>>>(
+                    xb, tile_scale, rows, uint32_t(cols), ld_x, q, scales, mma, sh.rps, status_word());
+                break;
+            }
+            int tpb2, nx2, rpc;
+            packed_row_shape(bpr / 2, &tpb2, &nx2, &rpc);
+            dim3 grid = grid_for_rows(mx_quantize_e4m3x2_kernel, tpb2, (rows + rpc - 1) / rpc, nx2, sms);
+            mx_quantize_e4m3x2_kernel<<<grid, tpb2, 0, s>>>(xb, tile_scale, rows, bpr, ld_x, q, scales, mma, rpc);
             break;
         }
     }

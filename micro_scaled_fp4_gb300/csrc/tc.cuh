@@ -34,6 +34,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
                  " selp.u32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps in hardware (up to `hint_ns`) instead of spinning, and wakes when the
+// phase completes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+                 " selp.u32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+constexpr uint32_t kSleepHintNs = 100000;             // 100 us per suspended try
+
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -45,12 +56,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                           uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
-            if (*abort) return false;
-            if (global_ns() - t0 > limit_ns) return false;
-        }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Drain wait: for asynchronous work this thread already issued (TMA loads that
+// will land, MMAs that will complete).  It ignores the abort flag, since the CTA
+// must not exit or free TMEM with that work in flight, and gives up only after
+// `limit_ns` (returns false).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -87,6 +109,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+// Named barrier with an AND reduction: every one of the `nthreads` threads
+// arrives with `pred` and all of them get the AND of the predicates.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t out;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+                 " selp.u32 %0, 1, 0, q;\n}" : "=r"(out) : "r"(uint32_t(pred)), "r"(id), "r"(nthreads) : "memory");
+    return out != 0;
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");

@@ -159,6 +159,34 @@ def test_fp8_to_mx_and_back(fq, oracle, shape):
     assert np.array_equal(host(yts).view(np.uint32), ytsr.view(np.uint32))
 
 
+@pytest.mark.parametrize("shape", [(37, 1024), (300, 7168), (3, 640), (3, 16384), (130, 2560)])
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("pad", [0, 512])
+def test_fp8_to_mx_layouts_strides_paths(fq, oracle, shape, layout, pad):
+    """E4M3 -> MXFP4 and back on every launch form: shapes whose rows go through
+    the shared-memory ring (cols % 512 == 0, a row that fits a stage) and shapes
+    that take the register path (cols 640; 16384-wide E4M3 rows), row-major and
+    MMA scale layouts, dense and padded rows (ld_x = cols + pad)."""
+    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
+    R, C = shape
+    e4, ts = W.fp8_activation(R, C, seed=R + pad, outlier_seed=C + layout)
+    big = np.zeros((R, C + pad), dtype=np.uint8)
+    big[:, :C] = e4
+    xd = dev(big)[:, :C].view(torch.float8_e4m3fn)
+    q, s = fq.mx_quantize(xd, tile_scale=dev(ts), layout=layout)
+    qr, sr = oracle.fp8_to_mx(e4, ts)
+    assert np.array_equal(host(q), qr)
+    got = host(s).reshape(-1)
+    if layout:
+        got = from_mma_layout(got, R, C // 32)
+    assert np.array_equal(got.reshape(R, C // 32), sr)
+    y, yts = fq.fp4_to_fp8(dev(qr), dev(sr))
+    yr, ytsr = oracle.mx_to_fp8(qr, sr)
+    assert np.array_equal(host(y), yr)
+    assert np.array_equal(host(yts).view(np.uint32), ytsr.view(np.uint32))
+
+
 def test_fp4_to_fp8_every_shift(fq, oracle):
     """Random codes under block exponents spread over the whole E8M0 range, so
     every shift d in [-254, 0] and every code meets the kernel's remap."""
