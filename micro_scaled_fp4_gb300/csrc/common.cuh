@@ -189,12 +189,12 @@ inline void row_launch_shape(int64_t bpr, int* tpb, int* nx) {
 
 // Like row_launch_shape, but when `units` (threads of work per row) does not
 // fill whole warps, a CTA takes *rpc rows side by side (rpc * units threads, a
-// multiple of 32, at most 512) so that no lane idles.
-inline void packed_row_shape(int64_t units, int* tpb, int* nx, int* rpc) {
+// multiple of 32, at most max_threads) so that no lane idles.
+inline void packed_row_shape(int64_t units, int* tpb, int* nx, int* rpc, int64_t max_threads = 512) {
     int64_t g = 32;
     while (units % g) g >>= 1;
     const int64_t r = 32 / g;
-    if (r > 1 && r * units <= 512) {
+    if (r > 1 && r * units <= max_threads) {
         *tpb = int(r * units);
         *nx = 1;
         *rpc = int(r);

@@ -81,36 +81,68 @@ __global__ void __launch_bounds__(256) nv_amax_kernel(const uint8_t* __restrict_
 // Stochastic rounding of v onto E2M1 with the 32-bit word r: up iff
 // r < frac * 2^32, frac the exact position of |v| between its two grid
 // neighbours; |v| >= 6 saturates; the sign is kept.  Returns the 4-bit code.
-// Integer form on the FP32 bits u of |v|: for |v| in [2^k, 2^(k+1)), k >= 0,
-// the grid points are 2^k and 1.5 * 2^k (step 2^(k-1)), the code below |v| is
-// 2(k + 1) + (mantissa bit 22) and frac * 2^32 = (mantissa bits 0..21) << 10;
-// in [0.5, 1) the step is 0.5 from 0.5 (code 1), frac * 2^32 = mantissa << 9;
-// below 0.5 the step is 0.5 from 0 and frac * 2^32 = |v| * 2^33 (exact),
-// whose ceiling decides the strict comparison.
+// Integer form on the FP32 bits u of |v|, without branches: for |v| in
+// [2^k, 2^(k+1)), k >= 0, the grid points are 2^k and 1.5 * 2^k (step
+// 2^(k-1)), the code below |v| is 2(k + 1) + (mantissa bit 22) and
+// frac * 2^32 = u << 10 (the mantissa bits below bit 22); in [0.5, 1) the step
+// is 0.5 from 0.5 (code 1), frac * 2^32 = u << 9; below 0.5 the step is 0.5
+// from 0 and frac * 2^32 = |v| * 2^33 (exact), whose ceiling decides the
+// strict comparison.
 __device__ __forceinline__ uint32_t sr_e2m1_code(float v, uint32_t r) {
     const uint32_t bits = f2u(v);
     const uint32_t u = bits & 0x7fffffffu;
     const uint32_t sign = (bits >> 28) & 8u;
-    uint32_t code, thr;
-    if (u >= 0x40c00000u) {                       // |v| >= 6
-        return sign | 7u;
-    } else if (u >= 0x3f800000u) {                // [1, 6)
-        code = (((u >> 23) - 126u) << 1) | ((u >> 22) & 1u);
-        thr = (u & 0x3fffffu) << 10;
-    } else if (u >= 0x3f000000u) {                // [0.5, 1)
-        code = 1u;
-        thr = (u & 0x7fffffu) << 9;
-    } else {                                      // [0, 0.5)
-        code = 0u;
-        thr = __float2uint_ru(__fmul_rn(u2f(u), 8589934592.0f));   // |v| * 2^33 < 2^32
+    const bool ge1 = u >= 0x3f800000u;
+    const uint32_t code_hi = ge1 ? ((((u >> 23) - 126u) << 1) | ((u >> 22) & 1u)) : 1u;
+    const uint32_t thr_hi = ge1 ? (u << 10) : (u << 9);
+    const uint32_t thr_lo = __float2uint_ru(__fmul_rn(u2f(u), 8589934592.0f));   // |v| * 2^33, < 2^32 below 0.5
+    const bool lt_half = u < 0x3f000000u;
+    const uint32_t code = lt_half ? 0u : code_hi;
+    const uint32_t thr = lt_half ? thr_lo : thr_hi;
+    const uint32_t q = u >= 0x40c00000u ? 7u : code + (r < thr ? 1u : 0u);
+    return sign | q;
+}
+
+// The ten round keys of Philox4x32-10 for one seed (key schedule (k0, k1) +=
+// (0x9E3779B9, 0xBB67AE85) per round), computed on the host and passed as a
+// kernel parameter, so that the rounds read them as constants.
+struct PhiloxKeys {
+    uint32_t k0[10], k1[10];
+};
+
+inline PhiloxKeys philox_keys(uint64_t seed) {
+    PhiloxKeys k;
+    uint32_t a = uint32_t(seed), b = uint32_t(seed >> 32);
+    for (int i = 0; i < 10; ++i) {
+        k.k0[i] = a;
+        k.k1[i] = b;
+        a += 0x9E3779B9u;
+        b += 0xBB67AE85u;
     }
-    return sign | (code + (r < thr ? 1u : 0u));
+    return k;
+}
+
+// Philox4x32-10 of the counter (c0, c1, 0, 0) under the keys K: each round is
+// two 32 x 32 -> 64-bit products and two three-way XORs.
+__device__ __forceinline__ uint4 philox_ctr64(uint32_t c0, uint32_t c1, const PhiloxKeys& K) {
+    uint32_t x = c0, y = c1, z = 0, w = 0;
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+        const uint64_t p0 = uint64_t(0xD2511F53u) * x, p1 = uint64_t(0xCD9E8D57u) * z;
+        const uint32_t nx = uint32_t(p1 >> 32) ^ y ^ K.k0[i];
+        const uint32_t nz = uint32_t(p0 >> 32) ^ w ^ K.k1[i];
+        y = uint32_t(p1);
+        w = uint32_t(p0);
+        x = nx;
+        z = nz;
+    }
+    return make_uint4(x, y, z, w);
 }
 
 template <bool SR>
 __global__ void __launch_bounds__(256) nv_quant_kernel(
     const uint8_t* __restrict__ x, int64_t rows, uint32_t tpr, int64_t ld_x_bytes, int rht,
-    uint64_t rht_seed, uint64_t sr_seed, const float* __restrict__ amax_ptr, float* __restrict__ amax_out,
+    uint64_t rht_seed, const PhiloxKeys sr_keys, const float* __restrict__ amax_ptr, float* __restrict__ amax_out,
     float* __restrict__ st_out, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout) {
     const uint32_t signs = rht ? rht_signs(rht_seed) : 0u;
     const float amax = *amax_ptr;
@@ -155,14 +187,13 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(
                                       __fmul_rn(t[8 * k + 6], rcp), __fmul_rn(t[8 * k + 7], rcp));
         } else {
             const uint64_t i0 = uint64_t(r) * cols + uint64_t(b) * 16;   // linear index, % 16 == 0
-            const uint32_t k0 = uint32_t(sr_seed), k1 = uint32_t(sr_seed >> 32);
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 uint32_t w = 0;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint64_t ctr = (i0 >> 2) + uint64_t(2 * k + h);
-                    const uint4 rnd = philox4x32_10(make_uint4(uint32_t(ctr), uint32_t(ctr >> 32), 0, 0), k0, k1);
+                    const uint4 rnd = philox_ctr64(uint32_t(ctr), uint32_t(ctr >> 32), sr_keys);
                     const int base = 8 * k + 4 * h;
                     const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
 #pragma unroll
@@ -233,15 +264,16 @@ extern "C" fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t col
     }
     if (rows == 0 || cols == 0) {
         // still publish s_t (and amax) for an empty tensor: both are 0
-        nv_quant_kernel<false><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, 0, amax_ptr, amax_out, tensor_scale_out, q, scales, 0);
+        nv_quant_kernel<false><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, philox_keys(0), amax_ptr, amax_out, tensor_scale_out,
+                                                 q, scales, 0);
         return check_launch("nv_quantize");
     }
     const int mma = layout == FP4Q_SCALES_MMA;
     if (rounding == FP4Q_SR)
-        nv_quant_kernel<true><<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, sr_seed, amax_ptr,
+        nv_quant_kernel<true><<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, philox_keys(sr_seed), amax_ptr,
                                                    amax_out, tensor_scale_out, q, scales, mma);
     else
-        nv_quant_kernel<false><<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, sr_seed, amax_ptr,
+        nv_quant_kernel<false><<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, philox_keys(sr_seed), amax_ptr,
                                                     amax_out, tensor_scale_out, q, scales, mma);
     return check_launch("nv_quantize");
 }
