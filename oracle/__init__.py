@@ -79,6 +79,8 @@ def _L():
                 "or_mx_dequantize_f64": [vp, vp, i64, i64, vp],
                 "or_fp8_to_mx": [vp, vp, i64, i64, i64, vp, vp],
                 "or_mx_to_fp8": [vp, vp, i64, i64, vp, vp],
+                "or_mx_to_fp8_col": [vp, vp, i64, i64, vp, vp],
+                "or_nv_quantize_2d": [vp, i64, i64, i64, ctypes.c_int, u64, vp, vp, vp, vp, vp],
                 "or_philox4x32_10": [vp, vp, vp],
                 "or_rht16_signs": [u64, vp],
                 "or_rht16": [vp, vp, vp],
@@ -268,16 +270,45 @@ def mx_to_fp8(q: np.ndarray, s: np.ndarray):
     return y, ts
 
 
+def mx_to_fp8_col(q: np.ndarray, s: np.ndarray):
+    """FP4RowToFP8Col: row-wise MXFP4 [R, C] -> (E4M3 of the transpose [C, R],
+    FP32 scale per 1x128 tile along R [C, R/128])."""
+    q = np.ascontiguousarray(q)
+    s = np.ascontiguousarray(s)
+    R, C2 = q.shape
+    C = 2 * C2
+    assert R % 128 == 0 and C % 32 == 0
+    y = np.empty((C, R), dtype=np.uint8)
+    ts = np.empty((C, R // 128), dtype=np.float32)
+    _L().or_mx_to_fp8_col(_p(q), _p(s), R, C, _p(y), _p(ts))
+    return y, ts
+
+
+def mx_quantize_col(x: np.ndarray):
+    """Column-wise MXFP4 (blocks of 32 along axis 0): by definition the
+    row-wise quantization of the transpose, returned in the transposed layout
+    (q [C, R/2], s [C, R/32])."""
+    return mx_quantize(np.ascontiguousarray(np.asarray(x).T))
+
+
 # ---------------------------------------------------------------------------
 # NVFP4
 # ---------------------------------------------------------------------------
-def nv_amax(x_bf16: np.ndarray, rht: bool, rht_seed: int) -> float:
+def _rht_mode(rht) -> int:
+    """False/0: no rotation; True/1: random-sign RHT from the seed; 2: the
+    deterministic H16 (no sign flips)."""
+    m = int(rht)
+    assert m in (0, 1, 2)
+    return m
+
+
+def nv_amax(x_bf16: np.ndarray, rht, rht_seed: int) -> float:
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     R, C = x.shape
-    return float(_L().or_nv_amax(_p(x), R, C, C, int(bool(rht)), int(rht_seed)))
+    return float(_L().or_nv_amax(_p(x), R, C, C, _rht_mode(rht), int(rht_seed)))
 
 
-def nv_quantize(x_bf16: np.ndarray, rht: bool = False, rht_seed: int = 0, rounding: str = "rne",
+def nv_quantize(x_bf16: np.ndarray, rht=False, rht_seed: int = 0, rounding: str = "rne",
                 sr_seed: int = 0, amax: float | None = None, row_offset: int = 0):
     """NVFP4 quantize of a BF16 tensor along the last axis.
 
@@ -294,9 +325,32 @@ def nv_quantize(x_bf16: np.ndarray, rht: bool = False, rht_seed: int = 0, roundi
     amax_out = np.zeros(1, dtype=np.float32)
     st_out = np.zeros(1, dtype=np.float32)
     amax_in = None if amax is None else np.array([amax], dtype=np.float32)
-    _L().or_nv_quantize(_p(x), R, C, C, int(bool(rht)), int(rht_seed), 1 if rounding == "sr" else 0,
+    _L().or_nv_quantize(_p(x), R, C, C, _rht_mode(rht), int(rht_seed), 1 if rounding == "sr" else 0,
                         int(sr_seed), None if amax_in is None else _p(amax_in), _p(amax_out),
                         _p(st_out), _p(q), _p(s), int(row_offset))
+    return {"q": q, "s": s, "s_t": np.float32(st_out[0]), "amax": np.float32(amax_out[0])}
+
+
+def nv_quantize_col(x_bf16: np.ndarray, **kw):
+    """Column-wise NVFP4 (16-blocks and RHT tiles along axis 0): by definition
+    the row-wise quantization of the transpose, in the transposed layout; the
+    stochastic-rounding words follow the transpose's linear element index."""
+    return nv_quantize(np.ascontiguousarray(np.asarray(x_bf16).T), **kw)
+
+
+def nv_quantize_2d(x_bf16: np.ndarray, rounding: str = "rne", sr_seed: int = 0, amax: float | None = None):
+    """NVFP4 with one E4M3 scale per 16x16 tile (weights), scales stored per
+    row ([R, C/16], 16 equal rows per tile).  Returns the dict of nv_quantize."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    R, C = x.shape
+    assert R % 16 == 0 and C % 16 == 0
+    q = np.empty((R, C // 2), dtype=np.uint8)
+    s = np.empty((R, C // 16), dtype=np.uint8)
+    amax_out = np.zeros(1, dtype=np.float32)
+    st_out = np.zeros(1, dtype=np.float32)
+    amax_in = None if amax is None else np.array([amax], dtype=np.float32)
+    _L().or_nv_quantize_2d(_p(x), R, C, C, 1 if rounding == "sr" else 0, int(sr_seed),
+                           None if amax_in is None else _p(amax_in), _p(amax_out), _p(st_out), _p(q), _p(s))
     return {"q": q, "s": s, "s_t": np.float32(st_out[0]), "amax": np.float32(amax_out[0])}
 
 

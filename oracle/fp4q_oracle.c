@@ -393,6 +393,19 @@ int or_e2m1_sr_d(double v, uint32_t r) {
 /* ------------------------------------------------------------------ */
 #define OR_NV_BLOCK 16
 
+/* Signs of the rotation for rht mode: 0 none, 1 random signs from the seed
+ * ([NVF] 2.B), 2 the deterministic H16 with D = I ("Pretraining Large
+ * Language Models with MXFP4 on Native FP4 Hardware", Wgrad section: the same
+ * Hadamard rotation at every step; the plain reading of "deterministic" is
+ * no sign flips). */
+static void nv_signs(int rht, uint64_t seed, float d[16]) {
+    if (rht == 1) {
+        or_rht16_signs(seed, d);
+    } else {
+        for (int j = 0; j < 16; ++j) d[j] = 1.0f;
+    }
+}
+
 static void nv_rotated_row(const uint16_t* xr, int64_t cols, int rht, const float d[16], float* yr) {
     for (int64_t t = 0; t < cols / 16; ++t) {
         float xin[16], yo[16];
@@ -406,7 +419,7 @@ static void nv_rotated_row(const uint16_t* xr, int64_t cols, int rht, const floa
 /* Tensor amax of the (optionally rotated) BF16 input. */
 float or_nv_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, int rht, uint64_t rht_seed) {
     float d[16];
-    or_rht16_signs(rht_seed, d);
+    nv_signs(rht, rht_seed, d);
     float amax = 0.0f;
 #pragma omp parallel for schedule(static) reduction(max : amax)
     for (int64_t r = 0; r < rows; ++r) {
@@ -430,7 +443,7 @@ void or_nv_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
                     const float* amax_in, float* amax_out, float* s_t_out,
                     uint8_t* q, uint8_t* s_e4m3, int64_t row_offset) {
     float d[16];
-    or_rht16_signs(rht_seed, d);
+    nv_signs(rht, rht_seed, d);
     float amax = amax_in ? *amax_in : or_nv_amax(x, rows, cols, ld_x, rht, rht_seed);
     float s_t = amax / 2688.0f;            /* 2688 = 6 * 448 */
     if (amax_out) *amax_out = amax;
@@ -470,6 +483,104 @@ void or_nv_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
                         code = or_e2m1_rne_d((double)v);
                 }
                 put_nibble(q + r * (cols / 2), c, code);
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* NVFP4 with 2D (16 x 16) block scaling, for weights.                  */
+/* [NVF] 2.B ("Mise a l'echelle bidimensionnelle"): weight blocks are   */
+/* 16 x 16, so the forward pass and the backward pass (which reads the  */
+/* weight transposed) quantize it identically.  Plain reading: one E4M3 */
+/* scale per 16 x 16 tile from that tile's amax, with the 1D rules of   */
+/* or_nv_quantize otherwise (tensor scale, scale rounding, rcp, RNE or  */
+/* SR by linear element index, signed zeros for a zero scale).  No RHT  */
+/* (the pages apply the RHT to Wgrad inputs, not to weights).  The      */
+/* scale is stored for every row of its tile ([rows, cols/16] layout,   */
+/* 16 equal rows per tile), so the 1D consumers read it unchanged.      */
+/* rows % 16 == 0.                                                       */
+/* ------------------------------------------------------------------ */
+void or_nv_quantize_2d(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, int rounding,
+                       uint64_t sr_seed, const float* amax_in, float* amax_out, float* s_t_out,
+                       uint8_t* q, uint8_t* s_e4m3) {
+    float amax = amax_in ? *amax_in : or_nv_amax(x, rows, cols, ld_x, 0, 0);
+    float s_t = amax / 2688.0f;
+    if (amax_out) *amax_out = amax;
+    if (s_t_out) *s_t_out = s_t;
+#pragma omp parallel for schedule(static)
+    for (int64_t tr = 0; tr < rows / 16; ++tr) {
+        for (int64_t b = 0; b < cols / OR_NV_BLOCK; ++b) {
+            float ab = 0.0f;
+            for (int i = 0; i < 16; ++i)
+                for (int j = 0; j < 16; ++j) {
+                    float v = fabsf(bf16_to_f32(x[(tr * 16 + i) * ld_x + b * 16 + j]));
+                    if (v > ab) ab = v;
+                }
+            uint8_t sb = 0;
+            float rcp = 0.0f;
+            int zero_block = 1;
+            if (s_t > 0.0f) {
+                float denom = 6.0f * s_t;
+                sb = or_e4m3_rn_satfinite(ab / denom);
+                if ((sb & 0x7f) != 0) {
+                    float sf = (float)or_e4m3_value(sb) * s_t;
+                    rcp = 1.0f / sf;
+                    zero_block = 0;
+                }
+            }
+            for (int i = 0; i < 16; ++i) {
+                int64_t r = tr * 16 + i;
+                s_e4m3[r * (cols / OR_NV_BLOCK) + b] = sb;
+                for (int j = 0; j < 16; ++j) {
+                    int64_t c = b * 16 + j;
+                    float y = bf16_to_f32(x[r * ld_x + c]);
+                    int code;
+                    if (zero_block) {
+                        code = signbit(y) ? 8 : 0;
+                    } else {
+                        float v = y * rcp;
+                        if (rounding == 1)
+                            code = or_e2m1_sr_d((double)v, or_sr_word(sr_seed, (uint64_t)(r * cols + c)));
+                        else
+                            code = or_e2m1_rne_d((double)v);
+                    }
+                    put_nibble(q + r * (cols / 2), c, code);
+                }
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* FP4RowToFP8Col: row-wise MXFP4 [rows, cols] -> FP8 of the transpose. */
+/* [HOP] Spanish summary, section 2 (kernels BF16ToFP4Row,              */
+/* FP4RowToFP8Row, FP4RowToFP8Col) and French summary section 2.C: one  */
+/* kernel dequantizes, transposes and re-quantizes (the weight-gradient */
+/* operand).  Plain reading: output y = E4M3 [cols, rows] with FP32     */
+/* scales per 1 x 128 tile along the output rows ([cols, rows/128]); a  */
+/* tile covers input rows r0 .. r0+127 of one input column c, its scale */
+/* is 2^Emax with Emax the largest block exponent among those 128       */
+/* elements, and each element is or_fp8_from_e2m1_shifted(code,         */
+/* E_element - Emax) -- the same rule as or_mx_to_fp8, so the tensor is */
+/* carried over exactly except for the flush below 2^-9 of its tile.    */
+/* rows % 128 == 0.                                                      */
+/* ------------------------------------------------------------------ */
+void or_mx_to_fp8_col(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t cols,
+                      uint8_t* y, float* tile_scale) {
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < cols; ++c) {
+        for (int64_t t = 0; t < rows / OR_FP8_TILE; ++t) {
+            int emax = -1000;
+            for (int j = 0; j < OR_FP8_TILE; ++j) {
+                int e = e8m0_exponent(s[(t * OR_FP8_TILE + j) * (cols / OR_MX_BLOCK) + c / OR_MX_BLOCK]);
+                if (e > emax) emax = e;
+            }
+            tile_scale[c * (rows / OR_FP8_TILE) + t] = (float)ldexp(1.0, emax);
+            for (int j = 0; j < OR_FP8_TILE; ++j) {
+                int64_t r = t * OR_FP8_TILE + j;
+                int e = e8m0_exponent(s[r * (cols / OR_MX_BLOCK) + c / OR_MX_BLOCK]);
+                y[c * rows + r] = or_fp8_from_e2m1_shifted(get_nibble(q + r * (cols / 2), c), e - emax);
             }
         }
     }

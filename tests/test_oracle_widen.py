@@ -1,0 +1,154 @@
+"""Pins of the oracle's column-path, 2D-scaling and deterministic-Hadamard steps.
+
+"Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs" (French
+summary 2.C, Spanish summary 2): FP4RowToFP8Col, one kernel that dequantizes,
+transposes and re-quantizes the weight-gradient operand.  "Pretraining Large
+Language Models with NVFP4" (2.B): 16x16 block scaling of the weights, so the
+forward pass and the transposed backward read identical values.  "Pretraining
+large language models with MXFP4 on Native FP4 Hardware" (Wgrad section): the
+deterministic Hadamard rotation H16, the same at every step.
+"""
+import numpy as np
+import pytest
+import scipy.linalg
+
+
+def _bf16(x):
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# deterministic H16 (rht = 2)
+# ---------------------------------------------------------------------------
+def test_deterministic_h16_is_the_scaled_sylvester_matrix(oracle):
+    """rht=2 rotates each 16-tile by H16/4 with no sign flips: for a BF16 tile
+    of small integers (exact in FP32) the rotated values are the product with
+    the Sylvester matrix from scipy, so the amax is known in closed form."""
+    H = scipy.linalg.hadamard(16).astype(np.float64)
+    rng = np.random.default_rng(11)
+    x = rng.integers(-8, 9, (4, 64)).astype(np.float32)
+    y = np.concatenate([(H @ x[:, 16 * t:16 * t + 16].T).T / 4 for t in range(4)], axis=1)
+    assert oracle.nv_amax(_bf16(x), 2, 0) == np.abs(y).max()
+    # and it is an involution: (H/4)(H/4) = I
+    assert np.array_equal((H / 4) @ (H / 4), np.eye(16))
+
+
+def test_deterministic_h16_ignores_the_seed_and_differs_from_rht(oracle):
+    rng = np.random.default_rng(12)
+    xb = _bf16((rng.standard_t(3, (32, 128)) * 1e-3).astype(np.float32))
+    a = oracle.nv_quantize(xb, rht=2, rht_seed=1)
+    b = oracle.nv_quantize(xb, rht=2, rht_seed=99)
+    c = oracle.nv_quantize(xb, rht=1, rht_seed=7)
+    assert np.array_equal(a["q"], b["q"]) and np.array_equal(a["s"], b["s"])
+    assert not np.array_equal(a["q"], c["q"])
+
+
+def test_deterministic_h16_cancels_in_the_contraction(oracle):
+    """The same rotation on both GEMM operands along K leaves A.B^T unchanged:
+    (A H/4)(B H/4)^T = A B^T, checked on exactly representable integers."""
+    H = scipy.linalg.hadamard(16).astype(np.float64) / 4
+    rng = np.random.default_rng(13)
+    A = rng.integers(-4, 5, (8, 16)).astype(np.float64)
+    B = rng.integers(-4, 5, (8, 16)).astype(np.float64)
+    assert np.array_equal((A @ H) @ (B @ H).T, A @ B.T)
+
+
+# ---------------------------------------------------------------------------
+# 2D (16 x 16) NVFP4
+# ---------------------------------------------------------------------------
+def test_2d_scaling_is_transpose_invariant(oracle):
+    """The dequantized 16x16-scaled tensor of W^T is the transpose of that of W
+    (the property the 2D scaling exists for); the 1D scaling does not have it."""
+    rng = np.random.default_rng(14)
+    w = (rng.standard_normal((64, 96)) * 0.02).astype(np.float32)
+    w[:, 5] *= 30.0                                           # one outlier column
+    wb = _bf16(w)
+    a = oracle.nv_quantize_2d(wb)
+    b = oracle.nv_quantize_2d(np.ascontiguousarray(wb.T))
+    assert a["amax"] == b["amax"]
+    da = oracle.nv_dequantize_f64(a["q"], a["s"], a["s_t"])
+    db = oracle.nv_dequantize_f64(b["q"], b["s"], b["s_t"])
+    assert np.array_equal(da, db.T)
+    a1 = oracle.nv_quantize(wb)
+    b1 = oracle.nv_quantize(np.ascontiguousarray(wb.T))
+    assert not np.array_equal(oracle.nv_dequantize_f64(a1["q"], a1["s"], a1["s_t"]),
+                              oracle.nv_dequantize_f64(b1["q"], b1["s"], b1["s_t"]).T)
+
+
+def test_2d_scaling_reduces_to_1d_when_rows_share_the_block_amax(oracle):
+    """If every row of every 16x16 tile has the same 16-element block amax, the
+    2D and 1D scales coincide, hence so do all codes."""
+    rng = np.random.default_rng(15)
+    base = (rng.standard_normal((16, 64)) * 0.1).astype(np.float32)
+    w = np.concatenate([base[rng.permutation(16)] for _ in range(4)], axis=0)   # 64 rows
+    # make each row's block amax equal within a tile: put the tile's max in every row
+    w = w.reshape(4, 16, 4, 16)
+    m = np.abs(w).max(axis=(1, 3), keepdims=True)
+    w[:, :, :, 0:1] = np.broadcast_to(m[:, :, :, 0:1] * 1.0, (4, 16, 4, 1))
+    w = w.reshape(64, 64)
+    wb = _bf16(w)
+    a = oracle.nv_quantize_2d(wb)
+    b = oracle.nv_quantize(wb)
+    assert np.array_equal(a["s"], b["s"]) and np.array_equal(a["q"], b["q"])
+
+
+def test_2d_scales_repeat_over_the_tile_rows(oracle):
+    rng = np.random.default_rng(16)
+    wb = _bf16((rng.standard_normal((48, 32)) * 0.05).astype(np.float32))
+    r = oracle.nv_quantize_2d(wb)
+    s = r["s"].reshape(3, 16, 2)
+    assert np.all(s == s[:, :1, :])
+    # the tile scale is the E4M3 rounding of tile amax / (6 s_t)
+    x = oracle.bf16_bits_to_f32(wb).reshape(3, 16, 2, 16)
+    ab = np.abs(x).max(axis=(1, 3)).astype(np.float32)
+    want = oracle.e4m3_rn_satfinite((ab / (np.float32(6.0) * r["s_t"])).astype(np.float32))
+    assert np.array_equal(s[:, 0, :], want)
+
+
+# ---------------------------------------------------------------------------
+# FP4RowToFP8Col
+# ---------------------------------------------------------------------------
+def test_fp4_row_to_fp8_col_is_lossless_and_transposed(oracle):
+    """With block exponents within 6 of each other down every 128-row tile, the
+    FP8 copy (times its tile scale) is exactly the transpose of the MXFP4 value,
+    and the tile scale is 2^(largest block exponent of the tile)."""
+    rng = np.random.default_rng(17)
+    R, C = 256, 96
+    q = rng.integers(0, 256, (R, C // 2), dtype=np.uint8)
+    base = rng.integers(110, 140, (R // 128, C // 32))
+    s = (np.repeat(base, 128, axis=0) - rng.integers(0, 7, (R, C // 32))).astype(np.uint8)
+    y, ts = oracle.mx_to_fp8_col(q, s)
+    assert y.shape == (C, R) and ts.shape == (C, R // 128)
+    e = s.astype(np.int64) - 127
+    emax = e.reshape(R // 128, 128, C // 32).max(axis=1)                 # [tiles, blocks]
+    assert np.array_equal(ts.astype(np.float64), np.exp2(np.repeat(emax.T, 32, axis=0)))
+    e8 = oracle.e4m3_values()[y] * np.repeat(ts.astype(np.float64), 128, axis=1)
+    assert np.array_equal(e8, oracle.mx_dequantize_f64(q, s).T)
+
+
+def test_fp4_row_to_fp8_col_flushes_only_deep_shifts(oracle):
+    R, C = 128, 32
+    q = np.full((R, C // 2), 0x77, dtype=np.uint8)            # all codes 6.0
+    s = np.full((R, 1), 127, dtype=np.uint8)
+    s[1:32] = 127 - 12                                        # 6 * 2^-12 < 2^-9: flushed
+    s[32:64] = 127 - 10                                       # 6 * 2^-10 = 3 * 2^-9
+    s[64:] = 127 - 9                                          # 6 * 2^-9
+    y, ts = oracle.mx_to_fp8_col(q, s)
+    assert np.all(ts == 1.0)
+    assert np.all(y[:, 0] == 0x4C)                            # 6.0 = 1.5 * 2^2 in E4M3
+    assert np.all(y[:, 1:32] == 0) and np.all(y[:, 32:64] == 0x03) and np.all(y[:, 64:] == 0x06)
+
+
+def test_fp4_row_to_fp8_col_agrees_with_the_row_kernel_on_a_transposed_tile(oracle):
+    """When each block exponent is constant along the rows of a 128x128 tile and
+    the codes form a symmetric pattern, the column conversion of the tile equals
+    the row conversion (a different code path of the oracle)."""
+    rng = np.random.default_rng(18)
+    codes = rng.integers(0, 16, (128, 128), dtype=np.uint8)
+    codes = np.triu(codes) + np.triu(codes, 1).T               # symmetric
+    q = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    s = np.full((128, 4), 120, dtype=np.uint8)
+    yc, tc = oracle.mx_to_fp8_col(q, s)
+    yr, tr = oracle.mx_to_fp8(q, s)
+    assert np.array_equal(yc, yr) and np.array_equal(tc, tr)
