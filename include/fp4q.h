@@ -12,8 +12,11 @@
  *
  * Conventions shared by all calls:
  *  - Tensors are row-major [rows, cols]; blocks run along the last
- *    (contiguous) axis.  block_axis must be 1 (the last axis); 0 is
- *    reserved for column-wise blocks and returns FP4Q_ERR_UNSUPPORTED_SHAPE.
+ *    (contiguous) axis (block_axis = 1).  block_axis = 0 (column-wise
+ *    blocks, for the weight-gradient operands) is accepted where a call says
+ *    so: the result is then the block_axis = 1 quantization of the transpose,
+ *    written in the transposed layout ([cols, rows/2] codes, scales of a
+ *    cols x rows/B matrix), without the transpose ever being stored.
  *  - Packed FP4 (E2M1): element i of a row sits in the low nibble of byte
  *    i/2 when i is even and in the high nibble when i is odd; a row of C
  *    elements takes C/2 bytes and rows are contiguous (row stride C/2).
@@ -96,6 +99,10 @@ size_t fp4q_scales_bytes(int64_t rows, int64_t scale_cols, fp4q_scale_layout lay
  *   cols       multiple of 32
  *   q          device out, [rows, cols/2] packed codes
  *   scales     device out, E8M0 bytes in `layout` (rows x cols/32)
+ *   block_axis 1; or 0 for a BF16 source with rows % 128 == 0 and
+ *              cols % 128 == 0: q [cols, rows/2] and scales (cols x rows/32)
+ *              of X^T ([HOP] 2.C: kernels with native support for transposed
+ *              layouts, for the weight-gradient GEMM).
  */
 fp4q_status fp4q_mx_quantize(const void* x, fp4q_dtype x_type, const float* tile_scale,
                              int64_t rows, int64_t cols, int64_t ld_x, int block_axis,
@@ -138,9 +145,11 @@ fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, int64_t row
  * (6 s_t));  sf = float(s_b) * s_t;  q = ROUND(y * (1 / sf)); all in FP32
  * with IEEE round-to-nearest operations.  amax == 0 or s_b == 0 gives
  * signed-zero codes.
- * [NVF] 2.B: rht != 0 applies y = (1/4) H16 diag(d) x on every 16-element
+ * [NVF] 2.B: rht == 1 applies y = (1/4) H16 diag(d) x on every 16-element
  * tile (Sylvester H16; d_j = -1 iff bit j of word 0 of Philox4x32-10 with
  * key = rht_seed and counter 0; butterflies with strides 1, 2, 4, 8 in FP32).
+ * rht == 2 applies the deterministic H16 (d = 1, the same rotation at every
+ * call: [MXN] Wgrad section); rht_seed is then ignored.
  * rounding == FP4Q_SR rounds each element up with probability equal to its
  * distance fraction: up iff r < frac * 2^32, r the (i mod 4)-th word of
  * Philox4x32-10(key = sr_seed, counter = i / 4), i = row * cols + col.
@@ -153,6 +162,9 @@ fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, int64_t row
  *   workspace        device, >= fp4q_nv_quantize_workspace_bytes() bytes, 16-B
  *                    aligned; used only when amax_in == NULL (may be NULL then
  *                    not); reset by the call itself.
+ *   block_axis       1; or 0 (rows % 128 == 0, cols % 64 == 0): blocks, RHT
+ *                    tiles and the stochastic-rounding index i follow X^T,
+ *                    q [cols, rows/2], scales (cols x rows/16).
  */
 size_t fp4q_nv_quantize_workspace_bytes(int64_t rows, int64_t cols);
 fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
@@ -161,6 +173,45 @@ fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t cols, int64_t 
                              float* amax_out, float* tensor_scale_out, uint8_t* q,
                              uint8_t* scales, fp4q_scale_layout layout, void* workspace,
                              size_t workspace_bytes, fp4q_stream_t stream);
+
+/*
+ * fp4q_nv_quantize_2d -- BF16 weights -> NVFP4 with one E4M3 scale per 16 x 16
+ * tile.  [NVF] 2.B (two-dimensional scaling): weight blocks of 16 x 16, so that
+ * the forward pass and the backward pass, which reads the weight transposed,
+ * use the same quantized values.  The rules of fp4q_nv_quantize with the block
+ * amax taken over the 16 x 16 tile; no rotation.  The tile's scale is written
+ * for each of its 16 rows (scales rows x cols/16 in `layout`), so the result
+ * feeds fp4q_block_scaled_gemm unchanged; the quantization of W^T is the
+ * transpose of that of W.
+ *   x         device BF16 [rows, ld_x], 32-byte aligned, ld_x % 16 == 0;
+ *             rows % 16 == 0, cols % 16 == 0
+ *   other arguments as fp4q_nv_quantize (SR index i = row * cols + col)
+ */
+fp4q_status fp4q_nv_quantize_2d(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                fp4q_rounding rounding, uint64_t sr_seed, const float* amax_in,
+                                float* amax_out, float* tensor_scale_out, uint8_t* q,
+                                uint8_t* scales, fp4q_scale_layout layout, void* workspace,
+                                size_t workspace_bytes, fp4q_stream_t stream);
+
+/*
+ * fp4q_fp4_row_to_fp8_col -- FP4RowToFP8Col: row-wise MXFP4 [rows, cols] ->
+ * FP8-E4M3 of the transpose [cols, rows] with one FP32 scale per 1x128 tile
+ * along the output rows.  [HOP] Spanish summary section 2 (kernels
+ * BF16ToFP4Row, FP4RowToFP8Row, FP4RowToFP8Col) and French summary 2.C: one
+ * kernel dequantizes, transposes and re-quantizes the weight-gradient operand.
+ * Output tile (c, rows r0 .. r0+127): scale 2^Emax, Emax the largest block
+ * exponent among its 128 elements; element = E4M3 of value(code) *
+ * 2^(E - Emax) by field remapping, as fp4q_fp4_to_fp8 (exact unless below
+ * 2^-9 of its tile, then a signed zero).
+ *   q           device, [rows, cols/2], 32-byte aligned
+ *   scales      device, ROWMAJOR E8M0 [rows, cols/32], 4-byte aligned
+ *   rows, cols  multiples of 128
+ *   y           device out, E4M3 [cols, rows], 32-byte aligned
+ *   tile_scale  device out, FP32 [cols, rows/128]
+ */
+fp4q_status fp4q_fp4_row_to_fp8_col(const uint8_t* q, const uint8_t* scales, int64_t rows,
+                                    int64_t cols, uint8_t* y, float* tile_scale,
+                                    fp4q_stream_t stream);
 
 /* One FP4 GEMM operand.  Host struct; the pointers in it are device pointers. */
 typedef struct fp4q_operand {

@@ -26,6 +26,11 @@ uint32_t* status_word();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// 32-bit shared-memory address of a __shared__ object (for ld/st.shared).
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 // Status-word bits (which kernel gave up a bounded wait).
 enum : uint32_t {
     kStatusGemmTimeout = 1u << 0,

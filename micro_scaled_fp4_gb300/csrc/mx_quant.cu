@@ -326,6 +326,56 @@ __global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_e4m3_staged_ker
     });
 }
 
+// Column-wise MXFP4 of BF16 (block axis 0): the row-wise quantization of X^T,
+// written in the transposed layout (q [cols, rows/2], scales [cols, rows/32])
+// without materialising X^T.  A CTA stages a 128-row x 128-column BF16 tile in
+// shared memory (rows padded by 16 bytes); thread t reads column pair
+// 2(t % 64), 2(t % 64) + 1 over rows 32(t / 64) .. + 31 with one 32-bit shared
+// load per row (lanes on consecutive words: no bank conflicts), repacks the
+// halves into the two columns' 32-element blocks and quantizes them with the
+// row-wise rule.
+constexpr int kMxColRows = 128, kMxColCols = 128;
+constexpr uint32_t kMxColStride = kMxColCols * 2 + 16;
+
+__global__ void __launch_bounds__(256) mx_quantize_col_kernel(
+    const uint8_t* __restrict__ x, int64_t rows, int64_t ld_x_bytes, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ s, int mma_layout) {
+    extern __shared__ __align__(16) uint8_t tile[];
+    const int64_t r0 = int64_t(blockIdx.y) * kMxColRows, c0 = int64_t(blockIdx.x) * kMxColCols;
+    const uint32_t base = smem_addr(tile);
+    for (uint32_t i = threadIdx.x; i < kMxColRows * 8; i += blockDim.x) {
+        const uint32_t r = i >> 3, ch = i & 7u;
+        const u32x8 v = ldg256(x + (r0 + r) * ld_x_bytes + c0 * 2 + ch * 32);
+        const uint32_t d = base + r * kMxColStride + ch * 32;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(d), "r"(v.v[0]), "r"(v.v[1]), "r"(v.v[2]),
+                     "r"(v.v[3]) : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(d + 16), "r"(v.v[4]), "r"(v.v[5]),
+                     "r"(v.v[6]), "r"(v.v[7]) : "memory");
+    }
+    __syncthreads();
+    const uint32_t cp = threadIdx.x & 63u, k = threadIdx.x >> 6;
+    RawBlock<kBF16> A, B;                      // columns 2cp and 2cp + 1, rows 32k .. 32k + 31
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        uint32_t w0, w1;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(base + (32 * k + 2 * j) * kMxColStride + 4 * cp));
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(base + (32 * k + 2 * j + 1) * kMxColStride + 4 * cp));
+        const uint32_t lo = __byte_perm(w0, w1, 0x5410), hi = __byte_perm(w0, w1, 0x7632);
+        if (j < 8) { A.a.v[j] = lo; B.a.v[j] = hi; } else { A.b.v[j - 8] = lo; B.b.v[j - 8] = hi; }
+    }
+    const uint32_t spr = uint32_t(rows / 32), blk = uint32_t(r0 / 32) + k;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint4 codes;
+        uint32_t sb;
+        quantize_block<kBF16>(h ? B : A, codes, sb);
+        const int64_t c = c0 + 2 * cp + h;
+        *reinterpret_cast<uint4*>(q + c * (rows / 2) + int64_t(blk) * 16) = codes;
+        const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(c), blk, spr) : uint64_t(c) * spr + blk;
+        s[so] = uint8_t(sb);
+    }
+}
+
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(256) mx_dequantize_kernel(
     const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, uint32_t bpr,
@@ -388,7 +438,32 @@ extern "C" fp4q_status fp4q_mx_quantize(const void* x, fp4q_dtype x_type, const 
         return fail(FP4Q_ERR_INVALID_ARGUMENT, "mx_quantize: bad scale layout");
     if (rows < 0 || cols < 0 || ld_x < cols)
         return fail(FP4Q_ERR_INVALID_ARGUMENT, "mx_quantize: need rows >= 0, cols >= 0, ld_x >= cols");
-    if (block_axis != 1) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "mx_quantize: only block_axis = 1 (last axis)");
+    if (block_axis == 0) {
+        if (x_type != FP4Q_BF16) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "mx_quantize: block_axis 0 needs a BF16 source");
+        if (rows % kMxColRows || cols % kMxColCols)
+            return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "mx_quantize: block_axis 0 needs rows %% 128 == 0, cols %% 128 == 0");
+        if (rows / kMxColRows > 65535)
+            return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "mx_quantize: block_axis 0 needs rows <= 8388480");
+        if (rows == 0 || cols == 0) return FP4Q_OK;
+        if (!x || !q || !scales) return fail(FP4Q_ERR_INVALID_ARGUMENT, "mx_quantize: null pointer");
+        if ((reinterpret_cast<uintptr_t>(x) & 31u) || (ld_x * 2) % 32 || !aligned16(q))
+            return fail(FP4Q_ERR_MISALIGNED, "mx_quantize: x 32-byte aligned with ld_x %% 16 == 0, q 16-byte aligned");
+        fp4q_status st = current_device(nullptr);
+        if (st != FP4Q_OK) return st;
+        const uint32_t smem = kMxColRows * kMxColStride;
+        static int attr_set[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (!attr_set[dev & 63]) {
+            cudaFuncSetAttribute(mx_quantize_col_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+            attr_set[dev & 63] = 1;
+        }
+        const dim3 grid(unsigned(cols / kMxColCols), unsigned(rows / kMxColRows), 1);
+        mx_quantize_col_kernel<<<grid, 256, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
+            static_cast<const uint8_t*>(x), rows, ld_x * 2, q, scales, layout == FP4Q_SCALES_MMA);
+        return check_launch("mx_quantize (block_axis 0)");
+    }
+    if (block_axis != 1) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "mx_quantize: block_axis must be 0 or 1");
     if (cols % 32) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "mx_quantize: cols %% 32 != 0");
     if (x_type == FP4Q_E4M3 && cols % 128)
         return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "mx_quantize: E4M3 source needs cols %% 128 == 0");

@@ -15,6 +15,8 @@
 // load, the butterflies in registers, the block amax in-thread, 8 bytes of
 // codes and one scale byte out.  The FP32 steps use explicit round-to-nearest
 // intrinsics so that no contraction or reassociation changes a result.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace fp4q {
@@ -54,7 +56,7 @@ __device__ __forceinline__ void load_tile(const uint8_t* p, float (&t)[16]) {
 __global__ void __launch_bounds__(256) nv_amax_kernel(const uint8_t* __restrict__ x, int64_t rows,
                                                       uint32_t tpr, int64_t ld_x_bytes, int rht,
                                                       uint64_t rht_seed, uint32_t* __restrict__ amax_bits) {
-    const uint32_t signs = rht ? rht_signs(rht_seed) : 0u;
+    const uint32_t signs = rht == 1 ? rht_signs(rht_seed) : 0u;
     const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
     uint32_t m = 0;
     if (b < tpr) {
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(
     const uint8_t* __restrict__ x, int64_t rows, uint32_t tpr, int64_t ld_x_bytes, int rht,
     uint64_t rht_seed, const PhiloxKeys sr_keys, const float* __restrict__ amax_ptr, float* __restrict__ amax_out,
     float* __restrict__ st_out, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout) {
-    const uint32_t signs = rht ? rht_signs(rht_seed) : 0u;
+    const uint32_t signs = rht == 1 ? rht_signs(rht_seed) : 0u;
     const float amax = *amax_ptr;
     const float s_t = __fdiv_rn(amax, 2688.0f);        // 6 * 448
     const float denom = __fmul_rn(6.0f, s_t);
@@ -209,6 +211,191 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(
     }
 }
 
+// Scale, reciprocal and codes of one 16-element block y (FP32) under the
+// tensor scale s_t, with the rules of nv_quant_kernel; `ab` is the block's
+// amax bits (the 2D form passes its tile's).  SR draws the words of linear
+// elements i0 .. i0 + 15 (i0 % 16 == 0).
+template <bool SR>
+__device__ __forceinline__ uint32_t nv_block_codes(const float (&t)[16], uint32_t ab, float s_t, float denom,
+                                                   uint64_t i0, const PhiloxKeys& sr_keys, uint2& words) {
+    uint32_t sb = 0;
+    float rcp = 0.0f;
+    if (s_t > 0.0f) {
+        sb = cvt_e4m3(__fdiv_rn(u2f(ab), denom));
+        if (sb & 0x7fu) rcp = __frcp_rn(__fmul_rn(e4m3x2_to_f32x2(sb).x, s_t));
+    }
+    uint32_t w[2];
+    if (rcp == 0.0f) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v |= ((f2u(t[8 * k + j]) >> 31) << 3) << (4 * j);
+            w[k] = v;
+        }
+    } else if constexpr (!SR) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            w[k] = cvt_e2m1x8(__fmul_rn(t[8 * k], rcp), __fmul_rn(t[8 * k + 1], rcp), __fmul_rn(t[8 * k + 2], rcp),
+                              __fmul_rn(t[8 * k + 3], rcp), __fmul_rn(t[8 * k + 4], rcp),
+                              __fmul_rn(t[8 * k + 5], rcp), __fmul_rn(t[8 * k + 6], rcp),
+                              __fmul_rn(t[8 * k + 7], rcp));
+    } else {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint64_t ctr = (i0 >> 2) + uint64_t(2 * k + h);
+                const uint4 rnd = philox_ctr64(uint32_t(ctr), uint32_t(ctr >> 32), sr_keys);
+                const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    v |= sr_e2m1_code(__fmul_rn(t[8 * k + 4 * h + e], rcp), rr[e]) << (4 * (4 * h + e));
+            }
+            w[k] = v;
+        }
+    }
+    words = make_uint2(w[0], w[1]);
+    return sb;
+}
+
+__device__ __forceinline__ float nv_tensor_scale(const float* amax_ptr, float* amax_out, float* st_out) {
+    const float amax = *amax_ptr;
+    const float s_t = __fdiv_rn(amax, 2688.0f);        // 6 * 448
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        if (amax_out) *amax_out = amax;
+        *st_out = s_t;
+    }
+    return s_t;
+}
+
+// 2D (16 x 16) block scaling for weights ("Pretraining Large Language Models
+// with NVFP4", 2.B): a half-warp holds one tile, lane j its row j's 16
+// elements; the tile amax is the max over the half-warp; every row of the
+// tile stores the same scale byte ([rows, cols/16] layout).  No rotation.
+template <bool SR>
+__global__ void __launch_bounds__(256) nv_quant_2d_kernel(
+    const uint8_t* __restrict__ x, int64_t rows, uint32_t tpr, int64_t ld_x_bytes, const PhiloxKeys sr_keys,
+    const float* __restrict__ amax_ptr, float* __restrict__ amax_out, float* __restrict__ st_out,
+    uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout) {
+    const float s_t = nv_tensor_scale(amax_ptr, amax_out, st_out);
+    const float denom = __fmul_rn(6.0f, s_t);
+    const int64_t units = (rows / 16) * int64_t(tpr);            // (tile row, block) pairs
+    const uint32_t j = threadIdx.x & 15u;
+    const uint64_t cols = uint64_t(tpr) * 16;
+    // the loop runs per warp (two units), so that both half-warps stay in the
+    // shuffles; a half-warp past the end works on nothing
+    const int64_t wstride = int64_t(gridDim.x) * (blockDim.x / 32);
+    for (int64_t wu = int64_t(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; 2 * wu < units; wu += wstride) {
+        const int64_t un = 2 * wu + ((threadIdx.x >> 4) & 1);
+        const bool valid = un < units;
+        const int64_t tr = valid ? un / tpr : 0;
+        const uint32_t b = valid ? uint32_t(un - tr * tpr) : 0u;
+        const int64_t r = tr * 16 + j;
+        float t[16];
+        uint32_t ab = 0;
+        if (valid) {
+            load_tile(x + r * ld_x_bytes + uint64_t(b) * 32, t);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ab = max(ab, f2u(t[e]) & 0x7fffffffu);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) ab = max(ab, __shfl_xor_sync(0xffffffffu, ab, o));
+        if (!valid) continue;
+        uint2 words;
+        const uint32_t sb = nv_block_codes<SR>(t, ab, s_t, denom, uint64_t(r) * cols + uint64_t(b) * 16, sr_keys, words);
+        *reinterpret_cast<uint2*>(q + uint64_t(r) * (cols / 2) + uint64_t(b) * 8) = words;
+        const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(r), b, tpr) : uint64_t(r) * tpr + b;
+        s[so] = uint8_t(sb);
+    }
+}
+
+// Column-wise NVFP4 (block axis 0): the row-wise quantization of X^T, written
+// in the transposed layout, without materialising X^T.  A CTA stages a
+// 128-row x 64-column BF16 tile in shared memory (rows padded by 16 bytes so
+// that the column reads below are conflict-free); thread t then reads column
+// pair 2(t % 32), 2(t % 32) + 1 over rows 16(t / 32) .. + 15 (one 32-bit
+// shared load per row gives both columns) and quantizes the two 16-element
+// blocks -- rotated along axis 0 when rht != 0 -- into rows c of q [cols, rows/2]
+// and scales [cols, rows/16].  MODE 0: tensor amax only; 1: RNE; 2: SR (linear
+// element index of X^T).
+constexpr int kColRows = 128, kColCols = 64;
+constexpr uint32_t kColStride = kColCols * 2 + 16;
+
+template <int MODE>
+__global__ void __launch_bounds__(256) nv_col_kernel(
+    const uint8_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x_bytes, int rht, uint64_t rht_seed,
+    const PhiloxKeys sr_keys, const float* __restrict__ amax_ptr, float* __restrict__ amax_out,
+    float* __restrict__ st_out, uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ s, int mma_layout) {
+    __shared__ __align__(16) uint8_t tile[kColRows * kColStride];
+    __shared__ uint32_t wmax[8];
+    const uint32_t signs = rht == 1 ? rht_signs(rht_seed) : 0u;
+    float s_t = 0.0f, denom = 0.0f;
+    if constexpr (MODE != 0) {
+        s_t = nv_tensor_scale(amax_ptr, amax_out, st_out);
+        denom = __fmul_rn(6.0f, s_t);
+    }
+    const int64_t r0 = int64_t(blockIdx.y) * kColRows, c0 = int64_t(blockIdx.x) * kColCols;
+    // stage the tile: 128 rows x 128 bytes, 32 bytes per load
+    for (uint32_t i = threadIdx.x; i < kColRows * 4; i += blockDim.x) {
+        const uint32_t r = i >> 2, ch = i & 3u;
+        const u32x8 v = ldg256(x + (r0 + r) * ld_x_bytes + c0 * 2 + ch * 32);
+        const uint32_t d = smem_addr(tile) + r * kColStride + ch * 32;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(d), "r"(v.v[0]), "r"(v.v[1]), "r"(v.v[2]),
+                     "r"(v.v[3]) : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(d + 16), "r"(v.v[4]), "r"(v.v[5]),
+                     "r"(v.v[6]), "r"(v.v[7]) : "memory");
+    }
+    __syncthreads();
+    const uint32_t cp = threadIdx.x & 31u, k = threadIdx.x >> 5;
+    float a[16], b[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        uint32_t w;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(smem_addr(tile) + (16 * k + j) * kColStride + 4 * cp));
+        a[j] = u2f(w << 16);
+        b[j] = u2f(w & 0xffff0000u);
+    }
+    if (rht) {
+        rht16(a, signs);
+        rht16(b, signs);
+    }
+    uint32_t ma = 0, mb = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        ma = max(ma, f2u(a[j]) & 0x7fffffffu);
+        mb = max(mb, f2u(b[j]) & 0x7fffffffu);
+    }
+    if constexpr (MODE == 0) {
+        uint32_t m = max(ma, mb);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t v = 0;
+            for (int w = 0; w < 8; ++w) v = max(v, wmax[w]);
+            if (v) atomicMax(amax_bits, v);
+        }
+    } else {
+        const uint32_t spr = uint32_t(rows / 16);                 // scale columns per output row
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t c = c0 + 2 * cp + h;
+            const int64_t rb = r0 + 16 * k;                          // first row of the block
+            uint2 words;
+            const uint32_t sb = nv_block_codes<MODE == 2>(h ? b : a, h ? mb : ma, s_t, denom,
+                                                         uint64_t(c) * uint64_t(rows) + uint64_t(rb), sr_keys, words);
+            *reinterpret_cast<uint2*>(q + c * (rows / 2) + rb / 2) = words;
+            const uint32_t blk = uint32_t(rb / 16);
+            const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(c), blk, spr) : uint64_t(c) * spr + blk;
+            s[so] = uint8_t(sb);
+        }
+    }
+}
+
 }  // namespace
 }  // namespace fp4q
 
@@ -220,42 +407,91 @@ extern "C" size_t fp4q_nv_quantize_workspace_bytes(int64_t rows, int64_t cols) {
     return 256;   // one 32-bit amax word (padded)
 }
 
+// Common argument checks; *amax_ptr is amax_in or, after the amax pass that
+// `amax_pass` launches, the workspace word.
+namespace {
+fp4q_status nv_prologue(const char* who, const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                        fp4q_rounding rounding, const float* amax_in, float* tensor_scale_out, uint8_t* q,
+                        uint8_t* scales, fp4q_scale_layout layout, void* workspace, size_t workspace_bytes) {
+    if (rounding != FP4Q_RNE && rounding != FP4Q_SR)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "%s: bad rounding mode", who);
+    if (layout != FP4Q_SCALES_ROWMAJOR && layout != FP4Q_SCALES_MMA)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "%s: bad scale layout", who);
+    if (rows < 0 || cols < 0 || ld_x < cols)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "%s: need rows >= 0, cols >= 0, ld_x >= cols", who);
+    if (cols % 16) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "%s: cols %% 16 != 0", who);
+    if (!tensor_scale_out) return fail(FP4Q_ERR_INVALID_ARGUMENT, "%s: tensor_scale_out is NULL", who);
+    if (rows > 0 && cols > 0 && (!x || !q || !scales)) return fail(FP4Q_ERR_INVALID_ARGUMENT, "%s: null pointer", who);
+    if (!amax_in && (!workspace || workspace_bytes < fp4q_nv_quantize_workspace_bytes(rows, cols)))
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "%s: workspace missing or too small", who);
+    if ((reinterpret_cast<uintptr_t>(x) & 31u) || (ld_x * 2) % 32 || (q && !aligned16(q)) ||
+        (workspace && !aligned16(workspace)))
+        return fail(FP4Q_ERR_MISALIGNED, "%s: x 32-byte aligned with ld_x %% 16 == 0; q, workspace 16-byte aligned",
+                    who);
+    return FP4Q_OK;
+}
+
+fp4q_status zero_amax_word(void* workspace, cudaStream_t s, const char* who) {
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "%s: memset: %s", who, cudaGetErrorString(e));
+    return FP4Q_OK;
+}
+}  // namespace
+
 extern "C" fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                                         int block_axis, int rht, uint64_t rht_seed,
                                         fp4q_rounding rounding, uint64_t sr_seed, const float* amax_in,
                                         float* amax_out, float* tensor_scale_out, uint8_t* q,
                                         uint8_t* scales, fp4q_scale_layout layout, void* workspace,
                                         size_t workspace_bytes, fp4q_stream_t stream) {
-    if (rounding != FP4Q_RNE && rounding != FP4Q_SR)
-        return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: bad rounding mode");
-    if (layout != FP4Q_SCALES_ROWMAJOR && layout != FP4Q_SCALES_MMA)
-        return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: bad scale layout");
-    if (rows < 0 || cols < 0 || ld_x < cols)
-        return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: need rows >= 0, cols >= 0, ld_x >= cols");
-    if (block_axis != 1) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "nv_quantize: only block_axis = 1");
-    if (cols % 16) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "nv_quantize: cols %% 16 != 0");
-    if (!tensor_scale_out) return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: tensor_scale_out is NULL");
-    if (rows > 0 && cols > 0 && (!x || !q || !scales))
-        return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: null pointer");
-    if (!amax_in && (!workspace || workspace_bytes < fp4q_nv_quantize_workspace_bytes(rows, cols)))
-        return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: workspace missing or too small");
-    if ((reinterpret_cast<uintptr_t>(x) & 31u) || (ld_x * 2) % 32 || (q && !aligned16(q)) ||
-        (workspace && !aligned16(workspace)))
-        return fail(FP4Q_ERR_MISALIGNED, "nv_quantize: x 32-byte aligned with ld_x %% 16 == 0; q, workspace 16-byte aligned");
-    int sms = 0;
-    fp4q_status st = current_device(&sms);
+    fp4q_status st = nv_prologue("nv_quantize", x, rows, cols, ld_x, rounding, amax_in, tensor_scale_out, q, scales,
+                                 layout, workspace, workspace_bytes);
     if (st != FP4Q_OK) return st;
+    if (rht < 0 || rht > 2) return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize: rht must be 0, 1 or 2");
+    if (block_axis != 0 && block_axis != 1) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "nv_quantize: block_axis 0 or 1");
+    if (block_axis == 0 && (rows % kColRows || cols % kColCols))
+        return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "nv_quantize: block_axis 0 needs rows %% 128 == 0, cols %% 64 == 0");
+    int sms = 0;
+    if ((st = current_device(&sms)) != FP4Q_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    const float* amax_ptr = amax_in;
+    const int mma = layout == FP4Q_SCALES_MMA;
+    const PhiloxKeys keys = philox_keys(sr_seed);
+    if (block_axis == 0) {
+        const dim3 grid(unsigned(cols / kColCols), unsigned(rows / kColRows), 1);
+        if (rows > 0 && unsigned(rows / kColRows) > 65535u)
+            return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "nv_quantize: block_axis 0 needs rows <= 8388480");
+        if (!amax_in) {
+            uint32_t* w = static_cast<uint32_t*>(workspace);
+            if ((st = zero_amax_word(w, s, "nv_quantize")) != FP4Q_OK) return st;
+            if (rows > 0 && cols > 0) {
+                nv_col_kernel<0><<<grid, 256, 0, s>>>(xb, rows, cols, ld_x * 2, rht, rht_seed, keys, nullptr, nullptr,
+                                                      nullptr, w, q, scales, mma);
+                if ((st = check_launch("nv_quantize amax")) != FP4Q_OK) return st;
+            }
+            amax_ptr = reinterpret_cast<const float*>(w);
+        }
+        if (rows == 0 || cols == 0) {
+            nv_quant_kernel<false><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, keys, amax_ptr, amax_out, tensor_scale_out, q,
+                                                     scales, 0);
+            return check_launch("nv_quantize");
+        }
+        if (rounding == FP4Q_SR)
+            nv_col_kernel<2><<<grid, 256, 0, s>>>(xb, rows, cols, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out,
+                                                  tensor_scale_out, nullptr, q, scales, mma);
+        else
+            nv_col_kernel<1><<<grid, 256, 0, s>>>(xb, rows, cols, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out,
+                                                  tensor_scale_out, nullptr, q, scales, mma);
+        return check_launch("nv_quantize");
+    }
     const uint32_t tpr = uint32_t(cols / 16);
     int tpb = 32, nx = 1;
     if (tpr) row_launch_shape(tpr, &tpb, &nx);
     dim3 grid(unsigned(nx), row_grid_y(rows, nx, sms, resident_per_sm(nv_quant_kernel<true>, tpb)), 1);
-    const uint8_t* xb = static_cast<const uint8_t*>(x);
-    const float* amax_ptr = amax_in;
     if (!amax_in) {
         uint32_t* w = static_cast<uint32_t*>(workspace);
-        cudaError_t e = cudaMemsetAsync(w, 0, sizeof(uint32_t), s);
-        if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "nv_quantize: memset: %s", cudaGetErrorString(e));
+        if ((st = zero_amax_word(w, s, "nv_quantize")) != FP4Q_OK) return st;
         if (rows > 0 && cols > 0) {
             nv_amax_kernel<<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, w);
             if ((st = check_launch("nv_quantize amax")) != FP4Q_OK) return st;
@@ -264,16 +500,61 @@ extern "C" fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t col
     }
     if (rows == 0 || cols == 0) {
         // still publish s_t (and amax) for an empty tensor: both are 0
-        nv_quant_kernel<false><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, philox_keys(0), amax_ptr, amax_out, tensor_scale_out,
-                                                 q, scales, 0);
+        nv_quant_kernel<false><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, keys, amax_ptr, amax_out, tensor_scale_out, q,
+                                                 scales, 0);
         return check_launch("nv_quantize");
     }
-    const int mma = layout == FP4Q_SCALES_MMA;
     if (rounding == FP4Q_SR)
-        nv_quant_kernel<true><<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, philox_keys(sr_seed), amax_ptr,
-                                                   amax_out, tensor_scale_out, q, scales, mma);
+        nv_quant_kernel<true><<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out,
+                                                   tensor_scale_out, q, scales, mma);
     else
-        nv_quant_kernel<false><<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, philox_keys(sr_seed), amax_ptr,
-                                                    amax_out, tensor_scale_out, q, scales, mma);
+        nv_quant_kernel<false><<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out,
+                                                    tensor_scale_out, q, scales, mma);
     return check_launch("nv_quantize");
+}
+
+extern "C" fp4q_status fp4q_nv_quantize_2d(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                           fp4q_rounding rounding, uint64_t sr_seed, const float* amax_in,
+                                           float* amax_out, float* tensor_scale_out, uint8_t* q, uint8_t* scales,
+                                           fp4q_scale_layout layout, void* workspace, size_t workspace_bytes,
+                                           fp4q_stream_t stream) {
+    fp4q_status st = nv_prologue("nv_quantize_2d", x, rows, cols, ld_x, rounding, amax_in, tensor_scale_out, q,
+                                 scales, layout, workspace, workspace_bytes);
+    if (st != FP4Q_OK) return st;
+    if (rows % 16) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "nv_quantize_2d: rows %% 16 != 0");
+    int sms = 0;
+    if ((st = current_device(&sms)) != FP4Q_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    const float* amax_ptr = amax_in;
+    const PhiloxKeys keys = philox_keys(sr_seed);
+    const uint32_t tpr = uint32_t(cols / 16);
+    if (!amax_in) {
+        uint32_t* w = static_cast<uint32_t*>(workspace);
+        if ((st = zero_amax_word(w, s, "nv_quantize_2d")) != FP4Q_OK) return st;
+        if (rows > 0 && cols > 0) {
+            int tpb = 32, nx = 1;
+            row_launch_shape(tpr, &tpb, &nx);
+            dim3 grid(unsigned(nx), row_grid_y(rows, nx, sms, resident_per_sm(nv_amax_kernel, tpb)), 1);
+            nv_amax_kernel<<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, 0, 0, w);
+            if ((st = check_launch("nv_quantize_2d amax")) != FP4Q_OK) return st;
+        }
+        amax_ptr = reinterpret_cast<const float*>(w);
+    }
+    if (rows == 0 || cols == 0) {
+        nv_quant_kernel<false><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, keys, amax_ptr, amax_out, tensor_scale_out, q,
+                                                 scales, 0);
+        return check_launch("nv_quantize_2d");
+    }
+    const int mma = layout == FP4Q_SCALES_MMA;
+    const int64_t units = (rows / 16) * int64_t(tpr);
+    const int per_sm = resident_per_sm(nv_quant_2d_kernel<true>, 256);
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((units + 15) / 16, int64_t(per_sm) * sms));
+    if (rounding == FP4Q_SR)
+        nv_quant_2d_kernel<true><<<unsigned(grid), 256, 0, s>>>(xb, rows, tpr, ld_x * 2, keys, amax_ptr, amax_out,
+                                                                tensor_scale_out, q, scales, mma);
+    else
+        nv_quant_2d_kernel<false><<<unsigned(grid), 256, 0, s>>>(xb, rows, tpr, ld_x * 2, keys, amax_ptr, amax_out,
+                                                                 tensor_scale_out, q, scales, mma);
+    return check_launch("nv_quantize_2d");
 }

@@ -32,7 +32,7 @@ EXPORTED = [
     "fp4q_mx_dequantize", "fp4q_fp4_to_fp8", "fp4q_nv_quantize_workspace_bytes", "fp4q_nv_quantize",
     "fp4q_block_scaled_gemm", "fp4q_device_status", "fp4q_moe_dispatch_workspace_bytes",
     "fp4q_moe_dispatch", "fp4q_rebased_scales_bytes", "fp4q_mx_rebase_scales", "fp4q_grouped_gemm",
-    "fp4q_moe_dispatch_static", "fp4q_check_wait_timeout",
+    "fp4q_moe_dispatch_static", "fp4q_check_wait_timeout", "fp4q_nv_quantize_2d", "fp4q_fp4_row_to_fp8_col",
 ]
 MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 * 1024 * 1024
 
@@ -92,6 +92,8 @@ def load() -> ctypes.CDLL:
                 "fp4q_mx_rebase_scales": [vp, i64, i64, vp, i64, vp, vp, vp, vp],
                 "fp4q_moe_dispatch_static": [vp, i64, ci, ci, vp, vp, i64, vp, vp, vp, vp, vp],
                 "fp4q_check_wait_timeout": [u64, vp],
+                "fp4q_nv_quantize_2d": [vp, i64, i64, i64, ci, u64, vp, vp, vp, vp, vp, ci, vp, ctypes.c_size_t, vp],
+                "fp4q_fp4_row_to_fp8_col": [vp, vp, i64, i64, vp, vp, vp],
                 "fp4q_grouped_gemm": [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ci, vp, vp, vp, vp],
             }
             for name, args in sigs.items():
@@ -165,6 +167,18 @@ def fp4q_nv_quantize(x, rows, cols, ld_x, block_axis, rht, rht_seed, rounding, s
         workspace_bytes, _stream(stream)))
 
 
+def fp4q_nv_quantize_2d(x, rows, cols, ld_x, rounding, sr_seed, amax_in, amax_out, tensor_scale_out, q, scales,
+                        layout, workspace, workspace_bytes, stream=None):
+    return _check("fp4q_nv_quantize_2d", load().fp4q_nv_quantize_2d(
+        _ptr(x), rows, cols, ld_x, rounding, sr_seed, _ptr(amax_in), _ptr(amax_out), _ptr(tensor_scale_out),
+        _ptr(q), _ptr(scales), layout, _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def fp4q_fp4_row_to_fp8_col(q, scales, rows, cols, y, tile_scale, stream=None):
+    return _check("fp4q_fp4_row_to_fp8_col", load().fp4q_fp4_row_to_fp8_col(
+        _ptr(q), _ptr(scales), rows, cols, _ptr(y), _ptr(tile_scale), _stream(stream)))
+
+
 def make_operand(q, scales, fmt, tensor_scale=None) -> fp4q_operand:
     return fp4q_operand(_ptr(q), _ptr(scales), fmt, _ptr(tensor_scale))
 
@@ -232,16 +246,20 @@ def _torch():
     return torch
 
 
-def mx_quantize(x, tile_scale=None, layout=FP4Q_SCALES_ROWMAJOR, stream=None):
-    """BF16 / FP32 / float8_e4m3fn [R, C] -> (q uint8 [R, C/2], scales uint8)."""
+def mx_quantize(x, tile_scale=None, layout=FP4Q_SCALES_ROWMAJOR, block_axis=1, stream=None):
+    """BF16 / FP32 / float8_e4m3fn [R, C] -> (q uint8, scales uint8).
+
+    block_axis 1: q [R, C/2], scales of R x C/32.  block_axis 0 (BF16): the
+    quantization of X^T, q [C, R/2], scales of C x R/32."""
     torch = _torch()
     R, C = x.shape
     xt = {torch.bfloat16: FP4Q_BF16, torch.float32: FP4Q_FP32, torch.float8_e4m3fn: FP4Q_E4M3,
           torch.uint8: FP4Q_E4M3}[x.dtype]
-    q = torch.empty((R, C // 2), dtype=torch.uint8, device=x.device)
-    s = torch.empty(fp4q_scales_bytes(R, C // 32, layout), dtype=torch.uint8, device=x.device)
-    fp4q_mx_quantize(x, xt, tile_scale, R, C, x.stride(0), 1, q, s, layout, stream)
-    return q, (s.view(R, C // 32) if layout == FP4Q_SCALES_ROWMAJOR else s)
+    OR, OC = (R, C) if block_axis == 1 else (C, R)
+    q = torch.empty((OR, OC // 2), dtype=torch.uint8, device=x.device)
+    s = torch.empty(fp4q_scales_bytes(OR, OC // 32, layout), dtype=torch.uint8, device=x.device)
+    fp4q_mx_quantize(x, xt, tile_scale, R, C, x.stride(0), block_axis, q, s, layout, stream)
+    return q, (s.view(OR, OC // 32) if layout == FP4Q_SCALES_ROWMAJOR else s)
 
 
 def mx_dequantize(q, s, dtype=None, stream=None):
@@ -251,6 +269,16 @@ def mx_dequantize(q, s, dtype=None, stream=None):
     y = torch.empty((R, C), dtype=dtype, device=q.device)
     fp4q_mx_dequantize(q, s, R, C, 1, y, FP4Q_BF16 if dtype == torch.bfloat16 else FP4Q_FP32, stream)
     return y
+
+
+def fp4_row_to_fp8_col(q, s, stream=None):
+    """Row-wise MXFP4 [R, C] -> (E4M3 of the transpose [C, R], FP32 tile scales [C, R/128])."""
+    torch = _torch()
+    R, C = q.shape[0], q.shape[1] * 2
+    y = torch.empty((C, R), dtype=torch.uint8, device=q.device)
+    ts = torch.empty((C, R // 128), dtype=torch.float32, device=q.device)
+    fp4q_fp4_row_to_fp8_col(q, s, R, C, y, ts, stream)
+    return y, ts
 
 
 def fp4_to_fp8(q, s, stream=None):
@@ -263,19 +291,27 @@ def fp4_to_fp8(q, s, stream=None):
 
 
 def nv_quantize(x, rht=False, rht_seed=0, rounding=FP4Q_RNE, sr_seed=0, amax=None,
-                layout=FP4Q_SCALES_ROWMAJOR, stream=None):
-    """BF16 [R, C] -> dict(q, scales, s_t (device [1]), amax (device [1]))."""
+                layout=FP4Q_SCALES_ROWMAJOR, block_axis=1, two_d=False, stream=None):
+    """BF16 [R, C] -> dict(q, scales, s_t (device [1]), amax (device [1])).
+
+    rht: 0/False none, 1/True random signs from rht_seed, 2 deterministic H16.
+    block_axis 0: the quantization of X^T (q [C, R/2]).  two_d: 16x16 tile
+    scales (fp4q_nv_quantize_2d; no rotation, block_axis 1)."""
     torch = _torch()
     R, C = x.shape
-    q = torch.empty((R, C // 2), dtype=torch.uint8, device=x.device)
-    s = torch.empty(fp4q_scales_bytes(R, C // 16, layout), dtype=torch.uint8, device=x.device)
+    OR, OC = (R, C) if block_axis == 1 else (C, R)
+    q = torch.empty((OR, OC // 2), dtype=torch.uint8, device=x.device)
+    s = torch.empty(fp4q_scales_bytes(OR, OC // 16, layout), dtype=torch.uint8, device=x.device)
     st = torch.empty(1, dtype=torch.float32, device=x.device)
     am = torch.empty(1, dtype=torch.float32, device=x.device)
     wsb = fp4q_nv_quantize_workspace_bytes(R, C)
     ws = torch.empty(wsb, dtype=torch.uint8, device=x.device)
-    fp4q_nv_quantize(x, R, C, x.stride(0), 1, rht, rht_seed, rounding, sr_seed, amax, am, st, q, s, layout,
-                     ws, wsb, stream)
-    return {"q": q, "scales": s.view(R, C // 16) if layout == FP4Q_SCALES_ROWMAJOR else s, "s_t": st,
+    if two_d:
+        fp4q_nv_quantize_2d(x, R, C, x.stride(0), rounding, sr_seed, amax, am, st, q, s, layout, ws, wsb, stream)
+    else:
+        fp4q_nv_quantize(x, R, C, x.stride(0), block_axis, int(rht), rht_seed, rounding, sr_seed, amax, am, st, q,
+                         s, layout, ws, wsb, stream)
+    return {"q": q, "scales": s.view(OR, OC // 16) if layout == FP4Q_SCALES_ROWMAJOR else s, "s_t": st,
             "amax": am}
 
 

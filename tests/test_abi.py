@@ -80,6 +80,17 @@ def test_argument_errors_need_no_gpu(lib):
         with pytest.raises(E) as e:
             fn()
         assert e.value.status == status, (e.value, status)
+    for fn, status in [
+        (lambda: lib.fp4q_nv_quantize_2d(x, 8, 64, 64, 0, 0, None, x, x, x, x, 0, x, 256, stream=0), 2),
+        (lambda: lib.fp4q_nv_quantize(x, 16, 64, 64, 0, 0, 0, 0, 0, None, x, x, x, x, 0, x, 256, 0), 2),
+        (lambda: lib.fp4q_nv_quantize(x, 16, 64, 64, 1, 3, 0, 0, 0, None, x, x, x, x, 0, x, 256, 0), 1),
+        (lambda: lib.fp4q_fp4_row_to_fp8_col(x, x, 16, 64, x, x, stream=0), 2),
+        (lambda: lib.fp4q_fp4_row_to_fp8_col(x + 16, x, 128, 128, x, x, stream=0), 3),
+        (lambda: lib.fp4q_mx_quantize(x, 1, None, 128, 128, 128, 0, x, x, 0, 0), 2),
+    ]:
+        with pytest.raises(E) as e:
+            fn()
+        assert e.value.status == status, (e.value, status)
     for limit in (0, 3_000_000_000):
         with pytest.raises(E) as e:
             lib.fp4q_check_wait_timeout(limit, stream=0)

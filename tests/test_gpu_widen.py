@@ -1,0 +1,183 @@
+"""GPU parity of the column path, the 2D weight scaling and the deterministic
+H16 against the oracle (bit-exact), through the C ABI.
+
+Column-wise quantize (block axis 0) and FP4RowToFP8Col: "Practical FP4
+Training for Large-Scale MoE Models on Hopper GPUs", French summary 2.C and
+Spanish summary 2.  16x16 NVFP4 weight scaling and the RHT on the Wgrad inputs:
+"Pretraining Large Language Models with NVFP4", 2.B.  Deterministic H16:
+"Pretraining large language models with MXFP4 on Native FP4 Hardware", Wgrad
+section.
+"""
+import numpy as np
+import pytest
+
+from _helpers import dev, dev_bf16, from_mma_layout, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fq():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import micro_scaled_fp4_gb300.fp4q as fq
+    fq.load()
+    return fq
+
+
+def _scales(fq, r, rows, scols, layout, key="scales"):
+    sg = host(r[key] if isinstance(r, dict) else r)
+    return from_mma_layout(sg.reshape(-1), rows, scols) if layout else sg
+
+
+# ---------------------------------------------------------------------------
+# deterministic H16 (rht = 2), row-wise
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("rounding", [0, 1])
+def test_nv_quantize_deterministic_h16(fq, oracle, rounding):
+    from micro_scaled_fp4_gb300 import workloads as W
+    x = W.gradient_bf16(129, 2048, seed=5)
+    r = fq.nv_quantize(dev_bf16(x), rht=2, rht_seed=99, rounding=rounding, sr_seed=1234)
+    ref = oracle.nv_quantize(x, rht=2, rounding="sr" if rounding else "rne", sr_seed=1234)
+    assert host(r["amax"])[0] == ref["amax"] and host(r["s_t"])[0] == ref["s_t"]
+    assert np.array_equal(host(r["q"]), ref["q"]) and np.array_equal(host(r["scales"]), ref["s"])
+
+
+# ---------------------------------------------------------------------------
+# column-wise NVFP4 and MXFP4 (block axis 0: quantization of X^T)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(128, 64), (384, 192), (256, 1024)])
+@pytest.mark.parametrize("rht", [0, 1, 2])
+@pytest.mark.parametrize("rounding", [0, 1])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_nv_quantize_column_wise(fq, oracle, shape, rht, rounding, layout):
+    from micro_scaled_fp4_gb300 import workloads as W
+    R, C = shape
+    x = W.gradient_bf16(R, C, seed=R + 3 * C)
+    r = fq.nv_quantize(dev_bf16(x), rht=rht, rht_seed=7, rounding=rounding, sr_seed=1234, layout=layout,
+                       block_axis=0)
+    ref = oracle.nv_quantize_col(x, rht=rht, rht_seed=7, rounding="sr" if rounding else "rne", sr_seed=1234)
+    assert host(r["amax"])[0] == ref["amax"] and host(r["s_t"])[0] == ref["s_t"]
+    assert np.array_equal(host(r["q"]), ref["q"])
+    assert np.array_equal(_scales(fq, r, C, R // 16, layout), ref["s"])
+
+
+@pytest.mark.parametrize("shape", [(128, 128), (384, 256), (256, 1152)])
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("pad", [0, 64])
+def test_mx_quantize_column_wise(fq, oracle, shape, layout, pad):
+    R, C = shape
+    rng = np.random.default_rng(R + C + pad)
+    xf = (rng.standard_normal((R, C)) * np.exp2(rng.integers(-6, 6, (R, 1)))).astype(np.float32)
+    xf[:, 7] *= 40.0
+    xb = ((xf.view(np.uint32) + 0x7FFF + ((xf.view(np.uint32) >> 16) & 1)) >> 16).astype(np.uint16)
+    big = np.zeros((R, C + pad), dtype=np.uint16)
+    big[:, :C] = xb
+    q, s = fq.mx_quantize(dev_bf16(big)[:, :C], layout=layout, block_axis=0)
+    qr, sr = oracle.mx_quantize_col(xb)
+    assert np.array_equal(host(q), qr)
+    assert np.array_equal(_scales(fq, s, C, R // 32, layout), sr)
+
+
+def test_nv_quantize_column_wise_full_size_sampled(fq, oracle):
+    """The 8192x14336 gradient quantized column-wise (the Wgrad operand along
+    the token axis) with the deterministic H16 and SR, then RNE: the tensor
+    amax exactly, 48 sampled output rows (input columns) against the oracle."""
+    from micro_scaled_fp4_gb300 import workloads as W
+    x = W.gradient_bf16()
+    R, C = x.shape
+    xd = dev_bf16(x)
+    amax = oracle.nv_amax(np.ascontiguousarray(x.T), 2, 0)
+    cols = np.sort(np.random.default_rng(1).choice(C, 48, replace=False))
+    for rounding in (1, 0):
+        r = fq.nv_quantize(xd, rht=2, rounding=rounding, sr_seed=1234, block_axis=0)
+        assert host(r["amax"])[0] == np.float32(amax)
+        qg, sg = host(r["q"]), host(r["scales"])
+        for c in cols:
+            ref = oracle.nv_quantize(np.ascontiguousarray(x[:, c:c + 1].T), rht=2, rounding="sr" if rounding else "rne",
+                                     sr_seed=1234, amax=amax, row_offset=int(c))
+            assert np.array_equal(qg[c], ref["q"][0]), c
+            assert np.array_equal(sg[c], ref["s"][0]), c
+
+
+# ---------------------------------------------------------------------------
+# 16x16 NVFP4 weights
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(16, 16), (64, 96), (4096, 7168)])
+@pytest.mark.parametrize("rounding", [0, 1])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_nv_quantize_2d(fq, oracle, shape, rounding, layout):
+    R, C = shape
+    rng = np.random.default_rng(R + C)
+    w = (rng.standard_normal((R, C)) * 0.02).astype(np.float32)
+    w[:, 3] *= 25.0
+    wb = ((w.view(np.uint32) + 0x7FFF + ((w.view(np.uint32) >> 16) & 1)) >> 16).astype(np.uint16)
+    r = fq.nv_quantize(dev_bf16(wb), rounding=rounding, sr_seed=77, layout=layout, two_d=True)
+    ref = oracle.nv_quantize_2d(wb, rounding="sr" if rounding else "rne", sr_seed=77)
+    assert host(r["amax"])[0] == ref["amax"] and host(r["s_t"])[0] == ref["s_t"]
+    assert np.array_equal(host(r["q"]), ref["q"])
+    assert np.array_equal(_scales(fq, r, R, C // 16, layout), ref["s"])
+
+
+def test_nv_2d_forward_and_transposed_weights_agree(fq, oracle):
+    """The property 2D scaling exists for, on the GPU path: quantizing W and W^T
+    gives transposed copies of the same values."""
+    import torch
+    rng = np.random.default_rng(21)
+    w = (rng.standard_normal((256, 512)) * 0.02).astype(np.float32)
+    wt = torch.from_numpy(w).cuda().to(torch.bfloat16)
+    a = fq.nv_quantize(wt, two_d=True)
+    b = fq.nv_quantize(wt.t().contiguous(), two_d=True)
+    da = oracle.nv_dequantize_f64(host(a["q"]), host(a["scales"]), host(a["s_t"])[0])
+    db = oracle.nv_dequantize_f64(host(b["q"]), host(b["scales"]), host(b["s_t"])[0])
+    assert np.array_equal(da, db.T)
+
+
+# ---------------------------------------------------------------------------
+# FP4RowToFP8Col
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(128, 128), (256, 384), (640, 256)])
+def test_fp4_row_to_fp8_col(fq, oracle, shape):
+    R, C = shape
+    rng = np.random.default_rng(R * 7 + C)
+    q = rng.integers(0, 256, (R, C // 2), dtype=np.uint8)
+    s = rng.integers(100, 160, (R, C // 32), dtype=np.uint8)
+    s[::7] = rng.integers(0, 255, (len(s[::7]), C // 32), dtype=np.uint8)   # wide spreads: deep shifts, flushes
+    y, ts = fq.fp4_row_to_fp8_col(dev(q), dev(s))
+    yr, tsr = oracle.mx_to_fp8_col(q, s)
+    assert np.array_equal(host(y), yr)
+    assert np.array_equal(host(ts).view(np.uint32), tsr.view(np.uint32))
+
+
+def test_fp4_row_to_fp8_col_full_size(fq, oracle):
+    """The 8192x7168 FP8 activation after direct FP8 -> MXFP4, converted to the
+    column (Wgrad) FP8 layout: bit-exact over the whole tensor."""
+    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
+    e4, ts = W.fp8_activation()
+    qr, sr = oracle.fp8_to_mx(e4, ts)
+    y, yts = fq.fp4_row_to_fp8_col(dev(qr), dev(sr))
+    yr, ytsr = oracle.mx_to_fp8_col(qr, sr)
+    assert np.array_equal(host(y), yr)
+    assert np.array_equal(host(yts).view(np.uint32), ytsr.view(np.uint32))
+
+
+def test_widen_argument_errors(fq):
+    import torch
+    x = torch.zeros((16, 64), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((16, 32), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((16, 4), dtype=torch.uint8, device="cuda")
+    f = torch.zeros(4, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    cases = [
+        (lambda: fq.fp4q_nv_quantize_2d(x, 8, 64, 64, 0, 0, None, f, f, q, s, 0, ws, 256), 2),       # rows % 16
+        (lambda: fq.fp4q_nv_quantize(x, 16, 64, 64, 0, 0, 0, 0, 0, None, f, f, q, s, 0, ws, 256), 2),  # rows % 128
+        (lambda: fq.fp4q_nv_quantize(x, 16, 64, 64, 1, 3, 0, 0, 0, None, f, f, q, s, 0, ws, 256), 1),  # rht 3
+        (lambda: fq.fp4q_fp4_row_to_fp8_col(q, s, 16, 64, q, f), 2),                                   # rows % 128
+        (lambda: fq.fp4q_mx_quantize(x, 1, None, 128, 128, 128, 0, q, s, 0), 2),                       # FP32 axis 0
+    ]
+    for fn, status in cases:
+        with pytest.raises(fq.Fp4qError) as e:
+            fn()
+        assert e.value.status == status
