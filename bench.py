@@ -205,13 +205,15 @@ def _events(torch, n):
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
 
-ROW_NAMES = ("c1", "c3", "gemm", "moe")
+ROW_NAMES = ("c1", "c3", "gemm", "moe", "col", "nv2d")
 
 
 def main_rows(fq, W, torch, peaks, which=ROW_NAMES, moe_tokens=65536):
     """The other hot-path rows, each timed with CUDA events (inputs > L2 or L2 flushed).
     `which` selects the rows: c1 (MXFP4 round trip), c3 (NVFP4 of a gradient),
-    gemm (dense block-scaled GEMM), moe (MoE expert FFN)."""
+    gemm (dense block-scaled GEMM), moe (MoE expert FFN), col (column path:
+    FP4RowToFP8Col, column-wise quantize, Wgrad GEMM with the deterministic
+    H16), nv2d (16x16-scaled NVFP4 weights)."""
     rows = {}
     stream = torch.cuda.current_stream()
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
@@ -240,6 +242,10 @@ def main_rows(fq, W, torch, peaks, which=ROW_NAMES, moe_tokens=65536):
         c3_row(fq, W, torch, peaks, timed, dev_bf16, rows)
     if "gemm" in which and getattr(lib, "fp4q_block_scaled_gemm", None) is not None:
         gemm_row(fq, W, torch, peaks, timed, dev_bf16, rows)
+    if "col" in which and getattr(lib, "fp4q_fp4_row_to_fp8_col", None) is not None:
+        col_rows(fq, W, torch, peaks, timed, dev_bf16, rows)
+    if "nv2d" in which and getattr(lib, "fp4q_nv_quantize_2d", None) is not None:
+        nv2d_row(fq, W, torch, peaks, timed, rows)
     torch.cuda.empty_cache()
     if "moe" in which and getattr(lib, "fp4q_grouped_gemm", None) is not None:
         rows[f"moe_ffn_{moe_tokens}x7168_top8_of_64"] = moe_row(fq, W, torch, peaks, timed, moe_tokens)
@@ -340,6 +346,100 @@ def gemm_row(fq, W, torch, peaks, timed, dev_bf16, rows):
         "peak_source": f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
         "mx_quantize_operand_ms": round(ms_qa, 4)}
     del ad, bd, qa, sa, qb, sb, D, ra, rb
+
+
+def col_rows(fq, W, torch, peaks, timed, dev_bf16, rows):
+    """Column path (the weight-gradient operands): FP4RowToFP8Col on the FP8
+    activation's MXFP4 form (8192x7168), column-wise NVFP4 of the 8192x14336
+    gradient with the deterministic H16 (SR and RNE passes) and column-wise
+    MXFP4 of a BF16 8192x8192 tensor, and the Wgrad GEMM dW = dY^T X
+    (8192 tokens, 8192 x 8192) on column-wise H16 NVFP4 operands."""
+    hbm = peaks["hbm_gbs"]
+    stream = torch.cuda.current_stream()
+    e4, ts = W.fp8_activation(ROWS, COLS)
+    x8, t8 = torch.from_numpy(e4).cuda(), torch.from_numpy(ts).cuda()
+    q, s = fq.mx_quantize(x8, tile_scale=t8)
+    y = torch.empty((COLS, ROWS), dtype=torch.uint8, device="cuda")
+    yt = torch.empty((COLS, ROWS // 128), dtype=torch.float32, device="cuda")
+    ms = timed(lambda: fq.fp4q_fp4_row_to_fp8_col(q, s, ROWS, COLS, y, yt, stream), 10, True)
+    nb = bytes_mx_to_fp8(ROWS, COLS)
+    row_ms = timed(lambda: fq.fp4q_fp4_to_fp8(q, s, ROWS, COLS, 1, y, yt, stream), 10, True)
+    rows["f1_fp4_row_to_fp8_col_8192x7168"] = {
+        "ms": round(ms, 4), "GB_per_s": round(nb / ms / 1e6, 1), "frac_hbm": round(nb / ms / 1e6 / hbm, 3),
+        "row_layout_ms": round(row_ms, 4), "row_layout_GB_per_s": round(nb / row_ms / 1e6, 1)}
+    del x8, t8, q, s, y, yt
+
+    R3, C3 = 8192, 14336
+    xg = dev_bf16(W.gradient_bf16(R3, C3))
+    q3 = torch.empty((C3, R3 // 2), dtype=torch.uint8, device="cuda")
+    s3 = torch.empty((C3, R3 // 16), dtype=torch.uint8, device="cuda")
+    st = torch.empty(1, dtype=torch.float32, device="cuda")
+    am = torch.empty(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+
+    def c3col(rounding, amax_in=None):
+        fq.fp4q_nv_quantize(xg, R3, C3, C3, 0, 2, 0, rounding, 1234, amax_in, am, st, q3, s3, 0, ws, 256, stream)
+    b_amax = R3 * C3 * 2
+    b_quant = R3 * C3 * 2 + R3 * C3 // 2 + R3 * C3 // 16
+    ms_sr = timed(lambda: c3col(fq.FP4Q_SR), 10, True)
+    ms_rne = timed(lambda: c3col(fq.FP4Q_RNE), 10, True)
+    amax_dev = am.clone()
+    ms_sr1 = timed(lambda: c3col(fq.FP4Q_SR, amax_dev), 10, True)
+    ms_rne1 = timed(lambda: c3col(fq.FP4Q_RNE, amax_dev), 10, True)
+    rows["f1_f3_nvfp4_col_h16_8192x14336"] = {
+        "sr_two_pass_ms": round(ms_sr, 4), "rne_two_pass_ms": round(ms_rne, 4),
+        "sr_quant_pass_GB_per_s": round(b_quant / ms_sr1 / 1e6, 1),
+        "rne_quant_pass_GB_per_s": round(b_quant / ms_rne1 / 1e6, 1),
+        "rne_two_pass_GB_per_s": round((b_amax + b_quant) / ms_rne / 1e6, 1),
+        "frac_hbm_rne_quant_pass": round(b_quant / ms_rne1 / 1e6 / hbm, 3),
+        "frac_hbm_sr_quant_pass": round(b_quant / ms_sr1 / 1e6 / hbm, 3)}
+    del xg, q3, s3
+
+    a, b = W.gemm_operands()
+    ad, bd = dev_bf16(a), dev_bf16(b)
+    qa = torch.empty((8192, 4096), dtype=torch.uint8, device="cuda")
+    sa = torch.empty((8192, 256), dtype=torch.uint8, device="cuda")
+    ms_mx = timed(lambda: fq.fp4q_mx_quantize(ad, fq.FP4Q_BF16, None, 8192, 8192, 8192, 0, qa, sa, 0, stream), 10,
+                  True)
+    nbq = 8192 * 8192 * (2 + 0.5 + 1 / 32)
+    rows["f1_mxfp4_col_bf16_8192x8192"] = {"ms": round(ms_mx, 4), "GB_per_s": round(nbq / ms_mx / 1e6, 1),
+                                           "frac_hbm": round(nbq / ms_mx / 1e6 / hbm, 3)}
+    # Wgrad: tokens along K for both operands (rows of a and b are the tokens here)
+    ra = fq.nv_quantize(ad, rht=2, layout=fq.FP4Q_SCALES_MMA, block_axis=0)
+    rb = fq.nv_quantize(bd, rht=2, layout=fq.FP4Q_SCALES_MMA, block_axis=0)
+    D = torch.empty((8192, 8192), dtype=torch.bfloat16, device="cuda")
+    An = fq.make_operand(ra["q"], ra["scales"], fq.FP4Q_NVFP4, ra["s_t"])
+    Bn = fq.make_operand(rb["q"], rb["scales"], fq.FP4Q_NVFP4, rb["s_t"])
+    ms_g = timed(lambda: fq.fp4q_block_scaled_gemm(An, Bn, 8192, 8192, 8192, D, fq.FP4Q_BF16, 8192, stream), 10, True)
+    peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    flops = 2.0 * 8192 ** 3
+    rows["f3_wgrad_h16_gemm_8192^3"] = {"ms": round(ms_g, 4), "TFLOPS": round(flops / ms_g / 1e9, 1),
+                                        "frac_peak": round(flops / ms_g / 1e9 / peak, 3)}
+    del ad, bd, qa, sa, ra, rb, D
+
+
+def nv2d_row(fq, W, torch, peaks, timed, rows):
+    """16x16-scaled NVFP4 of BF16 weights: one expert's W1 slab, 4096 x 7168,
+    times 8 (a 32768 x 7168 stack), RNE, two passes and quantize pass."""
+    stream = torch.cuda.current_stream()
+    R, C = 8 * 4096, 7168
+    w = W.moe_weights_torch(1, R, C, 10, "cuda")[0]
+    q = torch.empty((R, C // 2), dtype=torch.uint8, device="cuda")
+    s = torch.empty((R, C // 16), dtype=torch.uint8, device="cuda")
+    st = torch.empty(1, dtype=torch.float32, device="cuda")
+    am = torch.empty(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    ms2 = timed(lambda: fq.fp4q_nv_quantize_2d(w, R, C, C, fq.FP4Q_RNE, 0, None, am, st, q, s, 0, ws, 256, stream),
+                10, True)
+    amax_dev = am.clone()
+    ms1 = timed(lambda: fq.fp4q_nv_quantize_2d(w, R, C, C, fq.FP4Q_RNE, 0, amax_dev, am, st, q, s, 0, ws, 256,
+                                               stream), 10, True)
+    b_quant = R * C * (2 + 0.5 + 1 / 16)
+    rows["f2_nvfp4_2d_weights_32768x7168"] = {
+        "two_pass_ms": round(ms2, 4), "quant_pass_ms": round(ms1, 4),
+        "quant_pass_GB_per_s": round(b_quant / ms1 / 1e6, 1),
+        "frac_hbm_quant_pass": round(b_quant / ms1 / 1e6 / peaks["hbm_gbs"], 3)}
+    del w, q, s
 
 
 def moe_row(fq, W, torch, peaks, timed, T=65536):

@@ -181,3 +181,30 @@ def test_widen_argument_errors(fq):
         with pytest.raises(fq.Fp4qError) as e:
             fn()
         assert e.value.status == status
+
+
+# ---------------------------------------------------------------------------
+# Wgrad with the deterministic H16: dW = dY^T X, both operands quantized along
+# the token axis (column-wise) with the same rotation, NVFP4 GEMM
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("rounding", [0, 1])
+def test_wgrad_deterministic_h16(fq, oracle, rounding):
+    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
+    T, H, I = 512, 256, 384                       # tokens (K), output rows, output cols
+    dy = W.gradient_bf16(T, H, seed=31)
+    x = W.gradient_bf16(T, I, seed=32, scale=1.0)
+    ra = fq.nv_quantize(dev_bf16(dy), rht=2, rounding=rounding, sr_seed=5, layout=fq.FP4Q_SCALES_MMA, block_axis=0)
+    rb = fq.nv_quantize(dev_bf16(x), rht=2, rounding=rounding, sr_seed=6, layout=fq.FP4Q_SCALES_MMA, block_axis=0)
+    d32 = fq.gemm(ra["q"], ra["scales"], rb["q"], rb["scales"], fq.FP4Q_NVFP4, ra["s_t"], rb["s_t"],
+                  out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fq.fp4q_device_status() == 0
+    oa = oracle.nv_quantize_col(dy, rht=2, rounding="sr" if rounding else "rne", sr_seed=5)
+    ob = oracle.nv_quantize_col(x, rht=2, rounding="sr" if rounding else "rne", sr_seed=6)
+    assert np.array_equal(host(ra["q"]), oa["q"]) and np.array_equal(host(rb["q"]), ob["q"])
+    ref = oracle.nv_gemm_ref(oa["q"], oa["s"], oa["s_t"], ob["q"], ob["s"], ob["s_t"])
+    assert oracle.rel_frobenius(host(d32).astype(np.float64), ref) <= 1e-3
+    # the rotation cancels along the token axis: the product tracks dY^T X up to FP4 error
+    exact = oracle.bf16_bits_to_f32(dy).astype(np.float64).T @ oracle.bf16_bits_to_f32(x).astype(np.float64)
+    assert oracle.rel_frobenius(host(d32).astype(np.float64), exact) < 0.2
