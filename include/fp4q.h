@@ -70,7 +70,7 @@ typedef enum fp4q_status {
 typedef enum fp4q_dtype { FP4Q_BF16 = 0, FP4Q_FP32 = 1, FP4Q_E4M3 = 2 } fp4q_dtype;
 typedef enum fp4q_scale_layout { FP4Q_SCALES_ROWMAJOR = 0, FP4Q_SCALES_MMA = 1 } fp4q_scale_layout;
 typedef enum fp4q_rounding { FP4Q_RNE = 0, FP4Q_SR = 1 } fp4q_rounding;
-typedef enum fp4q_format { FP4Q_MXFP4 = 0, FP4Q_NVFP4 = 1 } fp4q_format;
+typedef enum fp4q_format { FP4Q_MXFP4 = 0, FP4Q_NVFP4 = 1, FP4Q_MXFP8 = 2 } fp4q_format;
 
 /* Human-readable name of a status code (static string). */
 const char* fp4q_status_string(fp4q_status status);
@@ -213,11 +213,28 @@ fp4q_status fp4q_fp4_row_to_fp8_col(const uint8_t* q, const uint8_t* scales, int
                                     int64_t cols, uint8_t* y, float* tile_scale,
                                     fp4q_stream_t stream);
 
+/*
+ * fp4q_fp8_tile_scales_to_e8m0 -- FP32 power-of-two scales, one per 1x128 tile
+ * (what fp4q_fp4_to_fp8 and fp4q_fp4_row_to_fp8_col write), -> E8M0 block
+ * scales, one per 32 elements, so that their FP8 output feeds
+ * fp4q_block_scaled_gemm as FP4Q_MXFP8 operands with no rounding: [HOP]
+ * section 1 and Spanish section 2 (FP4 storage, FP8 compute; the FP8 copy of
+ * an MXFP4 tensor carries a power-of-two tile scale, so E8M0 holds it exactly).
+ * A scale that is not a power of two in [2^-127, 2^127] gives 0xFF and sets
+ * bit 3 of the device status word.
+ *   tile_scale  device FP32 [rows, cols/128];  cols % 128 == 0
+ *   scales      device out, E8M0 (rows x cols/32) in `layout`
+ */
+fp4q_status fp4q_fp8_tile_scales_to_e8m0(const float* tile_scale, int64_t rows, int64_t cols,
+                                         uint8_t* scales, fp4q_scale_layout layout, fp4q_stream_t stream);
+
 /* One FP4 GEMM operand.  Host struct; the pointers in it are device pointers. */
 typedef struct fp4q_operand {
-    const uint8_t* q;           /* packed E2M1 [rows, K/2], row stride K/2 bytes      */
+    const uint8_t* q;           /* packed E2M1 [rows, K/2] (row stride K/2 bytes), or
+                                   E4M3 [rows, K] for MXFP8                           */
     const uint8_t* scales;      /* block scales in FP4Q_SCALES_MMA layout              */
-    fp4q_format format;         /* MXFP4: E8M0 per 32; NVFP4: E4M3 per 16              */
+    fp4q_format format;         /* MXFP4: E8M0 per 32; NVFP4: E4M3 per 16;
+                                   MXFP8: E8M0 per 32                                 */
     const float* tensor_scale;  /* NVFP4: device FP32 scalar s_t; MXFP4: NULL          */
 } fp4q_operand;
 
@@ -226,7 +243,11 @@ typedef struct fp4q_operand {
  * [MXN] investigation section: the forward GEMM of a linear layer, Y = X W^T,
  * with both operands FP4 along the reduction axis K.  [NVF] 2.B: for NVFP4
  * operands the result is scaled by s_tA * s_tB, and a Hadamard rotation
- * applied to both operands along K cancels in the product.
+ * applied to both operands along K cancels in the product.  FP4Q_MXFP8
+ * operands (E4M3 codes with E8M0 scales per 32, kind::mxf8f6f4) are the FP8
+ * consumer of fp4q_fp4_to_fp8 / fp4q_fp4_row_to_fp8_col ([HOP] section 1:
+ * FP4 storage, FP8 GEMMs); their scales come from
+ * fp4q_fp8_tile_scales_to_e8m0.
  *   A, B     operands of the same format; A has M rows, B has N rows, both K columns
  *   K        multiple of 128;  M, N >= 1
  *   D        device out, [M, ldd] of d_type (FP4Q_BF16, RNE from FP32, or FP4Q_FP32),
@@ -349,7 +370,8 @@ fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_scales, const
  * the last reset, else a bit mask of the kernels that gave up (FP4Q_ERR_TIMEOUT
  * is returned in that case): bit 0 fp4q_block_scaled_gemm, bit 1
  * fp4q_grouped_gemm, bit 2 the shared-memory-staged conversions of
- * fp4q_mx_quantize (E4M3 source) and fp4q_fp4_to_fp8, bit 31
+ * fp4q_mx_quantize (E4M3 source) and fp4q_fp4_to_fp8, bit 3 a tile scale
+ * fp4q_fp8_tile_scales_to_e8m0 could not convert, bit 31
  * fp4q_check_wait_timeout.  Synchronous: waits for the device first.
  */
 fp4q_status fp4q_device_status(uint32_t* status_out, int reset);

@@ -36,6 +36,7 @@ enum : uint32_t {
     kStatusGemmTimeout = 1u << 0,
     kStatusGroupedTimeout = 1u << 1,
     kStatusStreamTimeout = 1u << 2,
+    kStatusBadTileScale = 1u << 3,
     kStatusSelfCheck = 1u << 31
 };
 

@@ -269,10 +269,57 @@ __global__ void __launch_bounds__(256) fp4_row_to_fp8_col_kernel(
     }
 }
 
+// FP32 power-of-two tile scales (one per 1x128 tile, as fp4_to_fp8 and
+// fp4_row_to_fp8_col write them) -> E8M0 block scales, one per 32 elements
+// (the tile's exponent repeated over its four blocks), for the MXFP8 GEMM.
+// Exact: 2^e is E8M0 byte e + 127.  Anything that is not a power of two in
+// [2^-127, 2^127] gives 0xFF (NaN) and sets a status bit.
+__global__ void __launch_bounds__(256) fp8_tile_scales_to_e8m0_kernel(
+    const float* __restrict__ tile_scale, int64_t rows, uint32_t tiles_per_row, uint8_t* __restrict__ s,
+    int mma_layout, uint32_t* status) {
+    const int64_t n = rows * int64_t(tiles_per_row);
+    const uint32_t bpr = tiles_per_row * 4;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+        const uint32_t u = f2u(tile_scale[i]);
+        const uint32_t ef = u >> 23;
+        uint32_t b;
+        if (u == 0x00400000u) b = 0u;                                  // 2^-127 (FP32 subnormal)
+        else if ((u & 0x007fffffu) == 0 && ef >= 1u && ef <= 254u) b = ef;
+        else { b = 0xffu; atomicOr(status, kStatusBadTileScale); }
+        const int64_t r = i / tiles_per_row;
+        const uint32_t t = uint32_t(i - r * tiles_per_row);
+#pragma unroll
+        for (uint32_t k = 0; k < 4; ++k) {
+            const uint32_t c = 4 * t + k;
+            s[mma_layout ? mma_scale_offset(uint64_t(r), c, bpr) : uint64_t(r) * bpr + c] = uint8_t(b);
+        }
+    }
+}
+
 }  // namespace
 }  // namespace fp4q
 
 using namespace fp4q;
+
+extern "C" fp4q_status fp4q_fp8_tile_scales_to_e8m0(const float* tile_scale, int64_t rows, int64_t cols,
+                                                   uint8_t* scales, fp4q_scale_layout layout, fp4q_stream_t stream) {
+    if (rows < 0 || cols < 0) return fail(FP4Q_ERR_INVALID_ARGUMENT, "fp8_tile_scales_to_e8m0: negative size");
+    if (cols % 128) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "fp8_tile_scales_to_e8m0: cols %% 128 != 0");
+    if (layout != FP4Q_SCALES_ROWMAJOR && layout != FP4Q_SCALES_MMA)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "fp8_tile_scales_to_e8m0: bad scale layout");
+    if (rows == 0 || cols == 0) return FP4Q_OK;
+    if (!tile_scale || !scales) return fail(FP4Q_ERR_INVALID_ARGUMENT, "fp8_tile_scales_to_e8m0: null pointer");
+    if (reinterpret_cast<uintptr_t>(tile_scale) & 3u)
+        return fail(FP4Q_ERR_MISALIGNED, "fp8_tile_scales_to_e8m0: tile_scale 4-byte aligned");
+    int sms = 0;
+    fp4q_status st = current_device(&sms);
+    if (st != FP4Q_OK) return st;
+    const int64_t n = rows * (cols / 128);
+    const int64_t grid = std::min<int64_t>((n + 255) / 256, int64_t(sms) * 8);
+    fp8_tile_scales_to_e8m0_kernel<<<unsigned(grid), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        tile_scale, rows, uint32_t(cols / 128), scales, layout == FP4Q_SCALES_MMA, status_word());
+    return check_launch("fp8_tile_scales_to_e8m0");
+}
 
 extern "C" fp4q_status fp4q_fp4_row_to_fp8_col(const uint8_t* q, const uint8_t* scales, int64_t rows,
                                                int64_t cols, uint8_t* y, float* tile_scale,

@@ -72,7 +72,9 @@ struct GemmArgs {
     int M, N, K;
     int n_tiles;                     // output tiles along N
     int k_stages;
-    int nv;                          // 0 = MXFP4 (UE8M0 / 32), 1 = UE4M3 / 16
+    int nv;                          // 0 = MXFP4 / MXFP8 (UE8M0 / 32), 1 = NVFP4 (UE4M3 / 16)
+    int f8;                          // 1 = MXFP8 operands (E4M3, one byte per element)
+    int bk;                          // K elements per stage: 256 (FP4) or 128 (FP8); 128 bytes per row either way
     int groups;                      // 0 = dense
     const int64_t* offsets;          // grouped: [groups + 1] row offsets
     const uint8_t* sfa;
@@ -227,17 +229,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     ok = false;
                     break;
                 }
-                const int k_elems = min(BK, args.K - kb * BK);
+                const int k_elems = min(args.bk, args.K - kb * args.bk);
                 const uint32_t chunks = uint32_t(k_elems) / chunk_elems;
-                const uint64_t ct0 = uint64_t(kb * BK) / chunk_elems;
+                const uint64_t ct0 = uint64_t(kb) * uint64_t(args.bk) / chunk_elems;
                 const uint32_t sf_bytes = chunks * 512u * (t.b_row1 >= 0 ? 3u : 2u);
                 uint8_t* st = smem + stage * STAGE_BYTES;
                 const uint32_t fb = full_bar(stage);
                 tc::mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + sf_bytes);
-                tc::tma_load_2d(tc::smem_u32(st), &tmap_a, fb, kb * (BK / 2), t.a_row0);
-                tc::tma_load_2d(tc::smem_u32(st + A_BYTES), &tmap_b, fb, kb * (BK / 2), t.b_row0);
+                // x coordinate in bytes: 128 bytes of K per stage for both element widths
+                tc::tma_load_2d(tc::smem_u32(st), &tmap_a, fb, kb * 128, t.a_row0);
+                tc::tma_load_2d(tc::smem_u32(st + A_BYTES), &tmap_b, fb, kb * 128, t.b_row0);
                 // an absent second half still lands: rows past the end are zero-filled
-                tc::tma_load_2d(tc::smem_u32(st + A_BYTES + B_HALF_BYTES), &tmap_b, fb, kb * (BK / 2),
+                tc::tma_load_2d(tc::smem_u32(st + A_BYTES + B_HALF_BYTES), &tmap_b, fb, kb * 128,
                                 t.b_row1 >= 0 ? t.b_row1 : t.b_row0 + 128);
                 tc::bulk_load(tc::smem_u32(st + A_BYTES + B_BYTES),
                               args.sfa + uint64_t(t.a_sf_tile) * args.sf_tile_stride + ct0 * 512u, chunks * 512u, fb);
@@ -271,6 +274,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         const uint32_t idesc_nv = tc::idesc_block_scaled(BM, BN, false, 0, 0);
         const uint32_t idesc_mx0 = tc::idesc_block_scaled(BM, BN, true, 0, 0);
         const uint32_t idesc_mx1 = tc::idesc_block_scaled(BM, BN, true, 2, 2);
+        // MXFP8 (kind::mxf8f6f4, one UE8M0 byte per 32 elements): MMA j of a stage
+        // reads byte j of the stage's scale column
+        const uint32_t idesc_f8_0 = tc::idesc_block_scaled(BM, BN, true, 0, 0, 0, 0);
+        const uint32_t idesc_f8_1 = tc::idesc_block_scaled(BM, BN, true, 1, 1, 0, 0);
+        const uint32_t idesc_f8_2 = tc::idesc_block_scaled(BM, BN, true, 2, 2, 0, 0);
+        const uint32_t idesc_f8_3 = tc::idesc_block_scaled(BM, BN, true, 3, 3, 0, 0);
         int stage = 0;
         uint32_t phase = 0;
         int tcount = 0;
@@ -292,13 +301,23 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     ok = false;
                     break;
                 }
-                const int k_elems = min(BK, args.K - kb * BK);
+                const int k_elems = min(args.bk, args.K - kb * args.bk);
                 // descriptors of this stage: the 14-bit address field (bytes >> 4)
                 // of the stage-0 descriptors advanced by the stage offset
                 const uint32_t so = uint32_t(stage) * (STAGE_BYTES >> 4);
                 const uint32_t a_lo = d_lo0 + so, b_lo = d_lo0 + so + (A_BYTES >> 4);
                 const uint32_t sfa_lo = sf_lo0 + so, sfb_lo = sf_lo0 + so + (SFA_BYTES >> 4);
-                if (k_elems == BK) {
+                if (args.f8) {
+                    // 128 FP8 elements: one scale chunk (A) and one per B half, four K = 32 MMAs
+                    tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFA, tc::desc_from(sfa_lo, sf_hi));
+                    tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB, tc::desc_from(sfb_lo, sf_hi));
+                    tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 4, tc::desc_from(sfb_lo + 128, sf_hi));
+                    const uint32_t id[4] = {idesc_f8_0, idesc_f8_1, idesc_f8_2, idesc_f8_3};
+#pragma unroll
+                    for (uint32_t j = 0; j < 4; ++j)
+                        tc::mma_mxf8(tmem, tc::desc_from(a_lo + 2 * j, d_hi), tc::desc_from(b_lo + 2 * j, d_hi), id[j],
+                                     tmem + TMEM_SFA, tmem + TMEM_SFB, (kb | int(j)) ? 1u : 0u);
+                } else if (k_elems == BK) {
                     if (args.nv) {
 #pragma unroll
                         for (uint32_t c = 0; c < 4; ++c) {
@@ -542,10 +561,11 @@ fp4q_status get_encoder() {
     return FP4Q_OK;
 }
 
-// 2D map over packed FP4 bytes [rows, K/2]: 128-byte x 128-row boxes, 128B swizzle.
-fp4q_status encode_operand_map(CUtensorMap* map, const uint8_t* q, int64_t rows, int64_t K) {
-    cuuint64_t dims[2] = {cuuint64_t(K / 2), cuuint64_t(rows)};
-    cuuint64_t strides[1] = {cuuint64_t(K / 2)};
+// 2D map over operand bytes [rows, row_bytes] (K/2 for FP4, K for FP8):
+// 128-byte x 128-row boxes, 128B swizzle.
+fp4q_status encode_operand_map(CUtensorMap* map, const uint8_t* q, int64_t rows, int64_t row_bytes) {
+    cuuint64_t dims[2] = {cuuint64_t(row_bytes), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
     cuuint32_t box[2] = {128u, 128u};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(q), dims, strides, box, estr,
@@ -595,8 +615,8 @@ extern "C" fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_
                                               int64_t N, int64_t K, void* D, fp4q_dtype d_type, int64_t ldd,
                                               fp4q_stream_t stream) {
     if (!A || !B) return fail(FP4Q_ERR_INVALID_ARGUMENT, "gemm: operand is NULL");
-    if (A->format != B->format || (A->format != FP4Q_MXFP4 && A->format != FP4Q_NVFP4))
-        return fail(FP4Q_ERR_INVALID_ARGUMENT, "gemm: A and B must both be MXFP4 or both NVFP4");
+    if (A->format != B->format || (A->format != FP4Q_MXFP4 && A->format != FP4Q_NVFP4 && A->format != FP4Q_MXFP8))
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "gemm: A and B must have the same format (MXFP4, NVFP4 or MXFP8)");
     if (d_type != FP4Q_BF16 && d_type != FP4Q_FP32)
         return fail(FP4Q_ERR_INVALID_ARGUMENT, "gemm: d_type must be BF16 or FP32");
     if (M < 0 || N < 0 || K < 0 || ldd < N) return fail(FP4Q_ERR_INVALID_ARGUMENT, "gemm: bad sizes");
@@ -623,14 +643,18 @@ extern "C" fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_
     if (st != FP4Q_OK) return st;
     if ((st = get_encoder()) != FP4Q_OK) return st;
     CUtensorMap ma, mb;
-    if ((st = encode_operand_map(&ma, A->q, M, K)) != FP4Q_OK) return st;
-    if ((st = encode_operand_map(&mb, B->q, N, K)) != FP4Q_OK) return st;
+    const bool f8 = A->format == FP4Q_MXFP8;
+    const int64_t row_bytes = f8 ? K : K / 2;
+    if ((st = encode_operand_map(&ma, A->q, M, row_bytes)) != FP4Q_OK) return st;
+    if ((st = encode_operand_map(&mb, B->q, N, row_bytes)) != FP4Q_OK) return st;
     GemmArgs a = {};
     a.M = int(M);
     a.N = int(N);
     a.K = int(K);
     a.n_tiles = int((N + BN - 1) / BN);
-    a.k_stages = int((K + BK - 1) / BK);
+    a.f8 = f8 ? 1 : 0;
+    a.bk = f8 ? 128 : BK;
+    a.k_stages = int((K + a.bk - 1) / a.bk);
     a.nv = nv ? 1 : 0;
     a.groups = 0;
     a.sfa = A->scales;
@@ -679,12 +703,13 @@ extern "C" fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sc
     if (st != FP4Q_OK) return st;
     if ((st = get_encoder()) != FP4Q_OK) return st;
     CUtensorMap ma, mb;
-    if ((st = encode_operand_map(&ma, a_q, rows, K)) != FP4Q_OK) return st;
-    if ((st = encode_operand_map(&mb, b_q, groups * N, K)) != FP4Q_OK) return st;
+    if ((st = encode_operand_map(&ma, a_q, rows, K / 2)) != FP4Q_OK) return st;
+    if ((st = encode_operand_map(&mb, b_q, groups * N, K / 2)) != FP4Q_OK) return st;
     GemmArgs a = {};
     a.M = int(rows);
     a.N = int(N);
     a.K = int(K);
+    a.bk = BK;
     a.k_stages = int((K + BK - 1) / BK);
     a.nv = 1;
     a.groups = int(groups);

@@ -165,9 +165,12 @@ __device__ __forceinline__ uint64_t desc_from(uint32_t lo, uint32_t hi) {
 // B scale id [4,6), A type [7,10) and B type [10,13) (E2M1 = 1), K-major A
 // and B (bits 15, 16 = 0), N >> 3 in [17,23), scale type bit 23 (1 = UE8M0,
 // 0 = UE4M3), M >> 4 in [24,29), A scale id [29,31).
+// The element type codes: E2M1 = 1 for kind::mxf4 / mxf4nvf4; E4M3 = 0 for
+// kind::mxf8f6f4.
 __host__ __device__ constexpr uint32_t idesc_block_scaled(uint32_t m, uint32_t n, bool ue8m0,
-                                                          uint32_t a_sf_id, uint32_t b_sf_id) {
-    return (b_sf_id << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((ue8m0 ? 1u : 0u) << 23) |
+                                                          uint32_t a_sf_id, uint32_t b_sf_id,
+                                                          uint32_t a_type = 1, uint32_t b_type = 1) {
+    return (b_sf_id << 4) | (a_type << 7) | (b_type << 10) | ((n >> 3) << 17) | ((ue8m0 ? 1u : 0u) << 23) |
            ((m >> 4) << 24) | (a_sf_id << 29);
 }
 
@@ -181,6 +184,13 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d, uint64_t a, uint64_t b, uin
                                          uint32_t sfb, uint32_t accumulate) {
     asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
                  " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n}"
+                 :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
+}
+// FP8 E4M3 x E4M3 with one UE8M0 scale per 32 elements of K (K = 32 per MMA).
+__device__ __forceinline__ void mma_mxf8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                         uint32_t sfb, uint32_t accumulate) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+                 " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}"
                  :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
 }
 // 32 rows x 128 bits of shared memory -> TMEM, replicated to the four

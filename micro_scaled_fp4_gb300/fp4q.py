@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "FP4Q_OK", 1: "FP4Q_ERR_INVALID_ARGUMENT", 2: "FP4Q_ERR_UNSUP
 FP4Q_BF16, FP4Q_FP32, FP4Q_E4M3 = 0, 1, 2
 FP4Q_SCALES_ROWMAJOR, FP4Q_SCALES_MMA = 0, 1
 FP4Q_RNE, FP4Q_SR = 0, 1
-FP4Q_MXFP4, FP4Q_NVFP4 = 0, 1
+FP4Q_MXFP4, FP4Q_NVFP4, FP4Q_MXFP8 = 0, 1, 2
 
 FP4Q_EPI_STORE_BF16, FP4Q_EPI_SILU_GATE_MXFP4 = 0, 1
 
@@ -33,6 +33,7 @@ EXPORTED = [
     "fp4q_block_scaled_gemm", "fp4q_device_status", "fp4q_moe_dispatch_workspace_bytes",
     "fp4q_moe_dispatch", "fp4q_rebased_scales_bytes", "fp4q_mx_rebase_scales", "fp4q_grouped_gemm",
     "fp4q_moe_dispatch_static", "fp4q_check_wait_timeout", "fp4q_nv_quantize_2d", "fp4q_fp4_row_to_fp8_col",
+    "fp4q_fp8_tile_scales_to_e8m0",
 ]
 MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 * 1024 * 1024
 
@@ -94,6 +95,7 @@ def load() -> ctypes.CDLL:
                 "fp4q_check_wait_timeout": [u64, vp],
                 "fp4q_nv_quantize_2d": [vp, i64, i64, i64, ci, u64, vp, vp, vp, vp, vp, ci, vp, ctypes.c_size_t, vp],
                 "fp4q_fp4_row_to_fp8_col": [vp, vp, i64, i64, vp, vp, vp],
+                "fp4q_fp8_tile_scales_to_e8m0": [vp, i64, i64, vp, ci, vp],
                 "fp4q_grouped_gemm": [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ci, vp, vp, vp, vp],
             }
             for name, args in sigs.items():
@@ -177,6 +179,11 @@ def fp4q_nv_quantize_2d(x, rows, cols, ld_x, rounding, sr_seed, amax_in, amax_ou
 def fp4q_fp4_row_to_fp8_col(q, scales, rows, cols, y, tile_scale, stream=None):
     return _check("fp4q_fp4_row_to_fp8_col", load().fp4q_fp4_row_to_fp8_col(
         _ptr(q), _ptr(scales), rows, cols, _ptr(y), _ptr(tile_scale), _stream(stream)))
+
+
+def fp4q_fp8_tile_scales_to_e8m0(tile_scale, rows, cols, scales, layout, stream=None):
+    return _check("fp4q_fp8_tile_scales_to_e8m0", load().fp4q_fp8_tile_scales_to_e8m0(
+        _ptr(tile_scale), rows, cols, _ptr(scales), layout, _stream(stream)))
 
 
 def make_operand(q, scales, fmt, tensor_scale=None) -> fp4q_operand:
@@ -271,6 +278,15 @@ def mx_dequantize(q, s, dtype=None, stream=None):
     return y
 
 
+def fp8_mma_scales(tile_scale, stream=None):
+    """FP32 power-of-two 1x128 tile scales [R, C/128] -> E8M0 per 32 in the MMA layout."""
+    torch = _torch()
+    R, C = tile_scale.shape[0], tile_scale.shape[1] * 128
+    s = torch.empty(fp4q_scales_bytes(R, C // 32, FP4Q_SCALES_MMA), dtype=torch.uint8, device=tile_scale.device)
+    fp4q_fp8_tile_scales_to_e8m0(tile_scale, R, C, s, FP4Q_SCALES_MMA, stream)
+    return s
+
+
 def fp4_row_to_fp8_col(q, s, stream=None):
     """Row-wise MXFP4 [R, C] -> (E4M3 of the transpose [C, R], FP32 tile scales [C, R/128])."""
     torch = _torch()
@@ -316,15 +332,15 @@ def nv_quantize(x, rht=False, rht_seed=0, rounding=FP4Q_RNE, sr_seed=0, amax=Non
 
 
 def gemm(qa, sa, qb, sb, fmt=FP4Q_MXFP4, ts_a=None, ts_b=None, out_dtype=None, stream=None):
-    """D = A . B^T for packed FP4 operands with MMA-layout scales.
+    """D = A . B^T for packed FP4 (or MXFP8) operands with MMA-layout scales.
 
-    qa [M, K/2], qb [N, K/2] uint8; sa / sb scale buffers in FP4Q_SCALES_MMA
+    qa [M, K/2], qb [N, K/2] uint8 ([M, K], [N, K] E4M3 for MXFP8); sa / sb scale buffers in FP4Q_SCALES_MMA
     layout; ts_a / ts_b device FP32 [1] tensor scales for NVFP4.  Returns a
     [M, N] view of a row-padded output (row stride a multiple of 16 bytes).
     """
     torch = _torch()
     out_dtype = out_dtype or torch.bfloat16
-    M, N, K = qa.shape[0], qb.shape[0], qa.shape[1] * 2
+    M, N, K = qa.shape[0], qb.shape[0], qa.shape[1] * (1 if fmt == FP4Q_MXFP8 else 2)
     esz = 2 if out_dtype == torch.bfloat16 else 4
     ldd = (N * esz + 15) // 16 * 16 // esz
     D = torch.empty((M, ldd), dtype=out_dtype, device=qa.device)

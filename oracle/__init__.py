@@ -381,6 +381,15 @@ def nv_gemm_ref(qa, sa, sta, qb, sb, stb) -> np.ndarray:
     return gemm_ref(nv_dequantize_f64(qa, sa, sta), nv_dequantize_f64(qb, sb, stb))
 
 
+def fp8_gemm_ref(ya: np.ndarray, tsa: np.ndarray, yb: np.ndarray, tsb: np.ndarray) -> np.ndarray:
+    """float64 D = A . B^T of FP8 operands with FP32 scales per 1x128 tile:
+    A = value(E4M3 ya) * tsa (tile of the element), exact in float64."""
+    lut = e4m3_values()
+    a = lut[np.asarray(ya)] * np.repeat(np.asarray(tsa, dtype=np.float64), 128, axis=1)
+    b = lut[np.asarray(yb)] * np.repeat(np.asarray(tsb, dtype=np.float64), 128, axis=1)
+    return a @ b.T
+
+
 def rel_frobenius(y: np.ndarray, ref: np.ndarray) -> float:
     y = np.asarray(y, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)

@@ -208,3 +208,76 @@ def test_wgrad_deterministic_h16(fq, oracle, rounding):
     # the rotation cancels along the token axis: the product tracks dY^T X up to FP4 error
     exact = oracle.bf16_bits_to_f32(dy).astype(np.float64).T @ oracle.bf16_bits_to_f32(x).astype(np.float64)
     assert oracle.rel_frobenius(host(d32).astype(np.float64), exact) < 0.2
+
+
+# ---------------------------------------------------------------------------
+# the FP8 consumer: MXFP8 GEMM on the outputs of FP4 -> FP8 (row and column)
+# ---------------------------------------------------------------------------
+def _bf16_round(y):
+    u = np.ascontiguousarray(y, dtype=np.float32).view(np.uint32)
+    return (((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def test_fp8_tile_scales_to_e8m0(fq):
+    import torch
+    ts = np.exp2(np.arange(-127, 128, dtype=np.float64)).astype(np.float32).reshape(5, 51)
+    ts = np.concatenate([ts, np.full((5, 1), 2.0 ** 5, dtype=np.float32)], axis=1)      # [5, 52]
+    s = torch.empty((5, 52 * 4), dtype=torch.uint8, device="cuda")
+    fq.fp4q_device_status(reset=True)
+    fq.fp4q_fp8_tile_scales_to_e8m0(dev(ts), 5, 52 * 128, s, 0)
+    want = np.repeat(np.log2(ts.astype(np.float64)).astype(np.int64) + 127, 4, axis=1)
+    assert np.array_equal(host(s).astype(np.int64), want)
+    assert fq.fp4q_device_status() == 0
+    bad = ts.copy()
+    bad[2, 3] = 3.0                                            # not a power of two
+    fq.fp4q_fp8_tile_scales_to_e8m0(dev(bad), 5, 52 * 128, s, 0)
+    assert fq.fp4q_device_status(reset=True) & 8          # bit 3: a scale it could not convert
+    assert np.all(host(s)[2, 12:16] == 0xFF)
+    assert fq.fp4q_device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [(200, 300, 256), (128, 256, 1024), (1000, 512, 384)])
+def test_mxfp8_gemm_on_fp4_to_fp8_outputs(fq, oracle, shape):
+    """Forward-style FP8 GEMM: both operands stored MXFP4, expanded by the
+    bit-remap FP4 -> FP8 conversion, multiplied as MXFP8 on the tensor cores."""
+    import torch
+    M, N, K = shape
+    rng = np.random.default_rng(M + N + K)
+    a = (rng.standard_normal((M, K)) * np.exp2(rng.integers(-4, 4, (M, 1)))).astype(np.float32)
+    b = rng.standard_normal((N, K)).astype(np.float32)
+    qa, sa = fq.mx_quantize(torch.from_numpy(a).cuda().to(torch.bfloat16))
+    qb, sb = fq.mx_quantize(torch.from_numpy(b).cuda().to(torch.bfloat16))
+    ya, tsa = fq.fp4_to_fp8(qa, sa)
+    yb, tsb = fq.fp4_to_fp8(qb, sb)
+    d32 = fq.gemm(ya, fq.fp8_mma_scales(tsa), yb, fq.fp8_mma_scales(tsb), fq.FP4Q_MXFP8, out_dtype=torch.float32)
+    d16 = fq.gemm(ya, fq.fp8_mma_scales(tsa), yb, fq.fp8_mma_scales(tsb), fq.FP4Q_MXFP8, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert fq.fp4q_device_status() == 0
+    ref = oracle.fp8_gemm_ref(host(ya), host(tsa), host(yb), host(tsb))
+    assert oracle.rel_frobenius(host(d32).astype(np.float64), ref) <= 1e-3
+    assert oracle.rel_frobenius(host(d16.float()).astype(np.float64), _bf16_round(ref)) <= 1e-3
+    # lossless chain: the FP8 operands are the MXFP4 values, so this is also the MXFP4 product
+    mx = oracle.mx_gemm_ref(host(qa), host(sa), host(qb), host(sb))
+    assert oracle.rel_frobenius(ref, mx) < 1e-12
+
+
+def test_mxfp8_wgrad_on_fp4_row_to_fp8_col(fq, oracle):
+    """Backward-style FP8 GEMM: dW = dY^T X with both operands converted by
+    FP4RowToFP8Col from their row-wise MXFP4 storage (tokens become K)."""
+    import torch
+    T, H, I = 512, 256, 384
+    rng = np.random.default_rng(41)
+    dy = (rng.standard_t(3, (T, H)) * 1e-3).astype(np.float32)
+    x = rng.standard_normal((T, I)).astype(np.float32)
+    qd, sd = fq.mx_quantize(torch.from_numpy(dy).cuda().to(torch.bfloat16))
+    qx, sx = fq.mx_quantize(torch.from_numpy(x).cuda().to(torch.bfloat16))
+    yd, tsd = fq.fp4_row_to_fp8_col(qd, sd)            # [H, T]
+    yx, tsx = fq.fp4_row_to_fp8_col(qx, sx)            # [I, T]
+    d32 = fq.gemm(yd, fq.fp8_mma_scales(tsd), yx, fq.fp8_mma_scales(tsx), fq.FP4Q_MXFP8, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fq.fp4q_device_status() == 0
+    ref = oracle.fp8_gemm_ref(host(yd), host(tsd), host(yx), host(tsx))
+    assert oracle.rel_frobenius(host(d32).astype(np.float64), ref) <= 1e-3
+    # and it is dY_mx^T X_mx of the stored MXFP4 values (no flush at these spreads)
+    exact = oracle.mx_dequantize_f64(host(qd), host(sd)).T @ oracle.mx_dequantize_f64(host(qx), host(sx))
+    assert oracle.rel_frobenius(ref, exact) < 1e-9

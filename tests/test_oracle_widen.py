@@ -152,3 +152,24 @@ def test_fp4_row_to_fp8_col_agrees_with_the_row_kernel_on_a_transposed_tile(orac
     yc, tc = oracle.mx_to_fp8_col(q, s)
     yr, tr = oracle.mx_to_fp8(q, s)
     assert np.array_equal(yc, yr) and np.array_equal(tc, tr)
+
+
+# ---------------------------------------------------------------------------
+# FP8 GEMM reference (the FP8 consumer of the FP4 -> FP8 conversions)
+# ---------------------------------------------------------------------------
+def test_fp8_gemm_ref_against_exact_rationals(oracle):
+    from fractions import Fraction
+    rng = np.random.default_rng(19)
+    lut = oracle.e4m3_values()
+    ok = np.flatnonzero(np.isfinite(lut) & (np.abs(lut) <= 8))
+    M, N, K = 3, 4, 256
+    ya = rng.choice(ok, (M, K)).astype(np.uint8)
+    yb = rng.choice(ok, (N, K)).astype(np.uint8)
+    tsa = np.exp2(rng.integers(-3, 4, (M, K // 128))).astype(np.float32)
+    tsb = np.exp2(rng.integers(-3, 4, (N, K // 128))).astype(np.float32)
+    d = oracle.fp8_gemm_ref(ya, tsa, yb, tsb)
+    for i in range(M):
+        for j in range(N):
+            acc = sum(Fraction(float(lut[ya[i, k]])) * Fraction(float(tsa[i, k // 128])) *
+                      Fraction(float(lut[yb[j, k]])) * Fraction(float(tsb[j, k // 128])) for k in range(K))
+            assert Fraction(d[i, j]) == acc
