@@ -205,7 +205,7 @@ def _events(torch, n):
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
 
-ROW_NAMES = ("c1", "c3", "gemm", "moe", "col", "nv2d")
+ROW_NAMES = ("c1", "c3", "gemm", "moe", "col", "nv2d", "fp8")
 
 
 def main_rows(fq, W, torch, peaks, which=ROW_NAMES, moe_tokens=65536):
@@ -213,7 +213,8 @@ def main_rows(fq, W, torch, peaks, which=ROW_NAMES, moe_tokens=65536):
     `which` selects the rows: c1 (MXFP4 round trip), c3 (NVFP4 of a gradient),
     gemm (dense block-scaled GEMM), moe (MoE expert FFN), col (column path:
     FP4RowToFP8Col, column-wise quantize, Wgrad GEMM with the deterministic
-    H16), nv2d (16x16-scaled NVFP4 weights)."""
+    H16), nv2d (16x16-scaled NVFP4 weights), fp8 (MXFP8 GEMM on FP4 -> FP8
+    outputs)."""
     rows = {}
     stream = torch.cuda.current_stream()
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
@@ -246,6 +247,8 @@ def main_rows(fq, W, torch, peaks, which=ROW_NAMES, moe_tokens=65536):
         col_rows(fq, W, torch, peaks, timed, dev_bf16, rows)
     if "nv2d" in which and getattr(lib, "fp4q_nv_quantize_2d", None) is not None:
         nv2d_row(fq, W, torch, peaks, timed, rows)
+    if "fp8" in which and getattr(lib, "fp4q_fp8_tile_scales_to_e8m0", None) is not None:
+        fp8_row(fq, W, torch, peaks, timed, dev_bf16, rows)
     torch.cuda.empty_cache()
     if "moe" in which and getattr(lib, "fp4q_grouped_gemm", None) is not None:
         rows[f"moe_ffn_{moe_tokens}x7168_top8_of_64"] = moe_row(fq, W, torch, peaks, timed, moe_tokens)
@@ -416,6 +419,31 @@ def col_rows(fq, W, torch, peaks, timed, dev_bf16, rows):
     rows["f3_wgrad_h16_gemm_8192^3"] = {"ms": round(ms_g, 4), "TFLOPS": round(flops / ms_g / 1e9, 1),
                                         "frac_peak": round(flops / ms_g / 1e9 / peak, 3)}
     del ad, bd, qa, sa, ra, rb, D
+
+
+def fp8_row(fq, W, torch, peaks, timed, dev_bf16, rows):
+    """The FP8 consumer: C4's operands stored MXFP4, expanded to FP8 by the
+    bit-remap conversion, multiplied as MXFP8 (kind::mxf8f6f4) 8192^3."""
+    stream = torch.cuda.current_stream()
+    a, b = W.gemm_operands()
+    qa, sa = fq.mx_quantize(dev_bf16(a))
+    qb, sb = fq.mx_quantize(dev_bf16(b))
+    ya, tsa = fq.fp4_to_fp8(qa, sa)
+    yb, tsb = fq.fp4_to_fp8(qb, sb)
+    ea, eb = fq.fp8_mma_scales(tsa), fq.fp8_mma_scales(tsb)
+    D = torch.empty((8192, 8192), dtype=torch.bfloat16, device="cuda")
+    A = fq.make_operand(ya, ea, fq.FP4Q_MXFP8)
+    B = fq.make_operand(yb, eb, fq.FP4Q_MXFP8)
+    ms = timed(lambda: fq.fp4q_block_scaled_gemm(A, B, 8192, 8192, 8192, D, fq.FP4Q_BF16, 8192, stream), 10, True)
+    ms_s = timed(lambda: fq.fp4q_fp8_tile_scales_to_e8m0(tsa, 8192, 8192, ea, fq.FP4Q_SCALES_MMA, stream), 10, True)
+    peak8 = peaks["bf16_tflops"] * 2.0
+    flops = 2.0 * 8192 ** 3
+    rows["f4_mxfp8_gemm_8192^3"] = {"ms": round(ms, 4), "TFLOPS": round(flops / ms / 1e9, 1),
+                                    "frac_peak_fp8": round(flops / ms / 1e9 / peak8, 3),
+                                    "peak_TFLOPS": round(peak8, 1),
+                                    "peak_source": f"{peaks['source']} bf16 burst x 2 (nominal FP8:BF16)",
+                                    "scale_conversion_ms": round(ms_s, 4)}
+    del qa, sa, qb, sb, ya, yb, D
 
 
 def nv2d_row(fq, W, torch, peaks, timed, rows):
