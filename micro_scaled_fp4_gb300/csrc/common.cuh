@@ -185,8 +185,8 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 
 // Launch shape for row-wise block kernels: one thread per block of a row,
 // `bpr` blocks per row; returns threads per CTA and CTAs along the row.
-inline void row_launch_shape(int64_t bpr, int* tpb, int* nx) {
-    int64_t n = (bpr + 255) / 256;
+inline void row_launch_shape(int64_t bpr, int* tpb, int* nx, int64_t max_threads = 256) {
+    int64_t n = (bpr + max_threads - 1) / max_threads;
     int64_t per = (bpr + n - 1) / n;
     per = (per + 31) / 32 * 32;
     *tpb = int(per);
@@ -205,7 +205,7 @@ inline void packed_row_shape(int64_t units, int* tpb, int* nx, int* rpc, int64_t
         *nx = 1;
         *rpc = int(r);
     } else {
-        row_launch_shape(units, tpb, nx);
+        row_launch_shape(units, tpb, nx, max_threads < 256 ? max_threads : 256);
         *rpc = 1;
     }
 }

@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(
 struct RawPair { u32x8 a, b; float ts; };
 
 // A CTA covers rpc rows side by side (blockDim.x / rpc threads per row).
-__global__ void __launch_bounds__(256, 3) mx_quantize_e4m3x2_kernel(
+__global__ void __launch_bounds__(224, 4) mx_quantize_e4m3x2_kernel(
     const uint8_t* __restrict__ x, const float* __restrict__ tile_scale, int64_t rows,
     uint32_t bpr, int64_t ld_x, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout, int rpc) {
     const uint32_t upc = blockDim.x / uint32_t(rpc);
@@ -510,7 +510,7 @@ extern "C" fp4q_status fp4q_mx_quantize(const void* x, fp4q_dtype x_type, const 
                 break;
             }
             int tpb2, nx2, rpc;
-            packed_row_shape(bpr / 2, &tpb2, &nx2, &rpc, 256);
+            packed_row_shape(bpr / 2, &tpb2, &nx2, &rpc, 224);       // at most 224 threads: 4 CTAs per SM
             dim3 grid = grid_for_rows(mx_quantize_e4m3x2_kernel, tpb2, (rows + rpc - 1) / rpc, nx2, sms);
             mx_quantize_e4m3x2_kernel<<<grid, tpb2, 0, s>>>(xb, tile_scale, rows, bpr, ld_x, q, scales, mma, rpc);
             break;
