@@ -192,80 +192,54 @@ __global__ void __launch_bounds__(ring::kMaxThreads) fp4_to_fp8_staged_kernel(
 
 // FP4RowToFP8Col ("Practical FP4 Training for Large-Scale MoE Models on Hopper
 // GPUs", Spanish summary section 2; French summary 2.C: dequantize, transpose
-// and re-quantize in one kernel, with padded shared memory against bank
-// conflicts on the column accesses).  Input: row-wise MXFP4 [rows, cols];
-// output: E4M3 of the transpose [cols, rows] with one FP32 scale per 1x128
-// tile along the output rows ([cols, rows/128]).  A CTA converts a 128 x 128
-// tile: the 128 rows' scale words give the largest exponent of each of the
-// tile's four 32-column blocks (= each output tile's scale); warp w remaps
-// rows 32(w/2) .. + 31 of column half w % 2 with the shift table (one lane per
-// row) and drops each E4M3 byte into a transposed, padded shared tile; the
-// CTA then writes 64 contiguous bytes per thread.
+// and re-quantize in one kernel).  Input: row-wise MXFP4 [rows, cols]; output:
+// E4M3 of the transpose [cols, rows] with one FP32 scale per 1x128 tile along
+// the output rows ([cols, rows/128]).  A warp converts 128 input rows x 16
+// input columns (one 32-block half): lane l holds rows 4l .. 4l + 3, so the
+// output tile's scale (2^Emax over the 128 rows' block exponents) is a warp
+// max, each row is remapped with the shift table, and a 4 x 4 byte transpose
+// in registers (eight byte permutes per 16 bytes) turns the lane's 4 rows x 4
+// columns into four 32-bit words, one per output row: each store instruction
+// writes 128 contiguous bytes of one output row.  No shared-memory staging of
+// the tile is needed (the pages' Hopper kernel pads shared memory instead).
 constexpr int kColTile = 128;
-constexpr uint32_t kTStride = kColTile + 16;
 
 __global__ void __launch_bounds__(256) fp4_row_to_fp8_col_kernel(
     const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, int64_t cols,
     uint8_t* __restrict__ y, float* __restrict__ tile_scale) {
     __shared__ uint2 lut[kShiftRows];
-    __shared__ uint32_t srow[kColTile];          // the 4 scale bytes of each tile row
-    __shared__ uint32_t wmax[4];
-    __shared__ __align__(16) uint8_t T[kColTile * kTStride];
     lut_setup(lut);
-    const int64_t r0 = int64_t(blockIdx.y) * kColTile, c0 = int64_t(blockIdx.x) * kColTile;
+    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t spr = cols / 32;                                  // scale bytes per input row
-    if (threadIdx.x < kColTile) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(s + (r0 + threadIdx.x) * spr + c0 / 32);
-        srow[threadIdx.x] = w;
-        uint32_t m = w;
+    const int64_t r0 = int64_t(blockIdx.y) * kColTile;
+    const int64_t c0 = int64_t(blockIdx.x) * kColTile + 16 * warp;     // 16 columns of this warp
+    const int64_t rb = r0 + 4 * lane;
+    const int64_t spr = cols / 32;
+    uint2 cw[4];
+    uint32_t e[4];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = __vmaxu4(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) wmax[warp] = m;
+    for (int i = 0; i < 4; ++i) {
+        cw[i] = *reinterpret_cast<const uint2*>(q + (rb + i) * (cols / 2) + c0 / 2);
+        e[i] = s[(rb + i) * spr + c0 / 32];
     }
-    __syncthreads();
-    const uint32_t emax4 = __vmaxu4(__vmaxu4(wmax[0], wmax[1]), __vmaxu4(wmax[2], wmax[3]));
-    // phase 1: lane = input row, 64 columns (two blocks) per warp
-    {
-        const uint32_t r = 32u * uint32_t(warp >> 1) + uint32_t(lane), h = uint32_t(warp & 1);
-        const u32x8 cw = ldg256(q + (r0 + r) * (cols / 2) + c0 / 2 + 32 * h);
-        const uint32_t e_row = srow[r];
-        const uint32_t tb = smem_addr(T) + r;
+    const uint32_t emax = __reduce_max_sync(0xffffffffu, max(max(e[0], e[1]), max(e[2], e[3])));
+    if (lane < 16) tile_scale[(c0 + lane) * (rows / kColTile) + r0 / kColTile] = exp2i(int(emax) - 127);
+    uint32_t w[4][4];                                   // [row][column group of 4]
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const uint32_t b = 2 * h + j;                            // block of the tile
-            const uint32_t e = (e_row >> (8 * b)) & 0xffu, em = (emax4 >> (8 * b)) & 0xffu;
-            const uint2 L = lut[min(em - e, uint32_t(kShiftRows - 1))];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint2 o = remap8(cw.v[4 * j + k], L);         // columns 32b + 8k .. + 7
-                const uint32_t cbase = 32 * b + 8 * k;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t byte = ((i < 4 ? o.x : o.y) >> (8 * (i & 3))) & 0xffu;
-                    asm volatile("st.shared.u8 [%0], %1;" :: "r"(tb + (cbase + i) * kTStride), "r"(byte) : "memory");
-                }
-            }
-        }
+    for (int i = 0; i < 4; ++i) {
+        const uint2 L = lut[min(emax - e[i], uint32_t(kShiftRows - 1))];
+        const uint2 lo = remap8(cw[i].x, L), hi = remap8(cw[i].y, L);
+        w[i][0] = lo.x; w[i][1] = lo.y; w[i][2] = hi.x; w[i][3] = hi.y;
     }
-    if (threadIdx.x < kColTile)
-        tile_scale[(c0 + threadIdx.x) * (rows / kColTile) + r0 / kColTile] =
-            exp2i(int((emax4 >> (8 * (threadIdx.x >> 5))) & 0xffu) - 127);
-    __syncthreads();
-    // phase 2: output row c0 + c, 64 contiguous bytes per thread
-    {
-        const uint32_t c = threadIdx.x >> 1, half = threadIdx.x & 1;
-        const uint32_t src = smem_addr(T) + c * kTStride + 64 * half;
-        u32x8 o[2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(o[i >> 1].v[4 * (i & 1)]), "=r"(o[i >> 1].v[4 * (i & 1) + 1]),
-                           "=r"(o[i >> 1].v[4 * (i & 1) + 2]), "=r"(o[i >> 1].v[4 * (i & 1) + 3])
-                         : "r"(src + 16 * i));
-        uint8_t* dst = y + (c0 + c) * rows + r0 + 64 * half;
-        stg256(dst, o[0]);
-        stg256(dst + 32, o[1]);
+    for (int g = 0; g < 4; ++g) {
+        const uint32_t t0 = __byte_perm(w[0][g], w[1][g], 0x5140), t1 = __byte_perm(w[0][g], w[1][g], 0x7362);
+        const uint32_t t2 = __byte_perm(w[2][g], w[3][g], 0x5140), t3 = __byte_perm(w[2][g], w[3][g], 0x7362);
+        const uint32_t col[4] = {__byte_perm(t0, t2, 0x5410), __byte_perm(t0, t2, 0x7632),
+                                 __byte_perm(t1, t3, 0x5410), __byte_perm(t1, t3, 0x7632)};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint32_t*>(y + (c0 + 4 * g + k) * rows + rb) = col[k];
     }
 }
 

@@ -343,8 +343,10 @@ __global__ void __launch_bounds__(256) mx_quantize_col_kernel(
     extern __shared__ __align__(16) uint8_t tile[];
     const int64_t r0 = int64_t(blockIdx.y) * kMxColRows, c0 = int64_t(blockIdx.x) * kMxColCols;
     const uint32_t base = smem_addr(tile);
+    // 16 threads cover two rows: a quarter-warp stores chunks 0-3 (or 4-7) of
+    // both, which the 16-byte row padding puts on 8 different bank groups
     for (uint32_t i = threadIdx.x; i < kMxColRows * 8; i += blockDim.x) {
-        const uint32_t r = i >> 3, ch = i & 7u;
+        const uint32_t r = 2 * (i >> 4) + ((i >> 2) & 1u), ch = (i & 3u) + 4 * ((i >> 3) & 1u);
         const u32x8 v = ldg256(x + (r0 + r) * ld_x_bytes + c0 * 2 + ch * 32);
         const uint32_t d = base + r * kMxColStride + ch * 32;
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(d), "r"(v.v[0]), "r"(v.v[1]), "r"(v.v[2]),

@@ -281,17 +281,20 @@ __global__ void __launch_bounds__(256) nv_quant_2d_kernel(
     uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout) {
     const float s_t = nv_tensor_scale(amax_ptr, amax_out, st_out);
     const float denom = __fmul_rn(6.0f, s_t);
-    const int64_t units = (rows / 16) * int64_t(tpr);            // (tile row, block) pairs
-    const uint32_t j = threadIdx.x & 15u;
+    // A warp takes two adjacent blocks (b, b + 1) of the same 16 rows: lane
+    // 16 h + j holds row j of block b + h, so each row's 64 bytes are read
+    // together.  Units are (tile row, block pair); the loop runs per warp so
+    // both half-warps stay in the shuffles, and a half past the row end works
+    // on nothing.
+    const uint32_t pairs = (tpr + 1) / 2;
+    const int64_t units = (rows / 16) * int64_t(pairs);
+    const uint32_t j = threadIdx.x & 15u, h = (threadIdx.x >> 4) & 1u;
     const uint64_t cols = uint64_t(tpr) * 16;
-    // the loop runs per warp (two units), so that both half-warps stay in the
-    // shuffles; a half-warp past the end works on nothing
     const int64_t wstride = int64_t(gridDim.x) * (blockDim.x / 32);
-    for (int64_t wu = int64_t(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; 2 * wu < units; wu += wstride) {
-        const int64_t un = 2 * wu + ((threadIdx.x >> 4) & 1);
-        const bool valid = un < units;
-        const int64_t tr = valid ? un / tpr : 0;
-        const uint32_t b = valid ? uint32_t(un - tr * tpr) : 0u;
+    for (int64_t un = int64_t(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; un < units; un += wstride) {
+        const int64_t tr = un / pairs;
+        const uint32_t b = 2 * uint32_t(un - tr * pairs) + h;
+        const bool valid = b < tpr;
         const int64_t r = tr * 16 + j;
         float t[16];
         uint32_t ab = 0;
@@ -547,9 +550,9 @@ extern "C" fp4q_status fp4q_nv_quantize_2d(const void* x, int64_t rows, int64_t 
         return check_launch("nv_quantize_2d");
     }
     const int mma = layout == FP4Q_SCALES_MMA;
-    const int64_t units = (rows / 16) * int64_t(tpr);
+    const int64_t units = (rows / 16) * int64_t((tpr + 1) / 2);        // warp units
     const int per_sm = resident_per_sm(nv_quant_2d_kernel<true>, 256);
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((units + 15) / 16, int64_t(per_sm) * sms));
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((units + 7) / 8, int64_t(per_sm) * sms));
     if (rounding == FP4Q_SR)
         nv_quant_2d_kernel<true><<<unsigned(grid), 256, 0, s>>>(xb, rows, tpr, ld_x * 2, keys, amax_ptr, amax_out,
                                                                 tensor_scale_out, q, scales, mma);
