@@ -194,17 +194,17 @@ __global__ void __launch_bounds__(ring::kMaxThreads) fp4_to_fp8_staged_kernel(
 // GPUs", Spanish summary section 2; French summary 2.C: dequantize, transpose
 // and re-quantize in one kernel).  Input: row-wise MXFP4 [rows, cols]; output:
 // E4M3 of the transpose [cols, rows] with one FP32 scale per 1x128 tile along
-// the output rows ([cols, rows/128]).  A warp converts 128 input rows x 16
-// input columns (one 32-block half): lane l holds rows 4l .. 4l + 3, so the
-// output tile's scale (2^Emax over the 128 rows' block exponents) is a warp
-// max, each row is remapped with the shift table, and a 4 x 4 byte transpose
-// in registers (eight byte permutes per 16 bytes) turns the lane's 4 rows x 4
-// columns into four 32-bit words, one per output row: each store instruction
-// writes 128 contiguous bytes of one output row.  No shared-memory staging of
-// the tile is needed (the pages' Hopper kernel pads shared memory instead).
+// the output rows ([cols, rows/128]).  A warp converts 128 input rows x 64
+// input columns (two 32-blocks): lane l reads rows 4l .. 4l + 3 with one
+// 32-byte load each, so the two output tiles' scales (2^Emax over the 128
+// rows' block exponents) are warp maxima; each row is remapped with the shift
+// table, and a 4 x 4 byte transpose in registers (eight byte permutes per 16
+// bytes) turns the lane's 4 rows x 4 columns into four 32-bit words, one per
+// output row: every store instruction writes 128 contiguous bytes of one
+// output row.  No shared-memory staging of the tile is needed.
 constexpr int kColTile = 128;
 
-__global__ void __launch_bounds__(256) fp4_row_to_fp8_col_kernel(
+__global__ void __launch_bounds__(64) fp4_row_to_fp8_col_kernel(
     const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, int64_t cols,
     uint8_t* __restrict__ y, float* __restrict__ tile_scale) {
     __shared__ uint2 lut[kShiftRows];
@@ -212,34 +212,46 @@ __global__ void __launch_bounds__(256) fp4_row_to_fp8_col_kernel(
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t r0 = int64_t(blockIdx.y) * kColTile;
-    const int64_t c0 = int64_t(blockIdx.x) * kColTile + 16 * warp;     // 16 columns of this warp
+    const int64_t c0 = int64_t(blockIdx.x) * kColTile + 64 * warp;     // 64 columns of this warp
     const int64_t rb = r0 + 4 * lane;
     const int64_t spr = cols / 32;
-    uint2 cw[4];
-    uint32_t e[4];
+    u32x8 cw[4];
+    uint32_t e[4][2];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        cw[i] = *reinterpret_cast<const uint2*>(q + (rb + i) * (cols / 2) + c0 / 2);
-        e[i] = s[(rb + i) * spr + c0 / 32];
+        cw[i] = ldg256(q + (rb + i) * (cols / 2) + c0 / 2);
+        const uint32_t sw = *reinterpret_cast<const uint16_t*>(s + (rb + i) * spr + c0 / 32);
+        e[i][0] = sw & 0xffu;
+        e[i][1] = sw >> 8;
     }
-    const uint32_t emax = __reduce_max_sync(0xffffffffu, max(max(e[0], e[1]), max(e[2], e[3])));
-    if (lane < 16) tile_scale[(c0 + lane) * (rows / kColTile) + r0 / kColTile] = exp2i(int(emax) - 127);
-    uint32_t w[4][4];                                   // [row][column group of 4]
+    uint32_t emax[2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint2 L = lut[min(emax - e[i], uint32_t(kShiftRows - 1))];
-        const uint2 lo = remap8(cw[i].x, L), hi = remap8(cw[i].y, L);
-        w[i][0] = lo.x; w[i][1] = lo.y; w[i][2] = hi.x; w[i][3] = hi.y;
-    }
+    for (int b = 0; b < 2; ++b)
+        emax[b] = __reduce_max_sync(0xffffffffu, max(max(e[0][b], e[1][b]), max(e[2][b], e[3][b])));
+    tile_scale[(c0 + lane) * (rows / kColTile) + r0 / kColTile] = exp2i(int(emax[0]) - 127);
+    tile_scale[(c0 + 32 + lane) * (rows / kColTile) + r0 / kColTile] = exp2i(int(emax[1]) - 127);
+    uint2 L[4][2];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const uint32_t t0 = __byte_perm(w[0][g], w[1][g], 0x5140), t1 = __byte_perm(w[0][g], w[1][g], 0x7362);
-        const uint32_t t2 = __byte_perm(w[2][g], w[3][g], 0x5140), t3 = __byte_perm(w[2][g], w[3][g], 0x7362);
-        const uint32_t col[4] = {__byte_perm(t0, t2, 0x5410), __byte_perm(t0, t2, 0x7632),
-                                 __byte_perm(t1, t3, 0x5410), __byte_perm(t1, t3, 0x7632)};
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<uint32_t*>(y + (c0 + 4 * g + k) * rows + rb) = col[k];
+        for (int b = 0; b < 2; ++b) L[i][b] = lut[min(emax[b] - e[i][b], uint32_t(kShiftRows - 1))];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {                       // codes word k: columns 8k .. 8k + 7
+        uint2 o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = remap8(cw[i].v[k], L[i][k >> 2]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {                   // columns 8k + 4h .. + 3
+            const uint32_t w0 = h ? o[0].y : o[0].x, w1 = h ? o[1].y : o[1].x;
+            const uint32_t w2 = h ? o[2].y : o[2].x, w3 = h ? o[3].y : o[3].x;
+            const uint32_t t0 = __byte_perm(w0, w1, 0x5140), t1 = __byte_perm(w0, w1, 0x7362);
+            const uint32_t t2 = __byte_perm(w2, w3, 0x5140), t3 = __byte_perm(w2, w3, 0x7362);
+            const uint32_t col[4] = {__byte_perm(t0, t2, 0x5410), __byte_perm(t0, t2, 0x7632),
+                                     __byte_perm(t1, t3, 0x5410), __byte_perm(t1, t3, 0x7632)};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                *reinterpret_cast<uint32_t*>(y + (c0 + 8 * k + 4 * h + kk) * rows + rb) = col[kk];
+        }
     }
 }
 
@@ -310,8 +322,8 @@ extern "C" fp4q_status fp4q_fp4_row_to_fp8_col(const uint8_t* q, const uint8_t* 
     fp4q_status st = current_device(nullptr);
     if (st != FP4Q_OK) return st;
     const dim3 grid(unsigned(cols / kColTile), unsigned(rows / kColTile), 1);
-    fp4_row_to_fp8_col_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, scales, rows, cols, y,
-                                                                                       tile_scale);
+    fp4_row_to_fp8_col_kernel<<<grid, 64, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, scales, rows, cols, y,
+                                                                                      tile_scale);
     return check_launch("fp4_row_to_fp8_col");
 }
 
