@@ -4,7 +4,10 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "ring.cuh"
 #include "tc.cuh"
 
 namespace fp4q {
@@ -146,3 +149,31 @@ extern "C" fp4q_status fp4q_device_status(uint32_t* status_out, int reset) {
     *status_out = v;
     return v ? FP4Q_ERR_TIMEOUT : FP4Q_OK;
 }
+
+namespace fp4q {
+namespace ring {
+
+fp4q_status encode_bf16_tile_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                 uint32_t box_cols, uint32_t box_rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+            return fail(FP4Q_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(ld * 2)};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FP4Q_ERR_CUDA, "cuTensorMapEncodeTiled (BF16 tile) failed (%d)", int(r));
+    return FP4Q_OK;
+}
+
+}  // namespace ring
+}  // namespace fp4q

@@ -328,54 +328,62 @@ __global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_e4m3_staged_ker
 
 // Column-wise MXFP4 of BF16 (block axis 0): the row-wise quantization of X^T,
 // written in the transposed layout (q [cols, rows/2], scales [cols, rows/32])
-// without materialising X^T.  A CTA stages a 128-row x 128-column BF16 tile in
-// shared memory (rows padded by 16 bytes); thread t reads column pair
-// 2(t % 64), 2(t % 64) + 1 over rows 32(t / 64) .. + 31 with one 32-bit shared
-// load per row (lanes on consecutive words: no bank conflicts), repacks the
-// halves into the two columns' 32-element blocks and quantizes them with the
-// row-wise rule.
-constexpr int kMxColRows = 128, kMxColCols = 128;
-constexpr uint32_t kMxColStride = kMxColCols * 2 + 16;
+// without materialising X^T.  Persistent CTAs run a shared-memory ring
+// (ring.cuh): the producer thread brings 128-row x 128-column BF16 tiles in
+// with TMA tensor copies (dense 256-byte rows, 3 stages); consumer thread t
+// reads column pair 2(t % 64), 2(t % 64) + 1 over rows 32(t / 64) .. + 31
+// with one 32-bit shared load per row (a warp reads 32 consecutive words, no
+// bank conflicts), repacks the halves into the two columns' 32-element blocks
+// and quantizes them with the row-wise rule.
+constexpr int kMxColRows = 128, kMxColCols = 128, kMxColStages = 3;
+constexpr uint32_t kMxColTileBytes = kMxColRows * kMxColCols * 2;
 
-__global__ void __launch_bounds__(256) mx_quantize_col_kernel(
-    const uint8_t* __restrict__ x, int64_t rows, int64_t ld_x_bytes, uint8_t* __restrict__ q,
-    uint8_t* __restrict__ s, int mma_layout) {
-    extern __shared__ __align__(16) uint8_t tile[];
-    const int64_t r0 = int64_t(blockIdx.y) * kMxColRows, c0 = int64_t(blockIdx.x) * kMxColCols;
-    const uint32_t base = smem_addr(tile);
-    // 16 threads cover two rows: a quarter-warp stores chunks 0-3 (or 4-7) of
-    // both, which the 16-byte row padding puts on 8 different bank groups
-    for (uint32_t i = threadIdx.x; i < kMxColRows * 8; i += blockDim.x) {
-        const uint32_t r = 2 * (i >> 4) + ((i >> 2) & 1u), ch = (i & 3u) + 4 * ((i >> 3) & 1u);
-        const u32x8 v = ldg256(x + (r0 + r) * ld_x_bytes + c0 * 2 + ch * 32);
-        const uint32_t d = base + r * kMxColStride + ch * 32;
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(d), "r"(v.v[0]), "r"(v.v[1]), "r"(v.v[2]),
-                     "r"(v.v[3]) : "memory");
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(d + 16), "r"(v.v[4]), "r"(v.v[5]),
-                     "r"(v.v[6]), "r"(v.v[7]) : "memory");
+__global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_col_kernel(
+    const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_t cols, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ s, int mma_layout, uint32_t* status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const ring::Ring rg = ring::make_ring(smem, kMxColTileBytes, kMxColStages);
+    const int64_t ctiles = cols / kMxColCols, ngroups = (rows / kMxColRows) * ctiles;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) {
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tmap);
+            ring::produce(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, uint32_t fb, int64_t g) {
+                const int64_t rt = g / ctiles, ct = g - rt * ctiles;
+                tc::mbar_arrive_expect_tx(fb, kMxColTileBytes);
+                tc::tma_load_2d(tc::smem_u32(st), &tmap, fb, int(ct * kMxColCols), int(rt * kMxColRows));
+            });
+        }
+        return;
     }
-    __syncthreads();
-    const uint32_t cp = threadIdx.x & 63u, k = threadIdx.x >> 6;
-    RawBlock<kBF16> A, B;                      // columns 2cp and 2cp + 1, rows 32k .. 32k + 31
+    const uint32_t t = threadIdx.x - 32, cp = t & 63u, k = t >> 6;
+    const uint32_t spr = uint32_t(rows / 32);
+    ring::consume(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, int64_t g) {
+        const int64_t rt = g / ctiles, ct = g - rt * ctiles;
+        const int64_t r0 = rt * kMxColRows, c0 = ct * kMxColCols;
+        const uint32_t base = tc::smem_u32(st);
+        RawBlock<kBF16> A, B;                      // columns 2cp and 2cp + 1, rows 32k .. 32k + 31
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        uint32_t w0, w1;
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(base + (32 * k + 2 * j) * kMxColStride + 4 * cp));
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(base + (32 * k + 2 * j + 1) * kMxColStride + 4 * cp));
-        const uint32_t lo = __byte_perm(w0, w1, 0x5410), hi = __byte_perm(w0, w1, 0x7632);
-        if (j < 8) { A.a.v[j] = lo; B.a.v[j] = hi; } else { A.b.v[j - 8] = lo; B.b.v[j - 8] = hi; }
-    }
-    const uint32_t spr = uint32_t(rows / 32), blk = uint32_t(r0 / 32) + k;
+        for (int j = 0; j < 16; ++j) {
+            uint32_t w0, w1;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(base + (32 * k + 2 * j) * (kMxColCols * 2) + 4 * cp));
+            asm volatile("ld.shared.b32 %0, [%1];"
+                         : "=r"(w1) : "r"(base + (32 * k + 2 * j + 1) * (kMxColCols * 2) + 4 * cp));
+            const uint32_t lo = __byte_perm(w0, w1, 0x5410), hi = __byte_perm(w0, w1, 0x7632);
+            if (j < 8) { A.a.v[j] = lo; B.a.v[j] = hi; } else { A.b.v[j - 8] = lo; B.b.v[j - 8] = hi; }
+        }
+        const uint32_t blk = uint32_t(r0 / 32) + k;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint4 codes;
-        uint32_t sb;
-        quantize_block<kBF16>(h ? B : A, codes, sb);
-        const int64_t c = c0 + 2 * cp + h;
-        *reinterpret_cast<uint4*>(q + c * (rows / 2) + int64_t(blk) * 16) = codes;
-        const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(c), blk, spr) : uint64_t(c) * spr + blk;
-        s[so] = uint8_t(sb);
-    }
+        for (int h = 0; h < 2; ++h) {
+            uint4 codes;
+            uint32_t sb;
+            quantize_block<kBF16>(h ? B : A, codes, sb);
+            const int64_t c = c0 + 2 * cp + h;
+            *reinterpret_cast<uint4*>(q + c * (rows / 2) + int64_t(blk) * 16) = codes;
+            const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(c), blk, spr) : uint64_t(c) * spr + blk;
+            s[so] = uint8_t(sb);
+        }
+    });
 }
 
 template <bool OUT_BF16>
@@ -444,25 +452,22 @@ extern "C" fp4q_status fp4q_mx_quantize(const void* x, fp4q_dtype x_type, const 
         if (x_type != FP4Q_BF16) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "mx_quantize: block_axis 0 needs a BF16 source");
         if (rows % kMxColRows || cols % kMxColCols)
             return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "mx_quantize: block_axis 0 needs rows %% 128 == 0, cols %% 128 == 0");
-        if (rows / kMxColRows > 65535)
-            return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "mx_quantize: block_axis 0 needs rows <= 8388480");
         if (rows == 0 || cols == 0) return FP4Q_OK;
         if (!x || !q || !scales) return fail(FP4Q_ERR_INVALID_ARGUMENT, "mx_quantize: null pointer");
         if ((reinterpret_cast<uintptr_t>(x) & 31u) || (ld_x * 2) % 32 || !aligned16(q))
             return fail(FP4Q_ERR_MISALIGNED, "mx_quantize: x 32-byte aligned with ld_x %% 16 == 0, q 16-byte aligned");
-        fp4q_status st = current_device(nullptr);
+        int sms = 0;
+        fp4q_status st = current_device(&sms);
         if (st != FP4Q_OK) return st;
-        const uint32_t smem = kMxColRows * kMxColStride;
-        static int attr_set[64] = {};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (!attr_set[dev & 63]) {
-            cudaFuncSetAttribute(mx_quantize_col_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-            attr_set[dev & 63] = 1;
-        }
-        const dim3 grid(unsigned(cols / kMxColCols), unsigned(rows / kMxColRows), 1);
-        mx_quantize_col_kernel<<<grid, 256, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-            static_cast<const uint8_t*>(x), rows, ld_x * 2, q, scales, layout == FP4Q_SCALES_MMA);
+        CUtensorMap tmap;
+        if ((st = ring::encode_bf16_tile_map(&tmap, x, rows, cols, ld_x, kMxColCols, kMxColRows)) != FP4Q_OK)
+            return st;
+        const uint32_t smem = ring::smem_bytes(kMxColTileBytes, kMxColStages);
+        const int per_sm = resident_per_sm_smem(mx_quantize_col_kernel, ring::kMaxThreads, smem);
+        const int64_t ngroups = (rows / kMxColRows) * (cols / kMxColCols);
+        const int64_t grid = std::min<int64_t>(ngroups, int64_t(per_sm) * sms);
+        mx_quantize_col_kernel<<<unsigned(grid), ring::kMaxThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
+            tmap, rows, cols, q, scales, layout == FP4Q_SCALES_MMA, status_word());
         return check_launch("mx_quantize (block_axis 0)");
     }
     if (block_axis != 1) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "mx_quantize: block_axis must be 0 or 1");

@@ -18,6 +18,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "ring.cuh"
 
 namespace fp4q {
 namespace {
@@ -315,87 +316,92 @@ __global__ void __launch_bounds__(256) nv_quant_2d_kernel(
 }
 
 // Column-wise NVFP4 (block axis 0): the row-wise quantization of X^T, written
-// in the transposed layout, without materialising X^T.  A CTA stages a
-// 128-row x 64-column BF16 tile in shared memory (rows padded by 16 bytes so
-// that the column reads below are conflict-free); thread t then reads column
-// pair 2(t % 32), 2(t % 32) + 1 over rows 16(t / 32) .. + 15 (one 32-bit
-// shared load per row gives both columns) and quantizes the two 16-element
-// blocks -- rotated along axis 0 when rht != 0 -- into rows c of q [cols, rows/2]
-// and scales [cols, rows/16].  MODE 0: tensor amax only; 1: RNE; 2: SR (linear
-// element index of X^T).
+// in the transposed layout, without materialising X^T.  Persistent CTAs run a
+// shared-memory ring (ring.cuh): the producer thread brings 128-row x 64-column
+// BF16 tiles in with TMA tensor copies (dense 128-byte rows, 4 stages);
+// consumer thread t reads column pair 2(t % 32), 2(t % 32) + 1 over rows
+// 16(t / 32) .. + 15 (one 32-bit shared load per row; a warp reads 32
+// consecutive words, no bank conflicts) and quantizes the two 16-element
+// blocks -- rotated along axis 0 when rht != 0 -- into rows c of
+// q [cols, rows/2] and scales [cols, rows/16].  MODE 0: tensor amax only;
+// 1: RNE; 2: SR (linear element index of X^T).
 constexpr int kColRows = 128, kColCols = 64;
-constexpr uint32_t kColStride = kColCols * 2 + 16;
+constexpr uint32_t kColTileBytes = kColRows * kColCols * 2;
 
 template <int MODE>
-__global__ void __launch_bounds__(256) nv_col_kernel(
-    const uint8_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x_bytes, int rht, uint64_t rht_seed,
+__global__ void __launch_bounds__(ring::kMaxThreads) nv_col_kernel(
+    const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_t cols, int rht, uint64_t rht_seed,
     const PhiloxKeys sr_keys, const float* __restrict__ amax_ptr, float* __restrict__ amax_out,
     float* __restrict__ st_out, uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ q,
-    uint8_t* __restrict__ s, int mma_layout) {
-    __shared__ __align__(16) uint8_t tile[kColRows * kColStride];
-    __shared__ uint32_t wmax[8];
+    uint8_t* __restrict__ s, int mma_layout, uint32_t* status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const ring::Ring rg = ring::make_ring(smem, kColTileBytes);
+    const int64_t ctiles = cols / kColCols, ngroups = (rows / kColRows) * ctiles;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) {
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tmap);
+            ring::produce(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, uint32_t fb, int64_t g) {
+                const int64_t rt = g / ctiles, ct = g - rt * ctiles;
+                tc::mbar_arrive_expect_tx(fb, kColTileBytes);
+                tc::tma_load_2d(tc::smem_u32(st), &tmap, fb, int(ct * kColCols), int(rt * kColRows));
+            });
+        }
+        return;
+    }
     const uint32_t signs = rht == 1 ? rht_signs(rht_seed) : 0u;
     float s_t = 0.0f, denom = 0.0f;
     if constexpr (MODE != 0) {
         s_t = nv_tensor_scale(amax_ptr, amax_out, st_out);
         denom = __fmul_rn(6.0f, s_t);
     }
-    const int64_t r0 = int64_t(blockIdx.y) * kColRows, c0 = int64_t(blockIdx.x) * kColCols;
-    // stage the tile: 128 rows x 128 bytes, 32 bytes per load
-    for (uint32_t i = threadIdx.x; i < kColRows * 4; i += blockDim.x) {
-        const uint32_t r = i >> 2, ch = i & 3u;
-        const u32x8 v = ldg256(x + (r0 + r) * ld_x_bytes + c0 * 2 + ch * 32);
-        const uint32_t d = smem_addr(tile) + r * kColStride + ch * 32;
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(d), "r"(v.v[0]), "r"(v.v[1]), "r"(v.v[2]),
-                     "r"(v.v[3]) : "memory");
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(d + 16), "r"(v.v[4]), "r"(v.v[5]),
-                     "r"(v.v[6]), "r"(v.v[7]) : "memory");
-    }
-    __syncthreads();
-    const uint32_t cp = threadIdx.x & 31u, k = threadIdx.x >> 5;
-    float a[16], b[16];
+    const uint32_t t = threadIdx.x - 32, cp = t & 31u, k = t >> 5;
+    const uint32_t spr = uint32_t(rows / 16);                 // scale columns per output row
+    uint32_t m_all = 0;
+    ring::consume(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, int64_t g) {
+        const int64_t rt = g / ctiles, ct = g - rt * ctiles;
+        const int64_t r0 = rt * kColRows, c0 = ct * kColCols;
+        const uint32_t base = tc::smem_u32(st);
+        float a[16], b[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        uint32_t w;
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(smem_addr(tile) + (16 * k + j) * kColStride + 4 * cp));
-        a[j] = u2f(w << 16);
-        b[j] = u2f(w & 0xffff0000u);
-    }
-    if (rht) {
-        rht16(a, signs);
-        rht16(b, signs);
-    }
-    uint32_t ma = 0, mb = 0;
+        for (int j = 0; j < 16; ++j) {
+            uint32_t w;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(base + (16 * k + j) * (kColCols * 2) + 4 * cp));
+            a[j] = u2f(w << 16);
+            b[j] = u2f(w & 0xffff0000u);
+        }
+        if (rht) {
+            rht16(a, signs);
+            rht16(b, signs);
+        }
+        uint32_t ma = 0, mb = 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        ma = max(ma, f2u(a[j]) & 0x7fffffffu);
-        mb = max(mb, f2u(b[j]) & 0x7fffffffu);
-    }
+        for (int j = 0; j < 16; ++j) {
+            ma = max(ma, f2u(a[j]) & 0x7fffffffu);
+            mb = max(mb, f2u(b[j]) & 0x7fffffffu);
+        }
+        if constexpr (MODE == 0) {
+            m_all = max(m_all, max(ma, mb));
+        } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t c = c0 + 2 * cp + h;
+                const int64_t rb = r0 + 16 * k;                      // first row of the block
+                uint2 words;
+                const uint32_t sb = nv_block_codes<MODE == 2>(h ? b : a, h ? mb : ma, s_t, denom,
+                                                             uint64_t(c) * uint64_t(rows) + uint64_t(rb), sr_keys,
+                                                             words);
+                *reinterpret_cast<uint2*>(q + c * (rows / 2) + rb / 2) = words;
+                const uint32_t blk = uint32_t(rb / 16);
+                const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(c), blk, spr) : uint64_t(c) * spr + blk;
+                s[so] = uint8_t(sb);
+            }
+        }
+    });
     if constexpr (MODE == 0) {
-        uint32_t m = max(ma, mb);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            uint32_t v = 0;
-            for (int w = 0; w < 8; ++w) v = max(v, wmax[w]);
-            if (v) atomicMax(amax_bits, v);
-        }
-    } else {
-        const uint32_t spr = uint32_t(rows / 16);                 // scale columns per output row
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t c = c0 + 2 * cp + h;
-            const int64_t rb = r0 + 16 * k;                          // first row of the block
-            uint2 words;
-            const uint32_t sb = nv_block_codes<MODE == 2>(h ? b : a, h ? mb : ma, s_t, denom,
-                                                         uint64_t(c) * uint64_t(rows) + uint64_t(rb), sr_keys, words);
-            *reinterpret_cast<uint2*>(q + c * (rows / 2) + rb / 2) = words;
-            const uint32_t blk = uint32_t(rb / 16);
-            const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(c), blk, spr) : uint64_t(c) * spr + blk;
-            s[so] = uint8_t(sb);
-        }
+        for (int o = 16; o > 0; o >>= 1) m_all = max(m_all, __shfl_xor_sync(0xffffffffu, m_all, o));
+        if (lane == 0 && m_all) atomicMax(amax_bits, m_all);
     }
 }
 
@@ -462,17 +468,9 @@ extern "C" fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t col
     const int mma = layout == FP4Q_SCALES_MMA;
     const PhiloxKeys keys = philox_keys(sr_seed);
     if (block_axis == 0) {
-        const dim3 grid(unsigned(cols / kColCols), unsigned(rows / kColRows), 1);
-        if (rows > 0 && unsigned(rows / kColRows) > 65535u)
-            return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "nv_quantize: block_axis 0 needs rows <= 8388480");
         if (!amax_in) {
             uint32_t* w = static_cast<uint32_t*>(workspace);
             if ((st = zero_amax_word(w, s, "nv_quantize")) != FP4Q_OK) return st;
-            if (rows > 0 && cols > 0) {
-                nv_col_kernel<0><<<grid, 256, 0, s>>>(xb, rows, cols, ld_x * 2, rht, rht_seed, keys, nullptr, nullptr,
-                                                      nullptr, w, q, scales, mma);
-                if ((st = check_launch("nv_quantize amax")) != FP4Q_OK) return st;
-            }
             amax_ptr = reinterpret_cast<const float*>(w);
         }
         if (rows == 0 || cols == 0) {
@@ -480,13 +478,20 @@ extern "C" fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t col
                                                      scales, 0);
             return check_launch("nv_quantize");
         }
-        if (rounding == FP4Q_SR)
-            nv_col_kernel<2><<<grid, 256, 0, s>>>(xb, rows, cols, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out,
-                                                  tensor_scale_out, nullptr, q, scales, mma);
-        else
-            nv_col_kernel<1><<<grid, 256, 0, s>>>(xb, rows, cols, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out,
-                                                  tensor_scale_out, nullptr, q, scales, mma);
-        return check_launch("nv_quantize");
+        CUtensorMap tmap;
+        if ((st = ring::encode_bf16_tile_map(&tmap, x, rows, cols, ld_x, kColCols, kColRows)) != FP4Q_OK) return st;
+        const uint32_t smem = ring::smem_bytes(kColTileBytes);
+        const int64_t ngroups = (rows / kColRows) * (cols / kColCols);
+        auto launch = [&](auto kernel, uint32_t* bits) {
+            const int per_sm = resident_per_sm_smem(kernel, ring::kMaxThreads, smem);
+            const int64_t grid = std::min<int64_t>(ngroups, int64_t(per_sm) * sms);
+            kernel<<<unsigned(grid), ring::kMaxThreads, smem, s>>>(tmap, rows, cols, rht, rht_seed, keys, amax_ptr,
+                                                                    amax_out, tensor_scale_out, bits, q, scales, mma,
+                                                                    status_word());
+            return check_launch("nv_quantize (block_axis 0)");
+        };
+        if (!amax_in && (st = launch(nv_col_kernel<0>, static_cast<uint32_t*>(workspace))) != FP4Q_OK) return st;
+        return rounding == FP4Q_SR ? launch(nv_col_kernel<2>, nullptr) : launch(nv_col_kernel<1>, nullptr);
     }
     const uint32_t tpr = uint32_t(cols / 16);
     int tpb = 32, nx = 1;

@@ -7,6 +7,9 @@
 // whatever the consumers' register use, so the loads no longer wait behind the
 // conversion arithmetic.
 //
+// The groups may also be 2D tiles moved by TMA tensor copies (the column-wise
+// quantizers): `encode_bf16_tile_map` builds their tensor maps.
+//
 // Every wait is bounded.  A wait that runs out sets a bit in the library's
 // status word and an abort flag the other roles poll; the producer then waits
 // (bounded by time only) for the copies it has already issued before the CTA
@@ -20,10 +23,11 @@
 namespace fp4q {
 namespace ring {
 
-constexpr int kStages = 4;
+constexpr int kStages = 4;                             // default ring depth
+constexpr int kMaxStages = 8;
 constexpr int kMaxConsumerWarps = 8;
 constexpr int kMaxThreads = 32 * (1 + kMaxConsumerWarps);
-constexpr uint32_t kHeaderBytes = 128;                 // barriers + abort flag
+constexpr uint32_t kHeaderBytes = 256;                 // barriers (2 x kMaxStages) + abort flag
 constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s
 constexpr uint32_t kMaxStageBytes = 16384;
 
@@ -33,6 +37,7 @@ constexpr uint32_t kMaxStageBytes = 16384;
 // as evenly as possible (ties: more warps, fewer rows).  rps = 0 when one row
 // does not fit a stage.
 struct Shape { uint32_t rps, warps; };
+
 inline Shape ring_shape(uint32_t units, uint32_t row_bytes) {
     Shape best{0, 0};
     if (units == 0 || row_bytes == 0 || row_bytes > kMaxStageBytes) return best;
@@ -45,29 +50,38 @@ inline Shape ring_shape(uint32_t units, uint32_t row_bytes) {
         }
     return best;
 }
-inline uint32_t smem_bytes(uint32_t stage_bytes) { return kHeaderBytes + kStages * stage_bytes; }
+inline uint32_t smem_bytes(uint32_t stage_bytes, int stages = kStages) {
+    return kHeaderBytes + uint32_t(stages) * stage_bytes;
+}
+
+// Tensor map of a BF16 [rows, cols] matrix (row stride ld elements) for TMA
+// tile loads of box_cols x box_rows elements, no swizzle (dense rows).
+fp4q_status encode_bf16_tile_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                 uint32_t box_cols, uint32_t box_rows);
 
 struct Ring {
-    uint8_t* stage0;          // first stage (16-byte aligned)
+    uint8_t* stage0;          // first stage (128-byte aligned)
     uint32_t stage_bytes;
-    uint32_t bar0;            // full[kStages] then empty[kStages]
+    int stages;
+    uint32_t bar0;            // full[stages] then empty[stages]
     volatile int* abort;
 
     __device__ uint32_t full(int s) const { return bar0 + 8u * uint32_t(s); }
-    __device__ uint32_t empty(int s) const { return bar0 + 8u * uint32_t(kStages + s); }
+    __device__ uint32_t empty(int s) const { return bar0 + 8u * uint32_t(stages + s); }
     __device__ uint8_t* stage(int s) const { return stage0 + uint32_t(s) * stage_bytes; }
 };
 
 // Called by every thread of the CTA; thread 0 initialises the barriers.  The
 // CTA is one producer warp and blockDim.x / 32 - 1 consumer warps.
-__device__ __forceinline__ Ring make_ring(uint8_t* smem, uint32_t stage_bytes) {
+__device__ __forceinline__ Ring make_ring(uint8_t* smem, uint32_t stage_bytes, int stages = kStages) {
     Ring r;
     r.stage0 = smem + kHeaderBytes;
     r.stage_bytes = stage_bytes;
+    r.stages = stages;
     r.bar0 = tc::smem_u32(smem);
-    r.abort = reinterpret_cast<volatile int*>(smem + 8 * 2 * kStages);
+    r.abort = reinterpret_cast<volatile int*>(smem + 8 * 2 * kMaxStages);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < stages; ++s) {
             tc::mbar_init(r.full(s), 1);
             tc::mbar_init(r.empty(s), blockDim.x / 32 - 1);
         }
@@ -100,11 +114,11 @@ __device__ __forceinline__ void produce(const Ring& r, int64_t ngroups, uint32_t
         }
         issue(r.stage(stage), r.full(stage), g);
         ++issued;
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (++stage == r.stages) { stage = 0; phase ^= 1; }
     }
     // the copies already issued land before the CTA may exit
-    for (int64_t i = 0; i < kStages && i < issued; ++i) {
-        if (--stage < 0) { stage = kStages - 1; phase ^= 1; }
+    for (int64_t i = 0; i < r.stages && i < issued; ++i) {
+        if (--stage < 0) { stage = r.stages - 1; phase ^= 1; }
         if (!tc::mbar_wait_drain(r.full(stage), phase, kWaitLimitNs)) {
             flag_abort(r, status, bit);
             break;
@@ -130,7 +144,7 @@ __device__ __forceinline__ void consume(const Ring& r, int64_t ngroups, uint32_t
         fn(r.stage(stage), g);
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(r.empty(stage));
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (++stage == r.stages) { stage = 0; phase ^= 1; }
     }
 }
 
