@@ -225,17 +225,19 @@ inline unsigned row_grid_y(int64_t rows, int nx, int sms, int per_sm = 8) {
 // needed), remembered per kernel, device and size.
 template <typename Kernel>
 inline int resident_per_sm_smem(Kernel kernel, int threads, uint32_t smem) {
-    struct Entry { int dev; int threads; uint32_t smem; int n; };
+    // keyed by the kernel itself: instances of one template share a type
+    struct Entry { const void* fn; int dev; int threads; uint32_t smem; int n; };
     static Entry cache[16] = {};
     static int next = 0;
     int dev = 0;
     cudaGetDevice(&dev);
+    const void* fn = reinterpret_cast<const void*>(kernel);
     for (const Entry& e : cache)
-        if (e.n && e.dev == dev && e.threads == threads && e.smem == smem) return e.n;
+        if (e.n && e.fn == fn && e.dev == dev && e.threads == threads && e.smem == smem) return e.n;
     if (smem > 48 * 1024) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
-    cache[next] = Entry{dev, threads, smem, n};
+    cache[next] = Entry{fn, dev, threads, smem, n};
     next = (next + 1) % 16;
     return n;
 }
