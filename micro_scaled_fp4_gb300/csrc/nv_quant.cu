@@ -261,10 +261,12 @@ __device__ __forceinline__ uint32_t nv_block_codes(const float (&t)[16], uint32_
     return sb;
 }
 
-__device__ __forceinline__ float nv_tensor_scale(const float* amax_ptr, float* amax_out, float* st_out) {
+// `writer_tid`: the thread of CTA 0 that publishes amax and s_t.
+__device__ __forceinline__ float nv_tensor_scale(const float* amax_ptr, float* amax_out, float* st_out,
+                                                 uint32_t writer_tid = 0) {
     const float amax = *amax_ptr;
     const float s_t = __fdiv_rn(amax, 2688.0f);        // 6 * 448
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == writer_tid) {
         if (amax_out) *amax_out = amax;
         *st_out = s_t;
     }
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(ring::kMaxThreads) nv_col_kernel(
     const uint32_t signs = rht == 1 ? rht_signs(rht_seed) : 0u;
     float s_t = 0.0f, denom = 0.0f;
     if constexpr (MODE != 0) {
-        s_t = nv_tensor_scale(amax_ptr, amax_out, st_out);
+        s_t = nv_tensor_scale(amax_ptr, amax_out, st_out, 32);      // thread 0 is the producer
         denom = __fmul_rn(6.0f, s_t);
     }
     const uint32_t t = threadIdx.x - 32, cp = t & 31u, k = t >> 5;
