@@ -358,7 +358,10 @@ __global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_col_kernel(
     }
     const uint32_t t = threadIdx.x - 32, cp = t & 63u, k = t >> 6;
     const uint32_t spr = uint32_t(rows / 32);
-    ring::consume(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, int64_t g) {
+    // output tile staging: 128 output rows x (4 blocks x 16 code bytes | 4 scale bytes)
+    __shared__ __align__(16) uint8_t oq[kMxColCols * 64];
+    __shared__ __align__(16) uint8_t os[kMxColCols * 4];
+    ring::consume_together(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, int64_t g) {
         const int64_t rt = g / ctiles, ct = g - rt * ctiles;
         const int64_t r0 = rt * kMxColRows, c0 = ct * kMxColCols;
         const uint32_t base = tc::smem_u32(st);
@@ -378,11 +381,24 @@ __global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_col_kernel(
             uint4 codes;
             uint32_t sb;
             quantize_block<kBF16>(h ? B : A, codes, sb);
-            const int64_t c = c0 + 2 * cp + h;
-            *reinterpret_cast<uint4*>(q + c * (rows / 2) + int64_t(blk) * 16) = codes;
-            const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(c), blk, spr) : uint64_t(c) * spr + blk;
-            s[so] = uint8_t(sb);
+            const uint32_t cl = 2 * cp + h;
+            *reinterpret_cast<uint4*>(oq + cl * 64 + 16 * k) = codes;
+            if (mma_layout) s[mma_scale_offset(uint64_t(c0 + cl), blk, spr)] = uint8_t(sb);
+            else os[cl * 4 + k] = uint8_t(sb);
         }
+        // all 256 consumers staged the tile: 64 contiguous code bytes (and 4
+        // scale bytes) per output row
+        tc::named_bar_sync(2, blockDim.x - 32);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint32_t u = t + 256 * i, row = u >> 2, ch = u & 3u;
+            *reinterpret_cast<uint4*>(q + (c0 + row) * (rows / 2) + r0 / 2 + 16 * ch) =
+                *reinterpret_cast<const uint4*>(oq + row * 64 + 16 * ch);
+        }
+        if (!mma_layout && t < kMxColCols)
+            *reinterpret_cast<uint32_t*>(s + (c0 + t) * int64_t(spr) + r0 / 32) =
+                *reinterpret_cast<const uint32_t*>(os + t * 4);
+        tc::named_bar_sync(2, blockDim.x - 32);                // the staging may be rewritten
     });
 }
 

@@ -359,8 +359,11 @@ __global__ void __launch_bounds__(ring::kMaxThreads) nv_col_kernel(
     }
     const uint32_t t = threadIdx.x - 32, cp = t & 31u, k = t >> 5;
     const uint32_t spr = uint32_t(rows / 16);                 // scale columns per output row
+    // output tile staging: 64 output rows x (8 blocks x 8 code bytes | 8 scale bytes)
+    __shared__ __align__(16) uint8_t oq[kColCols * 64];
+    __shared__ __align__(16) uint8_t os[kColCols * 8];
     uint32_t m_all = 0;
-    ring::consume(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, int64_t g) {
+    ring::consume_together(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, int64_t g) {
         const int64_t rt = g / ctiles, ct = g - rt * ctiles;
         const int64_t r0 = rt * kColRows, c0 = ct * kColCols;
         const uint32_t base = tc::smem_u32(st);
@@ -387,17 +390,27 @@ __global__ void __launch_bounds__(ring::kMaxThreads) nv_col_kernel(
         } else {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int64_t c = c0 + 2 * cp + h;
+                const uint32_t cl = 2 * cp + h;                         // output row within the tile
+                const int64_t c = c0 + cl;
                 const int64_t rb = r0 + 16 * k;                      // first row of the block
                 uint2 words;
                 const uint32_t sb = nv_block_codes<MODE == 2>(h ? b : a, h ? mb : ma, s_t, denom,
                                                              uint64_t(c) * uint64_t(rows) + uint64_t(rb), sr_keys,
                                                              words);
-                *reinterpret_cast<uint2*>(q + c * (rows / 2) + rb / 2) = words;
-                const uint32_t blk = uint32_t(rb / 16);
-                const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(c), blk, spr) : uint64_t(c) * spr + blk;
-                s[so] = uint8_t(sb);
+                *reinterpret_cast<uint2*>(oq + cl * 64 + 8 * k) = words;
+                if (mma_layout) s[mma_scale_offset(uint64_t(c), uint32_t(rb / 16), spr)] = uint8_t(sb);
+                else os[cl * 8 + k] = uint8_t(sb);
             }
+            // all 256 consumers staged the tile: write 64 contiguous code bytes
+            // (and 8 scale bytes) per output row
+            tc::named_bar_sync(2, blockDim.x - 32);
+            const uint32_t row = t >> 2, ch = t & 3u;
+            *reinterpret_cast<uint4*>(q + (c0 + row) * (rows / 2) + r0 / 2 + 16 * ch) =
+                *reinterpret_cast<const uint4*>(oq + row * 64 + 16 * ch);
+            if (!mma_layout && t < kColCols)
+                *reinterpret_cast<uint2*>(s + (c0 + t) * int64_t(spr) + r0 / 16) =
+                    *reinterpret_cast<const uint2*>(os + t * 8);
+            tc::named_bar_sync(2, blockDim.x - 32);            // the staging may be rewritten
         }
     });
     if constexpr (MODE == 0) {

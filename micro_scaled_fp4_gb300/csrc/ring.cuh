@@ -148,5 +148,28 @@ __device__ __forceinline__ void consume(const Ring& r, int64_t ngroups, uint32_t
     }
 }
 
+// As consume, for consumers that synchronise among themselves inside `fn`
+// (named barrier 2): the go / give-up decision is taken by all consumer
+// threads together (a barrier AND-reduction on named barrier 1), so no warp
+// can stop while another waits for it at barrier 2.
+template <typename Consume>
+__device__ __forceinline__ void consume_together(const Ring& r, int64_t ngroups, uint32_t* status, uint32_t bit,
+                                                 Consume fn) {
+    const uint32_t nthreads = blockDim.x - 32;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
+        const bool got = tc::mbar_wait(r.full(stage), phase, r.abort, kWaitLimitNs);
+        if (!tc::named_bar_and(1, nthreads, got)) {
+            if (threadIdx.x == 32) flag_abort(r, status, bit);
+            break;
+        }
+        fn(r.stage(stage), g);
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) tc::mbar_arrive(r.empty(stage));
+        if (++stage == r.stages) { stage = 0; phase ^= 1; }
+    }
+}
+
 }  // namespace ring
 }  // namespace fp4q
