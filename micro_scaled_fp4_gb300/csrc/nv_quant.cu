@@ -274,29 +274,31 @@ __device__ __forceinline__ float nv_tensor_scale(const float* amax_ptr, float* a
 }
 
 // 2D (16 x 16) block scaling for weights ("Pretraining Large Language Models
-// with NVFP4", 2.B): a half-warp holds one tile, lane j its row j's 16
-// elements; the tile amax is the max over the half-warp; every row of the
-// tile stores the same scale byte ([rows, cols/16] layout).  No rotation.
+// with NVFP4", 2.B): one E4M3 scale per 16 x 16 tile from the tile amax, the
+// 1D rules otherwise, no rotation; every row of the tile stores the same scale
+// byte ([rows, cols/16] layout).  A CTA takes 16 rows x 16 blocks (256
+// columns): warp w holds blocks 2w, 2w + 1, lane 16 h + j row j of block 2w + h
+// (each row's 64 bytes read together), and the tile amax is a max over the
+// half-warp.  Codes and scales are staged per CTA tile so that each row's 128
+// code bytes go out contiguously.
 template <bool SR>
 __global__ void __launch_bounds__(256) nv_quant_2d_kernel(
     const uint8_t* __restrict__ x, int64_t rows, uint32_t tpr, int64_t ld_x_bytes, const PhiloxKeys sr_keys,
     const float* __restrict__ amax_ptr, float* __restrict__ amax_out, float* __restrict__ st_out,
     uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout) {
+    __shared__ __align__(16) uint8_t oq[16 * 128];
+    __shared__ uint8_t os[16 * 16];
     const float s_t = nv_tensor_scale(amax_ptr, amax_out, st_out);
     const float denom = __fmul_rn(6.0f, s_t);
-    // A warp takes two adjacent blocks (b, b + 1) of the same 16 rows: lane
-    // 16 h + j holds row j of block b + h, so each row's 64 bytes are read
-    // together.  Units are (tile row, block pair); the loop runs per warp so
-    // both half-warps stay in the shuffles, and a half past the row end works
-    // on nothing.
-    const uint32_t pairs = (tpr + 1) / 2;
-    const int64_t units = (rows / 16) * int64_t(pairs);
-    const uint32_t j = threadIdx.x & 15u, h = (threadIdx.x >> 4) & 1u;
+    const uint32_t ctiles = (tpr + 15) / 16;
+    const int64_t ntiles = (rows / 16) * int64_t(ctiles);
+    const uint32_t warp = threadIdx.x >> 5, j = threadIdx.x & 15u, h = (threadIdx.x >> 4) & 1u;
+    const uint32_t bl = 2 * warp + h;                              // block within the CTA tile
     const uint64_t cols = uint64_t(tpr) * 16;
-    const int64_t wstride = int64_t(gridDim.x) * (blockDim.x / 32);
-    for (int64_t un = int64_t(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; un < units; un += wstride) {
-        const int64_t tr = un / pairs;
-        const uint32_t b = 2 * uint32_t(un - tr * pairs) + h;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t tr = tile / ctiles;
+        const uint32_t ct = uint32_t(tile - tr * ctiles);
+        const uint32_t b = 16 * ct + bl, nblk = min(16u, tpr - 16 * ct);
         const bool valid = b < tpr;
         const int64_t r = tr * 16 + j;
         float t[16];
@@ -308,12 +310,25 @@ __global__ void __launch_bounds__(256) nv_quant_2d_kernel(
         }
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) ab = max(ab, __shfl_xor_sync(0xffffffffu, ab, o));
-        if (!valid) continue;
-        uint2 words;
-        const uint32_t sb = nv_block_codes<SR>(t, ab, s_t, denom, uint64_t(r) * cols + uint64_t(b) * 16, sr_keys, words);
-        *reinterpret_cast<uint2*>(q + uint64_t(r) * (cols / 2) + uint64_t(b) * 8) = words;
-        const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(r), b, tpr) : uint64_t(r) * tpr + b;
-        s[so] = uint8_t(sb);
+        if (valid) {
+            uint2 words;
+            const uint32_t sb = nv_block_codes<SR>(t, ab, s_t, denom, uint64_t(r) * cols + uint64_t(b) * 16, sr_keys,
+                                                   words);
+            *reinterpret_cast<uint2*>(oq + j * 128 + 8 * bl) = words;
+            if (mma_layout) s[mma_scale_offset(uint64_t(r), b, tpr)] = uint8_t(sb);
+            else os[j * 16 + bl] = uint8_t(sb);
+        }
+        __syncthreads();
+        {   // row t / 16, block t % 16: 8 code bytes (16 threads = one row's 128 bytes)
+            const uint32_t row = threadIdx.x >> 4, blk = threadIdx.x & 15u;
+            if (blk < nblk) {
+                const int64_t rr = tr * 16 + row;
+                *reinterpret_cast<uint2*>(q + rr * int64_t(cols / 2) + (16 * ct + blk) * 8) =
+                    *reinterpret_cast<const uint2*>(oq + row * 128 + 8 * blk);
+                if (!mma_layout) s[rr * int64_t(tpr) + 16 * ct + blk] = os[row * 16 + blk];
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -570,9 +585,9 @@ extern "C" fp4q_status fp4q_nv_quantize_2d(const void* x, int64_t rows, int64_t 
         return check_launch("nv_quantize_2d");
     }
     const int mma = layout == FP4Q_SCALES_MMA;
-    const int64_t units = (rows / 16) * int64_t((tpr + 1) / 2);        // warp units
+    const int64_t tiles = (rows / 16) * int64_t((tpr + 15) / 16);       // 16 rows x 16 blocks
     const int per_sm = resident_per_sm(nv_quant_2d_kernel<true>, 256);
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((units + 7) / 8, int64_t(per_sm) * sms));
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles, int64_t(per_sm) * sms));
     if (rounding == FP4Q_SR)
         nv_quant_2d_kernel<true><<<unsigned(grid), 256, 0, s>>>(xb, rows, tpr, ld_x * 2, keys, amax_ptr, amax_out,
                                                                 tensor_scale_out, q, scales, mma);
