@@ -358,7 +358,9 @@ __global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_col_kernel(
     }
     const uint32_t t = threadIdx.x - 32, cp = t & 63u, k = t >> 6;
     const uint32_t spr = uint32_t(rows / 32);
-    // output tile staging: 128 output rows x (4 blocks x 16 code bytes | 4 scale bytes)
+    // output tile staging, block-major: block k's 16 code bytes of output row
+    // cl at oq[k * 2048 + 16 * (cl ^ 2k)] (the XOR keeps the row-wise reads
+    // conflict-free)
     __shared__ __align__(16) uint8_t oq[kMxColCols * 64];
     __shared__ __align__(16) uint8_t os[kMxColCols * 4];
     ring::consume_together(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, int64_t g) {
@@ -382,7 +384,7 @@ __global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_col_kernel(
             uint32_t sb;
             quantize_block<kBF16>(h ? B : A, codes, sb);
             const uint32_t cl = 2 * cp + h;
-            *reinterpret_cast<uint4*>(oq + cl * 64 + 16 * k) = codes;
+            *reinterpret_cast<uint4*>(oq + k * 2048 + 16 * (cl ^ (2 * k))) = codes;
             if (mma_layout) s[mma_scale_offset(uint64_t(c0 + cl), blk, spr)] = uint8_t(sb);
             else os[cl * 4 + k] = uint8_t(sb);
         }
@@ -393,7 +395,7 @@ __global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_col_kernel(
         for (int i = 0; i < 2; ++i) {
             const uint32_t u = t + 256 * i, row = u >> 2, ch = u & 3u;
             *reinterpret_cast<uint4*>(q + (c0 + row) * (rows / 2) + r0 / 2 + 16 * ch) =
-                *reinterpret_cast<const uint4*>(oq + row * 64 + 16 * ch);
+                *reinterpret_cast<const uint4*>(oq + ch * 2048 + 16 * (row ^ (2 * ch)));
         }
         if (!mma_layout && t < kMxColCols)
             *reinterpret_cast<uint32_t*>(s + (c0 + t) * int64_t(spr) + r0 / 32) =

@@ -279,8 +279,9 @@ __device__ __forceinline__ float nv_tensor_scale(const float* amax_ptr, float* a
 // byte ([rows, cols/16] layout).  A CTA takes 16 rows x 16 blocks (256
 // columns): warp w holds blocks 2w, 2w + 1, lane 16 h + j row j of block 2w + h
 // (each row's 64 bytes read together), and the tile amax is a max over the
-// half-warp.  Codes and scales are staged per CTA tile so that each row's 128
-// code bytes go out contiguously.
+// half-warp.  Codes and scales are staged per CTA tile (block-major, rows
+// XOR-swizzled by the block index: conflict-free both ways) so that each row's
+// 128 code bytes go out contiguously.
 template <bool SR>
 __global__ void __launch_bounds__(256) nv_quant_2d_kernel(
     const uint8_t* __restrict__ x, int64_t rows, uint32_t tpr, int64_t ld_x_bytes, const PhiloxKeys sr_keys,
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__(256) nv_quant_2d_kernel(
             uint2 words;
             const uint32_t sb = nv_block_codes<SR>(t, ab, s_t, denom, uint64_t(r) * cols + uint64_t(b) * 16, sr_keys,
                                                    words);
-            *reinterpret_cast<uint2*>(oq + j * 128 + 8 * bl) = words;
+            *reinterpret_cast<uint2*>(oq + bl * 128 + 8 * (j ^ bl)) = words;     // block-major, XOR-swizzled rows
             if (mma_layout) s[mma_scale_offset(uint64_t(r), b, tpr)] = uint8_t(sb);
             else os[j * 16 + bl] = uint8_t(sb);
         }
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(256) nv_quant_2d_kernel(
             if (blk < nblk) {
                 const int64_t rr = tr * 16 + row;
                 *reinterpret_cast<uint2*>(q + rr * int64_t(cols / 2) + (16 * ct + blk) * 8) =
-                    *reinterpret_cast<const uint2*>(oq + row * 128 + 8 * blk);
+                    *reinterpret_cast<const uint2*>(oq + blk * 128 + 8 * (row ^ blk));
                 if (!mma_layout) s[rr * int64_t(tpr) + 16 * ct + blk] = os[row * 16 + blk];
             }
         }
@@ -374,7 +375,9 @@ __global__ void __launch_bounds__(ring::kMaxThreads) nv_col_kernel(
     }
     const uint32_t t = threadIdx.x - 32, cp = t & 31u, k = t >> 5;
     const uint32_t spr = uint32_t(rows / 16);                 // scale columns per output row
-    // output tile staging: 64 output rows x (8 blocks x 8 code bytes | 8 scale bytes)
+    // output tile staging, block-major: block k's 8 code bytes of output row cl
+    // at oq[k * 512 + 8 * (cl ^ 8 (k / 2))] -- the XOR spreads both the writes
+    // (a warp: one block, 32 rows) and the row-wise reads over all banks
     __shared__ __align__(16) uint8_t oq[kColCols * 64];
     __shared__ __align__(16) uint8_t os[kColCols * 8];
     uint32_t m_all = 0;
@@ -412,16 +415,17 @@ __global__ void __launch_bounds__(ring::kMaxThreads) nv_col_kernel(
                 const uint32_t sb = nv_block_codes<MODE == 2>(h ? b : a, h ? mb : ma, s_t, denom,
                                                              uint64_t(c) * uint64_t(rows) + uint64_t(rb), sr_keys,
                                                              words);
-                *reinterpret_cast<uint2*>(oq + cl * 64 + 8 * k) = words;
+                *reinterpret_cast<uint2*>(oq + k * 512 + 8 * (cl ^ (8 * (k >> 1)))) = words;
                 if (mma_layout) s[mma_scale_offset(uint64_t(c), uint32_t(rb / 16), spr)] = uint8_t(sb);
                 else os[cl * 8 + k] = uint8_t(sb);
             }
             // all 256 consumers staged the tile: write 64 contiguous code bytes
             // (and 8 scale bytes) per output row
             tc::named_bar_sync(2, blockDim.x - 32);
-            const uint32_t row = t >> 2, ch = t & 3u;
-            *reinterpret_cast<uint4*>(q + (c0 + row) * (rows / 2) + r0 / 2 + 16 * ch) =
-                *reinterpret_cast<const uint4*>(oq + row * 64 + 16 * ch);
+            const uint32_t row = t >> 2, ch = t & 3u;           // blocks 2ch, 2ch + 1 of output row `row`
+            const uint2 lo = *reinterpret_cast<const uint2*>(oq + (2 * ch) * 512 + 8 * (row ^ (8 * ch)));
+            const uint2 hi = *reinterpret_cast<const uint2*>(oq + (2 * ch + 1) * 512 + 8 * (row ^ (8 * ch)));
+            *reinterpret_cast<uint4*>(q + (c0 + row) * (rows / 2) + r0 / 2 + 16 * ch) = make_uint4(lo.x, lo.y, hi.x, hi.y);
             if (!mma_layout && t < kColCols)
                 *reinterpret_cast<uint2*>(s + (c0 + t) * int64_t(spr) + r0 / 16) =
                     *reinterpret_cast<const uint2*>(os + t * 8);
