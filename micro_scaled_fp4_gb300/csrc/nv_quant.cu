@@ -347,7 +347,7 @@ constexpr int kColRows = 128, kColCols = 64;
 constexpr uint32_t kColTileBytes = kColRows * kColCols * 2;
 
 template <int MODE>
-__global__ void __launch_bounds__(ring::kMaxThreads) nv_col_kernel(
+__global__ void __launch_bounds__(ring::kMaxThreads, MODE == 2 ? 2 : 3) nv_col_kernel(
     const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_t cols, int rht, uint64_t rht_seed,
     const PhiloxKeys sr_keys, const float* __restrict__ amax_ptr, float* __restrict__ amax_out,
     float* __restrict__ st_out, uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ q,
