@@ -241,6 +241,25 @@ def test_nv_quantize(fq, oracle, shape, rht, rounding, layout):
     assert np.array_equal(from_mma_layout(sg, R, C // 16) if layout else sg, ref["s"])
 
 
+@pytest.mark.parametrize("pad,offset", [(0, 0), (16, 0), (48, 16), (256, 256)])
+@pytest.mark.parametrize("rounding", [0, 1])
+def test_nv_quantize_strided_sources(fq, oracle, pad, offset, rounding):
+    """Row-strided BF16 views (row stride and base a multiple of 32 bytes, an
+    odd row count): the same result as the contiguous tensor."""
+    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
+    R, C = 37, 768
+    x = W.gradient_bf16(R, C, seed=11)
+    big = torch.zeros((R, C + pad + offset), dtype=torch.bfloat16, device="cuda")
+    big[:, offset:offset + C] = dev_bf16(x)
+    xv = big[:, offset:offset + C]
+    r = fq.nv_quantize(xv, rht=True, rht_seed=7, rounding=rounding, sr_seed=99)
+    ref = oracle.nv_quantize(x, rht=True, rht_seed=7, rounding="sr" if rounding else "rne", sr_seed=99)
+    assert host(r["amax"])[0] == ref["amax"]
+    assert np.array_equal(host(r["q"]), ref["q"])
+    assert np.array_equal(host(r["scales"]), ref["s"])
+
+
 def test_nv_quantize_zero_and_tiny(fq, oracle):
     x = np.zeros((4, 64), dtype=np.uint16)
     r = fq.nv_quantize(dev_bf16(x))
