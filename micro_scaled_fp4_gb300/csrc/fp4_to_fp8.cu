@@ -41,17 +41,25 @@ __device__ uint32_t shifted_magnitude(uint32_t c, int sh) {
     return 0u;
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
 // Eight packed codes (one 32-bit word, element j in nibble j) -> eight E4M3
 // bytes, given the magnitude row (lut.x = codes 0..3, lut.y = codes 4..7).
+// The magnitudes are two byte-permute lookups (selector nibbles = the codes'
+// low three bits).  The signs use prmt's sign-replicate selectors (selector
+// bit 3): nibble 2k + 1's sign bit is the top bit of byte k of w, nibble 2k's
+// the top bit of byte k of w << 4, so one permute spreads four signs to
+// 0x00 / 0xff bytes.
 __device__ __forceinline__ uint2 remap8(uint32_t w, uint2 lut) {
-    const uint32_t mag_lo = __byte_perm(lut.x, lut.y, w & 0x7777u);
-    const uint32_t mag_hi = __byte_perm(lut.x, lut.y, (w >> 16) & 0x7777u);
-    // nibble j's sign bit (4j + 3) goes to bit 8j + 7 of the output
-    const uint32_t a = __byte_perm(w, 0, 0x4140);   // bytes 0, 1 of w -> bytes 0, 2
-    const uint32_t c = __byte_perm(w, 0, 0x4342);   // bytes 2, 3 of w -> bytes 0, 2
-    const uint32_t sgn_lo = ((a << 4) & 0x00800080u) | ((a << 8) & 0x80008000u);
-    const uint32_t sgn_hi = ((c << 4) & 0x00800080u) | ((c << 8) & 0x80008000u);
-    return make_uint2(mag_lo | sgn_lo, mag_hi | sgn_hi);
+    const uint32_t wm = w & 0x77777777u;
+    const uint32_t mag_lo = prmt(lut.x, lut.y, wm), mag_hi = prmt(lut.x, lut.y, wm >> 16);
+    const uint32_t w4 = w << 4;
+    const uint32_t sgn_lo = prmt(w, w4, 0x9D8Cu), sgn_hi = prmt(w, w4, 0xBFAEu);
+    return make_uint2(mag_lo | (sgn_lo & 0x80808080u), mag_hi | (sgn_hi & 0x80808080u));
 }
 
 // One 32-element block: `cw` its 16 bytes of codes, `sw` the four E8M0 bytes of
