@@ -42,7 +42,11 @@ namespace fp4q {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 256;           // elements
-constexpr int STAGES = 3;
+// Ring depth: 3 stages, or 4 for MXFP8 operands, whose stages hold half the
+// K of an FP4 stage and whose MMAs therefore wait on the loads more often.
+// With 3 stages the BF16 output goes through a shared-memory staging area and
+// TMA stores; with 4 the staging area's room goes to the ring and the
+// epilogue stores BF16 rows straight from registers.
 constexpr uint32_t A_BYTES = BM * BK / 2;             // 16384
 constexpr uint32_t B_HALF_BYTES = 128 * BK / 2;       // 16384
 constexpr uint32_t B_BYTES = 2 * B_HALF_BYTES;
@@ -52,11 +56,16 @@ constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;   //
 // BF16 output staging: two 64-column x 128-row boxes, rows of 128 bytes with the
 // TMA 128-byte swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)).
 constexpr uint32_t BOX_BYTES = 128 * 128;             // 64 BF16 columns x 128 rows
-constexpr uint32_t STAGING_BYTES = 2 * BOX_BYTES;
-constexpr uint32_t STAGING_OFF = STAGES * STAGE_BYTES;
-constexpr uint32_t BARS_OFF = STAGING_OFF + STAGING_BYTES;
-constexpr uint32_t PREFIX_OFF = BARS_OFF + 256;
-constexpr uint32_t SMEM_BYTES = PREFIX_OFF + 4 * 260 + 1024;
+template <int NST>
+struct Layout {
+    static constexpr bool staged_store = NST <= 3;
+    static constexpr uint32_t staging_bytes = staged_store ? 2 * BOX_BYTES : 0;
+    static constexpr uint32_t staging_off = NST * STAGE_BYTES;
+    static constexpr uint32_t bars_off = staging_off + staging_bytes;
+    static constexpr uint32_t prefix_off = bars_off + 256;
+    static constexpr uint32_t smem_bytes = prefix_off + 4 * 260 + 1024;
+    static_assert(smem_bytes <= 232448, "GEMM shared memory above the 227 KB per-CTA limit");
+};
 constexpr int kThreads = 320;          // producer warp, MMA warp, 8 epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SFA = 256;                    // 16 columns
@@ -161,18 +170,19 @@ __device__ __forceinline__ void stage_bf16x32(uint32_t staging, int row, int c, 
     }
 }
 
-template <int EPI>
+template <int EPI, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_d, const GemmArgs args) {
+    using LY = Layout<STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BARS_OFF);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::bars_off);
     // bars[0..STAGES) full, [STAGES..2 STAGES) empty, then tmem_full, tmem_empty, mma drain
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
     volatile int* abort = reinterpret_cast<volatile int*>(bars + 13);
-    int* tile_prefix = reinterpret_cast<int*>(smem + PREFIX_OFF);
-    const uint32_t staging = tc::smem_u32(smem + STAGING_OFF);
+    int* tile_prefix = reinterpret_cast<int*>(smem + LY::prefix_off);
+    const uint32_t staging = tc::smem_u32(smem + LY::staging_off);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bar0 = tc::smem_u32(bars);
@@ -451,7 +461,42 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         args.h_scales[int64_t(row) * (hcols / 32) + col / 32] = uint8_t(e + 127);
                     }
                 }
-            } else if (args.d_bf16 && t.a_row0 + BM <= t.row_end + (args.groups ? 0 : BM)) {
+            } else if (!LY::staged_store && args.d_bf16) {
+                // BF16 from registers: the warp's 32 rows x 128 columns leave TMEM
+                // first and the accumulator goes back to the MMA thread; then each
+                // thread writes its row's 256 bytes with 16-byte stores.
+                uint32_t hold[4][16];
+#pragma unroll
+                for (int c = 0; c < 4; c += 2) {
+                    uint32_t r0[32], r1[32];
+                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(128 * hf + 32 * c), r0);
+                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(128 * hf + 32 * c + 32), r1);
+                    tc::tmem_ld_wait();
+                    to_bf16x32(r0, alpha, hold[c]);
+                    to_bf16x32(r1, alpha, hold[c + 1]);
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tmem_empty);
+                if (row_ok) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int col = t.col0 + 128 * hf + 32 * c;
+                        uint8_t* dst = args.D + (int64_t(row) * args.ldd + col) * 2;
+                        if (args.N - col >= 32) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                reinterpret_cast<uint4*>(dst)[i] =
+                                    make_uint4(hold[c][4 * i], hold[c][4 * i + 1], hold[c][4 * i + 2], hold[c][4 * i + 3]);
+                        } else if (col < args.N) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (i < args.N - col)
+                                    reinterpret_cast<uint16_t*>(dst)[i] = uint16_t(hold[c][i >> 1] >> (16 * (i & 1)));
+                        }
+                    }
+                }
+            } else if (LY::staged_store && args.d_bf16 && t.a_row0 + BM <= t.row_end + (args.groups ? 0 : BM)) {
                 // BF16 through shared memory and TMA stores.  Each warp moves its 32 rows
                 // x 128 columns out of TMEM into registers, then the accumulator goes
                 // back to the MMA thread; half 0 is staged and stored, then half 1.
@@ -589,21 +634,31 @@ fp4q_status encode_output_map(CUtensorMap* map, void* D, int64_t rows, int64_t N
     return FP4Q_OK;
 }
 
-template <int EPI>
-fp4q_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const GemmArgs& a,
-                   int tiles_upper, int sms, cudaStream_t stream) {
+template <int EPI, int NST>
+fp4q_status launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const GemmArgs& a,
+                          int tiles_upper, int sms, cudaStream_t stream) {
+    constexpr uint32_t smem = Layout<NST>::smem_bytes;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (!attr_set[dev & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(SMEM_BYTES));
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(smem));
         if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
         attr_set[dev & 63] = true;
     }
     const int grid = tiles_upper < sms ? tiles_upper : sms;
-    gemm_kernel<EPI><<<grid, kThreads, SMEM_BYTES, stream>>>(ma, mb, md, a);
+    gemm_kernel<EPI, NST><<<grid, kThreads, smem, stream>>>(ma, mb, md, a);
     return check_launch("block_scaled_gemm");
+}
+
+template <int EPI>
+fp4q_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const GemmArgs& a,
+                   int tiles_upper, int sms, cudaStream_t stream) {
+    if constexpr (EPI == kStore) {
+        if (a.f8) return launch_stages<EPI, 4>(ma, mb, md, a, tiles_upper, sms, stream);
+    }
+    return launch_stages<EPI, 3>(ma, mb, md, a, tiles_upper, sms, stream);
 }
 
 }  // namespace

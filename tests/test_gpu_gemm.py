@@ -47,6 +47,8 @@ def _check(oracle, d_bf16, d_f32, ref):
     eb = oracle.rel_frobenius(host(d_bf16.float()).astype(np.float64), _bf16_round(ref))
     assert e32 <= TOL, e32
     assert eb <= TOL, eb
+    # the BF16 epilogue writes the nearest-even BF16 of the FP32 result, every element in place
+    assert torch.equal(d_bf16, d_f32.to(torch.bfloat16))
     return e32, eb
 
 

@@ -256,6 +256,8 @@ def test_mxfp8_gemm_on_fp4_to_fp8_outputs(fq, oracle, shape):
     ref = oracle.fp8_gemm_ref(host(ya), host(tsa), host(yb), host(tsb))
     assert oracle.rel_frobenius(host(d32).astype(np.float64), ref) <= 1e-3
     assert oracle.rel_frobenius(host(d16.float()).astype(np.float64), _bf16_round(ref)) <= 1e-3
+    # the BF16 epilogue writes the nearest-even BF16 of the FP32 result, every element in place
+    assert torch.equal(d16, d32.to(torch.bfloat16))
     # lossless chain: the FP8 operands are the MXFP4 values, so this is also the MXFP4 product
     mx = oracle.mx_gemm_ref(host(qa), host(sa), host(qb), host(sb))
     assert oracle.rel_frobenius(ref, mx) < 1e-12
