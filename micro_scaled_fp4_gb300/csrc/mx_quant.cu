@@ -360,9 +360,12 @@ __global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_col_kernel(
     const uint32_t spr = uint32_t(rows / 32);
     // output tile staging, block-major: block k's 16 code bytes of output row
     // cl at oq[k * 2048 + 16 * (cl ^ 2k)] (the XOR keeps the row-wise reads
-    // conflict-free)
+    // conflict-free).  A thread stores its two rows 2 cp + h in the order
+    // h = (cp / 4) % 2 first, so any 8 lanes of one store instruction hit 8
+    // different 16-byte bank groups.  Scale byte (cl, k) at 4 (cl + cl / 32) + k
+    // (one padding word per 32 rows: lanes cp and cp + 16 in different banks).
     __shared__ __align__(16) uint8_t oq[kMxColCols * 64];
-    __shared__ __align__(16) uint8_t os[kMxColCols * 4];
+    __shared__ __align__(16) uint8_t os[kMxColCols * 4 + 16];
     ring::consume_together(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, int64_t g) {
         const int64_t rt = g / ctiles, ct = g - rt * ctiles;
         const int64_t r0 = rt * kMxColRows, c0 = ct * kMxColCols;
@@ -378,15 +381,20 @@ __global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_col_kernel(
             if (j < 8) { A.a.v[j] = lo; B.a.v[j] = hi; } else { A.b.v[j - 8] = lo; B.b.v[j - 8] = hi; }
         }
         const uint32_t blk = uint32_t(r0 / 32) + k;
+        uint4 codes[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            uint4 codes;
             uint32_t sb;
-            quantize_block<kBF16>(h ? B : A, codes, sb);
+            quantize_block<kBF16>(h ? B : A, codes[h], sb);
             const uint32_t cl = 2 * cp + h;
-            *reinterpret_cast<uint4*>(oq + k * 2048 + 16 * (cl ^ (2 * k))) = codes;
             if (mma_layout) s[mma_scale_offset(uint64_t(c0 + cl), blk, spr)] = uint8_t(sb);
-            else os[cl * 4 + k] = uint8_t(sb);
+            else os[4 * (cl + (cl >> 5)) + k] = uint8_t(sb);
+        }
+        const uint32_t h0 = (cp >> 2) & 1u;
+#pragma unroll
+        for (uint32_t i = 0; i < 2; ++i) {
+            const uint32_t h = h0 ^ i, cl = 2 * cp + h;
+            *reinterpret_cast<uint4*>(oq + k * 2048 + 16 * (cl ^ (2 * k))) = h ? codes[1] : codes[0];
         }
         // all 256 consumers staged the tile: 64 contiguous code bytes (and 4
         // scale bytes) per output row
@@ -399,7 +407,7 @@ __global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_col_kernel(
         }
         if (!mma_layout && t < kMxColCols)
             *reinterpret_cast<uint32_t*>(s + (c0 + t) * int64_t(spr) + r0 / 32) =
-                *reinterpret_cast<const uint32_t*>(os + t * 4);
+                *reinterpret_cast<const uint32_t*>(os + 4 * (t + (t >> 5)));
         tc::named_bar_sync(2, blockDim.x - 32);                // the staging may be rewritten
     });
 }

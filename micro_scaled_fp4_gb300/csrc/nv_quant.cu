@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(256) nv_quant_2d_kernel(
                                                    words);
             *reinterpret_cast<uint2*>(oq + bl * 128 + 8 * (j ^ bl)) = words;     // block-major, XOR-swizzled rows
             if (mma_layout) s[mma_scale_offset(uint64_t(r), b, tpr)] = uint8_t(sb);
-            else os[j * 16 + bl] = uint8_t(sb);
+            else os[j * 16 + (bl ^ (4 * (j >> 3)))] = uint8_t(sb);    // rows j, j + 8 in different banks
         }
         __syncthreads();
         {   // row t / 16, block t % 16: 8 code bytes (16 threads = one row's 128 bytes)
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(256) nv_quant_2d_kernel(
                 const int64_t rr = tr * 16 + row;
                 *reinterpret_cast<uint2*>(q + rr * int64_t(cols / 2) + (16 * ct + blk) * 8) =
                     *reinterpret_cast<const uint2*>(oq + blk * 128 + 8 * (row ^ blk));
-                if (!mma_layout) s[rr * int64_t(tpr) + 16 * ct + blk] = os[row * 16 + blk];
+                if (!mma_layout) s[rr * int64_t(tpr) + 16 * ct + blk] = os[row * 16 + (blk ^ (4 * (row >> 3)))];
             }
         }
         __syncthreads();
@@ -376,10 +376,13 @@ __global__ void __launch_bounds__(ring::kMaxThreads, MODE == 2 ? 2 : 3) nv_col_k
     const uint32_t t = threadIdx.x - 32, cp = t & 31u, k = t >> 5;
     const uint32_t spr = uint32_t(rows / 16);                 // scale columns per output row
     // output tile staging, block-major: block k's 8 code bytes of output row cl
-    // at oq[k * 512 + 8 * (cl ^ 8 (k / 2))] -- the XOR spreads both the writes
-    // (a warp: one block, 32 rows) and the row-wise reads over all banks
+    // at oq[k * 512 + 8 * (cl ^ 4 (k / 2))].  A thread writes its two rows
+    // (2 cp, 2 cp + 1) as one 16-byte store (any 8 lanes: 8 different 16-byte
+    // bank groups) and the row-wise reads (4 rows x 4 block pairs per 16
+    // lanes) land on 16 different bank pairs.  Scale bytes: (cl, k) at
+    // 8 cl + 4 (cl / 16) + k, which puts a warp's 32 stores in 32 banks.
     __shared__ __align__(16) uint8_t oq[kColCols * 64];
-    __shared__ __align__(16) uint8_t os[kColCols * 8];
+    __shared__ __align__(16) uint8_t os[kColCols * 8 + 16];
     uint32_t m_all = 0;
     ring::consume_together(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, int64_t g) {
         const int64_t rt = g / ctiles, ct = g - rt * ctiles;
@@ -406,29 +409,31 @@ __global__ void __launch_bounds__(ring::kMaxThreads, MODE == 2 ? 2 : 3) nv_col_k
         if constexpr (MODE == 0) {
             m_all = max(m_all, max(ma, mb));
         } else {
+            uint2 words[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const uint32_t cl = 2 * cp + h;                         // output row within the tile
                 const int64_t c = c0 + cl;
                 const int64_t rb = r0 + 16 * k;                      // first row of the block
-                uint2 words;
                 const uint32_t sb = nv_block_codes<MODE == 2>(h ? b : a, h ? mb : ma, s_t, denom,
                                                              uint64_t(c) * uint64_t(rows) + uint64_t(rb), sr_keys,
-                                                             words);
-                *reinterpret_cast<uint2*>(oq + k * 512 + 8 * (cl ^ (8 * (k >> 1)))) = words;
+                                                             words[h]);
                 if (mma_layout) s[mma_scale_offset(uint64_t(c), uint32_t(rb / 16), spr)] = uint8_t(sb);
-                else os[cl * 8 + k] = uint8_t(sb);
+                else os[8 * cl + 4 * (cl >> 4) + k] = uint8_t(sb);
             }
+            *reinterpret_cast<uint4*>(oq + k * 512 + 16 * (cp ^ (2 * (k >> 1)))) =
+                make_uint4(words[0].x, words[0].y, words[1].x, words[1].y);
             // all 256 consumers staged the tile: write 64 contiguous code bytes
             // (and 8 scale bytes) per output row
             tc::named_bar_sync(2, blockDim.x - 32);
             const uint32_t row = t >> 2, ch = t & 3u;           // blocks 2ch, 2ch + 1 of output row `row`
-            const uint2 lo = *reinterpret_cast<const uint2*>(oq + (2 * ch) * 512 + 8 * (row ^ (8 * ch)));
-            const uint2 hi = *reinterpret_cast<const uint2*>(oq + (2 * ch + 1) * 512 + 8 * (row ^ (8 * ch)));
+            const uint2 lo = *reinterpret_cast<const uint2*>(oq + (2 * ch) * 512 + 8 * (row ^ (4 * ch)));
+            const uint2 hi = *reinterpret_cast<const uint2*>(oq + (2 * ch + 1) * 512 + 8 * (row ^ (4 * ch)));
             *reinterpret_cast<uint4*>(q + (c0 + row) * (rows / 2) + r0 / 2 + 16 * ch) = make_uint4(lo.x, lo.y, hi.x, hi.y);
-            if (!mma_layout && t < kColCols)
-                *reinterpret_cast<uint2*>(s + (c0 + t) * int64_t(spr) + r0 / 16) =
-                    *reinterpret_cast<const uint2*>(os + t * 8);
+            if (!mma_layout && t < kColCols) {
+                const uint32_t* sw = reinterpret_cast<const uint32_t*>(os + 8 * t + 4 * (t >> 4));
+                *reinterpret_cast<uint2*>(s + (c0 + t) * int64_t(spr) + r0 / 16) = make_uint2(sw[0], sw[1]);
+            }
             tc::named_bar_sync(2, blockDim.x - 32);            // the staging may be rewritten
         }
     });
