@@ -138,6 +138,39 @@ fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, int64_t row
                             fp4q_stream_t stream);
 
 /*
+ * fp4q_fp8_pipeline_host -- the FP8 activation path on HOST buffers: E4M3
+ * activations with 1x128 FP32 tile scales are quantized straight to MXFP4
+ * ([HOP] abstract and section 1, as fp4q_mx_quantize with x_type FP4Q_E4M3)
+ * and re-expanded to FP8 for an FP8 consumer ([HOP] 2.B, as fp4q_fp4_to_fp8);
+ * the MXFP4 codes and scales and the FP8 copy are written back to host memory.
+ * Results are bit-identical to the two device calls.
+ * The rows go through the device in chunks of chunk_rows (0: 2048), using
+ * three slots of `workspace`: host -> device copies, the two conversion
+ * kernels (on `stream`) and device -> host copies of different chunks overlap
+ * on two internal copy streams (one pair per host thread and device, created
+ * on first use).  The call starts after the work already queued on `stream`
+ * and returns once everything is queued; the host outputs are complete when
+ * `stream` reaches the point of the call (e.g. after cudaStreamSynchronize).
+ * Host buffers should be page-locked for the copies to overlap; pageable
+ * memory gives the same results without the overlap.
+ *   x             host E4M3 [rows, cols];  tile_scale host FP32 [rows, cols/128]
+ *   cols          multiple of 128
+ *   q, scales     host out: codes [rows, cols/2], ROWMAJOR E8M0 [rows, cols/32]
+ *   y, y_tile_scale host out: E4M3 [rows, cols], FP32 [rows, cols/128]
+ *   workspace     device, >= fp4q_fp8_pipeline_host_workspace_bytes(cols,
+ *                 chunk_rows) bytes (chunk_rows capped at rows), 256-byte aligned;
+ *                 owned by the call until `stream` passes it
+ * Errors: negative sizes or a NULL pointer -> INVALID_ARGUMENT; cols % 128 ->
+ * UNSUPPORTED_SHAPE; misaligned workspace -> MISALIGNED; a failed copy, event
+ * or launch -> CUDA.  rows == 0 or cols == 0 does nothing.
+ */
+size_t fp4q_fp8_pipeline_host_workspace_bytes(int64_t cols, int64_t chunk_rows);
+fp4q_status fp4q_fp8_pipeline_host(const uint8_t* x, const float* tile_scale, int64_t rows,
+                                   int64_t cols, uint8_t* q, uint8_t* scales, uint8_t* y,
+                                   float* y_tile_scale, int64_t chunk_rows, void* workspace,
+                                   size_t workspace_bytes, fp4q_stream_t stream);
+
+/*
  * fp4q_nv_quantize -- BF16 -> NVFP4 (optional 16-point RHT, RNE or SR).
  * [NVF] 2.A: 16-element blocks of E2M1 with one E4M3 scale each under one
  * FP32 tensor scale.  With y the (optionally rotated) values and amax the

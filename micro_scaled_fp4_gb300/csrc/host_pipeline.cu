@@ -1,0 +1,165 @@
+// Host-buffer form of the FP8 activation path: E4M3 activations and their
+// 1x128 tile scales in host memory are quantized straight to MXFP4
+// ("Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs",
+// abstract and section 1) and re-expanded to FP8 for an FP8 consumer (same
+// page, section 2.B); the MXFP4 codes and scales and the FP8 copy come back to
+// host memory.
+//
+// The rows are cut into chunks that move through a ring of three device
+// slots in the caller's workspace.  Three streams overlap the transfers with
+// the conversion: a copy-in stream (host -> slot), the caller's stream (the
+// two conversion kernels on the slot) and a copy-out stream (slot -> host), in
+// order per chunk through events:
+//   copy-in c   waits  copy-out c - 3   (the slot is free again)
+//   convert c   waits  copy-in c
+//   copy-out c  waits  convert c
+// The call starts after the work already queued on the caller's stream and
+// that stream waits, at the end, for the last copy-out: the results are in
+// host memory once the caller's stream has reached that point.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace fp4q {
+namespace {
+
+constexpr int kSlots = 3;
+constexpr int64_t kDefaultChunkRows = 2048;
+constexpr int kMaxDevices = 64;
+
+inline uint64_t align256(uint64_t v) { return (v + 255u) & ~uint64_t(255); }
+
+// Byte offsets of one slot's buffers (every one 256-byte aligned).
+struct SlotLayout {
+    uint64_t x, ts, q, s, y, yt, bytes;
+};
+
+SlotLayout slot_layout(int64_t cols, int64_t chunk) {
+    SlotLayout L;
+    const uint64_t n = uint64_t(chunk), c = uint64_t(cols);
+    uint64_t o = 0;
+    L.x = o;  o += align256(n * c);               // E4M3 in
+    L.ts = o; o += align256(n * (c / 128) * 4);   // FP32 tile scales in
+    L.q = o;  o += align256(n * (c / 2));         // MXFP4 codes
+    L.s = o;  o += align256(n * (c / 32));        // E8M0 scales
+    L.y = o;  o += align256(n * c);               // E4M3 out
+    L.yt = o; o += align256(n * (c / 128) * 4);   // FP32 tile scales out
+    L.bytes = o;
+    return L;
+}
+
+int64_t chunk_for(int64_t rows, int64_t chunk_rows) {
+    const int64_t c = chunk_rows > 0 ? chunk_rows : kDefaultChunkRows;
+    return rows > 0 ? std::min(c, rows) : c;
+}
+
+// The copy streams and the ring's events, one set per host thread and device
+// (created on first use, kept until the process exits).
+struct Engine {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr;
+    cudaEvent_t loaded[kSlots] = {}, converted[kSlots] = {}, stored[kSlots] = {};
+};
+thread_local Engine t_engines[kMaxDevices];
+
+fp4q_status engine(Engine** e_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return fail(FP4Q_ERR_CUDA, "fp8_pipeline_host: no current device");
+    Engine& g = t_engines[dev];
+    if (!g.ready) {
+        const unsigned ev = cudaEventDisableTiming;
+        if ((e = cudaStreamCreateWithFlags(&g.in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&g.out, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&g.start, ev)) != cudaSuccess)
+            return fail(FP4Q_ERR_CUDA, "fp8_pipeline_host: stream setup: %s", cudaGetErrorString(e));
+        for (int k = 0; k < kSlots; ++k)
+            if ((e = cudaEventCreateWithFlags(&g.loaded[k], ev)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&g.converted[k], ev)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&g.stored[k], ev)) != cudaSuccess)
+                return fail(FP4Q_ERR_CUDA, "fp8_pipeline_host: event setup: %s", cudaGetErrorString(e));
+        g.ready = true;
+    }
+    *e_out = &g;
+    return FP4Q_OK;
+}
+
+}  // namespace
+}  // namespace fp4q
+
+using namespace fp4q;
+
+extern "C" size_t fp4q_fp8_pipeline_host_workspace_bytes(int64_t cols, int64_t chunk_rows) {
+    if (cols <= 0 || chunk_rows < 0) return 0;
+    return size_t(kSlots) * size_t(slot_layout(cols, chunk_for(0, chunk_rows)).bytes);
+}
+
+extern "C" fp4q_status fp4q_fp8_pipeline_host(const uint8_t* x, const float* tile_scale, int64_t rows,
+                                              int64_t cols, uint8_t* q, uint8_t* scales, uint8_t* y,
+                                              float* y_tile_scale, int64_t chunk_rows, void* workspace,
+                                              size_t workspace_bytes, fp4q_stream_t stream) {
+    if (rows < 0 || cols < 0 || chunk_rows < 0)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "fp8_pipeline_host: negative size");
+    if (cols % 128) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "fp8_pipeline_host: cols %% 128 != 0");
+    if (rows == 0 || cols == 0) return FP4Q_OK;
+    if (!x || !tile_scale || !q || !scales || !y || !y_tile_scale || !workspace)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "fp8_pipeline_host: null pointer");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(FP4Q_ERR_MISALIGNED, "fp8_pipeline_host: workspace must be 256-byte aligned");
+    const int64_t chunk = chunk_for(rows, chunk_rows);
+    const SlotLayout L = slot_layout(cols, chunk);
+    if (workspace_bytes < size_t(kSlots) * L.bytes)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "fp8_pipeline_host: workspace too small (%zu < %zu)",
+                    workspace_bytes, size_t(kSlots) * size_t(L.bytes));
+    int sms = 0;
+    fp4q_status st = current_device(&sms);
+    if (st != FP4Q_OK) return st;
+    Engine* g = nullptr;
+    if ((st = engine(&g)) != FP4Q_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const uint64_t c = uint64_t(cols), tpr = c / 128;
+    cudaError_t e;
+#define FP4Q_CUDA(call)                                                                         \
+    do {                                                                                        \
+        if ((e = (call)) != cudaSuccess)                                                        \
+            return fail(FP4Q_ERR_CUDA, "fp8_pipeline_host: %s: %s", #call, cudaGetErrorString(e)); \
+    } while (0)
+    // everything queued on the caller's stream before this call comes first
+    FP4Q_CUDA(cudaEventRecord(g->start, s));
+    FP4Q_CUDA(cudaStreamWaitEvent(g->in, g->start, 0));
+    FP4Q_CUDA(cudaStreamWaitEvent(g->out, g->start, 0));
+    const int64_t nchunks = (rows + chunk - 1) / chunk;
+    for (int64_t ci = 0; ci < nchunks; ++ci) {
+        const int k = int(ci % kSlots);
+        const uint64_t r0 = uint64_t(ci * chunk), n = uint64_t(std::min(chunk, rows - ci * chunk));
+        uint8_t* slot = ws + uint64_t(k) * L.bytes;
+        if (ci >= kSlots) FP4Q_CUDA(cudaStreamWaitEvent(g->in, g->stored[k], 0));
+        FP4Q_CUDA(cudaMemcpyAsync(slot + L.x, x + r0 * c, n * c, cudaMemcpyHostToDevice, g->in));
+        FP4Q_CUDA(cudaMemcpyAsync(slot + L.ts, tile_scale + r0 * tpr, n * tpr * 4, cudaMemcpyHostToDevice, g->in));
+        FP4Q_CUDA(cudaEventRecord(g->loaded[k], g->in));
+
+        FP4Q_CUDA(cudaStreamWaitEvent(s, g->loaded[k], 0));
+        if ((st = fp4q_mx_quantize(slot + L.x, FP4Q_E4M3, reinterpret_cast<const float*>(slot + L.ts), int64_t(n),
+                                   cols, cols, 1, slot + L.q, slot + L.s, FP4Q_SCALES_ROWMAJOR, stream)) != FP4Q_OK)
+            return st;
+        if ((st = fp4q_fp4_to_fp8(slot + L.q, slot + L.s, int64_t(n), cols, 1, slot + L.y,
+                                  reinterpret_cast<float*>(slot + L.yt), stream)) != FP4Q_OK)
+            return st;
+        FP4Q_CUDA(cudaEventRecord(g->converted[k], s));
+
+        FP4Q_CUDA(cudaStreamWaitEvent(g->out, g->converted[k], 0));
+        FP4Q_CUDA(cudaMemcpyAsync(q + r0 * (c / 2), slot + L.q, n * (c / 2), cudaMemcpyDeviceToHost, g->out));
+        FP4Q_CUDA(cudaMemcpyAsync(scales + r0 * (c / 32), slot + L.s, n * (c / 32), cudaMemcpyDeviceToHost, g->out));
+        FP4Q_CUDA(cudaMemcpyAsync(y + r0 * c, slot + L.y, n * c, cudaMemcpyDeviceToHost, g->out));
+        FP4Q_CUDA(cudaMemcpyAsync(y_tile_scale + r0 * tpr, slot + L.yt, n * tpr * 4, cudaMemcpyDeviceToHost, g->out));
+        FP4Q_CUDA(cudaEventRecord(g->stored[k], g->out));
+    }
+    // the caller's stream continues once every chunk is back in host memory
+    // (copy-out is in order on its stream: the last chunk's event covers all)
+    FP4Q_CUDA(cudaStreamWaitEvent(s, g->stored[int((nchunks - 1) % kSlots)], 0));
+#undef FP4Q_CUDA
+    return FP4Q_OK;
+}

@@ -33,7 +33,7 @@ EXPORTED = [
     "fp4q_block_scaled_gemm", "fp4q_device_status", "fp4q_moe_dispatch_workspace_bytes",
     "fp4q_moe_dispatch", "fp4q_rebased_scales_bytes", "fp4q_mx_rebase_scales", "fp4q_grouped_gemm",
     "fp4q_moe_dispatch_static", "fp4q_check_wait_timeout", "fp4q_nv_quantize_2d", "fp4q_fp4_row_to_fp8_col",
-    "fp4q_fp8_tile_scales_to_e8m0",
+    "fp4q_fp8_tile_scales_to_e8m0", "fp4q_fp8_pipeline_host_workspace_bytes", "fp4q_fp8_pipeline_host",
 ]
 MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 * 1024 * 1024
 
@@ -75,7 +75,8 @@ def load() -> ctypes.CDLL:
             L.fp4q_nv_quantize_workspace_bytes.restype = ctypes.c_size_t
             L.fp4q_nv_quantize_workspace_bytes.argtypes = [i64, i64]
             for name, args in {"fp4q_moe_dispatch_workspace_bytes": [i64, ci, ci],
-                               "fp4q_rebased_scales_bytes": [i64, i64, i64]}.items():
+                               "fp4q_rebased_scales_bytes": [i64, i64, i64],
+                               "fp4q_fp8_pipeline_host_workspace_bytes": [i64, i64]}.items():
                 fn = getattr(L, name, None)
                 if fn is not None:
                     fn.restype = ctypes.c_size_t
@@ -96,6 +97,7 @@ def load() -> ctypes.CDLL:
                 "fp4q_nv_quantize_2d": [vp, i64, i64, i64, ci, u64, vp, vp, vp, vp, vp, ci, vp, ctypes.c_size_t, vp],
                 "fp4q_fp4_row_to_fp8_col": [vp, vp, i64, i64, vp, vp, vp],
                 "fp4q_fp8_tile_scales_to_e8m0": [vp, i64, i64, vp, ci, vp],
+                "fp4q_fp8_pipeline_host": [vp, vp, i64, i64, vp, vp, vp, vp, i64, vp, ctypes.c_size_t, vp],
                 "fp4q_grouped_gemm": [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ci, vp, vp, vp, vp],
             }
             for name, args in sigs.items():
@@ -159,6 +161,36 @@ def fp4q_mx_dequantize(q, scales, rows, cols, block_axis, y, y_type, stream=None
 def fp4q_fp4_to_fp8(q, scales, rows, cols, block_axis, y, tile_scale, stream=None):
     return _check("fp4q_fp4_to_fp8", load().fp4q_fp4_to_fp8(
         _ptr(q), _ptr(scales), rows, cols, block_axis, _ptr(y), _ptr(tile_scale), _stream(stream)))
+
+
+def fp4q_fp8_pipeline_host_workspace_bytes(cols, chunk_rows=0):
+    return int(load().fp4q_fp8_pipeline_host_workspace_bytes(cols, chunk_rows))
+
+
+def fp4q_fp8_pipeline_host(x, tile_scale, rows, cols, q, scales, y, y_tile_scale, chunk_rows, workspace,
+                           workspace_bytes, stream=None):
+    """Host-buffer FP8 -> MXFP4 -> FP8 path (x, tile_scale, q, scales, y,
+    y_tile_scale are host tensors or addresses; workspace is device memory)."""
+    return _check("fp4q_fp8_pipeline_host", load().fp4q_fp8_pipeline_host(
+        _ptr(x), _ptr(tile_scale), rows, cols, _ptr(q), _ptr(scales), _ptr(y), _ptr(y_tile_scale), chunk_rows,
+        _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def fp8_pipeline_host(x, tile_scale, chunk_rows=0, pinned=True, stream=None):
+    """E4M3 host tensor [R, C] (uint8 or float8_e4m3fn) + FP32 tile scales
+    [R, C/128] -> host dict(q, scales, y, y_tile_scale); synchronizes the stream."""
+    torch = _torch()
+    R, C = x.shape
+    mk = (lambda shape, dt: torch.empty(shape, dtype=dt).pin_memory()) if pinned else \
+        (lambda shape, dt: torch.empty(shape, dtype=dt))
+    out = {"q": mk((R, C // 2), torch.uint8), "scales": mk((R, C // 32), torch.uint8),
+           "y": mk((R, C), torch.uint8), "y_tile_scale": mk((R, C // 128), torch.float32)}
+    wsb = fp4q_fp8_pipeline_host_workspace_bytes(C, min(chunk_rows or 2048, max(R, 1)))
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+    fp4q_fp8_pipeline_host(x, tile_scale, R, C, out["q"], out["scales"], out["y"], out["y_tile_scale"], chunk_rows,
+                           ws, wsb, stream)
+    torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+    return out
 
 
 def fp4q_nv_quantize(x, rows, cols, ld_x, block_axis, rht, rht_seed, rounding, sr_seed, amax_in, amax_out,

@@ -91,6 +91,21 @@ def test_argument_errors_need_no_gpu(lib):
         with pytest.raises(E) as e:
             fn()
         assert e.value.status == status, (e.value, status)
+    # host-buffer FP8 path: every argument error is returned before any CUDA call
+    wsb = lib.fp4q_fp8_pipeline_host_workspace_bytes(256, 64)
+    for fn, status in [
+        (lambda: lib.fp4q_fp8_pipeline_host(x, x, -1, 256, x, x, x, x, 64, x, wsb, stream=0), 1),
+        (lambda: lib.fp4q_fp8_pipeline_host(x, x, 64, 256, x, x, x, x, -5, x, wsb, stream=0), 1),
+        (lambda: lib.fp4q_fp8_pipeline_host(x, x, 64, 192, x, x, x, x, 64, x, wsb, stream=0), 2),
+        (lambda: lib.fp4q_fp8_pipeline_host(x, None, 64, 256, x, x, x, x, 64, x, wsb, stream=0), 1),
+        (lambda: lib.fp4q_fp8_pipeline_host(x, x, 64, 256, x, x, None, x, 64, x, wsb, stream=0), 1),
+        (lambda: lib.fp4q_fp8_pipeline_host(x, x, 64, 256, x, x, x, x, 64, x + 128, wsb, stream=0), 3),
+        (lambda: lib.fp4q_fp8_pipeline_host(x, x, 64, 256, x, x, x, x, 64, x, wsb - 1, stream=0), 1),
+        (lambda: lib.fp4q_fp8_pipeline_host(x, x, 200, 256, x, x, x, x, 128, x, wsb, stream=0), 1),
+    ]:
+        with pytest.raises(E) as e:
+            fn()
+        assert e.value.status == status, (e.value, status)
     for limit in (0, 3_000_000_000):
         with pytest.raises(E) as e:
             lib.fp4q_check_wait_timeout(limit, stream=0)
@@ -108,7 +123,19 @@ def test_argument_errors_need_no_gpu(lib):
         assert e.value.status == status, (args, e.value)
 
 
+def test_fp8_pipeline_host_workspace_bytes(lib):
+    # three slots of one chunk: E4M3 in, tile scales, codes, E8M0, E4M3 out, tile scales (each 256-B aligned)
+    def slot(n, c):
+        a = lambda v: (v + 255) // 256 * 256
+        return a(n * c) + a(n * c // 128 * 4) + a(n * c // 2) + a(n * c // 32) + a(n * c) + a(n * c // 128 * 4)
+    assert lib.fp4q_fp8_pipeline_host_workspace_bytes(7168, 1024) == 3 * slot(1024, 7168)
+    assert lib.fp4q_fp8_pipeline_host_workspace_bytes(7168, 0) == 3 * slot(2048, 7168)
+    assert lib.fp4q_fp8_pipeline_host_workspace_bytes(128, 3) == 3 * slot(3, 128)
+    assert lib.fp4q_fp8_pipeline_host_workspace_bytes(0, 64) == 0
+
+
 def test_empty_tensors_are_no_ops(lib):
+    lib.fp4q_fp8_pipeline_host(None, None, 0, 256, None, None, None, None, 0, None, 0, stream=0)
     lib.fp4q_mx_quantize(None, 0, None, 0, 64, 64, 1, None, None, 0, 0)
     lib.fp4q_mx_dequantize(None, None, 0, 64, 1, None, 0, 0)
     lib.fp4q_fp4_to_fp8(None, None, 5, 0, 1, None, None, 0)

@@ -222,6 +222,73 @@ def test_fp8_pipeline_full_size(fq, oracle):
 
 
 # ---------------------------------------------------------------------------
+# the FP8 path on host buffers (chunked, copies overlapped on streams)
+# ---------------------------------------------------------------------------
+def _check_host_outputs(out, qr, sr, yr, ytr):
+    assert np.array_equal(out["q"].numpy(), qr)
+    assert np.array_equal(out["scales"].numpy(), sr)
+    assert np.array_equal(out["y"].numpy(), yr)
+    assert np.array_equal(out["y_tile_scale"].numpy().view(np.uint32), ytr.view(np.uint32))
+
+
+@pytest.mark.parametrize("rows,cols,chunk", [(1000, 1024, 256), (5, 512, 0), (300, 7168, 1000), (777, 256, 64)])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_fp8_pipeline_host(fq, oracle, rows, cols, chunk, pinned):
+    """Host E4M3 + tile scales -> host MXFP4 and FP8, in chunks (ragged last
+    chunk, chunk larger than the tensor, default chunk), pinned or pageable
+    host memory: bit-identical to the oracle."""
+    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
+    e4, ts = W.fp8_activation(rows, cols, seed=rows + cols)
+    hx, ht = torch.from_numpy(e4), torch.from_numpy(ts)
+    if pinned:
+        hx, ht = hx.pin_memory(), ht.pin_memory()
+    out = fq.fp8_pipeline_host(hx, ht, chunk_rows=chunk, pinned=pinned)
+    qr, sr = oracle.fp8_to_mx(e4, ts)
+    yr, ytr = oracle.mx_to_fp8(qr, sr)
+    _check_host_outputs(out, qr, sr, yr, ytr)
+
+
+def test_fp8_pipeline_host_back_to_back_calls(fq, oracle):
+    """Two calls queued on one stream before any synchronisation reuse the
+    workspace slots: each call's results are its own."""
+    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
+    R, C, chunk = 700, 2048, 128
+    wsb = fq.fp4q_fp8_pipeline_host_workspace_bytes(C, chunk)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    runs = []
+    for seed in (3, 4):
+        e4, ts = W.fp8_activation(R, C, seed=seed)
+        hx, ht = torch.from_numpy(e4).pin_memory(), torch.from_numpy(ts).pin_memory()
+        out = {"q": torch.empty((R, C // 2), dtype=torch.uint8).pin_memory(),
+               "scales": torch.empty((R, C // 32), dtype=torch.uint8).pin_memory(),
+               "y": torch.empty((R, C), dtype=torch.uint8).pin_memory(),
+               "y_tile_scale": torch.empty((R, C // 128), dtype=torch.float32).pin_memory()}
+        fq.fp4q_fp8_pipeline_host(hx, ht, R, C, out["q"], out["scales"], out["y"], out["y_tile_scale"], chunk, ws,
+                                  wsb, stream)
+        runs.append((e4, ts, hx, ht, out))
+    stream.synchronize()
+    for e4, ts, _, _, out in runs:
+        qr, sr = oracle.fp8_to_mx(e4, ts)
+        yr, ytr = oracle.mx_to_fp8(qr, sr)
+        _check_host_outputs(out, qr, sr, yr, ytr)
+
+
+def test_fp8_pipeline_host_full_size(fq, oracle):
+    """The benchmark's 8192 x 7168 activation through the host-buffer call
+    with the default chunk: bit-identical to the oracle."""
+    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
+    e4, ts = W.fp8_activation()
+    out = fq.fp8_pipeline_host(torch.from_numpy(e4).pin_memory(), torch.from_numpy(ts).pin_memory())
+    qr, sr = oracle.fp8_to_mx(e4, ts)
+    yr, ytr = oracle.mx_to_fp8(qr, sr)
+    _check_host_outputs(out, qr, sr, yr, ytr)
+
+
+# ---------------------------------------------------------------------------
 # NVFP4
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("shape", [(1, 16), (5, 48), (129, 2048), (64, 14336)])
