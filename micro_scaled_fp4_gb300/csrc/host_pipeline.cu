@@ -5,11 +5,11 @@
 // page, section 2.B); the MXFP4 codes and scales and the FP8 copy come back to
 // host memory.
 //
-// The rows are cut into chunks that move through a ring of three device
-// slots in the caller's workspace.  Three streams overlap the transfers with
-// the conversion: a copy-in stream (host -> slot), the caller's stream (the
-// two conversion kernels on the slot) and a copy-out stream (slot -> host), in
-// order per chunk through events:
+// The rows are cut into chunks (the first a quarter of the others) that move
+// through a ring of three device slots in the caller's workspace.  Three
+// streams overlap the transfers with the conversion: a copy-in stream
+// (host -> slot), the caller's stream (the two conversion kernels on the slot)
+// and a copy-out stream (slot -> host), in order per chunk through events:
 //   copy-in c   waits  copy-out c - 3   (the slot is free again)
 //   convert c   waits  copy-in c
 //   copy-out c  waits  convert c
@@ -131,10 +131,15 @@ extern "C" fp4q_status fp4q_fp8_pipeline_host(const uint8_t* x, const float* til
     FP4Q_CUDA(cudaEventRecord(g->start, s));
     FP4Q_CUDA(cudaStreamWaitEvent(g->in, g->start, 0));
     FP4Q_CUDA(cudaStreamWaitEvent(g->out, g->start, 0));
-    const int64_t nchunks = (rows + chunk - 1) / chunk;
-    for (int64_t ci = 0; ci < nchunks; ++ci) {
+    // The first chunk is a quarter chunk: the device-to-host stream, the
+    // slower direction, starts after a quarter of the fill time.
+    const int64_t first = std::max<int64_t>(1, std::min(chunk / 4, rows));
+    int64_t ci = 0, k_last = 0;
+    for (int64_t r = 0; r < rows; ++ci) {
         const int k = int(ci % kSlots);
-        const uint64_t r0 = uint64_t(ci * chunk), n = uint64_t(std::min(chunk, rows - ci * chunk));
+        const uint64_t r0 = uint64_t(r), n = uint64_t(std::min(ci == 0 ? first : chunk, rows - r));
+        r += int64_t(n);
+        k_last = k;
         uint8_t* slot = ws + uint64_t(k) * L.bytes;
         if (ci >= kSlots) FP4Q_CUDA(cudaStreamWaitEvent(g->in, g->stored[k], 0));
         FP4Q_CUDA(cudaMemcpyAsync(slot + L.x, x + r0 * c, n * c, cudaMemcpyHostToDevice, g->in));
@@ -159,7 +164,7 @@ extern "C" fp4q_status fp4q_fp8_pipeline_host(const uint8_t* x, const float* til
     }
     // the caller's stream continues once every chunk is back in host memory
     // (copy-out is in order on its stream: the last chunk's event covers all)
-    FP4Q_CUDA(cudaStreamWaitEvent(s, g->stored[int((nchunks - 1) % kSlots)], 0));
+    FP4Q_CUDA(cudaStreamWaitEvent(s, g->stored[k_last], 0));
 #undef FP4Q_CUDA
     return FP4Q_OK;
 }
