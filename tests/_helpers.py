@@ -45,3 +45,11 @@ def to_mma_layout(s: np.ndarray) -> np.ndarray:
     out = np.zeros(((rows + 127) // 128) * ((scols + 3) // 4) * 512, dtype=np.uint8)
     out[mma_scale_index(rows, scols)] = s
     return out
+
+
+def rel_frobenius(y, ref) -> float:
+    """||y - ref||_F / ||ref||_F in float64 (the GEMM parity measure)."""
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(y - ref) / (den if den > 0 else 1.0))

@@ -10,7 +10,7 @@ against the BF16 rounding of the float64 result (BF16 rounding alone is
 import numpy as np
 import pytest
 
-from _helpers import dev_bf16, from_mma_layout, host
+from _helpers import dev_bf16, from_mma_layout, host, rel_frobenius
 
 pytestmark = pytest.mark.gpu
 
@@ -41,10 +41,16 @@ def _operands(M, N, K, seed):
     return W.to_bf16_bits(a), W.to_bf16_bits(b)
 
 
+def _same_operand(q_dev, s_dev, q_ref, s_ref, rows, scale_cols):
+    """The kernel's quantized operand (MMA-layout scales) equals the oracle's."""
+    assert np.array_equal(host(q_dev), q_ref)
+    assert np.array_equal(from_mma_layout(host(s_dev), rows, scale_cols), s_ref)
+
+
 def _check(oracle, d_bf16, d_f32, ref):
-    e32 = oracle.rel_frobenius(host(d_f32).astype(np.float64), ref)
+    e32 = rel_frobenius(host(d_f32).astype(np.float64), ref)
     import torch
-    eb = oracle.rel_frobenius(host(d_bf16.float()).astype(np.float64), _bf16_round(ref))
+    eb = rel_frobenius(host(d_bf16.float()).astype(np.float64), _bf16_round(ref))
     assert e32 <= TOL, e32
     assert eb <= TOL, eb
     # the BF16 epilogue writes the nearest-even BF16 of the FP32 result, every element in place
@@ -66,9 +72,12 @@ def test_mxfp4_gemm(fq, oracle, shape):
     d16 = fq.gemm(qa, sa, qb, sb, fq.FP4Q_MXFP4, out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
     assert fq.fp4q_device_status() == 0
-    ref = oracle.mx_gemm_ref(host(qa), from_mma_layout(host(sa), M, K // 32),
-                             host(qb), from_mma_layout(host(sb), N, K // 32))
-    _check(oracle, d16, d32, ref)
+    # the reference multiplies the oracle's own operands (equal to the kernel's)
+    qra, sra = oracle.mx_quantize(a)
+    qrb, srb = oracle.mx_quantize(b)
+    _same_operand(qa, sa, qra, sra, M, K // 32)
+    _same_operand(qb, sb, qrb, srb, N, K // 32)
+    _check(oracle, d16, d32, oracle.mx_gemm_ref(qra, sra, qrb, srb))
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -84,14 +93,18 @@ def test_nvfp4_gemm(fq, oracle, shape, rht):
     d16 = fq.gemm(*args, out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
     assert fq.fp4q_device_status() == 0
-    ref = oracle.nv_gemm_ref(host(ra["q"]), from_mma_layout(host(ra["scales"]), M, K // 16), host(ra["s_t"])[0],
-                             host(rb["q"]), from_mma_layout(host(rb["scales"]), N, K // 16), host(rb["s_t"])[0])
+    oa = oracle.nv_quantize(a, rht=rht, rht_seed=7)
+    ob = oracle.nv_quantize(b, rht=rht, rht_seed=7)
+    _same_operand(ra["q"], ra["scales"], oa["q"], oa["s"], M, K // 16)
+    _same_operand(rb["q"], rb["scales"], ob["q"], ob["s"], N, K // 16)
+    assert host(ra["s_t"])[0] == oa["s_t"] and host(rb["s_t"])[0] == ob["s_t"]
+    ref = oracle.nv_gemm_ref(oa["q"], oa["s"], oa["s_t"], ob["q"], ob["s"], ob["s_t"])
     _check(oracle, d16, d32, ref)
     if rht and M * N <= 2 ** 20:
         # the rotation cancels along K: the product tracks the unrotated A . B^T
         # up to the FP4 quantization error (reported bound, not the kernel's)
         exact = oracle.bf16_bits_to_f32(a).astype(np.float64) @ oracle.bf16_bits_to_f32(b).astype(np.float64).T
-        assert oracle.rel_frobenius(host(d32), exact) < 0.2
+        assert rel_frobenius(host(d32), exact) < 0.2
 
 
 def test_gemm_full_size_sampled(fq, oracle):
@@ -111,21 +124,31 @@ def test_gemm_full_size_sampled(fq, oracle):
     d = fq.gemm(qa, sa, qb, sb, fq.FP4Q_MXFP4)
     torch.cuda.synchronize()
     assert fq.fp4q_device_status() == 0
+    # MX quantization is row-local: the oracle quantizes only the sampled rows
+    qra, sra = oracle.mx_quantize(a[rows])
+    qrb, srb = oracle.mx_quantize(b[cols])
     sa_h, sb_h = from_mma_layout(host(sa), M, K // 32), from_mma_layout(host(sb), N, K // 32)
-    ref = oracle.mx_gemm_ref(host(qa)[rows], sa_h[rows], host(qb)[cols], sb_h[cols])
+    assert np.array_equal(host(qa)[rows], qra) and np.array_equal(sa_h[rows], sra)
+    assert np.array_equal(host(qb)[cols], qrb) and np.array_equal(sb_h[cols], srb)
+    ref = oracle.mx_gemm_ref(qra, sra, qrb, srb)
     dg = host(d.float())[np.ix_(rows, cols)]
-    assert oracle.rel_frobenius(dg, _bf16_round(ref)) <= TOL
+    assert rel_frobenius(dg, _bf16_round(ref)) <= TOL
     ra = fq.nv_quantize(ad, rht=True, rht_seed=7, layout=fq.FP4Q_SCALES_MMA)
     rb = fq.nv_quantize(bd, rht=True, rht_seed=7, layout=fq.FP4Q_SCALES_MMA)
     d = fq.gemm(ra["q"], ra["scales"], rb["q"], rb["scales"], fq.FP4Q_NVFP4, ra["s_t"], rb["s_t"])
     torch.cuda.synchronize()
     assert fq.fp4q_device_status() == 0
+    # NVFP4 rows depend on the whole tensor only through its amax
+    oa = oracle.nv_quantize(a[rows], rht=True, rht_seed=7, amax=oracle.nv_amax(a, True, 7))
+    ob = oracle.nv_quantize(b[cols], rht=True, rht_seed=7, amax=oracle.nv_amax(b, True, 7))
     sa_h = from_mma_layout(host(ra["scales"]), M, K // 16)
     sb_h = from_mma_layout(host(rb["scales"]), N, K // 16)
-    ref = oracle.nv_gemm_ref(host(ra["q"])[rows], sa_h[rows], host(ra["s_t"])[0],
-                             host(rb["q"])[cols], sb_h[cols], host(rb["s_t"])[0])
+    assert np.array_equal(host(ra["q"])[rows], oa["q"]) and np.array_equal(sa_h[rows], oa["s"])
+    assert np.array_equal(host(rb["q"])[cols], ob["q"]) and np.array_equal(sb_h[cols], ob["s"])
+    assert host(ra["s_t"])[0] == oa["s_t"] and host(rb["s_t"])[0] == ob["s_t"]
+    ref = oracle.nv_gemm_ref(oa["q"], oa["s"], oa["s_t"], ob["q"], ob["s"], ob["s_t"])
     dg = host(d.float())[np.ix_(rows, cols)]
-    assert oracle.rel_frobenius(dg, _bf16_round(ref)) <= TOL
+    assert rel_frobenius(dg, _bf16_round(ref)) <= TOL
 
 
 def test_gemm_argument_errors(fq):

@@ -11,7 +11,7 @@ section.
 import numpy as np
 import pytest
 
-from _helpers import dev, dev_bf16, from_mma_layout, host
+from _helpers import dev, dev_bf16, from_mma_layout, host, rel_frobenius
 
 pytestmark = pytest.mark.gpu
 
@@ -123,14 +123,20 @@ def test_nv_quantize_2d(fq, oracle, shape, rounding, layout):
 def test_nv_2d_forward_and_transposed_weights_agree(fq, oracle):
     """The property 2D scaling exists for, on the GPU path: quantizing W and W^T
     gives transposed copies of the same values."""
-    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
     rng = np.random.default_rng(21)
-    w = (rng.standard_normal((256, 512)) * 0.02).astype(np.float32)
-    wt = torch.from_numpy(w).cuda().to(torch.bfloat16)
-    a = fq.nv_quantize(wt, two_d=True)
-    b = fq.nv_quantize(wt.t().contiguous(), two_d=True)
-    da = oracle.nv_dequantize_f64(host(a["q"]), host(a["scales"]), host(a["s_t"])[0])
-    db = oracle.nv_dequantize_f64(host(b["q"]), host(b["scales"]), host(b["s_t"])[0])
+    w = W.to_bf16_bits((rng.standard_normal((256, 512)) * 0.02).astype(np.float32))
+    wt = np.ascontiguousarray(w.T)
+    a = fq.nv_quantize(dev_bf16(w), two_d=True)
+    b = fq.nv_quantize(dev_bf16(wt), two_d=True)
+    # both kernel results are the oracle's 2D quantizations of W and W^T ...
+    ra, rb = oracle.nv_quantize_2d(w), oracle.nv_quantize_2d(wt)
+    for got, ref in ((a, ra), (b, rb)):
+        assert np.array_equal(host(got["q"]), ref["q"]) and np.array_equal(host(got["scales"]), ref["s"])
+        assert host(got["s_t"])[0] == ref["s_t"]
+    # ... which hold transposed copies of the same values
+    da = oracle.nv_dequantize_f64(ra["q"], ra["s"], ra["s_t"])
+    db = oracle.nv_dequantize_f64(rb["q"], rb["s"], rb["s_t"])
     assert np.array_equal(da, db.T)
 
 
@@ -204,10 +210,10 @@ def test_wgrad_deterministic_h16(fq, oracle, rounding):
     ob = oracle.nv_quantize_col(x, rht=2, rounding="sr" if rounding else "rne", sr_seed=6)
     assert np.array_equal(host(ra["q"]), oa["q"]) and np.array_equal(host(rb["q"]), ob["q"])
     ref = oracle.nv_gemm_ref(oa["q"], oa["s"], oa["s_t"], ob["q"], ob["s"], ob["s_t"])
-    assert oracle.rel_frobenius(host(d32).astype(np.float64), ref) <= 1e-3
+    assert rel_frobenius(host(d32).astype(np.float64), ref) <= 1e-3
     # the rotation cancels along the token axis: the product tracks dY^T X up to FP4 error
     exact = oracle.bf16_bits_to_f32(dy).astype(np.float64).T @ oracle.bf16_bits_to_f32(x).astype(np.float64)
-    assert oracle.rel_frobenius(host(d32).astype(np.float64), exact) < 0.2
+    assert rel_frobenius(host(d32).astype(np.float64), exact) < 0.2
 
 
 # ---------------------------------------------------------------------------
@@ -241,25 +247,34 @@ def test_mxfp8_gemm_on_fp4_to_fp8_outputs(fq, oracle, shape):
     """Forward-style FP8 GEMM: both operands stored MXFP4, expanded by the
     bit-remap FP4 -> FP8 conversion, multiplied as MXFP8 on the tensor cores."""
     import torch
+    from micro_scaled_fp4_gb300 import workloads as W
     M, N, K = shape
     rng = np.random.default_rng(M + N + K)
-    a = (rng.standard_normal((M, K)) * np.exp2(rng.integers(-4, 4, (M, 1)))).astype(np.float32)
-    b = rng.standard_normal((N, K)).astype(np.float32)
-    qa, sa = fq.mx_quantize(torch.from_numpy(a).cuda().to(torch.bfloat16))
-    qb, sb = fq.mx_quantize(torch.from_numpy(b).cuda().to(torch.bfloat16))
+    a = W.to_bf16_bits((rng.standard_normal((M, K)) * np.exp2(rng.integers(-4, 4, (M, 1)))).astype(np.float32))
+    b = W.to_bf16_bits(rng.standard_normal((N, K)).astype(np.float32))
+    qa, sa = fq.mx_quantize(dev_bf16(a))
+    qb, sb = fq.mx_quantize(dev_bf16(b))
     ya, tsa = fq.fp4_to_fp8(qa, sa)
     yb, tsb = fq.fp4_to_fp8(qb, sb)
     d32 = fq.gemm(ya, fq.fp8_mma_scales(tsa), yb, fq.fp8_mma_scales(tsb), fq.FP4Q_MXFP8, out_dtype=torch.float32)
     d16 = fq.gemm(ya, fq.fp8_mma_scales(tsa), yb, fq.fp8_mma_scales(tsb), fq.FP4Q_MXFP8, out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
     assert fq.fp4q_device_status() == 0
-    ref = oracle.fp8_gemm_ref(host(ya), host(tsa), host(yb), host(tsb))
-    assert oracle.rel_frobenius(host(d32).astype(np.float64), ref) <= 1e-3
-    assert oracle.rel_frobenius(host(d16.float()).astype(np.float64), _bf16_round(ref)) <= 1e-3
+    # the oracle's own operands (the kernels' equal them bit for bit)
+    qra, sra = oracle.mx_quantize(a)
+    qrb, srb = oracle.mx_quantize(b)
+    yra, tsra = oracle.mx_to_fp8(qra, sra)
+    yrb, tsrb = oracle.mx_to_fp8(qrb, srb)
+    assert np.array_equal(host(ya), yra) and np.array_equal(host(yb), yrb)
+    assert np.array_equal(host(tsa).view(np.uint32), tsra.view(np.uint32))
+    assert np.array_equal(host(tsb).view(np.uint32), tsrb.view(np.uint32))
+    ref = oracle.fp8_gemm_ref(yra, tsra, yrb, tsrb)
+    assert rel_frobenius(host(d32).astype(np.float64), ref) <= 1e-3
+    assert rel_frobenius(host(d16.float()).astype(np.float64), _bf16_round(ref)) <= 1e-3
     # the BF16 epilogue writes the nearest-even BF16 of the FP32 result, every element in place
     assert torch.equal(d16, d32.to(torch.bfloat16))
     # lossless chain: the FP8 operands are the MXFP4 values, so this is also the MXFP4 product
-    mx = oracle.mx_gemm_ref(host(qa), host(sa), host(qb), host(sb))
+    mx = oracle.mx_gemm_ref(qra, sra, qrb, srb)
     assert oracle.rel_frobenius(ref, mx) < 1e-12
 
 
@@ -267,19 +282,28 @@ def test_mxfp8_wgrad_on_fp4_row_to_fp8_col(fq, oracle):
     """Backward-style FP8 GEMM: dW = dY^T X with both operands converted by
     FP4RowToFP8Col from their row-wise MXFP4 storage (tokens become K)."""
     import torch
+    from micro_scaled_fp4_gb300 import workloads as W
     T, H, I = 512, 256, 384
     rng = np.random.default_rng(41)
-    dy = (rng.standard_t(3, (T, H)) * 1e-3).astype(np.float32)
-    x = rng.standard_normal((T, I)).astype(np.float32)
-    qd, sd = fq.mx_quantize(torch.from_numpy(dy).cuda().to(torch.bfloat16))
-    qx, sx = fq.mx_quantize(torch.from_numpy(x).cuda().to(torch.bfloat16))
+    dy = W.to_bf16_bits((rng.standard_t(3, (T, H)) * 1e-3).astype(np.float32))
+    x = W.to_bf16_bits(rng.standard_normal((T, I)).astype(np.float32))
+    qd, sd = fq.mx_quantize(dev_bf16(dy))
+    qx, sx = fq.mx_quantize(dev_bf16(x))
     yd, tsd = fq.fp4_row_to_fp8_col(qd, sd)            # [H, T]
     yx, tsx = fq.fp4_row_to_fp8_col(qx, sx)            # [I, T]
     d32 = fq.gemm(yd, fq.fp8_mma_scales(tsd), yx, fq.fp8_mma_scales(tsx), fq.FP4Q_MXFP8, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert fq.fp4q_device_status() == 0
-    ref = oracle.fp8_gemm_ref(host(yd), host(tsd), host(yx), host(tsx))
-    assert oracle.rel_frobenius(host(d32).astype(np.float64), ref) <= 1e-3
+    # the oracle's own operands (the kernels' equal them bit for bit)
+    qrd, srd = oracle.mx_quantize(dy)
+    qrx, srx = oracle.mx_quantize(x)
+    yrd, tsrd = oracle.mx_to_fp8_col(qrd, srd)
+    yrx, tsrx = oracle.mx_to_fp8_col(qrx, srx)
+    assert np.array_equal(host(yd), yrd) and np.array_equal(host(yx), yrx)
+    assert np.array_equal(host(tsd).view(np.uint32), tsrd.view(np.uint32))
+    assert np.array_equal(host(tsx).view(np.uint32), tsrx.view(np.uint32))
+    ref = oracle.fp8_gemm_ref(yrd, tsrd, yrx, tsrx)
+    assert rel_frobenius(host(d32).astype(np.float64), ref) <= 1e-3
     # and it is dY_mx^T X_mx of the stored MXFP4 values (no flush at these spreads)
-    exact = oracle.mx_dequantize_f64(host(qd), host(sd)).T @ oracle.mx_dequantize_f64(host(qx), host(sx))
+    exact = oracle.mx_dequantize_f64(qrd, srd).T @ oracle.mx_dequantize_f64(qrx, srx)
     assert oracle.rel_frobenius(ref, exact) < 1e-9
