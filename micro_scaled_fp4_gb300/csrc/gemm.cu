@@ -72,6 +72,8 @@ constexpr uint32_t TMEM_SFA = 256;                    // 16 columns
 constexpr uint32_t TMEM_SFB = 272;                    // 32 columns
 constexpr uint64_t kWaitLimitNs = 4000000000ull;      // 4 s
 constexpr int kMaxGroups = 256;
+constexpr int kBandM = 32;                            // m-tiles per band of the dense tile order
+constexpr int64_t kBandAboveBytes = 48ll << 20;       // band only an A operand L2 cannot keep
 
 enum Epi { kStore = 0, kSiluGate = 1 };
 
@@ -85,6 +87,7 @@ struct GemmArgs {
     int f8;                          // 1 = MXFP8 operands (E4M3, one byte per element)
     int bk;                          // K elements per stage: 256 (FP4) or 128 (FP8); 128 bytes per row either way
     int groups;                      // 0 = dense
+    int band_m;                      // dense: m-tiles per band of the tile order
     const int64_t* offsets;          // grouped: [groups + 1] row offsets
     const uint8_t* sfa;
     const uint8_t* sfb;
@@ -123,8 +126,20 @@ __device__ __forceinline__ void flag_abort(volatile int* abort, uint32_t* status
 template <int EPI>
 __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile, const int* tile_prefix, int m_tiles) {
     TileInfo t;
-    const int nt = a.groups ? tile % a.n_tiles : tile / m_tiles;
-    const int mt = a.groups ? tile / a.n_tiles : tile % m_tiles;
+    int nt, mt;
+    if (a.groups) {
+        nt = tile % a.n_tiles;
+        mt = tile / a.n_tiles;
+    } else {
+        // dense: bands of band_m m-tiles; inside a band the m-tile runs fastest,
+        // so the tiles in flight at once share one band of A (kept in L2 while
+        // B streams past) instead of sweeping all of A every wave
+        const int band = tile / (a.band_m * a.n_tiles);
+        const int within = tile - band * a.band_m * a.n_tiles;
+        const int bs = min(a.band_m, m_tiles - band * a.band_m);
+        nt = within / bs;
+        mt = band * a.band_m + within % bs;
+    }
     if (a.groups) {
         int e = 0;
         while (e + 1 < a.groups && tile_prefix[e + 1] <= mt) ++e;
@@ -712,6 +727,8 @@ extern "C" fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_
     a.k_stages = int((K + a.bk - 1) / a.bk);
     a.nv = nv ? 1 : 0;
     a.groups = 0;
+    const int m_tiles = int((M + BM - 1) / BM);
+    a.band_m = M * row_bytes > kBandAboveBytes ? std::min(kBandM, m_tiles) : m_tiles;
     a.sfa = A->scales;
     a.sfb = B->scales;
     a.sf_tile_stride = uint64_t(nv ? K / 64 : K / 128) * 512u;
