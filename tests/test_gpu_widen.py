@@ -278,6 +278,29 @@ def test_mxfp8_gemm_on_fp4_to_fp8_outputs(fq, oracle, shape):
     assert oracle.rel_frobenius(ref, mx) < 1e-12
 
 
+def test_mxfp8_gemm_banded_tile_order(fq, oracle):
+    """An A operand too large for L2 (4224 x 12288 E4M3, 52 MB) runs the dense
+    GEMM's banded tile order: a full band of 32 m-tiles, a band of one, and a
+    ragged last n-tile.  Sampled rows from both bands, every column."""
+    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
+    M, N, K = 4224, 640, 12288
+    rng = np.random.default_rng(51)
+    a = W.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    b = W.to_bf16_bits(rng.standard_normal((N, K)).astype(np.float32))
+    ya, tsa = fq.fp4_to_fp8(*fq.mx_quantize(dev_bf16(a)))
+    yb, tsb = fq.fp4_to_fp8(*fq.mx_quantize(dev_bf16(b)))
+    d = fq.gemm(ya, fq.fp8_mma_scales(tsa), yb, fq.fp8_mma_scales(tsb), fq.FP4Q_MXFP8, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fq.fp4q_device_status() == 0
+    rows = np.sort(np.concatenate([rng.choice(4096, 40, replace=False), 4096 + np.arange(0, 128, 16)]))
+    yra, tsra = oracle.mx_to_fp8(*oracle.mx_quantize(a[rows]))      # row-local: only the sampled rows
+    yrb, tsrb = oracle.mx_to_fp8(*oracle.mx_quantize(b))
+    assert np.array_equal(host(ya)[rows], yra) and np.array_equal(host(yb), yrb)
+    ref = oracle.fp8_gemm_ref(yra, tsra, yrb, tsrb)
+    assert rel_frobenius(host(d)[rows].astype(np.float64), ref) <= 1e-3
+
+
 def test_mxfp8_wgrad_on_fp4_row_to_fp8_col(fq, oracle):
     """Backward-style FP8 GEMM: dW = dY^T X with both operands converted by
     FP4RowToFP8Col from their row-wise MXFP4 storage (tokens become K)."""
