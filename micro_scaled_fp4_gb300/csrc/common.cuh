@@ -7,6 +7,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <mutex>
 #include <stdint.h>
 
 #include "../../include/fp4q.h"
@@ -229,6 +230,8 @@ inline int resident_per_sm_smem(Kernel kernel, int threads, uint32_t smem) {
     struct Entry { const void* fn; int dev; int threads; uint32_t smem; int n; };
     static Entry cache[16] = {};
     static int next = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
     int dev = 0;
     cudaGetDevice(&dev);
     const void* fn = reinterpret_cast<const void*>(kernel);
@@ -243,20 +246,10 @@ inline int resident_per_sm_smem(Kernel kernel, int threads, uint32_t smem) {
 }
 
 // Resident CTAs per SM of `kernel` at `threads` per CTA (no dynamic shared
-// memory), looked up once per kernel and device.
+// memory), looked up once per kernel, device and block size.
 template <typename Kernel>
 inline int resident_per_sm(Kernel kernel, int threads) {
-    static int cache[64][5] = {};      // [device][threads / 64 bucket], 0 = unknown
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const int bucket = threads <= 64 ? 0 : threads <= 128 ? 1 : threads <= 192 ? 2 : threads <= 256 ? 3 : 4;
-    int& v = cache[dev & 63][bucket];
-    if (v == 0) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 4;
-        v = n;
-    }
-    return v;
+    return resident_per_sm_smem(kernel, threads, 0);
 }
 
 }  // namespace fp4q

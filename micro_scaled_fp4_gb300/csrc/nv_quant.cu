@@ -158,9 +158,7 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(
     const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= tpr) return;
     const uint64_t cols = uint64_t(tpr) * 16;
-    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-        float t[16];
-        load_tile(x + r * ld_x_bytes + uint64_t(b) * 32, t);
+    auto quantize_row = [&](int64_t r, float (&t)[16]) {
         if (rht) rht16(t, signs);
         uint32_t ab = 0;
 #pragma unroll
@@ -209,6 +207,11 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(
         *reinterpret_cast<uint2*>(q + uint64_t(r) * (cols / 2) + uint64_t(b) * 8) = make_uint2(words[0], words[1]);
         const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(r), b, tpr) : uint64_t(r) * tpr + b;
         s[so] = uint8_t(sb);
+    };
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        float t[16];
+        load_tile(x + r * ld_x_bytes + uint64_t(b) * 32, t);
+        quantize_row(r, t);
     }
 }
 
@@ -535,12 +538,15 @@ extern "C" fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t col
     const uint32_t tpr = uint32_t(cols / 16);
     int tpb = 32, nx = 1;
     if (tpr) row_launch_shape(tpr, &tpb, &nx);
-    dim3 grid(unsigned(nx), row_grid_y(rows, nx, sms, resident_per_sm(nv_quant_kernel<true>, tpb)), 1);
+    // grids sized by each kernel's own residency (the passes differ in registers)
+    auto grid_for = [&](auto kernel) {
+        return dim3(unsigned(nx), row_grid_y(rows, nx, sms, resident_per_sm(kernel, tpb)), 1);
+    };
     if (!amax_in) {
         uint32_t* w = static_cast<uint32_t*>(workspace);
         if ((st = zero_amax_word(w, s, "nv_quantize")) != FP4Q_OK) return st;
         if (rows > 0 && cols > 0) {
-            nv_amax_kernel<<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, w);
+            nv_amax_kernel<<<grid_for(nv_amax_kernel), tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, w);
             if ((st = check_launch("nv_quantize amax")) != FP4Q_OK) return st;
         }
         amax_ptr = reinterpret_cast<const float*>(w);
@@ -552,11 +558,11 @@ extern "C" fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t col
         return check_launch("nv_quantize");
     }
     if (rounding == FP4Q_SR)
-        nv_quant_kernel<true><<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out,
-                                                   tensor_scale_out, q, scales, mma);
+        nv_quant_kernel<true><<<grid_for(nv_quant_kernel<true>), tpb, 0, s>>>(
+            xb, rows, tpr, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out, tensor_scale_out, q, scales, mma);
     else
-        nv_quant_kernel<false><<<grid, tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out,
-                                                    tensor_scale_out, q, scales, mma);
+        nv_quant_kernel<false><<<grid_for(nv_quant_kernel<false>), tpb, 0, s>>>(
+            xb, rows, tpr, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out, tensor_scale_out, q, scales, mma);
     return check_launch("nv_quantize");
 }
 
