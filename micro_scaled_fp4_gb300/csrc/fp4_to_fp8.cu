@@ -29,17 +29,32 @@ constexpr int kShiftRows = 13;   // -d = 0..11 explicit, 12 = "12 or more"
 // (exponent field t + 7, mantissa m << 2); t = -7, -8, -9 are the subnormals
 // 4 + 2m, 2 + m and 1 + m (the last one rounds 1.5 to 2, ties to even);
 // smaller t lies below 2^-9 and flushes to zero.
-__device__ uint32_t shifted_magnitude(uint32_t c, int sh) {
+__host__ __device__ constexpr uint32_t shifted_magnitude(uint32_t c, int sh) {
     if (c == 0) return 0;
-    int k = c == 1 ? -1 : int(c >> 1) - 1;
-    uint32_t m = c == 1 ? 0u : (c & 1u);
-    int t = k - sh;
+    const int k = c == 1 ? -1 : int(c >> 1) - 1;
+    const uint32_t m = c == 1 ? 0u : (c & 1u);
+    const int t = k - sh;
     if (t >= -6) return (uint32_t(t + 7) << 3) | (m << 2);
     if (t == -7) return 4u + 2u * m;
     if (t == -8) return 2u + m;
     if (t == -9) return 1u + m;
     return 0u;
 }
+
+// The same table as a compile-time constant in global memory, for kernels
+// whose CTAs are too short-lived to build a shared copy: row sh holds the
+// magnitudes of codes 0..3 (lo) and 4..7 (hi).
+struct ShiftTable { uint32_t lo[kShiftRows], hi[kShiftRows]; };
+constexpr ShiftTable make_shift_table() {
+    ShiftTable t{};
+    for (int sh = 0; sh < kShiftRows; ++sh)
+        for (uint32_t c = 0; c < 4; ++c) {
+            t.lo[sh] |= shifted_magnitude(c, sh) << (8 * c);
+            t.hi[sh] |= shifted_magnitude(c + 4, sh) << (8 * c);
+        }
+    return t;
+}
+__device__ constexpr ShiftTable kShiftTable = make_shift_table();
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
@@ -215,9 +230,6 @@ constexpr int kColTile = 128;
 __global__ void __launch_bounds__(64) fp4_row_to_fp8_col_kernel(
     const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, int64_t cols,
     uint8_t* __restrict__ y, float* __restrict__ tile_scale) {
-    __shared__ uint2 lut[kShiftRows];
-    lut_setup(lut);
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t r0 = int64_t(blockIdx.y) * kColTile;
     const int64_t c0 = int64_t(blockIdx.x) * kColTile + 64 * warp;     // 64 columns of this warp
@@ -242,7 +254,10 @@ __global__ void __launch_bounds__(64) fp4_row_to_fp8_col_kernel(
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int b = 0; b < 2; ++b) L[i][b] = lut[min(emax[b] - e[i][b], uint32_t(kShiftRows - 1))];
+        for (int b = 0; b < 2; ++b) {
+            const uint32_t sh = min(emax[b] - e[i][b], uint32_t(kShiftRows - 1));
+            L[i][b] = make_uint2(__ldg(&kShiftTable.lo[sh]), __ldg(&kShiftTable.hi[sh]));
+        }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {                       // codes word k: columns 8k .. 8k + 7
         uint2 o[4];
