@@ -221,6 +221,33 @@ inline unsigned row_grid_y(int64_t rows, int nx, int sms, int per_sm = 8) {
     return unsigned(gy > 0 ? gy : 1);
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_overlapped()
+// may start while the previous kernel on its stream is still draining: its
+// CTAs run whatever needs no global memory, then grid_dependency_wait()
+// blocks until every prior grid on the stream has completed and its memory
+// is visible.  allow_dependent_launch() lets the next such kernel be launched
+// (it takes effect once every CTA of this grid has run it or exited, so all
+// of this grid's CTAs have started by then).  Without the launch attribute
+// both instructions do nothing.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                     Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Resident CTAs per SM of `kernel` at `threads` per CTA and `smem` bytes of
 // dynamic shared memory (raising the kernel's dynamic shared memory limit when
 // needed), remembered per kernel, device and size.

@@ -165,6 +165,8 @@ __global__ void __launch_bounds__(ring::kMaxThreads) fp4_to_fp8_staged_kernel(
     lut_setup(lut);                                      // make_ring's barrier publishes it
     const uint32_t code_bytes = cols / 2, scale_bytes = cols / 32;
     const ring::Ring rg = ring::make_ring(smem, rps * (code_bytes + scale_bytes));
+    allow_dependent_launch();
+    grid_dependency_wait();             // the codes may come from the previous kernel on the stream
     const int64_t ngroups = (rows + rps - 1) / rps;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bpr = cols / 32, ppr = cols / 64;
@@ -374,9 +376,11 @@ extern "C" fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, 
         const int per_sm = resident_per_sm_smem(fp4_to_fp8_staged_kernel, threads, smem);
         const int64_t ngroups = (rows + sh.rps - 1) / sh.rps;
         const int64_t grid = std::min<int64_t>(ngroups, int64_t(per_sm) * sms);
-        fp4_to_fp8_staged_kernel<<<unsigned(grid), threads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-            q, scales, rows, uint32_t(cols), y, tile_scale, sh.rps, status_word());
-        return check_launch("fp4_to_fp8");
+        const cudaError_t e = launch_overlapped(fp4_to_fp8_staged_kernel, dim3(unsigned(grid)), dim3(threads), smem,
+                                                reinterpret_cast<cudaStream_t>(stream), q, scales, rows,
+                                                uint32_t(cols), y, tile_scale, sh.rps, status_word());
+        if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "fp4_to_fp8: %s", cudaGetErrorString(e));
+        return FP4Q_OK;
     }
     int tpb, nx, rpc;
     packed_row_shape(bpr / 2, &tpb, &nx, &rpc);

@@ -201,6 +201,8 @@ struct RawPair { u32x8 a, b; float ts; };
 __global__ void __launch_bounds__(224, 4) mx_quantize_e4m3x2_kernel(
     const uint8_t* __restrict__ x, const float* __restrict__ tile_scale, int64_t rows,
     uint32_t bpr, int64_t ld_x, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout, int rpc) {
+    allow_dependent_launch();
+    grid_dependency_wait();             // the inputs may come from the previous kernel on the stream
     const uint32_t upc = blockDim.x / uint32_t(rpc);
     const uint32_t u = blockIdx.x * upc + threadIdx.x % upc;      // pair index in the row
     if (u >= (bpr >> 1)) return;
@@ -545,7 +547,9 @@ extern "C" fp4q_status fp4q_mx_quantize(const void* x, fp4q_dtype x_type, const 
             int tpb2, nx2, rpc;
             packed_row_shape(bpr / 2, &tpb2, &nx2, &rpc, 224);       // at most 224 threads: 4 CTAs per SM
             dim3 grid = grid_for_rows(mx_quantize_e4m3x2_kernel, tpb2, (rows + rpc - 1) / rpc, nx2, sms);
-            mx_quantize_e4m3x2_kernel<<<grid, tpb2, 0, s>>>(xb, tile_scale, rows, bpr, ld_x, q, scales, mma, rpc);
+            const cudaError_t e = launch_overlapped(mx_quantize_e4m3x2_kernel, grid, dim3(tpb2), 0, s, xb, tile_scale,
+                                                    rows, bpr, ld_x, q, scales, mma, rpc);
+            if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "mx_quantize: %s", cudaGetErrorString(e));
             break;
         }
     }
