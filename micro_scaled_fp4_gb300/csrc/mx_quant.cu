@@ -24,12 +24,6 @@ namespace {
 
 enum Src { kBF16 = 0, kFP32 = 1, kE4M3 = 2 };
 
-#ifndef FP4Q_E4M3_STAGED
-#define FP4Q_E4M3_STAGED 0
-#endif
-// E4M3 -> MXFP4 through the shared-memory ring (1) or the register path (0).
-constexpr bool kE4M3Staged = FP4Q_E4M3_STAGED != 0;
-
 // One 32-element block as loaded from memory.
 template <int SRC> struct RawBlock;
 template <> struct RawBlock<kBF16> { u32x8 a, b; };
@@ -239,95 +233,6 @@ __global__ void __launch_bounds__(224, 4) mx_quantize_e4m3x2_kernel(
     }
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
-
-// E4M3 source staged through shared memory (ring.cuh): each group of `rps` rows
-// arrives as one bulk copy of the codes (one per row when ld_x > cols) and one
-// of the rows' tile scales.  A consumer thread converts a pair of adjacent
-// blocks (64 codes, one 1x128 tile half) per step.  Its four 16-byte chunks
-// are read in the order k ^ ((lane >> 1) & 3): over any 8 consecutive lanes the
-// 16-byte bank groups are then all different (the plain order would put four
-// lanes on each group).  Chunk order does not matter to the block amax, and the
-// codes of chunk c go to bytes 8c .. 8c + 7 of the pair's output.
-__global__ void __launch_bounds__(ring::kMaxThreads) mx_quantize_e4m3_staged_kernel(
-    const uint8_t* __restrict__ x, const float* __restrict__ tile_scale, int64_t rows, uint32_t cols,
-    int64_t ld_x, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout, uint32_t rps,
-    uint32_t* status) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const uint32_t tile_bytes = cols / 32;                     // cols / 128 FP32 tile scales
-    const ring::Ring rg = ring::make_ring(smem, rps * (cols + tile_bytes));
-    const int64_t ngroups = (rows + rps - 1) / rps;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t bpr = cols / 32, ppr = cols / 64;
-    if (warp == 0) {
-        if (lane == 0)
-            ring::produce(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, uint32_t fb, int64_t g) {
-                const int64_t r0 = g * rps;
-                const uint32_t nr = uint32_t(min(int64_t(rps), rows - r0));
-                tc::mbar_arrive_expect_tx(fb, nr * (cols + tile_bytes));
-                if (ld_x == int64_t(cols)) {
-                    tc::bulk_load(tc::smem_u32(st), x + r0 * int64_t(cols), nr * cols, fb);
-                } else {
-                    for (uint32_t i = 0; i < nr; ++i)
-                        tc::bulk_load(tc::smem_u32(st + i * cols), x + (r0 + i) * ld_x, cols, fb);
-                }
-                tc::bulk_load(tc::smem_u32(st + rps * cols), tile_scale + r0 * (cols / 128), nr * tile_bytes, fb);
-            });
-        return;
-    }
-    const uint32_t ct = threadIdx.x - 32;                      // consumer thread
-    const uint32_t stride = blockDim.x - 32;
-    const uint32_t rr0 = ct / ppr, u0 = ct % ppr, dr = stride / ppr, du = stride % ppr;
-    const uint32_t sw = (uint32_t(lane) >> 1) & 3u;
-    ring::consume(rg, ngroups, status, kStatusStreamTimeout, [&](uint8_t* st, int64_t g) {
-        const int64_t r0 = g * rps;
-        const uint32_t nr = uint32_t(min(int64_t(rps), rows - r0));
-        const uint32_t units = nr * ppr;
-        const uint32_t sbase = tc::smem_u32(st), tbase = sbase + rps * cols;
-        uint32_t rr = rr0, u = u0;
-        for (uint32_t un = ct; un < units; un += stride) {
-            const uint32_t a = sbase + 64 * un;
-            const uint4 c0 = lds128(a + 16 * (0 ^ sw)), c1 = lds128(a + 16 * (1 ^ sw));
-            const uint4 c2 = lds128(a + 16 * (2 ^ sw)), c3 = lds128(a + 16 * (3 ^ sw));
-            RawBlock<kE4M3> A, B;
-            A.ts = B.ts = u2f(lds32(tbase + 4 * (rr * (cols / 128) + (u >> 1))));
-            A.a = u32x8{{c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w}};
-            B.a = u32x8{{c2.x, c2.y, c2.z, c2.w, c3.x, c3.y, c3.z, c3.w}};
-            uint4 qa, qb;
-            uint32_t sa, sb;
-            quantize_block<kE4M3>(A, qa, sa);
-            quantize_block<kE4M3>(B, qb, sb);
-            const int64_t r = r0 + rr;
-            uint8_t* qp = q + r * int64_t(cols / 2) + 32 * u;
-            *reinterpret_cast<uint2*>(qp + 8 * (0 ^ sw)) = make_uint2(qa.x, qa.y);
-            *reinterpret_cast<uint2*>(qp + 8 * (1 ^ sw)) = make_uint2(qa.z, qa.w);
-            *reinterpret_cast<uint2*>(qp + 8 * (2 ^ sw)) = make_uint2(qb.x, qb.y);
-            *reinterpret_cast<uint2*>(qp + 8 * (3 ^ sw)) = make_uint2(qb.z, qb.w);
-            // block A holds chunks of block (sw >> 1) of the pair, block B the other one
-            const uint32_t ba = 2 * u + (sw >> 1), bb = 2 * u + 1 - (sw >> 1);
-            if (mma_layout) {
-                s[mma_scale_offset(uint64_t(r), ba, bpr)] = uint8_t(sa);
-                s[mma_scale_offset(uint64_t(r), bb, bpr)] = uint8_t(sb);
-            } else {
-                *reinterpret_cast<uint16_t*>(s + r * int64_t(bpr) + 2 * u) =
-                    uint16_t((sw >> 1) ? (sb | (sa << 8)) : (sa | (sb << 8)));
-            }
-            u += du;
-            rr += dr;
-            if (u >= ppr) { u -= ppr; ++rr; }
-        }
-    });
-}
-
 // Column-wise MXFP4 of BF16 (block axis 0): the row-wise quantization of X^T,
 // written in the transposed layout (q [cols, rows/2], scales [cols, rows/32])
 // without materialising X^T.  Persistent CTAs run a shared-memory ring
@@ -531,19 +436,6 @@ extern "C" fp4q_status fp4q_mx_quantize(const void* x, fp4q_dtype x_type, const 
             break;
         }
         default: {
-            const uint32_t row_bytes = uint32_t(cols) + uint32_t(cols / 32);
-            const ring::Shape sh = kE4M3Staged && cols % 512 == 0 && aligned16(tile_scale) && cols <= (1 << 20)
-                                       ? ring::ring_shape(uint32_t(cols / 64), row_bytes) : ring::Shape{0, 0};
-            if (sh.rps) {
-                const uint32_t smem = ring::smem_bytes(sh.rps * row_bytes);
-                const int threads = 32 * int(1 + sh.warps);
-                const int per_sm = resident_per_sm_smem(mx_quantize_e4m3_staged_kernel, threads, smem);
-                const int64_t ngroups = (rows + sh.rps - 1) / sh.rps;
-                const int64_t grid = std::min<int64_t>(ngroups, int64_t(per_sm) * sms);
-                mx_quantize_e4m3_staged_kernel<<<unsigned(grid), threads, smem, s>>>(
-                    xb, tile_scale, rows, uint32_t(cols), ld_x, q, scales, mma, sh.rps, status_word());
-                break;
-            }
             int tpb2, nx2, rpc;
             packed_row_shape(bpr / 2, &tpb2, &nx2, &rpc, 224);       // at most 224 threads: 4 CTAs per SM
             dim3 grid = grid_for_rows(mx_quantize_e4m3x2_kernel, tpb2, (rows + rpc - 1) / rpc, nx2, sms);
