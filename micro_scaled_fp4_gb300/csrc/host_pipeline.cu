@@ -14,8 +14,9 @@
 //   convert c   waits  copy-in c
 //   copy-out c  waits  convert c
 // The call starts after the work already queued on the caller's stream and
-// that stream waits, at the end, for the last copy-out: the results are in
-// host memory once the caller's stream has reached that point.
+// that stream waits, at the end, for both copy streams (also when an enqueue
+// failed midway): the results are in host memory once the caller's stream has
+// reached that point.
 #include <algorithm>
 
 #include "common.cuh"
@@ -58,7 +59,7 @@ int64_t chunk_for(int64_t rows, int64_t chunk_rows) {
 struct Engine {
     bool ready = false;
     cudaStream_t in = nullptr, out = nullptr;
-    cudaEvent_t start = nullptr;
+    cudaEvent_t start = nullptr, in_done = nullptr, out_done = nullptr;
     cudaEvent_t loaded[kSlots] = {}, converted[kSlots] = {}, stored[kSlots] = {};
 };
 thread_local Engine t_engines[kMaxDevices];
@@ -73,7 +74,9 @@ fp4q_status engine(Engine** e_out) {
         const unsigned ev = cudaEventDisableTiming;
         if ((e = cudaStreamCreateWithFlags(&g.in, cudaStreamNonBlocking)) != cudaSuccess ||
             (e = cudaStreamCreateWithFlags(&g.out, cudaStreamNonBlocking)) != cudaSuccess ||
-            (e = cudaEventCreateWithFlags(&g.start, ev)) != cudaSuccess)
+            (e = cudaEventCreateWithFlags(&g.start, ev)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&g.in_done, ev)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&g.out_done, ev)) != cudaSuccess)
             return fail(FP4Q_ERR_CUDA, "fp8_pipeline_host: stream setup: %s", cudaGetErrorString(e));
         for (int k = 0; k < kSlots; ++k)
             if ((e = cudaEventCreateWithFlags(&g.loaded[k], ev)) != cudaSuccess ||
@@ -83,6 +86,53 @@ fp4q_status engine(Engine** e_out) {
         g.ready = true;
     }
     *e_out = &g;
+    return FP4Q_OK;
+}
+
+// Queues the chunks (copy-in, the two conversions on `s`, copy-out) through
+// the ring of slots.
+fp4q_status enqueue_chunks(Engine* g, const uint8_t* x, const float* tile_scale, int64_t rows, int64_t cols,
+                           uint8_t* q, uint8_t* scales, uint8_t* y, float* y_tile_scale, int64_t chunk,
+                           const SlotLayout& L, uint8_t* ws, cudaStream_t s, fp4q_stream_t stream) {
+    const uint64_t c = uint64_t(cols), tpr = c / 128;
+    cudaError_t e;
+    fp4q_status st;
+#define FP4Q_CUDA(call)                                                                         \
+    do {                                                                                        \
+        if ((e = (call)) != cudaSuccess)                                                        \
+            return fail(FP4Q_ERR_CUDA, "fp8_pipeline_host: %s: %s", #call, cudaGetErrorString(e)); \
+    } while (0)
+    // The first chunk is a quarter chunk: the device-to-host stream, the
+    // slower direction, starts after a quarter of the fill time.
+    const int64_t first = std::max<int64_t>(1, std::min(chunk / 4, rows));
+    int64_t ci = 0;
+    for (int64_t r = 0; r < rows; ++ci) {
+        const int k = int(ci % kSlots);
+        const uint64_t r0 = uint64_t(r), n = uint64_t(std::min(ci == 0 ? first : chunk, rows - r));
+        r += int64_t(n);
+        uint8_t* slot = ws + uint64_t(k) * L.bytes;
+        if (ci >= kSlots) FP4Q_CUDA(cudaStreamWaitEvent(g->in, g->stored[k], 0));
+        FP4Q_CUDA(cudaMemcpyAsync(slot + L.x, x + r0 * c, n * c, cudaMemcpyHostToDevice, g->in));
+        FP4Q_CUDA(cudaMemcpyAsync(slot + L.ts, tile_scale + r0 * tpr, n * tpr * 4, cudaMemcpyHostToDevice, g->in));
+        FP4Q_CUDA(cudaEventRecord(g->loaded[k], g->in));
+
+        FP4Q_CUDA(cudaStreamWaitEvent(s, g->loaded[k], 0));
+        if ((st = fp4q_mx_quantize(slot + L.x, FP4Q_E4M3, reinterpret_cast<const float*>(slot + L.ts), int64_t(n),
+                                   cols, cols, 1, slot + L.q, slot + L.s, FP4Q_SCALES_ROWMAJOR, stream)) != FP4Q_OK)
+            return st;
+        if ((st = fp4q_fp4_to_fp8(slot + L.q, slot + L.s, int64_t(n), cols, 1, slot + L.y,
+                                  reinterpret_cast<float*>(slot + L.yt), stream)) != FP4Q_OK)
+            return st;
+        FP4Q_CUDA(cudaEventRecord(g->converted[k], s));
+
+        FP4Q_CUDA(cudaStreamWaitEvent(g->out, g->converted[k], 0));
+        FP4Q_CUDA(cudaMemcpyAsync(q + r0 * (c / 2), slot + L.q, n * (c / 2), cudaMemcpyDeviceToHost, g->out));
+        FP4Q_CUDA(cudaMemcpyAsync(scales + r0 * (c / 32), slot + L.s, n * (c / 32), cudaMemcpyDeviceToHost, g->out));
+        FP4Q_CUDA(cudaMemcpyAsync(y + r0 * c, slot + L.y, n * c, cudaMemcpyDeviceToHost, g->out));
+        FP4Q_CUDA(cudaMemcpyAsync(y_tile_scale + r0 * tpr, slot + L.yt, n * tpr * 4, cudaMemcpyDeviceToHost, g->out));
+        FP4Q_CUDA(cudaEventRecord(g->stored[k], g->out));
+    }
+#undef FP4Q_CUDA
     return FP4Q_OK;
 }
 
@@ -120,51 +170,20 @@ extern "C" fp4q_status fp4q_fp8_pipeline_host(const uint8_t* x, const float* til
     if ((st = engine(&g)) != FP4Q_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const uint64_t c = uint64_t(cols), tpr = c / 128;
-    cudaError_t e;
-#define FP4Q_CUDA(call)                                                                         \
-    do {                                                                                        \
-        if ((e = (call)) != cudaSuccess)                                                        \
-            return fail(FP4Q_ERR_CUDA, "fp8_pipeline_host: %s: %s", #call, cudaGetErrorString(e)); \
-    } while (0)
     // everything queued on the caller's stream before this call comes first
-    FP4Q_CUDA(cudaEventRecord(g->start, s));
-    FP4Q_CUDA(cudaStreamWaitEvent(g->in, g->start, 0));
-    FP4Q_CUDA(cudaStreamWaitEvent(g->out, g->start, 0));
-    // The first chunk is a quarter chunk: the device-to-host stream, the
-    // slower direction, starts after a quarter of the fill time.
-    const int64_t first = std::max<int64_t>(1, std::min(chunk / 4, rows));
-    int64_t ci = 0, k_last = 0;
-    for (int64_t r = 0; r < rows; ++ci) {
-        const int k = int(ci % kSlots);
-        const uint64_t r0 = uint64_t(r), n = uint64_t(std::min(ci == 0 ? first : chunk, rows - r));
-        r += int64_t(n);
-        k_last = k;
-        uint8_t* slot = ws + uint64_t(k) * L.bytes;
-        if (ci >= kSlots) FP4Q_CUDA(cudaStreamWaitEvent(g->in, g->stored[k], 0));
-        FP4Q_CUDA(cudaMemcpyAsync(slot + L.x, x + r0 * c, n * c, cudaMemcpyHostToDevice, g->in));
-        FP4Q_CUDA(cudaMemcpyAsync(slot + L.ts, tile_scale + r0 * tpr, n * tpr * 4, cudaMemcpyHostToDevice, g->in));
-        FP4Q_CUDA(cudaEventRecord(g->loaded[k], g->in));
-
-        FP4Q_CUDA(cudaStreamWaitEvent(s, g->loaded[k], 0));
-        if ((st = fp4q_mx_quantize(slot + L.x, FP4Q_E4M3, reinterpret_cast<const float*>(slot + L.ts), int64_t(n),
-                                   cols, cols, 1, slot + L.q, slot + L.s, FP4Q_SCALES_ROWMAJOR, stream)) != FP4Q_OK)
-            return st;
-        if ((st = fp4q_fp4_to_fp8(slot + L.q, slot + L.s, int64_t(n), cols, 1, slot + L.y,
-                                  reinterpret_cast<float*>(slot + L.yt), stream)) != FP4Q_OK)
-            return st;
-        FP4Q_CUDA(cudaEventRecord(g->converted[k], s));
-
-        FP4Q_CUDA(cudaStreamWaitEvent(g->out, g->converted[k], 0));
-        FP4Q_CUDA(cudaMemcpyAsync(q + r0 * (c / 2), slot + L.q, n * (c / 2), cudaMemcpyDeviceToHost, g->out));
-        FP4Q_CUDA(cudaMemcpyAsync(scales + r0 * (c / 32), slot + L.s, n * (c / 32), cudaMemcpyDeviceToHost, g->out));
-        FP4Q_CUDA(cudaMemcpyAsync(y + r0 * c, slot + L.y, n * c, cudaMemcpyDeviceToHost, g->out));
-        FP4Q_CUDA(cudaMemcpyAsync(y_tile_scale + r0 * tpr, slot + L.yt, n * tpr * 4, cudaMemcpyDeviceToHost, g->out));
-        FP4Q_CUDA(cudaEventRecord(g->stored[k], g->out));
-    }
-    // the caller's stream continues once every chunk is back in host memory
-    // (copy-out is in order on its stream: the last chunk's event covers all)
-    FP4Q_CUDA(cudaStreamWaitEvent(s, g->stored[k_last], 0));
-#undef FP4Q_CUDA
-    return FP4Q_OK;
+    cudaError_t e = cudaEventRecord(g->start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(g->in, g->start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(g->out, g->start, 0);
+    if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "fp8_pipeline_host: stream ordering: %s", cudaGetErrorString(e));
+    st = enqueue_chunks(g, x, tile_scale, rows, cols, q, scales, y, y_tile_scale, chunk, L, ws, s, stream);
+    // The caller's stream continues once both copy streams are done with this
+    // call -- also after a failed enqueue, so that no copy the call issued is
+    // still running when the caller reuses its buffers.
+    cudaError_t j = cudaEventRecord(g->in_done, g->in);
+    if (j == cudaSuccess) j = cudaEventRecord(g->out_done, g->out);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(s, g->in_done, 0);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(s, g->out_done, 0);
+    if (st == FP4Q_OK && j != cudaSuccess)
+        st = fail(FP4Q_ERR_CUDA, "fp8_pipeline_host: stream ordering: %s", cudaGetErrorString(j));
+    return st;
 }

@@ -145,30 +145,34 @@ __global__ void __launch_bounds__(256) mx_rebase_kernel(const uint8_t* __restric
         }
     }
     __syncthreads();
+    // persistent: the group table above is built once per CTA, then each warp
+    // takes rows warp_id, warp_id + warps, ...
     const int lane = threadIdx.x & 31;
-    const int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (r >= rows || r >= off[groups]) return;
-    int lo = 0, hi = groups - 1;                     // group of row r: off[g] <= r < off[g + 1]
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (off[mid] <= r) lo = mid; else hi = mid - 1;
-    }
-    const int64_t prow = tpre[lo] * 128 + (r - off[lo]);   // row in the padded scale layout
-    uint32_t m = 0;
-    for (int j = lane; j < S32; j += 32) m = max(m, uint32_t(s[r * S32 + j]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const int base = int(m) - 127 - 8;
-    uint32_t bad = 0;
+    const int64_t nrows = min(rows, off[groups]);
+    const int64_t warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     const uint32_t S16 = uint32_t(S32) * 2;
-    for (int j = lane; j < S32; j += 32) {
-        const int kexp = int(s[r * S32 + j]) - 127 - base;
-        const uint32_t b = ue4m3_pow2(kexp);
-        bad += (kexp < -9);
-        *reinterpret_cast<uint16_t*>(out + mma_scale_offset(uint64_t(prow), uint32_t(2 * j), S16)) =
-            uint16_t(b | (b << 8));
+    uint32_t bad = 0;
+    for (int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < nrows; r += warps) {
+        int lo = 0, hi = groups - 1;                 // group of row r: off[g] <= r < off[g + 1]
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (off[mid] <= r) lo = mid; else hi = mid - 1;
+        }
+        const int64_t prow = tpre[lo] * 128 + (r - off[lo]);   // row in the padded scale layout
+        uint32_t m = 0;
+        for (int j = lane; j < S32; j += 32) m = max(m, uint32_t(s[r * S32 + j]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const int base = int(m) - 127 - 8;
+        for (int j = lane; j < S32; j += 32) {
+            const int kexp = int(s[r * S32 + j]) - 127 - base;
+            const uint32_t b = ue4m3_pow2(kexp);
+            bad += (kexp < -9);
+            *reinterpret_cast<uint16_t*>(out + mma_scale_offset(uint64_t(prow), uint32_t(2 * j), S16)) =
+                uint16_t(b | (b << 8));
+        }
+        if (lane == 0) row_scale[r] = exp2_wide(base);
     }
-    if (lane == 0) row_scale[r] = exp2_wide(base);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
     if (lane == 0 && bad && violations) atomicAdd(violations, bad);
@@ -243,9 +247,11 @@ extern "C" fp4q_status fp4q_mx_rebase_scales(const uint8_t* scales, int64_t rows
     if ((reinterpret_cast<uintptr_t>(offsets) & 7u) || (reinterpret_cast<uintptr_t>(ue4m3_mma) & 15u) ||
         (reinterpret_cast<uintptr_t>(row_scale) & 3u) || (reinterpret_cast<uintptr_t>(violations) & 3u))
         return fail(FP4Q_ERR_MISALIGNED, "mx_rebase_scales: offsets 8-byte, output 16-byte aligned");
-    fp4q_status st = current_device(nullptr);
+    int sms = 0;
+    fp4q_status st = current_device(&sms);
     if (st != FP4Q_OK) return st;
-    const int64_t blocks = (rows * 32 + 255) / 256;
+    const int64_t blocks = std::min<int64_t>((rows * 32 + 255) / 256,
+                                             int64_t(sms) * resident_per_sm(mx_rebase_kernel, 256));
     mx_rebase_kernel<<<unsigned(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         scales, rows, int(cols / 32), offsets, int(groups), ue4m3_mma, row_scale, violations);
     return check_launch("mx_rebase_scales");
