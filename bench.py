@@ -181,6 +181,22 @@ def cpu_oracle_rate(sample_rows: int, min_seconds: float = 0.0, max_passes: int 
     return nbytes / dt / 1e9, dt, cores, passes
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value of x over all ranks (the job's time is its slowest
+    rank's); x itself without a process group."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(nbytes_per_rank_step: int, ms_step: float, world: int) -> float:
+    """GB/s of the whole job: every rank moves its own replica's bytes per step."""
+    return world * nbytes_per_rank_step / ms_step / 1e6
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -634,13 +650,10 @@ def run_gpu(args, rank, world):
     ms_total = t_start.elapsed_time(t_end)
     a3_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs if e)
     a4_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs if e)
-    if dist:
-        tt = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, dist, "cuda")
     ms_step = ms_total / args.steps
     nbytes = bytes_fp8_to_mx(ROWS, COLS) + bytes_mx_to_fp8(ROWS, COLS)
-    value = world * nbytes / ms_step / 1e6          # GB/s over all ranks
+    value = whole_job_gbs(nbytes, ms_step, world)
 
     # ---- e2e through the C ABI with pinned host buffers ----
     hx = torch.from_numpy(e4).pin_memory()
