@@ -299,16 +299,31 @@ __global__ void __launch_bounds__(256) nv_quant_2d_kernel(
     const uint32_t warp = threadIdx.x >> 5, j = threadIdx.x & 15u, h = (threadIdx.x >> 4) & 1u;
     const uint32_t bl = 2 * warp + h;                              // block within the CTA tile
     const uint64_t cols = uint64_t(tpr) * 16;
+    // the next tile's 32 bytes are loaded before the current tile is processed,
+    // so a load is in flight across the two block barriers of each tile
+    auto fetch = [&](int64_t tile, u32x8& raw) {
+        const int64_t tr = tile / ctiles;
+        const uint32_t b = 16 * uint32_t(tile - tr * ctiles) + bl;
+        if (tile < ntiles && b < tpr) raw = ldg256(x + (tr * 16 + j) * ld_x_bytes + uint64_t(b) * 32);
+    };
+    u32x8 next{};
+    fetch(blockIdx.x, next);
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int64_t tr = tile / ctiles;
         const uint32_t ct = uint32_t(tile - tr * ctiles);
         const uint32_t b = 16 * ct + bl, nblk = min(16u, tpr - 16 * ct);
         const bool valid = b < tpr;
         const int64_t r = tr * 16 + j;
+        const u32x8 cur = next;
+        fetch(tile + gridDim.x, next);
         float t[16];
         uint32_t ab = 0;
         if (valid) {
-            load_tile(x + r * ld_x_bytes + uint64_t(b) * 32, t);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                t[2 * i] = u2f(cur.v[i] << 16);
+                t[2 * i + 1] = u2f(cur.v[i] & 0xffff0000u);
+            }
 #pragma unroll
             for (int e = 0; e < 16; ++e) ab = max(ab, f2u(t[e]) & 0x7fffffffu);
         }
@@ -601,13 +616,15 @@ extern "C" fp4q_status fp4q_nv_quantize_2d(const void* x, int64_t rows, int64_t 
     }
     const int mma = layout == FP4Q_SCALES_MMA;
     const int64_t tiles = (rows / 16) * int64_t((tpr + 15) / 16);       // 16 rows x 16 blocks
-    const int per_sm = resident_per_sm(nv_quant_2d_kernel<true>, 256);
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(tiles, int64_t(per_sm) * sms));
+    // persistent grid sized by the instance's own residency
+    auto grid_2d = [&](auto kernel) {
+        return unsigned(std::max<int64_t>(1, std::min<int64_t>(tiles, int64_t(resident_per_sm(kernel, 256)) * sms)));
+    };
     if (rounding == FP4Q_SR)
-        nv_quant_2d_kernel<true><<<unsigned(grid), 256, 0, s>>>(xb, rows, tpr, ld_x * 2, keys, amax_ptr, amax_out,
-                                                                tensor_scale_out, q, scales, mma);
+        nv_quant_2d_kernel<true><<<grid_2d(nv_quant_2d_kernel<true>), 256, 0, s>>>(
+            xb, rows, tpr, ld_x * 2, keys, amax_ptr, amax_out, tensor_scale_out, q, scales, mma);
     else
-        nv_quant_2d_kernel<false><<<unsigned(grid), 256, 0, s>>>(xb, rows, tpr, ld_x * 2, keys, amax_ptr, amax_out,
-                                                                 tensor_scale_out, q, scales, mma);
+        nv_quant_2d_kernel<false><<<grid_2d(nv_quant_2d_kernel<false>), 256, 0, s>>>(
+            xb, rows, tpr, ld_x * 2, keys, amax_ptr, amax_out, tensor_scale_out, q, scales, mma);
     return check_launch("nv_quantize_2d");
 }
