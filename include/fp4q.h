@@ -355,7 +355,8 @@ fp4q_status fp4q_moe_dispatch_static(const int32_t* topk, int64_t tokens, int to
  * Exact when E_j >= B_r - 9 for every block; blocks below that get scale 0
  * and are counted in *violations (if non-NULL; the caller zeroes it).
  * Output in the MMA layout with every group padded to whole 128-row tiles
- * (group g's tiles follow those of groups < g).
+ * (group g's tiles follow those of groups < g); the entries of the padding
+ * rows are unspecified (the GEMM's rows there are not stored).
  *   scales     device ROWMAJOR E8M0 [rows, cols/32];  cols % 128 == 0
  *   offsets    device int64 [groups + 1] row offsets (rows beyond offsets[groups] ignored)
  *   ue4m3_mma  device out, fp4q_rebased_scales_bytes(rows, cols, groups) bytes

@@ -178,6 +178,88 @@ __global__ void __launch_bounds__(256) mx_rebase_kernel(const uint8_t* __restric
     if (lane == 0 && bad && violations) atomicAdd(violations, bad);
 }
 
+// The same rebase, one padded 128-row tile at a time.  In the MMA scale layout
+// a 128-row tile's scales are one contiguous run of S16/4 chunks of 512 bytes,
+// so the CTA stages the tile's E8M0 rows in shared memory (rows padded by 4
+// bytes: the column reads of phase 2 then fall in 32 different banks), takes
+// each row's base, and writes every chunk as 16-byte stores -- thread (c4, i)
+// the bytes of rows i, i + 32, i + 64, i + 96 for columns 4 c4 .. 4 c4 + 3 --
+// so a warp writes 512 contiguous bytes.  Padding rows are written as 0.
+__global__ void __launch_bounds__(256) mx_rebase_tiles_kernel(const uint8_t* __restrict__ s, int S32,
+                                                              const int64_t* __restrict__ offsets, int groups,
+                                                              uint8_t* __restrict__ out, float* __restrict__ row_scale,
+                                                              uint32_t* __restrict__ violations) {
+    extern __shared__ __align__(16) uint8_t stage[];     // [128][S32 + 4] E8M0 bytes, then int base[128]
+    __shared__ int64_t off[kMaxExperts + 1];
+    __shared__ int64_t tpre[kMaxExperts + 1];
+    if (threadIdx.x == 0) {
+        int64_t acc = 0;
+        for (int g = 0; g <= groups; ++g) {
+            off[g] = offsets[g];
+            tpre[g] = acc;
+            if (g < groups) acc += (offsets[g + 1] - offsets[g] + 127) / 128;
+        }
+    }
+    __syncthreads();
+    const int RS = S32 + 4;                               // staged row stride (bytes)
+    int* base = reinterpret_cast<int*>(stage + 128 * RS);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ntiles = tpre[groups];
+    uint32_t bad = 0;
+    for (int64_t T = blockIdx.x; T < ntiles; T += gridDim.x) {
+        int lo = 0, hi = groups - 1;                      // group of padded tile T
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (tpre[mid] <= T) lo = mid; else hi = mid - 1;
+        }
+        const int64_t r0 = off[lo] + (T - tpre[lo]) * 128;
+        const int64_t left = off[lo + 1] - r0;
+        const int nreal = left < 128 ? int(left) : 128;
+        // phase 1: the tile's rows, 4 bytes per load (rows past the group: 0)
+        const int wpr = S32 / 4;
+        for (int w = threadIdx.x; w < 128 * wpr; w += blockDim.x) {
+            const int rr = w / wpr, cw = w - rr * wpr;
+            const uint32_t v = rr < nreal ? *reinterpret_cast<const uint32_t*>(s + (r0 + rr) * S32 + 4 * cw) : 0u;
+            *reinterpret_cast<uint32_t*>(stage + rr * RS + 4 * cw) = v;
+        }
+        __syncthreads();
+        for (int rr = warp; rr < 128; rr += int(blockDim.x >> 5)) {
+            uint32_t m = 0;
+            for (int j = lane; j < S32; j += 32) m = max(m, uint32_t(stage[rr * RS + j]));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) {
+                base[rr] = int(m) - 127 - 8;
+                if (rr < nreal) row_scale[r0 + rr] = exp2_wide(int(m) - 127 - 8);
+            }
+        }
+        __syncthreads();
+        // phase 2: 16-byte chunks of the tile's contiguous scale run
+        uint8_t* tile_out = out + uint64_t(T) * uint64_t(S32 / 2) * 512u;
+        for (int k = threadIdx.x; k < (S32 / 2) * 32; k += blockDim.x) {
+            const int c4 = k >> 5, i = k & 31;
+            uint32_t w[4];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const int rr = i + 32 * qq;
+                w[qq] = 0;
+                if (rr < nreal) {
+                    const int k0 = int(stage[rr * RS + 2 * c4]) - 127 - base[rr];
+                    const int k1 = int(stage[rr * RS + 2 * c4 + 1]) - 127 - base[rr];
+                    const uint32_t b0 = ue4m3_pow2(k0), b1 = ue4m3_pow2(k1);
+                    bad += uint32_t(k0 < -9) + uint32_t(k1 < -9);
+                    w[qq] = b0 | (b0 << 8) | (b1 << 16) | (b1 << 24);
+                }
+            }
+            *reinterpret_cast<uint4*>(tile_out + c4 * 512 + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        __syncthreads();                                  // the staging is reused by the next tile
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    if (lane == 0 && bad && violations) atomicAdd(violations, bad);
+}
+
 }  // namespace
 }  // namespace fp4q
 
@@ -250,6 +332,17 @@ extern "C" fp4q_status fp4q_mx_rebase_scales(const uint8_t* scales, int64_t rows
     int sms = 0;
     fp4q_status st = current_device(&sms);
     if (st != FP4Q_OK) return st;
+    const int S32 = int(cols / 32);
+    if (S32 <= 1024) {
+        // tile-wise form: the padded tiles number at most rows / 128 + groups
+        const uint32_t smem = uint32_t(128 * (S32 + 4) + 128 * 4);
+        const int64_t tiles_upper = (rows + 127) / 128 + groups;
+        const int64_t blocks = std::min<int64_t>(tiles_upper, int64_t(sms) *
+                                                 resident_per_sm_smem(mx_rebase_tiles_kernel, 256, smem));
+        mx_rebase_tiles_kernel<<<unsigned(blocks), 256, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
+            scales, S32, offsets, int(groups), ue4m3_mma, row_scale, violations);
+        return check_launch("mx_rebase_scales");
+    }
     const int64_t blocks = std::min<int64_t>((rows * 32 + 255) / 256,
                                              int64_t(sms) * resident_per_sm(mx_rebase_kernel, 256));
     mx_rebase_kernel<<<unsigned(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
