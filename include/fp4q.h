@@ -282,10 +282,12 @@ typedef struct fp4q_operand {
  * FP4 storage, FP8 GEMMs); their scales come from
  * fp4q_fp8_tile_scales_to_e8m0.
  *   A, B     operands of the same format; A has M rows, B has N rows, both K columns
- *   K        multiple of 128;  M, N >= 1
+ *   K        multiple of 128;  M, N >= 0 (M or N == 0: nothing is done;
+ *            K == 0: D is set to zero)
  *   D        device out, [M, ldd] of d_type (FP4Q_BF16, RNE from FP32, or FP4Q_FP32),
  *            ldd >= N, ldd * element size a multiple of 16 bytes
- * FP32 accumulation.
+ * FP32 accumulation.  Limits: M, N, K <= 2^30 and fewer than 2^31 output
+ * tiles of 128 x 256, else FP4Q_ERR_UNSUPPORTED_SHAPE.
  */
 fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M,
                                    int64_t N, int64_t K, void* D, fp4q_dtype d_type,
@@ -390,7 +392,9 @@ typedef enum fp4q_epilogue {
  *   d_scales       SILU_GATE: device ROWMAJOR E8M0 [rows, N/64]; else unused
  *   h_debug        SILU_GATE: optional device FP32 [rows, N/2] copy of h before
  *                  quantization (NULL: not written)
- * FP32 accumulation; limits: 1 <= groups <= 256.
+ * FP32 accumulation; limits: 1 <= groups <= 256, rows, K and groups * N at
+ * most 2^30, fewer than 2^31 output tiles of 128 x 256 (counting one partial
+ * tile per group), else FP4Q_ERR_UNSUPPORTED_SHAPE; K == 0 is unsupported.
  */
 fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_scales, const float* a_row_scale,
                               const uint8_t* b_q, const uint8_t* b_scales, const float* b_tensor_scale,

@@ -1,5 +1,6 @@
 // Status codes, per-thread error detail, device checks and the device status
 // word of the fp4q library.
+#include <atomic>
 #include <mutex>
 #include <stdarg.h>
 #include <stdio.h>
@@ -35,7 +36,7 @@ fp4q_status check_launch(const char* what) {
 namespace {
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
-    bool ready = false;
+    std::atomic<bool> ready{false};    // set (release) once the fields below are filled in
     bool supported = false;
     int sms = 0;
     uint32_t* status = nullptr;
@@ -50,9 +51,9 @@ fp4q_status current_device(int* sms) {
     if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return fail(FP4Q_ERR_UNSUPPORTED_DEVICE, "device index %d", dev);
     DeviceInfo& d = g_dev[dev];
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lock(g_dev_mutex);
-        if (!d.ready) {
+        if (!d.ready.load(std::memory_order_relaxed)) {
             int major = 0, minor = 0, count = 0;
             if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
                 cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -67,7 +68,7 @@ fp4q_status current_device(int* sms) {
                     return fail(FP4Q_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
                 d.status = static_cast<uint32_t*>(p);
             }
-            d.ready = true;
+            d.ready.store(true, std::memory_order_release);
         }
     }
     if (!d.supported)
@@ -155,7 +156,9 @@ namespace ring {
 
 fp4q_status encode_bf16_tile_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols, int64_t ld,
                                  uint32_t box_cols, uint32_t box_rows) {
-    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    // looked up on first use; concurrent first calls store the same pointer
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> encode_fn{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn.load(std::memory_order_acquire);
     if (!encode) {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -163,6 +166,7 @@ fp4q_status encode_bf16_tile_map(CUtensorMap* map, const void* x, int64_t rows, 
         if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
             return fail(FP4Q_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
         encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        encode_fn.store(encode, std::memory_order_release);
     }
     cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
     cuuint64_t strides[1] = {cuuint64_t(ld * 2)};

@@ -41,6 +41,8 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "tc.cuh"
 
@@ -690,18 +692,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+// Looked up on first use; concurrent first calls store the same pointer.
+std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode_fn{nullptr};
 
 fp4q_status get_encoder() {
-    if (g_encode) return FP4Q_OK;
+    if (g_encode_fn.load(std::memory_order_acquire)) return FP4Q_OK;
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
         return fail(FP4Q_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    g_encode_fn.store(reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn), std::memory_order_release);
     return FP4Q_OK;
 }
+
+// The encoder; valid once get_encoder() has returned FP4Q_OK.
+PFN_cuTensorMapEncodeTiled_v12000 encoder() { return g_encode_fn.load(std::memory_order_acquire); }
 
 // 2D map over operand bytes [rows, row_bytes] (K/2 for FP4, K for FP8):
 // 128-byte x 128-row boxes, 128B swizzle.
@@ -710,7 +716,7 @@ fp4q_status encode_operand_map(CUtensorMap* map, const uint8_t* q, int64_t rows,
     cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
     cuuint32_t box[2] = {128u, 128u};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(q), dims, strides, box, estr,
+    CUresult r = encoder()(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(q), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(FP4Q_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
@@ -724,7 +730,7 @@ fp4q_status encode_output_map(CUtensorMap* map, void* D, int64_t rows, int64_t N
     cuuint64_t strides[1] = {cuuint64_t(ld * 2)};
     cuuint32_t box[2] = {64u, 128u};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, dims, strides, box, estr,
+    CUresult r = encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(FP4Q_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d)", int(r));
@@ -737,13 +743,14 @@ fp4q_status launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const CU
                           int tiles_upper, int sms, cudaStream_t stream) {
     constexpr uint32_t smem = Layout<NST>::smem_bytes;
     auto kernel = gemm_kernel<EPI, NST, CL>;
-    static bool attr_set[64] = {};
+    // per device, set on first use (setting it twice from racing threads is harmless)
+    static std::atomic<bool> attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (!attr_set[dev & 63]) {
+    if (!attr_set[dev & 63].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
-        attr_set[dev & 63] = true;
+        attr_set[dev & 63].store(true, std::memory_order_release);
     }
     if constexpr (CL == 2) {
         const int m_tiles = (a.M + BM - 1) / BM;
@@ -803,6 +810,8 @@ extern "C" fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_
     if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30))
         return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "gemm: sizes beyond 2^30");
     if (M == 0 || N == 0) return FP4Q_OK;
+    if (((M + BM - 1) / BM) * ((N + BN - 1) / BN) > INT32_MAX)
+        return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "gemm: more than 2^31 output tiles");
     if (!A->q || !B->q || !A->scales || !B->scales || !D)
         return fail(FP4Q_ERR_INVALID_ARGUMENT, "gemm: null pointer");
     const bool nv = A->format == FP4Q_NVFP4;
@@ -871,6 +880,8 @@ extern "C" fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sc
     if (rows > (1 << 30) || groups * N > (1 << 30) || K > (1 << 30))
         return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "grouped_gemm: sizes beyond 2^30");
     if (rows == 0) return FP4Q_OK;
+    if (((rows + BM - 1) / BM + groups) * ((N + BN - 1) / BN) > INT32_MAX)
+        return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "grouped_gemm: more than 2^31 output tiles");
     if (!a_q || !a_scales || !a_row_scale || !b_q || !b_scales || !b_tensor_scale || !offsets || !D ||
         (epilogue == FP4Q_EPI_SILU_GATE_MXFP4 && !d_scales))
         return fail(FP4Q_ERR_INVALID_ARGUMENT, "grouped_gemm: null pointer");

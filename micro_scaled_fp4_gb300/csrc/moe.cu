@@ -18,6 +18,8 @@
 // UE4M3 value 2^(E_j - B) for both of its 16-element halves (exact for
 // E_j - B >= -9), written in the MMA scale layout with every group padded to
 // whole 128-row tiles; the row factor 2^B goes to the GEMM epilogue.
+#include <atomic>
+
 #include "common.cuh"
 
 namespace fp4q {
@@ -369,7 +371,7 @@ namespace {
 
 static __device__ __align__(256) uint8_t g_dispatch_scratch[FP4Q_MOE_DISPATCH_STATIC_SCRATCH_BYTES];
 
-void* g_dispatch_scratch_addr[64] = {};
+std::atomic<void*> g_dispatch_scratch_addr[64] = {};
 
 // Device address of the scratch array on the current device, looked up once
 // per device (the host-side name of the array is not a device address).
@@ -378,14 +380,14 @@ fp4q_status dispatch_scratch(void** out) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 64) return fail(FP4Q_ERR_UNSUPPORTED_DEVICE, "device index %d", dev);
-    if (!g_dispatch_scratch_addr[dev]) {
-        void* p = nullptr;
+    void* p = g_dispatch_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
         e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
         if (e != cudaSuccess || !p)
             return fail(FP4Q_ERR_CUDA, "cudaGetSymbolAddress(dispatch scratch): %s", cudaGetErrorString(e));
-        g_dispatch_scratch_addr[dev] = p;
+        g_dispatch_scratch_addr[dev].store(p, std::memory_order_release);
     }
-    *out = g_dispatch_scratch_addr[dev];
+    *out = p;
     return FP4Q_OK;
 }
 

@@ -117,10 +117,14 @@ def test_argument_errors_need_no_gpu(lib):
     B = lib.make_operand(x, x, lib.FP4Q_NVFP4, x)
     for args, status in [((A, B, 128, 128, 128, x, 0, 128), 1), ((A, A, 128, 128, 96, x, 0, 128), 2),
                          ((A, A, 128, 128, 128, x + 2, 0, 128), 3), ((A, A, 128, 128, 128, x, 0, 100), 1),
-                         ((A, A, 128, 128, 128, x, 0, 132), 3)]:
+                         ((A, A, 128, 128, 128, x, 0, 132), 3),
+                         ((A, A, 1 << 30, 1 << 30, 128, x, 0, 1 << 30), 2)]:     # 2^45 output tiles
         with pytest.raises(E) as e:
             lib.fp4q_block_scaled_gemm(*args, stream=0)
         assert e.value.status == status, (args, e.value)
+    with pytest.raises(E) as e:       # 2^43 output tiles of the grouped form
+        lib.fp4q_grouped_gemm(x, x, x, x, x, x, x, 1 << 30, 4, 1 << 28, 128, 0, x, None, None, stream=0)
+    assert e.value.status == 2
 
 
 def test_fp8_pipeline_host_workspace_bytes(lib):
