@@ -180,6 +180,9 @@ def fp8_pipeline_host(x, tile_scale, chunk_rows=0, pinned=True, stream=None):
     """E4M3 host tensor [R, C] (uint8 or float8_e4m3fn) + FP32 tile scales
     [R, C/128] -> host dict(q, scales, y, y_tile_scale); synchronizes the stream."""
     torch = _torch()
+    for name, t in (("x", x), ("tile_scale", tile_scale)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
     R, C = x.shape
     mk = (lambda shape, dt: torch.empty(shape, dtype=dt).pin_memory()) if pinned else \
         (lambda shape, dt: torch.empty(shape, dtype=dt))
@@ -285,12 +288,31 @@ def _torch():
     return torch
 
 
+def _on_device(name, t, rows_strided=False):
+    """Checks a helper's tensor argument before its address reaches a kernel:
+    a CUDA tensor on the current device, contiguous (``rows_strided``: unit
+    stride along the last axis, any row stride).  None passes (optional)."""
+    if t is None:
+        return
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise ValueError(f"{name} is on {t.device}; the library works on the current device cuda:{cur}")
+    ok = t.stride(-1) == 1 if (rows_strided and t.dim() == 2) else t.is_contiguous()
+    if not ok:
+        raise ValueError(f"{name} must be contiguous" + (" along its rows" if rows_strided else ""))
+
+
 def mx_quantize(x, tile_scale=None, layout=FP4Q_SCALES_ROWMAJOR, block_axis=1, stream=None):
     """BF16 / FP32 / float8_e4m3fn [R, C] -> (q uint8, scales uint8).
 
     block_axis 1: q [R, C/2], scales of R x C/32.  block_axis 0 (BF16): the
     quantization of X^T, q [C, R/2], scales of C x R/32."""
     torch = _torch()
+    _on_device("x", x, rows_strided=True)
+    _on_device("tile_scale", tile_scale)
     R, C = x.shape
     xt = {torch.bfloat16: FP4Q_BF16, torch.float32: FP4Q_FP32, torch.float8_e4m3fn: FP4Q_E4M3,
           torch.uint8: FP4Q_E4M3}[x.dtype]
@@ -303,6 +325,8 @@ def mx_quantize(x, tile_scale=None, layout=FP4Q_SCALES_ROWMAJOR, block_axis=1, s
 
 def mx_dequantize(q, s, dtype=None, stream=None):
     torch = _torch()
+    _on_device("q", q)
+    _on_device("s", s)
     dtype = dtype or torch.bfloat16
     R, C = q.shape[0], q.shape[1] * 2
     y = torch.empty((R, C), dtype=dtype, device=q.device)
@@ -313,6 +337,7 @@ def mx_dequantize(q, s, dtype=None, stream=None):
 def fp8_mma_scales(tile_scale, stream=None):
     """FP32 power-of-two 1x128 tile scales [R, C/128] -> E8M0 per 32 in the MMA layout."""
     torch = _torch()
+    _on_device("tile_scale", tile_scale)
     R, C = tile_scale.shape[0], tile_scale.shape[1] * 128
     s = torch.empty(fp4q_scales_bytes(R, C // 32, FP4Q_SCALES_MMA), dtype=torch.uint8, device=tile_scale.device)
     fp4q_fp8_tile_scales_to_e8m0(tile_scale, R, C, s, FP4Q_SCALES_MMA, stream)
@@ -322,6 +347,8 @@ def fp8_mma_scales(tile_scale, stream=None):
 def fp4_row_to_fp8_col(q, s, stream=None):
     """Row-wise MXFP4 [R, C] -> (E4M3 of the transpose [C, R], FP32 tile scales [C, R/128])."""
     torch = _torch()
+    _on_device("q", q)
+    _on_device("s", s)
     R, C = q.shape[0], q.shape[1] * 2
     y = torch.empty((C, R), dtype=torch.uint8, device=q.device)
     ts = torch.empty((C, R // 128), dtype=torch.float32, device=q.device)
@@ -331,6 +358,8 @@ def fp4_row_to_fp8_col(q, s, stream=None):
 
 def fp4_to_fp8(q, s, stream=None):
     torch = _torch()
+    _on_device("q", q)
+    _on_device("s", s)
     R, C = q.shape[0], q.shape[1] * 2
     y = torch.empty((R, C), dtype=torch.uint8, device=q.device)
     ts = torch.empty((R, C // 128), dtype=torch.float32, device=q.device)
@@ -346,6 +375,8 @@ def nv_quantize(x, rht=False, rht_seed=0, rounding=FP4Q_RNE, sr_seed=0, amax=Non
     block_axis 0: the quantization of X^T (q [C, R/2]).  two_d: 16x16 tile
     scales (fp4q_nv_quantize_2d; no rotation, block_axis 1)."""
     torch = _torch()
+    _on_device("x", x, rows_strided=True)
+    _on_device("amax", amax)
     R, C = x.shape
     OR, OC = (R, C) if block_axis == 1 else (C, R)
     q = torch.empty((OR, OC // 2), dtype=torch.uint8, device=x.device)
@@ -371,6 +402,8 @@ def gemm(qa, sa, qb, sb, fmt=FP4Q_MXFP4, ts_a=None, ts_b=None, out_dtype=None, s
     [M, N] view of a row-padded output (row stride a multiple of 16 bytes).
     """
     torch = _torch()
+    for name, t in (("qa", qa), ("sa", sa), ("qb", qb), ("sb", sb), ("ts_a", ts_a), ("ts_b", ts_b)):
+        _on_device(name, t)
     out_dtype = out_dtype or torch.bfloat16
     M, N, K = qa.shape[0], qb.shape[0], qa.shape[1] * (1 if fmt == FP4Q_MXFP8 else 2)
     esz = 2 if out_dtype == torch.bfloat16 else 4
@@ -386,6 +419,8 @@ def moe_dispatch(topk, q, s, n_experts, stream=None):
     """topk int32 [T, k] (device); q [T, C/2], s [T, C/32] ROWMAJOR.  Returns
     dict(offsets int64 [E+1], row_token int32 [T*k], q, s) of the dispatched rows."""
     torch = _torch()
+    for name, t in (("topk", topk), ("q", q), ("s", s)):
+        _on_device(name, t)
     T, k = topk.shape
     C = q.shape[1] * 2
     dev = q.device
@@ -402,6 +437,8 @@ def moe_dispatch(topk, q, s, n_experts, stream=None):
 def mx_rebase_scales(s, offsets, cols, groups, violations=None, stream=None):
     """ROWMAJOR E8M0 [R, cols/32] -> (UE4M3 MMA layout padded per group, FP32 row factor [R])."""
     torch = _torch()
+    for name, t in (("s", s), ("offsets", offsets), ("violations", violations)):
+        _on_device(name, t)
     R = s.shape[0]
     out = torch.zeros(fp4q_rebased_scales_bytes(R, cols, groups), dtype=torch.uint8, device=s.device)
     rs = torch.empty(R, dtype=torch.float32, device=s.device)
@@ -413,6 +450,9 @@ def grouped_gemm(a_q, a_scales, a_row_scale, b_q, b_scales, b_ts, offsets, group
                  h_debug=False, stream=None):
     """Returns D (BF16 [R, N]) or (h codes [R, N/4], h E8M0 [R, N/64], h FP32 or None) for the gated form."""
     torch = _torch()
+    for name, t in (("a_q", a_q), ("a_scales", a_scales), ("a_row_scale", a_row_scale), ("b_q", b_q),
+                    ("b_scales", b_scales), ("b_ts", b_ts), ("offsets", offsets)):
+        _on_device(name, t)
     R, K = a_q.shape[0], a_q.shape[1] * 2
     dev = a_q.device
     if epilogue == FP4Q_EPI_STORE_BF16:

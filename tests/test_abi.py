@@ -153,3 +153,17 @@ def test_no_cpu_fallback_when_library_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(fq, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         fq.load()
+
+
+def test_helpers_reject_host_and_strided_tensors(lib):
+    """The allocating helpers check their tensors before any address reaches
+    the library: a host tensor, or a transposed one, is a ValueError."""
+    import torch
+    x = torch.zeros((4, 64), dtype=torch.bfloat16)
+    for call in (lambda: lib.mx_quantize(x), lambda: lib.nv_quantize(x),
+                 lambda: lib.fp4_to_fp8(torch.zeros((4, 64), dtype=torch.uint8), torch.zeros((4, 4), dtype=torch.uint8)),
+                 lambda: lib.gemm(*(torch.zeros((128, 64), dtype=torch.uint8),) * 4)):
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call()
+    with pytest.raises(ValueError, match="host tensor"):
+        lib.fp8_pipeline_host(torch.zeros((128, 256), dtype=torch.uint8).t(), torch.zeros((128, 2)))
