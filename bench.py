@@ -677,12 +677,17 @@ def run_gpu(args, rank, world):
         e2e_step()
     torch.cuda.synchronize()
     e0, e1 = _events(torch, 2)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(e2e_steps):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        dist.barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda") / e2e_steps
     h2d = hx.numel() + ht.numel() * 4
     d2h = hq.numel() + hs.numel() + hy.numel() + hyt.numel() * 4
     clk = clocks.stop()
@@ -721,7 +726,8 @@ def run_gpu(args, rank, world):
                        "kernel_events": f"per-kernel CUDA events on every {EVENT_EVERY}th timed step",
                        "frac_hbm": round(value / world / peaks["hbm_gbs"], 3)},
             "wall_s_timed_region": round(wall, 4),
-            "e2e": {"value": round(nbytes / e2e_ms / 1e6, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "e2e": {"value": round(whole_job_gbs(nbytes, e2e_ms, world), 1), "unit": "GB/s",
+                    "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4),
                     "call": "fp4q_fp8_pipeline_host", "chunk_rows": args.e2e_chunk},
             "gpu_launches": 2 * args.steps, "roofline": roof, "cpu_baseline": cpu, "clocks": clk, "rows": rows}
