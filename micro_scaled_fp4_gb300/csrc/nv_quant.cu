@@ -84,26 +84,24 @@ __global__ void __launch_bounds__(256) nv_amax_kernel(const uint8_t* __restrict_
 // Stochastic rounding of v onto E2M1 with the 32-bit word r: up iff
 // r < frac * 2^32, frac the exact position of |v| between its two grid
 // neighbours; |v| >= 6 saturates; the sign is kept.  Returns the 4-bit code.
-// Integer form on the FP32 bits u of |v|, without branches: for |v| in
+// Integer form on the FP32 bits u of a = min(|v|, 6), without branches (the
+// clamp makes 6 and above land on code 7 with nothing to round up): for a in
 // [2^k, 2^(k+1)), k >= 0, the grid points are 2^k and 1.5 * 2^k (step
-// 2^(k-1)), the code below |v| is 2(k + 1) + (mantissa bit 22) and
-// frac * 2^32 = u << 10 (the mantissa bits below bit 22); in [0.5, 1) the step
-// is 0.5 from 0.5 (code 1), frac * 2^32 = u << 9; below 0.5 the step is 0.5
-// from 0 and frac * 2^32 = |v| * 2^33 (exact), whose ceiling decides the
+// 2^(k-1)), the code below a is 2(k + 1) + (mantissa bit 22) = (u >> 22) - 252
+// and frac * 2^32 = u << 10 (the mantissa bits below bit 22); in [0.5, 1) the
+// step is 0.5 from 0.5 (code 1), frac * 2^32 = u << 9; below 0.5 the step is
+// 0.5 from 0 and frac * 2^32 = a * 2^33 (exact), whose ceiling decides the
 // strict comparison.
 __device__ __forceinline__ uint32_t sr_e2m1_code(float v, uint32_t r) {
-    const uint32_t bits = f2u(v);
-    const uint32_t u = bits & 0x7fffffffu;
-    const uint32_t sign = (bits >> 28) & 8u;
-    const bool ge1 = u >= 0x3f800000u;
-    const uint32_t code_hi = ge1 ? ((((u >> 23) - 126u) << 1) | ((u >> 22) & 1u)) : 1u;
-    const uint32_t thr_hi = ge1 ? (u << 10) : (u << 9);
-    const uint32_t thr_lo = __float2uint_ru(__fmul_rn(u2f(u), 8589934592.0f));   // |v| * 2^33, < 2^32 below 0.5
+    const float a = fminf(fabsf(v), 6.0f);
+    const uint32_t u = f2u(a);
+    const uint32_t code_hi = uint32_t(max(int(u >> 22) - 252, 1));
+    const uint32_t thr_hi = u << (u >= 0x3f800000u ? 10 : 9);
+    const uint32_t thr_lo = __float2uint_ru(__fmul_rn(a, 8589934592.0f));   // a * 2^33, < 2^32 below 0.5
     const bool lt_half = u < 0x3f000000u;
     const uint32_t code = lt_half ? 0u : code_hi;
     const uint32_t thr = lt_half ? thr_lo : thr_hi;
-    const uint32_t q = u >= 0x40c00000u ? 7u : code + (r < thr ? 1u : 0u);
-    return sign | q;
+    return ((f2u(v) >> 28) & 8u) | (code + (r < thr ? 1u : 0u));
 }
 
 // The ten round keys of Philox4x32-10 for one seed (key schedule (k0, k1) +=
