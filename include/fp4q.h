@@ -415,6 +415,17 @@ fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_scales, const
 fp4q_status fp4q_device_status(uint32_t* status_out, int reset);
 
 /*
+ * fp4q_stream_status -- fp4q_device_status scoped to one stream: waits for
+ * `stream` only (not the whole device), then reads the status word of the
+ * current device into *status_out (optional; NULL: not written) and, if
+ * reset != 0, clears it, both ordered on `stream`.  The word is per device, so
+ * bits set by kernels on other streams show too.  Returns FP4Q_OK when the
+ * word is 0, FP4Q_ERR_TIMEOUT when a bit is set, FP4Q_ERR_CUDA when the stream
+ * cannot be waited for.  Synchronous on the host.
+ */
+fp4q_status fp4q_stream_status(uint32_t* status_out, int reset, fp4q_stream_t stream);
+
+/*
  * fp4q_check_wait_timeout -- self-check of the device-side failure path.  The
  * pages have no counterpart: this is library infrastructure.  Launches one
  * thread that waits, with the same bounded mbarrier wait the GEMM kernels use,

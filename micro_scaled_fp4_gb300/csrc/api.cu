@@ -151,6 +151,19 @@ extern "C" fp4q_status fp4q_device_status(uint32_t* status_out, int reset) {
     return v ? FP4Q_ERR_TIMEOUT : FP4Q_OK;
 }
 
+extern "C" fp4q_status fp4q_stream_status(uint32_t* status_out, int reset, fp4q_stream_t stream) {
+    fp4q_status st = current_device(nullptr);
+    if (st != FP4Q_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, status_word(), sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && reset) e = cudaMemsetAsync(status_word(), 0, sizeof v, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "stream_status: %s", cudaGetErrorString(e));
+    if (status_out) *status_out = v;
+    return v ? FP4Q_ERR_TIMEOUT : FP4Q_OK;
+}
+
 namespace fp4q {
 namespace ring {
 

@@ -34,6 +34,7 @@ EXPORTED = [
     "fp4q_moe_dispatch", "fp4q_rebased_scales_bytes", "fp4q_mx_rebase_scales", "fp4q_grouped_gemm",
     "fp4q_moe_dispatch_static", "fp4q_check_wait_timeout", "fp4q_nv_quantize_2d", "fp4q_fp4_row_to_fp8_col",
     "fp4q_fp8_tile_scales_to_e8m0", "fp4q_fp8_pipeline_host_workspace_bytes", "fp4q_fp8_pipeline_host",
+    "fp4q_stream_status",
 ]
 MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 * 1024 * 1024
 
@@ -90,6 +91,7 @@ def load() -> ctypes.CDLL:
                 "fp4q_block_scaled_gemm": [ctypes.POINTER(fp4q_operand), ctypes.POINTER(fp4q_operand), i64, i64,
                                            i64, vp, ci, i64, vp],
                 "fp4q_device_status": [ctypes.POINTER(ctypes.c_uint32), ci],
+                "fp4q_stream_status": [ctypes.POINTER(ctypes.c_uint32), ci, vp],
                 "fp4q_moe_dispatch": [vp, i64, ci, ci, vp, vp, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp],
                 "fp4q_mx_rebase_scales": [vp, i64, i64, vp, i64, vp, vp, vp, vp],
                 "fp4q_moe_dispatch_static": [vp, i64, ci, ci, vp, vp, i64, vp, vp, vp, vp, vp],
@@ -269,6 +271,16 @@ def fp4q_grouped_gemm(a_q, a_scales, a_row_scale, b_q, b_scales, b_tensor_scale,
 
 def fp4q_check_wait_timeout(limit_ns: int, stream=None):
     return _check("fp4q_check_wait_timeout", load().fp4q_check_wait_timeout(limit_ns, _stream(stream)))
+
+
+def fp4q_stream_status(reset: bool = False, stream=None) -> int:
+    """Waits for the stream, then returns the device status word (0 = no
+    device-side wait timed out)."""
+    v = ctypes.c_uint32(0)
+    st = load().fp4q_stream_status(ctypes.byref(v), int(bool(reset)), _stream(stream))
+    if st not in (FP4Q_OK, 6):
+        _check("fp4q_stream_status", st)
+    return int(v.value)
 
 
 def fp4q_device_status(reset: bool = False) -> int:

@@ -31,7 +31,8 @@ def lib():
 def test_header_declares_the_entry_points():
     names = _declared()
     for n in ["fp4q_mx_quantize", "fp4q_mx_dequantize", "fp4q_fp4_to_fp8", "fp4q_nv_quantize",
-              "fp4q_block_scaled_gemm", "fp4q_status_string", "fp4q_device_status"]:
+              "fp4q_block_scaled_gemm", "fp4q_status_string", "fp4q_device_status", "fp4q_stream_status",
+              "fp4q_grouped_gemm", "fp4q_nv_quantize_workspace_bytes"]:
         assert n in names, n
 
 

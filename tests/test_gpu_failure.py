@@ -31,6 +31,10 @@ def test_wait_that_runs_out_is_reported(fq, oracle):
     assert time.time() - t0 >= 0.15
     assert word == 1 << 31
     assert fq.fp4q_device_status() == 0                           # cleared by the reset
+    # the same through the stream-scoped read
+    fq.fp4q_check_wait_timeout(100_000_000)
+    assert fq.fp4q_stream_status(reset=True) == 1 << 31          # waits for the current stream
+    assert fq.fp4q_stream_status() == 0
     # the context is still usable
     from micro_scaled_fp4_gb300 import workloads as W
     x = W.activation_bf16(16, 256, seed=9)
