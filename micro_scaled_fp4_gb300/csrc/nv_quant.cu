@@ -24,10 +24,16 @@ namespace fp4q {
 namespace {
 
 // (1/4) H16 diag(d) x, d_j = -1 iff bit j of `signs` is set.  Butterflies with
-// strides 1, 2, 4, 8 map (a, b) -> (a + b, a - b) in FP32.
+// strides 1, 2, 4, 8 map (a, b) -> (a + b, a - b) in FP32.  SKIP_ZERO: no sign
+// flips when `signs` is 0 (the deterministic H16; a branch uniform over the
+// grid).  The column kernels, which serve the Wgrad operands with the
+// deterministic H16, take it; the row kernels keep the unconditional flips.
+template <bool SKIP_ZERO = false>
 __device__ __forceinline__ void rht16(float (&t)[16], uint32_t signs) {
+    if (!SKIP_ZERO || signs) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) t[j] = u2f(f2u(t[j]) ^ (((signs >> j) & 1u) << 31));
+        for (int j = 0; j < 16; ++j) t[j] = u2f(f2u(t[j]) ^ (((signs >> j) & 1u) << 31));
+    }
 #pragma unroll
     for (int h = 1; h < 16; h <<= 1)
 #pragma unroll
@@ -423,8 +429,8 @@ __global__ void __launch_bounds__(ring::kMaxThreads, MODE == 2 ? 2 : 3) nv_col_k
             b[j] = u2f(w & 0xffff0000u);
         }
         if (rht) {
-            rht16(a, signs);
-            rht16(b, signs);
+            rht16<true>(a, signs);
+            rht16<true>(b, signs);
         }
         uint32_t ma = 0, mb = 0;
 #pragma unroll
