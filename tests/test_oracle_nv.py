@@ -128,7 +128,8 @@ def test_nv_invariants(oracle):
         ratio = ab[normal] / sf[normal]
         assert np.all(ratio >= 6 / (1 + 2 ** -4) - 1e-5) and np.all(ratio <= 6 / (1 - 2 ** -4) + 1e-5)
         # RNE error <= half a grid step (with saturation above 6)
-        v = y.astype(np.float64) / np.repeat(sf, 16, axis=1)
+        with np.errstate(divide="ignore", invalid="ignore"):     # zero blocks (sf = 0) are masked below
+            v = y.astype(np.float64) / np.repeat(sf, 16, axis=1)
         step = np.where(np.abs(v) < 2, 0.5, np.where(np.abs(v) < 4, 1.0, 2.0))
         ok = np.repeat(sb, 16, axis=1) > 0
         err = np.abs(vals - np.clip(v, -6, 6))[ok]
