@@ -192,6 +192,25 @@ def test_moe_small(fq, oracle):
     assert offs[-1] == 1400
 
 
+def test_moe_k_tails(fq, oracle):
+    """K = 384 in both grouped GEMMs (a 128-element last stage), 5 experts."""
+    offs = _run_moe(fq, oracle, T=300, H=384, I=384, E=5, k=2, seed=30)
+    assert offs[-1] == 600
+
+
+def test_moe_most_experts(fq, oracle):
+    """256 experts (the limit), top-2 over 600 tokens: mostly tiny or empty
+    groups, all of them computed; the experts with at least 64 rows are checked
+    (the h-code comparison allows one flip per 1000 codes of an expert)."""
+    from micro_scaled_fp4_gb300 import workloads as W
+    T, E, k, seed = 600, 256, 2, 40
+    _, offs_ref = oracle.moe_dispatch(W.moe_routing(tokens=T, experts=E, top_k=k, seed=seed + 1), E)
+    big = [e for e in range(E) if offs_ref[e + 1] - offs_ref[e] >= 64]
+    assert big and np.sum(np.diff(offs_ref) == 0) > 0       # some large groups and some empty ones
+    offs = _run_moe(fq, oracle, T=T, H=256, I=128, E=E, k=k, seed=seed, check_experts=big)
+    assert offs[-1] == T * k and len(offs) == E + 1
+
+
 def test_moe_empty_expert(fq, oracle):
     """A routing that leaves experts empty and one expert with a single row."""
     import torch
