@@ -58,7 +58,8 @@ def _check(oracle, d_bf16, d_f32, ref):
     return e32, eb
 
 
-SHAPES = [(128, 256, 256), (128, 256, 128), (200, 300, 384), (1000, 520, 1024), (64, 64, 512), (512, 2048, 2048)]
+SHAPES = [(128, 256, 256), (128, 256, 128), (200, 300, 384), (1000, 520, 1024), (64, 64, 512), (512, 2048, 2048),
+          (1, 1032, 256), (3, 136, 128)]      # a single row; N = 4 x 256 + 8; a lone 128-element K stage
 
 
 @pytest.mark.parametrize("shape", SHAPES)
