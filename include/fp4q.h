@@ -359,10 +359,12 @@ fp4q_status fp4q_moe_dispatch_static(const int32_t* topk, int64_t tokens, int to
  * Output in the MMA layout with every group padded to whole 128-row tiles
  * (group g's tiles follow those of groups < g); the entries of the padding
  * rows are unspecified (the GEMM's rows there are not stored).
- *   scales     device ROWMAJOR E8M0 [rows, cols/32];  cols % 128 == 0
- *   offsets    device int64 [groups + 1] row offsets (rows beyond offsets[groups] ignored)
- *   ue4m3_mma  device out, fp4q_rebased_scales_bytes(rows, cols, groups) bytes
+ *   scales     device ROWMAJOR E8M0 [rows, cols/32], 4-byte aligned;  cols % 128 == 0
+ *   offsets    device int64 [groups + 1] row offsets, 8-byte aligned (rows beyond
+ *              offsets[groups] ignored)
+ *   ue4m3_mma  device out, fp4q_rebased_scales_bytes(rows, cols, groups) bytes, 16-byte aligned
  *   row_scale  device FP32 out [rows]
+ * A misaligned pointer returns FP4Q_ERR_MISALIGNED.
  */
 size_t fp4q_rebased_scales_bytes(int64_t rows, int64_t cols, int64_t groups);
 fp4q_status fp4q_mx_rebase_scales(const uint8_t* scales, int64_t rows, int64_t cols,

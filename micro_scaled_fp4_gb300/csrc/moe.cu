@@ -184,7 +184,8 @@ __global__ void __launch_bounds__(256) mx_rebase_kernel(const uint8_t* __restric
 // a 128-row tile's scales are one contiguous run of S16/4 chunks of 512 bytes,
 // so the CTA stages the tile's E8M0 rows in shared memory (rows padded by 4
 // bytes: the column reads of phase 2 then fall in 32 different banks), takes
-// each row's base, and writes every chunk as 16-byte stores -- thread (c4, i)
+// each row's base while staging it (a warp per row, 32-bit words, a byte-wise
+// max), and writes every chunk as 16-byte stores -- thread (c4, i)
 // the bytes of rows i, i + 32, i + 64, i + 96 for columns 4 c4 .. 4 c4 + 3 --
 // so a warp writes 512 contiguous bytes.  Padding rows are written as 0.
 __global__ void __launch_bounds__(256) mx_rebase_tiles_kernel(const uint8_t* __restrict__ s, int S32,
@@ -217,17 +218,19 @@ __global__ void __launch_bounds__(256) mx_rebase_tiles_kernel(const uint8_t* __r
         const int64_t r0 = off[lo] + (T - tpre[lo]) * 128;
         const int64_t left = off[lo + 1] - r0;
         const int nreal = left < 128 ? int(left) : 128;
-        // phase 1: the tile's rows, 4 bytes per load (rows past the group: 0)
+        // phase 1: warp w takes rows w, w + 8, ...; lane j loads the row's 32-bit
+        // words j, j + 32, ... (rows past the group: 0), stages them and keeps
+        // their byte maximum; a warp reduction gives the row's max E8M0 byte
         const int wpr = S32 / 4;
-        for (int w = threadIdx.x; w < 128 * wpr; w += blockDim.x) {
-            const int rr = w / wpr, cw = w - rr * wpr;
-            const uint32_t v = rr < nreal ? *reinterpret_cast<const uint32_t*>(s + (r0 + rr) * S32 + 4 * cw) : 0u;
-            *reinterpret_cast<uint32_t*>(stage + rr * RS + 4 * cw) = v;
-        }
-        __syncthreads();
         for (int rr = warp; rr < 128; rr += int(blockDim.x >> 5)) {
+            const uint8_t* src = s + (r0 + rr) * S32;
             uint32_t m = 0;
-            for (int j = lane; j < S32; j += 32) m = max(m, uint32_t(stage[rr * RS + j]));
+            for (int j = lane; j < wpr; j += 32) {
+                const uint32_t v = rr < nreal ? *reinterpret_cast<const uint32_t*>(src + 4 * j) : 0u;
+                *reinterpret_cast<uint32_t*>(stage + rr * RS + 4 * j) = v;
+                const uint32_t h = __vmaxu4(v, v >> 16);            // bytes 0 / 1: max of (0, 2) / (1, 3)
+                m = max(m, max(h & 0xffu, (h >> 8) & 0xffu));
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
             if (lane == 0) {
@@ -246,8 +249,9 @@ __global__ void __launch_bounds__(256) mx_rebase_tiles_kernel(const uint8_t* __r
                 const int rr = i + 32 * qq;
                 w[qq] = 0;
                 if (rr < nreal) {
-                    const int k0 = int(stage[rr * RS + 2 * c4]) - 127 - base[rr];
-                    const int k1 = int(stage[rr * RS + 2 * c4 + 1]) - 127 - base[rr];
+                    const uint32_t e2 = *reinterpret_cast<const uint16_t*>(stage + rr * RS + 2 * c4);
+                    const int k0 = int(e2 & 0xffu) - 127 - base[rr];
+                    const int k1 = int(e2 >> 8) - 127 - base[rr];
                     const uint32_t b0 = ue4m3_pow2(k0), b1 = ue4m3_pow2(k1);
                     bad += uint32_t(k0 < -9) + uint32_t(k1 < -9);
                     w[qq] = b0 | (b0 << 8) | (b1 << 16) | (b1 << 24);
@@ -329,8 +333,9 @@ extern "C" fp4q_status fp4q_mx_rebase_scales(const uint8_t* scales, int64_t rows
     if (!scales || !offsets || !ue4m3_mma || !row_scale)
         return fail(FP4Q_ERR_INVALID_ARGUMENT, "mx_rebase_scales: null pointer");
     if ((reinterpret_cast<uintptr_t>(offsets) & 7u) || (reinterpret_cast<uintptr_t>(ue4m3_mma) & 15u) ||
-        (reinterpret_cast<uintptr_t>(row_scale) & 3u) || (reinterpret_cast<uintptr_t>(violations) & 3u))
-        return fail(FP4Q_ERR_MISALIGNED, "mx_rebase_scales: offsets 8-byte, output 16-byte aligned");
+        (reinterpret_cast<uintptr_t>(scales) & 3u) || (reinterpret_cast<uintptr_t>(row_scale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(violations) & 3u))
+        return fail(FP4Q_ERR_MISALIGNED, "mx_rebase_scales: offsets 8-byte, output 16-byte, scales 4-byte aligned");
     int sms = 0;
     fp4q_status st = current_device(&sms);
     if (st != FP4Q_OK) return st;
