@@ -123,6 +123,9 @@ def test_argument_errors_need_no_gpu(lib):
         with pytest.raises(E) as e:
             lib.fp4q_block_scaled_gemm(*args, stream=0)
         assert e.value.status == status, (args, e.value)
+    with pytest.raises(E) as e:       # E8M0 scales not 4-byte aligned
+        lib.fp4q_mx_rebase_scales(x + 2, 4, 128, x, 1, x, x, None, stream=0)
+    assert e.value.status == 3
     with pytest.raises(E) as e:       # 2^43 output tiles of the grouped form
         lib.fp4q_grouped_gemm(x, x, x, x, x, x, x, 1 << 30, 4, 1 << 28, 128, 0, x, None, None, stream=0)
     assert e.value.status == 2
