@@ -50,6 +50,37 @@ def test_e2m1_rne_against_threshold_table_all_fp32_in_range(oracle):
         assert np.array_equal(oracle.e2m1_rne(v), _e2m1_threshold_rule(v))
 
 
+def test_e2m1_rne_every_finite_fp32(oracle):
+    # The rest of the 2^32 patterns: every finite FP32 below 2^-3 rounds to a
+    # signed zero and every one from 2^4 up saturates to a signed 6 (checked
+    # in 2^26-pattern chunks through the oracle's array form).
+    lo, hi, step = (127 - 3) << 23, (127 + 4) << 23, 1 << 26
+    for sign in (0, 1):
+        for a, b, want in ((0, lo, 0), (hi, 0x7f800000, 7)):
+            for c0 in range(a, b, step):
+                bits = np.arange(c0, min(b, c0 + step), dtype=np.uint32) | np.uint32(sign << 31)
+                codes = oracle.e2m1_rne(bits.view(np.float32))
+                assert np.all(codes == (want | (sign << 3))), (sign, hex(c0))
+
+
+def test_e2m1_threshold_rule_is_nearest_with_ties_to_even():
+    # The threshold table used above equals "the nearest E2M1 magnitude, ties to
+    # the even code" at every tie point, its FP32 neighbours and a dense grid.
+    grid = np.array(E2M1_SET)
+    mids = (grid[1:] + grid[:-1]) / 2
+    pts = [np.float32(m) for m in mids]
+    pts += [np.nextafter(np.float32(m), np.float32(0)) for m in mids]
+    pts += [np.nextafter(np.float32(m), np.float32(9)) for m in mids]
+    v = np.concatenate([np.array(pts, dtype=np.float32), np.linspace(0, 8, 100001, dtype=np.float32)])
+    d = np.abs(v.astype(np.float64)[:, None] - grid[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best                                       # one nearest code, or two at a tie
+    code = np.arange(8)[None, :]
+    even = cand & (code % 2 == 0)                          # the even code of a tie (mantissa bit 0)
+    want = np.where(cand.sum(axis=1) > 1, np.argmax(even, axis=1), np.argmax(cand, axis=1))
+    assert np.array_equal(_e2m1_threshold_rule(v), want.astype(np.uint8))
+
+
 def test_e2m1_rne_special_cases(oracle):
     v = np.array([0.0, -0.0, 6.0, -6.0, 1e30, -1e30, np.inf, -1e-40, 0.25, 0.2500001], dtype=np.float32)
     assert list(oracle.e2m1_rne(v)) == [0, 8, 7, 15, 7, 15, 7, 8, 0, 1]
