@@ -3,12 +3,15 @@
  *
  * C ABI.  Every pointer named "device" is GPU global memory owned by the
  * caller; the library allocates no device memory.  Every call is
- * asynchronous on `stream` (never synchronises) and validates its
+ * asynchronous on `stream` (never synchronises), except the status reads
+ * (fp4q_device_status, fp4q_stream_status), which say so, and validates its
  * arguments before launching: an argument error is returned immediately and
  * nothing is launched.  A launch failure returns FP4Q_ERR_CUDA.  Device-side
  * wait timeouts are recorded in a device status word read by
- * fp4q_device_status().  Inputs must be finite; non-finite inputs give
- * unspecified codes but never a fault.
+ * fp4q_device_status() or fp4q_stream_status().  Inputs must be finite;
+ * non-finite inputs give unspecified codes but never a fault.  Calls from
+ * several host threads are safe; calls that share buffers are ordered by the
+ * caller's streams.
  *
  * Conventions shared by all calls:
  *  - Tensors are row-major [rows, cols]; blocks run along the last
