@@ -23,11 +23,22 @@
 namespace fp4q {
 namespace {
 
+// (a0, a1), (b0, b1) -> (a0 + b0, a1 + b1), (a0 - b0, a1 - b1): two butterflies
+// in packed FP32 pairs (add / sub .rn.f32x2: each lane an IEEE round-to-nearest
+// operation, the same results as the scalar forms).
+__device__ __forceinline__ void butterfly_f32x2(float& a0, float& a1, float& b0, float& b1) {
+    asm("{\n .reg .b64 x, y, s, t;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n"
+        " add.rn.f32x2 s, x, y;\n sub.rn.f32x2 t, x, y;\n mov.b64 {%0, %1}, s;\n mov.b64 {%2, %3}, t;\n}"
+        : "+f"(a0), "+f"(a1), "+f"(b0), "+f"(b1));
+}
+
 // (1/4) H16 diag(d) x, d_j = -1 iff bit j of `signs` is set.  Butterflies with
-// strides 1, 2, 4, 8 map (a, b) -> (a + b, a - b) in FP32.  SKIP_ZERO: no sign
-// flips when `signs` is 0 (the deterministic H16; a branch uniform over the
-// grid).  The column kernels, which serve the Wgrad operands with the
-// deterministic H16, take it; the row kernels keep the unconditional flips.
+// strides 1, 2, 4, 8 map (a, b) -> (a + b, a - b) in FP32; strides 2, 4 and 8
+// pair elements (i, i + 1) with (i + h, i + h + 1) and run as packed pairs, and
+// so does the final x 1/4.  SKIP_ZERO: no sign flips when `signs` is 0 (the
+// deterministic H16; a branch uniform over the grid).  The column kernels,
+// which serve the Wgrad operands with the deterministic H16, take it; the row
+// kernels keep the unconditional flips.
 template <bool SKIP_ZERO = false>
 __device__ __forceinline__ void rht16(float (&t)[16], uint32_t signs) {
     if (!SKIP_ZERO || signs) {
@@ -35,16 +46,19 @@ __device__ __forceinline__ void rht16(float (&t)[16], uint32_t signs) {
         for (int j = 0; j < 16; ++j) t[j] = u2f(f2u(t[j]) ^ (((signs >> j) & 1u) << 31));
     }
 #pragma unroll
-    for (int h = 1; h < 16; h <<= 1)
+    for (int i = 0; i < 16; i += 2) {
+        const float a = t[i], b = t[i + 1];
+        t[i] = __fadd_rn(a, b);
+        t[i + 1] = __fsub_rn(a, b);
+    }
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (!(i & h)) {
-                const float a = t[i], b = t[i + h];
-                t[i] = __fadd_rn(a, b);
-                t[i + h] = __fsub_rn(a, b);
-            }
+    for (int h = 2; h < 16; h <<= 1)
 #pragma unroll
-    for (int j = 0; j < 16; ++j) t[j] = __fmul_rn(t[j], 0.25f);
+        for (int i = 0; i < 16; i += 2)
+            if (!(i & h)) butterfly_f32x2(t[i], t[i + 1], t[i + h], t[i + h + 1]);
+    const uint64_t quarter = f32x2_splat(0.25f);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) mul_f32x2(t[i], t[i + 1], quarter);
 }
 
 __device__ __forceinline__ uint32_t rht_signs(uint64_t seed) {
