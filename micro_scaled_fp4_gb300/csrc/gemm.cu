@@ -26,12 +26,6 @@
 //               B halves are the gate and up rows of the same 128 outputs;
 //               h = SiLU(gate) * up in FP32, then MXFP4 (one 32-element
 //               block per 32 accumulator columns) straight from registers.
-// Dense MXFP8 runs as clusters of two CTAs on m-tiles 2m and 2m + 1 of one B
-// tile: each CTA loads one 128-row half of B (and its scales) with a TMA
-// multicast into both CTAs, and each MMA thread's per-stage commit arrives on
-// the stage's "empty" barrier of both CTAs, so a stage is refilled only once
-// both have consumed it.  A pair member past the last m-tile still loads its
-// half of B, and stores nothing.
 // Every mbarrier wait is bounded in time; a wait that gives up sets a bit in
 // the library's status word and tells the other roles to stop.  The drain
 // waits that follow (TMA loads issued, MMAs issued) do not stop on that flag,
@@ -120,7 +114,6 @@ struct TileInfo {
     int b_row1;
     int group;
     int col0;         // first output column
-    bool phantom;     // pair member past the last m-tile: loads its B half for the peer, stores nothing
 };
 
 __device__ __forceinline__ void flag_abort(volatile int* abort, uint32_t* status, uint32_t bit) {
@@ -132,31 +125,10 @@ __device__ __forceinline__ void flag_abort(volatile int* abort, uint32_t* status
 
 // Output tile `tile` -> rows / columns / scale tiles.  Grouped tiles run
 // N-fastest, so the CTAs working at one time share A rows and one group's B.
-template <int EPI, int CL = 1>
-__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile, const int* tile_prefix, int m_tiles,
-                                                uint32_t crank = 0) {
+template <int EPI>
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile, const int* tile_prefix, int m_tiles) {
     TileInfo t;
-    t.phantom = false;
     int nt, mt;
-    if constexpr (CL == 2) {
-        // dense, two CTAs per unit: m-tiles 2 mp and 2 mp + 1 against one B tile,
-        // units banded over m-tile pairs like the single-CTA order
-        const int m_pairs = (m_tiles + 1) / 2, band_p = max(1, a.band_m / 2);
-        const int band = tile / (band_p * a.n_tiles);
-        const int within = tile - band * band_p * a.n_tiles;
-        const int bs = min(band_p, m_pairs - band * band_p);
-        nt = within / bs;
-        mt = 2 * (band * band_p + within % bs) + int(crank);
-        t.group = 0;
-        t.a_row0 = mt * BM;
-        t.row_end = a.M;
-        t.phantom = mt >= m_tiles;
-        t.a_sf_tile = t.phantom ? m_tiles - 1 : mt;     // a valid scale tile (its values are not used)
-        t.b_row0 = nt * BN;
-        t.b_row1 = (nt * BN + 128 < a.N) ? t.b_row0 + 128 : -1;
-        t.col0 = nt * BN;
-        return t;
-    }
     if (a.groups) {
         nt = tile % a.n_tiles;
         mt = tile / a.n_tiles;
@@ -215,37 +187,7 @@ __device__ __forceinline__ void stage_bf16x32(uint32_t staging, int row, int c, 
     }
 }
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// TMA tile load written to the same offset of every CTA in `mask`, each CTA's
-// mbarrier at `bar` (same offset) counting the bytes that land there.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask) : "memory");
-}
-__device__ __forceinline__ void bulk_load_mc(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                             uint16_t mask) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-                 " [%0], [%1], %2, [%3], %4;"
-                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "h"(mask) : "memory");
-}
-// Commit of this thread's tcgen05 work arriving on the mbarrier at `bar` in
-// every CTA of `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-                 :: "r"(bar), "h"(mask) : "memory");
-}
-
-template <int EPI, int STAGES, int CL>
+template <int EPI, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_d, const GemmArgs args) {
@@ -269,7 +211,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(full_bar(s), 1);
-            tc::mbar_init(empty_bar(s), CL);            // CL == 2: both CTAs' MMAs release a stage
+            tc::mbar_init(empty_bar(s), 1);
         }
         tc::mbar_init(tmem_full, 1);
         tc::mbar_init(tmem_empty, 8);       // one arrival per epilogue warp
@@ -295,14 +237,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t crank = CL == 2 ? cluster_ctarank() : 0u;
-    if constexpr (CL == 2) cluster_sync_all();          // both CTAs' barriers are initialised
 
     const int m_tiles = args.groups ? tile_prefix[args.groups] : (args.M + BM - 1) / BM;
-    // work units: output tiles, or (CL == 2) pairs of m-tiles sharing a B tile
-    const int num_tiles = CL == 2 ? ((m_tiles + 1) / 2) * args.n_tiles : m_tiles * args.n_tiles;
-    const int unit0 = CL == 2 ? int(blockIdx.x >> 1) : int(blockIdx.x);
-    const int unit_step = CL == 2 ? int(gridDim.x >> 1) : int(gridDim.x);
+    const int num_tiles = m_tiles * args.n_tiles;
+    const int unit0 = int(blockIdx.x);
+    const int unit_step = int(gridDim.x);
     const uint32_t chunk_elems = args.nv ? 64 : 128;  // K elements per 512-byte scale chunk
 
     if (warp == 0 && lane == 0) {
@@ -312,7 +251,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         int issued = 0;
         bool ok = true;
         for (int tile = unit0; tile < num_tiles && ok; tile += unit_step) {
-            const TileInfo t = decode_tile<EPI, CL>(args, tile, tile_prefix, m_tiles, crank);
+            const TileInfo t = decode_tile<EPI>(args, tile, tile_prefix, m_tiles);
             for (int kb = 0; kb < args.k_stages; ++kb) {
                 if (!tc::mbar_wait(empty_bar(stage), phase ^ 1, abort, kWaitLimitNs)) {
                     flag_abort(abort, args.status, args.status_bit);
@@ -331,18 +270,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 tc::bulk_load(tc::smem_u32(st + A_BYTES + B_BYTES),
                               args.sfa + uint64_t(t.a_sf_tile) * args.sf_tile_stride + ct0 * 512u, chunks * 512u, fb);
                 uint8_t* sfb_smem = st + A_BYTES + B_BYTES + SFA_BYTES;
-                if constexpr (CL == 2) {
-                    // this CTA loads B half `crank` (and its scales) into both CTAs of
-                    // the pair; the peer loads the other half.  An absent second half
-                    // still lands (rows past the end are zero-filled), without scales.
-                    const int brow = crank ? (t.b_row1 >= 0 ? t.b_row1 : t.b_row0 + 128) : t.b_row0;
-                    tma_load_2d_mc(tc::smem_u32(st + A_BYTES + crank * B_HALF_BYTES), &tmap_b, fb, kb * 128, brow,
-                                   uint16_t(0x3));
-                    if (crank == 0 || t.b_row1 >= 0)
-                        bulk_load_mc(tc::smem_u32(sfb_smem + crank * 4 * 512),
-                                     args.sfb + uint64_t(brow / 128) * args.sf_tile_stride + ct0 * 512u, chunks * 512u,
-                                     fb, uint16_t(0x3));
-                } else {
+                {
                     tc::tma_load_2d(tc::smem_u32(st + A_BYTES), &tmap_b, fb, kb * 128, t.b_row0);
                     // an absent second half still lands: rows past the end are zero-filled
                     tc::tma_load_2d(tc::smem_u32(st + A_BYTES + B_HALF_BYTES), &tmap_b, fb, kb * 128,
@@ -468,10 +396,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                                          tmem + TMEM_SFB + 8 * (j >> 1), acc);
                     }
                 }
-                if constexpr (CL == 2)
-                    tc_commit_mc(empty_bar(stage), uint16_t(0x3));   // the stage is free in both CTAs' eyes
-                else
-                    tc::tc_commit(empty_bar(stage));
+                tc::tc_commit(empty_bar(stage));
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
@@ -503,7 +428,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 break;
             }
             tc::fence_after_sync();
-            const TileInfo t = decode_tile<EPI, CL>(args, tile, tile_prefix, m_tiles, crank);
+            const TileInfo t = decode_tile<EPI>(args, tile, tile_prefix, m_tiles);
             const int row = t.a_row0 + q * 32 + lane;
             const bool row_ok = row < t.row_end;
             float alpha = dense_alpha;
@@ -593,7 +518,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         }
                     }
                 }
-            } else if (LY::staged_store && args.d_bf16 && !t.phantom &&
+            } else if (LY::staged_store && args.d_bf16 &&
                        t.a_row0 + BM <= t.row_end + (args.groups ? 0 : BM)) {
                 // BF16 through shared memory and TMA stores.  Each warp moves its 32 rows
                 // x 128 columns out of TMEM into registers, then the accumulator goes
@@ -682,7 +607,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     __syncwarp();          // the elected lanes rejoin their warps before the block barrier
     tc::fence_before_sync();
     __syncthreads();
-    if constexpr (CL == 2) cluster_sync_all();          // no copy or arrive from the peer is still on its way
     if (warp == 1) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, TMEM_COLS);
@@ -738,11 +662,11 @@ fp4q_status encode_output_map(CUtensorMap* map, void* D, int64_t rows, int64_t N
 }
 
 
-template <int EPI, int NST, int CL>
+template <int EPI, int NST>
 fp4q_status launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const GemmArgs& a,
                           int tiles_upper, int sms, cudaStream_t stream) {
     constexpr uint32_t smem = Layout<NST>::smem_bytes;
-    auto kernel = gemm_kernel<EPI, NST, CL>;
+    auto kernel = gemm_kernel<EPI, NST>;
     // per device, set on first use (setting it twice from racing threads is harmless)
     static std::atomic<bool> attr_set[64] = {};
     int dev = 0;
@@ -752,26 +676,6 @@ fp4q_status launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const CU
         if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
         attr_set[dev & 63].store(true, std::memory_order_release);
     }
-    if constexpr (CL == 2) {
-        const int m_tiles = (a.M + BM - 1) / BM;
-        const int units = ((m_tiles + 1) / 2) * a.n_tiles;
-        const int clusters = std::max(1, std::min(units, sms / 2));
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(unsigned(2 * clusters));
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ma, mb, md, a);
-        if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "block_scaled_gemm: %s", cudaGetErrorString(e));
-        return FP4Q_OK;
-    }
     const int grid = tiles_upper < sms ? tiles_upper : sms;
     kernel<<<grid, kThreads, smem, stream>>>(ma, mb, md, a);
     return check_launch("block_scaled_gemm");
@@ -780,16 +684,10 @@ fp4q_status launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const CU
 template <int EPI>
 fp4q_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const GemmArgs& a,
                    int tiles_upper, int sms, cudaStream_t stream) {
-    // Dense MXFP8 runs as CTA pairs sharing a B tile (each CTA multicasts half of
-    // it; 2788 -> 2853 TFLOP/s at 8192^3).  For FP4 operands the pairs measured
-    // level (MXFP4 +0.5 %, NVFP4 -1.7 %), so they stay single CTAs.
     if constexpr (EPI == kStore) {
-        if (a.f8) {
-            if (a.groups == 0) return launch_stages<EPI, 4, 2>(ma, mb, md, a, tiles_upper, sms, stream);
-            return launch_stages<EPI, 4, 1>(ma, mb, md, a, tiles_upper, sms, stream);
-        }
+        if (a.f8) return launch_stages<EPI, 4>(ma, mb, md, a, tiles_upper, sms, stream);
     }
-    return launch_stages<EPI, 3, 1>(ma, mb, md, a, tiles_upper, sms, stream);
+    return launch_stages<EPI, 3>(ma, mb, md, a, tiles_upper, sms, stream);
 }
 
 }  // namespace
