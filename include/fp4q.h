@@ -318,7 +318,8 @@ fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_operand* B,
  *   row_token   device int32 out [tokens * top_k]: token of each dispatched row
  *   q_out, scales_out  device out [tokens * top_k, cols/2], [tokens * top_k, cols/32]
  *   workspace   device, >= fp4q_moe_dispatch_workspace_bytes(), 16-byte aligned
- * Limits: 1 <= top_k <= 16, 1 <= n_experts <= 256.
+ * Limits: 1 <= top_k <= 16, 1 <= n_experts <= 256, tokens * top_k <= 2^31 - 1
+ * (else FP4Q_ERR_UNSUPPORTED_SHAPE; the workspace size is then 0).
  */
 size_t fp4q_moe_dispatch_workspace_bytes(int64_t tokens, int top_k, int n_experts);
 fp4q_status fp4q_moe_dispatch(const int32_t* topk, int64_t tokens, int top_k, int n_experts,

@@ -271,8 +271,12 @@ __global__ void __launch_bounds__(256) mx_rebase_tiles_kernel(const uint8_t* __r
 
 using namespace fp4q;
 
+// The dispatched rows (tokens x top_k) and the token ids are indexed in int32.
+static bool dispatch_too_large(int64_t tokens, int top_k) { return top_k > 0 && tokens > INT32_MAX / top_k; }
+
 extern "C" size_t fp4q_moe_dispatch_workspace_bytes(int64_t tokens, int top_k, int n_experts) {
-    if (tokens < 0 || top_k < 0 || n_experts < 0) return 0;
+    if (tokens < 0 || top_k < 1 || top_k > 16 || n_experts < 1 || n_experts > kMaxExperts) return 0;
+    if (dispatch_too_large(tokens, top_k)) return 0;
     const int64_t chunks = (tokens + kChunk - 1) / kChunk;
     return size_t(2 * chunks * n_experts + tokens * top_k) * 4u + 256u;
 }
@@ -284,6 +288,8 @@ extern "C" fp4q_status fp4q_moe_dispatch(const int32_t* topk, int64_t tokens, in
     if (tokens < 0 || top_k < 1 || top_k > 16 || n_experts < 1 || n_experts > kMaxExperts || cols < 0)
         return fail(FP4Q_ERR_INVALID_ARGUMENT, "moe_dispatch: need 1 <= top_k <= 16, 1 <= n_experts <= %d",
                     kMaxExperts);
+    if (dispatch_too_large(tokens, top_k))
+        return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "moe_dispatch: tokens x top_k above 2^31 - 1");
     if (cols % 32) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "moe_dispatch: cols %% 32 != 0");
     if (!offsets) return fail(FP4Q_ERR_INVALID_ARGUMENT, "moe_dispatch: offsets is NULL");
     if (tokens > 0 && (!topk || !q || !scales || !row_token || !q_out || !scales_out))
@@ -406,6 +412,8 @@ extern "C" fp4q_status fp4q_moe_dispatch_static(const int32_t* topk, int64_t tok
     if (tokens < 0 || top_k < 1 || top_k > 16 || n_experts < 1 || n_experts > kMaxExperts || cols < 0)
         return fail(FP4Q_ERR_INVALID_ARGUMENT, "moe_dispatch_static: need 1 <= top_k <= 16, 1 <= n_experts <= %d",
                     kMaxExperts);
+    if (dispatch_too_large(tokens, top_k))
+        return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "moe_dispatch_static: tokens x top_k above 2^31 - 1");
     const size_t need = fp4q_moe_dispatch_workspace_bytes(tokens, top_k, n_experts);
     if (need > size_t(FP4Q_MOE_DISPATCH_STATIC_SCRATCH_BYTES))
         return fail(FP4Q_ERR_UNSUPPORTED_SHAPE,

@@ -114,6 +114,16 @@ def test_argument_errors_need_no_gpu(lib):
     with pytest.raises(E) as e:       # scratch of the static-array dispatch would not fit
         lib.fp4q_moe_dispatch_static(x, 1 << 22, 8, 64, x, x, 64, x, x, x, x, stream=0)
     assert e.value.status == 2
+    # token counts whose dispatched rows (tokens x top_k) leave int32: rejected
+    # before any size arithmetic can wrap, and the workspace size says 0
+    for T, k in [(1 << 61, 8), ((2**31 - 1) // 8 + 1, 8), (1 << 31, 1)]:
+        assert lib.fp4q_moe_dispatch_workspace_bytes(T, k, 64) == 0
+        for fn in (lambda: lib.fp4q_moe_dispatch(x, T, k, 64, x, x, 64, x, x, x, x, x, 1 << 40, stream=0),
+                   lambda: lib.fp4q_moe_dispatch_static(x, T, k, 64, x, x, 64, x, x, x, x, stream=0)):
+            with pytest.raises(E) as e:
+                fn()
+            assert e.value.status == 2 and "2^31" in str(e.value), (T, k, e.value)
+    assert lib.fp4q_moe_dispatch_workspace_bytes((2**31 - 1) // 8, 8, 64) > 0
     A = lib.make_operand(x, x, lib.FP4Q_MXFP4)
     B = lib.make_operand(x, x, lib.FP4Q_NVFP4, x)
     for args, status in [((A, B, 128, 128, 128, x, 0, 128), 1), ((A, A, 128, 128, 96, x, 0, 128), 2),
