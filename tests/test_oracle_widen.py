@@ -106,6 +106,67 @@ def test_2d_scales_repeat_over_the_tile_rows(oracle):
     assert np.array_equal(s[:, 0, :], want)
 
 
+def _tile_reciprocals(oracle, x, s_t):
+    """1 / (E4M3(tile amax / (6 s_t)) * s_t) per 16x16 tile, in FP32, repeated
+    over the tile's elements (the 2D scale rule restated here)."""
+    R, C = x.shape
+    ab = np.abs(x).reshape(R // 16, 16, C // 16, 16).max(axis=(1, 3)).astype(np.float32)
+    sb = oracle.e4m3_values()[oracle.e4m3_rn_satfinite((ab / (np.float32(6.0) * s_t)).astype(np.float32))]
+    sf = (sb.astype(np.float32) * s_t).astype(np.float32)
+    rcp = (np.float32(1.0) / sf).astype(np.float32)
+    return np.repeat(np.repeat(rcp, 16, axis=0), 16, axis=1)
+
+
+def test_2d_sr_takes_the_word_of_each_elements_linear_index(oracle):
+    """SR in the 2D form: element (r, c) of an R x C weight is rounded with word
+    r * C + c of the Philox stream (the index is the element's, not its tile's
+    or the transpose's), over the same scales as the RNE pass.  The shape is not
+    square and spans several tiles in both directions, so a tile-wise or
+    transposed index, or scales that depend on the rounding, fail."""
+    from _helpers import unpack
+    rng = np.random.default_rng(18)
+    R, C = 48, 80
+    w = (rng.standard_normal((R, C)) * 0.02).astype(np.float32)
+    w[7, :] *= 25.0
+    wb = _bf16(w)
+    sr = oracle.nv_quantize_2d(wb, rounding="sr", sr_seed=1234)
+    rne = oracle.nv_quantize_2d(wb)
+    assert np.array_equal(sr["s"], rne["s"]) and sr["s_t"] == rne["s_t"]
+    x = oracle.bf16_bits_to_f32(wb)
+    s_t = (np.float32(np.abs(x).max()) / np.float32(2688.0)).astype(np.float32)
+    assert s_t == sr["s_t"]
+    v = (x * _tile_reciprocals(oracle, x, s_t)).astype(np.float32)
+    words = oracle.sr_words(1234, 0, R * C)
+    assert np.array_equal(unpack(sr["q"]), oracle.e2m1_sr(v, words.reshape(R, C)))
+    # the plausible wrong indexings give other codes on this input
+    assert not np.array_equal(unpack(sr["q"]), oracle.e2m1_sr(v, words.reshape(C, R).T))
+    tile_major = words.reshape(R // 16, C // 16, 16, 16).transpose(0, 2, 1, 3).reshape(R, C)
+    assert not np.array_equal(unpack(sr["q"]), oracle.e2m1_sr(v, tile_major))
+    # a different seed draws a different stream
+    assert not np.array_equal(sr["q"], oracle.nv_quantize_2d(wb, rounding="sr", sr_seed=1235)["q"])
+
+
+def test_2d_sr_is_unbiased_in_the_mean(oracle):
+    """Averaged over many seeds, the 2D SR result dequantizes to the input
+    (scales are fixed by the tile amax): per element within 6 sigma, sigma of
+    one draw being at most half a grid step times the scale (<= the scale)."""
+    rng = np.random.default_rng(19)
+    R, C = 32, 48
+    wb = _bf16((rng.standard_normal((R, C)) * 0.05).astype(np.float32))
+    n = 400
+    acc = np.zeros((R, C))
+    for k in range(n):
+        r = oracle.nv_quantize_2d(wb, rounding="sr", sr_seed=2000 + k)
+        acc += oracle.nv_dequantize_f64(r["q"], r["s"], r["s_t"])
+    x = oracle.bf16_bits_to_f32(wb).astype(np.float64)
+    r0 = oracle.nv_quantize_2d(wb)
+    sf = np.repeat(oracle.e4m3_values()[r0["s"]] * float(r0["s_t"]), 16, axis=1)
+    err = np.abs(acc / n - x)
+    assert np.all(err <= 6 * sf / np.sqrt(n) + 1e-12)
+    # and RNE is biased somewhere on the same input (the test can tell the two apart)
+    assert np.abs(oracle.nv_dequantize_f64(r0["q"], r0["s"], r0["s_t"]) - x).max() > 6 * sf.max() / np.sqrt(n)
+
+
 # ---------------------------------------------------------------------------
 # FP4RowToFP8Col
 # ---------------------------------------------------------------------------
