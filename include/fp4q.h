@@ -151,8 +151,9 @@ fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, int64_t row
  * three slots of `workspace`: host -> device copies, the two conversion
  * kernels (on `stream`) and device -> host copies of different chunks overlap
  * on two internal copy streams (one pair per host thread and device, created
- * on first use).  The call starts after the work already queued on `stream`
- * and returns once everything is queued; the host outputs are complete when
+ * on first use, destroyed by fp4q_fp8_pipeline_host_release).  The call
+ * starts after the work already queued on `stream` and returns once
+ * everything is queued; the host outputs are complete when
  * `stream` reaches the point of the call (e.g. after cudaStreamSynchronize).
  * Host buffers should be page-locked for the copies to overlap; pageable
  * memory gives the same results without the overlap.
@@ -172,6 +173,17 @@ fp4q_status fp4q_fp8_pipeline_host(const uint8_t* x, const float* tile_scale, in
                                    int64_t cols, uint8_t* q, uint8_t* scales, uint8_t* y,
                                    float* y_tile_scale, int64_t chunk_rows, void* workspace,
                                    size_t workspace_bytes, fp4q_stream_t stream);
+
+/*
+ * fp4q_fp8_pipeline_host_release -- destroys the two copy streams and the
+ * events fp4q_fp8_pipeline_host created for the calling host thread on the
+ * current device (otherwise they live until the process exits).  The pages
+ * have no counterpart: this is library housekeeping.  Waits for those two
+ * copy streams first, so no copy of an earlier call is cut short; a later
+ * fp4q_fp8_pipeline_host call on this thread creates them again.  Nothing to
+ * release returns FP4Q_OK.  Synchronous on the host.
+ */
+fp4q_status fp4q_fp8_pipeline_host_release(void);
 
 /*
  * fp4q_nv_quantize -- BF16 -> NVFP4 (optional 16-point RHT, RNE or SR).

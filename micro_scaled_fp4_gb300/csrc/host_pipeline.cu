@@ -55,7 +55,8 @@ int64_t chunk_for(int64_t rows, int64_t chunk_rows) {
 }
 
 // The copy streams and the ring's events, one set per host thread and device
-// (created on first use, kept until the process exits).
+// (created on first use, kept until fp4q_fp8_pipeline_host_release or the end
+// of the process).
 struct Engine {
     bool ready = false;
     cudaStream_t in = nullptr, out = nullptr;
@@ -186,4 +187,26 @@ extern "C" fp4q_status fp4q_fp8_pipeline_host(const uint8_t* x, const float* til
     if (st == FP4Q_OK && j != cudaSuccess)
         st = fail(FP4Q_ERR_CUDA, "fp8_pipeline_host: stream ordering: %s", cudaGetErrorString(j));
     return st;
+}
+
+extern "C" fp4q_status fp4q_fp8_pipeline_host_release(void) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return fail(FP4Q_ERR_CUDA, "fp8_pipeline_host_release: no current device");
+    Engine& g = t_engines[dev];
+    if (!g.ready) return FP4Q_OK;
+    // no copy of an earlier call may still be running on the streams
+    if ((e = cudaStreamSynchronize(g.in)) != cudaSuccess || (e = cudaStreamSynchronize(g.out)) != cudaSuccess)
+        return fail(FP4Q_ERR_CUDA, "fp8_pipeline_host_release: %s", cudaGetErrorString(e));
+    cudaStreamDestroy(g.in);
+    cudaStreamDestroy(g.out);
+    for (cudaEvent_t ev : {g.start, g.in_done, g.out_done}) cudaEventDestroy(ev);
+    for (int k = 0; k < kSlots; ++k) {
+        cudaEventDestroy(g.loaded[k]);
+        cudaEventDestroy(g.converted[k]);
+        cudaEventDestroy(g.stored[k]);
+    }
+    g = Engine();
+    return FP4Q_OK;
 }

@@ -34,7 +34,7 @@ EXPORTED = [
     "fp4q_moe_dispatch", "fp4q_rebased_scales_bytes", "fp4q_mx_rebase_scales", "fp4q_grouped_gemm",
     "fp4q_moe_dispatch_static", "fp4q_check_wait_timeout", "fp4q_nv_quantize_2d", "fp4q_fp4_row_to_fp8_col",
     "fp4q_fp8_tile_scales_to_e8m0", "fp4q_fp8_pipeline_host_workspace_bytes", "fp4q_fp8_pipeline_host",
-    "fp4q_stream_status",
+    "fp4q_stream_status", "fp4q_fp8_pipeline_host_release",
 ]
 MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 * 1024 * 1024
 
@@ -100,6 +100,7 @@ def load() -> ctypes.CDLL:
                 "fp4q_fp4_row_to_fp8_col": [vp, vp, i64, i64, vp, vp, vp],
                 "fp4q_fp8_tile_scales_to_e8m0": [vp, i64, i64, vp, ci, vp],
                 "fp4q_fp8_pipeline_host": [vp, vp, i64, i64, vp, vp, vp, vp, i64, vp, ctypes.c_size_t, vp],
+                "fp4q_fp8_pipeline_host_release": [],
                 "fp4q_grouped_gemm": [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ci, vp, vp, vp, vp],
             }
             for name, args in sigs.items():
@@ -176,6 +177,10 @@ def fp4q_fp8_pipeline_host(x, tile_scale, rows, cols, q, scales, y, y_tile_scale
     return _check("fp4q_fp8_pipeline_host", load().fp4q_fp8_pipeline_host(
         _ptr(x), _ptr(tile_scale), rows, cols, _ptr(q), _ptr(scales), _ptr(y), _ptr(y_tile_scale), chunk_rows,
         _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def fp4q_fp8_pipeline_host_release():
+    return _check("fp4q_fp8_pipeline_host_release", load().fp4q_fp8_pipeline_host_release())
 
 
 def fp8_pipeline_host(x, tile_scale, chunk_rows=0, pinned=True, stream=None):
