@@ -15,6 +15,14 @@ under "rows": MXFP4 round trip of BF16 256x4096; NVFP4 (RHT + SR, then RNE)
 of a BF16 8192x14336 gradient; block-scaled FP4 GEMM 8192^3 (MXFP4, and NVFP4
 with RHT operands).
 
+The roofline object is for the dominant kernel of the step, timed alone:
+N back-to-back launches of that kernel over the rotating input sets between
+two CUDA events on its stream.  Every other row flushes L2 before each timed
+call by READING a buffer twice the L2 size, so the timed kernel finds no dirty
+lines to write back.  CPU baselines (the oracle as it stands, on a bounded
+sample) are timed for every config on one core and on all host cores, each in
+a subprocess whose thread count is fixed by its environment.
+
 --impl reference times the CPU oracle (the only reference this method has)
 on a bounded sample of the same workload and prints the same kind of line.
 Multi-GPU (torchrun): every rank runs its own copy of the workload (weak
@@ -154,31 +162,133 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # reference arm: the CPU oracle
 # ---------------------------------------------------------------------------
-_SAMPLES = {}
+def _timed_loop(fn, seconds: float, max_passes: int = 1000):
+    """Runs fn until `seconds` have passed (at least once); seconds per pass, passes."""
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        if time.perf_counter() - t0 >= seconds or n >= max_passes:
+            break
+    return (time.perf_counter() - t0) / n, n
 
 
-def cpu_oracle_rate(sample_rows: int, min_seconds: float = 0.0, max_passes: int = 50):
-    """Oracle a3 + a4 on `sample_rows` rows of the workload, repeated until
-    `min_seconds` have passed (at least once); returns (GB/s, seconds per pass,
-    cores, passes)."""
+CPU_LEGS = ("c1", "c2", "c3", "c4", "c5")
+
+
+def cpu_leg(cfg: str, seconds: float, c2_rows: int = 256) -> dict:
+    """The oracle as it stands on a bounded sample of one config, repeated for
+    about `seconds`; the thread count is whatever this process's environment
+    sets (OMP_NUM_THREADS for the C oracle's OpenMP loops, the BLAS variables
+    for NumPy's float64 matmul).  Returns value / unit / sample."""
     import oracle
     from micro_scaled_fp4_gb300 import workloads as W
     oracle.build()
-    if sample_rows not in _SAMPLES:
-        _SAMPLES[sample_rows] = W.fp8_activation(sample_rows, COLS, seed=1, outlier_seed=2)
-    e4, ts = _SAMPLES[sample_rows]
-    passes = 0
-    t0 = time.perf_counter()
-    while True:
-        q, s = oracle.fp8_to_mx(e4, ts)
-        oracle.mx_to_fp8(q, s)
-        passes += 1
-        if time.perf_counter() - t0 >= min_seconds or passes >= max_passes:
-            break
-    dt = (time.perf_counter() - t0) / passes
-    nbytes = bytes_fp8_to_mx(sample_rows, COLS) + bytes_mx_to_fp8(sample_rows, COLS)
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return nbytes / dt / 1e9, dt, cores, passes
+    if cfg == "c1":
+        x = W.activation_bf16()
+
+        def f():
+            q, s = oracle.mx_quantize(x)
+            oracle.mx_dequantize(q, s)
+        dt, n = _timed_loop(f, seconds)
+        nb = 2 * 256 * 4096 * (2 + 0.5 + 1 / 32)
+        return {"value": nb / dt / 1e9, "unit": "GB/s",
+                "sample": f"the whole 256x4096 round trip (quantize + dequantize), {n} passes"}
+    if cfg == "c2":
+        e4, ts = W.fp8_activation(c2_rows, COLS, seed=1, outlier_seed=2)
+
+        def f():
+            q, s = oracle.fp8_to_mx(e4, ts)
+            oracle.mx_to_fp8(q, s)
+        dt, n = _timed_loop(f, seconds)
+        nb = bytes_fp8_to_mx(c2_rows, COLS) + bytes_mx_to_fp8(c2_rows, COLS)
+        return {"value": nb / dt / 1e9, "unit": "GB/s",
+                "sample": f"{c2_rows} of {ROWS} rows (a3 + a4), {n} passes"}
+    if cfg == "c3":
+        r, c = 64, 14336
+        x = W.gradient_bf16(r, c)
+
+        def f():
+            am = oracle.nv_amax(x, 1, 7)
+            oracle.nv_quantize(x, rht=1, rht_seed=7, rounding="sr", sr_seed=1234, amax=am)
+            oracle.nv_quantize(x, rht=1, rht_seed=7, amax=am)
+        dt, n = _timed_loop(f, seconds)
+        nb = r * c * (2 + 2 * (2 + 0.5 + 1 / 16))
+        return {"value": nb / dt / 1e9, "unit": "GB/s",
+                "sample": f"{r} of 8192 rows x {c} (amax pass + SR pass + RNE pass, RHT), {n} passes"}
+    if cfg == "c4":
+        m = 256
+        a, b = W.gemm_operands(m=m)
+        qa, sa = oracle.mx_quantize(a)
+        qb, sb = oracle.mx_quantize(b)
+        dt, n = _timed_loop(lambda: oracle.mx_gemm_ref(qa, sa, qb, sb), seconds)
+        return {"value": 2.0 * m * 8192 * 8192 / dt / 1e12, "unit": "TFLOPS",
+                "sample": f"{m} of 8192 rows of A x all of B (MXFP4, dequantize + float64 matmul), {n} passes"}
+    if cfg == "c5":
+        import torch
+        T, H, I, E, k, rows = 4096, 7168, 2048, 64, 8, 256
+        x = W.moe_activations(T, H, seed=8)
+        topk = W.moe_routing(tokens=T, experts=E, top_k=k, seed=9)
+        w1 = W.moe_weights_torch(1, 2 * I, H, 10, "cpu")[0].view(torch.int16).numpy().view(np.uint16)
+        w2 = W.moe_weights_torch(1, H, I, 11, "cpu")[0].view(torch.int16).numpy().view(np.uint16)
+        r1, r2 = oracle.nv_quantize(w1), oracle.nv_quantize(w2)       # offline, not timed
+        w1d = oracle.nv_dequantize_f64(r1["q"], r1["s"], r1["s_t"])
+        w2d = oracle.nv_dequantize_f64(r2["q"], r2["s"], r2["s_t"])
+
+        def f():
+            qx, sx = oracle.mx_quantize(x)
+            order, offs = oracle.moe_dispatch(topk, E)
+            tok = order[offs[0]:offs[0] + rows]
+            h = oracle.moe_up_gate(oracle.mx_dequantize_f64(qx[tok], sx[tok]), w1d, I)
+            qh, sh = oracle.mx_quantize(h.astype(np.float32))
+            oracle.gemm_ref(oracle.mx_dequantize_f64(qh, sh), w2d)
+        dt, n = _timed_loop(f, seconds)
+        flops = 2.0 * rows * H * 2 * I + 2.0 * rows * I * H
+        return {"value": flops / dt / 1e12, "unit": "TFLOPS",
+                "sample": f"{T} tokens quantized and routed, {rows} dispatched rows of expert 0 through "
+                          f"up-proj + SiLU gate + MXFP4 of h + down-proj (float64), {n} passes"}
+    raise ValueError(cfg)
+
+
+def host_cores() -> int:
+    return os.cpu_count() or 1
+
+
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+    except (OSError, subprocess.SubprocessError):
+        return "unknown"
+    for line in out.splitlines():
+        if line.startswith("Model name:"):
+            return line.split(":", 1)[1].strip()
+    return "unknown"
+
+
+def cpu_baseline(cfg: str, threads: int, seconds: float) -> dict:
+    """cpu_leg in a fresh Python process whose OpenMP and BLAS thread counts are
+    `threads` (set before the process starts, so they hold for the libraries
+    it loads); the result as a cpu_baseline object."""
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[v] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-leg", cfg, "--cpu-seconds", str(seconds)]
+    try:
+        res = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        out = json.loads(res.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"value": None, "cores": threads, "kind": "oracle", "error": str(e)[:160]}
+    return {"value": round(out["value"], 4), "unit": out["unit"], "cores": threads, "kind": "oracle",
+            "sample": out["sample"]}
+
+
+def cpu_baselines(cfg: str, seconds: float) -> dict:
+    """The oracle on all host cores (the object's own value) and on one core."""
+    allc = cpu_baseline(cfg, host_cores(), seconds)
+    allc["one_core"] = cpu_baseline(cfg, 1, seconds)
+    return allc
 
 
 def max_over_ranks(x: float, dist, device) -> float:
@@ -197,23 +307,31 @@ def whole_job_gbs(nbytes_per_rank_step: int, ms_step: float, world: int) -> floa
     return world * nbytes_per_rank_step / ms_step / 1e6
 
 
+def step_config(world: int) -> dict:
+    """The workload of the step, shared by both arms."""
+    nbytes = bytes_fp8_to_mx(ROWS, COLS) + bytes_mx_to_fp8(ROWS, COLS)
+    return {"workload": WORKLOAD, "rows": ROWS, "cols": COLS, "parallelism": f"replicas{world}",
+            "l2": f"{NSETS} rotating input sets ({NSETS * (nbytes // 2**20)} MB > L2)"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
     sample = 256
     for _ in range(args.warmup):
-        cpu_oracle_rate(sample)
+        cpu_leg("c2", 0.0, sample)
     vals, t_total = [], 0.0
     for _ in range(args.steps):
-        v, dt, cores, _ = cpu_oracle_rate(sample)
-        vals.append(v)
-        t_total += dt
+        t0 = time.perf_counter()
+        vals.append(cpu_leg("c2", 0.0, sample)["value"])
+        t_total += time.perf_counter() - t0
     value = statistics.mean(vals)
+    cores = int(os.environ.get("OMP_NUM_THREADS", host_cores()))
     desc = f"{sample} of {ROWS} rows of the workload per step (a3 + a4, scalar C oracle, OpenMP)"
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_total / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample_rows": sample},
+            "config": step_config(world),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -228,7 +346,6 @@ def _events(torch, n):
 
 
 ROW_NAMES = ("c1", "c3", "gemm", "moe", "col", "nv2d", "fp8")
-EVENT_EVERY = 10          # timed steps per per-kernel event sample
 
 
 def main_rows(fq, W, torch, peaks, which=ROW_NAMES, moe_tokens=65536):
@@ -240,14 +357,17 @@ def main_rows(fq, W, torch, peaks, which=ROW_NAMES, moe_tokens=65536):
     outputs)."""
     rows = {}
     stream = torch.cuda.current_stream()
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
+    # L2 flush by reading a buffer twice the L2 size: the lines it leaves are
+    # clean, so the timed kernel writes back nothing that is not its own
+    flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
+    flush_out = torch.empty((), dtype=torch.int32, device="cuda")
     lib = fq.load()
 
     def timed(fn, iters, do_flush):
         ts = []
         for i in range(iters + 3):
             if do_flush:
-                flush.zero_()
+                torch.amax(flush, dim=0, out=flush_out)
             e0, e1 = _events(torch, 2)
             e0.record(stream)
             fn()
@@ -611,16 +731,17 @@ def run_gpu(args, rank, world):
         yt = torch.empty((ROWS, COLS // 128), dtype=torch.float32, device="cuda")
         sets.append((x, t, q, s, y, yt))
 
-    def step(i, ev=None):
+    def a3(i):
         x, t, q, s, y, yt = sets[i % NSETS]
-        if ev:
-            ev[0].record(stream)
         fq.fp4q_mx_quantize(x, fq.FP4Q_E4M3, t, ROWS, COLS, COLS, 1, q, s, fq.FP4Q_SCALES_ROWMAJOR, stream)
-        if ev:
-            ev[1].record(stream)
+
+    def a4(i):
+        x, t, q, s, y, yt = sets[i % NSETS]
         fq.fp4q_fp4_to_fp8(q, s, ROWS, COLS, 1, y, yt, stream)
-        if ev:
-            ev[2].record(stream)
+
+    def step(i):
+        a3(i)
+        a4(i)
 
     for i in range(args.warmup):
         step(i)
@@ -628,11 +749,6 @@ def run_gpu(args, rank, world):
 
     clocks = ClockSampler(local)
     clocks.start()
-    # Per-kernel CUDA events on every EVENT_EVERY-th step of the timed loop: an
-    # event record between two kernels makes the stream wait for the first to
-    # drain (about 5.7 us per step with events around both kernels), so they
-    # sample the loop instead of bracketing every launch.
-    evs = [_events(torch, 3) if i % EVENT_EVERY == 0 else None for i in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -641,19 +757,34 @@ def run_gpu(args, rank, world):
     wall0 = time.perf_counter()
     t_start.record(stream)
     for i in range(args.steps):
-        step(i, evs[i])
+        step(i)
     t_end.record(stream)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     wall = time.perf_counter() - wall0
     ms_total = t_start.elapsed_time(t_end)
-    a3_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs if e)
-    a4_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs if e)
     ms_total = max_over_ranks(ms_total, dist, "cuda")
     ms_step = ms_total / args.steps
     nbytes = bytes_fp8_to_mx(ROWS, COLS) + bytes_mx_to_fp8(ROWS, COLS)
     value = whole_job_gbs(nbytes, ms_step, world)
+
+    # ---- each kernel alone: n back-to-back launches over the rotating sets,
+    # CUDA events on the launching stream around the whole run ----
+    def alone(launch, n):
+        for i in range(3):
+            launch(i)
+        e0, e1 = _events(torch, 2)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n):
+            launch(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+    n_alone = max(100, min(args.steps, 2000))
+    a3_ms = alone(a3, n_alone)
+    a4_ms = alone(a4, n_alone)
 
     # ---- e2e through the C ABI with pinned host buffers ----
     hx = torch.from_numpy(e4).pin_memory()
@@ -696,9 +827,15 @@ def run_gpu(args, rank, world):
     dom = ("fp8_to_mx", a3_ms, bytes_fp8_to_mx(ROWS, COLS), "mx_quant.cu") if a3_ms >= a4_ms else \
           ("mx_to_fp8", a4_ms, bytes_mx_to_fp8(ROWS, COLS), "fp4_to_fp8.cu")
     achieved = dom[2] / dom[1] / 1e6
+    if dom[1] > ms_step:
+        print(f"bench: the dominant kernel alone ({dom[1]:.5f} ms) is slower than the whole step "
+              f"({ms_step:.5f} ms)", file=sys.stderr)
     roof = {"kernel": dom[0], "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 3), "traffic": _traffic(dom[0]),
             "algorithmic_bytes_per_launch": dom[2], "ms_per_launch": round(dom[1], 5),
+            "timing": f"{n_alone} back-to-back launches of the kernel alone over the {NSETS} rotating input sets, "
+                      "CUDA events on its stream around the whole run",
+            "kernel_ms_within_step": bool(dom[1] <= ms_step),
             "peak_source": peaks["source"],
             "kernels": {"fp8_to_mx": {"ms": round(a3_ms, 5), "GB_per_s": round(bytes_fp8_to_mx(ROWS, COLS) / a3_ms / 1e6, 1)},
                         "mx_to_fp8": {"ms": round(a4_ms, 5), "GB_per_s": round(bytes_mx_to_fp8(ROWS, COLS) / a4_ms / 1e6, 1)}}}
@@ -710,10 +847,12 @@ def run_gpu(args, rank, world):
         torch.cuda.empty_cache()
         rows = main_rows(fq, W, torch, peaks, args.rows.split(","), args.moe_tokens)
     if rank == 0 and not args.no_cpu:
-        v, dt, cores, passes = cpu_oracle_rate(ROWS, min_seconds=10.0)
-        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": f"{passes} passes over all {ROWS} rows of the workload (a3 + a4), "
-                         f"{dt * passes:.1f} s in total"}
+        cpu = cpu_baselines("c2", args.cpu_seconds)
+        if rows is not None:
+            for key, cfg in (("mx_roundtrip_bf16_256x4096", "c1"), ("nvfp4_rht_8192x14336", "c3"),
+                             ("gemm_fp4_8192^3", "c4"), (f"moe_ffn_{args.moe_tokens}x7168_top8_of_64", "c5")):
+                if key in rows:
+                    rows[key]["cpu_baseline"] = cpu_baselines(cfg, args.cpu_seconds)
     if dist:
         dist.destroy_process_group()
     if rank != 0:
@@ -721,10 +860,9 @@ def run_gpu(args, rank, world):
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "rows": ROWS, "cols": COLS, "parallelism": f"replicas{world}",
-                       "l2": f"{NSETS} rotating input sets ({NSETS * (nbytes // 2**20)} MB > L2)",
-                       "kernel_events": f"per-kernel CUDA events on every {EVENT_EVERY}th timed step",
-                       "frac_hbm": round(value / world / peaks["hbm_gbs"], 3)},
+            "config": step_config(world),
+            "frac_hbm": round(value / world / peaks["hbm_gbs"], 3),
+            "host": {"nproc": host_cores(), "cpu": _cpu_model()},
             "wall_s_timed_region": round(wall, 4),
             "e2e": {"value": round(whole_job_gbs(nbytes, e2e_ms, world), 1), "unit": "GB/s",
                     "h2d_bytes_per_step": int(h2d),
@@ -746,7 +884,12 @@ def main():
                     help="comma-separated rows to report besides the step: " + ", ".join(ROW_NAMES))
     ap.add_argument("--moe-tokens", type=int, default=65536, help="tokens of the MoE row")
     ap.add_argument("--e2e-chunk", type=int, default=2048, help="rows per chunk of the host-buffer (e2e) call")
+    ap.add_argument("--cpu-seconds", type=float, default=4.0, help="seconds of oracle work per CPU baseline leg")
+    ap.add_argument("--cpu-leg", choices=CPU_LEGS, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_leg:
+        print(json.dumps(cpu_leg(args.cpu_leg, args.cpu_seconds)), flush=True)
+        return
     bad = [r for r in args.rows.split(",") if r not in ROW_NAMES]
     if bad:
         ap.error(f"unknown rows {bad}")
