@@ -15,9 +15,16 @@
 //   warp 0      TMA producer: A and B tiles (128-byte swizzle; B as two
 //               128-row halves) and the stage's block scales (contiguous
 //               chunks of the MMA scale layout) into a 3-stage ring.
-//   warp 1      allocates TMEM; one thread issues tcgen05.cp (scales ->
-//               TMEM) and tcgen05.mma kind::mxf4 (UE8M0 per 32) or
-//               kind::mxf4nvf4 (UE4M3 per 16), FP32 accumulator in TMEM.
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma kind::mxf4
+//               (UE8M0 per 32) or kind::mxf4nvf4 (UE4M3 per 16), FP32
+//               accumulator in TMEM, reading the stage's block scales from
+//               that stage's own TMEM scale buffer.
+//   warp 10     one thread copies each landed stage's block scales into the
+//               stage's TMEM scale buffer (tcgen05.cp) and releases the stage
+//               to the MMA thread.  Issued from the MMA thread, the copies
+//               held back the MMAs (a stage of MXFP4 took ~830 cycles of issue
+//               for ~530 of MMA); from their own thread, into buffers no MMA
+//               in flight reads, they overlap with the MMAs.
 //   warps 2..9  epilogue: tcgen05.ld of the 128 x 256 FP32 accumulator,
 //               one row and half the columns per thread (two warps per TMEM
 //               lane quadrant); the accumulator goes back to the MMA thread
@@ -26,6 +33,19 @@
 //               B halves are the gate and up rows of the same 128 outputs;
 //               h = SiLU(gate) * up in FP32, then MXFP4 (one 32-element
 //               block per 32 accumulator columns) straight from registers.
+// Paired form (a cluster of two CTAs on two SMs, every tcgen05 instruction
+// with .cta_group::2): the pair computes a 256 x 256 output tile with one MMA
+// of M = 256 issued by the even CTA.  Each CTA loads its own 128 rows of A,
+// its own 128-row half of the B tile and the block scales both of them need
+// (its A rows, both B halves) into its own shared memory; its TMA loads count
+// their bytes on the even CTA's "full" barrier, so the even CTA's MMA thread
+// issues a stage once both CTAs have it, and its scale copies
+// (tcgen05.cp .cta_group::2) fill each CTA's TMEM from that CTA's shared
+// memory.  The even CTA's commits arrive on the "empty" and
+// "accumulator full" barriers of both CTAs; each CTA's epilogue reads its own
+// 128 TMEM lanes (its 128 output rows x 256 columns) and arrives, across the
+// pair, on the even CTA's "accumulator empty" barrier.  Per SM this halves the
+// B bytes a stage brings in and the MMA instructions per flop.
 // Every mbarrier wait is bounded in time; a wait that gives up sets a bit in
 // the library's status word and tells the other roles to stop.  The drain
 // waits that follow (TMA loads issued, MMAs issued) do not stop on that flag,
@@ -55,25 +75,35 @@ constexpr uint32_t B_BYTES = 2 * B_HALF_BYTES;
 constexpr uint32_t SFA_BYTES = 4 * 512;               // up to 4 chunks (NVFP4)
 constexpr uint32_t SFB_BYTES = 2 * 4 * 512;           // 2 halves x 4 chunks
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;   // 55296
+constexpr uint32_t PAIR_STAGE_BYTES = A_BYTES + B_HALF_BYTES + SFA_BYTES + SFB_BYTES;   // 38912
 // BF16 output staging: two 64-column x 128-row boxes, rows of 128 bytes with the
 // TMA 128-byte swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)).
 constexpr uint32_t BOX_BYTES = 128 * 128;             // 64 BF16 columns x 128 rows
-template <int NST>
+// TMEM: FP32 accumulator in columns 0-255, then one block-scale buffer per
+// ring stage (A: 4 chunks x 4 columns, B: 2 halves x 4 chunks x 4 columns).
+constexpr uint32_t TMEM_SF = 256;
+constexpr uint32_t SF_COLS = 48;
+// Per-CTA shared memory: NST ring stages [A | B (the pair: one half) | A
+// scales | B scales], the BF16 staging boxes, barriers, the group prefix sums.
+template <int NST, bool PAIR>
 struct Layout {
-    static constexpr bool staged_store = NST <= 3;
+    static constexpr uint32_t stage_bytes = PAIR ? PAIR_STAGE_BYTES : STAGE_BYTES;
+    static constexpr uint32_t sfa_off = A_BYTES + (PAIR ? B_HALF_BYTES : B_BYTES);
+    static constexpr uint32_t sfb_off = sfa_off + SFA_BYTES;
+    static constexpr bool staged_store = NST * stage_bytes + 2 * BOX_BYTES + 256 + 8 * 260 + 1024 <= 232448;
     static constexpr uint32_t staging_bytes = staged_store ? 2 * BOX_BYTES : 0;
-    static constexpr uint32_t staging_off = NST * STAGE_BYTES;
+    static constexpr uint32_t staging_off = NST * stage_bytes;
     static constexpr uint32_t bars_off = staging_off + staging_bytes;
     static constexpr uint32_t prefix_off = bars_off + 256;
-    static constexpr uint32_t smem_bytes = prefix_off + 4 * 260 + 1024;
+    static constexpr uint32_t smem_bytes = prefix_off + 8 * 260 + 1024;
     static_assert(smem_bytes <= 232448, "GEMM shared memory above the 227 KB per-CTA limit");
+    static_assert(3 * NST + 4 <= 24, "barriers overlap the TMEM slot");
+    static_assert(TMEM_SF + SF_COLS * NST <= 512, "scale buffers beyond the TMEM allocation");
 };
-constexpr int kThreads = 320;          // producer warp, MMA warp, 8 epilogue warps
+constexpr int kThreads = 352;          // producer warp, MMA warp, 8 epilogue warps, scale-copy warp
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_SFA = 256;                    // 16 columns
-constexpr uint32_t TMEM_SFB = 272;                    // 32 columns
 constexpr uint64_t kWaitLimitNs = 4000000000ull;      // 4 s
-constexpr int kMaxGroups = 256;
+constexpr int kMaxGroups = 256;            // the prefix arrays hold kMaxGroups + 1 entries (260 reserved)
 constexpr int kBandM = 32;                            // m-tiles per band of the dense tile order
 constexpr int64_t kBandAboveBytes = 48ll << 20;       // band only an A operand L2 cannot keep
 
@@ -94,6 +124,7 @@ struct GemmArgs {
     const uint8_t* sfa;
     const uint8_t* sfb;
     uint64_t sf_tile_stride;         // bytes per 128-row tile of scales (A and B)
+    uint32_t sf_box_bytes;           // paired form: bytes of one scale box (a stage's chunks of one 128-row tile)
     const float* ts_a;               // dense NVFP4: A tensor scale
     const float* ts_b;               // dense NVFP4: B tensor scale; grouped: [groups]
     const float* a_row_scale;        // grouped: per-row factor of A
@@ -114,6 +145,7 @@ struct TileInfo {
     int b_row1;
     int group;
     int col0;         // first output column
+    bool phantom;     // paired form: this CTA's m-tile lies past the last one (loads for the pair, stores nothing)
 };
 
 __device__ __forceinline__ void flag_abort(volatile int* abort, uint32_t* status, uint32_t bit) {
@@ -125,9 +157,65 @@ __device__ __forceinline__ void flag_abort(volatile int* abort, uint32_t* status
 
 // Output tile `tile` -> rows / columns / scale tiles.  Grouped tiles run
 // N-fastest, so the CTAs working at one time share A rows and one group's B.
+// B rows of output-column tile nt of group `group` (both halves; b_row1 < 0:
+// the second half lies past N).
+template <int EPI>
+__device__ __forceinline__ void decode_b(const GemmArgs& a, int nt, TileInfo& t) {
+    const int gbase = t.group * a.N;
+    if (EPI == kSiluGate) {
+        t.b_row0 = gbase + nt * 128;
+        t.b_row1 = gbase + a.N / 2 + nt * 128;
+        t.col0 = nt * 128;
+    } else {
+        t.b_row0 = gbase + nt * BN;
+        t.b_row1 = (nt * BN + 128 < a.N) ? t.b_row0 + 128 : -1;
+        t.col0 = nt * BN;
+    }
+}
+
+// Paired form: work unit `unit` -> this CTA's share (CTA rank `crank` of the
+// pair takes m-tile 2 p + crank of the pair's m-tile pair p; both take the
+// same B tile).  Grouped units pair the m-tiles of one group; dense units are
+// banded over m-tile pairs like the single-CTA order.
+template <int EPI>
+__device__ __forceinline__ TileInfo decode_pair(const GemmArgs& a, int unit, const int* tile_prefix,
+                                                const int* pair_prefix, int m_tiles, uint32_t crank) {
+    TileInfo t;
+    int nt, mp;
+    if (a.groups) {
+        nt = unit % a.n_tiles;
+        mp = unit / a.n_tiles;
+        int e = 0;
+        while (e + 1 < a.groups && pair_prefix[e + 1] <= mp) ++e;
+        const int lt = 2 * (mp - pair_prefix[e]) + int(crank);      // m-tile within the group
+        const int tiles_e = tile_prefix[e + 1] - tile_prefix[e];
+        t.group = e;
+        t.phantom = lt >= tiles_e;
+        t.a_row0 = int(a.offsets[e]) + lt * BM;
+        t.row_end = int(a.offsets[e + 1]);
+        t.a_sf_tile = tile_prefix[e] + min(lt, tiles_e - 1);
+    } else {
+        const int m_pairs = (m_tiles + 1) / 2, band_p = max(1, a.band_m / 2);
+        const int band = unit / (band_p * a.n_tiles);
+        const int within = unit - band * band_p * a.n_tiles;
+        const int bs = min(band_p, m_pairs - band * band_p);
+        nt = within / bs;
+        mp = band * band_p + within % bs;
+        const int mt = 2 * mp + int(crank);
+        t.group = 0;
+        t.phantom = mt >= m_tiles;
+        t.a_row0 = mt * BM;
+        t.row_end = a.M;
+        t.a_sf_tile = min(mt, m_tiles - 1);
+    }
+    decode_b<EPI>(a, nt, t);
+    return t;
+}
+
 template <int EPI>
 __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile, const int* tile_prefix, int m_tiles) {
     TileInfo t;
+    t.phantom = false;
     int nt, mt;
     if (a.groups) {
         nt = tile % a.n_tiles;
@@ -155,16 +243,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile, con
         t.row_end = a.M;
     }
     t.a_sf_tile = mt;
-    const int gbase = t.group * a.N;
-    if (EPI == kSiluGate) {
-        t.b_row0 = gbase + nt * 128;
-        t.b_row1 = gbase + a.N / 2 + nt * 128;
-        t.col0 = nt * 128;
-    } else {
-        t.b_row0 = gbase + nt * BN;
-        t.b_row1 = (nt * BN + 128 < a.N) ? t.b_row0 + 128 : -1;
-        t.col0 = nt * BN;
-    }
+    decode_b<EPI>(a, nt, t);
     return t;
 }
 
@@ -187,62 +266,91 @@ __device__ __forceinline__ void stage_bf16x32(uint32_t staging, int row, int c, 
     }
 }
 
-template <int EPI, int STAGES>
+// PAIR: launched as clusters of two CTAs (see the file comment); CG is the
+// CTA group every tcgen05 instruction of the kernel names.
+template <int EPI, int STAGES, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-            const __grid_constant__ CUtensorMap tmap_d, const GemmArgs args) {
-    using LY = Layout<STAGES>;
+            const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sfa,
+            const __grid_constant__ CUtensorMap tmap_sfb, const GemmArgs args) {
+    using LY = Layout<STAGES, PAIR>;
+    constexpr int CG = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::bars_off);
-    // bars[0..STAGES) full, [STAGES..2 STAGES) empty, then tmem_full, tmem_empty, mma drain
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
-    volatile int* abort = reinterpret_cast<volatile int*>(bars + 13);
+    // bars[0..STAGES) full, [STAGES..2 STAGES) empty, then tmem_full, tmem_empty, mma drain,
+    // [2 STAGES + 3 .. 3 STAGES + 3) scales copied, then the copy thread's drain
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
+    volatile int* abort = reinterpret_cast<volatile int*>(bars + 25);
     int* tile_prefix = reinterpret_cast<int*>(smem + LY::prefix_off);
+    int* pair_prefix = tile_prefix + 260;
     const uint32_t staging = tc::smem_u32(smem + LY::staging_off);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bar0 = tc::smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto copied_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 3 + s); };
     const uint32_t tmem_full = bar0 + 8u * (2 * STAGES), tmem_empty = bar0 + 8u * (2 * STAGES + 1),
-                   drain_bar = bar0 + 8u * (2 * STAGES + 2);
+                   drain_bar = bar0 + 8u * (2 * STAGES + 2), cp_drain_bar = bar0 + 8u * (3 * STAGES + 3);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(full_bar(s), 1);
             tc::mbar_init(empty_bar(s), 1);
+            tc::mbar_init(copied_bar(s), 1);
         }
         tc::mbar_init(tmem_full, 1);
-        tc::mbar_init(tmem_empty, 8);       // one arrival per epilogue warp
+        // one arrival per epilogue warp (the pair: the even CTA's barrier takes both CTAs' warps)
+        tc::mbar_init(tmem_empty, PAIR ? 16 : 8);
         tc::mbar_init(drain_bar, 1);
+        tc::mbar_init(cp_drain_bar, 1);
         *abort = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&tmap_a);
         tc::tma_prefetch_desc(&tmap_b);
-        // 128-row tiles per group, prefix-summed (grouped form)
-        int acc = 0;
+        if constexpr (PAIR) {
+            tc::tma_prefetch_desc(&tmap_sfa);
+            tc::tma_prefetch_desc(&tmap_sfb);
+        }
+        // 128-row tiles per group and (paired form) pairs of them, prefix-summed
+        int acc = 0, accp = 0;
         tile_prefix[0] = 0;
+        pair_prefix[0] = 0;
         for (int e = 0; e < args.groups; ++e) {
             const int n = int(args.offsets[e + 1] - args.offsets[e]);
-            acc += (n + BM - 1) / BM;
+            const int tiles = (n + BM - 1) / BM;
+            acc += tiles;
+            accp += (tiles + 1) / 2;
             tile_prefix[e + 1] = acc;
+            pair_prefix[e + 1] = accp;
         }
     }
     if (warp == 1) {
-        tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
-        tc::tmem_relinquish();
+        tc::tmem_alloc_g<CG>(tc::smem_u32(tmem_slot), TMEM_COLS);
+        tc::tmem_relinquish_g<CG>();
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t crank = PAIR ? tc::cluster_ctarank() : 0u;
+    const bool leader = crank == 0;
+    // the pair: both CTAs' barriers are initialised and their TMEM allocated
+    if constexpr (PAIR) tc::cluster_sync_all();
 
     const int m_tiles = args.groups ? tile_prefix[args.groups] : (args.M + BM - 1) / BM;
-    const int num_tiles = m_tiles * args.n_tiles;
-    const int unit0 = int(blockIdx.x);
-    const int unit_step = int(gridDim.x);
+    const int m_units = !PAIR ? m_tiles : (args.groups ? pair_prefix[args.groups] : (m_tiles + 1) / 2);
+    const int num_tiles = m_units * args.n_tiles;
+    const int unit0 = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
+    const int unit_step = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
     const uint32_t chunk_elems = args.nv ? 64 : 128;  // K elements per 512-byte scale chunk
+    auto decode = [&](int unit) {
+        if constexpr (PAIR)
+            return decode_pair<EPI>(args, unit, tile_prefix, pair_prefix, m_tiles, crank);
+        else
+            return decode_tile<EPI>(args, unit, tile_prefix, m_tiles);
+    };
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer ----------------
@@ -251,7 +359,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         int issued = 0;
         bool ok = true;
         for (int tile = unit0; tile < num_tiles && ok; tile += unit_step) {
-            const TileInfo t = decode_tile<EPI>(args, tile, tile_prefix, m_tiles);
+            const TileInfo t = decode(tile);
             for (int kb = 0; kb < args.k_stages; ++kb) {
                 if (!tc::mbar_wait(empty_bar(stage), phase ^ 1, abort, kWaitLimitNs)) {
                     flag_abort(abort, args.status, args.status_bit);
@@ -262,15 +370,35 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 const uint32_t chunks = uint32_t(k_elems) / chunk_elems;
                 const uint64_t ct0 = uint64_t(kb) * uint64_t(args.bk) / chunk_elems;
                 const uint32_t sf_bytes = chunks * 512u * (t.b_row1 >= 0 ? 3u : 2u);
-                uint8_t* st = smem + stage * STAGE_BYTES;
+                uint8_t* st = smem + stage * LY::stage_bytes;
                 const uint32_t fb = full_bar(stage);
-                tc::mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + sf_bytes);
-                // x coordinate in bytes: 128 bytes of K per stage for both element widths
-                tc::tma_load_2d(tc::smem_u32(st), &tmap_a, fb, kb * 128, t.a_row0);
-                tc::bulk_load(tc::smem_u32(st + A_BYTES + B_BYTES),
-                              args.sfa + uint64_t(t.a_sf_tile) * args.sf_tile_stride + ct0 * 512u, chunks * 512u, fb);
-                uint8_t* sfb_smem = st + A_BYTES + B_BYTES + SFA_BYTES;
-                {
+                uint8_t* sfb_smem = st + LY::sfb_off;
+                if constexpr (PAIR) {
+                    // this CTA's A rows, B half `crank` and the scales of its A rows and
+                    // of both B halves (an absent second half takes the first's scale
+                    // tile: its columns are not stored); the bytes count on the even
+                    // CTA's full barrier, which expects both CTAs' boxes (every box
+                    // lands in full, zero-filled where it leaves the tensor)
+                    const uint32_t fbp = tc::map_to_rank(fb, 0);
+                    if (leader) tc::mbar_arrive_expect_tx(fb, 2u * (A_BYTES + B_HALF_BYTES + 3u * args.sf_box_bytes));
+                    const int brow = crank ? (t.b_row1 >= 0 ? t.b_row1 : t.b_row0 + 128) : t.b_row0;
+                    const int bsf1 = (t.b_row1 >= 0 ? t.b_row1 : t.b_row0) / 128;
+                    const uint64_t ck = ct0 * 512u;            // byte offset in a scale tile
+                    tc::tma_load_2d_pair(tc::smem_u32(st), &tmap_a, fbp, kb * 128, t.a_row0);
+                    tc::tma_load_2d_pair(tc::smem_u32(st + A_BYTES), &tmap_b, fbp, kb * 128, brow);
+                    tc::tma_load_2d_pair(tc::smem_u32(st + LY::sfa_off), &tmap_sfa, fbp, 0,
+                                         int((uint64_t(t.a_sf_tile) * args.sf_tile_stride + ck) / 256u));
+                    tc::tma_load_2d_pair(tc::smem_u32(sfb_smem), &tmap_sfb, fbp, 0,
+                                         int((uint64_t(t.b_row0 / 128) * args.sf_tile_stride + ck) / 256u));
+                    tc::tma_load_2d_pair(tc::smem_u32(sfb_smem + 4 * 512), &tmap_sfb, fbp, 0,
+                                         int((uint64_t(bsf1) * args.sf_tile_stride + ck) / 256u));
+                } else {
+                    tc::mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + sf_bytes);
+                    // x coordinate in bytes: 128 bytes of K per stage for both element widths
+                    tc::tma_load_2d(tc::smem_u32(st), &tmap_a, fb, kb * 128, t.a_row0);
+                    tc::bulk_load(tc::smem_u32(st + LY::sfa_off),
+                                  args.sfa + uint64_t(t.a_sf_tile) * args.sf_tile_stride + ct0 * 512u, chunks * 512u,
+                                  fb);
                     tc::tma_load_2d(tc::smem_u32(st + A_BYTES), &tmap_b, fb, kb * 128, t.b_row0);
                     // an absent second half still lands: rows past the end are zero-filled
                     tc::tma_load_2d(tc::smem_u32(st + A_BYTES + B_HALF_BYTES), &tmap_b, fb, kb * 128,
@@ -288,127 +416,179 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             }
         }
         // drain: every stage issued last must have landed before the CTA exits
-        for (int i = 0; i < STAGES && i < issued; ++i) {
-            if (--stage < 0) { stage = STAGES - 1; phase ^= 1; }
-            if (!tc::mbar_wait_drain(full_bar(stage), phase, kWaitLimitNs)) {
-                flag_abort(abort, args.status, args.status_bit);
-                break;
+        if (PAIR && !leader) {
+            // the odd CTA's loads count on the even CTA's barriers: it waits for
+            // the MMAs to have consumed its last fills (the data had landed)
+            for (int i = max(0, issued - STAGES); i < issued; ++i) {
+                if (!tc::mbar_wait_drain(empty_bar(i % STAGES), uint32_t(i / STAGES) & 1u, kWaitLimitNs)) {
+                    flag_abort(abort, args.status, args.status_bit);
+                    break;
+                }
+            }
+        } else {
+            for (int i = 0; i < STAGES && i < issued; ++i) {
+                if (--stage < 0) { stage = STAGES - 1; phase ^= 1; }
+                if (!tc::mbar_wait_drain(full_bar(stage), phase, kWaitLimitNs)) {
+                    flag_abort(abort, args.status, args.status_bit);
+                    break;
+                }
             }
         }
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ---------------- MMA issuer (the pair: the even CTA's) ----------------
         // Stage-0 descriptors, split into the low word (address field, advanced per
-        // stage / K step) and the constant high word.
+        // stage / K step) and the constant high word.  For the pair the same
+        // shared-memory offsets address both CTAs' tiles.
+        constexpr uint32_t MM = PAIR ? 2 * BM : BM;                 // rows of the MMA
         const uint64_t d0 = tc::smem_desc(tc::smem_u32(smem), 16, 1024, 2);
-        const uint64_t sf0 = tc::smem_desc(tc::smem_u32(smem + A_BYTES + B_BYTES), 0, 128, 0);
         const uint32_t d_lo0 = uint32_t(d0), d_hi = uint32_t(d0 >> 32);
-        const uint32_t sf_lo0 = uint32_t(sf0), sf_hi = uint32_t(sf0 >> 32);
-        const uint32_t idesc_nv = tc::idesc_block_scaled(BM, BN, false, 0, 0);
-        const uint32_t idesc_mx0 = tc::idesc_block_scaled(BM, BN, true, 0, 0);
-        const uint32_t idesc_mx1 = tc::idesc_block_scaled(BM, BN, true, 2, 2);
+        const uint32_t idesc_nv = tc::idesc_block_scaled(MM, BN, false, 0, 0);
+        const uint32_t idesc_mx0 = tc::idesc_block_scaled(MM, BN, true, 0, 0);
+        const uint32_t idesc_mx1 = tc::idesc_block_scaled(MM, BN, true, 2, 2);
         // MXFP8 (kind::mxf8f6f4, one UE8M0 byte per 32 elements): MMA j of a stage
         // reads byte j of the stage's scale column
-        const uint32_t idesc_f8_0 = tc::idesc_block_scaled(BM, BN, true, 0, 0, 0, 0);
-        const uint32_t idesc_f8_1 = tc::idesc_block_scaled(BM, BN, true, 1, 1, 0, 0);
-        const uint32_t idesc_f8_2 = tc::idesc_block_scaled(BM, BN, true, 2, 2, 0, 0);
-        const uint32_t idesc_f8_3 = tc::idesc_block_scaled(BM, BN, true, 3, 3, 0, 0);
+        const uint32_t idesc_f8_0 = tc::idesc_block_scaled(MM, BN, true, 0, 0, 0, 0);
+        const uint32_t idesc_f8_1 = tc::idesc_block_scaled(MM, BN, true, 1, 1, 0, 0);
+        const uint32_t idesc_f8_2 = tc::idesc_block_scaled(MM, BN, true, 2, 2, 0, 0);
+        const uint32_t idesc_f8_3 = tc::idesc_block_scaled(MM, BN, true, 3, 3, 0, 0);
+        constexpr uint16_t kBoth = 0x3;                             // both CTAs of the pair
         int stage = 0;
         uint32_t phase = 0;
         int tcount = 0;
         bool ok = true;
         for (int tile = unit0; tile < num_tiles && ok; tile += unit_step, ++tcount) {
-            if (!tc::mbar_wait(tmem_empty, (tcount & 1) ^ 1, abort, kWaitLimitNs)) {
+            const bool got = PAIR ? tc::mbar_wait_cluster(tmem_empty, (tcount & 1) ^ 1, abort, kWaitLimitNs)
+                                  : tc::mbar_wait(tmem_empty, (tcount & 1) ^ 1, abort, kWaitLimitNs);
+            if (!got) {
                 flag_abort(abort, args.status, args.status_bit);
                 break;
             }
             tc::fence_after_sync();
             for (int kb = 0; kb < args.k_stages; ++kb) {
-                // The stage's tiles and scales were written by TMA (async proxy) and
-                // completed on the mbarrier; the MMAs read them through the async proxy
-                // too, so no tcgen05 fence is needed here (one per stage costs about
-                // 300 cycles of tensor-pipe time).  The TMEM hand-off with the epilogue
-                // keeps its fences.
+                // The copy thread released the stage: its tiles have landed (for the
+                // pair, both CTAs' bytes) and its scales are in the stage's TMEM
+                // buffer.
+                if (!tc::mbar_wait(copied_bar(stage), phase, abort, kWaitLimitNs)) {
+                    flag_abort(abort, args.status, args.status_bit);
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const int k_elems = min(args.bk, args.K - kb * args.bk);
+                // descriptors of this stage: the 14-bit address field (bytes >> 4)
+                // of the stage-0 descriptors advanced by the stage offset
+                const uint32_t so = uint32_t(stage) * (LY::stage_bytes >> 4);
+                const uint32_t a_lo = d_lo0 + so, b_lo = d_lo0 + so + (A_BYTES >> 4);
+                // the stage's scale buffer: A chunk c at sfa + 4 c, B half h chunk c at sfb + 8 c + 4 h
+                const uint32_t sfa = tmem + TMEM_SF + SF_COLS * uint32_t(stage), sfb = sfa + 16u;
+                // The full-stage paths are unrolled with constant counts: this one
+                // thread's instruction stream paces the tensor pipe.
+                if (args.f8) {
+                    // 128 FP8 elements: one scale chunk (A) and one per B half, four K = 32 MMAs
+                    const uint32_t id[4] = {idesc_f8_0, idesc_f8_1, idesc_f8_2, idesc_f8_3};
+#pragma unroll
+                    for (uint32_t j = 0; j < 4; ++j)
+                        tc::mma_mxf8_g<CG>(tmem, tc::desc_from(a_lo + 2 * j, d_hi), tc::desc_from(b_lo + 2 * j, d_hi),
+                                           id[j], sfa, sfb, (kb | int(j)) ? 1u : 0u);
+                } else if (k_elems == BK) {
+                    if (args.nv) {
+                        // NVFP4: MMA j (64 K elements) takes scale chunk j (4 x 16)
+#pragma unroll
+                        for (uint32_t j = 0; j < 4; ++j)
+                            tc::mma_nvf4_g<CG>(tmem, tc::desc_from(a_lo + 2 * j, d_hi), tc::desc_from(b_lo + 2 * j, d_hi),
+                                               idesc_nv, sfa + 4 * j, sfb + 8 * j, (kb | int(j)) ? 1u : 0u);
+                    } else {
+                        // MXFP4: MMA j takes half of chunk j / 2 (scale ids 0 / 2: its first or second pair)
+#pragma unroll
+                        for (uint32_t j = 0; j < 4; ++j)
+                            tc::mma_mxf4_g<CG>(tmem, tc::desc_from(a_lo + 2 * j, d_hi), tc::desc_from(b_lo + 2 * j, d_hi),
+                                               (j & 1) ? idesc_mx1 : idesc_mx0, sfa + 4 * (j >> 1), sfb + 8 * (j >> 1),
+                                               (kb | int(j)) ? 1u : 0u);
+                    }
+                } else {
+                    // K tail: 128 elements (K % 256 == 128)
+                    const uint32_t nmma = uint32_t(k_elems) / 64;
+                    for (uint32_t j = 0; j < nmma; ++j) {
+                        const uint64_t da = tc::desc_from(a_lo + 2 * j, d_hi), db = tc::desc_from(b_lo + 2 * j, d_hi);
+                        const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+                        if (args.nv)
+                            tc::mma_nvf4_g<CG>(tmem, da, db, idesc_nv, sfa + 4 * j, sfb + 8 * j, acc);
+                        else
+                            tc::mma_mxf4_g<CG>(tmem, da, db, (j & 1) ? idesc_mx1 : idesc_mx0, sfa + 4 * (j >> 1),
+                                               sfb + 8 * (j >> 1), acc);
+                    }
+                }
+                tc::tc_commit_g<CG>(empty_bar(stage), kBoth);     // the stage is free (in both CTAs)
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+            tc::tc_commit_g<CG>(tmem_full, kBoth);
+        }
+        // drain: all MMAs and scale copies of this thread complete (a CTA that got
+        // no tile issued none)
+        if (tcount > 0 || !ok) {
+            tc::tc_commit_g<CG>(drain_bar, 0x1);
+            if (!tc::mbar_wait_drain(drain_bar, 0, kWaitLimitNs)) flag_abort(abort, args.status, args.status_bit);
+        }
+    } else if (warp == 10 && lane == 0 && leader) {
+        // ---------------- scale copies (the pair: the even CTA's) ----------------
+        // Per stage, once its bytes have landed: the 512-byte scale chunks (128
+        // rows x 4 scales) into the stage's TMEM buffer, replicated to the four
+        // lane quadrants (for the pair, each CTA's chunks into its own TMEM) -- A
+        // chunk c at column 4 c, B half h chunk c at 16 + 8 c + 4 h -- then a
+        // commit releases the stage to the MMA thread.  The buffer's previous
+        // contents were read by the MMAs of that stage's previous fill, which
+        // completed before the stage was refilled.
+        const uint64_t sf0 = tc::smem_desc(tc::smem_u32(smem + LY::sfa_off), 0, 128, 0);
+        const uint32_t sf_lo0 = uint32_t(sf0), sf_hi = uint32_t(sf0 >> 32);
+        int stage = 0;
+        uint32_t phase = 0;
+        int copied = 0;
+        bool ok = true;
+        for (int tile = unit0; tile < num_tiles && ok; tile += unit_step) {
+            for (int kb = 0; kb < args.k_stages; ++kb) {
                 if (!tc::mbar_wait(full_bar(stage), phase, abort, kWaitLimitNs)) {
                     flag_abort(abort, args.status, args.status_bit);
                     ok = false;
                     break;
                 }
-                const int k_elems = min(args.bk, args.K - kb * args.bk);
-                // descriptors of this stage: the 14-bit address field (bytes >> 4)
-                // of the stage-0 descriptors advanced by the stage offset
-                const uint32_t so = uint32_t(stage) * (STAGE_BYTES >> 4);
-                const uint32_t a_lo = d_lo0 + so, b_lo = d_lo0 + so + (A_BYTES >> 4);
+                tc::fence_after_sync();
+                const uint32_t so = uint32_t(stage) * (LY::stage_bytes >> 4);
                 const uint32_t sfa_lo = sf_lo0 + so, sfb_lo = sf_lo0 + so + (SFA_BYTES >> 4);
-                if (args.f8) {
-                    // 128 FP8 elements: one scale chunk (A) and one per B half, four K = 32 MMAs
-                    tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFA, tc::desc_from(sfa_lo, sf_hi));
-                    tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB, tc::desc_from(sfb_lo, sf_hi));
-                    tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 4, tc::desc_from(sfb_lo + 128, sf_hi));
-                    const uint32_t id[4] = {idesc_f8_0, idesc_f8_1, idesc_f8_2, idesc_f8_3};
+                const uint32_t sfa = tmem + TMEM_SF + SF_COLS * uint32_t(stage), sfb = sfa + 16u;
+                const uint32_t chunks = uint32_t(min(args.bk, args.K - kb * args.bk)) / chunk_elems;
+                if (chunks == 4) {
 #pragma unroll
-                    for (uint32_t j = 0; j < 4; ++j)
-                        tc::mma_mxf8(tmem, tc::desc_from(a_lo + 2 * j, d_hi), tc::desc_from(b_lo + 2 * j, d_hi), id[j],
-                                     tmem + TMEM_SFA, tmem + TMEM_SFB, (kb | int(j)) ? 1u : 0u);
-                } else if (k_elems == BK) {
-                    if (args.nv) {
+                    for (uint32_t c = 0; c < 4; ++c) {
+                        tc::tc_cp_g<CG>(sfa + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
+                        tc::tc_cp_g<CG>(sfb + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
+                        tc::tc_cp_g<CG>(sfb + 8 * c + 4, tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
+                    }
+                } else if (chunks == 2) {
 #pragma unroll
-                        for (uint32_t c = 0; c < 4; ++c) {
-                            tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFA + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
-                            tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
-                            tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c + 4,
-                                                     tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
-                        }
-#pragma unroll
-                        for (uint32_t j = 0; j < 4; ++j)
-                            tc::mma_nvf4(tmem, tc::desc_from(a_lo + 2 * j, d_hi), tc::desc_from(b_lo + 2 * j, d_hi),
-                                         idesc_nv, tmem + TMEM_SFA + 4 * j, tmem + TMEM_SFB + 8 * j,
-                                         (kb | int(j)) ? 1u : 0u);
-                    } else {
-#pragma unroll
-                        for (uint32_t c = 0; c < 2; ++c) {
-                            tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFA + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
-                            tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
-                            tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c + 4,
-                                                     tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
-                        }
-#pragma unroll
-                        for (uint32_t j = 0; j < 4; ++j)
-                            tc::mma_mxf4(tmem, tc::desc_from(a_lo + 2 * j, d_hi), tc::desc_from(b_lo + 2 * j, d_hi),
-                                         (j & 1) ? idesc_mx1 : idesc_mx0, tmem + TMEM_SFA + 4 * (j >> 1),
-                                         tmem + TMEM_SFB + 8 * (j >> 1), (kb | int(j)) ? 1u : 0u);
+                    for (uint32_t c = 0; c < 2; ++c) {
+                        tc::tc_cp_g<CG>(sfa + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
+                        tc::tc_cp_g<CG>(sfb + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
+                        tc::tc_cp_g<CG>(sfb + 8 * c + 4, tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
                     }
                 } else {
-                    // K tail: 128 elements (K % 256 == 128)
-                    const uint32_t chunks = uint32_t(k_elems) / chunk_elems;
-                    const uint32_t nmma = uint32_t(k_elems) / 64;
                     for (uint32_t c = 0; c < chunks; ++c) {
-                        tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFA + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
-                        tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
-                        tc::tc_cp_32x128b_warpx4(tmem + TMEM_SFB + 8 * c + 4, tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
-                    }
-                    for (uint32_t j = 0; j < nmma; ++j) {
-                        const uint64_t da = tc::desc_from(a_lo + 2 * j, d_hi), db = tc::desc_from(b_lo + 2 * j, d_hi);
-                        const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
-                        if (args.nv)
-                            tc::mma_nvf4(tmem, da, db, idesc_nv, tmem + TMEM_SFA + 4 * j, tmem + TMEM_SFB + 8 * j, acc);
-                        else
-                            tc::mma_mxf4(tmem, da, db, (j & 1) ? idesc_mx1 : idesc_mx0, tmem + TMEM_SFA + 4 * (j >> 1),
-                                         tmem + TMEM_SFB + 8 * (j >> 1), acc);
+                        tc::tc_cp_g<CG>(sfa + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
+                        tc::tc_cp_g<CG>(sfb + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
+                        tc::tc_cp_g<CG>(sfb + 8 * c + 4, tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
                     }
                 }
-                tc::tc_commit(empty_bar(stage));
+                tc::tc_commit_g<CG>(copied_bar(stage), 0x1);
+                ++copied;
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
-            if (!ok) break;
-            tc::tc_commit(tmem_full);
         }
-        // drain: all MMAs and scale copies of this thread complete (a CTA that got
-        // no tile issued none)
-        if (tcount > 0 || !ok) {
-            tc::tc_commit(drain_bar);
-            if (!tc::mbar_wait_drain(drain_bar, 0, kWaitLimitNs)) flag_abort(abort, args.status, args.status_bit);
+        // drain: the copies this thread issued complete before the CTA frees TMEM
+        if (copied > 0) {
+            tc::tc_commit_g<CG>(cp_drain_bar, 0x1);
+            if (!tc::mbar_wait_drain(cp_drain_bar, 0, kWaitLimitNs)) flag_abort(abort, args.status, args.status_bit);
         }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < 10) {
         // ---------------- epilogue ----------------
         // Eight warps: warp w reads TMEM lane quadrant w % 4 (rows 32q .. 32q + 31 of
         // the tile) and the column half hf of the tile, so each warp's share of
@@ -417,6 +597,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         const int hf = (warp - 2) >> 2;
         const int et = int(threadIdx.x) - 64;            // epilogue thread 0..255
         const float dense_alpha = (!args.groups && args.nv) ? __fmul_rn(*args.ts_a, *args.ts_b) : 1.0f;
+        // the accumulator goes back to the MMA thread: one arrival per warp, on the
+        // even CTA's barrier for the pair
+        const uint32_t acc_empty = PAIR ? tc::map_to_rank(tmem_empty, 0) : tmem_empty;
+        auto release_acc = [&]() {
+            if constexpr (PAIR)
+                tc::mbar_arrive_cluster(acc_empty);
+            else
+                tc::mbar_arrive(acc_empty);
+        };
         int tcount = 0;
         for (int tile = unit0; tile < num_tiles; tile += unit_step, ++tcount) {
             // The eight warps decide together whether the tile goes ahead: a warp
@@ -428,7 +617,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 break;
             }
             tc::fence_after_sync();
-            const TileInfo t = decode_tile<EPI>(args, tile, tile_prefix, m_tiles);
+            const TileInfo t = decode(tile);
             const int row = t.a_row0 + q * 32 + lane;
             const bool row_ok = row < t.row_end;
             float alpha = dense_alpha;
@@ -446,7 +635,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 tc::tmem_ld_wait();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(tmem_empty);
+                if (lane == 0) release_acc();
                 if (row_ok) {
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
@@ -499,7 +688,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 }
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(tmem_empty);
+                if (lane == 0) release_acc();
                 if (row_ok) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -518,7 +707,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         }
                     }
                 }
-            } else if (LY::staged_store && args.d_bf16 &&
+            } else if (LY::staged_store && args.d_bf16 && !t.phantom &&
                        t.a_row0 + BM <= t.row_end + (args.groups ? 0 : BM)) {
                 // BF16 through shared memory and TMA stores.  Each warp moves its 32 rows
                 // x 128 columns out of TMEM into registers, then the accumulator goes
@@ -536,7 +725,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 }
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(tmem_empty);
+                if (lane == 0) release_acc();
                 if (et == 0) tc::bulk_wait_read0();              // previous tile's stores have read the staging
                 tc::named_bar_sync(1, 256);
 #pragma unroll
@@ -567,7 +756,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     if (c == 3) {
                         tc::fence_before_sync();
                         __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(tmem_empty);
+                        if (lane == 0) release_acc();
                     }
                     const int col = t.col0 + 128 * hf + c * 32;
                     if (!row_ok || col >= args.N) continue;
@@ -607,9 +796,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     __syncwarp();          // the elected lanes rejoin their warps before the block barrier
     tc::fence_before_sync();
     __syncthreads();
+    // the pair: neither CTA frees TMEM while the other may still read its
+    // accumulator or arrive on its barriers
+    if constexpr (PAIR) tc::cluster_sync_all();
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, TMEM_COLS);
+        tc::tmem_dealloc_g<CG>(tmem, TMEM_COLS);
     }
 }
 
@@ -662,13 +854,31 @@ fp4q_status encode_output_map(CUtensorMap* map, void* D, int64_t rows, int64_t N
 }
 
 
-template <int EPI, int NST>
-fp4q_status launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const GemmArgs& a,
-                          int tiles_upper, int sms, cudaStream_t stream) {
-    constexpr uint32_t smem = Layout<NST>::smem_bytes;
-    auto kernel = gemm_kernel<EPI, NST>;
+// 2D map over a block-scale array in the MMA layout viewed as rows of 256
+// bytes; a box is one stage's scale chunks of one 128-row tile (box_rows rows).
+fp4q_status encode_scale_map(CUtensorMap* map, const uint8_t* s, uint64_t bytes, uint32_t box_rows) {
+    cuuint64_t dims[2] = {256u, cuuint64_t(bytes / 256u)};
+    cuuint64_t strides[1] = {256u};
+    cuuint32_t box[2] = {256u, box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = encoder()(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(s), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FP4Q_ERR_CUDA, "cuTensorMapEncodeTiled (scales) failed (%d)", int(r));
+    return FP4Q_OK;
+}
+
+struct Maps {
+    CUtensorMap a, b, d, sfa, sfb;
+};
+
+template <int EPI, int NST, bool PAIR>
+fp4q_status launch_stages(const Maps& m, const GemmArgs& a, int units_upper, int sms, cudaStream_t stream) {
+    constexpr uint32_t smem = Layout<NST, PAIR>::smem_bytes;
+    auto kernel = gemm_kernel<EPI, NST, PAIR>;
     // per device, set on first use (setting it twice from racing threads is harmless)
     static std::atomic<bool> attr_set[64] = {};
+    static std::atomic<int> max_clusters[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (!attr_set[dev & 63].load(std::memory_order_acquire)) {
@@ -676,18 +886,49 @@ fp4q_status launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const CU
         if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
         attr_set[dev & 63].store(true, std::memory_order_release);
     }
-    const int grid = tiles_upper < sms ? tiles_upper : sms;
-    kernel<<<grid, kThreads, smem, stream>>>(ma, mb, md, a);
+    if constexpr (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // pairs that fit on the GPU at once (one CTA per SM): the persistent grid
+        int mc = max_clusters[dev & 63].load(std::memory_order_acquire);
+        if (mc <= 0) {
+            cfg.gridDim = dim3(unsigned(sms & ~1));
+            const cudaError_t e = cudaOccupancyMaxActiveClusters(&mc, kernel, &cfg);
+            if (e != cudaSuccess || mc <= 0) mc = sms / 2;
+            max_clusters[dev & 63].store(mc, std::memory_order_release);
+        }
+        const int clusters = std::max(1, std::min(units_upper, mc));
+        cfg.gridDim = dim3(unsigned(2 * clusters));
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m.a, m.b, m.d, m.sfa, m.sfb, a);
+        if (e != cudaSuccess) return fail(FP4Q_ERR_CUDA, "block_scaled_gemm (pair): %s", cudaGetErrorString(e));
+        return FP4Q_OK;
+    }
+    const int grid = units_upper < sms ? units_upper : sms;
+    kernel<<<grid, kThreads, smem, stream>>>(m.a, m.b, m.d, m.sfa, m.sfb, a);
     return check_launch("block_scaled_gemm");
 }
 
+// Ring depth: the paired form keeps 5 stages of 38 KB next to the BF16
+// staging boxes; the single-CTA form 3 (FP4) or 4 (MXFP8, whose stages hold
+// half the K of an FP4 stage; its BF16 rows go out straight from registers).
+constexpr int kPairStages = 5;
+
 template <int EPI>
-fp4q_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const GemmArgs& a,
-                   int tiles_upper, int sms, cudaStream_t stream) {
+fp4q_status launch(const Maps& m, const GemmArgs& a, bool pair, int units_upper, int sms, cudaStream_t stream) {
+    if (pair) return launch_stages<EPI, kPairStages, true>(m, a, units_upper, sms, stream);
     if constexpr (EPI == kStore) {
-        if (a.f8) return launch_stages<EPI, 4>(ma, mb, md, a, tiles_upper, sms, stream);
+        if (a.f8) return launch_stages<EPI, 4, false>(m, a, units_upper, sms, stream);
     }
-    return launch_stages<EPI, 3>(ma, mb, md, a, tiles_upper, sms, stream);
+    return launch_stages<EPI, 3, false>(m, a, units_upper, sms, stream);
 }
 
 }  // namespace
@@ -728,11 +969,12 @@ extern "C" fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_
     fp4q_status st = current_device(&sms);
     if (st != FP4Q_OK) return st;
     if ((st = get_encoder()) != FP4Q_OK) return st;
-    CUtensorMap ma, mb;
+    Maps maps;
+    memset(&maps, 0, sizeof maps);
     const bool f8 = A->format == FP4Q_MXFP8;
     const int64_t row_bytes = f8 ? K : K / 2;
-    if ((st = encode_operand_map(&ma, A->q, M, row_bytes)) != FP4Q_OK) return st;
-    if ((st = encode_operand_map(&mb, B->q, N, row_bytes)) != FP4Q_OK) return st;
+    if ((st = encode_operand_map(&maps.a, A->q, M, row_bytes)) != FP4Q_OK) return st;
+    if ((st = encode_operand_map(&maps.b, B->q, N, row_bytes)) != FP4Q_OK) return st;
     GemmArgs a = {};
     a.M = int(M);
     a.N = int(N);
@@ -748,6 +990,7 @@ extern "C" fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_
     a.sfa = A->scales;
     a.sfb = B->scales;
     a.sf_tile_stride = uint64_t(nv ? K / 64 : K / 128) * 512u;
+    a.sf_box_bytes = uint32_t(a.bk / (nv ? 64 : 128)) * 512u;
     a.ts_a = A->tensor_scale;
     a.ts_b = B->tensor_scale;
     a.D = static_cast<uint8_t*>(D);
@@ -755,11 +998,19 @@ extern "C" fp4q_status fp4q_block_scaled_gemm(const fp4q_operand* A, const fp4q_
     a.d_bf16 = d_type == FP4Q_BF16;
     a.status = status_word();
     a.status_bit = kStatusGemmTimeout;
-    CUtensorMap md;
-    memset(&md, 0, sizeof md);
-    if (a.d_bf16 && (st = encode_output_map(&md, D, M, N, ldd)) != FP4Q_OK) return st;
-    const int tiles = int((M + BM - 1) / BM) * a.n_tiles;
-    return launch<kStore>(ma, mb, md, a, tiles, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (a.d_bf16 && (st = encode_output_map(&maps.d, D, M, N, ldd)) != FP4Q_OK) return st;
+    // paired CTAs whenever there are two m-tiles to pair
+    const bool pair = m_tiles >= 2;
+    if (pair) {
+        const uint32_t box_rows = a.sf_box_bytes / 256u;
+        if ((st = encode_scale_map(&maps.sfa, A->scales, uint64_t(m_tiles) * a.sf_tile_stride, box_rows)) != FP4Q_OK)
+            return st;
+        if ((st = encode_scale_map(&maps.sfb, B->scales, uint64_t((N + 127) / 128) * a.sf_tile_stride, box_rows)) !=
+            FP4Q_OK)
+            return st;
+    }
+    const int units = (pair ? (m_tiles + 1) / 2 : m_tiles) * a.n_tiles;
+    return launch<kStore>(maps, a, pair, units, sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_scales, const float* a_row_scale,
@@ -792,9 +1043,10 @@ extern "C" fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sc
     fp4q_status st = current_device(&sms);
     if (st != FP4Q_OK) return st;
     if ((st = get_encoder()) != FP4Q_OK) return st;
-    CUtensorMap ma, mb;
-    if ((st = encode_operand_map(&ma, a_q, rows, K / 2)) != FP4Q_OK) return st;
-    if ((st = encode_operand_map(&mb, b_q, groups * N, K / 2)) != FP4Q_OK) return st;
+    Maps maps;
+    memset(&maps, 0, sizeof maps);
+    if ((st = encode_operand_map(&maps.a, a_q, rows, K / 2)) != FP4Q_OK) return st;
+    if ((st = encode_operand_map(&maps.b, b_q, groups * N, K / 2)) != FP4Q_OK) return st;
     GemmArgs a = {};
     a.M = int(rows);
     a.N = int(N);
@@ -807,6 +1059,7 @@ extern "C" fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sc
     a.sfa = a_scales;
     a.sfb = b_scales;
     a.sf_tile_stride = uint64_t(K / 64) * 512u;
+    a.sf_box_bytes = uint32_t(BK / 64) * 512u;
     a.ts_b = b_tensor_scale;
     a.a_row_scale = a_row_scale;
     a.D = static_cast<uint8_t*>(D);
@@ -816,15 +1069,22 @@ extern "C" fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_sc
     a.h_debug = h_debug;
     a.status = status_word();
     a.status_bit = kStatusGroupedTimeout;
-    const int m_tiles_upper = int((rows + BM - 1) / BM + groups);
+    // the groups' m-tiles run as pairs (a group's odd last tile pairs with a
+    // CTA that stores nothing): at most half the tiles plus one per group
+    const int m_pairs_upper = int(((rows + BM - 1) / BM + groups) / 2 + groups);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    CUtensorMap md;
-    memset(&md, 0, sizeof md);
+    const uint32_t box_rows = a.sf_box_bytes / 256u;
+    const int m_tiles_upper = int((rows + BM - 1) / BM + groups);
+    if ((st = encode_scale_map(&maps.sfa, a_scales, uint64_t(m_tiles_upper) * a.sf_tile_stride, box_rows)) != FP4Q_OK)
+        return st;
+    if ((st = encode_scale_map(&maps.sfb, b_scales, uint64_t(groups * N / 128) * a.sf_tile_stride, box_rows)) !=
+        FP4Q_OK)
+        return st;
     if (epilogue == FP4Q_EPI_SILU_GATE_MXFP4) {
         a.n_tiles = int(N / 256);
-        return launch<kSiluGate>(ma, mb, md, a, m_tiles_upper * a.n_tiles, sms, s);
+        return launch<kSiluGate>(maps, a, true, m_pairs_upper * a.n_tiles, sms, s);
     }
-    if ((st = encode_output_map(&md, D, rows, N, N)) != FP4Q_OK) return st;
+    if ((st = encode_output_map(&maps.d, D, rows, N, N)) != FP4Q_OK) return st;
     a.n_tiles = int((N + BN - 1) / BN);
-    return launch<kStore>(ma, mb, md, a, m_tiles_upper * a.n_tiles, sms, s);
+    return launch<kStore>(maps, a, true, m_pairs_upper * a.n_tiles, sms, s);
 }

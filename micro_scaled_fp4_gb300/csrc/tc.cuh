@@ -1,6 +1,6 @@
 // Inline-PTX wrappers for the Blackwell (sm_103a) tensor-core path:
 // mbarriers with bounded waits, TMA tiled and bulk copies, tcgen05 TMEM
-// allocation, block-scaled MMA, scale-factor copies and accumulator loads.
+// allocation, block-scaled MMA, scale-factor copies, accumulator loads and stores.
 #pragma once
 
 #include <cuda.h>
@@ -193,12 +193,6 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d, uint64_t a, uint64_t b, uin
                  " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}"
                  :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
 }
-// 32 rows x 128 bits of shared memory -> TMEM, replicated to the four
-// 32-lane quadrants (the scale-factor copy shape).
-__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
-}
-
 // 32 lanes x 32 consecutive 32-bit columns -> 32 registers per thread.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -211,6 +205,137 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 4 consecutive 32-bit columns of this warp's 32 lanes <- one register each per thread.
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint4 v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(taddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+// Waits until this thread's tcgen05.st have completed.
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---- CTA pairs (a two-CTA cluster running one tcgen05 MMA over both SMs) ----
+// Every tcgen05 instruction of a kernel names the same CTA group: the
+// wrappers below take it as a template argument (1: this CTA alone, 2: the
+// CTA pair of the cluster).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of both CTAs of the cluster meet here (release / acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Shared-memory address `addr` of this CTA mapped to the same offset in CTA
+// `rank` of the cluster (a shared::cluster address).
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Arrive (release, cluster scope) on an mbarrier given by its shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
+}
+// Bounded wait, acquire at cluster scope: for phases completed by arrivals
+// from the other CTA of the pair.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t limit_ns) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        uint32_t ok;
+        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+                     " selp.u32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(bar), "r"(parity), "r"(kSleepHintNs) : "memory");
+        if (ok) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+// TMA tile load into this CTA's shared memory whose completion (bytes) is
+// counted on an mbarrier of this CTA or of the other CTA of the pair
+// (`bar`: shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4}], [%2];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y) : "memory");
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_alloc_g(uint32_t dst_smem, uint32_t ncols) {
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(dst_smem), "r"(ncols)
+                     : "memory");
+    else
+        tmem_alloc(dst_smem, ncols);
+}
+template <int CG>
+__device__ __forceinline__ void tmem_relinquish_g() {
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    else
+        tmem_relinquish();
+}
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc_g(uint32_t taddr, uint32_t ncols) {
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+    else
+        tmem_dealloc(taddr, ncols);
+}
+// Commit arriving on the barrier at `bar` in this CTA (CG 1) or, for the pair,
+// on the barrier at the same offset in every CTA of `mask`.
+template <int CG>
+__device__ __forceinline__ void tc_commit_g(uint32_t bar, uint16_t mask) {
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                     " [%0], %1;" :: "r"(bar), "h"(mask) : "memory");
+    else
+        tc_commit(bar);
+}
+// 32 rows x 128 bits of shared memory -> TMEM, replicated to the four 32-lane
+// quadrants (the scale-factor copy shape); for the pair, each CTA's shared
+// memory to its own TMEM at the same addresses.
+template <int CG>
+__device__ __forceinline__ void tc_cp_g(uint32_t taddr, uint64_t sdesc) {
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+}
+// Block-scaled MMAs; for the pair (M = 256 in the instruction descriptor) A's
+// rows 0-127 and D's lanes come from / go to the issuing CTA, rows 128-255
+// from / to the other CTA, and each CTA holds half of B's N rows.
+template <int CG>
+__device__ __forceinline__ void mma_mxf4_g(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                           uint32_t sfb, uint32_t accumulate) {
+    if constexpr (CG == 2)
+        asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+                     " tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n}"
+                     :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
+    else
+        mma_mxf4(d, a, b, idesc, sfa, sfb, accumulate);
+}
+template <int CG>
+__device__ __forceinline__ void mma_nvf4_g(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                           uint32_t sfb, uint32_t accumulate) {
+    if constexpr (CG == 2)
+        asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+                     " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n}"
+                     :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
+    else
+        mma_nvf4(d, a, b, idesc, sfa, sfb, accumulate);
+}
+template <int CG>
+__device__ __forceinline__ void mma_mxf8_g(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                           uint32_t sfb, uint32_t accumulate) {
+    if constexpr (CG == 2)
+        asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+                     " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}"
+                     :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
+    else
+        mma_mxf8(d, a, b, idesc, sfa, sfb, accumulate);
+}
 
 }  // namespace tc
 }  // namespace fp4q

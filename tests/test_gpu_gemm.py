@@ -58,8 +58,12 @@ def _check(oracle, d_bf16, d_f32, ref):
     return e32, eb
 
 
-SHAPES = [(128, 256, 256), (128, 256, 128), (200, 300, 384), (1000, 520, 1024), (64, 64, 512), (512, 2048, 2048),
-          (1, 1032, 256), (3, 136, 128)]      # a single row; N = 4 x 256 + 8; a lone 128-element K stage
+# M <= 128 runs on single CTAs, larger M on CTA pairs (256-row tiles over two
+# SMs): one whole pair tile; three m-tiles (the last pair's second CTA past
+# the end) with an N tail and a half last K stage; a single row; N = 4 x 256
+# + 8; a lone 128-element K stage.
+SHAPES = [(256, 256, 256), (128, 256, 256), (128, 256, 128), (200, 300, 384), (384, 136, 640), (1000, 520, 1024),
+          (64, 64, 512), (512, 2048, 2048), (1, 1032, 256), (3, 136, 128)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
