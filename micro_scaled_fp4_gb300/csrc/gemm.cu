@@ -19,12 +19,15 @@
 //               (UE8M0 per 32) or kind::mxf4nvf4 (UE4M3 per 16), FP32
 //               accumulator in TMEM, reading the stage's block scales from
 //               that stage's own TMEM scale buffer.
-//   warp 10     one thread copies each landed stage's block scales into the
-//               stage's TMEM scale buffer (tcgen05.cp) and releases the stage
-//               to the MMA thread.  Issued from the MMA thread, the copies
-//               held back the MMAs (a stage of MXFP4 took ~830 cycles of issue
-//               for ~530 of MMA); from their own thread, into buffers no MMA
-//               in flight reads, they overlap with the MMAs.
+//   warps 10-11 one thread each copies half of each landed stage's block
+//               scales into the stage's TMEM scale buffer (tcgen05.cp); the
+//               two commits release the stage to the MMA thread.  Issued from
+//               the MMA thread, the copies held back the MMAs (a stage of
+//               MXFP4 took ~830 cycles of issue for ~530 of MMA); from their
+//               own threads, into buffers no MMA in flight reads, they overlap
+//               with the MMAs.  The copy unit takes about 53 cycles per
+//               512-byte chunk, so an NVFP4 stage's 12 copies (~640 cycles)
+//               still exceed its 4 MMAs (~512).
 //   warps 2..9  epilogue: tcgen05.ld of the 128 x 256 FP32 accumulator,
 //               one row and half the columns per thread (two warps per TMEM
 //               lane quadrant); the accumulator goes back to the MMA thread
@@ -97,10 +100,10 @@ struct Layout {
     static constexpr uint32_t prefix_off = bars_off + 256;
     static constexpr uint32_t smem_bytes = prefix_off + 8 * 260 + 1024;
     static_assert(smem_bytes <= 232448, "GEMM shared memory above the 227 KB per-CTA limit");
-    static_assert(3 * NST + 4 <= 24, "barriers overlap the TMEM slot");
+    static_assert(3 * NST + 5 <= 24, "barriers overlap the TMEM slot");
     static_assert(TMEM_SF + SF_COLS * NST <= 512, "scale buffers beyond the TMEM allocation");
 };
-constexpr int kThreads = 352;          // producer warp, MMA warp, 8 epilogue warps, scale-copy warp
+constexpr int kThreads = 384;          // producer warp, MMA warp, 8 epilogue warps, 2 scale-copy warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;      // 4 s
 constexpr int kMaxGroups = 256;            // the prefix arrays hold kMaxGroups + 1 entries (260 reserved)
@@ -279,7 +282,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::bars_off);
     // bars[0..STAGES) full, [STAGES..2 STAGES) empty, then tmem_full, tmem_empty, mma drain,
-    // [2 STAGES + 3 .. 3 STAGES + 3) scales copied, then the copy thread's drain
+    // [2 STAGES + 3 .. 3 STAGES + 3) scales copied, then the two copy threads' drains
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
     volatile int* abort = reinterpret_cast<volatile int*>(bars + 25);
     int* tile_prefix = reinterpret_cast<int*>(smem + LY::prefix_off);
@@ -298,13 +301,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(full_bar(s), 1);
             tc::mbar_init(empty_bar(s), 1);
-            tc::mbar_init(copied_bar(s), 1);
+            tc::mbar_init(copied_bar(s), 2);     // both copy threads' commits
         }
         tc::mbar_init(tmem_full, 1);
         // one arrival per epilogue warp (the pair: the even CTA's barrier takes both CTAs' warps)
         tc::mbar_init(tmem_empty, PAIR ? 16 : 8);
         tc::mbar_init(drain_bar, 1);
         tc::mbar_init(cp_drain_bar, 1);
+        tc::mbar_init(cp_drain_bar + 8, 1);
         *abort = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&tmap_a);
@@ -530,15 +534,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             tc::tc_commit_g<CG>(drain_bar, 0x1);
             if (!tc::mbar_wait_drain(drain_bar, 0, kWaitLimitNs)) flag_abort(abort, args.status, args.status_bit);
         }
-    } else if (warp == 10 && lane == 0 && leader) {
+    } else if (warp >= 10 && lane == 0 && leader) {
         // ---------------- scale copies (the pair: the even CTA's) ----------------
         // Per stage, once its bytes have landed: the 512-byte scale chunks (128
         // rows x 4 scales) into the stage's TMEM buffer, replicated to the four
         // lane quadrants (for the pair, each CTA's chunks into its own TMEM) -- A
         // chunk c at column 4 c, B half h chunk c at 16 + 8 c + 4 h -- then a
-        // commit releases the stage to the MMA thread.  The buffer's previous
-        // contents were read by the MMAs of that stage's previous fill, which
-        // completed before the stage was refilled.
+        // commit releases the stage to the MMA thread.  Copy thread `half`
+        // takes chunks [half n / 2, (half + 1) n / 2) of the stage's n (one
+        // chunk: thread 0 the A chunk and B's first half, thread 1 B's second).
+        // The buffer's previous contents were read by the MMAs of that stage's
+        // previous fill, which completed before the stage was refilled.
+        const uint32_t half = uint32_t(warp - 10);
         const uint64_t sf0 = tc::smem_desc(tc::smem_u32(smem + LY::sfa_off), 0, 128, 0);
         const uint32_t sf_lo0 = uint32_t(sf0), sf_hi = uint32_t(sf0 >> 32);
         int stage = 0;
@@ -559,24 +566,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 const uint32_t chunks = uint32_t(min(args.bk, args.K - kb * args.bk)) / chunk_elems;
                 if (chunks == 4) {
 #pragma unroll
-                    for (uint32_t c = 0; c < 4; ++c) {
+                    for (uint32_t i = 0; i < 2; ++i) {
+                        const uint32_t c = 2 * half + i;
                         tc::tc_cp_g<CG>(sfa + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
                         tc::tc_cp_g<CG>(sfb + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
                         tc::tc_cp_g<CG>(sfb + 8 * c + 4, tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
                     }
                 } else if (chunks == 2) {
-#pragma unroll
-                    for (uint32_t c = 0; c < 2; ++c) {
-                        tc::tc_cp_g<CG>(sfa + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
-                        tc::tc_cp_g<CG>(sfb + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
-                        tc::tc_cp_g<CG>(sfb + 8 * c + 4, tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
-                    }
+                    const uint32_t c = half;
+                    tc::tc_cp_g<CG>(sfa + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
+                    tc::tc_cp_g<CG>(sfb + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
+                    tc::tc_cp_g<CG>(sfb + 8 * c + 4, tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
+                } else if (half == 0) {
+                    tc::tc_cp_g<CG>(sfa, tc::desc_from(sfa_lo, sf_hi));
+                    tc::tc_cp_g<CG>(sfb, tc::desc_from(sfb_lo, sf_hi));
                 } else {
-                    for (uint32_t c = 0; c < chunks; ++c) {
-                        tc::tc_cp_g<CG>(sfa + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
-                        tc::tc_cp_g<CG>(sfb + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
-                        tc::tc_cp_g<CG>(sfb + 8 * c + 4, tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
-                    }
+                    tc::tc_cp_g<CG>(sfb + 4, tc::desc_from(sfb_lo + 128, sf_hi));
                 }
                 tc::tc_commit_g<CG>(copied_bar(stage), 0x1);
                 ++copied;
@@ -585,8 +590,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         }
         // drain: the copies this thread issued complete before the CTA frees TMEM
         if (copied > 0) {
-            tc::tc_commit_g<CG>(cp_drain_bar, 0x1);
-            if (!tc::mbar_wait_drain(cp_drain_bar, 0, kWaitLimitNs)) flag_abort(abort, args.status, args.status_bit);
+            tc::tc_commit_g<CG>(cp_drain_bar + 8 * half, 0x1);
+            if (!tc::mbar_wait_drain(cp_drain_bar + 8 * half, 0, kWaitLimitNs))
+                flag_abort(abort, args.status, args.status_bit);
         }
     } else if (warp >= 2 && warp < 10) {
         // ---------------- epilogue ----------------
