@@ -450,7 +450,22 @@ def c3_row(fq, W, torch, peaks, timed, dev_bf16, rows):
     amax_dev = am.clone()
     ms_sr1 = timed(lambda: c3(fq.FP4Q_SR, amax_dev), 10, True)
     ms_rne1 = timed(lambda: c3(fq.FP4Q_RNE, amax_dev), 10, True)
+    # both roundings from one read (fp4q_nv_quantize_sr_rne): the amax pass plus
+    # one quantize pass writing the SR and the RNE codes over one set of scales
+    q3b = torch.empty_like(q3)
+
+    def c3_both(amax_in=None):
+        fq.fp4q_nv_quantize_sr_rne(xg, R3, C3, C3, 1, 7, 1234, amax_in, am, st, q3, q3b, s3, 0, ws, 256, stream)
+    b_both = R3 * C3 * 2 + 2 * (R3 * C3 // 2) + R3 * C3 // 16
+    ms_both = timed(c3_both, 10, True)
+    ms_both1 = timed(lambda: c3_both(amax_dev), 10, True)
     rows["nvfp4_rht_8192x14336"] = {
+        "sr_and_rne_one_call_ms": round(ms_both, 4),
+        "sr_and_rne_one_call_GB_per_s": round((b_amax + b_both) / ms_both / 1e6, 1),
+        "sr_and_rne_separate_calls_ms": round(ms_sr + ms_rne, 4),
+        "sr_rne_quant_pass_ms": round(ms_both1, 4),
+        "sr_rne_quant_pass_GB_per_s": round(b_both / ms_both1 / 1e6, 1),
+        "frac_hbm_sr_rne_quant_pass": round(b_both / ms_both1 / 1e6 / peaks["hbm_gbs"], 3),
         "sr_two_pass_ms": round(ms_sr, 4), "rne_two_pass_ms": round(ms_rne, 4),
         "sr_two_pass_GB_per_s": round((b_amax + b_quant) / ms_sr / 1e6, 1),
         "rne_two_pass_GB_per_s": round((b_amax + b_quant) / ms_rne / 1e6, 1),
@@ -459,7 +474,7 @@ def c3_row(fq, W, torch, peaks, timed, dev_bf16, rows):
         "rne_quant_pass_GB_per_s": round(b_quant / ms_rne1 / 1e6, 1),
         "frac_hbm_rne_quant_pass": round(b_quant / ms_rne1 / 1e6 / peaks["hbm_gbs"], 3),
         "frac_hbm_sr_quant_pass": round(b_quant / ms_sr1 / 1e6 / peaks["hbm_gbs"], 3)}
-    del xg, q3, s3
+    del xg, q3, q3b, s3
 
 
 def gemm_row(fq, W, torch, peaks, timed, dev_bf16, rows):

@@ -223,6 +223,24 @@ fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t cols, int64_t 
                              size_t workspace_bytes, fp4q_stream_t stream);
 
 /*
+ * fp4q_nv_quantize_sr_rne -- one NVFP4 quantization of a BF16 gradient with
+ * both roundings over the same scales: the stochastically rounded codes into
+ * q_sr and the round-to-nearest-even codes into q_rne, from one read of x and
+ * one rotation.  [NVF] 2.B: stochastic rounding on the gradients, the RNE
+ * codes being the deterministic counterpart of the same scaled values.
+ * Results are bit-identical to fp4q_nv_quantize with FP4Q_SR and then with
+ * FP4Q_RNE on the same x, seeds and amax (the scales of the two calls are the
+ * same bytes).  Row-wise blocks only (block_axis 1).
+ *   q_sr, q_rne   device out, [rows, cols/2] each, 16-byte aligned
+ *   other arguments as fp4q_nv_quantize
+ */
+fp4q_status fp4q_nv_quantize_sr_rne(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int rht,
+                                    uint64_t rht_seed, uint64_t sr_seed, const float* amax_in,
+                                    float* amax_out, float* tensor_scale_out, uint8_t* q_sr,
+                                    uint8_t* q_rne, uint8_t* scales, fp4q_scale_layout layout,
+                                    void* workspace, size_t workspace_bytes, fp4q_stream_t stream);
+
+/*
  * fp4q_nv_quantize_2d -- BF16 weights -> NVFP4 with one E4M3 scale per 16 x 16
  * tile.  [NVF] 2.B (two-dimensional scaling): weight blocks of 16 x 16, so that
  * the forward pass and the backward pass, which reads the weight transposed,

@@ -162,11 +162,16 @@ __device__ __forceinline__ uint4 philox_ctr64(uint32_t c0, uint32_t c1, const Ph
     return make_uint4(x, y, z, w);
 }
 
-template <bool SR>
+// Rounding of the quantize pass: kRne, kSr, or kSrRne (both, over the same
+// scales from one read and one rotation: SR codes into q, RNE codes into q2).
+enum NvMode { kRne = 0, kSr = 1, kSrRne = 2 };
+
+template <int MODE>
 __global__ void __launch_bounds__(256) nv_quant_kernel(
     const uint8_t* __restrict__ x, int64_t rows, uint32_t tpr, int64_t ld_x_bytes, int rht,
     uint64_t rht_seed, const PhiloxKeys sr_keys, const float* __restrict__ amax_ptr, float* __restrict__ amax_out,
-    float* __restrict__ st_out, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int mma_layout) {
+    float* __restrict__ st_out, uint8_t* __restrict__ q, uint8_t* __restrict__ q2, uint8_t* __restrict__ s,
+    int mma_layout) {
     const uint32_t signs = rht == 1 ? rht_signs(rht_seed) : 0u;
     const float amax = *amax_ptr;
     const float s_t = __fdiv_rn(amax, 2688.0f);        // 6 * 448
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(
             sb = cvt_e4m3(__fdiv_rn(u2f(ab), denom));
             if (sb & 0x7fu) rcp = __frcp_rn(__fmul_rn(e4m3x2_to_f32x2(sb).x, s_t));
         }
-        uint32_t words[2];
+        uint32_t words[2], words2[2];
         if (rcp == 0.0f) {
             // zero tensor or block scale underflow: signed-zero codes
 #pragma unroll
@@ -198,33 +203,47 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(
 #pragma unroll
                 for (int j = 0; j < 8; ++j) w |= ((f2u(t[8 * k + j]) >> 31) << 3) << (4 * j);
                 words[k] = w;
+                words2[k] = w;
             }
-        } else if constexpr (!SR) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-                words[k] = cvt_e2m1x8(__fmul_rn(t[8 * k], rcp), __fmul_rn(t[8 * k + 1], rcp),
-                                      __fmul_rn(t[8 * k + 2], rcp), __fmul_rn(t[8 * k + 3], rcp),
-                                      __fmul_rn(t[8 * k + 4], rcp), __fmul_rn(t[8 * k + 5], rcp),
-                                      __fmul_rn(t[8 * k + 6], rcp), __fmul_rn(t[8 * k + 7], rcp));
         } else {
-            const uint64_t i0 = uint64_t(r) * cols + uint64_t(b) * 16;   // linear index, % 16 == 0
+            // v = y * (1 / sf), the pairs as packed IEEE products
+            float v[16];
+            const uint64_t rcp2 = f32x2_splat(rcp);
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                uint32_t w = 0;
+            for (int j = 0; j < 16; j += 2) {
+                v[j] = t[j];
+                v[j + 1] = t[j + 1];
+                mul_f32x2(v[j], v[j + 1], rcp2);
+            }
+            if constexpr (MODE != kSr) {
+                uint32_t(&rw)[2] = MODE == kRne ? words : words2;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint64_t ctr = (i0 >> 2) + uint64_t(2 * k + h);
-                    const uint4 rnd = philox_ctr64(uint32_t(ctr), uint32_t(ctr >> 32), sr_keys);
-                    const int base = 8 * k + 4 * h;
-                    const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+                for (int k = 0; k < 2; ++k)
+                    rw[k] = cvt_e2m1x8(v[8 * k], v[8 * k + 1], v[8 * k + 2], v[8 * k + 3], v[8 * k + 4], v[8 * k + 5],
+                                       v[8 * k + 6], v[8 * k + 7]);
+            }
+            if constexpr (MODE != kRne) {
+                const uint64_t i0 = uint64_t(r) * cols + uint64_t(b) * 16;   // linear index, % 16 == 0
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w |= sr_e2m1_code(__fmul_rn(t[base + e], rcp), rr[e]) << (4 * (4 * h + e));
+                for (int k = 0; k < 2; ++k) {
+                    uint32_t w = 0;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t ctr = (i0 >> 2) + uint64_t(2 * k + h);
+                        const uint4 rnd = philox_ctr64(uint32_t(ctr), uint32_t(ctr >> 32), sr_keys);
+                        const int base = 8 * k + 4 * h;
+                        const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) w |= sr_e2m1_code(v[base + e], rr[e]) << (4 * (4 * h + e));
+                    }
+                    words[k] = w;
                 }
-                words[k] = w;
             }
         }
         *reinterpret_cast<uint2*>(q + uint64_t(r) * (cols / 2) + uint64_t(b) * 8) = make_uint2(words[0], words[1]);
+        if constexpr (MODE == kSrRne)
+            *reinterpret_cast<uint2*>(q2 + uint64_t(r) * (cols / 2) + uint64_t(b) * 8) =
+                make_uint2(words2[0], words2[1]);
         const uint64_t so = mma_layout ? mma_scale_offset(uint64_t(r), b, tpr) : uint64_t(r) * tpr + b;
         s[so] = uint8_t(sb);
     };
@@ -559,8 +578,8 @@ extern "C" fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t col
             amax_ptr = reinterpret_cast<const float*>(w);
         }
         if (rows == 0 || cols == 0) {
-            nv_quant_kernel<false><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, keys, amax_ptr, amax_out, tensor_scale_out, q,
-                                                     scales, 0);
+            nv_quant_kernel<kRne><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, keys, amax_ptr, amax_out, tensor_scale_out, q,
+                                                   nullptr, scales, 0);
             return check_launch("nv_quantize");
         }
         CUtensorMap tmap;
@@ -596,17 +615,62 @@ extern "C" fp4q_status fp4q_nv_quantize(const void* x, int64_t rows, int64_t col
     }
     if (rows == 0 || cols == 0) {
         // still publish s_t (and amax) for an empty tensor: both are 0
-        nv_quant_kernel<false><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, keys, amax_ptr, amax_out, tensor_scale_out, q,
-                                                 scales, 0);
+        nv_quant_kernel<kRne><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, keys, amax_ptr, amax_out, tensor_scale_out, q,
+                                               nullptr, scales, 0);
         return check_launch("nv_quantize");
     }
     if (rounding == FP4Q_SR)
-        nv_quant_kernel<true><<<grid_for(nv_quant_kernel<true>), tpb, 0, s>>>(
-            xb, rows, tpr, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out, tensor_scale_out, q, scales, mma);
+        nv_quant_kernel<kSr><<<grid_for(nv_quant_kernel<kSr>), tpb, 0, s>>>(
+            xb, rows, tpr, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out, tensor_scale_out, q, nullptr, scales,
+            mma);
     else
-        nv_quant_kernel<false><<<grid_for(nv_quant_kernel<false>), tpb, 0, s>>>(
-            xb, rows, tpr, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out, tensor_scale_out, q, scales, mma);
+        nv_quant_kernel<kRne><<<grid_for(nv_quant_kernel<kRne>), tpb, 0, s>>>(
+            xb, rows, tpr, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out, tensor_scale_out, q, nullptr, scales,
+            mma);
     return check_launch("nv_quantize");
+}
+
+extern "C" fp4q_status fp4q_nv_quantize_sr_rne(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int rht,
+                                               uint64_t rht_seed, uint64_t sr_seed, const float* amax_in,
+                                               float* amax_out, float* tensor_scale_out, uint8_t* q_sr,
+                                               uint8_t* q_rne, uint8_t* scales, fp4q_scale_layout layout,
+                                               void* workspace, size_t workspace_bytes, fp4q_stream_t stream) {
+    fp4q_status st = nv_prologue("nv_quantize_sr_rne", x, rows, cols, ld_x, FP4Q_SR, amax_in, tensor_scale_out, q_sr,
+                                 scales, layout, workspace, workspace_bytes);
+    if (st != FP4Q_OK) return st;
+    if (rht < 0 || rht > 2) return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize_sr_rne: rht must be 0, 1 or 2");
+    if (rows > 0 && cols > 0 && !q_rne) return fail(FP4Q_ERR_INVALID_ARGUMENT, "nv_quantize_sr_rne: q_rne is NULL");
+    if (q_rne && !aligned16(q_rne)) return fail(FP4Q_ERR_MISALIGNED, "nv_quantize_sr_rne: q_rne 16-byte aligned");
+    int sms = 0;
+    if ((st = current_device(&sms)) != FP4Q_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    const float* amax_ptr = amax_in;
+    const PhiloxKeys keys = philox_keys(sr_seed);
+    const uint32_t tpr = uint32_t(cols / 16);
+    int tpb = 32, nx = 1;
+    if (tpr) row_launch_shape(tpr, &tpb, &nx);
+    auto grid_for = [&](auto kernel) {
+        return dim3(unsigned(nx), row_grid_y(rows, nx, sms, resident_per_sm(kernel, tpb)), 1);
+    };
+    if (!amax_in) {
+        uint32_t* w = static_cast<uint32_t*>(workspace);
+        if ((st = zero_amax_word(w, s, "nv_quantize_sr_rne")) != FP4Q_OK) return st;
+        if (rows > 0 && cols > 0) {
+            nv_amax_kernel<<<grid_for(nv_amax_kernel), tpb, 0, s>>>(xb, rows, tpr, ld_x * 2, rht, rht_seed, w);
+            if ((st = check_launch("nv_quantize_sr_rne amax")) != FP4Q_OK) return st;
+        }
+        amax_ptr = reinterpret_cast<const float*>(w);
+    }
+    if (rows == 0 || cols == 0) {
+        nv_quant_kernel<kRne><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, keys, amax_ptr, amax_out, tensor_scale_out, q_sr,
+                                               nullptr, scales, 0);
+        return check_launch("nv_quantize_sr_rne");
+    }
+    nv_quant_kernel<kSrRne><<<grid_for(nv_quant_kernel<kSrRne>), tpb, 0, s>>>(
+        xb, rows, tpr, ld_x * 2, rht, rht_seed, keys, amax_ptr, amax_out, tensor_scale_out, q_sr, q_rne, scales,
+        layout == FP4Q_SCALES_MMA);
+    return check_launch("nv_quantize_sr_rne");
 }
 
 extern "C" fp4q_status fp4q_nv_quantize_2d(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
@@ -638,8 +702,8 @@ extern "C" fp4q_status fp4q_nv_quantize_2d(const void* x, int64_t rows, int64_t 
         amax_ptr = reinterpret_cast<const float*>(w);
     }
     if (rows == 0 || cols == 0) {
-        nv_quant_kernel<false><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, keys, amax_ptr, amax_out, tensor_scale_out, q,
-                                                 scales, 0);
+        nv_quant_kernel<kRne><<<1, 32, 0, s>>>(xb, 0, 0, 0, 0, 0, keys, amax_ptr, amax_out, tensor_scale_out, q,
+                                               nullptr, scales, 0);
         return check_launch("nv_quantize_2d");
     }
     const int mma = layout == FP4Q_SCALES_MMA;

@@ -34,7 +34,7 @@ EXPORTED = [
     "fp4q_moe_dispatch", "fp4q_rebased_scales_bytes", "fp4q_mx_rebase_scales", "fp4q_grouped_gemm",
     "fp4q_moe_dispatch_static", "fp4q_check_wait_timeout", "fp4q_nv_quantize_2d", "fp4q_fp4_row_to_fp8_col",
     "fp4q_fp8_tile_scales_to_e8m0", "fp4q_fp8_pipeline_host_workspace_bytes", "fp4q_fp8_pipeline_host",
-    "fp4q_stream_status", "fp4q_fp8_pipeline_host_release",
+    "fp4q_stream_status", "fp4q_fp8_pipeline_host_release", "fp4q_nv_quantize_sr_rne",
 ]
 MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 * 1024 * 1024
 
@@ -97,6 +97,8 @@ def load() -> ctypes.CDLL:
                 "fp4q_moe_dispatch_static": [vp, i64, ci, ci, vp, vp, i64, vp, vp, vp, vp, vp],
                 "fp4q_check_wait_timeout": [u64, vp],
                 "fp4q_nv_quantize_2d": [vp, i64, i64, i64, ci, u64, vp, vp, vp, vp, vp, ci, vp, ctypes.c_size_t, vp],
+                "fp4q_nv_quantize_sr_rne": [vp, i64, i64, i64, ci, u64, u64, vp, vp, vp, vp, vp, vp, ci, vp,
+                                            ctypes.c_size_t, vp],
                 "fp4q_fp4_row_to_fp8_col": [vp, vp, i64, i64, vp, vp, vp],
                 "fp4q_fp8_tile_scales_to_e8m0": [vp, i64, i64, vp, ci, vp],
                 "fp4q_fp8_pipeline_host": [vp, vp, i64, i64, vp, vp, vp, vp, i64, vp, ctypes.c_size_t, vp],
@@ -209,6 +211,14 @@ def fp4q_nv_quantize(x, rows, cols, ld_x, block_axis, rht, rht_seed, rounding, s
         _ptr(x), rows, cols, ld_x, block_axis, int(rht), rht_seed, rounding, sr_seed, _ptr(amax_in),
         _ptr(amax_out), _ptr(tensor_scale_out), _ptr(q), _ptr(scales), layout, _ptr(workspace),
         workspace_bytes, _stream(stream)))
+
+
+def fp4q_nv_quantize_sr_rne(x, rows, cols, ld_x, rht, rht_seed, sr_seed, amax_in, amax_out, tensor_scale_out, q_sr,
+                            q_rne, scales, layout, workspace, workspace_bytes, stream=None):
+    return _check("fp4q_nv_quantize_sr_rne", load().fp4q_nv_quantize_sr_rne(
+        _ptr(x), rows, cols, ld_x, int(rht), rht_seed, sr_seed, _ptr(amax_in), _ptr(amax_out),
+        _ptr(tensor_scale_out), _ptr(q_sr), _ptr(q_rne), _ptr(scales), layout, _ptr(workspace), workspace_bytes,
+        _stream(stream)))
 
 
 def fp4q_nv_quantize_2d(x, rows, cols, ld_x, rounding, sr_seed, amax_in, amax_out, tensor_scale_out, q, scales,
@@ -409,6 +419,26 @@ def nv_quantize(x, rht=False, rht_seed=0, rounding=FP4Q_RNE, sr_seed=0, amax=Non
                          s, layout, ws, wsb, stream)
     return {"q": q, "scales": s.view(OR, OC // 16) if layout == FP4Q_SCALES_ROWMAJOR else s, "s_t": st,
             "amax": am}
+
+
+def nv_quantize_sr_rne(x, rht=False, rht_seed=0, sr_seed=0, amax=None, layout=FP4Q_SCALES_ROWMAJOR, stream=None):
+    """BF16 [R, C] -> dict(q_sr, q_rne, scales, s_t, amax): both roundings over one
+    set of scales (fp4q_nv_quantize_sr_rne)."""
+    torch = _torch()
+    _on_device("x", x, rows_strided=True)
+    _on_device("amax", amax)
+    R, C = x.shape
+    q_sr = torch.empty((R, C // 2), dtype=torch.uint8, device=x.device)
+    q_rne = torch.empty((R, C // 2), dtype=torch.uint8, device=x.device)
+    s = torch.empty(fp4q_scales_bytes(R, C // 16, layout), dtype=torch.uint8, device=x.device)
+    st = torch.empty(1, dtype=torch.float32, device=x.device)
+    am = torch.empty(1, dtype=torch.float32, device=x.device)
+    wsb = fp4q_nv_quantize_workspace_bytes(R, C)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=x.device)
+    fp4q_nv_quantize_sr_rne(x, R, C, x.stride(0), int(rht), rht_seed, sr_seed, amax, am, st, q_sr, q_rne, s, layout,
+                            ws, wsb, stream)
+    return {"q_sr": q_sr, "q_rne": q_rne, "scales": s.view(R, C // 16) if layout == FP4Q_SCALES_ROWMAJOR else s,
+            "s_t": st, "amax": am}
 
 
 def gemm(qa, sa, qb, sb, fmt=FP4Q_MXFP4, ts_a=None, ts_b=None, out_dtype=None, stream=None):

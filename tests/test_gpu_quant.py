@@ -358,14 +358,55 @@ def test_nv_quantize_zero_and_tiny(fq, oracle):
     assert np.array_equal(host(r["q"]), ref["q"]) and np.array_equal(host(r["scales"]), ref["s"])
 
 
+@pytest.mark.parametrize("shape", [(1, 16), (5, 48), (64, 256), (129, 1040), (300, 7168)])
+@pytest.mark.parametrize("rht", [0, 1, 2])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_nv_quantize_sr_rne(fq, oracle, shape, rht, layout):
+    """Both roundings from one pass equal the oracle's SR and RNE quantizations
+    of the same tensor (same scales), across tiles, ragged rows and all three
+    rotation modes."""
+    from micro_scaled_fp4_gb300 import workloads as W
+    R, C = shape
+    x = W.gradient_bf16(R, C, seed=R * 7 + C)
+    r = fq.nv_quantize_sr_rne(dev_bf16(x), rht=rht, rht_seed=7, sr_seed=1234, layout=layout)
+    sr = oracle.nv_quantize(x, rht=rht, rht_seed=7, rounding="sr", sr_seed=1234)
+    rne = oracle.nv_quantize(x, rht=rht, rht_seed=7)
+    assert np.array_equal(host(r["q_sr"]), sr["q"])
+    assert np.array_equal(host(r["q_rne"]), rne["q"])
+    sg = host(r["scales"]) if layout == 0 else from_mma_layout(host(r["scales"]), R, C // 16)
+    assert np.array_equal(sg, sr["s"]) and np.array_equal(sg, rne["s"])
+    assert host(r["s_t"])[0] == sr["s_t"] and host(r["amax"])[0] == sr["amax"]
+
+
+def test_nv_quantize_sr_rne_zero_and_given_amax(fq, oracle):
+    """An all-zero tensor (s_t = 0: signed-zero codes in both outputs) and a
+    caller-supplied amax (one pass)."""
+    import torch
+    x = np.zeros((8, 64), dtype=np.uint16)
+    x[3, 5] = 0x8000                                  # -0
+    r = fq.nv_quantize_sr_rne(dev_bf16(x), rht=0, sr_seed=1)
+    ref = oracle.nv_quantize(x)
+    assert np.array_equal(host(r["q_sr"]), ref["q"]) and np.array_equal(host(r["q_rne"]), ref["q"])
+    from micro_scaled_fp4_gb300 import workloads as W
+    xg = W.gradient_bf16(32, 512, seed=9)
+    am = oracle.nv_amax(xg, 1, 7) * 2.0
+    r = fq.nv_quantize_sr_rne(dev_bf16(xg), rht=1, rht_seed=7, sr_seed=5,
+                              amax=torch.tensor([am], dtype=torch.float32, device="cuda"))
+    sr = oracle.nv_quantize(xg, rht=1, rht_seed=7, rounding="sr", sr_seed=5, amax=am)
+    rne = oracle.nv_quantize(xg, rht=1, rht_seed=7, amax=am)
+    assert np.array_equal(host(r["q_sr"]), sr["q"]) and np.array_equal(host(r["q_rne"]), rne["q"])
+    assert np.array_equal(host(r["scales"]), sr["s"])
+
+
 def test_nv_quantize_full_size(fq, oracle):
     """The whole 8192x14336 Student-t(3)*1e-3 gradient with the RHT (seed 7):
-    SR pass (seed 1234) then RNE pass, as the benchmark runs them.  Tensor
-    amax, tensor scale, every code and every scale of both passes equal the
-    oracle's quantization of the whole tensor."""
+    SR pass (seed 1234) then RNE pass, and both from the one-pass call.  Tensor
+    amax, tensor scale, every code and every scale equal the oracle's
+    quantization of the whole tensor."""
     from micro_scaled_fp4_gb300 import workloads as W
     x = W.gradient_bf16()
     xd = dev_bf16(x)
+    both = fq.nv_quantize_sr_rne(xd, rht=True, rht_seed=7, sr_seed=1234)
     for rounding in ("sr", "rne"):
         r = fq.nv_quantize(xd, rht=True, rht_seed=7, rounding=1 if rounding == "sr" else 0, sr_seed=1234)
         ref = oracle.nv_quantize(x, rht=True, rht_seed=7, rounding=rounding, sr_seed=1234)
@@ -373,6 +414,9 @@ def test_nv_quantize_full_size(fq, oracle):
         qg, sg = host(r["q"]), host(r["scales"])
         assert np.count_nonzero(qg != ref["q"]) == 0, rounding
         assert np.count_nonzero(sg != ref["s"]) == 0, rounding
+        # the one-pass form of both roundings, as the benchmark times it
+        assert np.count_nonzero(host(both["q_" + rounding]) != ref["q"]) == 0, rounding
+        assert np.count_nonzero(host(both["scales"]) != ref["s"]) == 0, rounding
         del r, qg, sg, ref
 
 
