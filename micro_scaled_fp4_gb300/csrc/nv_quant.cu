@@ -74,23 +74,59 @@ __device__ __forceinline__ void unpack_tile(const u32x8& a, float (&t)[16]) {
     }
 }
 
+// The sign flips of the RHT as eight pairs of +-1.0 (d_j = -1 iff bit j of
+// `signs`), for packed multiplies: exact, and on the FMA pipe where the bit
+// flips would take the integer pipe.
+struct SignPairs {
+    uint64_t p[8];
+};
+__device__ __forceinline__ SignPairs sign_pairs(uint32_t signs) {
+    SignPairs sp;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float lo = ((signs >> (2 * i)) & 1u) ? -1.0f : 1.0f, hi = ((signs >> (2 * i + 1)) & 1u) ? -1.0f : 1.0f;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(sp.p[i]) : "f"(lo), "f"(hi));
+    }
+    return sp;
+}
+// rht16 with the sign flips given as packed pairs.
+__device__ __forceinline__ void rht16_pairs(float (&t)[16], const SignPairs& sp) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mul_f32x2(t[2 * i], t[2 * i + 1], sp.p[i]);
+    rht16<true>(t, 0u);
+}
+
 __global__ void __launch_bounds__(256) nv_amax_kernel(const uint8_t* __restrict__ x, int64_t rows,
                                                       uint32_t tpr, int64_t ld_x_bytes, int rht,
                                                       uint64_t rht_seed, uint32_t* __restrict__ amax_bits) {
     const uint32_t signs = rht == 1 ? rht_signs(rht_seed) : 0u;
     const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
-    uint32_t m = 0;
+    float fm = 0.0f;
     if (b < tpr) {
-        // (a prefetch of the next row, as in nv_quant_kernel, made this pass
-        // slower: 50.8 -> 54.1 us on the 8192 x 14336 gradient)
-        for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const SignPairs sp = sign_pairs(signs);
+        const uint8_t* col = x + uint64_t(b) * 32;
+        auto take = [&](const u32x8& v) {
             float t[16];
-            unpack_tile(ldg256(x + r * ld_x_bytes + uint64_t(b) * 32), t);
-            if (rht) rht16(t, signs);
+            unpack_tile(v, t);
+            if (rht) rht16_pairs(t, sp);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) m = max(m, f2u(t[j]) & 0x7fffffffu);
+            for (int j = 0; j < 16; ++j) fm = fmaxf(fm, fabsf(t[j]));
+        };
+        // four of the thread's rows per iteration, their loads issued together
+        // (one load in flight per thread left the pass waiting on memory)
+        const int64_t g = gridDim.y;
+        int64_t r = blockIdx.y;
+        for (; r + 3 * g < rows; r += 4 * g) {
+            const u32x8 v0 = ldg256(col + r * ld_x_bytes), v1 = ldg256(col + (r + g) * ld_x_bytes);
+            const u32x8 v2 = ldg256(col + (r + 2 * g) * ld_x_bytes), v3 = ldg256(col + (r + 3 * g) * ld_x_bytes);
+            take(v0);
+            take(v1);
+            take(v2);
+            take(v3);
         }
+        for (; r < rows; r += g) take(ldg256(col + r * ld_x_bytes));
     }
+    uint32_t m = f2u(fm);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     __shared__ uint32_t wmax[8];
@@ -126,6 +162,21 @@ __device__ __forceinline__ uint32_t sr_e2m1_code(float v, uint32_t r) {
     return ((f2u(v) >> 28) & 8u) | (code + (r < thr ? 1u : 0u));
 }
 
+// Magnitude (the low 3 bits) of sr_e2m1_code(v, r); the caller supplies the
+// sign bit, e.g. from the RNE code of the same v (the RNE convert keeps the
+// sign of v, also for results that round to zero).
+__device__ __forceinline__ uint32_t sr_e2m1_mag(float v, uint32_t r) {
+    const float a = fminf(fabsf(v), 6.0f);
+    const uint32_t u = f2u(a);
+    const uint32_t code_hi = uint32_t(max(int(u >> 22) - 252, 1));
+    const uint32_t thr_hi = u << (u >= 0x3f800000u ? 10 : 9);
+    const uint32_t thr_lo = __float2uint_ru(__fmul_rn(a, 8589934592.0f));   // a * 2^33, < 2^32 below 0.5
+    const bool lt_half = u < 0x3f000000u;
+    const uint32_t code = lt_half ? 0u : code_hi;
+    const uint32_t thr = lt_half ? thr_lo : thr_hi;
+    return code + (r < thr ? 1u : 0u);
+}
+
 // The ten round keys of Philox4x32-10 for one seed (key schedule (k0, k1) +=
 // (0x9E3779B9, 0xBB67AE85) per round), computed on the host and passed as a
 // kernel parameter, so that the rounds read them as constants.
@@ -146,16 +197,18 @@ inline PhiloxKeys philox_keys(uint64_t seed) {
 }
 
 // Philox4x32-10 of the counter (c0, c1, 0, 0) under the keys K: each round is
-// two 32 x 32 -> 64-bit products and two three-way XORs.
+// two 32 x 32 -> 64-bit products (as separate high and low halves, 2 % faster
+// in the SR pass than 64-bit products) and two three-way XORs.
 __device__ __forceinline__ uint4 philox_ctr64(uint32_t c0, uint32_t c1, const PhiloxKeys& K) {
     uint32_t x = c0, y = c1, z = 0, w = 0;
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
-        const uint64_t p0 = uint64_t(0xD2511F53u) * x, p1 = uint64_t(0xCD9E8D57u) * z;
-        const uint32_t nx = uint32_t(p1 >> 32) ^ y ^ K.k0[i];
-        const uint32_t nz = uint32_t(p0 >> 32) ^ w ^ K.k1[i];
-        y = uint32_t(p1);
-        w = uint32_t(p0);
+        const uint32_t h0 = __umulhi(0xD2511F53u, x), l0 = 0xD2511F53u * x;
+        const uint32_t h1 = __umulhi(0xCD9E8D57u, z), l1 = 0xCD9E8D57u * z;
+        const uint32_t nx = h1 ^ y ^ K.k0[i];
+        const uint32_t nz = h0 ^ w ^ K.k1[i];
+        y = l1;
+        w = l0;
         x = nx;
         z = nz;
     }
@@ -183,11 +236,13 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(
     const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= tpr) return;
     const uint64_t cols = uint64_t(tpr) * 16;
+    const SignPairs sp = sign_pairs(signs);
     auto quantize_row = [&](int64_t r, float (&t)[16]) {
-        if (rht) rht16(t, signs);
-        uint32_t ab = 0;
+        if (rht) rht16_pairs(t, sp);
+        float am = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) ab = max(ab, f2u(t[j]) & 0x7fffffffu);
+        for (int j = 0; j < 16; ++j) am = fmaxf(am, fabsf(t[j]));
+        const uint32_t ab = f2u(am);
         uint32_t sb = 0;
         float rcp = 0.0f;
         if (s_t > 0.0f) {
@@ -215,18 +270,17 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(
                 v[j + 1] = t[j + 1];
                 mul_f32x2(v[j], v[j + 1], rcp2);
             }
-            if constexpr (MODE != kSr) {
-                uint32_t(&rw)[2] = MODE == kRne ? words : words2;
+            // RNE codes: every mode computes them, the SR codes take their signs
+            uint32_t(&rw)[2] = MODE == kRne ? words : words2;
 #pragma unroll
-                for (int k = 0; k < 2; ++k)
-                    rw[k] = cvt_e2m1x8(v[8 * k], v[8 * k + 1], v[8 * k + 2], v[8 * k + 3], v[8 * k + 4], v[8 * k + 5],
-                                       v[8 * k + 6], v[8 * k + 7]);
-            }
+            for (int k = 0; k < 2; ++k)
+                rw[k] = cvt_e2m1x8(v[8 * k], v[8 * k + 1], v[8 * k + 2], v[8 * k + 3], v[8 * k + 4], v[8 * k + 5],
+                                   v[8 * k + 6], v[8 * k + 7]);
             if constexpr (MODE != kRne) {
                 const uint64_t i0 = uint64_t(r) * cols + uint64_t(b) * 16;   // linear index, % 16 == 0
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
-                    uint32_t w = 0;
+                    uint32_t w = words2[k] & 0x88888888u;                    // the signs
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const uint64_t ctr = (i0 >> 2) + uint64_t(2 * k + h);
@@ -234,7 +288,7 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(
                         const int base = 8 * k + 4 * h;
                         const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) w |= sr_e2m1_code(v[base + e], rr[e]) << (4 * (4 * h + e));
+                        for (int e = 0; e < 4; ++e) w += sr_e2m1_mag(v[base + e], rr[e]) << (4 * (4 * h + e));
                     }
                     words[k] = w;
                 }
@@ -371,8 +425,10 @@ __global__ void __launch_bounds__(256) nv_quant_2d_kernel(
                 t[2 * i] = u2f(cur.v[i] << 16);
                 t[2 * i + 1] = u2f(cur.v[i] & 0xffff0000u);
             }
+            float fm = 0.0f;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) ab = max(ab, f2u(t[e]) & 0x7fffffffu);
+            for (int e = 0; e < 16; ++e) fm = fmaxf(fm, fabsf(t[e]));
+            ab = f2u(fm);
         }
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) ab = max(ab, __shfl_xor_sync(0xffffffffu, ab, o));
@@ -465,12 +521,13 @@ __global__ void __launch_bounds__(ring::kMaxThreads, MODE == 2 ? 2 : 3) nv_col_k
             rht16<true>(a, signs);
             rht16<true>(b, signs);
         }
-        uint32_t ma = 0, mb = 0;
+        float fa = 0.0f, fb = 0.0f;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            ma = max(ma, f2u(a[j]) & 0x7fffffffu);
-            mb = max(mb, f2u(b[j]) & 0x7fffffffu);
+            fa = fmaxf(fa, fabsf(a[j]));
+            fb = fmaxf(fb, fabsf(b[j]));
         }
+        const uint32_t ma = f2u(fa), mb = f2u(fb);
         if constexpr (MODE == 0) {
             m_all = max(m_all, max(ma, mb));
         } else {
