@@ -604,16 +604,26 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         const int et = int(threadIdx.x) - 64;            // epilogue thread 0..255
         const float dense_alpha = (!args.groups && args.nv) ? __fmul_rn(*args.ts_a, *args.ts_b) : 1.0f;
         // the accumulator goes back to the MMA thread: one arrival per warp, on the
-        // even CTA's barrier for the pair
+        // even CTA's barrier for the pair.  The arrival follows tcgen05.wait::ld
+        // and publishes no memory, so it is relaxed.
         const uint32_t acc_empty = PAIR ? tc::map_to_rank(tmem_empty, 0) : tmem_empty;
         auto release_acc = [&]() {
             if constexpr (PAIR)
-                tc::mbar_arrive_cluster(acc_empty);
+                tc::mbar_arrive_cluster_relaxed(acc_empty);
             else
                 tc::mbar_arrive(acc_empty);
         };
         int tcount = 0;
         for (int tile = unit0; tile < num_tiles; tile += unit_step, ++tcount) {
+            // The tile's coordinates and row factor come first, while the MMAs
+            // still run: after the accumulator arrives they took ~650 cycles of
+            // the hand-off in which the tensor pipe waits.
+            const TileInfo t = decode(tile);
+            const int row = t.a_row0 + q * 32 + lane;
+            const bool row_ok = row < t.row_end;
+            float alpha = dense_alpha;
+            if (args.groups && row_ok) alpha = __fmul_rn(args.a_row_scale[row], args.ts_b[t.group]);
+            const uint32_t lane_addr = tmem + (uint32_t(q * 32) << 16);
             // The eight warps decide together whether the tile goes ahead: a warp
             // that gave up while another saw the accumulator arrive would leave
             // that one alone at the staging barriers below.
@@ -623,12 +633,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 break;
             }
             tc::fence_after_sync();
-            const TileInfo t = decode(tile);
-            const int row = t.a_row0 + q * 32 + lane;
-            const bool row_ok = row < t.row_end;
-            float alpha = dense_alpha;
-            if (args.groups && row_ok) alpha = __fmul_rn(args.a_row_scale[row], args.ts_b[t.group]);
-            const uint32_t lane_addr = tmem + (uint32_t(q * 32) << 16);
             if constexpr (EPI == kSiluGate) {
                 // h columns [64 hf, 64 hf + 64) of the tile: gate accumulator columns
                 // 64 hf + j, up columns 128 + 64 hf + j
@@ -717,41 +721,44 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                        t.a_row0 + BM <= t.row_end + (args.groups ? 0 : BM)) {
                 // BF16 through shared memory and TMA stores.  Each warp moves its 32 rows
                 // x 128 columns out of TMEM into registers, then the accumulator goes
-                // back to the MMA thread; half 0 is staged and stored, then half 1.
+                // back to the MMA thread.  The tile leaves in four 64-column quarters
+                // through the two staging boxes in turn: quarter q is staged while the
+                // store of quarter q - 1 reads the other box (with whole 128-column
+                // halves, staging waited for each half's store to have read the
+                // staging: ~5500 cycles per tile, more than the MMAs of a K = 2048 tile).
+                // The four loads go out together and the accumulator goes back before
+                // any conversion: with the BF16 conversion between the loads, the read
+                // phase took ~2500 cycles per tile, all of it idle tensor pipe.
                 const int srow = q * 32 + lane;                  // row within the tile
-                uint32_t hold[4][16];
+                uint32_t raw[4][32];
 #pragma unroll
-                for (int c = 0; c < 4; c += 2) {
-                    uint32_t r0[32], r1[32];
-                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(128 * hf + 32 * c), r0);
-                    tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(128 * hf + 32 * c + 32), r1);
-                    tc::tmem_ld_wait();
-                    to_bf16x32(r0, alpha, hold[c]);
-                    to_bf16x32(r1, alpha, hold[c + 1]);
-                }
+                for (int c = 0; c < 4; ++c) tc::tmem_ld_32x32b_x32(lane_addr + uint32_t(128 * hf + 32 * c), raw[c]);
+                tc::tmem_ld_wait();
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) release_acc();
-                if (et == 0) tc::bulk_wait_read0();              // previous tile's stores have read the staging
-                tc::named_bar_sync(1, 256);
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    if (hf == h2) {
+                for (int qq = 0; qq < 4; ++qq) {
+                    const int box = qq & 1;
+                    // the box's previous store (two quarters ago, possibly the previous
+                    // tile's) has read it: at most one store group still reading
+                    if (et == 0) tc::bulk_wait_read1();
+                    tc::named_bar_sync(1, 256);
+                    if (hf == (qq >> 1)) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) stage_bf16x32(staging, srow, c, hold[c]);
+                        for (int cc = 2 * box; cc < 2 * box + 2; ++cc) {
+                            uint32_t p[16];
+                            to_bf16x32(raw[cc], alpha, p);
+                            stage_bf16x32(staging, srow, cc, p);
+                        }
                     }
                     tc::fence_proxy_async_smem();
                     tc::named_bar_sync(1, 256);
                     if (et == 0) {
-                        for (int b = 0; b < 2; ++b) {
-                            const int col = t.col0 + 128 * h2 + 64 * b;
-                            if (col < args.N)
-                                tc::tma_store_2d(&tmap_d, staging + uint32_t(b) * BOX_BYTES, col, t.a_row0);
-                        }
+                        const int col = t.col0 + 64 * qq;
+                        if (col < args.N) tc::tma_store_2d(&tmap_d, staging + uint32_t(box) * BOX_BYTES, col, t.a_row0);
                         tc::bulk_commit();
-                        if (h2 == 0) tc::bulk_wait_read0();
                     }
-                    if (h2 == 0) tc::named_bar_sync(1, 256);
                 }
             } else {
                 // direct stores (FP32 output, or a tile that ends inside its group)
