@@ -59,6 +59,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "common.cuh"
 #include "tc.cuh"
@@ -460,76 +461,87 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         uint32_t phase = 0;
         int tcount = 0;
         bool ok = true;
-        for (int tile = unit0; tile < num_tiles && ok; tile += unit_step, ++tcount) {
-            const bool got = PAIR ? tc::mbar_wait_cluster(tmem_empty, (tcount & 1) ^ 1, abort, kWaitLimitNs)
-                                  : tc::mbar_wait(tmem_empty, (tcount & 1) ^ 1, abort, kWaitLimitNs);
-            if (!got) {
-                flag_abort(abort, args.status, args.status_bit);
-                break;
-            }
-            tc::fence_after_sync();
-            for (int kb = 0; kb < args.k_stages; ++kb) {
-                // The copy thread released the stage: its tiles have landed (for the
-                // pair, both CTAs' bytes) and its scales are in the stage's TMEM
-                // buffer.
-                if (!tc::mbar_wait(copied_bar(stage), phase, abort, kWaitLimitNs)) {
-                    flag_abort(abort, args.status, args.status_bit);
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-                const int k_elems = min(args.bk, args.K - kb * args.bk);
+        // This one thread's instruction stream paces the tensor pipe (a stage's
+        // four MMAs take 512 cycles; with the operand format decided per stage the
+        // thread needed ~700), so the loop is specialised per format: no format or
+        // K-tail test inside a full stage.
+        auto run = [&](auto fmt) {
+            constexpr int F = decltype(fmt)::value;                  // 0 MXFP4, 1 NVFP4, 2 MXFP8
+            // MMAs of stage `kb`: NM of them (K = 64 each for FP4, 32 for FP8)
+            auto issue = [&](int kb, auto nm) {
+                constexpr uint32_t NM = decltype(nm)::value;
                 // descriptors of this stage: the 14-bit address field (bytes >> 4)
                 // of the stage-0 descriptors advanced by the stage offset
                 const uint32_t so = uint32_t(stage) * (LY::stage_bytes >> 4);
-                const uint32_t a_lo = d_lo0 + so, b_lo = d_lo0 + so + (A_BYTES >> 4);
+                const uint32_t a_lo = d_lo0 + so, b_lo = a_lo + (A_BYTES >> 4);
                 // the stage's scale buffer: A chunk c at sfa + 4 c, B half h chunk c at sfb + 8 c + 4 h
                 const uint32_t sfa = tmem + TMEM_SF + SF_COLS * uint32_t(stage), sfb = sfa + 16u;
-                // The full-stage paths are unrolled with constant counts: this one
-                // thread's instruction stream paces the tensor pipe.
-                if (args.f8) {
-                    // 128 FP8 elements: one scale chunk (A) and one per B half, four K = 32 MMAs
-                    const uint32_t id[4] = {idesc_f8_0, idesc_f8_1, idesc_f8_2, idesc_f8_3};
 #pragma unroll
-                    for (uint32_t j = 0; j < 4; ++j)
-                        tc::mma_mxf8_g<CG>(tmem, tc::desc_from(a_lo + 2 * j, d_hi), tc::desc_from(b_lo + 2 * j, d_hi),
-                                           id[j], sfa, sfb, (kb | int(j)) ? 1u : 0u);
-                } else if (k_elems == BK) {
-                    if (args.nv) {
-                        // NVFP4: MMA j (64 K elements) takes scale chunk j (4 x 16)
-#pragma unroll
-                        for (uint32_t j = 0; j < 4; ++j)
-                            tc::mma_nvf4_g<CG>(tmem, tc::desc_from(a_lo + 2 * j, d_hi), tc::desc_from(b_lo + 2 * j, d_hi),
-                                               idesc_nv, sfa + 4 * j, sfb + 8 * j, (kb | int(j)) ? 1u : 0u);
+                for (uint32_t j = 0; j < NM; ++j) {
+                    const uint64_t da = tc::desc_from(a_lo + 2 * j, d_hi), db = tc::desc_from(b_lo + 2 * j, d_hi);
+                    const uint32_t acc = (kb | int(j)) ? 1u : 0u;
+                    if constexpr (F == 2) {
+                        // FP8: one scale chunk (A) and one per B half; MMA j reads byte j of each scale column
+                        const uint32_t id = j == 0 ? idesc_f8_0 : j == 1 ? idesc_f8_1 : j == 2 ? idesc_f8_2 : idesc_f8_3;
+                        tc::mma_mxf8_g<CG>(tmem, da, db, id, sfa, sfb, acc);
+                    } else if constexpr (F == 1) {
+                        // NVFP4: MMA j takes scale chunk j (4 x 16)
+                        tc::mma_nvf4_g<CG>(tmem, da, db, idesc_nv, sfa + 4 * j, sfb + 8 * j, acc);
                     } else {
                         // MXFP4: MMA j takes half of chunk j / 2 (scale ids 0 / 2: its first or second pair)
-#pragma unroll
-                        for (uint32_t j = 0; j < 4; ++j)
-                            tc::mma_mxf4_g<CG>(tmem, tc::desc_from(a_lo + 2 * j, d_hi), tc::desc_from(b_lo + 2 * j, d_hi),
-                                               (j & 1) ? idesc_mx1 : idesc_mx0, sfa + 4 * (j >> 1), sfb + 8 * (j >> 1),
-                                               (kb | int(j)) ? 1u : 0u);
-                    }
-                } else {
-                    // K tail: 128 elements (K % 256 == 128)
-                    const uint32_t nmma = uint32_t(k_elems) / 64;
-                    for (uint32_t j = 0; j < nmma; ++j) {
-                        const uint64_t da = tc::desc_from(a_lo + 2 * j, d_hi), db = tc::desc_from(b_lo + 2 * j, d_hi);
-                        const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
-                        if (args.nv)
-                            tc::mma_nvf4_g<CG>(tmem, da, db, idesc_nv, sfa + 4 * j, sfb + 8 * j, acc);
-                        else
-                            tc::mma_mxf4_g<CG>(tmem, da, db, (j & 1) ? idesc_mx1 : idesc_mx0, sfa + 4 * (j >> 1),
-                                               sfb + 8 * (j >> 1), acc);
+                        tc::mma_mxf4_g<CG>(tmem, da, db, (j & 1) ? idesc_mx1 : idesc_mx0, sfa + 4 * (j >> 1),
+                                           sfb + 8 * (j >> 1), acc);
                     }
                 }
+            };
+            // The copy thread released the stage: its tiles have landed (for the
+            // pair, both CTAs' bytes) and its scales are in the stage's TMEM buffer.
+            auto stage_ready = [&]() {
+                if (!tc::mbar_wait(copied_bar(stage), phase, abort, kWaitLimitNs)) {
+                    flag_abort(abort, args.status, args.status_bit);
+                    ok = false;
+                    return false;
+                }
+                tc::fence_after_sync();
+                return true;
+            };
+            auto stage_done = [&]() {
                 tc::tc_commit_g<CG>(empty_bar(stage), kBoth);     // the stage is free (in both CTAs)
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            };
+            // FP4 stages hold 256 K elements; a K % 256 == 128 tail is one last
+            // stage of two MMAs.  FP8 stages (128 elements) are always full.
+            const int full = F == 2 ? args.k_stages : args.K / BK;
+            for (int tile = unit0; tile < num_tiles && ok; tile += unit_step, ++tcount) {
+                const bool got = PAIR ? tc::mbar_wait_cluster(tmem_empty, (tcount & 1) ^ 1, abort, kWaitLimitNs)
+                                      : tc::mbar_wait(tmem_empty, (tcount & 1) ^ 1, abort, kWaitLimitNs);
+                if (!got) {
+                    flag_abort(abort, args.status, args.status_bit);
+                    break;
+                }
+                tc::fence_after_sync();
+                for (int kb = 0; kb < full; ++kb) {
+                    if (!stage_ready()) break;
+                    issue(kb, std::integral_constant<uint32_t, 4>{});
+                    stage_done();
+                }
+                if (F != 2 && ok && full < args.k_stages) {
+                    if (stage_ready()) {
+                        issue(full, std::integral_constant<uint32_t, 2>{});
+                        stage_done();
+                    }
+                }
+                if (!ok) break;
+                tc::tc_commit_g<CG>(tmem_full, kBoth);
             }
-            if (!ok) break;
-            tc::tc_commit_g<CG>(tmem_full, kBoth);
-        }
-        // drain: all MMAs and scale copies of this thread complete (a CTA that got
-        // no tile issued none)
+        };
+        if (args.f8)
+            run(std::integral_constant<int, 2>{});
+        else if (args.nv)
+            run(std::integral_constant<int, 1>{});
+        else
+            run(std::integral_constant<int, 0>{});
+        // drain: all MMAs of this thread complete (a CTA that got no tile issued none)
         if (tcount > 0 || !ok) {
             tc::tc_commit_g<CG>(drain_bar, 0x1);
             if (!tc::mbar_wait_drain(drain_bar, 0, kWaitLimitNs)) flag_abort(abort, args.status, args.status_bit);
