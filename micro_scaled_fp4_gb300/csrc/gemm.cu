@@ -101,7 +101,7 @@ struct Layout {
     static constexpr uint32_t prefix_off = bars_off + 256;
     static constexpr uint32_t smem_bytes = prefix_off + 8 * 260 + 1024;
     static_assert(smem_bytes <= 232448, "GEMM shared memory above the 227 KB per-CTA limit");
-    static_assert(3 * NST + 5 <= 24, "barriers overlap the TMEM slot");
+    static_assert(4 * NST + 5 <= 30, "barriers overlap the TMEM slot");
     static_assert(TMEM_SF + SF_COLS * NST <= 512, "scale buffers beyond the TMEM allocation");
 };
 constexpr int kThreads = 384;          // producer warp, MMA warp, 8 epilogue warps, 2 scale-copy warps
@@ -282,10 +282,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::bars_off);
-    // bars[0..STAGES) full, [STAGES..2 STAGES) empty, then tmem_full, tmem_empty, mma drain,
-    // [2 STAGES + 3 .. 3 STAGES + 3) scales copied, then the two copy threads' drains
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
-    volatile int* abort = reinterpret_cast<volatile int*>(bars + 25);
+    // bars[0..STAGES) operands landed, [STAGES..2 STAGES) empty, then tmem_full,
+    // tmem_empty, mma drain, [2 STAGES + 3 .. 3 STAGES + 3) scales copied, the two
+    // copy threads' drains, [3 STAGES + 5 .. 4 STAGES + 5) scales landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 30);
+    volatile int* abort = reinterpret_cast<volatile int*>(bars + 31);
     int* tile_prefix = reinterpret_cast<int*>(smem + LY::prefix_off);
     int* pair_prefix = tile_prefix + 260;
     const uint32_t staging = tc::smem_u32(smem + LY::staging_off);
@@ -295,6 +296,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto copied_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 3 + s); };
+    auto sfull_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + 5 + s); };
     const uint32_t tmem_full = bar0 + 8u * (2 * STAGES), tmem_empty = bar0 + 8u * (2 * STAGES + 1),
                    drain_bar = bar0 + 8u * (2 * STAGES + 2), cp_drain_bar = bar0 + 8u * (3 * STAGES + 3);
 
@@ -303,6 +305,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             tc::mbar_init(full_bar(s), 1);
             tc::mbar_init(empty_bar(s), 1);
             tc::mbar_init(copied_bar(s), 2);     // both copy threads' commits
+            tc::mbar_init(sfull_bar(s), 1);
         }
         tc::mbar_init(tmem_full, 1);
         // one arrival per epilogue warp (the pair: the even CTA's barrier takes both CTAs' warps)
@@ -382,39 +385,47 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     // this CTA's A rows, B half `crank` and the scales of its A rows and
                     // of both B halves (an absent second half takes the first's scale
                     // tile: its columns are not stored); the bytes count on the even
-                    // CTA's full barrier, which expects both CTAs' boxes (every box
-                    // lands in full, zero-filled where it leaves the tensor)
-                    const uint32_t fbp = tc::map_to_rank(fb, 0);
-                    if (leader) tc::mbar_arrive_expect_tx(fb, 2u * (A_BYTES + B_HALF_BYTES + 3u * args.sf_box_bytes));
+                    // CTA's barriers, which expect both CTAs' boxes (every box lands in
+                    // full, zero-filled where it leaves the tensor).  The scales go
+                    // first and count on their own barrier: their copies to TMEM then
+                    // overlap the operands' landing instead of following it.
+                    const uint32_t fbp = tc::map_to_rank(fb, 0), sbp = tc::map_to_rank(sfull_bar(stage), 0);
+                    if (leader) {
+                        tc::mbar_arrive_expect_tx(sfull_bar(stage), 2u * 3u * args.sf_box_bytes);
+                        tc::mbar_arrive_expect_tx(fb, 2u * (A_BYTES + B_HALF_BYTES));
+                    }
                     const int brow = crank ? (t.b_row1 >= 0 ? t.b_row1 : t.b_row0 + 128) : t.b_row0;
                     const int bsf1 = (t.b_row1 >= 0 ? t.b_row1 : t.b_row0) / 128;
                     const uint64_t ck = ct0 * 512u;            // byte offset in a scale tile
+                    tc::tma_load_2d_pair(tc::smem_u32(st + LY::sfa_off), &tmap_sfa, sbp, 0,
+                                         int((uint64_t(t.a_sf_tile) * args.sf_tile_stride + ck) / 256u));
+                    tc::tma_load_2d_pair(tc::smem_u32(sfb_smem), &tmap_sfb, sbp, 0,
+                                         int((uint64_t(t.b_row0 / 128) * args.sf_tile_stride + ck) / 256u));
+                    tc::tma_load_2d_pair(tc::smem_u32(sfb_smem + 4 * 512), &tmap_sfb, sbp, 0,
+                                         int((uint64_t(bsf1) * args.sf_tile_stride + ck) / 256u));
                     tc::tma_load_2d_pair(tc::smem_u32(st), &tmap_a, fbp, kb * 128, t.a_row0);
                     tc::tma_load_2d_pair(tc::smem_u32(st + A_BYTES), &tmap_b, fbp, kb * 128, brow);
-                    tc::tma_load_2d_pair(tc::smem_u32(st + LY::sfa_off), &tmap_sfa, fbp, 0,
-                                         int((uint64_t(t.a_sf_tile) * args.sf_tile_stride + ck) / 256u));
-                    tc::tma_load_2d_pair(tc::smem_u32(sfb_smem), &tmap_sfb, fbp, 0,
-                                         int((uint64_t(t.b_row0 / 128) * args.sf_tile_stride + ck) / 256u));
-                    tc::tma_load_2d_pair(tc::smem_u32(sfb_smem + 4 * 512), &tmap_sfb, fbp, 0,
-                                         int((uint64_t(bsf1) * args.sf_tile_stride + ck) / 256u));
                 } else {
-                    tc::mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + sf_bytes);
-                    // x coordinate in bytes: 128 bytes of K per stage for both element widths
-                    tc::tma_load_2d(tc::smem_u32(st), &tmap_a, fb, kb * 128, t.a_row0);
+                    // scales first, on their own barrier (as in the paired form)
+                    const uint32_t sb = sfull_bar(stage);
+                    tc::mbar_arrive_expect_tx(sb, sf_bytes);
+                    tc::mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
                     tc::bulk_load(tc::smem_u32(st + LY::sfa_off),
                                   args.sfa + uint64_t(t.a_sf_tile) * args.sf_tile_stride + ct0 * 512u, chunks * 512u,
-                                  fb);
+                                  sb);
+                    tc::bulk_load(tc::smem_u32(sfb_smem),
+                                  args.sfb + uint64_t(t.b_row0 / 128) * args.sf_tile_stride + ct0 * 512u,
+                                  chunks * 512u, sb);
+                    if (t.b_row1 >= 0)
+                        tc::bulk_load(tc::smem_u32(sfb_smem + 4 * 512),
+                                      args.sfb + uint64_t(t.b_row1 / 128) * args.sf_tile_stride + ct0 * 512u,
+                                      chunks * 512u, sb);
+                    // x coordinate in bytes: 128 bytes of K per stage for both element widths
+                    tc::tma_load_2d(tc::smem_u32(st), &tmap_a, fb, kb * 128, t.a_row0);
                     tc::tma_load_2d(tc::smem_u32(st + A_BYTES), &tmap_b, fb, kb * 128, t.b_row0);
                     // an absent second half still lands: rows past the end are zero-filled
                     tc::tma_load_2d(tc::smem_u32(st + A_BYTES + B_HALF_BYTES), &tmap_b, fb, kb * 128,
                                     t.b_row1 >= 0 ? t.b_row1 : t.b_row0 + 128);
-                    tc::bulk_load(tc::smem_u32(sfb_smem),
-                                  args.sfb + uint64_t(t.b_row0 / 128) * args.sf_tile_stride + ct0 * 512u,
-                                  chunks * 512u, fb);
-                    if (t.b_row1 >= 0)
-                        tc::bulk_load(tc::smem_u32(sfb_smem + 4 * 512),
-                                      args.sfb + uint64_t(t.b_row1 / 128) * args.sf_tile_stride + ct0 * 512u,
-                                      chunks * 512u, fb);
                 }
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -433,7 +444,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         } else {
             for (int i = 0; i < STAGES && i < issued; ++i) {
                 if (--stage < 0) { stage = STAGES - 1; phase ^= 1; }
-                if (!tc::mbar_wait_drain(full_bar(stage), phase, kWaitLimitNs)) {
+                if (!tc::mbar_wait_drain(full_bar(stage), phase, kWaitLimitNs) ||
+                    !tc::mbar_wait_drain(sfull_bar(stage), phase, kWaitLimitNs)) {
                     flag_abort(abort, args.status, args.status_bit);
                     break;
                 }
@@ -494,10 +506,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                     }
                 }
             };
-            // The copy thread released the stage: its tiles have landed (for the
-            // pair, both CTAs' bytes) and its scales are in the stage's TMEM buffer.
+            // The stage's operand tiles have landed (for the pair, both CTAs'
+            // bytes) and the copy threads have put its scales in its TMEM buffer.
+            // The two are separate barriers: the scales land first and their
+            // copies overlap the operands' landing (with one barrier for both, a
+            // stage went round the ring in ~3600 cycles, landing 1650 and copies
+            // 780 of them; this thread has the time for a second wait).
             auto stage_ready = [&]() {
-                if (!tc::mbar_wait(copied_bar(stage), phase, abort, kWaitLimitNs)) {
+                if (!tc::mbar_wait(full_bar(stage), phase, abort, kWaitLimitNs) ||
+                    !tc::mbar_wait(copied_bar(stage), phase, abort, kWaitLimitNs)) {
                     flag_abort(abort, args.status, args.status_bit);
                     ok = false;
                     return false;
@@ -548,13 +565,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         }
     } else if (warp >= 10 && lane == 0 && leader) {
         // ---------------- scale copies (the pair: the even CTA's) ----------------
-        // Per stage, once its bytes have landed: the 512-byte scale chunks (128
+        // Per stage, once its scales have landed: the 512-byte scale chunks (128
         // rows x 4 scales) into the stage's TMEM buffer, replicated to the four
         // lane quadrants (for the pair, each CTA's chunks into its own TMEM) -- A
         // chunk c at column 4 c, B half h chunk c at 16 + 8 c + 4 h -- then a
-        // commit releases the stage to the MMA thread.  Copy thread `half`
-        // takes chunks [half n / 2, (half + 1) n / 2) of the stage's n (one
-        // chunk: thread 0 the A chunk and B's first half, thread 1 B's second).
+        // commit on the stage's copied barrier, which the MMA thread waits for
+        // besides the operands' barrier.  Copy thread `half` takes chunks
+        // [half n / 2, (half + 1) n / 2) of the stage's n (one chunk: thread 0
+        // the A chunk and B's first half, thread 1 B's second).
         // The buffer's previous contents were read by the MMAs of that stage's
         // previous fill, which completed before the stage was refilled.
         const uint32_t half = uint32_t(warp - 10);
@@ -566,7 +584,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         bool ok = true;
         for (int tile = unit0; tile < num_tiles && ok; tile += unit_step) {
             for (int kb = 0; kb < args.k_stages; ++kb) {
-                if (!tc::mbar_wait(full_bar(stage), phase, abort, kWaitLimitNs)) {
+                if (!tc::mbar_wait(sfull_bar(stage), phase, abort, kWaitLimitNs)) {
                     flag_abort(abort, args.status, args.status_bit);
                     ok = false;
                     break;
