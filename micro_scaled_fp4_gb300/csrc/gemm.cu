@@ -76,33 +76,49 @@ constexpr int BM = 128, BN = 256, BK = 256;           // elements
 constexpr uint32_t A_BYTES = BM * BK / 2;             // 16384
 constexpr uint32_t B_HALF_BYTES = 128 * BK / 2;       // 16384
 constexpr uint32_t B_BYTES = 2 * B_HALF_BYTES;
-constexpr uint32_t SFA_BYTES = 4 * 512;               // up to 4 chunks (NVFP4)
-constexpr uint32_t SFB_BYTES = 2 * 4 * 512;           // 2 halves x 4 chunks
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;   // 55296
-constexpr uint32_t PAIR_STAGE_BYTES = A_BYTES + B_HALF_BYTES + SFA_BYTES + SFB_BYTES;   // 38912
 // BF16 output staging: two 64-column x 128-row boxes, rows of 128 bytes with the
 // TMA 128-byte swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)).
 constexpr uint32_t BOX_BYTES = 128 * 128;             // 64 BF16 columns x 128 rows
 // TMEM: FP32 accumulator in columns 0-255, then one block-scale buffer per
-// ring stage (A: 4 chunks x 4 columns, B: 2 halves x 4 chunks x 4 columns).
+// ring stage (A: n chunks x 4 columns, B: 2 halves x n chunks x 4 columns,
+// n = 4 or, in the six-stage layout, 2).
 constexpr uint32_t TMEM_SF = 256;
-constexpr uint32_t SF_COLS = 48;
 // Per-CTA shared memory: NST ring stages [A | B (the pair: one half) | A
 // scales | B scales], the BF16 staging boxes, barriers, the group prefix sums.
+//
+// Six stages (paired, dense MXFP4 only): the ring is latency-bound -- a stage
+// takes ~3400 cycles from its refill to its release, of which the landing from
+// L2 is ~1650 -- so a sixth stage buys ~15 % on long K.  It fits by holding
+// MXFP4's scales only (2 chunks of A and of each B half), one staging box, no
+// group prefix sums and no alignment slack: the kernel requires its dynamic
+// shared memory to start on a 1024-byte boundary (it does: after the 1 KB the
+// hardware reserves) and reports an error otherwise.
 template <int NST, bool PAIR>
 struct Layout {
-    static constexpr uint32_t stage_bytes = PAIR ? PAIR_STAGE_BYTES : STAGE_BYTES;
+    static constexpr bool mx_only = NST == 6;
+    static constexpr uint32_t sf_chunks = mx_only ? 2 : 4;          // scale chunks per 128 rows a stage holds
+    static constexpr uint32_t sfa_bytes = sf_chunks * 512;
+    static constexpr uint32_t sfb_half_bytes = sf_chunks * 512;
+    static constexpr uint32_t stage_bytes = A_BYTES + (PAIR ? B_HALF_BYTES : B_BYTES) + sfa_bytes + 2 * sfb_half_bytes;
     static constexpr uint32_t sfa_off = A_BYTES + (PAIR ? B_HALF_BYTES : B_BYTES);
-    static constexpr uint32_t sfb_off = sfa_off + SFA_BYTES;
-    static constexpr bool staged_store = NST * stage_bytes + 2 * BOX_BYTES + 256 + 8 * 260 + 1024 <= 232448;
-    static constexpr uint32_t staging_bytes = staged_store ? 2 * BOX_BYTES : 0;
+    static constexpr uint32_t sfb_off = sfa_off + sfa_bytes;
+    // TMEM columns per stage: A chunk c at 4 c, B half h chunk c at sfb_col + 8 c + 4 h
+    static constexpr uint32_t sfb_col = 4 * sf_chunks;
+    static constexpr uint32_t sf_cols = 3 * sfb_col;
+    static constexpr uint32_t prefix_bytes = mx_only ? 0 : 8 * 260;
+    static constexpr uint32_t slack = mx_only ? 0 : 1024;
+    static constexpr uint32_t nbox_max = mx_only ? 1 : 2;
+    static constexpr bool staged_store = NST * stage_bytes + nbox_max * BOX_BYTES + 256 + prefix_bytes + slack <= 232448;
+    static constexpr uint32_t nbox = staged_store ? nbox_max : 0;
+    static constexpr uint32_t staging_bytes = nbox * BOX_BYTES;
     static constexpr uint32_t staging_off = NST * stage_bytes;
     static constexpr uint32_t bars_off = staging_off + staging_bytes;
     static constexpr uint32_t prefix_off = bars_off + 256;
-    static constexpr uint32_t smem_bytes = prefix_off + 8 * 260 + 1024;
+    static constexpr uint32_t smem_bytes = prefix_off + prefix_bytes + slack;
     static_assert(smem_bytes <= 232448, "GEMM shared memory above the 227 KB per-CTA limit");
     static_assert(4 * NST + 5 <= 30, "barriers overlap the TMEM slot");
-    static_assert(TMEM_SF + SF_COLS * NST <= 512, "scale buffers beyond the TMEM allocation");
+    static_assert(TMEM_SF + sf_cols * NST <= 512, "scale buffers beyond the TMEM allocation");
+    static_assert(!mx_only || (PAIR && staged_store), "the six-stage layout is the paired, staged one");
 };
 constexpr int kThreads = 384;          // producer warp, MMA warp, 8 epilogue warps, 2 scale-copy warps
 constexpr uint32_t TMEM_COLS = 512;
@@ -281,6 +297,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     constexpr int CG = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    if constexpr (LY::slack == 0) {
+        // no room to align: every CTA of the launch sees the same offset and leaves
+        if (smem != smem_raw) {
+            if (threadIdx.x == 0) atomicOr(args.status, args.status_bit);
+            return;
+        }
+    }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::bars_off);
     // bars[0..STAGES) operands landed, [STAGES..2 STAGES) empty, then tmem_full,
     // tmem_empty, mma drain, [2 STAGES + 3 .. 3 STAGES + 3) scales copied, the two
@@ -322,16 +345,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             tc::tma_prefetch_desc(&tmap_sfb);
         }
         // 128-row tiles per group and (paired form) pairs of them, prefix-summed
-        int acc = 0, accp = 0;
-        tile_prefix[0] = 0;
-        pair_prefix[0] = 0;
-        for (int e = 0; e < args.groups; ++e) {
-            const int n = int(args.offsets[e + 1] - args.offsets[e]);
-            const int tiles = (n + BM - 1) / BM;
-            acc += tiles;
-            accp += (tiles + 1) / 2;
-            tile_prefix[e + 1] = acc;
-            pair_prefix[e + 1] = accp;
+        if constexpr (!LY::mx_only) {
+            int acc = 0, accp = 0;
+            tile_prefix[0] = 0;
+            pair_prefix[0] = 0;
+            for (int e = 0; e < args.groups; ++e) {
+                const int n = int(args.offsets[e + 1] - args.offsets[e]);
+                const int tiles = (n + BM - 1) / BM;
+                acc += tiles;
+                accp += (tiles + 1) / 2;
+                tile_prefix[e + 1] = acc;
+                pair_prefix[e + 1] = accp;
+            }
         }
     }
     if (warp == 1) {
@@ -401,7 +426,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                                          int((uint64_t(t.a_sf_tile) * args.sf_tile_stride + ck) / 256u));
                     tc::tma_load_2d_pair(tc::smem_u32(sfb_smem), &tmap_sfb, sbp, 0,
                                          int((uint64_t(t.b_row0 / 128) * args.sf_tile_stride + ck) / 256u));
-                    tc::tma_load_2d_pair(tc::smem_u32(sfb_smem + 4 * 512), &tmap_sfb, sbp, 0,
+                    tc::tma_load_2d_pair(tc::smem_u32(sfb_smem + LY::sfb_half_bytes), &tmap_sfb, sbp, 0,
                                          int((uint64_t(bsf1) * args.sf_tile_stride + ck) / 256u));
                     tc::tma_load_2d_pair(tc::smem_u32(st), &tmap_a, fbp, kb * 128, t.a_row0);
                     tc::tma_load_2d_pair(tc::smem_u32(st + A_BYTES), &tmap_b, fbp, kb * 128, brow);
@@ -417,7 +442,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                                   args.sfb + uint64_t(t.b_row0 / 128) * args.sf_tile_stride + ct0 * 512u,
                                   chunks * 512u, sb);
                     if (t.b_row1 >= 0)
-                        tc::bulk_load(tc::smem_u32(sfb_smem + 4 * 512),
+                        tc::bulk_load(tc::smem_u32(sfb_smem + LY::sfb_half_bytes),
                                       args.sfb + uint64_t(t.b_row1 / 128) * args.sf_tile_stride + ct0 * 512u,
                                       chunks * 512u, sb);
                     // x coordinate in bytes: 128 bytes of K per stage for both element widths
@@ -487,7 +512,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 const uint32_t so = uint32_t(stage) * (LY::stage_bytes >> 4);
                 const uint32_t a_lo = d_lo0 + so, b_lo = a_lo + (A_BYTES >> 4);
                 // the stage's scale buffer: A chunk c at sfa + 4 c, B half h chunk c at sfb + 8 c + 4 h
-                const uint32_t sfa = tmem + TMEM_SF + SF_COLS * uint32_t(stage), sfb = sfa + 16u;
+                const uint32_t sfa = tmem + TMEM_SF + LY::sf_cols * uint32_t(stage), sfb = sfa + LY::sfb_col;
 #pragma unroll
                 for (uint32_t j = 0; j < NM; ++j) {
                     const uint64_t da = tc::desc_from(a_lo + 2 * j, d_hi), db = tc::desc_from(b_lo + 2 * j, d_hi);
@@ -591,8 +616,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 }
                 tc::fence_after_sync();
                 const uint32_t so = uint32_t(stage) * (LY::stage_bytes >> 4);
-                const uint32_t sfa_lo = sf_lo0 + so, sfb_lo = sf_lo0 + so + (SFA_BYTES >> 4);
-                const uint32_t sfa = tmem + TMEM_SF + SF_COLS * uint32_t(stage), sfb = sfa + 16u;
+                const uint32_t sfa_lo = sf_lo0 + so, sfb_lo = sf_lo0 + so + (LY::sfa_bytes >> 4);
+                const uint32_t sfa = tmem + TMEM_SF + LY::sf_cols * uint32_t(stage), sfb = sfa + LY::sfb_col;
+                constexpr uint32_t h1 = LY::sfb_half_bytes >> 4;     // B's second half, in 16-byte units
                 const uint32_t chunks = uint32_t(min(args.bk, args.K - kb * args.bk)) / chunk_elems;
                 if (chunks == 4) {
 #pragma unroll
@@ -600,18 +626,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                         const uint32_t c = 2 * half + i;
                         tc::tc_cp_g<CG>(sfa + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
                         tc::tc_cp_g<CG>(sfb + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
-                        tc::tc_cp_g<CG>(sfb + 8 * c + 4, tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
+                        tc::tc_cp_g<CG>(sfb + 8 * c + 4, tc::desc_from(sfb_lo + h1 + 32 * c, sf_hi));
                     }
                 } else if (chunks == 2) {
                     const uint32_t c = half;
                     tc::tc_cp_g<CG>(sfa + 4 * c, tc::desc_from(sfa_lo + 32 * c, sf_hi));
                     tc::tc_cp_g<CG>(sfb + 8 * c, tc::desc_from(sfb_lo + 32 * c, sf_hi));
-                    tc::tc_cp_g<CG>(sfb + 8 * c + 4, tc::desc_from(sfb_lo + 128 + 32 * c, sf_hi));
+                    tc::tc_cp_g<CG>(sfb + 8 * c + 4, tc::desc_from(sfb_lo + h1 + 32 * c, sf_hi));
                 } else if (half == 0) {
                     tc::tc_cp_g<CG>(sfa, tc::desc_from(sfa_lo, sf_hi));
                     tc::tc_cp_g<CG>(sfb, tc::desc_from(sfb_lo, sf_hi));
                 } else {
-                    tc::tc_cp_g<CG>(sfb + 4, tc::desc_from(sfb_lo + 128, sf_hi));
+                    tc::tc_cp_g<CG>(sfb + 4, tc::desc_from(sfb_lo + h1, sf_hi));
                 }
                 tc::tc_commit_g<CG>(copied_bar(stage), 0x1);
                 ++copied;
@@ -768,17 +794,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 if (lane == 0) release_acc();
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
-                    const int box = qq & 1;
-                    // the box's previous store (two quarters ago, possibly the previous
-                    // tile's) has read it: at most one store group still reading
-                    if (et == 0) tc::bulk_wait_read1();
+                    const int box = LY::nbox == 2 ? (qq & 1) : 0;
+                    // the box's previous store (two quarters ago with two boxes, the
+                    // last one with one; possibly the previous tile's) has read it
+                    if (et == 0) {
+                        if constexpr (LY::nbox == 2)
+                            tc::bulk_wait_read1();
+                        else
+                            tc::bulk_wait_read0();
+                    }
                     tc::named_bar_sync(1, 256);
                     if (hf == (qq >> 1)) {
 #pragma unroll
-                        for (int cc = 2 * box; cc < 2 * box + 2; ++cc) {
+                        for (int cc = 2 * (qq & 1); cc < 2 * (qq & 1) + 2; ++cc) {
                             uint32_t p[16];
                             to_bf16x32(raw[cc], alpha, p);
-                            stage_bf16x32(staging, srow, cc, p);
+                            stage_bf16x32(staging, srow, LY::nbox == 2 ? cc : (cc & 1), p);
                         }
                     }
                     tc::fence_proxy_async_smem();
@@ -961,13 +992,20 @@ fp4q_status launch_stages(const Maps& m, const GemmArgs& a, int units_upper, int
 }
 
 // Ring depth: the paired form keeps 5 stages of 38 KB next to the BF16
-// staging boxes; the single-CTA form 3 (FP4) or 4 (MXFP8, whose stages hold
-// half the K of an FP4 stage; its BF16 rows go out straight from registers).
+// staging boxes, or, for dense MXFP4, 6 stages of 35 KB (see Layout); the
+// single-CTA form 3 (FP4) or 4 (MXFP8, whose stages hold half the K of an FP4
+// stage; its BF16 rows go out straight from registers).
 constexpr int kPairStages = 5;
+constexpr int kPairStagesMx = 6;
 
 template <int EPI>
 fp4q_status launch(const Maps& m, const GemmArgs& a, bool pair, int units_upper, int sms, cudaStream_t stream) {
-    if (pair) return launch_stages<EPI, kPairStages, true>(m, a, units_upper, sms, stream);
+    if (pair) {
+        if constexpr (EPI == kStore) {
+            if (!a.groups && !a.nv && !a.f8) return launch_stages<EPI, kPairStagesMx, true>(m, a, units_upper, sms, stream);
+        }
+        return launch_stages<EPI, kPairStages, true>(m, a, units_upper, sms, stream);
+    }
     if constexpr (EPI == kStore) {
         if (a.f8) return launch_stages<EPI, 4, false>(m, a, units_upper, sms, stream);
     }
