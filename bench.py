@@ -377,6 +377,24 @@ def main_rows(fq, W, torch, peaks, which=ROW_NAMES, moe_tokens=65536):
         torch.cuda.synchronize()
         return statistics.mean(a.elapsed_time(b) for a, b in ts)
 
+    def b2b(launch, n=200):
+        """n back-to-back launches (launch(i) picks input set i), CUDA events on
+        the stream around the whole run: the streaming kernels' steady rate, as
+        for the step's kernels.  Each row's sets together exceed L2, so every
+        launch reads its inputs from HBM; a single call after an L2 flush also
+        pays the kernel's start and drain (~3 us on a 20 us kernel)."""
+        for i in range(3):
+            launch(i)
+        e0, e1 = _events(torch, 2)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n):
+            launch(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+    timed.b2b = b2b
+
     def dev_bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
@@ -459,7 +477,15 @@ def c3_row(fq, W, torch, peaks, timed, dev_bf16, rows):
     b_both = R3 * C3 * 2 + 2 * (R3 * C3 // 2) + R3 * C3 // 16
     ms_both = timed(c3_both, 10, True)
     ms_both1 = timed(lambda: c3_both(amax_dev), 10, True)
+    # back to back (the 235 MB input exceeds L2)
+    hbm = peaks["hbm_gbs"]
+    bb_rne1 = timed.b2b(lambda i: c3(fq.FP4Q_RNE, amax_dev), 100)
+    bb_both1 = timed.b2b(lambda i: c3_both(amax_dev), 100)
     rows["nvfp4_rht_8192x14336"] = {
+        "back_to_back": {"rne_quant_pass_ms": round(bb_rne1, 4),
+                         "frac_hbm_rne_quant_pass": round(b_quant / bb_rne1 / 1e6 / hbm, 3),
+                         "sr_rne_quant_pass_ms": round(bb_both1, 4),
+                         "frac_hbm_sr_rne_quant_pass": round(b_both / bb_both1 / 1e6 / hbm, 3)},
         "sr_and_rne_one_call_ms": round(ms_both, 4),
         "sr_and_rne_one_call_GB_per_s": round((b_amax + b_both) / ms_both / 1e6, 1),
         "sr_and_rne_separate_calls_ms": round(ms_sr + ms_rne, 4),
@@ -525,10 +551,16 @@ def col_rows(fq, W, torch, peaks, timed, dev_bf16, rows):
     ms = timed(lambda: fq.fp4q_fp4_row_to_fp8_col(q, s, ROWS, COLS, y, yt, stream), 10, True)
     nb = bytes_mx_to_fp8(ROWS, COLS)
     row_ms = timed(lambda: fq.fp4q_fp4_to_fp8(q, s, ROWS, COLS, 1, y, yt, stream), 10, True)
+    # back to back over NSETS copies of the input (NSETS x 31 MB in, 59 MB out per launch)
+    sets = [(q, s)] + [(q.clone(), s.clone()) for _ in range(NSETS - 1)]
+    bb = timed.b2b(lambda i: fq.fp4q_fp4_row_to_fp8_col(sets[i % NSETS][0], sets[i % NSETS][1], ROWS, COLS, y, yt,
+                                                       stream))
     rows["f1_fp4_row_to_fp8_col_8192x7168"] = {
+        "back_to_back": {"ms": round(bb, 4), "GB_per_s": round(nb / bb / 1e6, 1),
+                         "frac_hbm": round(nb / bb / 1e6 / hbm, 3)},
         "ms": round(ms, 4), "GB_per_s": round(nb / ms / 1e6, 1), "frac_hbm": round(nb / ms / 1e6 / hbm, 3),
         "row_layout_ms": round(row_ms, 4), "row_layout_GB_per_s": round(nb / row_ms / 1e6, 1)}
-    del x8, t8, q, s, y, yt
+    del x8, t8, q, s, y, yt, sets
 
     R3, C3 = 8192, 14336
     xg = dev_bf16(W.gradient_bf16(R3, C3))
@@ -547,7 +579,10 @@ def col_rows(fq, W, torch, peaks, timed, dev_bf16, rows):
     amax_dev = am.clone()
     ms_sr1 = timed(lambda: c3col(fq.FP4Q_SR, amax_dev), 10, True)
     ms_rne1 = timed(lambda: c3col(fq.FP4Q_RNE, amax_dev), 10, True)
+    bb_rne1 = timed.b2b(lambda i: c3col(fq.FP4Q_RNE, amax_dev), 100)       # 235 MB input > L2
     rows["f1_f3_nvfp4_col_h16_8192x14336"] = {
+        "back_to_back": {"rne_quant_pass_ms": round(bb_rne1, 4),
+                         "frac_hbm_rne_quant_pass": round(b_quant / bb_rne1 / 1e6 / hbm, 3)},
         "sr_two_pass_ms": round(ms_sr, 4), "rne_two_pass_ms": round(ms_rne, 4),
         "sr_quant_pass_GB_per_s": round(b_quant / ms_sr1 / 1e6, 1),
         "rne_quant_pass_GB_per_s": round(b_quant / ms_rne1 / 1e6, 1),
@@ -563,7 +598,13 @@ def col_rows(fq, W, torch, peaks, timed, dev_bf16, rows):
     ms_mx = timed(lambda: fq.fp4q_mx_quantize(ad, fq.FP4Q_BF16, None, 8192, 8192, 8192, 0, qa, sa, 0, stream), 10,
                   True)
     nbq = 8192 * 8192 * (2 + 0.5 + 1 / 32)
-    rows["f1_mxfp4_col_bf16_8192x8192"] = {"ms": round(ms_mx, 4), "GB_per_s": round(nbq / ms_mx / 1e6, 1),
+    ad2 = ad.clone()                                                        # two 134 MB inputs
+    bb_mx = timed.b2b(lambda i: fq.fp4q_mx_quantize(ad if i % 2 == 0 else ad2, fq.FP4Q_BF16, None, 8192, 8192, 8192, 0,
+                                                    qa, sa, 0, stream), 100)
+    del ad2
+    rows["f1_mxfp4_col_bf16_8192x8192"] = {"back_to_back": {"ms": round(bb_mx, 4),
+                                                            "frac_hbm": round(nbq / bb_mx / 1e6 / hbm, 3)},
+                                           "ms": round(ms_mx, 4), "GB_per_s": round(nbq / ms_mx / 1e6, 1),
                                            "frac_hbm": round(nbq / ms_mx / 1e6 / hbm, 3)}
     # Wgrad: tokens along K for both operands (rows of a and b are the tokens here)
     ra = fq.nv_quantize(ad, rht=2, layout=fq.FP4Q_SCALES_MMA, block_axis=0)
@@ -621,7 +662,11 @@ def nv2d_row(fq, W, torch, peaks, timed, rows):
     ms1 = timed(lambda: fq.fp4q_nv_quantize_2d(w, R, C, C, fq.FP4Q_RNE, 0, amax_dev, am, st, q, s, 0, ws, 256,
                                                stream), 10, True)
     b_quant = R * C * (2 + 0.5 + 1 / 16)
+    bb1 = timed.b2b(lambda i: fq.fp4q_nv_quantize_2d(w, R, C, C, fq.FP4Q_RNE, 0, amax_dev, am, st, q, s, 0, ws, 256,
+                                                     stream), 50)           # 470 MB input > L2
     rows["f2_nvfp4_2d_weights_32768x7168"] = {
+        "back_to_back": {"quant_pass_ms": round(bb1, 4),
+                         "frac_hbm_quant_pass": round(b_quant / bb1 / 1e6 / peaks["hbm_gbs"], 3)},
         "two_pass_ms": round(ms2, 4), "quant_pass_ms": round(ms1, 4),
         "quant_pass_GB_per_s": round(b_quant / ms1 / 1e6, 1),
         "frac_hbm_quant_pass": round(b_quant / ms1 / 1e6 / peaks["hbm_gbs"], 3)}

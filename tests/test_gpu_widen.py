@@ -139,7 +139,7 @@ def test_nv_2d_forward_and_transposed_weights_agree(fq, oracle):
 # ---------------------------------------------------------------------------
 # FP4RowToFP8Col
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("shape", [(128, 128), (256, 384), (640, 256)])
+@pytest.mark.parametrize("shape", [(128, 128), (256, 384), (640, 256), (128, 512), (256, 2560), (640, 1024)])
 def test_fp4_row_to_fp8_col(fq, oracle, shape):
     R, C = shape
     rng = np.random.default_rng(R * 7 + C)
