@@ -90,9 +90,10 @@ constexpr uint32_t TMEM_SF = 256;
 // takes ~3400 cycles from its refill to its release, of which the landing from
 // L2 is ~1650 -- so a sixth stage buys ~15 % on long K.  It fits by holding
 // MXFP4's scales only (2 chunks of A and of each B half), one staging box, no
-// group prefix sums and no alignment slack: the kernel requires its dynamic
-// shared memory to start on a 1024-byte boundary (it does: after the 1 KB the
-// hardware reserves) and reports an error otherwise.
+// group prefix sums and 768 bytes of alignment slack (what is left of 227 KB):
+// the kernel requires its dynamic shared memory to start within 768 bytes
+// below a 1024-byte boundary (it starts on one, after the 1 KB the hardware
+// reserves) and reports an error otherwise.
 template <int NST, bool PAIR>
 struct Layout {
     static constexpr bool mx_only = NST == 6;
@@ -106,15 +107,18 @@ struct Layout {
     static constexpr uint32_t sfb_col = 4 * sf_chunks;
     static constexpr uint32_t sf_cols = 3 * sfb_col;
     static constexpr uint32_t prefix_bytes = mx_only ? 0 : 8 * 260;
-    static constexpr uint32_t slack = mx_only ? 0 : 1024;
+    static constexpr uint32_t slack_max = 1024;
     static constexpr uint32_t nbox_max = mx_only ? 1 : 2;
-    static constexpr bool staged_store = NST * stage_bytes + nbox_max * BOX_BYTES + 256 + prefix_bytes + slack <= 232448;
+    static constexpr bool staged_store =
+        NST * stage_bytes + nbox_max * BOX_BYTES + 256 + prefix_bytes + (mx_only ? 0 : slack_max) <= 232448;
     static constexpr uint32_t nbox = staged_store ? nbox_max : 0;
     static constexpr uint32_t staging_bytes = nbox * BOX_BYTES;
     static constexpr uint32_t staging_off = NST * stage_bytes;
     static constexpr uint32_t bars_off = staging_off + staging_bytes;
     static constexpr uint32_t prefix_off = bars_off + 256;
-    static constexpr uint32_t smem_bytes = prefix_off + prefix_bytes + slack;
+    static constexpr uint32_t used_bytes = prefix_off + prefix_bytes;
+    static constexpr uint32_t slack = used_bytes + slack_max <= 232448 ? slack_max : 232448 - used_bytes;
+    static constexpr uint32_t smem_bytes = used_bytes + slack;
     static_assert(smem_bytes <= 232448, "GEMM shared memory above the 227 KB per-CTA limit");
     static_assert(4 * NST + 5 <= 30, "barriers overlap the TMEM slot");
     static_assert(TMEM_SF + sf_cols * NST <= 512, "scale buffers beyond the TMEM allocation");
@@ -297,9 +301,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     constexpr int CG = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    if constexpr (LY::slack == 0) {
-        // no room to align: every CTA of the launch sees the same offset and leaves
-        if (smem != smem_raw) {
+    if constexpr (LY::slack < 1023) {
+        // too little room to align every offset: every CTA of the launch sees the
+        // same one and leaves
+        if (uint32_t(smem - smem_raw) > LY::slack) {
             if (threadIdx.x == 0) atomicOr(args.status, args.status_bit);
             return;
         }
