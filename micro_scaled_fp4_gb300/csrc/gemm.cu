@@ -14,24 +14,28 @@
 // per step, K consumed 256 elements (128 bytes) per pipeline stage:
 //   warp 0      TMA producer: A and B tiles (128-byte swizzle; B as two
 //               128-row halves) and the stage's block scales (contiguous
-//               chunks of the MMA scale layout) into a 3-stage ring.
+//               chunks of the MMA scale layout) into a ring of 3 to 6 stages;
+//               the scales go first and land on their own barrier.
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma kind::mxf4
 //               (UE8M0 per 32) or kind::mxf4nvf4 (UE4M3 per 16), FP32
 //               accumulator in TMEM, reading the stage's block scales from
-//               that stage's own TMEM scale buffer.
-//   warps 10-11 one thread each copies half of each landed stage's block
-//               scales into the stage's TMEM scale buffer (tcgen05.cp); the
-//               two commits release the stage to the MMA thread.  Issued from
-//               the MMA thread, the copies held back the MMAs (a stage of
-//               MXFP4 took ~830 cycles of issue for ~530 of MMA); from their
-//               own threads, into buffers no MMA in flight reads, they overlap
-//               with the MMAs.  The copy unit takes about 53 cycles per
-//               512-byte chunk, so an NVFP4 stage's 12 copies (~640 cycles)
-//               still exceed its 4 MMAs (~512).
+//               that stage's own TMEM scale buffer, once the stage's operands
+//               have landed and its scales have been copied.
+//   warps 10-11 one thread each copies half of each stage's block scales into
+//               the stage's TMEM scale buffer (tcgen05.cp) as soon as they
+//               have landed, while the operands still land; the two commits
+//               release the scales to the MMA thread.  Issued from the MMA
+//               thread, the copies held back the MMAs (a stage of MXFP4 took
+//               ~830 cycles of issue for ~530 of MMA); from their own threads,
+//               into buffers no MMA in flight reads, they overlap with the
+//               MMAs.  The copy unit takes about 60 cycles per 512-byte chunk
+//               (2 KB of TMEM once replicated to the four lane quadrants), so
+//               an NVFP4 stage's 12 copies still exceed its 4 MMAs (~512).
 //   warps 2..9  epilogue: tcgen05.ld of the 128 x 256 FP32 accumulator,
 //               one row and half the columns per thread (two warps per TMEM
 //               lane quadrant); the accumulator goes back to the MMA thread
-//               as soon as it has been read.  STORE: scale, BF16
+//               as soon as it has been read (a relaxed arrive: it publishes
+//               no memory).  STORE: scale, BF16
 //               (round to nearest even) or FP32 stores.  SILU_GATE: the two
 //               B halves are the gate and up rows of the same 128 outputs;
 //               h = SiLU(gate) * up in FP32, then MXFP4 (one 32-element
@@ -48,7 +52,9 @@
 // "accumulator full" barriers of both CTAs; each CTA's epilogue reads its own
 // 128 TMEM lanes (its 128 output rows x 256 columns) and arrives, across the
 // pair, on the even CTA's "accumulator empty" barrier.  Per SM this halves the
-// B bytes a stage brings in and the MMA instructions per flop.
+// B bytes a stage brings in and the MMA instructions per flop.  Dense MXFP4
+// runs the paired form with six stages (see Layout), everything else paired
+// with five; a dense GEMM of one 128-row tile runs the single-CTA form.
 // Every mbarrier wait is bounded in time; a wait that gives up sets a bit in
 // the library's status word and tells the other roles to stop.  The drain
 // waits that follow (TMA loads issued, MMAs issued) do not stop on that flag,
