@@ -74,11 +74,12 @@ namespace fp4q {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 256;           // elements
-// Ring depth: 3 stages, or 4 for MXFP8 operands, whose stages hold half the
-// K of an FP4 stage and whose MMAs therefore wait on the loads more often.
-// With 3 stages the BF16 output goes through a shared-memory staging area and
-// TMA stores; with 4 the staging area's room goes to the ring and the
-// epilogue stores BF16 rows straight from registers.
+// Ring depth (single-CTA form): 3 stages, or 4 for MXFP8 operands, whose
+// stages hold half the K of an FP4 stage and whose MMAs therefore wait on the
+// loads more often.  With 3 stages the BF16 output goes through a
+// shared-memory staging area and TMA stores; with 4 the staging area's room
+// goes to the ring and the epilogue stores BF16 rows straight from registers.
+// The paired form keeps 5 stages (6 for dense MXFP4) next to the staging.
 constexpr uint32_t A_BYTES = BM * BK / 2;             // 16384
 constexpr uint32_t B_HALF_BYTES = 128 * BK / 2;       // 16384
 constexpr uint32_t B_BYTES = 2 * B_HALF_BYTES;
