@@ -442,7 +442,10 @@ fp4q_status fp4q_grouped_gemm(const uint8_t* a_q, const uint8_t* a_scales, const
  * fp4q_device_status -- read (and, if reset != 0, clear) the device status
  * word of the current device: 0 when no device-side wait has timed out since
  * the last reset, else a bit mask of the kernels that gave up (FP4Q_ERR_TIMEOUT
- * is returned in that case): bit 0 fp4q_block_scaled_gemm, bit 1
+ * is returned in that case): bit 0 fp4q_block_scaled_gemm (also set, with
+ * D left unwritten, when the dense MXFP4 form finds its dynamic shared
+ * memory starting more than 768 bytes below a 1024-byte boundary, which a
+ * launch without static shared memory never does), bit 1
  * fp4q_grouped_gemm, bit 2 the shared-memory-staged conversions of
  * fp4q_mx_quantize (E4M3 source) and fp4q_fp4_to_fp8, bit 3 a tile scale
  * fp4q_fp8_tile_scales_to_e8m0 could not convert, bit 31
