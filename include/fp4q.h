@@ -395,7 +395,9 @@ fp4q_status fp4q_moe_dispatch_static(const int32_t* topk, int64_t tokens, int to
  * rows are unspecified (the GEMM's rows there are not stored).
  *   scales     device ROWMAJOR E8M0 [rows, cols/32], 4-byte aligned;  cols % 128 == 0
  *   offsets    device int64 [groups + 1] row offsets, 8-byte aligned (rows beyond
- *              offsets[groups] ignored)
+ *              offsets[groups] ignored).  The kernel clamps each offset into
+ *              [previous offset, rows] (the first into [0, rows]), so offsets that
+ *              decrease or exceed rows cannot make it read or write out of bounds
  *   ue4m3_mma  device out, fp4q_rebased_scales_bytes(rows, cols, groups) bytes, 16-byte aligned
  *   row_scale  device FP32 out [rows]
  * A misaligned pointer returns FP4Q_ERR_MISALIGNED.

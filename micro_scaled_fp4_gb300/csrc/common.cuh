@@ -6,6 +6,7 @@
 //   E4M3  "FN" 8-bit float, bias 7, max 448, smallest subnormal 2^-9.
 #pragma once
 
+#include <algorithm>
 #include <cuda_runtime.h>
 #include <mutex>
 #include <stdint.h>
@@ -249,8 +250,11 @@ inline cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 b
 }
 
 // Resident CTAs per SM of `kernel` at `threads` per CTA and `smem` bytes of
-// dynamic shared memory (raising the kernel's dynamic shared memory limit when
-// needed), remembered per kernel, device and size.
+// dynamic shared memory, remembered per kernel, device and size.  Above 48 KB
+// the kernel's dynamic shared memory limit is raised to all the device's
+// opt-in maximum leaves beside the kernel's static shared memory, never to
+// `smem` itself: a limit set for one size would otherwise shrink below a
+// larger size whose entry is already remembered.
 template <typename Kernel>
 inline int resident_per_sm_smem(Kernel kernel, int threads, uint32_t smem) {
     // keyed by the kernel itself: instances of one template share a type
@@ -264,7 +268,15 @@ inline int resident_per_sm_smem(Kernel kernel, int threads, uint32_t smem) {
     const void* fn = reinterpret_cast<const void*>(kernel);
     for (const Entry& e : cache)
         if (e.n && e.fn == fn && e.dev == dev && e.threads == threads && e.smem == smem) return e.n;
-    if (smem > 48 * 1024) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (smem > 48 * 1024) {
+        // the limit covers dynamic memory only: static + dynamic must fit the opt-in maximum
+        int optin = 0;
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaFuncAttributes fa{};
+        cudaFuncGetAttributes(&fa, kernel);
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             std::max(int(smem), optin - int(fa.sharedSizeBytes)));
+    }
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
     cache[next] = Entry{fn, dev, threads, smem, n};

@@ -132,29 +132,39 @@ __device__ __forceinline__ uint32_t ue4m3_pow2(int k) {
     return 0u;
 }
 
+// Group table of the rebase kernels (thread 0): the offsets clamped to a
+// non-decreasing run inside [0, rows] -- well-formed offsets pass unchanged,
+// and malformed ones can then neither read past the scales nor place more
+// padded tiles than fp4q_rebased_scales_bytes covers -- and tpre[g], the
+// padded 128-row tiles of the groups before g.
+__device__ void rebase_group_table(const int64_t* __restrict__ offsets, int groups, int64_t rows, int64_t* off,
+                                   int64_t* tpre) {
+    int64_t acc = 0, prev = 0;
+    for (int g = 0; g <= groups; ++g) {
+        const int64_t o = min(max(offsets[g], prev), rows);
+        if (g > 0) acc += (o - prev + 127) / 128;        // tiles of group g - 1
+        off[g] = o;
+        tpre[g] = acc;
+        prev = o;
+    }
+}
+
 __global__ void __launch_bounds__(256) mx_rebase_kernel(const uint8_t* __restrict__ s, int64_t rows, int S32,
                                                         const int64_t* __restrict__ offsets, int groups,
                                                         uint8_t* __restrict__ out, float* __restrict__ row_scale,
                                                         uint32_t* __restrict__ violations) {
     __shared__ int64_t off[kMaxExperts + 1];
     __shared__ int64_t tpre[kMaxExperts + 1];
-    if (threadIdx.x == 0) {
-        int64_t acc = 0;
-        for (int g = 0; g <= groups; ++g) {
-            off[g] = offsets[g];
-            tpre[g] = acc;
-            if (g < groups) acc += (offsets[g + 1] - offsets[g] + 127) / 128;
-        }
-    }
+    if (threadIdx.x == 0) rebase_group_table(offsets, groups, rows, off, tpre);
     __syncthreads();
     // persistent: the group table above is built once per CTA, then each warp
     // takes rows warp_id, warp_id + warps, ...
     const int lane = threadIdx.x & 31;
-    const int64_t nrows = min(rows, off[groups]);
+    const int64_t nrows = off[groups];
     const int64_t warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     const uint32_t S16 = uint32_t(S32) * 2;
     uint32_t bad = 0;
-    for (int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < nrows; r += warps) {
+    for (int64_t r = off[0] + ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5); r < nrows; r += warps) {
         int lo = 0, hi = groups - 1;                 // group of row r: off[g] <= r < off[g + 1]
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -182,31 +192,31 @@ __global__ void __launch_bounds__(256) mx_rebase_kernel(const uint8_t* __restric
 
 // The same rebase, one padded 128-row tile at a time.  In the MMA scale layout
 // a 128-row tile's scales are one contiguous run of S16/4 chunks of 512 bytes,
-// so the CTA stages the tile's E8M0 rows in shared memory (rows padded by 4
-// bytes: the column reads of phase 2 then fall in 32 different banks), takes
-// each row's base while staging it (a warp per row, 32-bit words, a byte-wise
-// max), and writes every chunk as 16-byte stores -- thread (c4, i)
-// the bytes of rows i, i + 32, i + 64, i + 96 for columns 4 c4 .. 4 c4 + 3 --
-// so a warp writes 512 contiguous bytes.  Padding rows are written as 0.
-__global__ void __launch_bounds__(256) mx_rebase_tiles_kernel(const uint8_t* __restrict__ s, int S32,
-                                                              const int64_t* __restrict__ offsets, int groups,
-                                                              uint8_t* __restrict__ out, float* __restrict__ row_scale,
+// and its E8M0 source rows are one contiguous run of 128 * S32 bytes (fewer at
+// a group's end).  Phase 1 stages that run in shared memory, each thread
+// loading up to eight 32-bit words before it stores any, so a tile takes few
+// load round trips (rows padded by 4 bytes: the column reads of phase 2 then
+// fall in 32 different banks; rows past the group are zero); then two threads
+// per row take the row's maximum E8M0 byte.
+// Phase 2 writes every chunk as 16-byte stores -- thread (c4, i) the bytes of
+// rows i, i + 32, i + 64, i + 96 for columns 4 c4 .. 4 c4 + 3 -- so a warp
+// writes 512 contiguous bytes.  Padding rows are written as 0.
+// wdiv = ceil(2^32 / (S32 / 4)): k / (S32 / 4) == (k * wdiv) >> 32 for every
+// word index k < 128 * S32 / 4 of a tile.
+__global__ void __launch_bounds__(256) mx_rebase_tiles_kernel(const uint8_t* __restrict__ s, int64_t rows, int S32,
+                                                              uint64_t wdiv, const int64_t* __restrict__ offsets,
+                                                              int groups, uint8_t* __restrict__ out,
+                                                              float* __restrict__ row_scale,
                                                               uint32_t* __restrict__ violations) {
     extern __shared__ __align__(16) uint8_t stage[];     // [128][S32 + 4] E8M0 bytes, then int base[128]
     __shared__ int64_t off[kMaxExperts + 1];
     __shared__ int64_t tpre[kMaxExperts + 1];
-    if (threadIdx.x == 0) {
-        int64_t acc = 0;
-        for (int g = 0; g <= groups; ++g) {
-            off[g] = offsets[g];
-            tpre[g] = acc;
-            if (g < groups) acc += (offsets[g + 1] - offsets[g] + 127) / 128;
-        }
-    }
+    if (threadIdx.x == 0) rebase_group_table(offsets, groups, rows, off, tpre);
     __syncthreads();
     const int RS = S32 + 4;                               // staged row stride (bytes)
+    const uint32_t wpr = uint32_t(S32) / 4;               // 32-bit words per row
     int* base = reinterpret_cast<int*>(stage + 128 * RS);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31;
     const int64_t ntiles = tpre[groups];
     uint32_t bad = 0;
     for (int64_t T = blockIdx.x; T < ntiles; T += gridDim.x) {
@@ -218,24 +228,39 @@ __global__ void __launch_bounds__(256) mx_rebase_tiles_kernel(const uint8_t* __r
         const int64_t r0 = off[lo] + (T - tpre[lo]) * 128;
         const int64_t left = off[lo + 1] - r0;
         const int nreal = left < 128 ? int(left) : 128;
-        // phase 1: warp w takes rows w, w + 8, ...; lane j loads the row's 32-bit
-        // words j, j + 32, ... (rows past the group: 0), stages them and keeps
-        // their byte maximum; a warp reduction gives the row's max E8M0 byte
-        const int wpr = S32 / 4;
-        for (int rr = warp; rr < 128; rr += int(blockDim.x >> 5)) {
-            const uint8_t* src = s + (r0 + rr) * S32;
+        // phase 1: word k of the tile's run -> row k / wpr, word k % wpr
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(s + r0 * S32);
+        const uint32_t nw = uint32_t(nreal) * wpr, total = 128u * wpr;
+        for (uint32_t k0 = threadIdx.x; k0 < total; k0 += 8 * blockDim.x) {
+            uint32_t v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t k = k0 + u * blockDim.x;
+                v[u] = k < nw ? __ldg(src + k) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t k = k0 + u * blockDim.x;
+                if (k < total) {
+                    const uint32_t rr = uint32_t((uint64_t(k) * wdiv) >> 32);
+                    *reinterpret_cast<uint32_t*>(stage + rr * RS + 4 * (k - rr * wpr)) = v[u];
+                }
+            }
+        }
+        __syncthreads();
+        // row bases: threads 2 rr and 2 rr + 1 take the even and odd words of row rr
+        for (uint32_t t = threadIdx.x; t < 256u; t += blockDim.x) {
+            const uint32_t rr = t >> 1;
             uint32_t m = 0;
-            for (int j = lane; j < wpr; j += 32) {
-                const uint32_t v = rr < nreal ? *reinterpret_cast<const uint32_t*>(src + 4 * j) : 0u;
-                *reinterpret_cast<uint32_t*>(stage + rr * RS + 4 * j) = v;
+            for (uint32_t j = t & 1u; j < wpr; j += 2) {
+                const uint32_t v = *reinterpret_cast<const uint32_t*>(stage + rr * RS + 4 * j);
                 const uint32_t h = __vmaxu4(v, v >> 16);            // bytes 0 / 1: max of (0, 2) / (1, 3)
                 m = max(m, max(h & 0xffu, (h >> 8) & 0xffu));
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) {
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            if ((t & 1u) == 0) {
                 base[rr] = int(m) - 127 - 8;
-                if (rr < nreal) row_scale[r0 + rr] = exp2_wide(int(m) - 127 - 8);
+                if (int(rr) < nreal) row_scale[r0 + rr] = exp2_wide(int(m) - 127 - 8);
             }
         }
         __syncthreads();
@@ -352,8 +377,10 @@ extern "C" fp4q_status fp4q_mx_rebase_scales(const uint8_t* scales, int64_t rows
         const int64_t tiles_upper = (rows + 127) / 128 + groups;
         const int64_t blocks = std::min<int64_t>(tiles_upper, int64_t(sms) *
                                                  resident_per_sm_smem(mx_rebase_tiles_kernel, 256, smem));
+        const uint64_t wpr = uint64_t(S32 / 4);
         mx_rebase_tiles_kernel<<<unsigned(blocks), 256, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-            scales, S32, offsets, int(groups), ue4m3_mma, row_scale, violations);
+            scales, rows, S32, ((uint64_t(1) << 32) + wpr - 1) / wpr, offsets, int(groups), ue4m3_mma, row_scale,
+            violations);
         return check_launch("mx_rebase_scales");
     }
     const int64_t blocks = std::min<int64_t>((rows * 32 + 255) / 256,

@@ -415,6 +415,38 @@ def moe_dispatch(topk_experts: np.ndarray, n_experts: int):
     return tokens[order], offsets
 
 
+def mx_rebase_scales(e8m0: np.ndarray):
+    """MXFP4 block scales -> UE4M3 scales per 16 elements and a per-row
+    factor, so MXFP4 rows can enter a block-scaled product whose other operand
+    is NVFP4 (one scale type per product).  The pages quantize activations to
+    MXFP4 before the expert dispatch ("Practical FP4 Training for Large-Scale
+    MoE Models on Hopper GPUs", section 2.A) while NVFP4 ("Pretraining Large
+    Language Models with NVFP4", section 2.B) scales blocks of 16 by E4M3; they
+    do not say how the two meet, so this is the build's own reading, written
+    out plainly.  Per row with block exponents E_j = byte_j - 127:
+      B = max_j E_j - 8;  block j's scale 2^E_j = 2^(E_j - B) * 2^B;
+      2^(E_j - B) is a UE4M3 value for E_j - B in [-9, 8] (normal from -6,
+      subnormal 2^-7, 2^-8, 2^-9), and both 16-element halves of block j take
+      that byte; E_j - B < -9 is not representable: the byte is 0 and the
+      block is counted as a violation.
+    Returns (ue4m3 [R, 2 S32] uint8, row factor 2^B [R] float32, violations).
+    Pinned by hand-derived rows and by the reconstruction
+    e4m3_value(byte) * 2^B == 2^E_j on every representable block
+    (tests/test_oracle_gemm.py)."""
+    e = np.asarray(e8m0, dtype=np.int64) - 127
+    R = e.shape[0]
+    B = (e.max(axis=1) if e.shape[1] else np.zeros(R, np.int64)) - 8
+    k = e - B[:, None]                                   # in [-254 - 8, 8]
+    ue = np.zeros(e.shape, dtype=np.uint8)
+    normal = k >= -6
+    ue[normal] = ((k[normal] + 7) << 3).astype(np.uint8)
+    sub = (k >= -9) & ~normal
+    ue[sub] = (1 << (k[sub] + 9)).astype(np.uint8)
+    violations = int(np.count_nonzero(k < -9))
+    factor = np.array([np.ldexp(np.float32(1.0), int(b)) for b in B], dtype=np.float32)
+    return np.repeat(ue, 2, axis=1), factor, violations
+
+
 def silu(g: np.ndarray) -> np.ndarray:
     """SiLU(g) = g / (1 + exp(-g)) in float64."""
     g = np.asarray(g, dtype=np.float64)

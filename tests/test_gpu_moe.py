@@ -299,3 +299,73 @@ def test_moe_full_size(fq, oracle):
     GEMM stages (h against float64, Y) and the experts' NVFP4 weights on 24
     sampled rows of every non-empty expert."""
     _run_moe(fq, oracle, T=65536, H=7168, I=2048, E=64, k=8, seed=8, check_rows=24, requant_all=True)
+
+
+@pytest.mark.parametrize("cols_seq", [(7168,), (2048, 128), (32768, 16384, 32768), (33024,)])
+def test_mx_rebase_scales_exact(fq, oracle, cols_seq):
+    """fp4q_mx_rebase_scales against the oracle's rebase on every grouped row:
+    the UE4M3 bytes (read back through the padded MMA layout), the FP32 row
+    factors bit for bit, and the violation count.  Ragged groups (empty, 1,
+    127-129, 255, 256 and 300 rows), rows past offsets[groups] that must be
+    ignored, all-zero rows, the largest E8M0 byte and planted blocks just
+    inside (E - B = -9) and outside (-10) the representable range.  cols 128
+    is the narrowest tile form (one 32-bit word per row), 32768 the widest
+    (132 KB of shared memory, run again after a narrower one), 33024 takes the
+    row-wise kernel."""
+    import torch
+    sizes = [0, 1, 127, 128, 129, 0, 255, 256, 300, 2]
+    G = len(sizes)
+    offs = np.zeros(G + 1, dtype=np.int64)
+    offs[1:] = np.cumsum(sizes)
+    n = int(offs[-1])
+    R = n + 5                                              # 5 rows past the last group
+    for cols in cols_seq:
+        S32 = cols // 32
+        rng = np.random.default_rng(cols)
+        s = rng.integers(110, 140, (R, S32), dtype=np.uint8)
+        s[rng.random((R, S32)) < 0.02] = 0
+        s[3] = 0                                           # all-zero row
+        s[7, 0] = 254
+        for r in range(10, n, 37):                         # E - B = -9 and -10 beside the row max
+            s[r, :] = 130
+            s[r, -1] = 130 - 17
+            if S32 > 2:
+                s[r, 1] = 130 - 18
+        ue_ref, f_ref, v_ref = oracle.mx_rebase_scales(s[:n])
+        viol = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ue, rs = fq.mx_rebase_scales(dev(s), dev(offs), cols, G, viol)
+        torch.cuda.synchronize()
+        S16 = cols // 16
+        ue_h = host(ue)
+        nrows_pad = (ue_h.size // 512) // ((S16 + 3) // 4) * 128
+        got = from_mma_layout(ue_h, nrows_pad, S16)[_padded_rows(offs)]
+        assert np.array_equal(got, ue_ref), cols
+        assert np.array_equal(host(rs)[:n].view(np.uint32), f_ref.view(np.uint32)), cols
+        assert int(viol.item()) == v_ref and v_ref > 0, cols
+
+
+@pytest.mark.parametrize("cols", [2048, 33024])
+def test_mx_rebase_scales_clamps_malformed_offsets(fq, oracle, cols):
+    """Offsets that decrease or run past `rows` are clamped, each into
+    [previous offset, rows]: the call writes nothing past
+    fp4q_rebased_scales_bytes (a canary follows the output) and the rows of
+    the clamped groups are rebased as with those offsets."""
+    import torch
+    R, G = 350, 4
+    bad = np.array([0, 300, 100, 400, 50], dtype=np.int64)
+    clamped = np.array([0, 300, 300, 350, 350], dtype=np.int64)
+    s = np.random.default_rng(5).integers(110, 140, (R, cols // 32), dtype=np.uint8)
+    size = fq.fp4q_rebased_scales_bytes(R, cols, G)
+    out = torch.full((size + 8192,), 0xAB, dtype=torch.uint8, device="cuda")
+    rs = torch.zeros(R + 64, dtype=torch.float32, device="cuda")
+    rs[R:] = 7.0
+    fq.fp4q_mx_rebase_scales(dev(s), R, cols, dev(bad), G, out, rs, None, None)
+    torch.cuda.synchronize()
+    out_h = host(out)
+    assert np.all(out_h[size:] == 0xAB) and np.all(host(rs)[R:] == 7.0)
+    S16 = cols // 16
+    nrows_pad = (size // 512) // ((S16 + 3) // 4) * 128
+    got = from_mma_layout(out_h[:size], nrows_pad, S16)[_padded_rows(clamped)]
+    ue_ref, f_ref, _ = oracle.mx_rebase_scales(s)
+    assert np.array_equal(got, ue_ref)
+    assert np.array_equal(host(rs)[:R].view(np.uint32), f_ref.view(np.uint32))

@@ -62,3 +62,38 @@ def test_silu_closed_forms(oracle):
     assert abs(s[1] - 1.0 / (1.0 + np.exp(-1.0))) < 1e-16
     assert abs(s[1] - s[2] - 1.0) < 1e-15          # silu(x) - silu(-x) = x
     assert abs(s[3] - 30.0) < 1e-11 and abs(s[4]) < 1e-11
+
+
+def test_mx_rebase_hand_derived_rows(oracle):
+    # Row bytes 127, 119, 110, 109, 0 -> E = 0, -8, -17, -18, -127; B = max E - 8 = -8.
+    # E - B = 8, 0, -9, -10, -119: UE4M3 0x78 (2^8), 0x38 (1.0), 0x01 (2^-9, the
+    # smallest subnormal), then two unrepresentable blocks (byte 0, counted).
+    ue, f, v = oracle.mx_rebase_scales(np.array([[127, 119, 110, 109, 0]], dtype=np.uint8))
+    assert list(ue[0]) == [0x78, 0x78, 0x38, 0x38, 0x01, 0x01, 0, 0, 0, 0]
+    assert f[0] == np.float32(2.0 ** -8) and v == 2
+    # all-zero bytes (E = -127 everywhere): B = -135, an FP32 subnormal factor,
+    # and every block is the top UE4M3 power 2^8
+    ue, f, v = oracle.mx_rebase_scales(np.zeros((1, 3), dtype=np.uint8))
+    assert np.all(ue == 0x78) and f[0] == np.float32(2.0 ** -135) and f[0] > 0 and v == 0
+    # the largest finite E8M0 byte (254, E = 127): B = 119
+    ue, f, v = oracle.mx_rebase_scales(np.array([[254, 238, 240, 233]], dtype=np.uint8))
+    assert f[0] == np.float32(2.0 ** 119)
+    # E - B: 8, -8, -6, -13 -> 0x78, 0x02 (2^-8), 0x08 (2^-6, the smallest normal), 0 (violation)
+    assert list(ue[0]) == [0x78, 0x78, 0x02, 0x02, 0x08, 0x08, 0, 0] and v == 1
+
+
+def test_mx_rebase_reconstructs_every_representable_block(oracle):
+    # e4m3_value(byte) * 2^B == 2^E exactly where E - B >= -9, byte 0 elsewhere,
+    # and the violation count is the number of blocks below B - 9
+    rng = np.random.default_rng(11)
+    s = rng.integers(0, 255, (64, 40), dtype=np.uint8)
+    s[:32] = rng.integers(100, 140, (32, 40), dtype=np.uint8)     # rows with few violations
+    ue, f, v = oracle.mx_rebase_scales(s)
+    e = s.astype(np.int64) - 127
+    B = e.max(axis=1) - 8
+    ok = (e - B[:, None]) >= -9
+    vals = oracle.e4m3_values()[ue[:, 0::2]] * f.astype(np.float64)[:, None]
+    assert np.array_equal(vals[ok], np.exp2(e[ok].astype(np.float64)))
+    assert np.all(ue[:, 0::2][~ok] == 0) and v == int((~ok).sum()) and v > 0
+    assert np.array_equal(ue[:, 0::2], ue[:, 1::2])
+    assert np.array_equal(f.astype(np.float64), np.exp2(B.astype(np.float64)))
