@@ -423,7 +423,9 @@ typedef enum fp4q_epilogue {
  *   b_q            device [groups, N, K/2];  b_scales device, the groups' NVFP4
  *                  E4M3 scales in MMA layout, back to back;  b_tensor_scale
  *                  device FP32 [groups]
- *   offsets        device int64 [groups + 1]
+ *   offsets        device int64 [groups + 1], clamped by the kernel like those of
+ *                  fp4q_mx_rebase_scales (each into [previous offset, rows]), so
+ *                  malformed offsets cannot make it read or write out of bounds
  *   N, K           N % 128 == 0 (gated: N % 256 == 0), K % 128 == 0
  *   D              STORE_BF16: device BF16 [rows, N];  SILU_GATE: device codes
  *                  [rows, N/4] (h has N/2 columns)

@@ -113,7 +113,7 @@ struct Layout {
     // TMEM columns per stage: A chunk c at 4 c, B half h chunk c at sfb_col + 8 c + 4 h
     static constexpr uint32_t sfb_col = 4 * sf_chunks;
     static constexpr uint32_t sf_cols = 3 * sfb_col;
-    static constexpr uint32_t prefix_bytes = mx_only ? 0 : 8 * 260;
+    static constexpr uint32_t prefix_bytes = mx_only ? 0 : 12 * 260;   // tile, pair prefix sums, clamped offsets
     static constexpr uint32_t slack_max = 1024;
     static constexpr uint32_t nbox_max = mx_only ? 1 : 2;
     static constexpr bool staged_store =
@@ -134,7 +134,7 @@ struct Layout {
 constexpr int kThreads = 384;          // producer warp, MMA warp, 8 epilogue warps, 2 scale-copy warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;      // 4 s
-constexpr int kMaxGroups = 256;            // the prefix arrays hold kMaxGroups + 1 entries (260 reserved)
+constexpr int kMaxGroups = 256;            // the prefix / offset arrays hold kMaxGroups + 1 entries (260 reserved)
 constexpr int kBandM = 32;                            // m-tiles per band of the dense tile order
 constexpr int64_t kBandAboveBytes = 48ll << 20;       // band only an A operand L2 cannot keep
 
@@ -210,7 +210,8 @@ __device__ __forceinline__ void decode_b(const GemmArgs& a, int nt, TileInfo& t)
 // banded over m-tile pairs like the single-CTA order.
 template <int EPI>
 __device__ __forceinline__ TileInfo decode_pair(const GemmArgs& a, int unit, const int* tile_prefix,
-                                                const int* pair_prefix, int m_tiles, uint32_t crank) {
+                                                const int* pair_prefix, const int* goff, int m_tiles,
+                                                uint32_t crank) {
     TileInfo t;
     int nt, mp;
     if (a.groups) {
@@ -222,8 +223,8 @@ __device__ __forceinline__ TileInfo decode_pair(const GemmArgs& a, int unit, con
         const int tiles_e = tile_prefix[e + 1] - tile_prefix[e];
         t.group = e;
         t.phantom = lt >= tiles_e;
-        t.a_row0 = int(a.offsets[e]) + lt * BM;
-        t.row_end = int(a.offsets[e + 1]);
+        t.a_row0 = goff[e] + lt * BM;
+        t.row_end = goff[e + 1];
         t.a_sf_tile = tile_prefix[e] + min(lt, tiles_e - 1);
     } else {
         const int m_pairs = (m_tiles + 1) / 2, band_p = max(1, a.band_m / 2);
@@ -244,7 +245,8 @@ __device__ __forceinline__ TileInfo decode_pair(const GemmArgs& a, int unit, con
 }
 
 template <int EPI>
-__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile, const int* tile_prefix, int m_tiles) {
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile, const int* tile_prefix, const int* goff,
+                                                int m_tiles) {
     TileInfo t;
     t.phantom = false;
     int nt, mt;
@@ -266,8 +268,8 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile, con
         while (e + 1 < a.groups && tile_prefix[e + 1] <= mt) ++e;
         const int local = mt - tile_prefix[e];
         t.group = e;
-        t.a_row0 = int(a.offsets[e]) + local * BM;
-        t.row_end = int(a.offsets[e + 1]);
+        t.a_row0 = goff[e] + local * BM;
+        t.row_end = goff[e + 1];
     } else {
         t.group = 0;
         t.a_row0 = mt * BM;
@@ -324,6 +326,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     volatile int* abort = reinterpret_cast<volatile int*>(bars + 31);
     int* tile_prefix = reinterpret_cast<int*>(smem + LY::prefix_off);
     int* pair_prefix = tile_prefix + 260;
+    int* goff = pair_prefix + 260;                  // the group offsets, clamped
     const uint32_t staging = tc::smem_u32(smem + LY::staging_off);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -356,18 +359,25 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             tc::tma_prefetch_desc(&tmap_sfa);
             tc::tma_prefetch_desc(&tmap_sfb);
         }
-        // 128-row tiles per group and (paired form) pairs of them, prefix-summed
+        // 128-row tiles per group and (paired form) pairs of them, prefix-summed.
+        // Each offset is clamped into [previous offset, M] (the first into
+        // [0, M]): well-formed offsets pass unchanged, and malformed ones can
+        // make no tile read a row scale or store a row outside [0, M).
         if constexpr (!LY::mx_only) {
-            int acc = 0, accp = 0;
+            int acc = 0, accp = 0, prev = 0;
             tile_prefix[0] = 0;
             pair_prefix[0] = 0;
-            for (int e = 0; e < args.groups; ++e) {
-                const int n = int(args.offsets[e + 1] - args.offsets[e]);
-                const int tiles = (n + BM - 1) / BM;
-                acc += tiles;
-                accp += (tiles + 1) / 2;
-                tile_prefix[e + 1] = acc;
-                pair_prefix[e + 1] = accp;
+            for (int e = 0; args.groups > 0 && e <= args.groups; ++e) {     // dense: no offsets
+                const int o = int(min(max(args.offsets[e], int64_t(prev)), int64_t(args.M)));
+                goff[e] = o;
+                if (e > 0) {
+                    const int tiles = (o - prev + BM - 1) / BM;      // group e - 1
+                    acc += tiles;
+                    accp += (tiles + 1) / 2;
+                    tile_prefix[e] = acc;
+                    pair_prefix[e] = accp;
+                }
+                prev = o;
             }
         }
     }
@@ -392,9 +402,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     const uint32_t chunk_elems = args.nv ? 64 : 128;  // K elements per 512-byte scale chunk
     auto decode = [&](int unit) {
         if constexpr (PAIR)
-            return decode_pair<EPI>(args, unit, tile_prefix, pair_prefix, m_tiles, crank);
+            return decode_pair<EPI>(args, unit, tile_prefix, pair_prefix, goff, m_tiles, crank);
         else
-            return decode_tile<EPI>(args, unit, tile_prefix, m_tiles);
+            return decode_tile<EPI>(args, unit, tile_prefix, goff, m_tiles);
     };
 
     if (warp == 0 && lane == 0) {

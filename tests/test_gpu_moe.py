@@ -369,3 +369,46 @@ def test_mx_rebase_scales_clamps_malformed_offsets(fq, oracle, cols):
     ue_ref, f_ref, _ = oracle.mx_rebase_scales(s)
     assert np.array_equal(got, ue_ref)
     assert np.array_equal(host(rs)[:R].view(np.uint32), f_ref.view(np.uint32))
+
+
+def test_grouped_gemm_clamps_malformed_offsets(fq):
+    """Offsets that decrease or run past `rows` are clamped by the grouped GEMM
+    as by the rebase (each into [previous offset, rows]): both epilogues write
+    nothing past their outputs (canaries follow D, the h scales and h_debug)
+    and give, bit for bit, the results of the clamped offsets."""
+    import torch
+    from micro_scaled_fp4_gb300 import workloads as W
+    R, H, N, G = 350, 256, 256, 4
+    bad = np.array([0, 300, 100, 400, 50], dtype=np.int64)
+    clamped = np.array([0, 300, 300, 350, 350], dtype=np.int64)
+    q, s = fq.mx_quantize(dev_bf16(W.moe_activations(R, H, seed=70)))
+    w = W.moe_weights_torch(G, N, H, 71, "cuda")
+    wq, ws, wt, _ = _quantize_experts(fq, w, G, N, H)
+    CAN = 4096
+
+    def run(offs, epi):
+        o = dev(offs)
+        ue = torch.zeros(fq.fp4q_rebased_scales_bytes(R, H, G), dtype=torch.uint8, device="cuda")
+        rs = torch.zeros(R, dtype=torch.float32, device="cuda")
+        fq.fp4q_mx_rebase_scales(s, R, H, o, G, ue, rs, None, None)
+        if epi == fq.FP4Q_EPI_STORE_BF16:
+            d = torch.full((R * N * 2 + CAN,), 0xAB, dtype=torch.uint8, device="cuda")
+            fq.fp4q_grouped_gemm(q, ue, rs, wq, ws, wt, o, R, G, N, H, epi, d, None, None, None)
+            torch.cuda.synchronize()
+            return [d]
+        d = torch.full((R * (N // 4) + CAN,), 0xAB, dtype=torch.uint8, device="cuda")
+        hs = torch.full((R * (N // 64) + CAN,), 0xAB, dtype=torch.uint8, device="cuda")
+        hd = torch.full((R * (N // 2) + CAN // 4,), 7.0, dtype=torch.float32, device="cuda")
+        fq.fp4q_grouped_gemm(q, ue, rs, wq, ws, wt, o, R, G, N, H, epi, d, hs, hd, None)
+        torch.cuda.synchronize()
+        return [d, hs, hd]
+
+    for epi in (fq.FP4Q_EPI_STORE_BF16, fq.FP4Q_EPI_SILU_GATE_MXFP4):
+        got, ref = run(bad, epi), run(clamped, epi)
+        assert fq.fp4q_device_status() == 0
+        for g_t, r_t in zip(got, ref):
+            g_h, r_h = host(g_t), host(r_t)
+            tail = g_h.size - (CAN // 4 if g_h.dtype == np.float32 else CAN)
+            canary = np.float32(7.0) if g_h.dtype == np.float32 else 0xAB
+            assert np.all(g_h[tail:] == canary) and np.all(r_h[tail:] == canary), epi
+            assert np.array_equal(g_h[:tail].view(np.uint8), r_h[:tail].view(np.uint8)), epi
