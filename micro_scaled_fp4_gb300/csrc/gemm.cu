@@ -91,13 +91,14 @@ constexpr uint32_t BOX_BYTES = 128 * 128;             // 64 BF16 columns x 128 r
 // n = 4 or, in the six-stage layout, 2).
 constexpr uint32_t TMEM_SF = 256;
 // Per-CTA shared memory: NST ring stages [A | B (the pair: one half) | A
-// scales | B scales], the BF16 staging boxes, barriers, the group prefix sums.
+// scales | B scales], the BF16 staging boxes, barriers, the group prefix sums
+// and the clamped group offsets.
 //
 // Six stages (paired, dense MXFP4 only): the ring is latency-bound -- a stage
 // takes ~3400 cycles from its refill to its release, of which the landing from
 // L2 is ~1650 -- so a sixth stage buys ~15 % on long K.  It fits by holding
 // MXFP4's scales only (2 chunks of A and of each B half), one staging box, no
-// group prefix sums and 768 bytes of alignment slack (what is left of 227 KB):
+// group tables and 768 bytes of alignment slack (what is left of 227 KB):
 // the kernel requires its dynamic shared memory to start within 768 bytes
 // below a 1024-byte boundary (it starts on one, after the 1 KB the hardware
 // reserves) and reports an error otherwise.
