@@ -82,7 +82,8 @@ const char* fp4q_status_string(fp4q_status status);
 const char* fp4q_last_error(void);
 
 /* Bytes of a block-scale matrix of `rows` x `scale_cols` in `layout`
- * (ROWMAJOR: rows * scale_cols; MMA: padded to 128 x 4 tiles). */
+ * (ROWMAJOR: rows * scale_cols; MMA: padded to 128 x 4 tiles); 0 for negative
+ * sizes and for sizes whose byte count does not fit a size_t. */
 size_t fp4q_scales_bytes(int64_t rows, int64_t scale_cols, fp4q_scale_layout layout);
 
 /*
@@ -164,9 +165,10 @@ fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, int64_t row
  *   workspace     device, >= fp4q_fp8_pipeline_host_workspace_bytes(cols,
  *                 chunk_rows) bytes (chunk_rows capped at rows), 256-byte aligned;
  *                 owned by the call until `stream` passes it
- * Errors: negative sizes or a NULL pointer -> INVALID_ARGUMENT; cols % 128 ->
- * UNSUPPORTED_SHAPE; misaligned workspace -> MISALIGNED; a failed copy, event
- * or launch -> CUDA.  rows == 0 or cols == 0 does nothing.
+ * Errors: negative sizes or a NULL pointer -> INVALID_ARGUMENT; cols % 128,
+ * cols > 2^31 or a chunk of more than 2^40 elements -> UNSUPPORTED_SHAPE (the
+ * workspace query then returns 0); misaligned workspace -> MISALIGNED; a
+ * failed copy, event or launch -> CUDA.  rows == 0 or cols == 0 does nothing.
  */
 size_t fp4q_fp8_pipeline_host_workspace_bytes(int64_t cols, int64_t chunk_rows);
 fp4q_status fp4q_fp8_pipeline_host(const uint8_t* x, const float* tile_scale, int64_t rows,
@@ -400,7 +402,9 @@ fp4q_status fp4q_moe_dispatch_static(const int32_t* topk, int64_t tokens, int to
  *              decrease or exceed rows cannot make it read or write out of bounds
  *   ue4m3_mma  device out, fp4q_rebased_scales_bytes(rows, cols, groups) bytes, 16-byte aligned
  *   row_scale  device FP32 out [rows]
- * A misaligned pointer returns FP4Q_ERR_MISALIGNED.
+ * A misaligned pointer returns FP4Q_ERR_MISALIGNED.  fp4q_rebased_scales_bytes
+ * returns 0 for negative sizes and for sizes whose byte count does not fit a
+ * size_t.
  */
 size_t fp4q_rebased_scales_bytes(int64_t rows, int64_t cols, int64_t groups);
 fp4q_status fp4q_mx_rebase_scales(const uint8_t* scales, int64_t rows, int64_t cols,

@@ -126,11 +126,17 @@ extern "C" const char* fp4q_status_string(fp4q_status s) {
 
 extern "C" const char* fp4q_last_error(void) { return t_last_error; }
 
+// 0 when the size does not fit a size_t (sizes no allocation could hold)
 extern "C" size_t fp4q_scales_bytes(int64_t rows, int64_t scale_cols, fp4q_scale_layout layout) {
-    if (rows < 0 || scale_cols < 0) return 0;
-    if (layout == FP4Q_SCALES_MMA)
-        return size_t((rows + 127) / 128) * size_t((scale_cols + 3) / 4) * 512u;
-    return size_t(rows) * size_t(scale_cols);
+    if (rows < 0 || scale_cols < 0 || rows > (int64_t(1) << 60) || scale_cols > (int64_t(1) << 60)) return 0;
+    size_t n = 0;
+    if (layout == FP4Q_SCALES_MMA) {
+        if (__builtin_mul_overflow(size_t((rows + 127) / 128), size_t((scale_cols + 3) / 4), &n) ||
+            __builtin_mul_overflow(n, size_t(512), &n))
+            return 0;
+        return n;
+    }
+    return __builtin_mul_overflow(size_t(rows), size_t(scale_cols), &n) ? 0 : n;
 }
 
 extern "C" fp4q_status fp4q_device_status(uint32_t* status_out, int reset) {

@@ -142,9 +142,16 @@ fp4q_status enqueue_chunks(Engine* g, const uint8_t* x, const float* tile_scale,
 
 using namespace fp4q;
 
+// A slot of chunk x cols elements must stay far inside 64-bit sizes.
+static bool slot_too_large(int64_t cols, int64_t chunk) {
+    return cols > (int64_t(1) << 31) || chunk > (int64_t(1) << 40) / std::max<int64_t>(cols, 1);
+}
+
 extern "C" size_t fp4q_fp8_pipeline_host_workspace_bytes(int64_t cols, int64_t chunk_rows) {
     if (cols <= 0 || chunk_rows < 0) return 0;
-    return size_t(kSlots) * size_t(slot_layout(cols, chunk_for(0, chunk_rows)).bytes);
+    const int64_t chunk = chunk_for(0, chunk_rows);
+    if (slot_too_large(cols, chunk)) return 0;
+    return size_t(kSlots) * size_t(slot_layout(cols, chunk).bytes);
 }
 
 extern "C" fp4q_status fp4q_fp8_pipeline_host(const uint8_t* x, const float* tile_scale, int64_t rows,
@@ -160,6 +167,9 @@ extern "C" fp4q_status fp4q_fp8_pipeline_host(const uint8_t* x, const float* til
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
         return fail(FP4Q_ERR_MISALIGNED, "fp8_pipeline_host: workspace must be 256-byte aligned");
     const int64_t chunk = chunk_for(rows, chunk_rows);
+    if (slot_too_large(cols, chunk))
+        return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "fp8_pipeline_host: chunk of %lld x %lld elements too large",
+                    static_cast<long long>(chunk), static_cast<long long>(cols));
     const SlotLayout L = slot_layout(cols, chunk);
     if (workspace_bytes < size_t(kSlots) * L.bytes)
         return fail(FP4Q_ERR_INVALID_ARGUMENT, "fp8_pipeline_host: workspace too small (%zu < %zu)",

@@ -367,9 +367,15 @@ extern "C" fp4q_status fp4q_moe_dispatch(const int32_t* topk, int64_t tokens, in
     return FP4Q_OK;
 }
 
+// 0 when the size does not fit a size_t (sizes no allocation could hold)
 extern "C" size_t fp4q_rebased_scales_bytes(int64_t rows, int64_t cols, int64_t groups) {
-    if (rows < 0 || cols < 0 || groups < 0) return 0;
-    return size_t((rows + 127) / 128 + groups) * size_t((cols / 16 + 3) / 4) * 512u;
+    const int64_t big = int64_t(1) << 60;
+    if (rows < 0 || cols < 0 || groups < 0 || rows > big || cols > big || groups > big) return 0;
+    size_t n = 0;
+    if (__builtin_mul_overflow(size_t((rows + 127) / 128 + groups), size_t((cols / 16 + 3) / 4), &n) ||
+        __builtin_mul_overflow(n, size_t(512), &n))
+        return 0;
+    return n;
 }
 
 extern "C" fp4q_status fp4q_mx_rebase_scales(const uint8_t* scales, int64_t rows, int64_t cols,

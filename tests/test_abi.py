@@ -56,6 +56,14 @@ def test_scales_bytes(lib):
     assert lib.fp4q_scales_bytes(129, 5, lib.FP4Q_SCALES_MMA) == 2 * 2 * 512
     assert lib.fp4q_scales_bytes(0, 5, lib.FP4Q_SCALES_MMA) == 0
     assert lib.fp4q_nv_quantize_workspace_bytes(8192, 14336) >= 4
+    # byte counts that do not fit a size_t give 0 instead of a wrapped size
+    huge = (1 << 63) - 1
+    for layout in (lib.FP4Q_SCALES_ROWMAJOR, lib.FP4Q_SCALES_MMA):
+        assert lib.fp4q_scales_bytes(huge, 4, layout) == 0
+        assert lib.fp4q_scales_bytes(1 << 40, 1 << 40, layout) == 0
+    assert lib.fp4q_rebased_scales_bytes(huge, 128, 1) == 0
+    assert lib.fp4q_rebased_scales_bytes(1 << 40, 1 << 40, 8) == 0
+    assert lib.fp4q_rebased_scales_bytes(300, 256, 4) == (3 + 4) * 4 * 512
 
 
 def test_argument_errors_need_no_gpu(lib):
@@ -103,6 +111,7 @@ def test_argument_errors_need_no_gpu(lib):
         (lambda: lib.fp4q_fp8_pipeline_host(x, x, 64, 256, x, x, x, x, 64, x + 128, wsb, stream=0), 3),
         (lambda: lib.fp4q_fp8_pipeline_host(x, x, 64, 256, x, x, x, x, 64, x, wsb - 1, stream=0), 1),
         (lambda: lib.fp4q_fp8_pipeline_host(x, x, 200, 256, x, x, x, x, 128, x, wsb, stream=0), 1),
+        (lambda: lib.fp4q_fp8_pipeline_host(x, x, 1 << 41, 7168, x, x, x, x, 1 << 41, x, wsb, stream=0), 2),
     ]:
         with pytest.raises(E) as e:
             fn()
@@ -150,6 +159,8 @@ def test_fp8_pipeline_host_workspace_bytes(lib):
     assert lib.fp4q_fp8_pipeline_host_workspace_bytes(7168, 0) == 3 * slot(2048, 7168)
     assert lib.fp4q_fp8_pipeline_host_workspace_bytes(128, 3) == 3 * slot(3, 128)
     assert lib.fp4q_fp8_pipeline_host_workspace_bytes(0, 64) == 0
+    assert lib.fp4q_fp8_pipeline_host_workspace_bytes(1 << 32, 64) == 0          # cols > 2^31
+    assert lib.fp4q_fp8_pipeline_host_workspace_bytes(7168, 1 << 62) == 0        # chunk past 2^40 elements
 
 
 def test_empty_tensors_are_no_ops(lib):
