@@ -284,6 +284,46 @@ def mx_to_fp8_col(q: np.ndarray, s: np.ndarray):
     return y, ts
 
 
+def mx_to_fp8_col_grouped(q: np.ndarray, s: np.ndarray, offsets):
+    """FP4RowToFP8Col on ragged expert groups ("Practical FP4 Training for
+    Large-Scale MoE Models on Hopper GPUs", Spanish summary section 2 for the
+    kernel, French summary 2.C for ragged per-expert tensors with precomputed
+    offsets).  The 1x128 tiles of the transposed output run along each group's
+    rows and restart at its first row; the pages leave the group's last,
+    partial tile open, and the reading taken here is the plainest one: its
+    scale is 2^Emax over its real rows only, and the output pads every group
+    to whole tiles with zeros.  Written as the dense rule (mx_to_fp8_col) on
+    each group's rows padded to a multiple of 128 with zero codes and zero
+    E8M0 bytes: a zero byte (2^-127) never raises a tile's maximum, and zero
+    codes give zero bytes.  Returns (E4M3 [C, 128 T], FP32 tile scales
+    [C, T]), T = sum over groups of ceil(n_g / 128), group g's rows at columns
+    128 T_g .. 128 T_g + n_g - 1 (T_g its tiles' start).  Pinned by
+    tests/test_oracle_widen.py (tile-aligned groups equal the dense rule on
+    their rows; a hand-derived partial tile; an element-wise brute force)."""
+    q = np.ascontiguousarray(q)
+    s = np.ascontiguousarray(s)
+    offsets = [int(v) for v in offsets]
+    C = 2 * q.shape[1]
+    tiles = [(offsets[g + 1] - offsets[g] + 127) // 128 for g in range(len(offsets) - 1)]
+    T = sum(tiles)
+    y = np.zeros((C, 128 * T), dtype=np.uint8)
+    ts = np.zeros((C, T), dtype=np.float32)
+    t0 = 0
+    for g, tg in enumerate(tiles):
+        lo, hi = offsets[g], offsets[g + 1]
+        if tg == 0:
+            continue
+        qg = np.zeros((128 * tg, C // 2), dtype=np.uint8)
+        sg = np.zeros((128 * tg, C // 32), dtype=np.uint8)
+        qg[: hi - lo] = q[lo:hi]
+        sg[: hi - lo] = s[lo:hi]
+        yg, tsg = mx_to_fp8_col(qg, sg)
+        y[:, 128 * t0: 128 * (t0 + tg)] = yg
+        ts[:, t0: t0 + tg] = tsg
+        t0 += tg
+    return y, ts
+
+
 def mx_quantize_col(x: np.ndarray):
     """Column-wise MXFP4 (blocks of 32 along axis 0): by definition the
     row-wise quantization of the transpose, returned in the transposed layout

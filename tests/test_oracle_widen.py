@@ -215,6 +215,66 @@ def test_fp4_row_to_fp8_col_agrees_with_the_row_kernel_on_a_transposed_tile(orac
     assert np.array_equal(yc, yr) and np.array_equal(tc, tr)
 
 
+def test_fp4_row_to_fp8_col_grouped_equals_the_dense_rule_on_tile_aligned_groups(oracle):
+    """Groups whose sizes are multiples of 128 are laid out back to back with no
+    padding, so the grouped form is the dense form of the whole tensor."""
+    rng = np.random.default_rng(19)
+    R, C = 512, 64
+    q = rng.integers(0, 256, (R, C // 2), dtype=np.uint8)
+    s = rng.integers(110, 140, (R, C // 32), dtype=np.uint8)
+    y, ts = oracle.mx_to_fp8_col_grouped(q, s, [0, 128, 128, 384, 512])
+    yd, tsd = oracle.mx_to_fp8_col(q, s)
+    assert np.array_equal(y, yd) and np.array_equal(ts, tsd)
+
+
+def test_fp4_row_to_fp8_col_grouped_partial_tile_by_hand(oracle):
+    """Groups of 3 and 2 rows, one 32-column block: each group is one tile whose
+    scale is 2^(max E of its own rows), with its rows at the start of the tile
+    and zeros after them; the second group's large exponent does not reach the
+    first group's tile."""
+    q = np.zeros((5, 16), dtype=np.uint8)
+    q[:, 0] = [0x77, 0x22, 0x11, 0x77, 0x44]          # element 0 codes 7, 2, 1, 7, 4
+    s = np.array([[127], [126], [125], [140], [127]], dtype=np.uint8)
+    y, ts = oracle.mx_to_fp8_col_grouped(q, s, [0, 3, 5])
+    assert y.shape == (32, 256) and ts.shape == (32, 2)
+    assert np.all(ts[:, 0] == 1.0) and np.all(ts[:, 1] == np.float32(2.0 ** 13))
+    # group 0 (Emax 0): 6.0 -> 0x4C; 1.0 * 2^-1 = 0.5 -> 0x30; 0.5 * 2^-2 = 2^-3 -> 0x20
+    assert list(y[0, :3]) == [0x4C, 0x30, 0x20] and list(y[1, :3]) == [0x4C, 0x30, 0x20]
+    # group 1 (Emax 13): 6.0 -> 0x4C; 2.0 * 2^-13 -> 2^-12 < 2^-9: flushed to zero
+    assert list(y[0, 128:130]) == [0x4C, 0x00]
+    assert np.all(y[:, 3:128] == 0) and np.all(y[:, 130:] == 0)
+
+
+def test_fp4_row_to_fp8_col_grouped_element_brute_force(oracle):
+    """Element by element from the definition: output (c, 128 T_g + j) is the
+    E4M3 of code (off_g + j, c) shifted by its block exponent minus the maximum
+    block exponent of its 128-row tile within the group."""
+    rng = np.random.default_rng(20)
+    offs = [0, 0, 1, 130, 258, 300]
+    R, C = 300, 64
+    q = rng.integers(0, 256, (R, C // 2), dtype=np.uint8)
+    s = rng.integers(100, 140, (R, C // 32), dtype=np.uint8)
+    y, ts = oracle.mx_to_fp8_col_grouped(q, s, offs)
+    codes = np.empty((R, C), dtype=np.int64)
+    codes[:, 0::2] = q & 0xF
+    codes[:, 1::2] = q >> 4
+    e = s.astype(np.int64) - 127
+    t0 = 0
+    for g in range(len(offs) - 1):
+        n = offs[g + 1] - offs[g]
+        for t in range((n + 127) // 128):
+            lo, hi = offs[g] + 128 * t, min(offs[g] + 128 * (t + 1), offs[g + 1])
+            for c in range(0, C, 7):
+                emax = e[lo:hi, c // 32].max()
+                assert ts[c, t0 + t] == np.float32(2.0 ** emax)
+                for r in range(lo, hi):
+                    want = oracle.fp8_from_e2m1_shifted(codes[r, c], e[r, c // 32] - emax)
+                    assert y[c, 128 * (t0 + t) + (r - lo)] == want
+            assert np.all(y[:, 128 * (t0 + t) + (hi - lo): 128 * (t0 + t + 1)] == 0)
+        t0 += (n + 127) // 128
+    assert y.shape[1] == 128 * t0
+
+
 # ---------------------------------------------------------------------------
 # FP8 GEMM reference (the FP8 consumer of the FP4 -> FP8 conversions)
 # ---------------------------------------------------------------------------
