@@ -562,6 +562,35 @@ def col_rows(fq, W, torch, peaks, timed, dev_bf16, rows):
         "row_layout_ms": round(row_ms, 4), "row_layout_GB_per_s": round(nb / row_ms / 1e6, 1)}
     del x8, t8, q, s, y, yt, sets
 
+    # the same on ragged expert groups: the 2048-wide expert activation of 8192
+    # tokens routed top-8 over 64 experts (65536 dispatched rows), each group
+    # padded to whole 128-row tiles in the output
+    topk = W.moe_routing(tokens=8192, experts=64, top_k=8, seed=33)
+    goffs = np.zeros(65, dtype=np.int64)
+    goffs[1:] = np.cumsum(np.bincount(topk.reshape(-1), minlength=64))
+    RG, CG = int(goffs[-1]), 2048
+    tiles = int(sum((goffs[g + 1] - goffs[g] + 127) // 128 for g in range(64)))
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(36)
+    gsets = [(torch.randint(0, 256, (RG, CG // 2), dtype=torch.uint8, device="cuda", generator=gen),
+              torch.randint(110, 140, (RG, CG // 32), dtype=torch.uint8, device="cuda", generator=gen))
+             for _ in range(NSETS)]
+    go = torch.from_numpy(goffs).cuda()
+    ld = fq.fp4q_fp4_row_to_fp8_col_grouped_ld(RG, 64)
+    gy = torch.empty((CG, ld), dtype=torch.uint8, device="cuda")
+    gt = torch.empty((CG, ld // 128), dtype=torch.float32, device="cuda")
+    nbg = RG * (CG // 2 + CG // 32) + CG * 128 * tiles + 4 * CG * tiles
+    gms = timed(lambda: fq.fp4q_fp4_row_to_fp8_col_grouped(gsets[0][0], gsets[0][1], RG, CG, go, 64, gy, gt,
+                                                           stream), 10, True)
+    gbb = timed.b2b(lambda i: fq.fp4q_fp4_row_to_fp8_col_grouped(gsets[i % NSETS][0], gsets[i % NSETS][1], RG, CG,
+                                                                 go, 64, gy, gt, stream))
+    rows["f1_fp4_row_to_fp8_col_grouped_65536x2048_64experts"] = {
+        "back_to_back": {"ms": round(gbb, 4), "GB_per_s": round(nbg / gbb / 1e6, 1),
+                         "frac_hbm": round(nbg / gbb / 1e6 / hbm, 3)},
+        "ms": round(gms, 4), "GB_per_s": round(nbg / gms / 1e6, 1), "frac_hbm": round(nbg / gms / 1e6 / hbm, 3),
+        "tiles": tiles, "bytes": nbg}
+    del gsets, go, gy, gt
+
     R3, C3 = 8192, 14336
     xg = dev_bf16(W.gradient_bf16(R3, C3))
     q3 = torch.empty((C3, R3 // 2), dtype=torch.uint8, device="cuda")

@@ -282,6 +282,35 @@ fp4q_status fp4q_fp4_row_to_fp8_col(const uint8_t* q, const uint8_t* scales, int
                                     fp4q_stream_t stream);
 
 /*
+ * fp4q_fp4_row_to_fp8_col_grouped -- FP4RowToFP8Col on ragged expert groups:
+ * [HOP] French summary 2.C (per-expert tensors of ragged sizes, located by
+ * precomputed offsets) with the element and tile rules of
+ * fp4q_fp4_row_to_fp8_col.  The 1x128 tiles run along each group's rows and
+ * restart at its first row; a group's last tile may be partial, and its scale
+ * is 2^Emax over its real rows.  The output pads each group to whole tiles:
+ * with T_g the tiles of the groups before g, group g's rows
+ * offsets[g] .. offsets[g+1] - 1 land at columns 128 T_g .. 128 T_g + n_g - 1
+ * of every output row, the rest of its last tile is 0, and columns from
+ * 128 T_groups on are not written -- the padded per-group tile layout of
+ * fp4q_mx_rebase_scales, which a grouped weight-gradient GEMM reads.
+ *   q, scales   device, the rows' MXFP4 codes [rows, cols/2] (32-byte aligned)
+ *               and ROWMAJOR E8M0 [rows, cols/32] (4-byte aligned)
+ *   cols        multiple of 128;  rows, cols <= 2^31 - 1
+ *   offsets     device int64 [groups + 1], 1 <= groups <= 256, clamped by the
+ *               kernel like those of fp4q_mx_rebase_scales (each into
+ *               [previous offset, rows]; rows past offsets[groups] ignored)
+ *   y           device out, E4M3 [cols, ld], ld =
+ *               fp4q_fp4_row_to_fp8_col_grouped_ld(rows, groups)
+ *               = 128 * (ceil(rows / 128) + groups), 32-byte aligned
+ *   tile_scale  device out, FP32 [cols, ld / 128]: tile t of output row c
+ * fp4q_fp4_row_to_fp8_col_grouped_ld returns 0 for arguments the call rejects.
+ */
+int64_t fp4q_fp4_row_to_fp8_col_grouped_ld(int64_t rows, int64_t groups);
+fp4q_status fp4q_fp4_row_to_fp8_col_grouped(const uint8_t* q, const uint8_t* scales, int64_t rows,
+                                            int64_t cols, const int64_t* offsets, int64_t groups,
+                                            uint8_t* y, float* tile_scale, fp4q_stream_t stream);
+
+/*
  * fp4q_fp8_tile_scales_to_e8m0 -- FP32 power-of-two scales, one per 1x128 tile
  * (what fp4q_fp4_to_fp8 and fp4q_fp4_row_to_fp8_col write), -> E8M0 block
  * scales, one per 32 elements, so that their FP8 output feeds

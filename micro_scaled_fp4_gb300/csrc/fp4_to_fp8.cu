@@ -229,29 +229,39 @@ __global__ void __launch_bounds__(ring::kMaxThreads) fp4_to_fp8_staged_kernel(
 // output row.  No shared-memory staging of the tile is needed.
 constexpr int kColTile = 128;
 
-__global__ void __launch_bounds__(64) fp4_row_to_fp8_col_kernel(
-    const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, int64_t cols,
-    uint8_t* __restrict__ y, float* __restrict__ tile_scale) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t r0 = int64_t(blockIdx.y) * kColTile;
-    const int64_t c0 = int64_t(blockIdx.x) * kColTile + 64 * warp;     // 64 columns of this warp
+// One warp of FP4RowToFP8Col: input rows r0 .. r0 + 127 (MASKED: only the first
+// nreal are read, the others count as zero codes with E8M0 byte 0, which never
+// raise the tile maximum) x input columns c0 .. c0 + 63 -> bytes ycol ..
+// ycol + 127 of output rows c0 .. c0 + 63 (row stride ld_y) and their tile
+// scales at tile_scale[(c0 + k) * ld_ts + tcol].
+template <bool MASKED>
+__device__ __forceinline__ void row_to_col_warp(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
+                                                int64_t cols, int64_t r0, int nreal, int64_t c0,
+                                                uint8_t* __restrict__ y, int64_t ld_y, int64_t ycol,
+                                                float* __restrict__ tile_scale, int64_t ld_ts, int64_t tcol,
+                                                int lane) {
     const int64_t rb = r0 + 4 * lane;
     const int64_t spr = cols / 32;
     u32x8 cw[4];
     uint32_t e[4][2];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        cw[i] = ldg256(q + (rb + i) * (cols / 2) + c0 / 2);
-        const uint32_t sw = *reinterpret_cast<const uint16_t*>(s + (rb + i) * spr + c0 / 32);
-        e[i][0] = sw & 0xffu;
-        e[i][1] = sw >> 8;
+        if (!MASKED || 4 * lane + i < nreal) {
+            cw[i] = ldg256(q + (rb + i) * (cols / 2) + c0 / 2);
+            const uint32_t sw = *reinterpret_cast<const uint16_t*>(s + (rb + i) * spr + c0 / 32);
+            e[i][0] = sw & 0xffu;
+            e[i][1] = sw >> 8;
+        } else {
+            cw[i] = u32x8{};
+            e[i][0] = e[i][1] = 0u;
+        }
     }
     uint32_t emax[2];
 #pragma unroll
     for (int b = 0; b < 2; ++b)
         emax[b] = __reduce_max_sync(0xffffffffu, max(max(e[0][b], e[1][b]), max(e[2][b], e[3][b])));
-    tile_scale[(c0 + lane) * (rows / kColTile) + r0 / kColTile] = exp2i(int(emax[0]) - 127);
-    tile_scale[(c0 + 32 + lane) * (rows / kColTile) + r0 / kColTile] = exp2i(int(emax[1]) - 127);
+    tile_scale[(c0 + lane) * ld_ts + tcol] = exp2i(int(emax[0]) - 127);
+    tile_scale[(c0 + 32 + lane) * ld_ts + tcol] = exp2i(int(emax[1]) - 127);
     uint2 L[4][2];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -260,6 +270,7 @@ __global__ void __launch_bounds__(64) fp4_row_to_fp8_col_kernel(
             const uint32_t sh = min(emax[b] - e[i][b], uint32_t(kShiftRows - 1));
             L[i][b] = make_uint2(__ldg(&kShiftTable.lo[sh]), __ldg(&kShiftTable.hi[sh]));
         }
+    uint8_t* yl = y + ycol + 4 * lane;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {                       // codes word k: columns 8k .. 8k + 7
         uint2 o[4];
@@ -275,8 +286,107 @@ __global__ void __launch_bounds__(64) fp4_row_to_fp8_col_kernel(
                                      __byte_perm(t1, t3, 0x5410), __byte_perm(t1, t3, 0x7632)};
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                *reinterpret_cast<uint32_t*>(y + (c0 + 8 * k + 4 * h + kk) * rows + rb) = col[kk];
+                *reinterpret_cast<uint32_t*>(yl + (c0 + 8 * k + 4 * h + kk) * ld_y) = col[kk];
         }
+    }
+}
+
+// FP4RowToFP8Col ("Practical FP4 Training for Large-Scale MoE Models on Hopper
+// GPUs", Spanish summary section 2; French summary 2.C: dequantize, transpose
+// and re-quantize in one kernel).  Input: row-wise MXFP4 [rows, cols]; output:
+// E4M3 of the transpose [cols, rows] with one FP32 scale per 1x128 tile along
+// the output rows ([cols, rows/128]).  A warp converts 128 input rows x 64
+// input columns (two 32-blocks): lane l reads rows 4l .. 4l + 3 with one
+// 32-byte load each, so the two output tiles' scales (2^Emax over the 128
+// rows' block exponents) are warp maxima; each row is remapped with the shift
+// table, and a 4 x 4 byte transpose in registers (eight byte permutes per 16
+// bytes) turns the lane's 4 rows x 4 columns into four 32-bit words, one per
+// output row: every store instruction writes 128 contiguous bytes of one
+// output row.  No shared-memory staging of the tile is needed.
+__global__ void __launch_bounds__(64) fp4_row_to_fp8_col_kernel(
+    const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, int64_t cols,
+    uint8_t* __restrict__ y, float* __restrict__ tile_scale) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r0 = int64_t(blockIdx.y) * kColTile;
+    const int64_t c0 = int64_t(blockIdx.x) * kColTile + 64 * warp;     // 64 columns of this warp
+    row_to_col_warp<false>(q, s, cols, r0, kColTile, c0, y, rows, r0, tile_scale, rows / kColTile, r0 / kColTile,
+                           lane);
+}
+
+// The same on ragged expert groups (French summary 2.C: per-expert tensors
+// located by precomputed offsets): the tiles restart at each group's first row
+// and each group is padded to whole tiles in the output (group g's rows at
+// columns 128 T_g .. 128 T_g + n_g - 1 of every output row, zeros up to its
+// next tile; T_g = the tiles of the groups before g).  Persistent CTAs of
+// eight warps; warp 0 first builds the group tables: the offsets clamped into
+// a non-decreasing run inside [0, rows] (the clamp of offset g is its prefix
+// maximum, clamped to [0, rows]) and the tile prefix sums, each lane taking
+// nine consecutive entries.  Each warp then takes (tile, 64-column) items.
+constexpr int kGroupedMax = 256;
+
+__global__ void __launch_bounds__(256) fp4_row_to_fp8_col_grouped_kernel(
+    const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, int64_t cols,
+    const int64_t* __restrict__ offsets, int groups, uint8_t* __restrict__ y, int64_t ld_y,
+    float* __restrict__ tile_scale) {
+    __shared__ int64_t off[kGroupedMax + 1];
+    __shared__ int64_t tpre[kGroupedMax + 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) {
+        constexpr int kPer = (kGroupedMax + 1 + 31) / 32;        // 9 entries per lane
+        const int g0 = kPer * lane;
+        int64_t v[kPer];
+        int64_t run = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            v[j] = g0 + j <= groups ? offsets[g0 + j] : 0;
+            run = max(run, v[j]);
+            v[j] = run;                                          // running maximum within the lane
+        }
+        int64_t before = 0;                                      // maximum over the lanes below
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t up = __shfl_up_sync(0xffffffffu, run, o);
+            if (lane >= o) run = max(run, up);
+        }
+        before = __shfl_up_sync(0xffffffffu, run, 1);
+        if (lane == 0) before = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+            if (g0 + j <= groups) off[g0 + j] = min(max(v[j], before), rows);
+        __syncwarp();
+        int64_t t[kPer], sum = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            t[j] = g0 + j < groups ? (off[g0 + j + 1] - off[g0 + j] + 127) / 128 : 0;
+            sum += t[j];
+        }
+        int64_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t up = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += up;
+        }
+        int64_t acc = incl - sum;                                // tiles of the lanes below
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            if (g0 + j <= groups) tpre[g0 + j] = acc;
+            acc += t[j];
+        }
+    }
+    __syncthreads();
+    const int64_t ncc = cols / 64, ntiles = tpre[groups], items = ntiles * ncc;
+    const int64_t wstep = int64_t(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t it = int64_t(blockIdx.x) * (blockDim.x >> 5) + warp; it < items; it += wstep) {
+        const int64_t tile = it / ncc, c0 = (it - tile * ncc) * 64;
+        int lo = 0, hi = groups - 1;                             // the group of the tile
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (tpre[mid] <= tile) lo = mid; else hi = mid - 1;
+        }
+        const int64_t r0 = off[lo] + (tile - tpre[lo]) * kColTile;
+        const int nreal = int(min(int64_t(kColTile), off[lo + 1] - r0));
+        row_to_col_warp<true>(q, s, cols, r0, nreal, c0, y, ld_y, tile * kColTile, tile_scale, ld_y / kColTile,
+                              tile, lane);
     }
 }
 
@@ -350,6 +460,40 @@ extern "C" fp4q_status fp4q_fp4_row_to_fp8_col(const uint8_t* q, const uint8_t* 
     fp4_row_to_fp8_col_kernel<<<grid, 64, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, scales, rows, cols, y,
                                                                                       tile_scale);
     return check_launch("fp4_row_to_fp8_col");
+}
+
+extern "C" int64_t fp4q_fp4_row_to_fp8_col_grouped_ld(int64_t rows, int64_t groups) {
+    if (rows < 0 || groups < 1 || groups > kGroupedMax || rows > INT32_MAX) return 0;
+    return kColTile * ((rows + kColTile - 1) / kColTile + groups);
+}
+
+extern "C" fp4q_status fp4q_fp4_row_to_fp8_col_grouped(const uint8_t* q, const uint8_t* scales, int64_t rows,
+                                                       int64_t cols, const int64_t* offsets, int64_t groups,
+                                                       uint8_t* y, float* tile_scale, fp4q_stream_t stream) {
+    if (rows < 0 || cols < 0 || groups < 1 || groups > kGroupedMax)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "fp4_row_to_fp8_col_grouped: need rows, cols >= 0, 1 <= groups <= %d",
+                    kGroupedMax);
+    if (cols % kColTile) return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "fp4_row_to_fp8_col_grouped: cols %% 128 != 0");
+    if (rows > INT32_MAX || cols > INT32_MAX)
+        return fail(FP4Q_ERR_UNSUPPORTED_SHAPE, "fp4_row_to_fp8_col_grouped: rows and cols at most 2^31 - 1");
+    if (rows == 0 || cols == 0) return FP4Q_OK;
+    if (!q || !scales || !offsets || !y || !tile_scale)
+        return fail(FP4Q_ERR_INVALID_ARGUMENT, "fp4_row_to_fp8_col_grouped: null pointer");
+    if ((reinterpret_cast<uintptr_t>(q) & 31u) || (reinterpret_cast<uintptr_t>(y) & 31u) ||
+        (reinterpret_cast<uintptr_t>(scales) & 3u) || (reinterpret_cast<uintptr_t>(tile_scale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(offsets) & 7u))
+        return fail(FP4Q_ERR_MISALIGNED,
+                    "fp4_row_to_fp8_col_grouped: q, y 32-byte aligned; scales, tile_scale 4-byte; offsets 8-byte");
+    int sms = 0;
+    fp4q_status st = current_device(&sms);
+    if (st != FP4Q_OK) return st;
+    const int64_t ld = fp4q_fp4_row_to_fp8_col_grouped_ld(rows, groups);
+    const int64_t items_upper = (ld / kColTile) * (cols / 64);
+    const int64_t blocks = std::min<int64_t>((items_upper + 7) / 8,
+                                             int64_t(sms) * resident_per_sm(fp4_row_to_fp8_col_grouped_kernel, 256));
+    fp4_row_to_fp8_col_grouped_kernel<<<unsigned(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        q, scales, rows, cols, offsets, int(groups), y, ld, tile_scale);
+    return check_launch("fp4_row_to_fp8_col_grouped");
 }
 
 extern "C" fp4q_status fp4q_fp4_to_fp8(const uint8_t* q, const uint8_t* scales, int64_t rows,

@@ -35,6 +35,7 @@ EXPORTED = [
     "fp4q_moe_dispatch_static", "fp4q_check_wait_timeout", "fp4q_nv_quantize_2d", "fp4q_fp4_row_to_fp8_col",
     "fp4q_fp8_tile_scales_to_e8m0", "fp4q_fp8_pipeline_host_workspace_bytes", "fp4q_fp8_pipeline_host",
     "fp4q_stream_status", "fp4q_fp8_pipeline_host_release", "fp4q_nv_quantize_sr_rne",
+    "fp4q_fp4_row_to_fp8_col_grouped_ld", "fp4q_fp4_row_to_fp8_col_grouped",
 ]
 MOE_DISPATCH_STATIC_SCRATCH_BYTES = 4 * 1024 * 1024
 
@@ -82,6 +83,10 @@ def load() -> ctypes.CDLL:
                 if fn is not None:
                     fn.restype = ctypes.c_size_t
                     fn.argtypes = args
+            fn = getattr(L, "fp4q_fp4_row_to_fp8_col_grouped_ld", None)
+            if fn is not None:
+                fn.restype = i64
+                fn.argtypes = [i64, i64]
             sigs = {
                 "fp4q_mx_quantize": [vp, ci, vp, i64, i64, i64, ci, vp, vp, ci, vp],
                 "fp4q_mx_dequantize": [vp, vp, i64, i64, ci, vp, ci, vp],
@@ -100,6 +105,7 @@ def load() -> ctypes.CDLL:
                 "fp4q_nv_quantize_sr_rne": [vp, i64, i64, i64, ci, u64, u64, vp, vp, vp, vp, vp, vp, ci, vp,
                                             ctypes.c_size_t, vp],
                 "fp4q_fp4_row_to_fp8_col": [vp, vp, i64, i64, vp, vp, vp],
+                "fp4q_fp4_row_to_fp8_col_grouped": [vp, vp, i64, i64, vp, i64, vp, vp, vp],
                 "fp4q_fp8_tile_scales_to_e8m0": [vp, i64, i64, vp, ci, vp],
                 "fp4q_fp8_pipeline_host": [vp, vp, i64, i64, vp, vp, vp, vp, i64, vp, ctypes.c_size_t, vp],
                 "fp4q_fp8_pipeline_host_release": [],
@@ -231,6 +237,15 @@ def fp4q_nv_quantize_2d(x, rows, cols, ld_x, rounding, sr_seed, amax_in, amax_ou
 def fp4q_fp4_row_to_fp8_col(q, scales, rows, cols, y, tile_scale, stream=None):
     return _check("fp4q_fp4_row_to_fp8_col", load().fp4q_fp4_row_to_fp8_col(
         _ptr(q), _ptr(scales), rows, cols, _ptr(y), _ptr(tile_scale), _stream(stream)))
+
+
+def fp4q_fp4_row_to_fp8_col_grouped_ld(rows, groups):
+    return load().fp4q_fp4_row_to_fp8_col_grouped_ld(rows, groups)
+
+
+def fp4q_fp4_row_to_fp8_col_grouped(q, scales, rows, cols, offsets, groups, y, tile_scale, stream=None):
+    return _check("fp4q_fp4_row_to_fp8_col_grouped", load().fp4q_fp4_row_to_fp8_col_grouped(
+        _ptr(q), _ptr(scales), rows, cols, _ptr(offsets), groups, _ptr(y), _ptr(tile_scale), _stream(stream)))
 
 
 def fp4q_fp8_tile_scales_to_e8m0(tile_scale, rows, cols, scales, layout, stream=None):
@@ -380,6 +395,21 @@ def fp4_row_to_fp8_col(q, s, stream=None):
     y = torch.empty((C, R), dtype=torch.uint8, device=q.device)
     ts = torch.empty((C, R // 128), dtype=torch.float32, device=q.device)
     fp4q_fp4_row_to_fp8_col(q, s, R, C, y, ts, stream)
+    return y, ts
+
+
+def fp4_row_to_fp8_col_grouped(q, s, offsets, groups, stream=None):
+    """Row-wise MXFP4 [R, C] in ragged groups (offsets [groups + 1], device) ->
+    (E4M3 [C, ld], FP32 tile scales [C, ld/128]), each group padded to whole
+    128-row tiles (ld = 128 * (ceil(R / 128) + groups))."""
+    torch = _torch()
+    for name, t in (("q", q), ("s", s), ("offsets", offsets)):
+        _on_device(name, t)
+    R, C = q.shape[0], q.shape[1] * 2
+    ld = fp4q_fp4_row_to_fp8_col_grouped_ld(R, groups)
+    y = torch.empty((C, ld), dtype=torch.uint8, device=q.device)
+    ts = torch.empty((C, ld // 128), dtype=torch.float32, device=q.device)
+    fp4q_fp4_row_to_fp8_col_grouped(q, s, R, C, offsets, groups, y, ts, stream)
     return y, ts
 
 

@@ -64,6 +64,12 @@ def test_scales_bytes(lib):
     assert lib.fp4q_rebased_scales_bytes(huge, 128, 1) == 0
     assert lib.fp4q_rebased_scales_bytes(1 << 40, 1 << 40, 8) == 0
     assert lib.fp4q_rebased_scales_bytes(300, 256, 4) == (3 + 4) * 4 * 512
+    # row length of the grouped FP4RowToFP8Col output: 128 * (ceil(rows / 128) + groups)
+    assert lib.fp4q_fp4_row_to_fp8_col_grouped_ld(300, 4) == 128 * (3 + 4)
+    assert lib.fp4q_fp4_row_to_fp8_col_grouped_ld(0, 1) == 128
+    assert lib.fp4q_fp4_row_to_fp8_col_grouped_ld(300, 0) == 0
+    assert lib.fp4q_fp4_row_to_fp8_col_grouped_ld(300, 257) == 0
+    assert lib.fp4q_fp4_row_to_fp8_col_grouped_ld(1 << 31, 4) == 0
 
 
 def test_argument_errors_need_no_gpu(lib):
@@ -112,6 +118,14 @@ def test_argument_errors_need_no_gpu(lib):
         (lambda: lib.fp4q_fp8_pipeline_host(x, x, 64, 256, x, x, x, x, 64, x, wsb - 1, stream=0), 1),
         (lambda: lib.fp4q_fp8_pipeline_host(x, x, 200, 256, x, x, x, x, 128, x, wsb, stream=0), 1),
         (lambda: lib.fp4q_fp8_pipeline_host(x, x, 1 << 41, 7168, x, x, x, x, 1 << 41, x, wsb, stream=0), 2),
+        (lambda: lib.fp4q_fp4_row_to_fp8_col_grouped(x, x, -1, 256, x, 4, x, x, stream=0), 1),
+        (lambda: lib.fp4q_fp4_row_to_fp8_col_grouped(x, x, 300, 256, x, 0, x, x, stream=0), 1),
+        (lambda: lib.fp4q_fp4_row_to_fp8_col_grouped(x, x, 300, 256, x, 257, x, x, stream=0), 1),
+        (lambda: lib.fp4q_fp4_row_to_fp8_col_grouped(x, x, 300, 192, x, 4, x, x, stream=0), 2),
+        (lambda: lib.fp4q_fp4_row_to_fp8_col_grouped(x, x, 1 << 31, 256, x, 4, x, x, stream=0), 2),
+        (lambda: lib.fp4q_fp4_row_to_fp8_col_grouped(x, x, 300, 256, None, 4, x, x, stream=0), 1),
+        (lambda: lib.fp4q_fp4_row_to_fp8_col_grouped(x + 16, x, 300, 256, x, 4, x, x, stream=0), 3),
+        (lambda: lib.fp4q_fp4_row_to_fp8_col_grouped(x, x, 300, 256, x + 4, 4, x, x, stream=0), 3),
     ]:
         with pytest.raises(E) as e:
             fn()

@@ -165,6 +165,71 @@ def test_fp4_row_to_fp8_col_full_size(fq, oracle):
     assert np.array_equal(host(yts).view(np.uint32), ytsr.view(np.uint32))
 
 
+def _grouped_col_run(fq, q, s, offs, G, canary=True):
+    """Raw call of fp4q_fp4_row_to_fp8_col_grouped into canary-filled outputs of
+    the documented size; returns host (y [C, ld], tile scales [C, ld/128])."""
+    import torch
+    R, C = q.shape[0], 2 * q.shape[1]
+    ld = fq.fp4q_fp4_row_to_fp8_col_grouped_ld(R, G)
+    y = torch.full((C, ld), 0xAB, dtype=torch.uint8, device="cuda")
+    ts = torch.full((C, ld // 128), 7.0, dtype=torch.float32, device="cuda")
+    fq.fp4q_fp4_row_to_fp8_col_grouped(dev(q), dev(s), R, C, dev(np.asarray(offs, dtype=np.int64)), G, y, ts)
+    torch.cuda.synchronize()
+    return host(y), host(ts)
+
+
+def _check_grouped_col(oracle, y, ts, q, s, offs):
+    yr, tsr = oracle.mx_to_fp8_col_grouped(q, s, offs)
+    T = tsr.shape[1]
+    assert np.array_equal(y[:, : 128 * T], yr)
+    assert np.array_equal(ts[:, :T].view(np.uint32), tsr.view(np.uint32))
+    assert np.all(y[:, 128 * T:] == 0xAB) and np.all(ts[:, T:] == 7.0)      # nothing written past the groups
+
+
+@pytest.mark.parametrize("C", [128, 256, 2048])
+def test_fp4_row_to_fp8_col_grouped(fq, oracle, C):
+    """Ragged expert groups (empty, 1, 127-129, 255, 300 and 2 rows) and rows
+    past the last offset: every group's tiles restart at its first row, its last
+    tile is partial and padded with zeros, bit-exact against the oracle."""
+    sizes = [0, 1, 127, 128, 129, 0, 255, 300, 2]
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    R = int(offs[-1]) + 9
+    rng = np.random.default_rng(C + 5)
+    q = rng.integers(0, 256, (R, C // 2), dtype=np.uint8)
+    s = rng.integers(100, 160, (R, C // 32), dtype=np.uint8)
+    s[::7] = rng.integers(0, 255, (len(s[::7]), C // 32), dtype=np.uint8)   # wide spreads: deep shifts, flushes
+    y, ts = _grouped_col_run(fq, q, s, offs, len(sizes))
+    _check_grouped_col(oracle, y, ts, q[: offs[-1]], s[: offs[-1]], offs)
+
+
+def test_fp4_row_to_fp8_col_grouped_moe_size(fq, oracle):
+    """8192 tokens routed top-8 over 64 experts (Zipf 1.1): the 65536
+    dispatched rows of the 2048-wide expert activation h, converted to the
+    column FP8 layout of the down-projection's weight gradient; every byte and
+    tile scale checked."""
+    from micro_scaled_fp4_gb300 import workloads as W
+    topk = W.moe_routing(tokens=8192, experts=64, top_k=8, seed=33)
+    _, offs = oracle.moe_dispatch(topk, 64)
+    R, C = int(offs[-1]), 2048
+    rng = np.random.default_rng(34)
+    q = rng.integers(0, 256, (R, C // 2), dtype=np.uint8)
+    s = rng.integers(110, 140, (R, C // 32), dtype=np.uint8)
+    y, ts = _grouped_col_run(fq, q, s, offs, 64)
+    _check_grouped_col(oracle, y, ts, q, s, offs)
+
+
+def test_fp4_row_to_fp8_col_grouped_clamps_malformed_offsets(fq, oracle):
+    """Offsets that decrease or run past `rows` are clamped (each into
+    [previous offset, rows]) and give the result of the clamped offsets;
+    nothing is written past the groups."""
+    rng = np.random.default_rng(35)
+    R, C = 350, 256
+    q = rng.integers(0, 256, (R, C // 2), dtype=np.uint8)
+    s = rng.integers(110, 140, (R, C // 32), dtype=np.uint8)
+    y, ts = _grouped_col_run(fq, q, s, [0, 300, 100, 400, 50], 4)
+    _check_grouped_col(oracle, y, ts, q, s, [0, 300, 300, 350, 350])
+
+
 def test_widen_argument_errors(fq):
     import torch
     x = torch.zeros((16, 64), dtype=torch.bfloat16, device="cuda")
