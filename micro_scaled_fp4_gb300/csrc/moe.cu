@@ -190,20 +190,6 @@ __global__ void __launch_bounds__(256) mx_rebase_kernel(const uint8_t* __restric
     if (lane == 0 && bad && violations) atomicAdd(violations, bad);
 }
 
-// The same rebase, one padded 128-row tile at a time.  In the MMA scale layout
-// a 128-row tile's scales are one contiguous run of S16/4 chunks of 512 bytes,
-// and its E8M0 source rows are one contiguous run of 128 * S32 bytes (fewer at
-// a group's end).  Phase 1 stages that run in shared memory, each thread
-// loading up to eight 32-bit words before it stores any, so a tile takes few
-// load round trips (rows padded by 4 bytes: the column reads of phase 2 then
-// fall in 32 different banks; rows past the group are zero); then two threads
-// per row take the row's maximum E8M0 byte.
-// Phase 2 writes every chunk as 16-byte stores -- thread (c4, i) the bytes of
-// rows i, i + 32, i + 64, i + 96 for columns 4 c4 .. 4 c4 + 3 -- so a warp
-// writes 512 contiguous bytes; it converts four E8M0 bytes at a time
-// (rebase4).  Padding rows are written as 0.
-// wdiv = ceil(2^32 / (S32 / 4)): k / (S32 / 4) == (k * wdiv) >> 32 for every
-// word index k < 128 * S32 / 4 of a tile.
 // Four E8M0 bytes (w) of rows whose maximum byte is the matching byte of m ->
 // their UE4M3 bytes, byte-parallel.  With d = m - w (>= 0) the exponent
 // difference E - B is 8 - d, so the UE4M3 byte is (15 - d) << 3 for d <= 14
@@ -220,6 +206,20 @@ __device__ __forceinline__ uint32_t rebase4(uint32_t w, uint32_t m, uint32_t& ba
     return normal | sub;
 }
 
+// The same rebase, one padded 128-row tile at a time.  In the MMA scale layout
+// a 128-row tile's scales are one contiguous run of S16/4 chunks of 512 bytes,
+// and its E8M0 source rows are one contiguous run of 128 * S32 bytes (fewer at
+// a group's end).  Phase 1 stages that run in shared memory, each thread
+// loading up to eight 32-bit words before it stores any, so a tile takes few
+// load round trips (rows padded by 4 bytes: the column reads of phase 2 then
+// fall in 32 different banks; rows past the group are zero); then two threads
+// per row take the row's maximum E8M0 byte.
+// Phase 2 writes every chunk as 16-byte stores -- thread (c4, i) the bytes of
+// rows i, i + 32, i + 64, i + 96 for columns 4 c4 .. 4 c4 + 3 -- so a warp
+// writes 512 contiguous bytes; it converts four E8M0 bytes at a time
+// (rebase4).  Padding rows are written as 0.
+// wdiv = ceil(2^32 / (S32 / 4)): k / (S32 / 4) == (k * wdiv) >> 32 for every
+// word index k < 128 * S32 / 4 of a tile.
 __global__ void __launch_bounds__(256) mx_rebase_tiles_kernel(const uint8_t* __restrict__ s, int64_t rows, int S32,
                                                               uint64_t wdiv, const int64_t* __restrict__ offsets,
                                                               int groups, uint8_t* __restrict__ out,
