@@ -57,7 +57,7 @@ TRAFFIC = {
     "fp8_to_mx": {"bytes_per_launch": 60579584 + 2470144, "src_sha": "cc401b8614be28fe",
                   "src": ["mx_quant.cu", "common.cuh", "ring.cuh", "tc.cuh"],
                   "profile": "profiles/fp8_pipeline_8192x7168.md"},
-    "mx_to_fp8": {"bytes_per_launch": 31212800 + 5800448, "src_sha": "1e765662d9a77e0e",
+    "mx_to_fp8": {"bytes_per_launch": 31214592 + 5374976, "src_sha": "7bb34dc406d17efc",
                   "src": ["fp4_to_fp8.cu", "common.cuh", "ring.cuh", "tc.cuh"],
                   "profile": "profiles/fp8_pipeline_8192x7168.md"},
 }
