@@ -152,6 +152,8 @@ def e2m1_sr(v: np.ndarray, r: np.ndarray) -> np.ndarray:
 
 
 def mx_shared_exponent(amax: float) -> int:
+    """E = floor(log2 amax) - 2, -127 for amax 0, clamped to [-127, 127].
+    Pinned by tests/test_oracle_mx.py (edges and clamps)."""
     return _L().or_mx_shared_exponent(float(amax))
 
 
@@ -327,7 +329,8 @@ def mx_to_fp8_col_grouped(q: np.ndarray, s: np.ndarray, offsets):
 def mx_quantize_col(x: np.ndarray):
     """Column-wise MXFP4 (blocks of 32 along axis 0): by definition the
     row-wise quantization of the transpose, returned in the transposed layout
-    (q [C, R/2], s [C, R/32])."""
+    (q [C, R/2], s [C, R/32]).  Pinned by a hand-derived case
+    (tests/test_oracle_mx.py)."""
     return mx_quantize(np.ascontiguousarray(np.asarray(x).T))
 
 
@@ -374,7 +377,9 @@ def nv_quantize(x_bf16: np.ndarray, rht=False, rht_seed: int = 0, rounding: str 
 def nv_quantize_col(x_bf16: np.ndarray, **kw):
     """Column-wise NVFP4 (16-blocks and RHT tiles along axis 0): by definition
     the row-wise quantization of the transpose, in the transposed layout; the
-    stochastic-rounding words follow the transpose's linear element index."""
+    stochastic-rounding words follow the transpose's linear element index.
+    Pinned by its structure on constant columns (tests/test_oracle_nv.py) and
+    the Wgrad contraction tests (tests/test_oracle_widen.py)."""
     return nv_quantize(np.ascontiguousarray(np.asarray(x_bf16).T), **kw)
 
 
@@ -418,6 +423,8 @@ def mx_gemm_ref(qa, sa, qb, sb) -> np.ndarray:
 
 
 def nv_gemm_ref(qa, sa, sta, qb, sb, stb) -> np.ndarray:
+    """float64 Y = A . B^T of dequantized NVFP4 operands.  Pinned by an exact
+    rational triple loop (tests/test_oracle_gemm.py)."""
     return gemm_ref(nv_dequantize_f64(qa, sa, sta), nv_dequantize_f64(qb, sb, stb))
 
 
@@ -494,6 +501,7 @@ def silu(g: np.ndarray) -> np.ndarray:
 
 
 def moe_up_gate(x_rows_deq: np.ndarray, w1_deq: np.ndarray, inter: int) -> np.ndarray:
-    """U = X_e W1_e^T; h = SiLU(U[:, :inter]) * U[:, inter:] (float64)."""
+    """U = X_e W1_e^T; h = SiLU(U[:, :inter]) * U[:, inter:] (float64).
+    Pinned by a closed form on one-hot token rows (tests/test_oracle_gemm.py)."""
     u = gemm_ref(x_rows_deq, w1_deq)
     return silu(u[:, :inter]) * u[:, inter:]

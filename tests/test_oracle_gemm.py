@@ -97,3 +97,41 @@ def test_mx_rebase_reconstructs_every_representable_block(oracle):
     assert np.all(ue[:, 0::2][~ok] == 0) and v == int((~ok).sum()) and v > 0
     assert np.array_equal(ue[:, 0::2], ue[:, 1::2])
     assert np.array_equal(f.astype(np.float64), np.exp2(B.astype(np.float64)))
+
+
+def test_nv_gemm_ref_against_exact_rationals(oracle):
+    """Y = s_tA s_tB sum_k (qA sA)(qB sB): an exact rational triple loop pins the
+    float64 product of the dequantized NVFP4 operands, within the float64
+    dot-product bound K 2^-52 sum |terms| (each dequantized value is exact, but
+    a product of two carries up to 60 significant bits)."""
+    rng = np.random.default_rng(3)
+    M, N, K = 5, 4, 64
+    qa = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    qb = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = rng.integers(0x08, 0x7E, (M, K // 16), dtype=np.uint8)      # positive finite E4M3
+    sb = rng.integers(0x08, 0x7E, (N, K // 16), dtype=np.uint8)
+    sta, stb = np.float32(3.0 / 2688.0), np.float32(5.0 / 2688.0)
+    y = oracle.nv_gemm_ref(qa, sa, sta, qb, sb, stb)
+    e2m1 = oracle.e2m1_values()
+    e4m3 = oracle.e4m3_values()
+    def val(q, s, st, r, k):
+        code = (q[r, k // 2] >> (4 * (k % 2))) & 0xF
+        return Fraction(float(e2m1[code])) * Fraction(float(e4m3[s[r, k // 16]])) * Fraction(float(st))
+    for m in range(M):
+        for n in range(N):
+            terms = [val(qa, sa, sta, m, k) * val(qb, sb, stb, n, k) for k in range(K)]
+            exact = sum(terms)
+            assert abs(Fraction(float(y[m, n])) - exact) <= K * Fraction(1, 2 ** 52) * sum(abs(t) for t in terms)
+
+
+def test_moe_up_gate_closed_form(oracle):
+    """h = SiLU(X W_g^T) * (X W_u^T): with one-hot token rows the projections are
+    columns of W, so h is SiLU(W_g[j, i]) * W_u[j, i] for token i, channel j."""
+    rng = np.random.default_rng(4)
+    T, H, I = 3, 5, 4
+    x = np.eye(T, H)
+    w1 = rng.standard_normal((2 * I, H))
+    h = oracle.moe_up_gate(x, w1, I)
+    g, u = w1[:I, :T].T, w1[I:, :T].T                  # [T, I]
+    want = g / (1.0 + np.exp(-g)) * u
+    assert h.shape == (T, I) and np.allclose(h, want, rtol=1e-15, atol=0)

@@ -222,3 +222,33 @@ def test_mx_to_fp8_flush_counts_only_deep_shifts(oracle):
     assert np.all(y[0, 32:64] == 0)                        # 6 * 2^-12 < 2^-9 -> flushed
     assert np.all(y[0, 64:96] == 0x03)                     # 6 * 2^-10 = 3 * 2^-9
     assert np.all(y[0, 96:128] == 0x06)                    # 6 * 2^-9
+
+
+def test_mx_shared_exponent_edges(oracle):
+    """E = floor(log2 amax) - 2 (E2M1's largest exponent), -127 for a zero
+    block, clamped to the E8M0 range [-127, 127]."""
+    assert oracle.mx_shared_exponent(6.0) == 0
+    assert oracle.mx_shared_exponent(4.0) == 0
+    assert oracle.mx_shared_exponent(3.999) == -1
+    assert oracle.mx_shared_exponent(1.5 * 2.0 ** 100) == 98
+    assert oracle.mx_shared_exponent(0.0) == -127
+    assert oracle.mx_shared_exponent(2.0 ** -126) == -127          # -128 clamped
+    assert oracle.mx_shared_exponent(2.0 ** -140) == -127
+    assert oracle.mx_shared_exponent(2.0 ** 200) == 127
+
+
+def test_mx_quantize_col_hand_derived(oracle):
+    """Blocks of 32 run down the columns and the result is laid out by column:
+    column 0 holds 4.0, 0.5, -1.5 and zeros (amax 4: E = 0, codes 6, 1, 0xB
+    and 0), column 1 is all 1.0 (amax 1: E = -2, 1 / 2^-2 = 4 -> code 6)."""
+    x = np.zeros((32, 2), dtype=np.float32)
+    x[0, 0], x[1, 0], x[2, 0] = 4.0, 0.5, -1.5
+    x[:, 1] = 1.0
+    q, s = oracle.mx_quantize_col(x)
+    assert q.shape == (2, 16) and s.shape == (2, 1)
+    assert s[0, 0] == 127 and s[1, 0] == 125
+    codes = np.empty((2, 32), dtype=np.uint8)
+    codes[:, 0::2] = q & 0xF
+    codes[:, 1::2] = q >> 4
+    assert list(codes[0, :3]) == [6, 1, 0xB] and np.all(codes[0, 3:] == 0)
+    assert np.all(codes[1] == 6)

@@ -197,3 +197,22 @@ def test_nv_sr_unbiased_in_the_mean(oracle):
     sf = np.repeat(oracle.e4m3_values()[r0["s"]] * float(r0["s_t"]), 16, axis=1)
     # per-element sd of one draw is <= step/2 * sf <= sf; 6 sigma bound on the mean
     assert np.all(np.abs(mean - xf) <= 6 * sf / math.sqrt(n) + 1e-12)
+
+
+def test_nv_quantize_col_runs_down_the_columns(oracle):
+    """Column-wise NVFP4 of a matrix whose columns are constant: every 16-row
+    block of column c sees the same 16 values, so row c of the transposed
+    result repeats one scale byte and one code, and the dequantized value is
+    the column's value within the E4M3 scale's rounding (2^-4 relative); a
+    reduction along the wrong axis would mix the columns' magnitudes."""
+    R, C = 64, 16
+    v = (np.linspace(0.25, 3.0, C) * np.where(np.arange(C) % 2, -1.0, 1.0)).astype(np.float32)
+    x = _bf16(np.tile(v, (R, 1)))
+    r = oracle.nv_quantize_col(x)
+    q, s = r["q"], r["s"]
+    assert q.shape == (C, R // 2) and s.shape == (C, R // 16)
+    assert np.all(s == s[:, :1]) and np.all(q == q[:, :1])
+    y = oracle.nv_dequantize_f64(q, s, r["s_t"])
+    vb = oracle.bf16_bits_to_f32(_bf16(v)).astype(np.float64)
+    assert np.all(np.abs(y - vb[:, None]) <= np.abs(vb[:, None]) * 2.0 ** -4)
+    assert len(np.unique(s[:, 0])) > 4                 # the columns' scales differ
