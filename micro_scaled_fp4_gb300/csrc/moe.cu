@@ -190,20 +190,14 @@ __global__ void __launch_bounds__(256) mx_rebase_kernel(const uint8_t* __restric
     if (lane == 0 && bad && violations) atomicAdd(violations, bad);
 }
 
-// Four E8M0 bytes (w) of rows whose maximum byte is the matching byte of m ->
-// their UE4M3 bytes, byte-parallel.  With d = m - w (>= 0) the exponent
-// difference E - B is 8 - d, so the UE4M3 byte is (15 - d) << 3 for d <= 14
-// (normal), 4, 2, 1 for d = 15, 16, 17 (the subnormals 2^-7 .. 2^-9, picked
-// from a byte table by a permute whose selector nibbles are min(d - 14, 4)),
-// and 0 for d >= 18, which is counted in `bad`.
-__device__ __forceinline__ uint32_t rebase4(uint32_t w, uint32_t m, uint32_t& bad) {
-    const uint32_t d = __vsubus4(m, w);
-    const uint32_t normal = __vsub4(0x0F0F0F0Fu, __vminu4(d, 0x0F0F0F0Fu)) << 3;   // bytes < 16: no carry
-    const uint32_t ds = __vminu4(__vsubus4(d, 0x0E0E0E0Eu), 0x04040404u);
-    const uint32_t x = ds | (ds >> 4);                 // byte 0: ds0 | ds1 << 4, byte 2: ds2 | ds3 << 4
-    const uint32_t sub = __byte_perm(0x01020400u, 0u, (x & 0xFFu) | ((x >> 8) & 0xFF00u));
-    bad += uint32_t(__popc(__vcmpgeu4(d, 0x12121212u))) >> 3;
-    return normal | sub;
+// UE4M3 byte of a block whose E8M0 byte lies d = (row maximum byte) - byte
+// below its row's maximum: the exponent difference E - B is 8 - d, so the
+// byte is (15 - d) << 3 for d <= 14 (normal), 4, 2, 1 for d = 15, 16, 17
+// (the subnormals 2^-7 .. 2^-9) and 0 for d >= 18 (not representable,
+// counted in `bad`).  Branch-free, so lanes with different d never diverge.
+__device__ __forceinline__ uint32_t rebased_byte(uint32_t d, uint32_t& bad) {
+    bad += uint32_t(d >= 18u);
+    return d <= 14u ? (15u - d) << 3 : 4u >> min(d - 15u, 3u);
 }
 
 // The same rebase, one padded 128-row tile at a time.  In the MMA scale layout
@@ -216,8 +210,8 @@ __device__ __forceinline__ uint32_t rebase4(uint32_t w, uint32_t m, uint32_t& ba
 // per row take the row's maximum E8M0 byte.
 // Phase 2 writes every chunk as 16-byte stores -- thread (c4, i) the bytes of
 // rows i, i + 32, i + 64, i + 96 for columns 4 c4 .. 4 c4 + 3 -- so a warp
-// writes 512 contiguous bytes; it converts four E8M0 bytes at a time
-// (rebase4).  Padding rows are written as 0.
+// writes 512 contiguous bytes (rebased_byte per scale byte).  Padding rows
+// are written as 0.
 // wdiv = ceil(2^32 / (S32 / 4)): k / (S32 / 4) == (k * wdiv) >> 32 for every
 // word index k < 128 * S32 / 4 of a tile.
 __global__ void __launch_bounds__(256) mx_rebase_tiles_kernel(const uint8_t* __restrict__ s, int64_t rows, int S32,
@@ -285,21 +279,15 @@ __global__ void __launch_bounds__(256) mx_rebase_tiles_kernel(const uint8_t* __r
         uint8_t* tile_out = out + uint64_t(T) * uint64_t(S32 / 2) * 512u;
         for (int k = threadIdx.x; k < (S32 / 2) * 32; k += blockDim.x) {
             const int c4 = k >> 5, i = k & 31;
-            uint32_t e[4], m[4];
+            uint32_t w[4];
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
                 const int rr = i + 32 * qq;
-                e[qq] = *reinterpret_cast<const uint16_t*>(stage + rr * RS + 2 * c4);
-                m[qq] = mm[rr];
+                const uint32_t e2 = *reinterpret_cast<const uint16_t*>(stage + rr * RS + 2 * c4);
+                const uint32_t m = mm[rr] & 0xffu;
+                const uint32_t b0 = rebased_byte(m - (e2 & 0xffu), bad), b1 = rebased_byte(m - (e2 >> 8), bad);
+                w[qq] = rr < nreal ? b0 | (b0 << 8) | (b1 << 16) | (b1 << 24) : 0u;
             }
-            // rows i, i + 32 in oa and i + 64, i + 96 in ob, two blocks each
-            const uint32_t oa = rebase4(e[0] | (e[1] << 16), m[0] | (m[1] << 16), bad);
-            const uint32_t ob = rebase4(e[2] | (e[3] << 16), m[2] | (m[3] << 16), bad);
-            uint32_t w[4] = {__byte_perm(oa, 0u, 0x1100u), __byte_perm(oa, 0u, 0x3322u),
-                             __byte_perm(ob, 0u, 0x1100u), __byte_perm(ob, 0u, 0x3322u)};
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq)
-                if (i + 32 * qq >= nreal) w[qq] = 0u;
             *reinterpret_cast<uint4*>(tile_out + c4 * 512 + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         __syncthreads();                                  // the staging is reused by the next tile
