@@ -112,6 +112,41 @@ def test_nvfp4_gemm(fq, oracle, shape, rht):
         assert rel_frobenius(host(d32), exact) < 0.2
 
 
+@pytest.mark.parametrize("case", range(9))
+def test_gemm_random_shapes(fq, oracle, case):
+    """Seeded random M, N in [1, 900) and K a multiple of 128 up to 1152, for
+    MXFP4, NVFP4 and NVFP4 with RHT operands (case % 3): operands equal to the
+    oracle's, FP32 and BF16 outputs within 1e-3 of the float64 product."""
+    import torch
+    rng = np.random.default_rng(7000 + case)
+    M, N, K = int(rng.integers(1, 900)), int(rng.integers(1, 900)), 128 * int(rng.integers(1, 10))
+    a, b = _operands(M, N, K, 8000 + case)
+    if case % 3 == 0:
+        qa, sa = fq.mx_quantize(dev_bf16(a), layout=fq.FP4Q_SCALES_MMA)
+        qb, sb = fq.mx_quantize(dev_bf16(b), layout=fq.FP4Q_SCALES_MMA)
+        args = (qa, sa, qb, sb, fq.FP4Q_MXFP4)
+        qra, sra = oracle.mx_quantize(a)
+        qrb, srb = oracle.mx_quantize(b)
+        _same_operand(qa, sa, qra, sra, M, K // 32)
+        _same_operand(qb, sb, qrb, srb, N, K // 32)
+        ref = oracle.mx_gemm_ref(qra, sra, qrb, srb)
+    else:
+        rht = case % 3 == 2
+        ra = fq.nv_quantize(dev_bf16(a), rht=rht, rht_seed=9, layout=fq.FP4Q_SCALES_MMA)
+        rb = fq.nv_quantize(dev_bf16(b), rht=rht, rht_seed=9, layout=fq.FP4Q_SCALES_MMA)
+        args = (ra["q"], ra["scales"], rb["q"], rb["scales"], fq.FP4Q_NVFP4, ra["s_t"], rb["s_t"])
+        oa = oracle.nv_quantize(a, rht=rht, rht_seed=9)
+        ob = oracle.nv_quantize(b, rht=rht, rht_seed=9)
+        _same_operand(ra["q"], ra["scales"], oa["q"], oa["s"], M, K // 16)
+        _same_operand(rb["q"], rb["scales"], ob["q"], ob["s"], N, K // 16)
+        ref = oracle.nv_gemm_ref(oa["q"], oa["s"], oa["s_t"], ob["q"], ob["s"], ob["s_t"])
+    d32 = fq.gemm(*args, out_dtype=torch.float32)
+    d16 = fq.gemm(*args, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert fq.fp4q_device_status() == 0
+    _check(oracle, d16, d32, ref)
+
+
 def test_gemm_full_size(fq, oracle):
     """8192^3, MXFP4 (A with 0.5 % outlier rows x40) and NVFP4 with the RHT on
     both operands, BF16 output as the benchmark runs it.  Every code and scale
