@@ -191,6 +191,19 @@ def test_moe_small(fq, oracle):
     assert offs[-1] == 1400
 
 
+@pytest.mark.parametrize("case", range(3))
+def test_moe_random_configs(fq, oracle, case):
+    """Seeded random MoE configurations (tokens, hidden and intermediate widths
+    in multiples of 128, expert count, top-k) through the whole chain, every
+    stage checked as in the fixed cases."""
+    rng = np.random.default_rng(9000 + case)
+    E = int(rng.integers(2, 21))
+    T, H, I, k = int(rng.integers(50, 600)), 128 * int(rng.integers(1, 7)), 128 * int(rng.integers(1, 5)), \
+        int(rng.integers(1, min(4, E) + 1))
+    offs = _run_moe(fq, oracle, T=T, H=H, I=I, E=E, k=k, seed=9100 + case)
+    assert offs[-1] == T * k
+
+
 def test_moe_k_tails(fq, oracle):
     """K = 384 in both grouped GEMMs (a 128-element last stage), 5 experts."""
     offs = _run_moe(fq, oracle, T=300, H=384, I=384, E=5, k=2, seed=30)
